@@ -1,0 +1,311 @@
+"""CPU oracle for the speculative-decoding verify pass -- TEST INFRASTRUCTURE.
+
+Only the tests, ``__graft_entry__.smoke()`` and the bench's CPU-baseline leg may
+import this package.  The product path (``speculative_decoding_verify_gb300``)
+never does, and shares no code with it.
+
+Every function is a thin numpy wrapper over ``sdv_oracle.c`` (plain C, built with
+``-O2 -ffp-contract=off``, OpenMP over output rows only).  Each one follows the
+page passage cited in the C source:
+
+* block dequant / integer block dots / multi-position matmul (fp64 accumulate):
+  "Inside OpenJet Engine", section "One GPU launch for a speculative cycle";
+* RMSNorm + per-32 int8 requantisation, SiLU*mul requantisation: same section
+  (the producer requantises activations for the next consumer);
+* softmax statistics, greedy chain/tree acceptance: "How Kinetic is fast",
+  sections "RAD-1" and "Why the output does not change";
+* rejection sampling and the certainty drafter: "Speculative Decoding with
+  Open-Weights Models", section "Mathematical Integrity: Rejection Sampling for
+  LLMs", and "How Kinetic is fast", section "Why the output does not change";
+* Philox4x32-10: Salmon et al., SC'11.
+
+Parity status: every function here is pinned by a ``-m "not gpu"`` test in
+``tests/test_oracle_pins.py`` against something other than itself.  The
+free-running 64-layer stack composition (``stack_pass``) is pinned only through
+its stages; its end-to-end float output is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SO = os.path.join(_HERE, "libsdv_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+Q8_0 = 0
+Q4_32 = 1
+BLOCK_BYTES = {Q8_0: 34, Q4_32: 18}
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I = ctypes.c_int
+_F = ctypes.c_float
+
+
+def build(force: bool = False) -> str:
+    src = os.path.join(_HERE, "sdv_oracle.c")
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(src):
+        tmp = _SO + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp", "-fPIC",
+                               "-shared", "-o", tmp, src, "-lm"])
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def _get():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_SO)
+            sig = {
+                "oracle_num_threads": ([], _I),
+                "oracle_f16_to_f32": ([ctypes.c_uint16], _F),
+                "oracle_dequant": ([_I, _P, _I64, _P], None),
+                "oracle_block_dots": ([_I, _P, _I64, _I64, _P, _I, _P], None),
+                "oracle_qmatmul": ([_I, _P, _I64, _I64, _P, _P, _I, _P, _P, _P], None),
+                "oracle_rmsnorm_quant": ([_P, _P, _F, _I, _I64, _P, _P], None),
+                "oracle_cexp": ([_F], _F),
+                "oracle_silu_mul_requant": ([_P, _P, _I, _I64, _P, _P, _P], None),
+                "oracle_softmax_stats": ([_P, _I, _I64, _F, _P, _P, _P], None),
+                "oracle_softmax_probs": ([_P, _I64, _F, _F, _F, _P], None),
+                "oracle_accept_greedy_chain": ([_P, _P, _I, _P], _I),
+                "oracle_accept_greedy_tree": ([_P, _P, _P, _I, _P], _I),
+                "oracle_philox4x32_10": ([_P, _P, _P], None),
+                "oracle_uniforms": ([ctypes.c_uint64, _I64, _P, _P], None),
+                "oracle_draw_icdf": ([_P, _I64, _F], ctypes.c_int32),
+                "oracle_accept_sample_u": ([_P, _I64, _I, _P, _P, _F, _P, _P, _P], _I),
+                "oracle_accept_sample": ([_P, _I64, _I, _P, _P, _F, ctypes.c_uint64, _I64, _P], _I),
+                "oracle_accept_sample_trials": ([_P, _I64, _I, _P, _P, _F, ctypes.c_uint64, _I64, _I64, _P, _P],
+                                                None),
+            }
+            for name, (args, res) in sig.items():
+                f = getattr(lib, name)
+                f.argtypes = args
+                f.restype = res
+            _lib = lib
+    return _lib
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a, a.ctypes.data
+
+
+def num_threads() -> int:
+    return _get().oracle_num_threads()
+
+
+def f16_to_f32(bits: int) -> float:
+    return float(_get().oracle_f16_to_f32(bits))
+
+
+def dequant(qtype: int, blocks: np.ndarray, n_out: int, k_in: int) -> np.ndarray:
+    blocks, p = _c(blocks, np.uint8)
+    assert blocks.size == n_out * (k_in // 32) * BLOCK_BYTES[qtype]
+    out = np.empty((n_out, k_in), dtype=np.float32)
+    _get().oracle_dequant(qtype, p, n_out * (k_in // 32), out.ctypes.data)
+    return out
+
+
+def block_dots(qtype: int, w: np.ndarray, n_out: int, k_in: int, q: np.ndarray) -> np.ndarray:
+    w, pw = _c(w, np.uint8)
+    q, pq = _c(q, np.int8)
+    M = q.shape[0]
+    out = np.empty((M, n_out, k_in // 32), dtype=np.int32)
+    _get().oracle_block_dots(qtype, pw, n_out, k_in, pq, M, out.ctypes.data)
+    return out
+
+
+def qmatmul(qtype: int, w: np.ndarray, n_out: int, k_in: int, q: np.ndarray, scales: np.ndarray,
+            residual: np.ndarray | None = None):
+    """Returns (y fp32 [M][n_out], absbound fp64 [M][n_out])."""
+    w, pw = _c(w, np.uint8)
+    q, pq = _c(q, np.int8)
+    scales, ps = _c(scales, np.float32)
+    M = q.shape[0]
+    assert q.shape == (M, k_in) and scales.shape == (M, k_in // 32)
+    pr = None
+    if residual is not None:
+        residual, pr = _c(residual, np.float32)
+        assert residual.shape == (M, n_out)
+    y = np.empty((M, n_out), dtype=np.float32)
+    ab = np.empty((M, n_out), dtype=np.float64)
+    _get().oracle_qmatmul(qtype, pw, n_out, k_in, pq, ps, M, pr, y.ctypes.data, ab.ctypes.data)
+    return y, ab
+
+
+def rmsnorm_quant(x: np.ndarray, norm_w: np.ndarray | None, eps: float = 1e-6):
+    """Returns (q int8 [M][K], scales fp32 [M][K/32]); norm_w None = requantise only."""
+    x, px = _c(x, np.float32)
+    M, K = x.shape
+    pw = None
+    if norm_w is not None:
+        norm_w, pw = _c(norm_w, np.float32)
+    q = np.empty((M, K), dtype=np.int8)
+    s = np.empty((M, K // 32), dtype=np.float32)
+    _get().oracle_rmsnorm_quant(px, pw, eps, M, K, q.ctypes.data, s.ctypes.data)
+    return q, s
+
+
+def cexp(x) -> np.ndarray:
+    f = _get().oracle_cexp
+    x = np.asarray(x, dtype=np.float32)
+    return np.array([f(float(v)) for v in x.ravel()], dtype=np.float32).reshape(x.shape)
+
+
+def silu_mul_requant(g: np.ndarray, u: np.ndarray):
+    """Returns (q int8 [M][F], scales fp32 [M][F/32], h fp32 [M][F])."""
+    g, pg = _c(g, np.float32)
+    u, pu = _c(u, np.float32)
+    M, F = g.shape
+    q = np.empty((M, F), dtype=np.int8)
+    s = np.empty((M, F // 32), dtype=np.float32)
+    h = np.empty((M, F), dtype=np.float32)
+    _get().oracle_silu_mul_requant(pg, pu, M, F, q.ctypes.data, s.ctypes.data, h.ctypes.data)
+    return q, s, h
+
+
+def softmax_stats(logits: np.ndarray, T: float = 1.0):
+    """Returns (row_max [M], row_sumexp [M], argmax [M])."""
+    logits, pl = _c(logits, np.float32)
+    M, V = logits.shape
+    m = np.empty(M, dtype=np.float32)
+    z = np.empty(M, dtype=np.float32)
+    a = np.empty(M, dtype=np.int32)
+    _get().oracle_softmax_stats(pl, M, V, T, m.ctypes.data, z.ctypes.data, a.ctypes.data)
+    return m, z, a
+
+
+def softmax_probs(logits_row: np.ndarray, T: float = 1.0) -> np.ndarray:
+    l, pl = _c(logits_row.reshape(1, -1), np.float32)
+    m, z, _ = softmax_stats(l, T)
+    p = np.empty(l.shape[1], dtype=np.float32)
+    _get().oracle_softmax_probs(pl, l.shape[1], T, float(m[0]), float(z[0]), p.ctypes.data)
+    return p
+
+
+def accept_greedy_chain(argmax: np.ndarray, drafts: np.ndarray) -> np.ndarray:
+    argmax, pa = _c(argmax, np.int32)
+    drafts, pd = _c(drafts, np.int32)
+    K = drafts.size
+    assert argmax.size == K + 1
+    out = np.empty(K + 1, dtype=np.int32)
+    n = _get().oracle_accept_greedy_chain(pa, pd, K, out.ctypes.data)
+    return out[:n].copy()
+
+
+def accept_greedy_tree(argmax: np.ndarray, tokens: np.ndarray, parent: np.ndarray) -> np.ndarray:
+    argmax, pa = _c(argmax, np.int32)
+    tokens, pt = _c(tokens, np.int32)
+    parent, pp = _c(parent, np.int32)
+    M = tokens.size
+    out = np.empty(M, dtype=np.int32)
+    n = _get().oracle_accept_greedy_tree(pa, pt, pp, M, out.ctypes.data)
+    return out[:n].copy()
+
+
+def philox4x32_10(ctr, key) -> np.ndarray:
+    c, pc = _c(np.array(ctr, dtype=np.uint32), np.uint32)
+    k, pk = _c(np.array(key, dtype=np.uint32), np.uint32)
+    out = np.empty(4, dtype=np.uint32)
+    _get().oracle_philox4x32_10(pc, pk, out.ctypes.data)
+    return out
+
+
+def uniforms(seed: int, pos: int):
+    a = ctypes.c_float()
+    r = ctypes.c_float()
+    _get().oracle_uniforms(seed, pos, ctypes.byref(a), ctypes.byref(r))
+    return a.value, r.value
+
+
+def draw_icdf(w: np.ndarray, u: float) -> int:
+    w, pw = _c(w, np.float32)
+    return int(_get().oracle_draw_icdf(pw, w.size, u))
+
+
+def accept_sample_u(logits, q_probs, drafts, T, u_acc, u_res) -> np.ndarray:
+    logits, pl = _c(logits, np.float32)
+    K1, V = logits.shape
+    K = K1 - 1
+    pq = None
+    if q_probs is not None:
+        q_probs, pq = _c(q_probs, np.float32)
+        assert q_probs.shape == (K, V)
+    drafts, pd = _c(drafts, np.int32)
+    ua, pua = _c(u_acc, np.float32)
+    ur, pur = _c(u_res, np.float32)
+    out = np.empty(K + 1, dtype=np.int32)
+    n = _get().oracle_accept_sample_u(pl, V, K, pq, pd, T, pua, pur, out.ctypes.data)
+    return out[:n].copy()
+
+
+def accept_sample(logits, q_probs, drafts, T: float, seed: int, base_pos: int) -> np.ndarray:
+    logits, pl = _c(logits, np.float32)
+    K1, V = logits.shape
+    K = K1 - 1
+    pq = None
+    if q_probs is not None:
+        q_probs, pq = _c(q_probs, np.float32)
+        assert q_probs.shape == (K, V)
+    drafts, pd = _c(drafts, np.int32)
+    out = np.empty(K + 1, dtype=np.int32)
+    n = _get().oracle_accept_sample(pl, V, K, pq, pd, T, seed, base_pos, out.ctypes.data)
+    return out[:n].copy()
+
+
+def accept_sample_trials(logits, q_probs, drafts_per_trial, T: float, seed: int, base_pos: int):
+    """Independent repetitions at positions base_pos + t*(K+1).  Returns (counts [n], tokens [n][K+1])."""
+    logits, pl = _c(logits, np.float32)
+    K1, V = logits.shape
+    K = K1 - 1
+    pq = None
+    if q_probs is not None:
+        q_probs, pq = _c(q_probs, np.float32)
+    d, pd = _c(drafts_per_trial, np.int32)
+    n = d.shape[0]
+    counts = np.empty(n, dtype=np.int32)
+    toks = np.full((n, K + 1), -1, dtype=np.int32)
+    _get().oracle_accept_sample_trials(pl, V, K, pq, pd, T, seed, base_pos, n, counts.ctypes.data,
+                                       toks.ctypes.data)
+    return counts, toks
+
+
+# ---------------------------------------------------------------------------
+# Composition of the 27B-shaped projection stack (attention omitted).
+# Per layer: RMSNorm -> requant -> QKV; O takes the requantised V slice (the
+# output of attention whose only key is the token itself); residual add after
+# O and after down; RMSNorm -> gate|up -> SiLU*mul -> requant -> down.  A final
+# RMSNorm feeds the vocabulary head.
+# ---------------------------------------------------------------------------
+
+def stack_layer(h: np.ndarray, wts: dict, norm1: np.ndarray, norm2: np.ndarray, hidden: int, ffn: int,
+                wq: int = Q4_32, eps: float = 1e-6, trace: dict | None = None) -> np.ndarray:
+    M = h.shape[0]
+    q1, s1 = rmsnorm_quant(h, norm1, eps)
+    qkv, _ = qmatmul(wq, wts["qkv"], 3 * hidden, hidden, q1, s1)
+    qv, sv = rmsnorm_quant(np.ascontiguousarray(qkv[:, 2 * hidden:]), None)
+    h2, _ = qmatmul(wq, wts["o"], hidden, hidden, qv, sv, residual=h)
+    q3, s3 = rmsnorm_quant(h2, norm2, eps)
+    gu, _ = qmatmul(wq, wts["gate_up"], 2 * ffn, hidden, q3, s3)
+    q4, s4, _ = silu_mul_requant(np.ascontiguousarray(gu[:, :ffn]), np.ascontiguousarray(gu[:, ffn:]))
+    h3, _ = qmatmul(wq, wts["down"], hidden, ffn, q4, s4, residual=h2)
+    if trace is not None:
+        trace.update(q1=q1, s1=s1, qkv=qkv, qv=qv, sv=sv, h2=h2, q3=q3, s3=s3, gu=gu, q4=q4, s4=s4, h3=h3)
+    return h3
+
+
+def head(h: np.ndarray, final_norm: np.ndarray, head_w: np.ndarray, vocab: int, hidden: int, T: float = 1.0,
+         eps: float = 1e-6, head_q: int = Q8_0):
+    """Returns (logits, argmax, row_max, row_sumexp)."""
+    q, s = rmsnorm_quant(h, final_norm, eps)
+    logits, _ = qmatmul(head_q, head_w, vocab, hidden, q, s)
+    m, z, a = softmax_stats(logits, T)
+    return logits, a, m, z

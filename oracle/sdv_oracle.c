@@ -1,0 +1,506 @@
+/*
+ * sdv_oracle.c - plain, slow, obviously correct CPU oracle for the
+ * speculative-decoding verify pass.
+ *
+ * TEST INFRASTRUCTURE ONLY.  The product (the CUDA library) never links,
+ * loads or calls this file; only the tests, the smoke check and the bench's
+ * CPU-baseline leg do.  It shares no code, header, table or constant
+ * generator with the CUDA path.
+ *
+ * Sources (pages on speculative decoding):
+ *  - "Inside OpenJet Engine: making speculative decoding pay", section
+ *    "One GPU launch for a speculative cycle": GGUF Q8_0 weights, integer
+ *    dot products with int8 activations, requantised activations.
+ *  - "Speculative Decoding with Open-Weights Models" (micrologics), section
+ *    "Mathematical Integrity: Rejection Sampling for LLMs": accept x with
+ *    min(1, p(x)/q(x)); on rejection draw from max(0, p - q) renormalised;
+ *    and its walkthrough: a bonus token from the last row when all drafts pass.
+ *  - "How Kinetic is fast", section "Why the output does not change": greedy
+ *    keeps a guess only when it is the model's top token; a certainty drafter
+ *    keeps x with probability p(x) and otherwise draws from p without x.
+ *    Section "RAD-1": tree drafts, each row seeing only its own path.
+ *
+ * Where a floating-point result decides an integer (an activation code, an
+ * accept decision, a drawn token) the oracle computes it in fp32 in the
+ * canonical order the kernels also use, so both sides take the decision in
+ * the same precision.  Everything else (the matmul) accumulates in fp64.
+ * Build with -ffp-contract=off: every fp32 operation below is one rounding,
+ * and fmaf() is used only where the canonical algorithm says "fused".
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* ------------------------------------------------------------------ */
+/* fp16 decode (IEEE 754 binary16 -> binary32, exact)                  */
+/* ------------------------------------------------------------------ */
+float oracle_f16_to_f32(uint16_t h) {
+    int sign = (h >> 15) & 1, exp = (h >> 10) & 0x1F, man = h & 0x3FF;
+    float v;
+    if (exp == 0) v = ldexpf((float)man, -24);                 /* zero or subnormal */
+    else if (exp == 31) v = man ? NAN : INFINITY;
+    else v = ldexpf((float)(man | 0x400), exp - 25);           /* 1.m * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* ------------------------------------------------------------------ */
+/* Block formats.  Q8_0: fp16 d (little endian) then 32 int8 q; value   */
+/* d*q.  4-bit: fp16 d then 16 bytes, byte j = element j (low nibble)   */
+/* and element j+16 (high nibble); value d*(code-8).                    */
+/* ------------------------------------------------------------------ */
+static int block_bytes(int qtype) { return qtype == 0 ? 34 : 18; }
+
+static float block_scale(const uint8_t *blk) { return oracle_f16_to_f32((uint16_t)(blk[0] | (blk[1] << 8))); }
+
+/* integer weight of element i (0..31) of one block */
+static int block_wq(int qtype, const uint8_t *blk, int i) {
+    if (qtype == 0) return (int)(int8_t)blk[2 + i];
+    int code = i < 16 ? (blk[2 + i] & 0x0F) : (blk[2 + i - 16] >> 4);
+    return code - 8;
+}
+
+void oracle_dequant(int qtype, const uint8_t *blocks, int64_t nblocks, float *out) {
+    int bb = block_bytes(qtype);
+    for (int64_t b = 0; b < nblocks; ++b) {
+        const uint8_t *blk = blocks + b * bb;
+        float d = block_scale(blk);
+        for (int i = 0; i < 32; ++i) out[b * 32 + i] = d * (float)block_wq(qtype, blk, i);
+    }
+}
+
+/* integer block dot: sum_i wq_i * aq_i over one 32-block (exact in int32) */
+static int32_t block_dot(int qtype, const uint8_t *blk, const int8_t *a) {
+    int32_t s = 0;
+    for (int i = 0; i < 32; ++i) s += block_wq(qtype, blk, i) * (int32_t)a[i];
+    return s;
+}
+
+/* dots[m][n][b] for weights [N][K/32] blocks and activations q[M][K] */
+void oracle_block_dots(int qtype, const uint8_t *w, int64_t N, int64_t K, const int8_t *q, int M, int32_t *dots) {
+    int64_t KB = K / 32;
+    int bb = block_bytes(qtype);
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; ++n)
+        for (int m = 0; m < M; ++m)
+            for (int64_t b = 0; b < KB; ++b)
+                dots[((int64_t)m * N + n) * KB + b] = block_dot(qtype, w + (n * KB + b) * bb, q + (int64_t)m * K + b * 32);
+}
+
+/*
+ * Multi-position quantised matmul (one weight read serves all M rows):
+ *   y[m][n] = residual[m][n] + sum_b d_w[n,b] * d_a[m,b] * dot_b(n, m)
+ * accumulated in fp64 and rounded to fp32 once.  absb[m][n] (optional) is the
+ * absolute-sum bound |residual| + sum_b |d_w d_a dot_b| used by the tolerance.
+ */
+void oracle_qmatmul(int qtype, const uint8_t *w, int64_t N, int64_t K, const int8_t *q, const float *scales, int M,
+                    const float *residual, float *y, double *absb) {
+    int64_t KB = K / 32;
+    int bb = block_bytes(qtype);
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; ++n) {
+        for (int m = 0; m < M; ++m) {
+            double acc = 0.0, ab = 0.0;
+            for (int64_t b = 0; b < KB; ++b) {
+                const uint8_t *blk = w + (n * KB + b) * bb;
+                int32_t dot = block_dot(qtype, blk, q + (int64_t)m * K + b * 32);
+                double t = (double)block_scale(blk) * (double)scales[(int64_t)m * KB + b] * (double)dot;
+                acc += t;
+                ab += fabs(t);
+            }
+            if (residual) {
+                acc += (double)residual[(int64_t)m * N + n];
+                ab += fabs((double)residual[(int64_t)m * N + n]);
+            }
+            y[(int64_t)m * N + n] = (float)acc;
+            if (absb) absb[(int64_t)m * N + n] = ab;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* Activation requantisation, per 32-block of a row y:                  */
+/*   amax = max |y|, d = amax / 127 (IEEE division),                    */
+/*   q = round-half-away-from-zero(y / d) clamped to [-127, 127],       */
+/*   q = 0 when d = 0.                                                  */
+/* ------------------------------------------------------------------ */
+static void requant_row(const float *y, int64_t K, int8_t *q, float *scales) {
+    for (int64_t b = 0; b < K / 32; ++b) {
+        float amax = 0.0f;
+        for (int i = 0; i < 32; ++i) {
+            float a = fabsf(y[b * 32 + i]);
+            if (a > amax) amax = a;
+        }
+        float d = amax / 127.0f;
+        scales[b] = d;
+        for (int i = 0; i < 32; ++i) {
+            int v = 0;
+            if (d != 0.0f) {
+                v = (int)roundf(y[b * 32 + i] / d);
+                if (v > 127) v = 127;
+                if (v < -127) v = -127;
+            }
+            q[b * 32 + i] = (int8_t)v;
+        }
+    }
+}
+
+/*
+ * RMSNorm + requantisation of M rows (norm_w == NULL: requantisation only).
+ * Sum of squares in the canonical order: 256 partial sums, partial j adding
+ * x_i*x_i for i = j, j+256, j+512, ... in increasing i; then a pairwise tree
+ * over the partials at strides 128, 64, ..., 1.  mean = s / K,
+ * inv = 1 / sqrt(mean + eps) (correctly rounded division and square root),
+ * y = (x * inv) * w (two rounded multiplies), then requantise.
+ */
+void oracle_rmsnorm_quant(const float *x, const float *norm_w, float eps, int M, int64_t K, int8_t *q, float *scales) {
+    float *y = (float *)malloc((size_t)K * sizeof(float));
+    for (int m = 0; m < M; ++m) {
+        const float *xr = x + (int64_t)m * K;
+        if (norm_w) {
+            float part[256];
+            for (int j = 0; j < 256; ++j) {
+                float s = 0.0f;
+                for (int64_t i = j; i < K; i += 256) s = s + xr[i] * xr[i];
+                part[j] = s;
+            }
+            for (int stride = 128; stride >= 1; stride >>= 1)
+                for (int j = 0; j < stride; ++j) part[j] = part[j] + part[j + stride];
+            float mean = part[0] / (float)K;
+            float inv = 1.0f / sqrtf(mean + eps);
+            for (int64_t i = 0; i < K; ++i) y[i] = (xr[i] * inv) * norm_w[i];
+        } else {
+            memcpy(y, xr, (size_t)K * sizeof(float));
+        }
+        requant_row(y, K, q + (int64_t)m * K, scales + (int64_t)m * (K / 32));
+    }
+    free(y);
+}
+
+/* ------------------------------------------------------------------ */
+/* Canonical exponential cexp(x), used wherever an exponential feeds an */
+/* integer decision.  Cody & Waite argument reduction (W. J. Cody and   */
+/* W. Waite, Software Manual for the Elementary Functions, 1980):       */
+/*   k = rint(x * log2(e)), r = x - k*ln2 with ln2 split into a 16-bit  */
+/*   head (exact times any |k| < 256) and a tail, each applied by one   */
+/*   fused multiply-add; e^r by its Taylor series to degree 7 in Horner */
+/*   form with fused multiply-adds; scale by 2^k as two exact powers of */
+/*   two so that a subnormal result is rounded once.                    */
+/* ------------------------------------------------------------------ */
+float oracle_cexp(float x) {
+    if (x != x) return x;
+    if (x > 100.0f) return INFINITY;
+    if (x < -104.0f) return 0.0f;
+    const float log2e = 1.44269504088896340736f;
+    const float ln2_hi = 0.693145751953125f;           /* ln 2 truncated to 16 significant bits */
+    const float ln2_lo = 1.42860682030941723212e-6f;   /* ln 2 - ln2_hi */
+    float k = rintf(x * log2e);
+    float r = fmaf(-k, ln2_hi, x);
+    r = fmaf(-k, ln2_lo, r);
+    /* 1/n! for n = 7 .. 0 */
+    float p = 1.0f / 5040.0f;
+    p = fmaf(p, r, 1.0f / 720.0f);
+    p = fmaf(p, r, 1.0f / 120.0f);
+    p = fmaf(p, r, 1.0f / 24.0f);
+    p = fmaf(p, r, 1.0f / 6.0f);
+    p = fmaf(p, r, 0.5f);
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
+    int ki = (int)k;
+    int k1 = ki / 2, k2 = ki - k1;                      /* both within [-76, 76] */
+    return (p * ldexpf(1.0f, k1)) * ldexpf(1.0f, k2);
+}
+
+/* ------------------------------------------------------------------ */
+/* SiLU gate: h = silu(g) * u with silu(g) = g / (1 + cexp(-g)), each    */
+/* operation rounded; h is requantised per 32-block like any activation */
+/* ------------------------------------------------------------------ */
+void oracle_silu_mul_requant(const float *g, const float *u, int M, int64_t F, int8_t *q, float *scales, float *h_out) {
+    float *h = (float *)malloc((size_t)F * sizeof(float));
+    for (int m = 0; m < M; ++m) {
+        for (int64_t i = 0; i < F; ++i) {
+            float gv = g[(int64_t)m * F + i];
+            float s = gv / (1.0f + oracle_cexp(-gv));
+            h[i] = s * u[(int64_t)m * F + i];
+        }
+        if (h_out) memcpy(h_out + (int64_t)m * F, h, (size_t)F * sizeof(float));
+        requant_row(h, F, q + (int64_t)m * F, scales + (int64_t)m * (F / 32));
+    }
+    free(h);
+}
+
+/* ------------------------------------------------------------------ */
+/* Softmax statistics over a vocabulary row, z_i = l_i / T.             */
+/* Tiles of 1024 consecutive tokens (the last one shorter).  Per tile:  */
+/* m_t = max z, s_t = pairwise tree over 1024 slots (zero padded) of     */
+/* cexp(z_i - m_t) at strides 512, 256, ..., 1.  m = max_t m_t and       */
+/* Z = sequential fold over t of s_t * cexp(m_t - m).  Argmax is over the */
+/* raw logits (temperature free), lowest index among equal maxima.       */
+/* p_i = cexp(z_i - m) / Z.                                              */
+/* ------------------------------------------------------------------ */
+#define TILE 1024
+
+static float tree1024(float *v) {
+    for (int s = TILE / 2; s >= 1; s >>= 1)
+        for (int j = 0; j < s; ++j) v[j] = v[j] + v[j + s];
+    return v[0];
+}
+
+static void row_stats(const float *l, int64_t V, float T, float *row_max, float *row_sumexp, int32_t *argmax) {
+    int64_t nt = (V + TILE - 1) / TILE;
+    float *mt = (float *)malloc((size_t)nt * sizeof(float)), *st = (float *)malloc((size_t)nt * sizeof(float));
+    float v[TILE];
+    int64_t best = 0;
+    float bestv = l[0];
+    for (int64_t t = 0; t < nt; ++t) {
+        int64_t i0 = t * TILE, n = V - i0 < TILE ? V - i0 : TILE;
+        float m = -INFINITY;
+        for (int64_t i = 0; i < n; ++i) {
+            float z = l[i0 + i] / T;
+            if (z > m) m = z;
+            if (l[i0 + i] > bestv) { bestv = l[i0 + i]; best = i0 + i; }
+        }
+        for (int64_t i = 0; i < TILE; ++i) v[i] = i < n ? oracle_cexp(l[i0 + i] / T - m) : 0.0f;
+        mt[t] = m;
+        st[t] = tree1024(v);
+    }
+    float m = -INFINITY;
+    for (int64_t t = 0; t < nt; ++t) if (mt[t] > m) m = mt[t];
+    float Z = 0.0f;
+    for (int64_t t = 0; t < nt; ++t) Z = Z + st[t] * oracle_cexp(mt[t] - m);
+    if (row_max) *row_max = m;
+    if (row_sumexp) *row_sumexp = Z;
+    if (argmax) *argmax = (int32_t)best;
+    free(mt);
+    free(st);
+}
+
+void oracle_softmax_stats(const float *logits, int M, int64_t V, float T, float *row_max, float *row_sumexp, int32_t *argmax) {
+    for (int m = 0; m < M; ++m)
+        row_stats(logits + (int64_t)m * V, V, T, row_max + m, row_sumexp + m, argmax + m);
+}
+
+void oracle_softmax_probs(const float *logits, int64_t V, float T, float row_max, float row_sumexp, float *p) {
+    for (int64_t i = 0; i < V; ++i) p[i] = oracle_cexp(logits[i] / T - row_max) / row_sumexp;
+}
+
+/* ------------------------------------------------------------------ */
+/* Greedy acceptance.                                                   */
+/* Chain: row 0 holds the current token and rows 1..K the drafts; row i */
+/* predicts the token after position i.  n = largest j with             */
+/* drafts[i-1] == argmax[i-1] for all i <= j; emit drafts[0..n-1] then  */
+/* argmax[n].  Returns the count n + 1.                                 */
+/* Tree: node 0 is the root, parent[i] < i.  Node i is accepted when    */
+/* its parent is and tokens[i] == argmax[parent[i]].  The deepest       */
+/* accepted node (lowest index among equals) ends the emitted path:     */
+/* its tokens from the root's child down, then that node's argmax.      */
+/* ------------------------------------------------------------------ */
+int oracle_accept_greedy_chain(const int32_t *argmax, const int32_t *drafts, int K, int32_t *out) {
+    int n = 0;
+    while (n < K && drafts[n] == argmax[n]) { out[n] = drafts[n]; ++n; }
+    out[n] = argmax[n];
+    return n + 1;
+}
+
+int oracle_accept_greedy_tree(const int32_t *argmax, const int32_t *tokens, const int32_t *parent, int M, int32_t *out) {
+    int *ok = (int *)calloc((size_t)M, sizeof(int)), *depth = (int *)calloc((size_t)M, sizeof(int));
+    ok[0] = 1;
+    int best = 0;
+    for (int i = 1; i < M; ++i) {
+        int p = parent[i];
+        if (p < 0 || p >= i) continue; /* malformed: not accepted */
+        depth[i] = depth[p] + 1;
+        ok[i] = ok[p] && tokens[i] == argmax[p];
+        if (ok[i] && depth[i] > depth[best]) best = i;
+    }
+    int d = depth[best];
+    for (int i = best, j = d - 1; i != 0; i = parent[i], --j) out[j] = tokens[i];
+    out[d] = argmax[best];
+    free(ok);
+    free(depth);
+    return d + 1;
+}
+
+/* ------------------------------------------------------------------ */
+/* Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: */
+/* as easy as 1, 2, 3", SC'11).  One round: the two 32x32->64 products  */
+/* of counter words 0 and 2 with the round multipliers; the new counter */
+/* is (hi(c2*M1) ^ c1 ^ k0, lo(c2*M1), hi(c0*M0) ^ c3 ^ k1, lo(c0*M0)). */
+/* The key is bumped by the Weyl constants between rounds.              */
+/* ------------------------------------------------------------------ */
+void oracle_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4]) {
+    uint32_t c[4] = {ctr_in[0], ctr_in[1], ctr_in[2], ctr_in[3]};
+    uint32_t k0 = key_in[0], k1 = key_in[1];
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) { k0 += 0x9E3779B9u; k1 += 0xBB67AE85u; }
+        uint64_t p0 = (uint64_t)0xD2511F53u * c[0];
+        uint64_t p1 = (uint64_t)0xCD9E8D57u * c[2];
+        uint32_t n0 = (uint32_t)(p1 >> 32) ^ c[1] ^ k0;
+        uint32_t n1 = (uint32_t)p1;
+        uint32_t n2 = (uint32_t)(p0 >> 32) ^ c[3] ^ k1;
+        uint32_t n3 = (uint32_t)p0;
+        c[0] = n0; c[1] = n1; c[2] = n2; c[3] = n3;
+    }
+    memcpy(out, c, sizeof(c));
+}
+
+/* uniforms of position pos: word 0 -> accept test, word 1 -> residual or bonus draw,
+ * u = (word >> 8) * 2^-24 in [0, 1) */
+void oracle_uniforms(uint64_t seed, int64_t pos, float *u_acc, float *u_res) {
+    uint32_t ctr[4] = {(uint32_t)(uint64_t)pos, (uint32_t)((uint64_t)pos >> 32), 0, 0};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t o[4];
+    oracle_philox4x32_10(ctr, key, o);
+    *u_acc = (float)(o[0] >> 8) * 5.9604644775390625e-08f;
+    *u_res = (float)(o[1] >> 8) * 5.9604644775390625e-08f;
+}
+
+/* ------------------------------------------------------------------ */
+/* Inverse-CDF draw from unnormalised non-negative weights w[V] with a  */
+/* uniform u: S_t = 1024-slot tree sums (as in the softmax tiles),      */
+/* S = sequential fold, target = u * S; the first tile whose running    */
+/* fold exceeds target (else the last tile with S_t > 0); inside it, 32 */
+/* chunks of 32 slots with sequential chunk sums and the same rule;     */
+/* inside the chunk, a sequential running sum and the first slot with   */
+/* w > 0 where it exceeds the remainder (else the chunk's last slot with */
+/* w > 0).  Returns -1 when S is not positive.                          */
+/* ------------------------------------------------------------------ */
+int32_t oracle_draw_icdf(const float *w, int64_t V, float u) {
+    int64_t nt = (V + TILE - 1) / TILE;
+    float *S = (float *)malloc((size_t)nt * sizeof(float));
+    float v[TILE];
+    for (int64_t t = 0; t < nt; ++t) {
+        int64_t i0 = t * TILE;
+        for (int64_t i = 0; i < TILE; ++i) v[i] = i0 + i < V ? w[i0 + i] : 0.0f;
+        S[t] = tree1024(v);
+    }
+    float tot = 0.0f;
+    for (int64_t t = 0; t < nt; ++t) tot = tot + S[t];
+    if (!(tot > 0.0f)) { free(S); return -1; }
+    float target = u * tot;
+    int64_t tsel = -1;
+    float C = 0.0f, Cprev = 0.0f;
+    for (int64_t t = 0; t < nt; ++t) {
+        float Cn = C + S[t];
+        if (Cn > target) { tsel = t; Cprev = C; break; }
+        C = Cn;
+    }
+    if (tsel < 0) {
+        for (int64_t t = nt - 1; t >= 0; --t) if (S[t] > 0.0f) { tsel = t; break; }
+        /* Cprev: the fold up to tile tsel */
+        Cprev = 0.0f;
+        for (int64_t t = 0; t < tsel; ++t) Cprev = Cprev + S[t];
+    }
+    free(S);
+    float rem = target - Cprev;
+    int64_t i0 = tsel * TILE;
+    float c[32];
+    for (int j = 0; j < 32; ++j) {
+        float s = 0.0f;
+        for (int i = 0; i < 32; ++i) {
+            int64_t idx = i0 + j * 32 + i;
+            s = s + (idx < V ? w[idx] : 0.0f);
+        }
+        c[j] = s;
+    }
+    int jsel = -1;
+    float D = 0.0f, Dprev = 0.0f;
+    for (int j = 0; j < 32; ++j) {
+        float Dn = D + c[j];
+        if (Dn > rem) { jsel = j; Dprev = D; break; }
+        D = Dn;
+    }
+    if (jsel < 0) {
+        for (int j = 31; j >= 0; --j) if (c[j] > 0.0f) { jsel = j; break; }
+        Dprev = 0.0f;
+        for (int j = 0; j < jsel; ++j) Dprev = Dprev + c[j];
+    }
+    float rem2 = rem - Dprev;
+    int64_t base = i0 + (int64_t)jsel * 32;
+    float e = 0.0f;
+    int64_t last = -1;
+    for (int i = 0; i < 32; ++i) {
+        int64_t idx = base + i;
+        float wi = idx < V ? w[idx] : 0.0f;
+        e = e + wi;
+        if (wi > 0.0f) {
+            last = idx;
+            if (e > rem2) return (int32_t)idx;
+        }
+    }
+    return (int32_t)last;
+}
+
+/*
+ * Rejection-sampling acceptance over K drafts with explicit uniforms
+ * (u_acc[i], u_res[i] for i = 0..K).  p_i = softmax(l_i / T) as above;
+ * q_i = draft distribution row i, or NULL for a certainty drafter (q one-hot
+ * at the draft).  Draft x = drafts[i] is kept iff u_acc[i] * q_i(x) < p_i(x)
+ * (equivalent to u < min(1, p/q) because u < 1).  On the first rejection the
+ * emitted token is drawn from w = max(0, p_i - q_i) (certainty drafter: p_i
+ * with x zeroed) with u_res[i] and the pass stops; if every draft is kept a
+ * bonus token is drawn from p_K with u_res[K].  If w sums to zero the draw
+ * falls back to p_i.  Returns the count of emitted tokens (kept + 1).
+ */
+int oracle_accept_sample_u(const float *logits, int64_t V, int K, const float *q_probs, const int32_t *drafts,
+                           float T, const float *u_acc, const float *u_res, int32_t *out) {
+    float *p = (float *)malloc((size_t)V * sizeof(float)), *w = (float *)malloc((size_t)V * sizeof(float));
+    int n = 0;
+    for (int i = 0; i <= K; ++i) {
+        const float *l = logits + (int64_t)i * V;
+        float m, Z;
+        row_stats(l, V, T, &m, &Z, NULL);
+        oracle_softmax_probs(l, V, T, m, Z, p);
+        int32_t tok;
+        if (i == K) {
+            tok = oracle_draw_icdf(p, V, u_res[i]);
+        } else {
+            int32_t x = drafts[i];
+            float qx = q_probs ? q_probs[(int64_t)i * V + x] : 1.0f;
+            if (u_acc[i] * qx < p[x]) { out[n++] = x; continue; }
+            for (int64_t j = 0; j < V; ++j) {
+                float qj = q_probs ? q_probs[(int64_t)i * V + j] : (j == x ? 1.0f : 0.0f);
+                float d = p[j] - qj;
+                w[j] = d > 0.0f ? d : 0.0f;
+            }
+            tok = oracle_draw_icdf(w, V, u_res[i]);
+            if (tok < 0) tok = oracle_draw_icdf(p, V, u_res[i]);
+        }
+        out[n++] = tok;
+        break;
+    }
+    free(p);
+    free(w);
+    return n;
+}
+
+/* The same with the uniforms of positions base_pos .. base_pos + K from
+ * Philox4x32-10 keyed by seed (counter = position). */
+int oracle_accept_sample(const float *logits, int64_t V, int K, const float *q_probs, const int32_t *drafts,
+                         float T, uint64_t seed, int64_t base_pos, int32_t *out) {
+    float ua[64], ur[64];
+    if (K > 63) return -1;
+    for (int i = 0; i <= K; ++i) oracle_uniforms(seed, base_pos + i, &ua[i], &ur[i]);
+    return oracle_accept_sample_u(logits, V, K, q_probs, drafts, T, ua, ur, out);
+}
+
+/* n_trials independent repetitions at positions base_pos + t*(K+1); writes
+ * each trial's count and tokens (row-major [n_trials][K+1]). */
+void oracle_accept_sample_trials(const float *logits, int64_t V, int K, const float *q_probs, const int32_t *drafts_per_trial,
+                                 float T, uint64_t seed, int64_t base_pos, int64_t n_trials, int32_t *counts, int32_t *tokens) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < n_trials; ++t)
+        counts[t] = oracle_accept_sample(logits, V, K, q_probs, drafts_per_trial + t * K, T, seed,
+                                         base_pos + t * (K + 1), tokens + t * (K + 1));
+}

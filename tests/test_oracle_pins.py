@@ -1,0 +1,460 @@
+"""Pins of the CPU oracle against things other than itself (no GPU needed).
+
+Each test fixes an oracle function to an independent truth: a numpy library
+routine applied to integer codes the test chose itself, a closed form, the
+worked example on the Kinetic page, published Philox known-answer vectors,
+exact enumeration of the acceptance rule over its uniform grid, or a large
+Monte-Carlo run.  A plausible mistake in the oracle (a swapped nibble, a
+dropped residual, a wrong comparison, a wrong Philox word) fails one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import sdgen
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------------------
+# helpers: pack chosen integer codes into GGUF block bytes (format definition)
+# ---------------------------------------------------------------------------
+
+def pack_blocks(qtype, wq, d16):
+    """wq int [N][K] (Q8_0: -127..127; 4-bit: -8..7), d16 float16 [N][K/32] -> block bytes."""
+    N, K = wq.shape
+    KB = K // 32
+    bb = oracle.BLOCK_BYTES[qtype]
+    out = np.zeros((N, KB, bb), dtype=np.uint8)
+    out[:, :, 0:2] = d16.astype(np.float16).view(np.uint8).reshape(N, KB, 2)
+    w = wq.reshape(N, KB, 32)
+    if qtype == oracle.Q8_0:
+        out[:, :, 2:] = w.astype(np.int8).view(np.uint8)
+    else:
+        code = (w + 8).astype(np.uint8)
+        out[:, :, 2:] = code[:, :, :16] | (code[:, :, 16:] << 4)
+    return out.reshape(N, KB * bb)
+
+
+def rand_case(rng, qtype, N, K, M):
+    lim = 127 if qtype == oracle.Q8_0 else 8
+    wq = rng.integers(-lim, lim if qtype == oracle.Q4_32 else lim + 1, size=(N, K))
+    d16 = (rng.random((N, K // 32)) * 1e-3 + 1e-5).astype(np.float16)
+    aq = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+    sa = (rng.random((M, K // 32)) * 0.05 + 1e-3).astype(np.float32)
+    return wq, d16, aq, sa
+
+
+# ---------------------------------------------------------------------------
+# fp16 decode
+# ---------------------------------------------------------------------------
+
+def test_f16_decode_all_patterns():
+    bits = np.arange(65536, dtype=np.uint16)
+    ref = bits.view(np.float16).astype(np.float32)
+    got = np.array([oracle.f16_to_f32(int(b)) for b in bits[::7]], dtype=np.float32)
+    r = ref[::7]
+    nan = np.isnan(r)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), r[~nan].view(np.uint32))
+
+
+# ---------------------------------------------------------------------------
+# block dots and dequant: numpy integer matmul on codes the test chose
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("qtype", [oracle.Q8_0, oracle.Q4_32])
+def test_block_dots_match_numpy_integer_matmul(qtype):
+    rng = np.random.default_rng(1)
+    N, K, M = 37, 256, 5
+    wq, d16, aq, _ = rand_case(rng, qtype, N, K, M)
+    blocks = pack_blocks(qtype, wq, d16)
+    dots = oracle.block_dots(qtype, blocks, N, K, aq)
+    KB = K // 32
+    ref = np.einsum("nbi,mbi->mnb", wq.reshape(N, KB, 32).astype(np.int64),
+                    aq.reshape(M, KB, 32).astype(np.int64))
+    assert np.array_equal(dots, ref)
+    bound = 516128 if qtype == oracle.Q8_0 else 32 * 8 * 127
+    assert np.abs(dots).max() <= bound
+
+
+def test_block_dots_extremes_and_q4_identity():
+    # extremes: every product at its maximum magnitude
+    N, K = 2, 32
+    wq8 = np.full((N, K), 127)
+    wq8[1] = -127
+    a = np.full((1, K), -127, dtype=np.int8)
+    blk = pack_blocks(oracle.Q8_0, wq8, np.ones((N, 1), np.float16))
+    assert list(oracle.block_dots(oracle.Q8_0, blk, N, K, a)[0, :, 0]) == [-516128, 516128]
+    # 4-bit: sum (code-8) a == sum code*a - 8 sum a
+    rng = np.random.default_rng(2)
+    wq = rng.integers(-8, 8, size=(3, 64))
+    aq = rng.integers(-127, 128, size=(2, 64)).astype(np.int8)
+    blk = pack_blocks(oracle.Q4_32, wq, np.ones((3, 2), np.float16))
+    dots = oracle.block_dots(oracle.Q4_32, blk, 3, 64, aq).astype(np.int64)
+    code = (wq + 8).reshape(3, 2, 32).astype(np.int64)
+    a = aq.reshape(2, 2, 32).astype(np.int64)
+    alt = np.einsum("nbi,mbi->mnb", code, a) - 8 * a.sum(axis=2)[:, None, :]
+    assert np.array_equal(dots, alt)
+
+
+@pytest.mark.parametrize("qtype", [oracle.Q8_0, oracle.Q4_32])
+def test_dequant_matches_codes_times_fp16_scale(qtype):
+    rng = np.random.default_rng(3)
+    wq, d16, _, _ = rand_case(rng, qtype, 9, 128, 1)
+    v = oracle.dequant(qtype, pack_blocks(qtype, wq, d16), 9, 128)
+    ref = (np.repeat(d16.astype(np.float32), 32, axis=1).astype(np.float64) * wq).astype(np.float32)
+    assert np.array_equal(v, ref)
+
+
+@pytest.mark.parametrize("qtype", [oracle.Q8_0, oracle.Q4_32])
+def test_generator_roundtrip_error_bound(qtype):
+    # weights ~ N(0, 0.02) quantised by the generator: |w - dequant| <= d/2 (plus fp16 rounding of d)
+    N, K = 64, 512
+    k = sdgen.key(99, qtype)
+    w = sdgen.normal(k, (N, K), std=0.02)
+    blocks = sdgen.quantize(qtype, w)
+    assert np.array_equal(blocks, sdgen.quantized_normal(qtype, k, N, K, std=0.02))
+    v = oracle.dequant(qtype, blocks, N, K)
+    amax = np.abs(w.reshape(N, K // 32, 32)).max(axis=2)
+    d = amax / (127.0 if qtype == oracle.Q8_0 else 7.5)
+    lev = 127 if qtype == oracle.Q8_0 else 8
+    bound = np.repeat(d * 0.5 + amax * 2.0 ** -11 * (lev / (lev - 1)) + 1e-12, 32, axis=1)
+    assert np.all(np.abs(w - v) <= bound)
+
+
+# ---------------------------------------------------------------------------
+# multi-position matmul: numpy float64 matmul of dequantised operands
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("qtype", [oracle.Q8_0, oracle.Q4_32])
+@pytest.mark.parametrize("with_residual", [False, True])
+def test_qmatmul_matches_numpy_float64(qtype, with_residual):
+    rng = np.random.default_rng(4)
+    N, K, M = 45, 320, 5
+    wq, d16, aq, sa = rand_case(rng, qtype, N, K, M)
+    blocks = pack_blocks(qtype, wq, d16)
+    res = rng.standard_normal((M, N)).astype(np.float32) if with_residual else None
+    y, ab = oracle.qmatmul(qtype, blocks, N, K, aq, sa, residual=res)
+    W = oracle.dequant(qtype, blocks, N, K).astype(np.float64)
+    A = aq.astype(np.float64) * np.repeat(sa.astype(np.float64), 32, axis=1)
+    ref = A @ W.T
+    absref = np.abs(A) @ np.abs(W).T
+    if res is not None:
+        ref = ref + res
+        absref = absref + np.abs(res)
+    assert np.all(np.abs(y.astype(np.float64) - ref) <= 2.0 ** -24 * np.abs(ref) + 1e-12 * absref + 1e-30)
+    assert np.all(ab >= np.abs(y) * (1 - 1e-6))
+    # the absolute bound is >= the per-block absolute sum, and equals it for sign-aligned data
+    assert np.all(ab <= absref * (1 + 1e-12) + 1e-30)
+
+
+# ---------------------------------------------------------------------------
+# RMSNorm + requantisation
+# ---------------------------------------------------------------------------
+
+def test_rmsnorm_constant_row_closed_form():
+    K = 1024
+    c = 0.5  # c*c and all partial sums are exact, so mean == c*c exactly
+    x = np.full((1, K), c, dtype=np.float32)
+    w = sdgen.norm_weight(sdgen.key(5), K)
+    q, s = oracle.rmsnorm_quant(x, w, 1e-6)
+    inv = np.float32(1.0) / np.sqrt(np.float32(c * c) + np.float32(1e-6), dtype=np.float32)
+    y = (np.float32(c) * inv) * w
+    closed = w.astype(np.float64) * c / math.sqrt(c * c + 1e-6)
+    assert np.all(np.abs(y - closed) <= 4 * np.spacing(np.abs(closed).astype(np.float32)))
+    yb = y.reshape(1, K // 32, 32)
+    d = np.abs(yb).max(axis=2) / np.float32(127.0)
+    assert np.array_equal(s, d.astype(np.float32))
+    deq = q.reshape(1, K // 32, 32).astype(np.float64) * s[..., None]
+    assert np.all(np.abs(deq - yb) <= s[..., None] * 0.5 * (1 + 1e-6))
+
+
+@pytest.mark.parametrize("K", [1024, 5120, 17408])
+def test_rmsnorm_quant_vs_float64_definition(K):
+    M = 3
+    x = sdgen.normal(sdgen.key(6, K), (M, K))
+    x[1] *= 40.0
+    x[2, :32] = 0.0  # an all-zero block: d = 0, q = 0
+    w = sdgen.norm_weight(sdgen.key(7, K), K)
+    q, s = oracle.rmsnorm_quant(x, w, 1e-6)
+    x64 = x.astype(np.float64)
+    y = x64 / np.sqrt((x64 ** 2).mean(axis=1, keepdims=True) + 1e-6) * w
+    deq = q.astype(np.float64) * np.repeat(s.astype(np.float64), 32, axis=1)
+    tol = np.repeat(s.astype(np.float64), 32, axis=1) * 0.5 + np.abs(y) * 1e-6 + 1e-30
+    assert np.all(np.abs(deq - y) <= tol)
+    qb = np.abs(q.reshape(M, K // 32, 32).astype(np.int32)).max(axis=2)
+    assert np.all((qb == 127) | (s == 0))
+    # requantise-only mode is the identity norm
+    q2, s2 = oracle.rmsnorm_quant(x, None)
+    deq2 = q2.astype(np.float64) * np.repeat(s2.astype(np.float64), 32, axis=1)
+    assert np.all(np.abs(deq2 - x64) <= np.repeat(s2, 32, axis=1) * 0.5 * (1 + 1e-6) + 1e-30)
+
+
+# ---------------------------------------------------------------------------
+# canonical exponential
+# ---------------------------------------------------------------------------
+
+def test_cexp_within_2ulp_of_fp64_exp():
+    xs = np.concatenate([np.linspace(-103.9, 88.7, 200001, dtype=np.float32),
+                         np.float32(np.random.default_rng(8).standard_normal(20000) * 5)])
+    got = oracle.cexp(xs).astype(np.float64)
+    ref = np.exp(xs.astype(np.float64))
+    fin = np.isfinite(got) & (ref < 3.0e38) & (ref > 1.2e-38)
+    ulp = np.spacing(ref[fin].astype(np.float32)).astype(np.float64)
+    assert np.max(np.abs(got[fin] - ref[fin]) / ulp) <= 2.0
+    assert oracle.cexp([0.0])[0] == 1.0
+    assert oracle.cexp([-200.0])[0] == 0.0 and np.isinf(oracle.cexp([120.0])[0])
+    # subnormal range is rounded once: within one subnormal step
+    xs2 = np.linspace(-103.0, -88.0, 2001, dtype=np.float32)
+    got2 = oracle.cexp(xs2).astype(np.float64)
+    assert np.all(np.abs(got2 - np.exp(xs2.astype(np.float64))) <= 2.0 ** -149 * 2 + np.exp(xs2.astype(np.float64)) * 2.5e-7)
+
+
+def test_silu_mul_requant_vs_float64():
+    M, F = 2, 1024
+    g = sdgen.normal(sdgen.key(9), (M, F)) * 4
+    u = sdgen.normal(sdgen.key(10), (M, F))
+    g[0, :8] = [0.0, -0.0, 90.0, -90.0, 1e-30, -1e-30, 20.0, -20.0]
+    q, s, h = oracle.silu_mul_requant(g, u)
+    g64 = g.astype(np.float64)
+    ref = g64 / (1 + np.exp(-g64)) * u
+    assert np.all(np.abs(h - ref) <= 4 * np.spacing(np.abs(ref).astype(np.float32)) + 1e-37)
+    deq = q.astype(np.float64) * np.repeat(s.astype(np.float64), 32, axis=1)
+    assert np.all(np.abs(deq - h) <= np.repeat(s, 32, axis=1) * 0.5 * (1 + 1e-6) + 1e-30)
+
+
+# ---------------------------------------------------------------------------
+# softmax statistics and argmax
+# ---------------------------------------------------------------------------
+
+def test_softmax_uniform_logits():
+    V = 151936
+    l = np.full((2, V), 3.25, dtype=np.float32)
+    m, z, a = oracle.softmax_stats(l, 1.0)
+    assert list(m) == [3.25, 3.25] and list(z) == [float(V)] * 2 and list(a) == [0, 0]
+    p = oracle.softmax_probs(l[0])
+    assert np.all(p == np.float32(1.0) / np.float32(V))
+
+
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_softmax_stats_vs_float64(T):
+    V = 151936
+    l = sdgen.normal(sdgen.key(11), (3, V)) * 3
+    l[1, 777] = l[1].max() + 1.0
+    l[1, 99999] = l[1, 777]  # tie: lowest index wins
+    l[2, V - 1] = 40.0       # maximum in the short last tile
+    m, z, a = oracle.softmax_stats(l, T)
+    zz = l.astype(np.float64) / T
+    mref = zz.max(axis=1)
+    zref = np.exp(zz - mref[:, None]).sum(axis=1)
+    assert np.array_equal(m, (l / np.float32(T)).max(axis=1))
+    assert np.all(np.abs(z - zref) <= 1e-5 * zref)
+    assert list(a) == list(np.argmax(l, axis=1)) and a[1] == 777 and a[2] == V - 1
+    p = oracle.softmax_probs(l[0], T)
+    pref = np.exp(zz[0] - mref[0]) / zref[0]
+    assert abs(p.astype(np.float64).sum() - 1.0) < 1e-4
+    assert np.all(np.abs(p - pref) <= 1e-5 * pref + 1e-12)
+
+
+# ---------------------------------------------------------------------------
+# greedy acceptance
+# ---------------------------------------------------------------------------
+
+def test_worked_example_rad1():
+    g = json.load(open(os.path.join(GOLDEN, "rad1_worked_example.json")))
+    for case in g["cases"].values():
+        kept = oracle.accept_greedy_chain(np.array(case["argmax"]), np.array(case["drafts"]))
+        assert list(kept) == case["kept"]
+        assert len(kept) - 1 == case["accepted"]
+
+
+def test_greedy_chain_edges():
+    am = np.array([5, 6, 7, 8], dtype=np.int32)
+    assert list(oracle.accept_greedy_chain(am[:1], np.array([], np.int32))) == [5]          # K = 0
+    assert list(oracle.accept_greedy_chain(am, np.array([5, 6, 7]))) == [5, 6, 7, 8]        # all kept + bonus
+    assert list(oracle.accept_greedy_chain(am, np.array([4, 6, 7]))) == [5]                 # first rejected
+    assert list(oracle.accept_greedy_chain(am, np.array([5, 6, 0]))) == [5, 6, 7]           # last rejected
+
+
+def test_greedy_tree_chain_special_case_and_example():
+    rng = np.random.default_rng(12)
+    for _ in range(200):
+        K = int(rng.integers(0, 8))
+        am = rng.integers(0, 4, size=K + 1).astype(np.int32)
+        dr = rng.integers(0, 4, size=K).astype(np.int32)
+        chain = oracle.accept_greedy_chain(am, dr)
+        tokens = np.concatenate([[9], dr]).astype(np.int32)
+        parent = np.arange(-1, K, dtype=np.int32)
+        assert list(oracle.accept_greedy_tree(am, tokens, parent)) == list(chain)
+    # 16-node tree: root, binary depth 3, spine below node 7.  Argmax chain along 0->1->3->7->15.
+    parent, depth = sdgen.tree16(0)
+    am = np.arange(100, 116, dtype=np.int32)
+    tokens = np.full(16, 1, dtype=np.int32)
+    tokens[1], tokens[3], tokens[7], tokens[15] = am[0], am[1], am[3], am[7]
+    tokens[2] = am[0]          # a sibling that also matches the root's argmax
+    tokens[5] = am[2]          # ... and its child too (depth 2), shorter than the main path
+    kept = oracle.accept_greedy_tree(am, tokens, parent)
+    assert list(kept) == [am[0], am[1], am[3], am[7], am[15]]
+    # equal-depth tie: lowest BFS index wins
+    tokens2 = np.full(16, 1, dtype=np.int32)
+    tokens2[1], tokens2[2] = am[0], am[0]
+    tokens2[3], tokens2[5] = am[1], am[2]
+    assert list(oracle.accept_greedy_tree(am, tokens2, parent)) == [am[0], am[1], am[3]]
+
+
+def test_drafted_greedy_equals_plain_greedy_toy_model():
+    """A toy deterministic model: embedding -> 2-layer stack -> head.  Decoding with
+    drafts verified in one batched pass gives exactly the plain greedy sequence."""
+    Vt, H, F, L = 256, 64, 96, 2
+    E = sdgen.normal(sdgen.key(20), (Vt, H))
+    wts = []
+    for l in range(L):
+        wts.append(dict(qkv=sdgen.quantized_normal(sdgen.Q4_32, sdgen.key(21, l), 3 * H, H, std=0.2),
+                        o=sdgen.quantized_normal(sdgen.Q4_32, sdgen.key(22, l), H, H, std=0.2),
+                        gate_up=sdgen.quantized_normal(sdgen.Q4_32, sdgen.key(23, l), 2 * F, H, std=0.2),
+                        down=sdgen.quantized_normal(sdgen.Q4_32, sdgen.key(24, l), H, F, std=0.2)))
+    n1 = [sdgen.norm_weight(sdgen.key(25, l), H) for l in range(L)]
+    n2 = [sdgen.norm_weight(sdgen.key(26, l), H) for l in range(L)]
+    fn = sdgen.norm_weight(sdgen.key(27), H)
+    hw = sdgen.quantized_normal(sdgen.Q8_0, sdgen.key(28), Vt, H, std=0.2)
+
+    def argmax_rows(tokens):
+        h = E[np.asarray(tokens)]
+        for l in range(L):
+            h = oracle.stack_layer(h, wts[l], n1[l], n2[l], H, F)
+        return oracle.head(h, fn, hw, Vt, H)[1]
+
+    t0, steps = 3, 24
+    plain = [t0]
+    for _ in range(steps):
+        plain.append(int(argmax_rows([plain[-1]])[0]))
+    rng = np.random.default_rng(29)
+    out = [t0]
+    K = 4
+    while len(out) < steps + 1:
+        cur = out[-1]
+        # noisy drafter: the true next token with prob 0.75, else random
+        drafts = []
+        prev = cur
+        for _ in range(K):
+            nxt = int(argmax_rows([prev])[0]) if rng.random() < 0.75 else int(rng.integers(0, Vt))
+            drafts.append(nxt)
+            prev = nxt
+        am = argmax_rows([cur] + drafts)
+        out.extend(int(t) for t in oracle.accept_greedy_chain(am, np.array(drafts, np.int32)))
+    assert out[:steps + 1] == plain
+
+
+# ---------------------------------------------------------------------------
+# Philox4x32-10
+# ---------------------------------------------------------------------------
+
+def test_philox_known_answer_vectors():
+    g = json.load(open(os.path.join(GOLDEN, "philox4x32_10_kat.json")))
+    for v in g["vectors"]:
+        out = oracle.philox4x32_10([int(x, 16) for x in v["ctr"]], [int(x, 16) for x in v["key"]])
+        assert [f"{int(x):08x}" for x in out] == v["out"]
+
+
+def test_philox_uniforms_properties():
+    n = 200000
+    ua = np.empty(n)
+    ur = np.empty(n)
+    for i in range(n):
+        ua[i], ur[i] = oracle.uniforms(1234, i)
+    for u in (ua, ur):
+        assert u.min() >= 0.0 and u.max() < 1.0
+        assert np.all(u * 2 ** 24 == np.floor(u * 2 ** 24))
+        h, _ = np.histogram(u, bins=64, range=(0, 1))
+        chi2 = ((h - n / 64) ** 2 / (n / 64)).sum()
+        assert chi2 < 120  # 63 dof; p ~ 1e-5
+    assert abs(np.corrcoef(ua, ur)[0, 1]) < 0.01
+    assert abs(np.corrcoef(ua[:-1], ua[1:])[0, 1]) < 0.01
+
+
+# ---------------------------------------------------------------------------
+# rejection sampling: exact enumeration over the uniform grid + Monte Carlo
+# ---------------------------------------------------------------------------
+
+def _grid_law(fn, n_bits=24):
+    """Exact law of fn(u) over the uniform grid u = k 2^-24 (k < 2^24) for fn piecewise
+    constant in u with few pieces: binary-search the breakpoints."""
+    N = 1 << n_bits
+    law = {}
+    k = 0
+    while k < N:
+        tok = fn(k / N)
+        lo, hi = k, N
+        while hi - lo > 1:
+            mid = (lo + hi) // 2
+            if fn(mid / N) == tok:
+                lo = mid
+            else:
+                hi = mid
+        law[tok] = law.get(tok, 0) + (hi - k)
+        k = hi
+    return {t: c / N for t, c in law.items()}
+
+
+@pytest.mark.parametrize("certainty", [False, True])
+def test_rejection_sampling_exact_law(certainty):
+    """Emitted-token law of one verified draft, enumerated exactly over the uniforms,
+    equals the target distribution p (the rejection-sampling guarantee)."""
+    V = 16
+    l = sdgen.normal(sdgen.key(40), (2, V)) * 1.5
+    p = oracle.softmax_probs(l[0]).astype(np.float64)
+    qrow = None if certainty else oracle.softmax_probs(l[0] + sdgen.normal(sdgen.key(41), (V,)))
+    qfull = None if certainty else qrow[None, :]
+    top = 1.0 - 2.0 ** -24
+    for x in range(V) if certainty else [None]:
+        law = np.zeros(V)
+        for xd in ([x] if certainty else range(V)):
+            dr = np.array([xd], np.int32)
+            qx = 1.0 if certainty else float(qrow[xd])
+            acc = _grid_law(lambda u: len(oracle.accept_sample_u(l, qfull, dr, 1.0, [u, 0.0], [0.0, 0.0])) == 2)
+            pacc = acc.get(True, 0.0)
+            assert abs(pacc - min(1.0, p[xd] / qx)) <= 2.0 ** -23
+            weight = 1.0 if certainty else qx
+            law[xd] += weight * pacc
+            if pacc < 1.0:
+                res = _grid_law(lambda u: int(oracle.accept_sample_u(l, qfull, dr, 1.0, [top, 0.0], [u, 0.0])[0]))
+                qv = np.eye(V)[xd] if certainty else qrow.astype(np.float64)
+                w = np.maximum(0.0, p - qv)
+                r = w / w.sum()
+                for t, pr in res.items():
+                    assert abs(pr - r[t]) <= 2e-6
+                    law[t] += weight * (1 - pacc) * pr
+        assert np.all(np.abs(law - p) <= 4e-6), np.abs(law - p).max()
+
+
+@pytest.mark.parametrize("certainty", [False, True])
+def test_rejection_sampling_monte_carlo_1e6(certainty):
+    V, K, n = 16, 2, 1_000_000
+    l = sdgen.normal(sdgen.key(50), (K + 1, V)) * 1.5
+    if certainty:
+        q = None
+        # a fixed certainty draft per row (the drafter's single guess)
+        drafts = np.tile(np.array([3, 11], np.int32), (n, 1))
+    else:
+        q = np.stack([oracle.softmax_probs(l[i] + sdgen.normal(sdgen.key(51, i), (V,))) for i in range(K)])
+        # drafts sampled from q (input synthesis, independent of the verify uniforms)
+        u = sdgen.uniforms(sdgen.key(52), n * K).reshape(n, K)
+        cdf = np.cumsum(q.astype(np.float64), axis=1)
+        drafts = np.stack([np.minimum(np.searchsorted(cdf[i] / cdf[i, -1], u[:, i], side="right"), V - 1)
+                           for i in range(K)], axis=1).astype(np.int32)
+    counts, toks = oracle.accept_sample_trials(l, q, drafts, 1.0, seed=777, base_pos=0)
+    assert np.all((counts >= 1) & (counts <= K + 1))
+    p0 = oracle.softmax_probs(l[0]).astype(np.float64)
+    p1 = oracle.softmax_probs(l[1]).astype(np.float64)
+    for p, sel in ((p0, toks[:, 0]), (p1, toks[counts >= 2, 1])):
+        N = sel.size
+        freq = np.bincount(sel, minlength=V) / N
+        sigma = np.sqrt(p * (1 - p) / N)
+        assert np.all(np.abs(freq - p) <= 3 * sigma + 1e-12), (freq - p) / sigma
+        chi2 = (((freq - p) * N) ** 2 / (p * N)).sum()
+        assert chi2 < 45  # 15 dof: p ~ 1e-4
