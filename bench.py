@@ -1,0 +1,473 @@
+"""Benchmark of the speculative-decoding verify pass on GB300.
+
+Workload (default): the 27B-shaped dense projection stack -- 64 layers of
+RMSNorm -> 4-bit QKV 5120->15360 -> O 5120->5120 (+residual) -> RMSNorm ->
+4-bit gate|up 5120->2x17408 -> SiLU*mul -> requant -> down 17408->5120
+(+residual) -- then a final RMSNorm, the 5120x151936 Q8_0 head with fused
+argmax/softmax statistics and greedy acceptance of K = 4 drafts (M = K+1 = 5
+positions).  Weights N(0, 0.02) block-quantised, hidden rows N(0, 1), synthetic
+and seeded.  One step = one verify pass; its 14.23 GB of weights are read from
+HBM once per step (far above the 129 MB L2, so no step reuses another's data).
+
+Prints one JSON line: metric = weight-stream GB/s of the pass (value), with
+verified positions/s, the HBM fraction, the dominant kernel's roofline, the
+clocks seen during the timed region, an end-to-end figure through host buffers
+and the CPU oracle's throughput on a bounded sample of the same work.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "weight-stream GB/s (% of HBM peak) per verify pass at K+1=5; verified pos/s"
+NOMINAL_HBM_GBS = 8000.0
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        if self.proc is None:
+            return out
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append(f)
+            except Exception:
+                pass
+        os.unlink(self.path)
+        sm = sorted(float(r[1]) for r in rows if r[1].replace(".", "").isdigit())
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for nm, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        out.update(sm_mhz=sm[len(sm) // 2] if sm else None, sm_max_mhz=max(mx) if mx else None,
+                   reasons=sorted(reasons), samples=len(rows))
+        return out
+
+
+# ---------------------------------------------------------------------------
+# model construction
+# ---------------------------------------------------------------------------
+def build_stack(spec, M, device, timings):
+    import numpy as np
+    import torch
+
+    import sdgen
+    from speculative_decoding_verify_gb300.verify_pass import VerifyStack, repack_matrix
+
+    t0 = time.time()
+    layers, norms = [], []
+    for l in range(spec.layers):
+        lw = {}
+        for name, n, k in spec.matrices():
+            blocks = sdgen.pinned_quantized_normal(spec.wq, spec.weight_key(l, name), n, k)
+            lw[name] = repack_matrix(spec.wq, blocks, n, k, pair=(name == "gate_up"), device=device)
+        layers.append(lw)
+        n1, n2 = spec.norms(l)
+        norms.append((torch.from_numpy(n1).to(device), torch.from_numpy(n2).to(device)))
+        if l % 16 == 15:
+            log(f"  layers 0..{l} resident ({time.time() - t0:.0f} s)")
+    hb = sdgen.pinned_quantized_normal(spec.head_q, spec.weight_key(0, "head"), spec.vocab, spec.hidden)
+    head = repack_matrix(spec.head_q, hb, spec.vocab, spec.hidden, device=device)
+    fn = torch.from_numpy(spec.final_norm()).to(device)
+    timings["build_s"] = time.time() - t0
+    return VerifyStack(layers, norms, fn, head, spec.hidden, spec.ffn, spec.vocab, M, wq=spec.wq,
+                       head_q=spec.head_q, device=device)
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "speculative_decoding_verify_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(d, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic():
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, if it was taken
+    on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "qmm_q4_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    kv = {}
+    for line in open(p):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    try:
+        return float(kv["dram_bytes_per_full_launch"])
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# per-kernel durations of one eagerly launched pass (CUDA events on the stream)
+# ---------------------------------------------------------------------------
+def profile_pass(stack):
+    import torch
+
+    from speculative_decoding_verify_gb300 import (EPI_NONE, EPI_REQUANT, EPI_SILU_MUL_REQUANT, accept_greedy,
+                                                   head_logits, qmatmul_multipos, rmsnorm_quant_acts)
+    s = torch.cuda.current_stream()
+    ev = []
+
+    def mark(kind, nbytes):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(s)
+        ev.append((kind, nbytes, e))
+
+    H, F, V, wq = stack.H, stack.F, stack.V, stack.wq
+    bb = 18
+    first = torch.cuda.Event(enable_timing=True)
+    first.record(s)
+    for l in range(len(stack.layers)):
+        w = stack.layers[l]
+        n1, n2 = stack.norms[l]
+        rmsnorm_quant_acts(stack.h, n1, stack.qa, stack.sa, stack.eps)
+        mark("rmsnorm_quant", 0)
+        qmatmul_multipos(wq, w["qkv"], 3 * H, H, stack.qa, stack.sa, stack.ws, epilogue=EPI_REQUANT,
+                         requant_col0=2 * H, q_next=stack.qv, scales_next=stack.sv)
+        mark("qmm_q4", 3 * H * H // 32 * bb)
+        qmatmul_multipos(wq, w["o"], H, H, stack.qv, stack.sv, stack.ws, y=stack.h, residual=stack.h)
+        mark("qmm_q4", H * H // 32 * bb)
+        rmsnorm_quant_acts(stack.h, n2, stack.qa, stack.sa, stack.eps)
+        mark("rmsnorm_quant", 0)
+        qmatmul_multipos(wq, w["gate_up"], 2 * F, H, stack.qa, stack.sa, stack.ws, epilogue=EPI_SILU_MUL_REQUANT,
+                         q_next=stack.qf, scales_next=stack.sf)
+        mark("qmm_q4", 2 * F * H // 32 * bb)
+        qmatmul_multipos(wq, w["down"], H, F, stack.qf, stack.sf, stack.ws, y=stack.h, residual=stack.h)
+        mark("qmm_q4", H * F // 32 * bb)
+    rmsnorm_quant_acts(stack.h, stack.final_norm, stack.qa, stack.sa, stack.eps)
+    mark("rmsnorm_quant", 0)
+    head_logits(stack.head_w, V, H, stack.qa, stack.sa, stack.ws, stack.logits, stack.argmax, stack.row_max,
+                stack.row_sumexp)
+    mark("head_q8", V * H // 32 * 34)
+    accept_greedy(stack.argmax, stack.tokens, stack.parent, stack.M, stack.out_tokens, stack.out_count)
+    mark("accept_greedy", 0)
+    torch.cuda.synchronize()
+    out = {}
+    prev = first
+    for kind, nb, e in ev:
+        ms = prev.elapsed_time(e)
+        d = out.setdefault(kind, {"launches": 0, "ms": 0.0, "bytes": 0})
+        d["launches"] += 1
+        d["ms"] += ms
+        d["bytes"] += nb
+        prev = e
+    return out
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle on a bounded sample of the same work
+# ---------------------------------------------------------------------------
+def oracle_sample(spec, M, budget_s=12.0, max_layers=2):
+    import numpy as np
+
+    import oracle
+    import sdgen
+
+    oracle.build()
+    h = spec.hidden_in(M)
+    nbytes = 0
+    t_total = 0.0
+    layers = 0
+    for l in range(max_layers):
+        wts = {name: spec.weights(l, name) for name, _, _ in spec.matrices()}
+        n1, n2 = spec.norms(l)
+        t0 = time.time()
+        h = oracle.stack_layer(h, wts, n1, n2, spec.hidden, spec.ffn, spec.wq)
+        t_total += time.time() - t0
+        nbytes += sum(w.nbytes for w in wts.values())
+        layers += 1
+        if t_total > budget_s:
+            break
+    return {"value": nbytes / t_total / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{layers} layer(s) of the 64-layer stack at M={M} (all four 4-bit matrices, "
+                      f"{nbytes / 1e6:.0f} MB of weights), {t_total:.1f} s"}
+
+
+def reference_arm(args, spec, M):
+    """The oracle timed as the reference implementation on the host cores."""
+    import numpy as np
+
+    import oracle
+    import sdgen
+
+    oracle.build()
+    # one step = the oracle's multi-position matmul over a 3584 x 5120 slice of layer 0's O projection
+    # (10.3 MB of 4-bit weights) -- a bounded sample of the pass's weight stream
+    n, k = 3584, spec.hidden
+    w = sdgen.quantized_normal(spec.wq, spec.weight_key(0, "o"), spec.hidden, k)[:n].copy()
+    q, s = oracle.rmsnorm_quant(spec.hidden_in(M), None)
+    for _ in range(args.warmup):
+        oracle.qmatmul(spec.wq, w, n, k, q, s)
+    t0 = time.time()
+    for _ in range(args.steps):
+        oracle.qmatmul(spec.wq, w, n, k, q, s)
+    dt = time.time() - t0
+    v = w.nbytes * args.steps / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+            "config": {"workload": "config-4 verify pass weight stream (27B-shaped 4-bit stack + Q8_0 head), "
+                                   "sampled: 3584x5120 slice of one 4-bit projection per step", "M": M},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": f"{args.steps} steps of a 3584x5120 4-bit projection at M={M}"},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layers", type=int, default=64)
+    ap.add_argument("--M", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-pdl", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    import sdgen
+    spec = sdgen.StackSpec(layers=args.layers)
+    M = args.M
+
+    if args.impl == "reference":
+        if rank == 0:
+            reference_arm(args, spec, M)
+        return
+
+    import numpy as np
+    import torch
+
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device(device))
+
+    from speculative_decoding_verify_gb300 import build as b
+    if rank == 0 or world == 1:
+        b.build()
+    if dist:
+        dist.barrier()
+    sdgen.build()
+    import speculative_decoding_verify_gb300 as sdv
+    sdv.lib()
+    if args.no_pdl:
+        sdv.set_pdl(False)
+
+    timings = {}
+    log(f"[rank {rank}] building the {spec.layers}-layer stack ({spec.weight_bytes() / 1e9:.2f} GB of weights)")
+    stack = build_stack(spec, M, device, timings)
+    h0 = torch.from_numpy(spec.hidden_in(M)).to(device)
+
+    # drafts: the target's argmax with probability 0.75 per position, else uniform (from an untimed pass)
+    stack.h.copy_(h0)
+    stack.run()
+    torch.cuda.synchronize()
+    am = stack.argmax.cpu().numpy()
+    drafts = sdgen.drafts_p(sdgen.key(4, 7), am[:M - 1], spec.vocab)
+    stack.tokens[:M - 1].copy_(torch.from_numpy(drafts))
+    if sdv.device_status() != 0:
+        raise RuntimeError("device status after the first pass")
+
+    # the timed step: copy the input rows into the residual stream, then the captured pass
+    h_dev = torch.empty_like(h0)
+    h_dev.copy_(h0)
+
+    def body():
+        stack.h.copy_(h_dev)
+        stack.run()
+
+    stack.run = stack.run  # keep the plain pass for profiling
+    g_stream = torch.cuda.Stream()
+    g_stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(g_stream):
+        body()
+    torch.cuda.current_stream().wait_stream(g_stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        body()
+    torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    # timed region
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    clk = clocks.stop()
+    kept = int(stack.out_count.cpu()[0])
+    if sdv.device_status() != 0:
+        raise RuntimeError("device status after the timed region")
+    if dist:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    wbytes = spec.weight_bytes()
+    gbs = wbytes / (ms * 1e-3) / 1e9 * world
+    pos_s = M / (ms * 1e-3) * world
+
+    # end to end through the ABI with host buffers: H2D of the input rows and drafts, the pass, D2H of the
+    # accepted tokens and their count, every step
+    h_host = torch.from_numpy(spec.hidden_in(M)).pin_memory()
+    d_host = torch.from_numpy(np.ascontiguousarray(drafts)).pin_memory()
+    out_host = torch.zeros(M, dtype=torch.int32).pin_memory()
+    cnt_host = torch.zeros(1, dtype=torch.int32).pin_memory()
+    e2e_steps = max(10, args.steps // 4)
+
+    def e2e_step():
+        h_dev.copy_(h_host, non_blocking=True)
+        stack.tokens[:M - 1].copy_(d_host, non_blocking=True)
+        graph.replay()
+        out_host.copy_(stack.out_tokens, non_blocking=True)
+        cnt_host.copy_(stack.out_count, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+        torch.cuda.current_stream().synchronize()
+    e2e_ms = (time.perf_counter() - t0) / e2e_steps * 1e3
+    if dist:
+        t = torch.tensor([e2e_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = h_host.numel() * 4 + d_host.numel() * 4
+    d2h = out_host.numel() * 4 + cnt_host.numel() * 4
+
+    # per-kernel durations (one eagerly launched pass, events between launches)
+    stack.h.copy_(h_dev)
+    prof = profile_pass(stack)
+    prof_total = sum(v["ms"] for v in prof.values())
+    q4 = prof["qmm_q4"]
+    peak, peak_kind = measured_peaks()
+    achieved = q4["bytes"] / (q4["ms"] * 1e-3) / 1e9
+    traffic = committed_traffic()
+    roof = {"bound": "hbm", "kernel": "qmm_kernel<Q4_32> (4-bit multi-position matmul)",
+            "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": q4["bytes"] / q4["launches"],
+            "avg_launch_ms": q4["ms"] / q4["launches"], "launches_per_pass": q4["launches"],
+            "share_of_eager_pass": q4["ms"] / prof_total,
+            "kernels": {k: {"launches": v["launches"], "ms": round(v["ms"], 4), "share": round(v["ms"] / prof_total, 4)}
+                        for k, v in prof.items()}}
+
+    line = {"metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int8", "data": "synthetic (seeded N(0,0.02) weights, N(0,1) hidden rows)",
+            "config": {"workload": "config-4 verify pass: 64-layer 27B-shaped 4-bit projection stack + 5120x151936 "
+                                   "Q8_0 head + greedy accept, K+1=5",
+                       "M": M, "layers": spec.layers, "hidden": spec.hidden, "ffn": spec.ffn, "vocab": spec.vocab,
+                       "weight_bytes_per_pass": wbytes, "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                       "l2": "inputs larger than L2: 14.2 GB of weights streamed per step vs 129 MB L2",
+                       "pdl": not args.no_pdl, "graph": "one CUDA graph per pass"},
+            "pos_per_s": pos_s, "hbm_frac_of_measured": gbs / world / peak,
+            "hbm_frac_of_nominal_8TBps": gbs / world / NOMINAL_HBM_GBS,
+            "accepted_tokens_last_pass": kept,
+            "roofline": roof, "clocks": clk,
+            "e2e": {"value": wbytes / (e2e_ms * 1e-3) / 1e9 * world, "unit": "GB/s", "ms_per_step": e2e_ms,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": stack.launches_per_pass() * args.steps,
+            "build_s": timings.get("build_s")}
+
+    del stack, graph
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_cpu_baseline:
+        try:
+            line["cpu_baseline"] = oracle_sample(spec, M)
+        except Exception as ex:  # the baseline is reported, never required
+            line["cpu_baseline"] = {"value": None, "error": str(ex)[:200]}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,226 @@
+/*
+ * sdverify.h - C ABI of the GB300 (sm_103a) speculative-decoding verify pass.
+ *
+ * One verify pass reads block-quantised weights once and serves the current
+ * token plus K drafts (M = K+1 positions) with that single read; the full-
+ * vocabulary head follows, then greedy or rejection-sampling acceptance.
+ *
+ * General rules for every call below.
+ *  - Pointers are DEVICE pointers unless a parameter says otherwise, owned by
+ *    the caller, and must stay valid until the stream has passed the call.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream).  The return value covers argument validation
+ *    (SD_EINVAL / SD_EUNSUPPORTED) and launch errors (SD_ECUDA) only.  Device-
+ *    side conditions (a bounded wait that ran out, a bounds check) are recorded
+ *    in a per-device status word read by sd_device_status().
+ *  - Kernels are launched with programmatic dependent launch: each one may
+ *    start streaming its weights while the previous kernel on the stream is
+ *    still running, and waits for it before touching any dependent data.
+ *  - The library allocates nothing except one status word per device, created
+ *    on first use.  Scratch space is passed in as a caller-owned workspace.
+ *  - Dimensions: k_in % 32 == 0 (blocks of 32 run along the reduction
+ *    dimension), 1 <= M <= 16, n_out >= 1.  Weight, activation and logits
+ *    pointers must be 16-byte aligned; workspaces 256-byte aligned.
+ *
+ * Quantised formats (GGUF order, as read from a model file):
+ *  - SD_Q8_0:  per 32 weights, fp16 scale d (little endian) then 32 int8 q;
+ *              value d*q; 34 bytes per block.
+ *  - SD_Q4_32: per 32 weights, fp16 scale d then 16 bytes; byte j holds
+ *              element j in its low nibble and element j+16 in its high
+ *              nibble; value d*(code-8); 18 bytes per block.
+ * A weight matrix is [n_out rows][k_in/32 blocks] of such blocks.
+ */
+#ifndef SDVERIFY_H
+#define SDVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *sd_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    SD_OK = 0,
+    SD_EINVAL = 1,        /* bad argument: null, misaligned, out-of-range size */
+    SD_EUNSUPPORTED = 2,  /* valid but not supported (format, M > 16) */
+    SD_ECUDA = 3,         /* a CUDA runtime call or launch failed */
+    SD_ETIMEOUT = 4,      /* a bounded device-side wait ran out (from sd_device_status) */
+    SD_EDEVICE = 5        /* a device-side check failed (from sd_device_status) */
+} sd_status;
+
+typedef enum { SD_Q8_0 = 0, SD_Q4_32 = 1 } sd_qtype;
+
+/* Repack flags */
+#define SD_REPACK_PAIR_GATE_UP 1u /* rows [0,F) are gate and [F,2F) are up; store them pairwise */
+
+/* Matmul epilogues */
+#define SD_EPI_NONE 0u              /* y = residual + W a */
+#define SD_EPI_REQUANT 1u           /* also requantise columns [requant_col0, n_out) into q_next/scales_next */
+#define SD_EPI_SILU_MUL_REQUANT 2u  /* gate|up pair: h = silu(g) * u, requantised into q_next/scales_next */
+
+const char *sd_status_string(sd_status s);
+int sd_abi_version(void); /* 1 */
+
+/*
+ * Load-time repack ("Inside OpenJet Engine", section "One GPU launch for a
+ * speculative cycle": Q8_0 weights are rearranged at load time for aligned
+ * access without changing their values).
+ *
+ * src: GGUF-order blocks [n_out][k_in/32] (device).  dst: dst_bytes >=
+ * sd_repacked_bytes(...).  Layout of dst: tiles of 32 rows (the last tile
+ * zero-padded); per (tile t, block b) one 16-byte-aligned record holding the
+ * 32 rows' codes followed by their 32 fp16 scales:
+ *   SD_Q4_32: 576 B = 32 x 16 code bytes (byte order of the block kept) + 64 B scales
+ *   SD_Q8_0: 1088 B = 32 x 16 B (elements 0..15) + 32 x 16 B (elements 16..31) + 64 B scales
+ * records ordered (t, b).  With SD_REPACK_PAIR_GATE_UP (n_out = 2F) the
+ * record of gate tile j is followed by the record of up tile j, pairs ordered
+ * (j, b).  Values and bytes are unchanged; only their places move.
+ * Errors: SD_EINVAL on null/misaligned pointers, k_in % 32 != 0, odd n_out
+ * with the pair flag, or dst_bytes too small.
+ */
+size_t sd_repacked_bytes(int qtype, int64_t n_out, int64_t k_in, uint32_t flags);
+sd_status sd_repack_weights(int qtype, const void *src_blocks, int64_t n_out, int64_t k_in, uint32_t flags,
+                            void *dst, size_t dst_bytes, sd_stream_t stream);
+
+/*
+ * RMSNorm fused with per-32-block int8 requantisation of M activation rows
+ * ("Inside OpenJet Engine", section "One GPU launch for a speculative cycle":
+ * the producing phase requantises activations for the next consumer,
+ * including the next RMS normalisation's weight).
+ *
+ * x: fp32 [M][ldx] (row stride ldx >= K elements).  norm_w: fp32 [K], or NULL
+ * for requantisation only.  Out: q int8 [M][K], scales fp32 [M][K/32].
+ * Arithmetic (bit-exact contract): s = sum x^2 as 256 strided partials
+ * (partial j over i = j mod 256, increasing i) folded by a pairwise tree at
+ * strides 128..1; inv = 1/sqrt(s/K + eps) correctly rounded; y = (x*inv)*w;
+ * per block d = amax/127, q = round-half-away(y/d) clamped to +-127 (0 if d=0).
+ */
+sd_status sd_rmsnorm_quant_acts(const float *x, int64_t ldx, const float *norm_w, float eps, int32_t M,
+                                int64_t K, int8_t *q, float *scales, sd_stream_t stream);
+
+/*
+ * Multi-position quantised matmul: one pass over the repacked weights serves
+ * all M positions ("Inside OpenJet Engine", section "One GPU launch for a
+ * speculative cycle": integer dot products with int8 activations, weight reads
+ * serving multiple verification positions).
+ *
+ *   y[m][n] = residual[m][n] + sum_b d_w[n,b] * d_a[m,b] * dot_b(n, m)
+ *
+ * dot_b is the exact int32 dot of one 32-block (4-bit: sum (code-8) a).
+ * w: repacked by sd_repack_weights with the same qtype/n_out/k_in (and the
+ * pair flag iff epilogue == SD_EPI_SILU_MUL_REQUANT).  q int8 [M][k_in],
+ * scales fp32 [M][k_in/32].  y fp32 [M][n_out] (may be NULL for the two
+ * requantising epilogues); residual fp32 [M][n_out] or NULL (may alias y).
+ * SD_EPI_REQUANT: requant_col0 % 32 == 0; q_next int8 [M][n_out-col0],
+ * scales_next fp32 [M][(n_out-col0)/32] receive the per-32 requantisation of
+ * y's columns [col0, n_out).  SD_EPI_SILU_MUL_REQUANT: n_out = 2F, F % 32 ==
+ * 0; q_next [M][F], scales_next [M][F/32] receive requant(silu(g)*u) with g =
+ * columns [0,F), u = [F,2F) and silu(g) = g / (1 + exp(-g)); if y is given it
+ * receives g|u.  The reduction order of each output depends on (n_out, k_in,
+ * the device's SM count) only, never on M, so a row computed among M
+ * positions equals the same row computed alone, bit for bit.
+ * workspace: ws_bytes >= sd_qmatmul_workspace_bytes(...), zero-filled by the
+ * caller once; every call leaves it zero-filled again.  Calls sharing one
+ * workspace must be ordered on one stream.
+ */
+size_t sd_qmatmul_workspace_bytes(int qtype, int64_t n_out, int64_t k_in, uint32_t epilogue);
+sd_status sd_qmatmul_multipos(int qtype, const void *w, int64_t n_out, int64_t k_in, const int8_t *q,
+                              const float *scales, int32_t M, float *y, const float *residual, uint32_t epilogue,
+                              int64_t requant_col0, int8_t *q_next, float *scales_next, void *workspace,
+                              size_t ws_bytes, sd_stream_t stream);
+
+/*
+ * Full-vocabulary output head with fused per-row argmax and softmax
+ * statistics ("Inside OpenJet Engine", section "One GPU launch for a
+ * speculative cycle": full-vocabulary output head + verification inside the
+ * cycle; "How Kinetic is fast", section "Why the output does not change").
+ *
+ * w: Q8_0 head repacked (vocab rows, hidden = k_in).  Out: logits fp32
+ * [M][vocab]; argmax int32 [M] over the raw logits (lowest index on ties);
+ * row_max, row_sumexp fp32 [M] of z = logits / temperature: tiles of 1024
+ * tokens, per tile m_t = max z and s_t = pairwise tree (strides 512..1, zero
+ * padded) of exp(z - m_t); m = max m_t, Z = sequential fold of s_t *
+ * exp(m_t - m).  exp is the canonical Cody-Waite/Taylor exponential shared
+ * by the acceptance kernel, so these statistics equal what sd_accept_sample
+ * recomputes.  Workspace as for the matmul (sd_head_workspace_bytes).
+ */
+size_t sd_head_workspace_bytes(int64_t vocab, int64_t hidden);
+sd_status sd_head_logits(const void *w, int64_t vocab, int64_t hidden, const int8_t *q, const float *scales,
+                         int32_t M, float temperature, float *logits, int32_t *argmax, float *row_max,
+                         float *row_sumexp, void *workspace, size_t ws_bytes, sd_stream_t stream);
+
+/*
+ * Greedy acceptance ("How Kinetic is fast", section "Why the output does not
+ * change": keep a guess only when it is the model's top token; section
+ * "RAD-1": tree drafts, each row seeing only its own path).
+ *
+ * parent == NULL (chain): tokens = drafts [M-1]; row i predicts the token
+ * after position i.  n = largest j with tokens[i-1] == argmax[i-1] for all
+ * i <= j; out_tokens[0..n] = tokens[0..n-1], argmax[n]; *out_count = n+1.
+ * parent != NULL (tree, nodes in BFS order, parent[0] = -1, parent[i] < i):
+ * tokens [M] (tokens[0] unused).  Node i is accepted when its parent is and
+ * tokens[i] == argmax[parent[i]]; the deepest accepted node (lowest index
+ * among equals) ends the path; out = the path's tokens, then its argmax.
+ * out_tokens: int32 [M]; out_count: int32 [1].
+ */
+sd_status sd_accept_greedy(const int32_t *argmax, const int32_t *tokens, const int32_t *parent, int32_t M,
+                           int32_t *out_tokens, int32_t *out_count, sd_stream_t stream);
+
+/*
+ * Rejection-sampling acceptance ("Speculative Decoding with Open-Weights
+ * Models", section "Mathematical Integrity: Rejection Sampling for LLMs":
+ * accept x with min(1, p(x)/q(x)), on rejection draw from max(0, p-q)
+ * renormalised; its walkthrough draws a bonus token from the last row when
+ * every draft is kept.  "How Kinetic is fast", section "Why the output does
+ * not change": a certainty drafter keeps x with probability p(x) and otherwise
+ * draws from p without x).
+ *
+ * logits fp32 [K+1][vocab]; row_max / row_sumexp from sd_head_logits at the
+ * same temperature, or NULL to recompute them identically; q_probs fp32
+ * [K][vocab], or NULL for a certainty drafter (q one-hot at the draft);
+ * drafts int32 [K].  Uniforms: Philox4x32-10 keyed by seed with counter
+ * (position lo, position hi, 0, 0), position = base_pos + row; word 0 ->
+ * accept uniform, word 1 -> residual or bonus uniform, u = (w >> 8) * 2^-24.
+ * Draft i is kept iff u * q_i(x) < p_i(x).  The residual draw is an inverse
+ * CDF over 1024-token tiles, 32-token chunks and single tokens with sequential
+ * folds.  K <= 15.  out_tokens int32 [K+1]; *out_count = kept + 1.
+ */
+sd_status sd_accept_sample(const float *logits, int64_t vocab, int32_t K, const float *row_max,
+                           const float *row_sumexp, const float *q_probs, const int32_t *drafts, float temperature,
+                           uint64_t seed, int64_t base_pos, int32_t *out_tokens, int32_t *out_count,
+                           sd_stream_t stream);
+
+/* Synchronises `stream`, returns and clears the current device's status word
+ * (SD_OK, SD_ETIMEOUT or SD_EDEVICE); SD_ECUDA if synchronising failed. */
+sd_status sd_device_status(sd_stream_t stream);
+
+/* Programmatic dependent launch on (1, default) or off (0) for later launches. */
+void sd_set_pdl(int enable);
+
+/* ---- test hooks (not part of the verify pass) ---- */
+
+/* Per-block int32 dots [M][n_out][k_in/32] from repacked weights, with the
+ * same device routine the matmul uses. */
+sd_status sd_debug_block_dots(int qtype, const void *w, int64_t n_out, int64_t k_in, const int8_t *q, int32_t M,
+                              int32_t *dots, sd_stream_t stream);
+/* The matmul's SiLU*mul requantisation applied to given g, u fp32 [M][F]. */
+sd_status sd_debug_silu_mul_requant(const float *g, const float *u, int32_t M, int64_t F, int8_t *q, float *scales,
+                                    sd_stream_t stream);
+/* The canonical exponential on n values. */
+sd_status sd_debug_cexp(const float *x, int64_t n, float *y, sd_stream_t stream);
+/* Philox4x32-10 words for counters (pos, 0, 0) .. (pos+n-1): out uint32 [n][4]. */
+sd_status sd_debug_philox(uint64_t seed, int64_t pos, int64_t n, uint32_t *out, sd_stream_t stream);
+/* One CTA waits on an mbarrier that nothing completes, bounded by `limit_ns`
+ * nanoseconds of polling (1 .. 10^10); on expiry it records SD_ETIMEOUT in the
+ * status word and returns.  Exercises the timeout path without hanging the
+ * device: every wait inside the verify kernels is bounded the same way (2 s). */
+sd_status sd_debug_wait_timeout(int64_t limit_ns, sd_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SDVERIFY_H */

@@ -1,0 +1,213 @@
+"""GB300 (sm_103a) speculative-decoding verify pass: thin Python binding.
+
+Every function marshals torch tensors (device memory owned by the caller) into
+the C ABI of ``libsdverify.so`` (declared in ``include/sdverify.h``) and calls
+it on the current CUDA stream.  All arithmetic runs in the library's kernels;
+there is no CPU or PyTorch fallback: if the library is missing, ``lib()``
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libsdverify.so")
+
+Q8_0 = 0
+Q4_32 = 1
+BLOCK_BYTES = {Q8_0: 34, Q4_32: 18}
+REPACK_PAIR_GATE_UP = 1
+EPI_NONE = 0
+EPI_REQUANT = 1
+EPI_SILU_MUL_REQUANT = 2
+
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: "device wait timed out",
+          5: "device-side check failed"}
+
+_lib = None
+
+
+class SdError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(code, code)} ({code})")
+        self.code = code
+
+
+def lib():
+    """Load libsdverify.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with speculative_decoding_verify_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, I32, I64, U32, U64, F, SZ = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int32, ctypes.c_int64,
+                                           ctypes.c_uint32, ctypes.c_uint64, ctypes.c_float, ctypes.c_size_t)
+        sig = {
+            "sd_status_string": ([I], ctypes.c_char_p),
+            "sd_abi_version": ([], I),
+            "sd_repacked_bytes": ([I, I64, I64, U32], SZ),
+            "sd_repack_weights": ([I, P, I64, I64, U32, P, SZ, P], I),
+            "sd_rmsnorm_quant_acts": ([P, I64, P, F, I32, I64, P, P, P], I),
+            "sd_qmatmul_workspace_bytes": ([I, I64, I64, U32], SZ),
+            "sd_qmatmul_multipos": ([I, P, I64, I64, P, P, I32, P, P, U32, I64, P, P, P, SZ, P], I),
+            "sd_head_workspace_bytes": ([I64, I64], SZ),
+            "sd_head_logits": ([P, I64, I64, P, P, I32, F, P, P, P, P, P, SZ, P], I),
+            "sd_accept_greedy": ([P, P, P, I32, P, P, P], I),
+            "sd_accept_sample": ([P, I64, I32, P, P, P, P, F, U64, I64, P, P, P], I),
+            "sd_device_status": ([P], I),
+            "sd_set_pdl": ([I], None),
+            "sd_debug_block_dots": ([I, P, I64, I64, P, I32, P, P], I),
+            "sd_debug_silu_mul_requant": ([P, P, I32, I64, P, P, P], I),
+            "sd_debug_cexp": ([P, I64, P, P], I),
+            "sd_debug_philox": ([U64, I64, I64, P, P], I),
+            "sd_debug_wait_timeout": ([I64, P], I),
+        }
+        for name, (args, res) in sig.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = L
+    return _lib
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        raise SdError(code, what)
+
+
+def _dev(t, dtype, name):
+    if t is None:
+        return
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous CUDA {dtype} tensor")
+
+
+# ---------------------------------------------------------------------------
+# verify-pass calls
+# ---------------------------------------------------------------------------
+
+def repacked_bytes(qtype: int, n_out: int, k_in: int, pair: bool = False) -> int:
+    return int(lib().sd_repacked_bytes(qtype, n_out, k_in, REPACK_PAIR_GATE_UP if pair else 0))
+
+
+def repack_weights(qtype: int, src: torch.Tensor, n_out: int, k_in: int, pair: bool = False,
+                   out: torch.Tensor | None = None) -> torch.Tensor:
+    """GGUF-order blocks (uint8 CUDA tensor) -> repacked records (uint8 CUDA tensor)."""
+    _dev(src, torch.uint8, "src")
+    nb = repacked_bytes(qtype, n_out, k_in, pair)
+    if nb == 0:
+        raise ValueError("bad repack shape")
+    if out is None:
+        out = torch.empty(nb, dtype=torch.uint8, device=src.device)
+    _check(lib().sd_repack_weights(qtype, _p(src), n_out, k_in, REPACK_PAIR_GATE_UP if pair else 0, _p(out),
+                                   out.numel(), _stream()), "sd_repack_weights")
+    return out
+
+
+def rmsnorm_quant_acts(x: torch.Tensor, norm_w: torch.Tensor | None, q: torch.Tensor, scales: torch.Tensor,
+                       eps: float = 1e-6, K: int | None = None, ldx: int | None = None):
+    M = x.shape[0]
+    K = K if K is not None else x.shape[1]
+    ldx = ldx if ldx is not None else x.stride(0)
+    _check(lib().sd_rmsnorm_quant_acts(_p(x), ldx, _p(norm_w), eps, M, K, _p(q), _p(scales), _stream()),
+           "sd_rmsnorm_quant_acts")
+
+
+def qmatmul_workspace_bytes(qtype: int, n_out: int, k_in: int, epilogue: int = EPI_NONE) -> int:
+    return int(lib().sd_qmatmul_workspace_bytes(qtype, n_out, k_in, epilogue))
+
+
+def head_workspace_bytes(vocab: int, hidden: int) -> int:
+    return int(lib().sd_head_workspace_bytes(vocab, hidden))
+
+
+def workspace(nbytes: int, device=None) -> torch.Tensor:
+    """Zero-filled workspace (the calls leave its counters at zero again)."""
+    return torch.zeros(max(256, (nbytes + 255) // 256 * 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def qmatmul_multipos(qtype: int, w: torch.Tensor, n_out: int, k_in: int, q: torch.Tensor, scales: torch.Tensor,
+                     ws: torch.Tensor, y: torch.Tensor | None = None, residual: torch.Tensor | None = None,
+                     epilogue: int = EPI_NONE, requant_col0: int = 0, q_next: torch.Tensor | None = None,
+                     scales_next: torch.Tensor | None = None):
+    M = q.shape[0]
+    _check(lib().sd_qmatmul_multipos(qtype, _p(w), n_out, k_in, _p(q), _p(scales), M, _p(y), _p(residual), epilogue,
+                                     requant_col0, _p(q_next), _p(scales_next), _p(ws), ws.numel(), _stream()),
+           "sd_qmatmul_multipos")
+
+
+def head_logits(w: torch.Tensor, vocab: int, hidden: int, q: torch.Tensor, scales: torch.Tensor, ws: torch.Tensor,
+                logits: torch.Tensor, argmax: torch.Tensor, row_max: torch.Tensor, row_sumexp: torch.Tensor,
+                temperature: float = 1.0):
+    M = q.shape[0]
+    _check(lib().sd_head_logits(_p(w), vocab, hidden, _p(q), _p(scales), M, temperature, _p(logits), _p(argmax),
+                                _p(row_max), _p(row_sumexp), _p(ws), ws.numel(), _stream()), "sd_head_logits")
+
+
+def accept_greedy(argmax: torch.Tensor, tokens: torch.Tensor | None, parent: torch.Tensor | None, M: int,
+                  out_tokens: torch.Tensor, out_count: torch.Tensor):
+    _check(lib().sd_accept_greedy(_p(argmax), _p(tokens), _p(parent), M, _p(out_tokens), _p(out_count), _stream()),
+           "sd_accept_greedy")
+
+
+def accept_sample(logits: torch.Tensor, K: int, drafts: torch.Tensor | None, out_tokens: torch.Tensor,
+                  out_count: torch.Tensor, q_probs: torch.Tensor | None = None, row_max: torch.Tensor | None = None,
+                  row_sumexp: torch.Tensor | None = None, temperature: float = 1.0, seed: int = 0, base_pos: int = 0):
+    V = logits.shape[1]
+    _check(lib().sd_accept_sample(_p(logits), V, K, _p(row_max), _p(row_sumexp), _p(q_probs), _p(drafts),
+                                  temperature, seed, base_pos, _p(out_tokens), _p(out_count), _stream()),
+           "sd_accept_sample")
+
+
+def device_status() -> int:
+    return int(lib().sd_device_status(_stream()))
+
+
+def set_pdl(enable: bool):
+    lib().sd_set_pdl(1 if enable else 0)
+
+
+# ---------------------------------------------------------------------------
+# test hooks
+# ---------------------------------------------------------------------------
+
+def debug_block_dots(qtype: int, w: torch.Tensor, n_out: int, k_in: int, q: torch.Tensor) -> torch.Tensor:
+    M = q.shape[0]
+    dots = torch.empty((M, n_out, k_in // 32), dtype=torch.int32, device=q.device)
+    _check(lib().sd_debug_block_dots(qtype, _p(w), n_out, k_in, _p(q), M, _p(dots), _stream()), "sd_debug_block_dots")
+    return dots
+
+
+def debug_silu_mul_requant(g: torch.Tensor, u: torch.Tensor):
+    M, F = g.shape
+    q = torch.empty((M, F), dtype=torch.int8, device=g.device)
+    s = torch.empty((M, F // 32), dtype=torch.float32, device=g.device)
+    _check(lib().sd_debug_silu_mul_requant(_p(g), _p(u), M, F, _p(q), _p(s), _stream()), "sd_debug_silu_mul_requant")
+    return q, s
+
+
+def debug_cexp(x: torch.Tensor) -> torch.Tensor:
+    y = torch.empty_like(x)
+    _check(lib().sd_debug_cexp(_p(x), x.numel(), _p(y), _stream()), "sd_debug_cexp")
+    return y
+
+
+def debug_philox(seed: int, pos: int, n: int, device="cuda") -> torch.Tensor:
+    out = torch.empty((n, 4), dtype=torch.int32, device=device)
+    _check(lib().sd_debug_philox(seed, pos, n, _p(out), _stream()), "sd_debug_philox")
+    return out
+
+
+def debug_wait_timeout(limit_ns: int):
+    _check(lib().sd_debug_wait_timeout(limit_ns, _stream()), "sd_debug_wait_timeout")

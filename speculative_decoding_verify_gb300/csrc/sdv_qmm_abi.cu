@@ -1,0 +1,187 @@
+// sdv_qmm_abi.cu - C entry points of the multi-position matmul and the head,
+// and the block-dot test hook.
+#include "sdv_qmatmul.cuh"
+
+namespace sdv {
+
+// one thread per (m, n, b): the same block-dot routines as the matmul, on the
+// repacked records (row r of tile t at record (t, b))
+__global__ void block_dots_kernel(int qtype, const uint8_t *__restrict__ w, int64_t n_out, int32_t KB,
+                                  const int8_t *__restrict__ q, int32_t M, int32_t *__restrict__ dots) {
+    const int64_t total = static_cast<int64_t>(M) * n_out * KB;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t b = i % KB;
+        const int64_t n = (i / KB) % n_out;
+        const int m = static_cast<int>(i / (KB * n_out));
+        const int64_t t = n / 32;
+        const int r = static_cast<int>(n % 32);
+        const uint4 *ap = reinterpret_cast<const uint4 *>(q + static_cast<int64_t>(m) * KB * 32 + b * 32);
+        const uint4 a0 = ap[0], a1 = ap[1];
+        int d;
+        if (qtype == SD_Q4_32) {
+            const uint8_t *rec = w + (t * KB + b) * 576;
+            uint32_t lo[4], hi[4];
+            unpack_q4(*reinterpret_cast<const uint4 *>(rec + r * 16), lo, hi);
+            int sum = 0;
+            sum = dp4a(0x01010101, static_cast<int>(a0.x), sum);
+            sum = dp4a(0x01010101, static_cast<int>(a0.y), sum);
+            sum = dp4a(0x01010101, static_cast<int>(a0.z), sum);
+            sum = dp4a(0x01010101, static_cast<int>(a0.w), sum);
+            sum = dp4a(0x01010101, static_cast<int>(a1.x), sum);
+            sum = dp4a(0x01010101, static_cast<int>(a1.y), sum);
+            sum = dp4a(0x01010101, static_cast<int>(a1.z), sum);
+            sum = dp4a(0x01010101, static_cast<int>(a1.w), sum);
+            d = dot_q4(lo, hi, a0, a1, FP_BIAS_BITS - 8 * sum);
+        } else {
+            const uint8_t *rec = w + (t * KB + b) * 1088;
+            d = dot_q8(*reinterpret_cast<const uint4 *>(rec + r * 16), *reinterpret_cast<const uint4 *>(rec + 512 + r * 16),
+                       a0, a1, FP_BIAS_BITS);
+        }
+        dots[i] = static_cast<int32_t>(biased_to_float(d));
+    }
+}
+
+static inline cudaStream_t cs(sd_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+static cudaError_t dispatch(int qtype, bool pair, QmmArgs &a, QmmPlan &p, cudaStream_t s) {
+    if (qtype == SD_Q4_32) return pair ? qmm_dispatch<SD_Q4_32, 1>(a, p, s) : qmm_dispatch<SD_Q4_32, 0>(a, p, s);
+    return qmm_dispatch<SD_Q8_0, 0>(a, p, s);
+}
+
+static void fill_plan(QmmArgs &a, const QmmPlan &p) {
+    a.KB = p.KB;
+    a.NU = p.NU;
+    a.KS = p.KS;
+    a.KBs = p.KBs;
+    a.KBlast = p.KBlast;
+    a.W = p.W;
+    a.G = p.G;
+    a.P = p.P;
+    a.step_bytes = p.step_bytes;
+}
+
+}  // namespace sdv
+
+using namespace sdv;
+
+extern "C" {
+
+size_t sd_qmatmul_workspace_bytes(int qtype, int64_t n_out, int64_t k_in, uint32_t epilogue) {
+    if (qtype != SD_Q8_0 && qtype != SD_Q4_32) return 0;
+    QmmPlan p;
+    if (!make_plan(qtype, n_out, k_in, epilogue == SD_EPI_SILU_MUL_REQUANT, false, num_sms(), p)) return 0;
+    return p.ws_total;
+}
+
+size_t sd_head_workspace_bytes(int64_t vocab, int64_t hidden) {
+    QmmPlan p;
+    if (!make_plan(SD_Q8_0, vocab, hidden, false, true, num_sms(), p)) return 0;
+    return p.ws_total;
+}
+
+sd_status sd_qmatmul_multipos(int qtype, const void *w, int64_t n_out, int64_t k_in, const int8_t *q,
+                              const float *scales, int32_t M, float *y, const float *residual, uint32_t epilogue,
+                              int64_t requant_col0, int8_t *q_next, float *scales_next, void *workspace,
+                              size_t ws_bytes, sd_stream_t stream) {
+    if (qtype != SD_Q8_0 && qtype != SD_Q4_32) return SD_EINVAL;
+    if (M < 1) return SD_EINVAL;
+    if (M > 16) return SD_EUNSUPPORTED;
+    if (!w || !q || !scales || !workspace) return SD_EINVAL;
+    if (!aligned(w, 16) || !aligned(q, 16) || !aligned(scales, 4) || !aligned(workspace, 256)) return SD_EINVAL;
+    if (k_in <= 0 || k_in % 32 || n_out <= 0) return SD_EINVAL;
+    const bool pair = epilogue == SD_EPI_SILU_MUL_REQUANT;
+    int64_t nq = 0;
+    if (epilogue == SD_EPI_NONE) {
+        if (!y) return SD_EINVAL;
+    } else if (epilogue == SD_EPI_REQUANT) {
+        if (!q_next || !scales_next || n_out % 32 || requant_col0 < 0 || requant_col0 >= n_out ||
+            requant_col0 % 32)
+            return SD_EINVAL;
+        nq = n_out - requant_col0;
+    } else if (pair) {
+        if (qtype != SD_Q4_32) return SD_EUNSUPPORTED;
+        if (!q_next || !scales_next || residual || n_out % 64) return SD_EINVAL;
+        nq = n_out / 2;
+    } else {
+        return SD_EINVAL;
+    }
+    if (y && !aligned(y, 4)) return SD_EINVAL;
+    QmmPlan p;
+    if (!make_plan(qtype, n_out, k_in, pair, false, num_sms(), p)) return SD_EINVAL;
+    if (ws_bytes < p.ws_total) return SD_EINVAL;
+    int *st = status_ptr();
+    if (!st) return SD_ECUDA;
+    QmmArgs a = {};
+    fill_plan(a, p);
+    a.w = static_cast<const uint8_t *>(w);
+    a.n_out = n_out;
+    a.q = q;
+    a.sc = scales;
+    a.M = M;
+    a.y = y;
+    a.residual = residual;
+    a.epi = epilogue;
+    a.col0 = requant_col0;
+    a.q_next = q_next;
+    a.s_next = scales_next;
+    a.nq = nq;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    a.part = reinterpret_cast<float *>(ws);
+    a.cnt = reinterpret_cast<uint32_t *>(ws + p.ws_part);
+    a.status = st;
+    return dispatch(qtype, pair, a, p, cs(stream)) == cudaSuccess ? SD_OK : SD_ECUDA;
+}
+
+sd_status sd_head_logits(const void *w, int64_t vocab, int64_t hidden, const int8_t *q, const float *scales, int32_t M,
+                         float temperature, float *logits, int32_t *argmax, float *row_max, float *row_sumexp,
+                         void *workspace, size_t ws_bytes, sd_stream_t stream) {
+    if (M < 1) return SD_EINVAL;
+    if (M > 16) return SD_EUNSUPPORTED;
+    if (!w || !q || !scales || !logits || !argmax || !row_max || !row_sumexp || !workspace) return SD_EINVAL;
+    if (!aligned(w, 16) || !aligned(q, 16) || !aligned(logits, 16) || !aligned(workspace, 256)) return SD_EINVAL;
+    if (!(temperature > 0.0f) || temperature > 3.0e38f) return SD_EINVAL;
+    if (hidden <= 0 || hidden % 32 || vocab <= 0) return SD_EINVAL;
+    QmmPlan p;
+    if (!make_plan(SD_Q8_0, vocab, hidden, false, true, num_sms(), p)) return SD_EINVAL;
+    if (ws_bytes < p.ws_total) return SD_EINVAL;
+    int *st = status_ptr();
+    if (!st) return SD_ECUDA;
+    QmmArgs a = {};
+    fill_plan(a, p);
+    a.w = static_cast<const uint8_t *>(w);
+    a.n_out = vocab;
+    a.q = q;
+    a.sc = scales;
+    a.M = M;
+    a.y = logits;
+    a.epi = SD_EPI_NONE;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    a.part = reinterpret_cast<float *>(ws);
+    a.cnt = reinterpret_cast<uint32_t *>(ws + p.ws_part);
+    const int64_t nst = (vocab + STAT_TILE - 1) / STAT_TILE;
+    uint8_t *stb = ws + p.ws_part + p.ws_cnt;
+    a.st_part = reinterpret_cast<float4 *>(stb);
+    a.st_cnt = reinterpret_cast<uint32_t *>(stb + align_up(static_cast<size_t>(nst) * MPAD * sizeof(float4), 256));
+    a.st_done = a.st_cnt + nst;
+    a.n_stiles = static_cast<int32_t>(nst);
+    a.head = 1;
+    a.T = temperature;
+    a.argmax = argmax;
+    a.row_max = row_max;
+    a.row_sumexp = row_sumexp;
+    a.status = st;
+    return dispatch(SD_Q8_0, false, a, p, cs(stream)) == cudaSuccess ? SD_OK : SD_ECUDA;
+}
+
+sd_status sd_debug_block_dots(int qtype, const void *w, int64_t n_out, int64_t k_in, const int8_t *q, int32_t M,
+                              int32_t *dots, sd_stream_t stream) {
+    if ((qtype != SD_Q8_0 && qtype != SD_Q4_32) || !w || !q || !dots || M < 1 || M > 16) return SD_EINVAL;
+    if (k_in <= 0 || k_in % 32 || n_out <= 0 || !aligned(w, 16) || !aligned(q, 16)) return SD_EINVAL;
+    const int64_t total = static_cast<int64_t>(M) * n_out * (k_in / 32);
+    const int grid = static_cast<int>(total / 256 + 1 < 8192 ? total / 256 + 1 : 8192);
+    block_dots_kernel<<<grid, 256, 0, cs(stream)>>>(qtype, static_cast<const uint8_t *>(w), n_out,
+                                                    static_cast<int32_t>(k_in / 32), q, M, dots);
+    return cudaGetLastError() == cudaSuccess ? SD_OK : SD_ECUDA;
+}
+
+}  // extern "C"

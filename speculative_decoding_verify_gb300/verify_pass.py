@@ -1,0 +1,117 @@
+"""The verify pass of a dense quantised projection stack, driven through the C ABI.
+
+Per layer (attention and recurrent mixers omitted): RMSNorm + requant -> QKV
+(H -> 3H, the V columns requantised in the matmul epilogue) -> O (+ residual)
+-> RMSNorm + requant -> gate|up (H -> 2F, SiLU*mul + requant epilogue) -> down
+(+ residual); then a final RMSNorm, the vocabulary head with fused argmax and
+softmax statistics, and greedy (chain or tree) acceptance.  One weight read per
+matrix serves all M = K+1 positions.  ``capture()`` records the whole pass as
+one CUDA graph; launches inside it use programmatic dependent launch so each
+kernel streams its weights while the previous one finishes.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (EPI_NONE, EPI_REQUANT, EPI_SILU_MUL_REQUANT, Q4_32, Q8_0, accept_greedy, head_logits,
+               head_workspace_bytes, qmatmul_multipos, qmatmul_workspace_bytes, repack_weights, rmsnorm_quant_acts,
+               workspace)
+
+
+class VerifyStack:
+    """Device-resident weights + activation buffers for one M."""
+
+    def __init__(self, layers, norms, final_norm, head_w, hidden: int, ffn: int, vocab: int, M: int,
+                 wq: int = Q4_32, head_q: int = Q8_0, eps: float = 1e-6, tree_parent: torch.Tensor | None = None,
+                 device="cuda"):
+        """layers: list of dicts {qkv, o, gate_up, down} of REPACKED uint8 CUDA tensors (gate_up repacked with
+        the gate|up pairing).  norms: list of (norm1, norm2) fp32 CUDA tensors [hidden]."""
+        assert head_q == Q8_0
+        self.layers, self.norms, self.final_norm, self.head_w = layers, norms, final_norm, head_w
+        self.H, self.F, self.V, self.M, self.wq, self.eps = hidden, ffn, vocab, M, wq, eps
+        H, F, V = hidden, ffn, vocab
+        f32 = dict(dtype=torch.float32, device=device)
+        i8 = dict(dtype=torch.int8, device=device)
+        i32 = dict(dtype=torch.int32, device=device)
+        self.h = torch.zeros((M, H), **f32)
+        self.qa = torch.zeros((M, H), **i8)
+        self.sa = torch.zeros((M, H // 32), **f32)
+        self.qv = torch.zeros((M, H), **i8)
+        self.sv = torch.zeros((M, H // 32), **f32)
+        self.qf = torch.zeros((M, F), **i8)
+        self.sf = torch.zeros((M, F // 32), **f32)
+        self.logits = torch.zeros((M, V), **f32)
+        self.argmax = torch.zeros(M, **i32)
+        self.row_max = torch.zeros(M, **f32)
+        self.row_sumexp = torch.zeros(M, **f32)
+        self.tokens = torch.zeros(max(M, 1), **i32)   # drafts (chain) or node tokens (tree)
+        self.parent = tree_parent
+        self.out_tokens = torch.zeros(M, **i32)
+        self.out_count = torch.zeros(1, **i32)
+        ws = max(qmatmul_workspace_bytes(wq, 3 * H, H, EPI_REQUANT),
+                 qmatmul_workspace_bytes(wq, H, H, EPI_NONE),
+                 qmatmul_workspace_bytes(wq, 2 * F, H, EPI_SILU_MUL_REQUANT),
+                 qmatmul_workspace_bytes(wq, H, F, EPI_NONE),
+                 head_workspace_bytes(V, H))
+        self.ws = workspace(ws, device)
+        self.graph = None
+
+    # -- the pass -------------------------------------------------------------
+    def layer(self, l: int):
+        H, F, wq = self.H, self.F, self.wq
+        w = self.layers[l]
+        n1, n2 = self.norms[l]
+        rmsnorm_quant_acts(self.h, n1, self.qa, self.sa, self.eps)
+        qmatmul_multipos(wq, w["qkv"], 3 * H, H, self.qa, self.sa, self.ws, epilogue=EPI_REQUANT,
+                         requant_col0=2 * H, q_next=self.qv, scales_next=self.sv)
+        qmatmul_multipos(wq, w["o"], H, H, self.qv, self.sv, self.ws, y=self.h, residual=self.h)
+        rmsnorm_quant_acts(self.h, n2, self.qa, self.sa, self.eps)
+        qmatmul_multipos(wq, w["gate_up"], 2 * F, H, self.qa, self.sa, self.ws, epilogue=EPI_SILU_MUL_REQUANT,
+                         q_next=self.qf, scales_next=self.sf)
+        qmatmul_multipos(wq, w["down"], H, F, self.qf, self.sf, self.ws, y=self.h, residual=self.h)
+
+    def head(self, temperature: float = 1.0):
+        rmsnorm_quant_acts(self.h, self.final_norm, self.qa, self.sa, self.eps)
+        head_logits(self.head_w, self.V, self.H, self.qa, self.sa, self.ws, self.logits, self.argmax, self.row_max,
+                    self.row_sumexp, temperature)
+
+    def accept(self):
+        accept_greedy(self.argmax, self.tokens, self.parent, self.M, self.out_tokens, self.out_count)
+
+    def run(self):
+        """One verify pass over self.h (input hidden rows) and self.tokens (drafts)."""
+        for l in range(len(self.layers)):
+            self.layer(l)
+        self.head()
+        self.accept()
+
+    def capture(self):
+        """Record run() as one CUDA graph (replayed by replay())."""
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.run()  # warm-up outside capture: sets kernel attributes, loads modules
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.run()
+        self.graph = g
+        return g
+
+    def replay(self):
+        self.graph.replay()
+
+    def launches_per_pass(self) -> int:
+        return 6 * len(self.layers) + 3
+
+
+def repack_matrix(qtype: int, blocks_host, n_out: int, k_in: int, pair: bool = False, device="cuda"):
+    """Upload GGUF-order blocks (numpy uint8 or pinned torch tensor) and repack them on the device."""
+    if not isinstance(blocks_host, torch.Tensor):
+        blocks_host = torch.from_numpy(blocks_host)
+    src = blocks_host.to(device, non_blocking=True).reshape(-1)
+    out = repack_weights(qtype, src, n_out, k_in, pair)
+    torch.cuda.current_stream().synchronize()  # weights must be resident before any pass reads them
+    del src
+    return out
