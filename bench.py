@@ -217,7 +217,7 @@ def profile_pass(stack):
 # ---------------------------------------------------------------------------
 # CPU baseline: the oracle on a bounded sample of the same work
 # ---------------------------------------------------------------------------
-def oracle_sample(spec, M, budget_s=12.0, max_layers=2):
+def oracle_sample(spec, M, budget_s=12.0, max_layers=64):
     import numpy as np
 
     import oracle

@@ -72,13 +72,20 @@ int sd_abi_version(void); /* 1 */
  *
  * src: GGUF-order blocks [n_out][k_in/32] (device).  dst: dst_bytes >=
  * sd_repacked_bytes(...).  Layout of dst: tiles of 32 rows (the last tile
- * zero-padded); per (tile t, block b) one 16-byte-aligned record holding the
- * 32 rows' codes followed by their 32 fp16 scales:
- *   SD_Q4_32: 576 B = 32 x 16 code bytes (byte order of the block kept) + 64 B scales
- *   SD_Q8_0: 1088 B = 32 x 16 B (elements 0..15) + 32 x 16 B (elements 16..31) + 64 B scales
- * records ordered (t, b).  With SD_REPACK_PAIR_GATE_UP (n_out = 2F) the
- * record of gate tile j is followed by the record of up tile j, pairs ordered
- * (j, b).  Values and bytes are unchanged; only their places move.
+ * padded with zero scales); per (tile t, block b) one 16-byte-aligned record
+ * of the 32 rows' codes followed by their 32 fp16 scales, records ordered
+ * (t, b).  Inside a record the codes are placed where lane l = 4g + c of a
+ * warp finds its mma.sync m16n8k16 operand fragments (rows 16t'+g and
+ * 16t'+g+8, k = 16s+2c, +1, +8, +9 for row half t' and k step s):
+ *   SD_Q4_32 (576 B): 16 code bytes per lane; word 2t'+s, nibble i holds
+ *     (row 16t'+g + 8*[i&2], k 16s+2c + 8*[i&1] + (i>>2)); then 64 B scales.
+ *   SD_Q8_0 (1088 B): two 512-B planes (t' = 0, 1) of 16 bytes per lane; word
+ *     2s+h holds (row 16t'+g, k0), (row 16t'+g, k0+1), (row 16t'+g+8, k0),
+ *     (row 16t'+g+8, k0+1), k0 = 16s+2c+8h; then 64 B scales.
+ *   Scales: 8 groups of 4 fp16, group g = rows g, g+8, 16+g, 24+g.
+ * With SD_REPACK_PAIR_GATE_UP (n_out = 2F) the record of gate tile j is
+ * followed by the record of up tile j, pairs ordered (j, b).  Values are
+ * unchanged; only their places move.
  * Errors: SD_EINVAL on null/misaligned pointers, k_in % 32 != 0, odd n_out
  * with the pair flag, or dst_bytes too small.
  */
@@ -124,8 +131,8 @@ sd_status sd_rmsnorm_quant_acts(const float *x, int64_t ldx, const float *norm_w
  * the device's SM count) only, never on M, so a row computed among M
  * positions equals the same row computed alone, bit for bit.
  * workspace: ws_bytes >= sd_qmatmul_workspace_bytes(...), zero-filled by the
- * caller once; every call leaves it zero-filled again.  Calls sharing one
- * workspace must be ordered on one stream.
+ * caller once; every call returns its counters to zero (partial sums are
+ * scratch).  Calls sharing one workspace must be ordered on one stream.
  */
 size_t sd_qmatmul_workspace_bytes(int qtype, int64_t n_out, int64_t k_in, uint32_t epilogue);
 sd_status sd_qmatmul_multipos(int qtype, const void *w, int64_t n_out, int64_t k_in, const int8_t *q,

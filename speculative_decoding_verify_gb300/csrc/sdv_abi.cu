@@ -52,7 +52,13 @@ bool pdl_enabled() { return g_pdl != 0; }
 // load-time repack: GGUF blocks -> 32-row tile records (values unchanged)
 // ---------------------------------------------------------------------------
 
-// one thread per (record, row): copies the row's code bytes and fp16 scale
+// GGUF code byte / nibble of (row, k) of one block, k in 0..31
+__device__ __forceinline__ int q4_code(const uint8_t *blk, int k) {
+    return k < 16 ? (blk[2 + k] & 0x0F) : (blk[2 + k - 16] >> 4);
+}
+
+// One thread per (record, lane): writes the lane's code bytes in fragment order
+// (see sdv_qmatmul.cuh) and, for lanes with c == 0, the group's four scales.
 __global__ void repack_kernel(int qtype, const uint8_t *__restrict__ src, int64_t n_out, int64_t KB, int pair,
                               int64_t F, uint8_t *__restrict__ dst, int64_t n_records) {
     const int bb = qtype == SD_Q8_0 ? 34 : 18;
@@ -60,34 +66,59 @@ __global__ void repack_kernel(int qtype, const uint8_t *__restrict__ src, int64_
     const int code_bytes = qtype == SD_Q8_0 ? 1024 : 512;
     int64_t total = n_records * 32;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-        int64_t r_id = i >> 5;
-        int row = static_cast<int>(i & 31);
-        // record r_id -> (tile, block); pair mode: records come in (gate, up) pairs per (pair j, block b)
-        int64_t tile, b;
-        int64_t src_row;
+        const int64_t r_id = i >> 5;
+        const int lane = static_cast<int>(i & 31), g = lane >> 2, c = lane & 3;
+        int64_t row0, b, rows_valid;  // source row of record row 0; rows beyond rows_valid are padding
         if (pair) {
-            int64_t pr = r_id >> 1, half = r_id & 1;
-            int64_t j = pr / KB;
+            const int64_t pr = r_id >> 1, half = r_id & 1, j = pr / KB;
             b = pr - j * KB;
-            int64_t rr = j * 32 + row;  // row within gate (or up)
-            src_row = rr < F ? rr + half * F : -1;
-            tile = 0;
+            row0 = j * 32 + half * F;
+            rows_valid = F - j * 32;  // gate and up halves have F rows each
         } else {
-            tile = r_id / KB;
+            const int64_t tile = r_id / KB;
             b = r_id - tile * KB;
-            int64_t rr = tile * 32 + row;
-            src_row = rr < n_out ? rr : -1;
+            row0 = tile * 32;
+            rows_valid = n_out - row0;
         }
+        auto blk = [&](int rr) -> const uint8_t * {
+            return rr < rows_valid ? src + ((row0 + rr) * KB + b) * bb : nullptr;
+        };
         uint8_t *d = dst + r_id * rec;
-        const uint8_t *s = src_row >= 0 ? src + (src_row * KB + b) * bb : nullptr;
-        if (qtype == SD_Q8_0) {
-            for (int e = 0; e < 16; ++e) d[row * 16 + e] = s ? s[2 + e] : 0;
-            for (int e = 0; e < 16; ++e) d[512 + row * 16 + e] = s ? s[2 + 16 + e] : 0;
+        if (qtype == SD_Q4_32) {
+            uint32_t words[4];
+            for (int j = 0; j < 4; ++j) {
+                const int t = j >> 1, s = j & 1;
+                uint32_t wv = 0;
+                for (int nib = 0; nib < 8; ++nib) {
+                    const int dr = (nib & 2) ? 8 : 0;            // nibbles 2, 3, 6, 7: row + 8
+                    const int dk = ((nib & 1) ? 8 : 0) + (nib >> 2);  // 1, 3, 5, 7: k + 8; 4..7: k + 1
+                    const uint8_t *bl = blk(16 * t + g + dr);
+                    const int code = bl ? q4_code(bl, 16 * s + 2 * c + dk) : 8;
+                    wv |= static_cast<uint32_t>(code) << (4 * nib);
+                }
+                words[j] = wv;
+            }
+            for (int j = 0; j < 4; ++j)
+                for (int e = 0; e < 4; ++e) d[lane * 16 + 4 * j + e] = static_cast<uint8_t>(words[j] >> (8 * e));
         } else {
-            for (int e = 0; e < 16; ++e) d[row * 16 + e] = s ? s[2 + e] : 0;
+            for (int w = 0; w < 8; ++w) {
+                const int ts = w >> 1, h = w & 1, t = ts >> 1, s = ts & 1;
+                const int k0 = 16 * s + 2 * c + 8 * h;
+                const uint8_t *bg = blk(16 * t + g), *bg8 = blk(16 * t + g + 8);
+                const uint8_t v[4] = {bg ? bg[2 + k0] : (uint8_t)0, bg ? bg[2 + k0 + 1] : (uint8_t)0,
+                                      bg8 ? bg8[2 + k0] : (uint8_t)0, bg8 ? bg8[2 + k0 + 1] : (uint8_t)0};
+                uint8_t *o = d + (t ? 512 : 0) + lane * 16 + 4 * (w & 3);
+                for (int e = 0; e < 4; ++e) o[e] = v[e];
+            }
         }
-        d[code_bytes + row * 2 + 0] = s ? s[0] : 0;
-        d[code_bytes + row * 2 + 1] = s ? s[1] : 0;
+        if (c == 0) {
+            const int rr[4] = {g, g + 8, 16 + g, 24 + g};
+            for (int e = 0; e < 4; ++e) {
+                const uint8_t *bl = blk(rr[e]);
+                d[code_bytes + g * 8 + 2 * e] = bl ? bl[0] : 0;
+                d[code_bytes + g * 8 + 2 * e + 1] = bl ? bl[1] : 0;
+            }
+        }
     }
 }
 

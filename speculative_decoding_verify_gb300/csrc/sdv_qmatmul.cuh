@@ -3,8 +3,8 @@
 //
 // Work decomposition ("stream-K"): the weights of a matrix are 32-row tiles
 // (or gate|up tile pairs) x k-blocks.  The k range is cut into KS splits of at
-// most 160 blocks so the int8 activations of one split fit in shared memory.
-// Steps (one record of 32 rows x 32 weights, or a gate|up pair of records) are
+// most 80 blocks so the activations of one split fit in shared memory.  Steps
+// (one record of 32 rows x 32 weights, or a gate|up pair of records) are
 // ordered (split, unit, block) and every CTA of a grid of min(#SMs, steps)
 // CTAs takes one contiguous, equal share.  A unit whose steps all fall in one
 // CTA is finished directly; otherwise each CTA writes its partial sums to the
@@ -14,12 +14,15 @@
 //
 // Inside a CTA: warp 8 (one elected lane) streams records with TMA bulk copies
 // into a ring of shared-memory stages guarded by mbarriers; warps 0..7 consume
-// them, lane r owning row r of the record.  Per record and position the lane
-// forms the exact int32 block dot with dp4a (4-bit: sum code*a - 8 sum a, the
-// second term preloaded as the chain's start value together with the 2^23+2^22
-// bias that turns the int32 into its fp32 value with one subtraction) and adds
-// d_w * d_a * dot to its accumulator.  The 8 warps' partials are added in warp
-// order at the end of each piece.
+// them.  Each record's exact int32 block dots come from mma.sync m16n8k16
+// (f16 operands, f32 accumulate): the weight codes enter as the fp16 values
+// 1024 + code (4-bit, one LOP3 per two values; codes in bits 4..7 of a byte
+// enter as 1024 + 16 code against activations pre-divided by 16) or 1152 + q
+// (Q8_0, one PRMT per two values), activations as exact fp16 integers, and the
+// accumulator starts at minus the offsets' contribution, so it ends at the
+// exact integer dot (every partial sum is an integer below 2^23).  Each lane
+// then adds d_w * d_a * dot for its 8 (row, position) results.  The 8 warps'
+// partials are added in warp order at the end of each piece.
 #pragma once
 
 #include "sdv_common.cuh"
@@ -28,12 +31,10 @@ namespace sdv {
 
 constexpr int NCW = 8;                 // consumer warps
 constexpr int QMM_THREADS = (NCW + 1) * 32;
-constexpr int KB_SPLIT_MAX = 160;      // blocks per k-split
+constexpr int KB_SPLIT_MAX = 80;       // blocks per k-split
 constexpr int MPAD = 16;               // position stride of workspace partials
 constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s bound on any in-kernel wait
 constexpr int STAT_TILE = 1024;        // vocabulary tile of the softmax statistics
-constexpr int FP_BIAS_BITS = 0x4B400000;  // bit pattern of 1.5 * 2^23
-constexpr float FP_BIAS = 12582912.0f;
 
 struct QmmArgs {
     const uint8_t *w;
@@ -101,49 +102,112 @@ __device__ __forceinline__ int npieces(const QmmArgs &a, int s, int u) {
 }
 
 // ---------------------------------------------------------------------------
-// block dots of one record row (lane) against one position's activations
+// record layout and exact block dots on the tensor cores
+//
+// Lane l = 4g + c of a warp owns, for a 32-row x 32-weight record, the A
+// fragments of mma m16n8k16 for row tiles t = 0, 1 (rows 16t + g, 16t + g + 8)
+// and k steps s = 0, 1 (k = 16s + 2c, +1 and 16s + 2c + 8, +9).
+//  4-bit: 16 code bytes per lane, word j = 2t + s; nibble i of the word holds
+//    i=0,4: (row 16t+g,   k 16s+2c, +1)   i=2,6: (row 16t+g+8, k 16s+2c, +1)
+//    i=1,5: (row 16t+g,   k 16s+2c+8, +9) i=3,7: (row 16t+g+8, k 16s+2c+8, +9)
+//  Q8_0: 32 code bytes per lane in two 16-byte planes (words 0..3 for t = 0,
+//    words 4..7 for t = 1); word 2(2t+s)+h holds bytes (row 16t+g, k0), (row
+//    16t+g, k0+1), (row 16t+g+8, k0), (row 16t+g+8, k0+1) with k0 = 16s+2c+8h.
+//  Scales: 8 groups of 4 fp16, group g = rows g, g+8, 16+g, 24+g.
 // ---------------------------------------------------------------------------
 
-// 4-bit: w = the lane's 16 code bytes; a0/a1 = activation bytes 0..15 / 16..31;
-// init = -8 * sum(a) + bias.  Low nibbles are elements 0..15, high nibbles 16..31.
-__device__ __forceinline__ int dot_q4(const uint32_t (&lo)[4], const uint32_t (&hi)[4], uint4 a0, uint4 a1, int init) {
-    int d = init;
-    d = dp4a(static_cast<int>(lo[0]), static_cast<int>(a0.x), d);
-    d = dp4a(static_cast<int>(lo[1]), static_cast<int>(a0.y), d);
-    d = dp4a(static_cast<int>(lo[2]), static_cast<int>(a0.z), d);
-    d = dp4a(static_cast<int>(lo[3]), static_cast<int>(a0.w), d);
-    d = dp4a(static_cast<int>(hi[0]), static_cast<int>(a1.x), d);
-    d = dp4a(static_cast<int>(hi[1]), static_cast<int>(a1.y), d);
-    d = dp4a(static_cast<int>(hi[2]), static_cast<int>(a1.z), d);
-    d = dp4a(static_cast<int>(hi[3]), static_cast<int>(a1.w), d);
-    return d;
+__device__ __forceinline__ void mma_init(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1, float c0,
+                                         float c1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%11,%10,%11};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c0), "f"(c1));
 }
 
-__device__ __forceinline__ void unpack_q4(uint4 c, uint32_t (&lo)[4], uint32_t (&hi)[4]) {
-    lo[0] = c.x & 0x0F0F0F0Fu;
-    lo[1] = c.y & 0x0F0F0F0Fu;
-    lo[2] = c.z & 0x0F0F0F0Fu;
-    lo[3] = c.w & 0x0F0F0F0Fu;
-    hi[0] = (c.x >> 4) & 0x0F0F0F0Fu;
-    hi[1] = (c.y >> 4) & 0x0F0F0F0Fu;
-    hi[2] = (c.z >> 4) & 0x0F0F0F0Fu;
-    hi[3] = (c.w >> 4) & 0x0F0F0F0Fu;
+__device__ __forceinline__ void mma_acc(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ int dot_q8(uint4 c0, uint4 c1, uint4 a0, uint4 a1, int init) {
-    int d = init;
-    d = dp4a(static_cast<int>(c0.x), static_cast<int>(a0.x), d);
-    d = dp4a(static_cast<int>(c0.y), static_cast<int>(a0.y), d);
-    d = dp4a(static_cast<int>(c0.z), static_cast<int>(a0.z), d);
-    d = dp4a(static_cast<int>(c0.w), static_cast<int>(a0.w), d);
-    d = dp4a(static_cast<int>(c1.x), static_cast<int>(a1.x), d);
-    d = dp4a(static_cast<int>(c1.y), static_cast<int>(a1.y), d);
-    d = dp4a(static_cast<int>(c1.z), static_cast<int>(a1.z), d);
-    d = dp4a(static_cast<int>(c1.w), static_cast<int>(a1.w), d);
-    return d;
+// 4-bit codes of one lane -> fp16 pairs (1024 + code, or 1024 + 16 code in the k+8 halves)
+__device__ __forceinline__ void q4_frag(uint4 w, uint32_t (&a)[2][2][4]) {
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t x = ws[j], y = x >> 8;
+        a[j >> 1][j & 1][0] = (x & 0x000F000Fu) | 0x64006400u;
+        a[j >> 1][j & 1][1] = (y & 0x000F000Fu) | 0x64006400u;
+        a[j >> 1][j & 1][2] = (x & 0x00F000F0u) | 0x64006400u;
+        a[j >> 1][j & 1][3] = (y & 0x00F000F0u) | 0x64006400u;
+    }
 }
 
-__device__ __forceinline__ float biased_to_float(int d) { return __fsub_rn(__int_as_float(d), FP_BIAS); }
+// Q8_0 codes of one lane -> fp16 pairs 1152 + q (offset binary in the mantissa)
+__device__ __forceinline__ void q8_frag(uint4 p0, uint4 p1, uint32_t (&a)[2][2][4]) {
+    const uint32_t ws[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        const uint32_t x = ws[w] ^ 0x80808080u;
+        const int ts = w >> 1, h = w & 1;
+        a[ts >> 1][ts & 1][2 * h] = __byte_perm(x, 0x64646464u, 0x5140);
+        a[ts >> 1][ts & 1][2 * h + 1] = __byte_perm(x, 0x64646464u, 0x7362);
+    }
+}
+
+// the two row tiles' exact dots of one record against one 8-position tile:
+// d[t][i] = dot(row 16t + g + 8(i>>1), position 2c + (i&1))
+__device__ __forceinline__ void record_dots(const uint32_t (&a)[2][2][4], uint4 bf, float2 corr, float (&d)[2][4]) {
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        mma_init(d[t], a[t][0], bf.x, bf.y, corr.x, corr.y);
+        mma_acc(d[t], a[t][1], bf.z, bf.w);
+    }
+}
+
+// B fragment of one lane for one block and 8-position tile: fp16 activations
+// at (position n = g, k = 16s + 2c, +1, 16s + 2c + 8, +9), the k+8 halves
+// divided by 16 for the 4-bit format.  `arow` = the position's 32 int8 values
+// (nullptr: a padding position).
+template <int QT>
+__device__ __forceinline__ uint4 b_frag(const int8_t *arow, int c) {
+    if (!arow) return make_uint4(0u, 0u, 0u, 0u);
+    uint32_t r[4];
+#pragma unroll
+    for (int s = 0; s < 2; ++s)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int k = 16 * s + 2 * c + 8 * h;
+            const float sc = (QT == SD_Q4_32 && h == 1) ? 0.0625f : 1.0f;
+            const __half lo = __float2half_rn(static_cast<float>(arow[k]) * sc);
+            const __half hi = __float2half_rn(static_cast<float>(arow[k + 1]) * sc);
+            r[2 * s + h] = static_cast<uint32_t>(__half_as_ushort(lo)) |
+                           (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
+        }
+    return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+// accumulator start removing the code offsets: 4-bit -(1032 S_lo + 72 S_hi)
+// with S_lo / S_hi the sums of the activations at k % 16 < 8 / >= 8; Q8_0
+// -1152 S.  Exact integers (|.| < 2^23).
+template <int QT>
+__device__ __forceinline__ float dot_corr(const int8_t *arow) {
+    if (!arow) return 0.0f;
+    const uint4 *p = reinterpret_cast<const uint4 *>(arow);
+    const uint4 x0 = p[0], x1 = p[1];
+    int lo = 0, hi = 0;
+    lo = dp4a(0x01010101, static_cast<int>(x0.x), lo);
+    lo = dp4a(0x01010101, static_cast<int>(x0.y), lo);
+    hi = dp4a(0x01010101, static_cast<int>(x0.z), hi);
+    hi = dp4a(0x01010101, static_cast<int>(x0.w), hi);
+    lo = dp4a(0x01010101, static_cast<int>(x1.x), lo);
+    lo = dp4a(0x01010101, static_cast<int>(x1.y), lo);
+    hi = dp4a(0x01010101, static_cast<int>(x1.z), hi);
+    hi = dp4a(0x01010101, static_cast<int>(x1.w), hi);
+    const int v = QT == SD_Q4_32 ? -(1032 * lo + 72 * hi) : -1152 * (lo + hi);
+    return static_cast<float>(v);
+}
 
 // ---------------------------------------------------------------------------
 // epilogue of one finished (unit, position): lane = row
@@ -269,7 +333,7 @@ __device__ inline void head_final_fold(const QmmArgs &a, int lane, int warp) {
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <int QT, int PAIR, int MT, bool EXACT>
+template <int QT, int PAIR, int NT>
 __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ int s_flag;
@@ -279,14 +343,16 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
     constexpr int REC = QT == SD_Q8_0 ? 1088 : 576;  // bytes of one 32-row record
     constexpr int CODE = QT == SD_Q8_0 ? 1024 : 512; // code bytes of a record
     constexpr int ROWS = PAIR ? 64 : 32;
-    const int M = EXACT ? MT : a.M;
+    constexpr int MT = 8 * NT;  // position slots
+    const int M = a.M;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int lg = lane >> 2, lc = lane & 3;
 
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *empty = full + a.NS;
     uint8_t *ring = smem + a.off_ring;
-    uint8_t *act = smem + a.off_act;
-    float2 *meta = reinterpret_cast<float2 *>(smem + a.off_meta);
+    uint4 *bsm = reinterpret_cast<uint4 *>(smem + a.off_act);     // [block][ntile][lane] B fragments
+    float *meta = reinterpret_cast<float *>(smem + a.off_meta);   // [block][ntile][corr 8 | d_a 8]
     float *red = reinterpret_cast<float *>(smem + a.off_red);
 
     const int64_t lo = static_cast<int64_t>(blockIdx.x) * a.W / a.G;
@@ -353,45 +419,38 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
         const int j1 = static_cast<int>(j0 + (hi - g) < len ? j0 + (hi - g) : len);
 
         if (s != cur_s) {
-            // stage this split's int8 activations: act[jb][m][32], meta[jb][m] = {d_a, chain start}
+            // stage this split's activations as B fragments + per-(block, position) {corr, d_a}
             named_bar_sync(1, NCW * 32);
             const int64_t K = static_cast<int64_t>(a.KB) * 32;
             const int b0 = s * a.KBs;
-            const int nchunk = len * M * 2;
-            for (int c = tid; c < nchunk; c += NCW * 32) {
-                int jb = c / (M * 2), rem = c - jb * (M * 2), m = rem >> 1, h = rem & 1;
-                uint4 v = *reinterpret_cast<const uint4 *>(a.q + m * K + static_cast<int64_t>(b0 + jb) * 32 + h * 16);
-                *reinterpret_cast<uint4 *>(act + (jb * MT + m) * 32 + h * 16) = v;
+            for (int c = tid; c < len * NT * 32; c += NCW * 32) {
+                const int jb = c / (NT * 32), rem = c - jb * (NT * 32), nt = rem >> 5, l = rem & 31;
+                const int n = nt * 8 + (l >> 2);
+                const int8_t *arow = n < M ? a.q + n * K + static_cast<int64_t>(b0 + jb) * 32 : nullptr;
+                bsm[(jb * NT + nt) * 32 + l] = b_frag<QT>(arow, l & 3);
             }
-            for (int c = tid; c < len * M; c += NCW * 32) {
-                int jb = c / M, m = c - jb * M;
-                float da = a.sc[static_cast<int64_t>(m) * a.KB + b0 + jb];
-                int init = FP_BIAS_BITS;
-                if (QT == SD_Q4_32) {
-                    const uint4 *p = reinterpret_cast<const uint4 *>(a.q + m * K + static_cast<int64_t>(b0 + jb) * 32);
-                    uint4 x0 = p[0], x1 = p[1];
-                    int sum = 0;
-                    sum = dp4a(0x01010101, static_cast<int>(x0.x), sum);
-                    sum = dp4a(0x01010101, static_cast<int>(x0.y), sum);
-                    sum = dp4a(0x01010101, static_cast<int>(x0.z), sum);
-                    sum = dp4a(0x01010101, static_cast<int>(x0.w), sum);
-                    sum = dp4a(0x01010101, static_cast<int>(x1.x), sum);
-                    sum = dp4a(0x01010101, static_cast<int>(x1.y), sum);
-                    sum = dp4a(0x01010101, static_cast<int>(x1.z), sum);
-                    sum = dp4a(0x01010101, static_cast<int>(x1.w), sum);
-                    init += -8 * sum;
-                }
-                meta[jb * MT + m] = make_float2(da, __int_as_float(init));
+            for (int c = tid; c < len * MT; c += NCW * 32) {
+                const int jb = c / MT, n = c - jb * MT, nt = n >> 3, p = n & 7;
+                const int8_t *arow = n < M ? a.q + n * K + static_cast<int64_t>(b0 + jb) * 32 : nullptr;
+                float *mp = meta + (jb * NT + nt) * 16;
+                mp[p] = dot_corr<QT>(arow);
+                mp[8 + p] = n < M ? a.sc[static_cast<int64_t>(n) * a.KB + b0 + jb] : 0.0f;
             }
             named_bar_sync(1, NCW * 32);
             cur_s = s;
         }
 
-        float acc[MT], accu[PAIR ? MT : 1];
+        // acc[nt][t][i]: row 16t + lg + 8(i>>1), position 8nt + 2lc + (i&1); accu: the up rows
+        float acc[NT][2][4], accu[PAIR ? NT : 1][2][4];
 #pragma unroll
-        for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int m = 0; m < (PAIR ? MT : 1); ++m) accu[m] = 0.0f;
+            for (int t = 0; t < 2; ++t)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[nt][t][i] = 0.0f;
+                    if (PAIR) accu[PAIR ? nt : 0][t][i] = 0.0f;
+                }
 
         bool aborted = false;
         for (int jj = j0; jj < j1; jj += a.SB) {
@@ -408,52 +467,36 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
             for (int r = warp; r < n; r += NCW) {
                 const uint8_t *rec = sbase + static_cast<size_t>(r) * a.step_bytes;
                 const int jb = jj + r;
-                const uint8_t *ab = act + jb * MT * 32;
-                const float2 *mb = meta + jb * MT;
-                if (QT == SD_Q4_32) {
-                    uint32_t lo4[4], hi4[4], lou[4], hiu[4];
-                    unpack_q4(*reinterpret_cast<const uint4 *>(rec + lane * 16), lo4, hi4);
-                    const float dw = __half2float(*reinterpret_cast<const __half *>(rec + CODE + lane * 2));
-                    float dwu = 0.0f;
-                    if (PAIR) {
-                        unpack_q4(*reinterpret_cast<const uint4 *>(rec + REC + lane * 16), lou, hiu);
-                        dwu = __half2float(*reinterpret_cast<const __half *>(rec + REC + CODE + lane * 2));
-                    }
 #pragma unroll
-                    for (int m = 0; m < MT; ++m) {
-                        if (EXACT || m < M) {
-                            const uint4 a0 = *reinterpret_cast<const uint4 *>(ab + m * 32);
-                            const uint4 a1 = *reinterpret_cast<const uint4 *>(ab + m * 32 + 16);
-                            const float2 mm = mb[m];
-                            const int init = __float_as_int(mm.y);
-                            acc[m] = __fmaf_rn(__fmul_rn(dw, mm.x), biased_to_float(dot_q4(lo4, hi4, a0, a1, init)), acc[m]);
-                            if (PAIR)
-                                accu[m] = __fmaf_rn(__fmul_rn(dwu, mm.x), biased_to_float(dot_q4(lou, hiu, a0, a1, init)),
-                                                    accu[m]);
-                        }
+                for (int half = 0; half < (PAIR ? 2 : 1); ++half) {
+                    const uint8_t *rh = rec + half * REC;
+                    uint32_t af[2][2][4];
+                    if (QT == SD_Q4_32) {
+                        q4_frag(*reinterpret_cast<const uint4 *>(rh + lane * 16), af);
+                    } else {
+                        q8_frag(*reinterpret_cast<const uint4 *>(rh + lane * 16),
+                                *reinterpret_cast<const uint4 *>(rh + 512 + lane * 16), af);
                     }
-                } else {
-                    const uint4 c0 = *reinterpret_cast<const uint4 *>(rec + lane * 16);
-                    const uint4 c1 = *reinterpret_cast<const uint4 *>(rec + 512 + lane * 16);
-                    const float dw = __half2float(*reinterpret_cast<const __half *>(rec + CODE + lane * 2));
-                    uint4 cu0 = make_uint4(0, 0, 0, 0), cu1 = cu0;
-                    float dwu = 0.0f;
-                    if (PAIR) {
-                        cu0 = *reinterpret_cast<const uint4 *>(rec + REC + lane * 16);
-                        cu1 = *reinterpret_cast<const uint4 *>(rec + REC + 512 + lane * 16);
-                        dwu = __half2float(*reinterpret_cast<const __half *>(rec + REC + CODE + lane * 2));
-                    }
+                    const uint2 sw = *reinterpret_cast<const uint2 *>(rh + CODE + lg * 8);
+                    const float2 dw0 = __half22float2(*reinterpret_cast<const __half2 *>(&sw.x));  // rows g, g+8
+                    const float2 dw1 = __half22float2(*reinterpret_cast<const __half2 *>(&sw.y));  // rows 16+g, 24+g
 #pragma unroll
-                    for (int m = 0; m < MT; ++m) {
-                        if (EXACT || m < M) {
-                            const uint4 a0 = *reinterpret_cast<const uint4 *>(ab + m * 32);
-                            const uint4 a1 = *reinterpret_cast<const uint4 *>(ab + m * 32 + 16);
-                            const float2 mm = mb[m];
-                            const int init = __float_as_int(mm.y);
-                            acc[m] = __fmaf_rn(__fmul_rn(dw, mm.x), biased_to_float(dot_q8(c0, c1, a0, a1, init)), acc[m]);
-                            if (PAIR)
-                                accu[m] = __fmaf_rn(__fmul_rn(dwu, mm.x), biased_to_float(dot_q8(cu0, cu1, a0, a1, init)),
-                                                    accu[m]);
+                    for (int nt = 0; nt < NT; ++nt) {
+                        if (NT == 1 || nt * 8 < M) {
+                            const uint4 bf = bsm[(jb * NT + nt) * 32 + lane];
+                            const float *mp = meta + (jb * NT + nt) * 16;
+                            const float2 corr = *reinterpret_cast<const float2 *>(mp + 2 * lc);
+                            const float2 da = *reinterpret_cast<const float2 *>(mp + 8 + 2 * lc);
+                            float d[2][4];
+                            record_dots(af, bf, corr, d);
+                            float (&ac)[2][4] = half ? accu[PAIR ? nt : 0] : acc[nt];
+                            const float wr[2][2] = {{dw0.x, dw0.y}, {dw1.x, dw1.y}};
+#pragma unroll
+                            for (int t = 0; t < 2; ++t)
+#pragma unroll
+                                for (int i = 0; i < 4; ++i)
+                                    ac[t][i] = __fmaf_rn(d[t][i], __fmul_rn(wr[t][i >> 1], (i & 1) ? da.y : da.x),
+                                                         ac[t][i]);
                         }
                     }
                 }
@@ -466,12 +509,15 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
         // ---- finish the piece: add the 8 warps' partials in warp order ----
         if (aborted) s_cabort = 1;
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            if (EXACT || m < M) {
-                red[(warp * MT + m) * ROWS + lane] = acc[m];
-                if (PAIR) red[(warp * MT + m) * ROWS + 32 + lane] = accu[m];
-            }
-        }
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int m = nt * 8 + 2 * lc + (i & 1), row = 16 * t + lg + 8 * (i >> 1);
+                    red[(warp * MT + m) * ROWS + row] = acc[nt][t][i];
+                    if (PAIR) red[(warp * MT + m) * ROWS + 32 + row] = accu[PAIR ? nt : 0][t][i];
+                }
         named_bar_sync(1, NCW * 32);
         if (s_cabort) return;  // uniform: written only before the barrier above
 
@@ -623,18 +669,16 @@ inline bool make_plan(int qtype, int64_t n_out, int64_t k_in, bool pair, bool he
     return true;
 }
 
-// shared-memory layout for MT position slots; returns total bytes
-inline size_t plan_smem(QmmPlan &p, int MT, bool pair, uint32_t &off_ring, uint32_t &off_act, uint32_t &off_meta,
+// shared-memory layout for NT 8-position tiles; returns total bytes
+inline size_t plan_smem(QmmPlan &p, int NT, bool pair, uint32_t &off_ring, uint32_t &off_act, uint32_t &off_meta,
                         uint32_t &off_red) {
     const int rows = pair ? 64 : 32;
-    p.SB = p.step_bytes >= 1000 ? NCW : 2 * NCW;  // ~9-18 KB stages
+    p.SB = p.step_bytes >= 1000 ? NCW : 2 * NCW;  // ~9 KB stages
     const size_t stage = static_cast<size_t>(p.SB) * p.step_bytes;
-    const size_t act = static_cast<size_t>(p.KBs) * MT * 32;
-    const size_t meta = static_cast<size_t>(p.KBs) * MT * 8;
-    const size_t red = static_cast<size_t>(NCW) * MT * rows * 4;
+    const size_t act = static_cast<size_t>(p.KBs) * NT * 512;   // B fragments
+    const size_t meta = static_cast<size_t>(p.KBs) * NT * 64;   // corr + d_a per position
+    const size_t red = static_cast<size_t>(NCW) * 8 * NT * rows * 4;
     const size_t fixed = 256 + act + meta + red;
-    // ~72 KB of stages in flight; with M <= 5 the whole CTA stays near 110 KB so the
-    // next kernel's CTA can be resident (and prefetching) beside it
     size_t ring = 72 * 1024;
     if (fixed + ring > 220 * 1024) ring = fixed + 2 * stage < 220 * 1024 ? 220 * 1024 - fixed : 2 * stage;
     int ns = static_cast<int>(ring / stage);
@@ -648,15 +692,15 @@ inline size_t plan_smem(QmmPlan &p, int MT, bool pair, uint32_t &off_ring, uint3
     return align_up(off_red + red, 128);
 }
 
-template <int QT, int PAIR, int MT, bool EXACT>
+template <int QT, int PAIR, int NT>
 cudaError_t qmm_launch(QmmArgs a, size_t smem, cudaStream_t s) {
-    auto k = qmm_kernel<QT, PAIR, MT, EXACT>;
+    auto k = qmm_kernel<QT, PAIR, NT>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     return launch(k, dim3(a.G), dim3(QMM_THREADS), smem, s, a);
 }
 
-// dispatch on M (exact instantiations for 1..8, a guarded 16-slot one above)
+// dispatch on M: one 8-position tile for M <= 8, two above
 template <int QT, int PAIR>
 cudaError_t qmm_dispatch(QmmArgs a, QmmPlan &p, cudaStream_t s);
 

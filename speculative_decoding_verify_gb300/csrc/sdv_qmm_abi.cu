@@ -4,40 +4,37 @@
 
 namespace sdv {
 
-// one thread per (m, n, b): the same block-dot routines as the matmul, on the
-// repacked records (row r of tile t at record (t, b))
-__global__ void block_dots_kernel(int qtype, const uint8_t *__restrict__ w, int64_t n_out, int32_t KB,
+// One warp per (tile, block): the matmul's own fragment conversion and
+// mma-based exact dots on the repacked record, for every 8-position tile.
+template <int QT>
+__global__ void block_dots_kernel(const uint8_t *__restrict__ w, int64_t n_out, int32_t KB,
                                   const int8_t *__restrict__ q, int32_t M, int32_t *__restrict__ dots) {
-    const int64_t total = static_cast<int64_t>(M) * n_out * KB;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t b = i % KB;
-        const int64_t n = (i / KB) % n_out;
-        const int m = static_cast<int>(i / (KB * n_out));
-        const int64_t t = n / 32;
-        const int r = static_cast<int>(n % 32);
-        const uint4 *ap = reinterpret_cast<const uint4 *>(q + static_cast<int64_t>(m) * KB * 32 + b * 32);
-        const uint4 a0 = ap[0], a1 = ap[1];
-        int d;
-        if (qtype == SD_Q4_32) {
-            const uint8_t *rec = w + (t * KB + b) * 576;
-            uint32_t lo[4], hi[4];
-            unpack_q4(*reinterpret_cast<const uint4 *>(rec + r * 16), lo, hi);
-            int sum = 0;
-            sum = dp4a(0x01010101, static_cast<int>(a0.x), sum);
-            sum = dp4a(0x01010101, static_cast<int>(a0.y), sum);
-            sum = dp4a(0x01010101, static_cast<int>(a0.z), sum);
-            sum = dp4a(0x01010101, static_cast<int>(a0.w), sum);
-            sum = dp4a(0x01010101, static_cast<int>(a1.x), sum);
-            sum = dp4a(0x01010101, static_cast<int>(a1.y), sum);
-            sum = dp4a(0x01010101, static_cast<int>(a1.z), sum);
-            sum = dp4a(0x01010101, static_cast<int>(a1.w), sum);
-            d = dot_q4(lo, hi, a0, a1, FP_BIAS_BITS - 8 * sum);
-        } else {
-            const uint8_t *rec = w + (t * KB + b) * 1088;
-            d = dot_q8(*reinterpret_cast<const uint4 *>(rec + r * 16), *reinterpret_cast<const uint4 *>(rec + 512 + r * 16),
-                       a0, a1, FP_BIAS_BITS);
-        }
-        dots[i] = static_cast<int32_t>(biased_to_float(d));
+    constexpr int REC = QT == SD_Q8_0 ? 1088 : 576;
+    const int64_t tile = blockIdx.x / KB;
+    const int b = static_cast<int>(blockIdx.x - tile * KB);
+    const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+    const int64_t K = static_cast<int64_t>(KB) * 32;
+    const uint8_t *rec = w + (tile * KB + b) * REC;
+    uint32_t af[2][2][4];
+    if (QT == SD_Q4_32)
+        q4_frag(*reinterpret_cast<const uint4 *>(rec + lane * 16), af);
+    else
+        q8_frag(*reinterpret_cast<const uint4 *>(rec + lane * 16), *reinterpret_cast<const uint4 *>(rec + 512 + lane * 16),
+                af);
+    for (int nt = 0; nt * 8 < M; ++nt) {
+        const int nb = nt * 8 + g;
+        const uint4 bf = b_frag<QT>(nb < M ? q + nb * K + b * 32 : nullptr, c);
+        const int m0 = nt * 8 + 2 * c, m1 = m0 + 1;
+        const float2 corr = make_float2(dot_corr<QT>(m0 < M ? q + m0 * K + b * 32 : nullptr),
+                                        dot_corr<QT>(m1 < M ? q + m1 * K + b * 32 : nullptr));
+        float d[2][4];
+        record_dots(af, bf, corr, d);
+        for (int t = 0; t < 2; ++t)
+            for (int i = 0; i < 4; ++i) {
+                const int m = m0 + (i & 1);
+                const int64_t n = tile * 32 + 16 * t + g + 8 * (i >> 1);
+                if (m < M && n < n_out) dots[(static_cast<int64_t>(m) * n_out + n) * KB + b] = static_cast<int32_t>(d[t][i]);
+            }
     }
 }
 
@@ -177,10 +174,14 @@ sd_status sd_debug_block_dots(int qtype, const void *w, int64_t n_out, int64_t k
                               int32_t *dots, sd_stream_t stream) {
     if ((qtype != SD_Q8_0 && qtype != SD_Q4_32) || !w || !q || !dots || M < 1 || M > 16) return SD_EINVAL;
     if (k_in <= 0 || k_in % 32 || n_out <= 0 || !aligned(w, 16) || !aligned(q, 16)) return SD_EINVAL;
-    const int64_t total = static_cast<int64_t>(M) * n_out * (k_in / 32);
-    const int grid = static_cast<int>(total / 256 + 1 < 8192 ? total / 256 + 1 : 8192);
-    block_dots_kernel<<<grid, 256, 0, cs(stream)>>>(qtype, static_cast<const uint8_t *>(w), n_out,
-                                                    static_cast<int32_t>(k_in / 32), q, M, dots);
+    const int64_t blocks = (n_out + 31) / 32 * (k_in / 32);
+    if (blocks > 0x7fffffff) return SD_EINVAL;
+    if (qtype == SD_Q4_32)
+        block_dots_kernel<SD_Q4_32><<<static_cast<unsigned>(blocks), 32, 0, cs(stream)>>>(
+            static_cast<const uint8_t *>(w), n_out, static_cast<int32_t>(k_in / 32), q, M, dots);
+    else
+        block_dots_kernel<SD_Q8_0><<<static_cast<unsigned>(blocks), 32, 0, cs(stream)>>>(
+            static_cast<const uint8_t *>(w), n_out, static_cast<int32_t>(k_in / 32), q, M, dots);
     return cudaGetLastError() == cudaSuccess ? SD_OK : SD_ECUDA;
 }
 

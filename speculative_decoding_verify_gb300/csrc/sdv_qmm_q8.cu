@@ -7,26 +7,16 @@ namespace sdv {
 
 template <>
 cudaError_t qmm_dispatch<SD_Q8_0, 0>(QmmArgs a, QmmPlan &p, cudaStream_t s) {
-    const int MT = a.M <= 8 ? a.M : 16;
+    const int NT = a.M <= 8 ? 1 : 2;
     uint32_t o_ring, o_act, o_meta, o_red;
-    const size_t smem = plan_smem(p, MT, 0 != 0, o_ring, o_act, o_meta, o_red);
+    const size_t smem = plan_smem(p, NT, 0 != 0, o_ring, o_act, o_meta, o_red);
     a.SB = p.SB;
     a.NS = p.NS;
     a.off_ring = o_ring;
     a.off_act = o_act;
     a.off_meta = o_meta;
     a.off_red = o_red;
-    switch (a.M) {
-        case 1: return qmm_launch<SD_Q8_0, 0, 1, true>(a, smem, s);
-        case 2: return qmm_launch<SD_Q8_0, 0, 2, true>(a, smem, s);
-        case 3: return qmm_launch<SD_Q8_0, 0, 3, true>(a, smem, s);
-        case 4: return qmm_launch<SD_Q8_0, 0, 4, true>(a, smem, s);
-        case 5: return qmm_launch<SD_Q8_0, 0, 5, true>(a, smem, s);
-        case 6: return qmm_launch<SD_Q8_0, 0, 6, true>(a, smem, s);
-        case 7: return qmm_launch<SD_Q8_0, 0, 7, true>(a, smem, s);
-        case 8: return qmm_launch<SD_Q8_0, 0, 8, true>(a, smem, s);
-        default: return qmm_launch<SD_Q8_0, 0, 16, false>(a, smem, s);
-    }
+    return NT == 1 ? qmm_launch<SD_Q8_0, 0, 1>(a, smem, s) : qmm_launch<SD_Q8_0, 0, 2>(a, smem, s);
 }
 
 }  // namespace sdv

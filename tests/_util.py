@@ -34,38 +34,59 @@ def assert_close(g, o, absb, what=""):
 
 
 def unpack_repacked(qtype, buf, n_out, k_in, pair=False):
-    """Inverse of the documented repack layout -> GGUF-order blocks [n_out][k_in/32 * bb]."""
+    """Inverse of the documented repack layout -> GGUF-order blocks [n_out][k_in/32 * bb].
+
+    Record = 32 rows x one 32-weight block; lane l = 4g + c holds the A fragments of
+    mma m16n8k16 for rows 16t+g (+8) and k 16s+2c (+1, +8, +9).  4-bit: word 2t+s of the
+    lane's 16 bytes, nibble i at (row 16t+g+8[i&2], k 16s+2c+8[i&1]+(i>>2)).  Q8_0:
+    plane t (512 B each), word 2s+h holds (row 16t+g, k0), (.., k0+1), (row 16t+g+8, k0),
+    (.., k0+1) with k0 = 16s+2c+8h.  Scales: group g = rows g, g+8, 16+g, 24+g."""
     buf = np.asarray(buf, dtype=np.uint8)
     KB = k_in // 32
     bb = oracle.BLOCK_BYTES[qtype]
     rec = 1088 if qtype == oracle.Q8_0 else 576
-    code = 1024 if qtype == oracle.Q8_0 else 512
+    code_b = 1024 if qtype == oracle.Q8_0 else 512
+    halves = 2 if pair else 1
+    rows_per = n_out // 2 if pair else n_out
+    nt = (rows_per + 31) // 32
+    recs = buf.reshape(nt, KB, halves, rec)
+    vals = np.zeros((nt, halves, 32, KB, 32), dtype=np.int32)   # [tile][half][row][block][k]: code or q
+    dsc = np.zeros((nt, halves, 32, KB, 2), dtype=np.uint8)
+    for lane in range(32):
+        g, c = lane >> 2, lane & 3
+        if qtype == oracle.Q4_32:
+            words = recs[:, :, :, lane * 16:(lane + 1) * 16].reshape(nt, KB, halves, 4, 4).astype(np.uint32)
+            words = (words[..., 0] | (words[..., 1] << 8) | (words[..., 2] << 16) | (words[..., 3] << 24))
+            for j in range(4):
+                t, s_ = j >> 1, j & 1
+                for i in range(8):
+                    row = 16 * t + g + (8 if i & 2 else 0)
+                    k = 16 * s_ + 2 * c + (8 if i & 1 else 0) + (i >> 2)
+                    vals[:, :, row, :, k] = ((words[:, :, :, j] >> (4 * i)) & 0xF).transpose(0, 2, 1)
+        else:
+            for t in range(2):
+                plane = recs[:, :, :, t * 512 + lane * 16:t * 512 + (lane + 1) * 16].reshape(nt, KB, halves, 4, 4)
+                for wq in range(4):
+                    s_, h = wq >> 1, wq & 1
+                    k0 = 16 * s_ + 2 * c + 8 * h
+                    for e, (dr, dk) in enumerate(((0, 0), (0, 1), (8, 0), (8, 1))):
+                        vals[:, :, 16 * t + g + dr, :, k0 + dk] = plane[:, :, :, wq, e].astype(np.int8).transpose(0, 2, 1)
+        if c == 0:
+            for e, row in enumerate((g, g + 8, 16 + g, 24 + g)):
+                off = code_b + g * 8 + 2 * e
+                dsc[:, :, row, :, :] = recs[:, :, :, off:off + 2].transpose(0, 2, 1, 3)
     out = np.zeros((n_out, KB, bb), dtype=np.uint8)
-    if pair:
-        F = n_out // 2
-        nt = (F + 31) // 32
-        recs = buf.reshape(nt, KB, 2, rec)
-    else:
-        nt = (n_out + 31) // 32
-        recs = buf.reshape(nt, KB, 1, rec)
-    for t in range(nt):
-        for h in range(recs.shape[2]):
-            r = recs[t, :, h, :]                   # [KB][rec]
-            rows = np.arange(32) + t * 32
-            if pair:
-                rows = rows + h * (n_out // 2)
-                valid = (np.arange(32) + t * 32) < n_out // 2
-            else:
-                valid = rows < n_out
-            for i in np.nonzero(valid)[0]:
-                n = rows[i]
-                out[n, :, 0] = r[:, code + 2 * i]
-                out[n, :, 1] = r[:, code + 2 * i + 1]
-                if qtype == oracle.Q8_0:
-                    out[n, :, 2:18] = r[:, i * 16:(i + 1) * 16]
-                    out[n, :, 18:34] = r[:, 512 + i * 16:512 + (i + 1) * 16]
-                else:
-                    out[n, :, 2:18] = r[:, i * 16:(i + 1) * 16]
+    for h in range(halves):
+        blockrows = np.arange(nt * 32)
+        valid = blockrows < rows_per
+        v = vals[:, h].reshape(nt * 32, KB, 32)[valid]
+        d = dsc[:, h].reshape(nt * 32, KB, 2)[valid]
+        r0 = h * rows_per
+        out[r0:r0 + rows_per, :, 0:2] = d
+        if qtype == oracle.Q8_0:
+            out[r0:r0 + rows_per, :, 2:] = v.astype(np.int8).view(np.uint8)
+        else:
+            out[r0:r0 + rows_per, :, 2:] = (v[:, :, :16] | (v[:, :, 16:] << 4)).astype(np.uint8)
     return out.reshape(n_out, KB * bb)
 
 

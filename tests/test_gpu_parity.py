@@ -27,12 +27,13 @@ def sdv():
     return m
 
 
-def gpu_qmm(sdv, qtype, blocks, n, k, q, s, residual=None, epi=0, col0=0, want_y=True):
+def gpu_qmm(sdv, qtype, blocks, n, k, q, s, residual=None, epi=0, col0=0, want_y=True, ws=None):
     pair = epi == sdv.EPI_SILU_MUL_REQUANT
     w = sdv.repack_weights(qtype, cuda(blocks).reshape(-1), n, k, pair)
     torch.cuda.synchronize()
     M = q.shape[0]
-    ws = sdv.workspace(sdv.qmatmul_workspace_bytes(qtype, n, k, epi))
+    if ws is None:
+        ws = sdv.workspace(sdv.qmatmul_workspace_bytes(qtype, n, k, epi))
     y = torch.full((M, n), float("nan"), dtype=torch.float32, device="cuda") if want_y else None
     res = cuda(residual) if residual is not None else None
     qn = sn = None
@@ -166,7 +167,7 @@ def test_qmatmul_vs_oracle(sdv, qtype, shape, M):
     yo, ab = oracle.qmatmul(qtype, blocks, n, k, q, s)
     assert_close(y, yo, ab, f"qmm q{qtype} {shape} M={M}")
     # a second call on the same workspace (its counters must be back at zero) gives the same bits
-    y2, _, _, _ = gpu_qmm(sdv, qtype, blocks, n, k, q, s)
+    y2, _, _, _ = gpu_qmm(sdv, qtype, blocks, n, k, q, s, ws=ws)
     assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
 
 
