@@ -131,8 +131,10 @@ sd_status sd_rmsnorm_quant_acts(const float *x, int64_t ldx, const float *norm_w
  * the device's SM count) only, never on M, so a row computed among M
  * positions equals the same row computed alone, bit for bit.
  * workspace: ws_bytes >= sd_qmatmul_workspace_bytes(...), zero-filled by the
- * caller once; every call returns its counters to zero (partial sums are
- * scratch).  Calls sharing one workspace must be ordered on one stream.
+ * caller once.  Its first 160 KB are counters at fixed offsets that every call
+ * returns to zero; the rest is scratch.  One workspace may therefore serve
+ * calls of any shape (sized for the largest), as long as they are ordered on
+ * one stream.  After an SD_ETIMEOUT it must be zero-filled again.
  */
 size_t sd_qmatmul_workspace_bytes(int qtype, int64_t n_out, int64_t k_in, uint32_t epilogue);
 sd_status sd_qmatmul_multipos(int qtype, const void *w, int64_t n_out, int64_t k_in, const int8_t *q,

@@ -44,11 +44,19 @@ def build(force: bool = False, verbose: bool = False, ptxas_log: str | None = No
     os.makedirs(BUILD_DIR, exist_ok=True)
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cuh")]
     headers.append(os.path.join(ROOT, "include", "sdverify.h"))
+    stamp = os.path.join(BUILD_DIR, "flags.txt")
+    want = os.environ.get("SDV_NVCC_FLAGS", "")
+    if not os.path.exists(stamp) or open(stamp).read() != want:
+        force = True
+        with open(stamp, "w") as f:
+            f.write(want)
     srcs = sources()
     flags = ["-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
              "-I", os.path.join(ROOT, "include")] + ARCH
     if ptxas_log:
         flags += ["-Xptxas", "-v"]
+    extra = os.environ.get("SDV_NVCC_FLAGS", "").split()
+    flags += extra
     objs = []
     jobs = []
     for s in srcs:

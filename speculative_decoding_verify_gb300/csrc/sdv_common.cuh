@@ -5,7 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/sdverify.h"
+#include "sdverify.h"
 
 namespace sdv {
 

@@ -3,7 +3,7 @@
 //
 // Work decomposition ("stream-K"): the weights of a matrix are 32-row tiles
 // (or gate|up tile pairs) x k-blocks.  The k range is cut into KS splits of at
-// most 80 blocks so the activations of one split fit in shared memory.  Steps
+// most 160 blocks so the activations of one split fit in shared memory.  Steps
 // (one record of 32 rows x 32 weights, or a gate|up pair of records) are
 // ordered (split, unit, block) and every CTA of a grid of min(#SMs, steps)
 // CTAs takes one contiguous, equal share.  A unit whose steps all fall in one
@@ -29,12 +29,18 @@
 
 namespace sdv {
 
-constexpr int NCW = 8;                 // consumer warps
+#ifndef SDV_NCW
+#define SDV_NCW 8
+#endif
+constexpr int NCW = SDV_NCW;           // consumer warps
 constexpr int QMM_THREADS = (NCW + 1) * 32;
-constexpr int KB_SPLIT_MAX = 80;       // blocks per k-split
+constexpr int KB_SPLIT_MAX = 160;      // blocks per k-split
 constexpr int MPAD = 16;               // position stride of workspace partials
 constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s bound on any in-kernel wait
 constexpr int STAT_TILE = 1024;        // vocabulary tile of the softmax statistics
+constexpr int WS_UNIT_CNT = 32768;     // workspace counters: units (tiles / tile pairs) per call
+constexpr int WS_STAT_CNT = 2048;      // workspace counters: 1024-token statistics tiles
+constexpr size_t WS_CNT_BYTES = 160 * 1024;  // >= (WS_UNIT_CNT + WS_STAT_CNT + 1) * 4, 256-aligned
 
 struct QmmArgs {
     const uint8_t *w;
@@ -71,8 +77,15 @@ struct QmmArgs {
     uint32_t *st_done;   // [1]
     int32_t n_stiles;
     int *status;
-    uint32_t off_ring, off_act, off_meta, off_red;
+    uint32_t off_ring, off_act, off_meta, off_red, off_tmp;
 };
+
+// fetch-and-add with release (orders the CTA's prior writes, seen through a bar.sync) and acquire
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
 
 __device__ __forceinline__ void decode_step(const QmmArgs &a, int64_t g, int &s, int &u, int &j, int &len) {
     int64_t per = static_cast<int64_t>(a.NU) * a.KBs;
@@ -166,26 +179,34 @@ __device__ __forceinline__ void record_dots(const uint32_t (&a)[2][2][4], uint4 
     }
 }
 
-// B fragment of one lane for one block and 8-position tile: fp16 activations
-// at (position n = g, k = 16s + 2c, +1, 16s + 2c + 8, +9), the k+8 halves
-// divided by 16 for the 4-bit format.  `arow` = the position's 32 int8 values
-// (nullptr: a padding position).
+// Raw int8 B operand of one lane for one block and 8-position tile: the bytes at
+// k = 2c, 2c+1, 2c+8, 2c+9, 16+2c, 17+2c, 24+2c, 25+2c of position g's 32
+// activations, as two 32-bit words (pairs in k order).  `arow` nullptr: padding.
+__device__ __forceinline__ uint2 b_raw(const int8_t *arow, int c) {
+    if (!arow) return make_uint2(0u, 0u);
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(arow);
+    const int sh = 16 * (c & 1), j = c >> 1;
+    const uint32_t p0 = (w[j] >> sh) & 0xFFFFu, p1 = (w[2 + j] >> sh) & 0xFFFFu;
+    const uint32_t p2 = (w[4 + j] >> sh) & 0xFFFFu, p3 = (w[6 + j] >> sh) & 0xFFFFu;
+    return make_uint2(p0 | (p1 << 16), p2 | (p3 << 16));
+}
+
+// int8 pair (low 16 bits of x, k order) -> exact fp16 pair; `div16` also scales by 1/16 (exact)
+__device__ __forceinline__ uint32_t i8pair_to_h2(uint32_t x, bool div16) {
+    const uint32_t u = __byte_perm(x ^ 0x8080u, 0x64646464u, 0x5140);  // (1024 + a + 128) per half
+    __half2 h = *reinterpret_cast<const __half2 *>(&u);
+    if (div16) h = __hfma2(h, __float2half2_rn(0.0625f), __float2half2_rn(-72.0f));  // (1152 + a)/16 - 72 = a/16
+    else h = __hsub2(h, __float2half2_rn(1152.0f));
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// fp16 B fragment registers from the raw operand: {s0 k 2c.., s0 k 2c+8.., s1 k 2c.., s1 k 2c+8..};
+// the k+8 halves divided by 16 for the 4-bit format
 template <int QT>
-__device__ __forceinline__ uint4 b_frag(const int8_t *arow, int c) {
-    if (!arow) return make_uint4(0u, 0u, 0u, 0u);
-    uint32_t r[4];
-#pragma unroll
-    for (int s = 0; s < 2; ++s)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int k = 16 * s + 2 * c + 8 * h;
-            const float sc = (QT == SD_Q4_32 && h == 1) ? 0.0625f : 1.0f;
-            const __half lo = __float2half_rn(static_cast<float>(arow[k]) * sc);
-            const __half hi = __float2half_rn(static_cast<float>(arow[k + 1]) * sc);
-            r[2 * s + h] = static_cast<uint32_t>(__half_as_ushort(lo)) |
-                           (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
-        }
-    return make_uint4(r[0], r[1], r[2], r[3]);
+__device__ __forceinline__ uint4 b_frag_from_raw(uint2 r) {
+    const bool d = QT == SD_Q4_32;
+    return make_uint4(i8pair_to_h2(r.x, false), i8pair_to_h2(r.x >> 16, d), i8pair_to_h2(r.y, false),
+                      i8pair_to_h2(r.y >> 16, d));
 }
 
 // accumulator start removing the code offsets: 4-bit -(1032 S_lo + 72 S_hi)
@@ -330,6 +351,36 @@ __device__ inline void head_final_fold(const QmmArgs &a, int lane, int warp) {
     }
 }
 
+// Adds `n_done` finished 32-row tiles to statistics tile `st`; the CTA that completes the tile
+// computes its statistics, and the CTA that completes the last tile folds them.  Called by all
+// consumer threads (bar.sync inside); the finished logits were written before the call.
+__device__ __forceinline__ void head_flush(const QmmArgs &a, int st, int n_done, int tid, int lane, int warp,
+                                           int &s_flag) {
+    if (st < 0 || n_done == 0) return;
+    named_bar_sync(1, NCW * 32);
+    if (tid == 0) {
+        const int tiles_in_st = (a.NU - st * (STAT_TILE / 32)) < (STAT_TILE / 32) ? (a.NU - st * (STAT_TILE / 32))
+                                                                                   : (STAT_TILE / 32);
+        const unsigned old = atom_add_acq_rel(&a.st_cnt[st], static_cast<uint32_t>(n_done));
+        s_flag = (static_cast<int>(old) + n_done == tiles_in_st) ? 1 : 0;
+    }
+    named_bar_sync(1, NCW * 32);
+    if (!s_flag) return;
+    head_tile_stats(a, st, lane, warp);
+    named_bar_sync(1, NCW * 32);
+    if (tid == 0) {
+        a.st_cnt[st] = 0u;
+        const unsigned old = atom_add_acq_rel(a.st_done, 1u);
+        s_flag = (static_cast<int>(old) == a.n_stiles - 1) ? 1 : 0;
+    }
+    named_bar_sync(1, NCW * 32);
+    if (s_flag) {
+        head_final_fold(a, lane, warp);
+        if (tid == 0) *a.st_done = 0u;
+    }
+    named_bar_sync(1, NCW * 32);
+}
+
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
@@ -337,6 +388,7 @@ template <int QT, int PAIR, int NT>
 __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ int s_flag;
+    __shared__ int s_st_cur, s_st_n;  // head: current statistics tile and tiles finished in it
     __shared__ volatile int s_abort;   // set by anyone whose bounded wait ran out
     __shared__ volatile int s_cabort;  // set by consumers only, read after a consumer barrier
 
@@ -351,7 +403,10 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *empty = full + a.NS;
     uint8_t *ring = smem + a.off_ring;
-    uint4 *bsm = reinterpret_cast<uint4 *>(smem + a.off_act);     // [block][ntile][lane] B fragments
+    // B operands of the split: fp16 fragments [block][lane] (one position tile) or raw int8
+    // fragments [block][tile][lane] converted at use (two position tiles)
+    uint4 *bsm = reinterpret_cast<uint4 *>(smem + a.off_act);
+    uint2 *bsm8 = reinterpret_cast<uint2 *>(smem + a.off_act);
     float *meta = reinterpret_cast<float *>(smem + a.off_meta);   // [block][ntile][corr 8 | d_a 8]
     float *red = reinterpret_cast<float *>(smem + a.off_red);
 
@@ -365,6 +420,8 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
         }
         s_abort = 0;
         s_cabort = 0;
+        s_st_cur = -1;
+        s_st_n = 0;
         fence_barrier_init();
     }
     __syncthreads();
@@ -419,22 +476,39 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
         const int j1 = static_cast<int>(j0 + (hi - g) < len ? j0 + (hi - g) : len);
 
         if (s != cur_s) {
-            // stage this split's activations as B fragments + per-(block, position) {corr, d_a}
+            // stage this split's activations straight from global memory: B operands (fp16 fragments,
+            // or raw int8 for two position tiles) and per-(block, position) {corr, d_a}
             named_bar_sync(1, NCW * 32);
             const int64_t K = static_cast<int64_t>(a.KB) * 32;
             const int b0 = s * a.KBs;
-            for (int c = tid; c < len * NT * 32; c += NCW * 32) {
-                const int jb = c / (NT * 32), rem = c - jb * (NT * 32), nt = rem >> 5, l = rem & 31;
-                const int n = nt * 8 + (l >> 2);
-                const int8_t *arow = n < M ? a.q + n * K + static_cast<int64_t>(b0 + jb) * 32 : nullptr;
-                bsm[(jb * NT + nt) * 32 + l] = b_frag<QT>(arow, l & 3);
+            const int nitems = len * NT * 32;
+            for (int base = tid; base < nitems; base += 4 * NCW * 32) {
+                uint2 raw[4];
+#pragma unroll
+                for (int u4 = 0; u4 < 4; ++u4) {
+                    const int c = base + u4 * NCW * 32;
+                    raw[u4] = make_uint2(0u, 0u);
+                    if (c < nitems) {
+                        const int jb = c / (NT * 32), rem = c - jb * (NT * 32), nt = rem >> 5, l = rem & 31;
+                        const int n = nt * 8 + (l >> 2);
+                        raw[u4] = b_raw(n < M ? a.q + n * K + static_cast<int64_t>(b0 + jb) * 32 : nullptr, l & 3);
+                    }
+                }
+#pragma unroll
+                for (int u4 = 0; u4 < 4; ++u4) {
+                    const int c = base + u4 * NCW * 32;
+                    if (c < nitems) {
+                        if (NT == 1) bsm[c] = b_frag_from_raw<QT>(raw[u4]);
+                        else bsm8[c] = raw[u4];
+                    }
+                }
             }
             for (int c = tid; c < len * MT; c += NCW * 32) {
                 const int jb = c / MT, n = c - jb * MT, nt = n >> 3, p = n & 7;
-                const int8_t *arow = n < M ? a.q + n * K + static_cast<int64_t>(b0 + jb) * 32 : nullptr;
                 float *mp = meta + (jb * NT + nt) * 16;
-                mp[p] = dot_corr<QT>(arow);
-                mp[8 + p] = n < M ? a.sc[static_cast<int64_t>(n) * a.KB + b0 + jb] : 0.0f;
+                const bool real = n < M;
+                mp[p] = dot_corr<QT>(real ? a.q + n * K + static_cast<int64_t>(b0 + jb) * 32 : nullptr);
+                mp[8 + p] = real ? a.sc[static_cast<int64_t>(n) * a.KB + b0 + jb] : 0.0f;
             }
             named_bar_sync(1, NCW * 32);
             cur_s = s;
@@ -464,39 +538,76 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
                 break;
             }
             const uint8_t *sbase = ring + static_cast<size_t>(stg) * a.SB * a.step_bytes;
-            for (int r = warp; r < n; r += NCW) {
-                const uint8_t *rec = sbase + static_cast<size_t>(r) * a.step_bytes;
-                const int jb = jj + r;
+            // each warp takes steps warp and warp + NCW of the stage; for a gate|up pair the two
+            // halves of one step are the two records
+            constexpr int RPW = PAIR ? 2 : 2;  // records handled together per warp
+            const int r0 = warp, r1 = warp + NCW;
+            const int nrec = PAIR ? (r0 < n ? 2 : 0) : ((r0 < n) + (r1 < n));
+            if (nrec > 0) {
+                const uint8_t *rp[RPW];
+                int jbr[RPW];
 #pragma unroll
-                for (int half = 0; half < (PAIR ? 2 : 1); ++half) {
-                    const uint8_t *rh = rec + half * REC;
-                    uint32_t af[2][2][4];
-                    if (QT == SD_Q4_32) {
-                        q4_frag(*reinterpret_cast<const uint4 *>(rh + lane * 16), af);
+                for (int q = 0; q < RPW; ++q) {
+                    if (PAIR) {
+                        rp[q] = sbase + static_cast<size_t>(r0) * a.step_bytes + q * REC;
+                        jbr[q] = jj + r0;
                     } else {
-                        q8_frag(*reinterpret_cast<const uint4 *>(rh + lane * 16),
-                                *reinterpret_cast<const uint4 *>(rh + 512 + lane * 16), af);
+                        rp[q] = sbase + static_cast<size_t>(q ? r1 : r0) * a.step_bytes;
+                        jbr[q] = jj + (q ? r1 : r0);
                     }
-                    const uint2 sw = *reinterpret_cast<const uint2 *>(rh + CODE + lg * 8);
-                    const float2 dw0 = __half22float2(*reinterpret_cast<const __half2 *>(&sw.x));  // rows g, g+8
-                    const float2 dw1 = __half22float2(*reinterpret_cast<const __half2 *>(&sw.y));  // rows 16+g, 24+g
+                }
+                uint32_t af[RPW][2][2][4];
+                float2 dwf[RPW][2];
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        if (NT == 1 || nt * 8 < M) {
-                            const uint4 bf = bsm[(jb * NT + nt) * 32 + lane];
-                            const float *mp = meta + (jb * NT + nt) * 16;
-                            const float2 corr = *reinterpret_cast<const float2 *>(mp + 2 * lc);
-                            const float2 da = *reinterpret_cast<const float2 *>(mp + 8 + 2 * lc);
-                            float d[2][4];
-                            record_dots(af, bf, corr, d);
-                            float (&ac)[2][4] = half ? accu[PAIR ? nt : 0] : acc[nt];
-                            const float wr[2][2] = {{dw0.x, dw0.y}, {dw1.x, dw1.y}};
+                for (int q = 0; q < RPW; ++q) {
+                    if (q < nrec) {
+                        if (QT == SD_Q4_32) {
+                            q4_frag(*reinterpret_cast<const uint4 *>(rp[q] + lane * 16), af[q]);
+                        } else {
+                            q8_frag(*reinterpret_cast<const uint4 *>(rp[q] + lane * 16),
+                                    *reinterpret_cast<const uint4 *>(rp[q] + 512 + lane * 16), af[q]);
+                        }
+                        const uint2 sw = *reinterpret_cast<const uint2 *>(rp[q] + CODE + lg * 8);
+                        dwf[q][0] = __half22float2(*reinterpret_cast<const __half2 *>(&sw.x));  // rows g, g+8
+                        dwf[q][1] = __half22float2(*reinterpret_cast<const __half2 *>(&sw.y));  // rows 16+g, 24+g
+                    }
+                }
 #pragma unroll
-                            for (int t = 0; t < 2; ++t)
+                for (int nt = 0; nt < NT; ++nt) {
+                    if (NT == 1 || nt * 8 < M) {
+                        float d[RPW][2][4];
+                        float2 da[RPW];
 #pragma unroll
-                                for (int i = 0; i < 4; ++i)
-                                    ac[t][i] = __fmaf_rn(d[t][i], __fmul_rn(wr[t][i >> 1], (i & 1) ? da.y : da.x),
-                                                         ac[t][i]);
+                        for (int q = 0; q < RPW; ++q) {
+                            if (q < nrec && (q == 0 || !PAIR)) {
+                                const int jb = jbr[q];
+                                const uint4 bf = NT == 1 ? bsm[jb * 32 + lane]
+                                                         : b_frag_from_raw<QT>(bsm8[(jb * NT + nt) * 32 + lane]);
+                                const float *mp = meta + (jb * NT + nt) * 16;
+                                const float2 corr = *reinterpret_cast<const float2 *>(mp + 2 * lc);
+                                da[q] = *reinterpret_cast<const float2 *>(mp + 8 + 2 * lc);
+                                record_dots(af[q], bf, corr, d[q]);
+                                if (PAIR) {  // the up half shares the step's activations
+                                    da[1] = da[0];
+                                    record_dots(af[1], bf, corr, d[1]);
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int q = 0; q < RPW; ++q) {
+                            if (q < nrec) {
+                                float (&ac)[2][4] = (PAIR && q == 1) ? accu[PAIR ? nt : 0] : acc[nt];
+#pragma unroll
+                                for (int t = 0; t < 2; ++t) {
+                                    const float w0 = t ? dwf[q][1].x : dwf[q][0].x;
+                                    const float w1 = t ? dwf[q][1].y : dwf[q][0].y;
+#pragma unroll
+                                    for (int i = 0; i < 4; ++i)
+                                        ac[t][i] = __fmaf_rn(d[q][t][i], __fmul_rn((i >> 1) ? w1 : w0,
+                                                                                   (i & 1) ? da[q].y : da[q].x),
+                                                             ac[t][i]);
+                                }
+                            }
                         }
                     }
                 }
@@ -537,18 +648,15 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
                 pp[m * ROWS + lane] = v;
                 if (PAIR) pp[m * ROWS + 32 + lane] = vu;
             }
-            __threadfence();
-            named_bar_sync(1, NCW * 32);
+            named_bar_sync(1, NCW * 32);  // the partial sums above happen before thread 0's fence
             if (tid == 0) {
                 int expected = 0;
                 for (int s2 = 0; s2 < a.KS; ++s2) expected += npieces(a, s2, u);
-                __threadfence();
-                unsigned old = atomicAdd(&a.cnt[u], 1u);
+                const unsigned old = atom_add_acq_rel(&a.cnt[u], 1u);
                 s_flag = (static_cast<int>(old) == expected - 1) ? 1 : 0;
             }
             named_bar_sync(1, NCW * 32);
-            finish = s_flag != 0;
-            if (finish) __threadfence();
+            finish = s_flag != 0;  // thread 0 fenced after its atomic; reads below bypass L1
         }
 
         if (finish) {
@@ -587,41 +695,24 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
             if (!direct && tid == 0) a.cnt[u] = 0u;
 
             if (a.head) {
-                __threadfence();
-                named_bar_sync(1, NCW * 32);
+                // count finished tiles per 1024-token statistics tile; one counter update per
+                // (CTA, statistics tile) run, issued when the run ends
                 const int st = u / (STAT_TILE / 32);
-                if (tid == 0) {
-                    const int tiles_in_st = (a.NU - st * (STAT_TILE / 32)) < (STAT_TILE / 32)
-                                                ? (a.NU - st * (STAT_TILE / 32))
-                                                : (STAT_TILE / 32);
-                    __threadfence();
-                    unsigned old = atomicAdd(&a.st_cnt[st], 1u);
-                    s_flag = (static_cast<int>(old) == tiles_in_st - 1) ? 1 : 0;
-                }
-                named_bar_sync(1, NCW * 32);
-                if (s_flag) {
-                    __threadfence();
-                    head_tile_stats(a, st, lane, warp);
-                    __threadfence();
-                    named_bar_sync(1, NCW * 32);
+                if (st != s_st_cur) {
+                    head_flush(a, s_st_cur, s_st_n, tid, lane, warp, s_flag);
                     if (tid == 0) {
-                        a.st_cnt[st] = 0u;
-                        __threadfence();
-                        unsigned old = atomicAdd(a.st_done, 1u);
-                        s_flag = (static_cast<int>(old) == a.n_stiles - 1) ? 1 : 0;
+                        s_st_cur = st;
+                        s_st_n = 0;
                     }
                     named_bar_sync(1, NCW * 32);
-                    if (s_flag) {
-                        __threadfence();
-                        head_final_fold(a, lane, warp);
-                        if (tid == 0) *a.st_done = 0u;
-                    }
                 }
+                if (tid == 0) s_st_n += 1;
             }
         }
         named_bar_sync(1, NCW * 32);  // red[] and s_flag are reused by the next piece
         g += j1 - j0;
     }
+    if (a.head) head_flush(a, s_st_cur, s_st_n, tid, lane, warp, s_flag);
 }
 
 // ---------------------------------------------------------------------------
@@ -659,28 +750,34 @@ inline bool make_plan(int qtype, int64_t n_out, int64_t k_in, bool pair, bool he
     p.SB = 0;
     p.NS = 0;
     const int rows = pair ? 64 : 32;
-    p.ws_part = align_up(static_cast<size_t>(p.NU) * p.KS * p.P * rows * MPAD * sizeof(float), 256);
-    p.ws_cnt = align_up(static_cast<size_t>(p.NU) * sizeof(uint32_t), 256);
+    // counters first, at fixed offsets shared by every call: units [0, WS_UNIT_CNT), statistics
+    // tiles [WS_UNIT_CNT, WS_UNIT_CNT + WS_STAT_CNT), the statistics "done" counter after them.
+    // Each call returns the counters it used to zero, so a workspace can serve calls of any shape.
+    if (p.NU > WS_UNIT_CNT) return false;
     const int64_t nst = (n_out + STAT_TILE - 1) / STAT_TILE;
-    p.ws_stats = head ? align_up(static_cast<size_t>(nst) * MPAD * sizeof(float4), 256) +
-                            align_up(static_cast<size_t>(nst + 1) * sizeof(uint32_t), 256)
-                      : 0;
+    if (head && nst > WS_STAT_CNT) return false;
+    p.ws_cnt = WS_CNT_BYTES;
+    p.ws_part = align_up(static_cast<size_t>(p.NU) * p.KS * p.P * rows * MPAD * sizeof(float), 256);
+    p.ws_stats = head ? align_up(static_cast<size_t>(nst) * MPAD * sizeof(float4), 256) : 0;
     p.ws_total = p.ws_part + p.ws_cnt + p.ws_stats;
     return true;
 }
 
 // shared-memory layout for NT 8-position tiles; returns total bytes
 inline size_t plan_smem(QmmPlan &p, int NT, bool pair, uint32_t &off_ring, uint32_t &off_act, uint32_t &off_meta,
-                        uint32_t &off_red) {
+                        uint32_t &off_red, uint32_t &off_tmp) {
     const int rows = pair ? 64 : 32;
-    p.SB = p.step_bytes >= 1000 ? NCW : 2 * NCW;  // ~9 KB stages
+    p.SB = pair ? NCW : 2 * NCW;  // two records per consumer warp per stage
     const size_t stage = static_cast<size_t>(p.SB) * p.step_bytes;
-    const size_t act = static_cast<size_t>(p.KBs) * NT * 512;   // B fragments
+    const size_t act = static_cast<size_t>(p.KBs) * (NT == 1 ? 512 : 2 * 256);  // fp16 or raw int8 fragments
     const size_t meta = static_cast<size_t>(p.KBs) * NT * 64;   // corr + d_a per position
     const size_t red = static_cast<size_t>(NCW) * 8 * NT * rows * 4;
-    const size_t fixed = 256 + act + meta + red;
-    size_t ring = 72 * 1024;
-    if (fixed + ring > 220 * 1024) ring = fixed + 2 * stage < 220 * 1024 ? 220 * 1024 - fixed : 2 * stage;
+    const size_t tmp = 0;
+    const size_t fixed = 256 + act + meta + red + tmp;
+    size_t ring = 96 * 1024;
+    if (ring < 4 * stage) ring = 4 * stage;
+    if (fixed + ring > 222 * 1024) ring = (222 * 1024 - fixed) / stage * stage;
+    if (ring < 2 * stage) ring = 2 * stage;
     int ns = static_cast<int>(ring / stage);
     if (ns > 12) ns = 12;
     if (ns < 2) ns = 2;
@@ -689,7 +786,8 @@ inline size_t plan_smem(QmmPlan &p, int NT, bool pair, uint32_t &off_ring, uint3
     off_act = static_cast<uint32_t>(align_up(off_ring + ns * stage, 128));
     off_meta = static_cast<uint32_t>(align_up(off_act + act, 16));
     off_red = static_cast<uint32_t>(align_up(off_meta + meta, 16));
-    return align_up(off_red + red, 128);
+    off_tmp = static_cast<uint32_t>(align_up(off_red + red, 16));
+    return align_up(off_tmp + tmp, 128);
 }
 
 template <int QT, int PAIR, int NT>

@@ -23,7 +23,7 @@ __global__ void block_dots_kernel(const uint8_t *__restrict__ w, int64_t n_out, 
                 af);
     for (int nt = 0; nt * 8 < M; ++nt) {
         const int nb = nt * 8 + g;
-        const uint4 bf = b_frag<QT>(nb < M ? q + nb * K + b * 32 : nullptr, c);
+        const uint4 bf = b_frag_from_raw<QT>(b_raw(nb < M ? q + nb * K + b * 32 : nullptr, c));
         const int m0 = nt * 8 + 2 * c, m1 = m0 + 1;
         const float2 corr = make_float2(dot_corr<QT>(m0 < M ? q + m0 * K + b * 32 : nullptr),
                                         dot_corr<QT>(m1 < M ? q + m1 * K + b * 32 : nullptr));
@@ -123,8 +123,8 @@ sd_status sd_qmatmul_multipos(int qtype, const void *w, int64_t n_out, int64_t k
     a.s_next = scales_next;
     a.nq = nq;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    a.part = reinterpret_cast<float *>(ws);
-    a.cnt = reinterpret_cast<uint32_t *>(ws + p.ws_part);
+    a.cnt = reinterpret_cast<uint32_t *>(ws);
+    a.part = reinterpret_cast<float *>(ws + p.ws_cnt);
     a.status = st;
     return dispatch(qtype, pair, a, p, cs(stream)) == cudaSuccess ? SD_OK : SD_ECUDA;
 }
@@ -153,13 +153,12 @@ sd_status sd_head_logits(const void *w, int64_t vocab, int64_t hidden, const int
     a.y = logits;
     a.epi = SD_EPI_NONE;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    a.part = reinterpret_cast<float *>(ws);
-    a.cnt = reinterpret_cast<uint32_t *>(ws + p.ws_part);
+    a.cnt = reinterpret_cast<uint32_t *>(ws);
+    a.st_cnt = a.cnt + WS_UNIT_CNT;
+    a.st_done = a.st_cnt + WS_STAT_CNT;
+    a.part = reinterpret_cast<float *>(ws + p.ws_cnt);
     const int64_t nst = (vocab + STAT_TILE - 1) / STAT_TILE;
-    uint8_t *stb = ws + p.ws_part + p.ws_cnt;
-    a.st_part = reinterpret_cast<float4 *>(stb);
-    a.st_cnt = reinterpret_cast<uint32_t *>(stb + align_up(static_cast<size_t>(nst) * MPAD * sizeof(float4), 256));
-    a.st_done = a.st_cnt + nst;
+    a.st_part = reinterpret_cast<float4 *>(ws + p.ws_cnt + p.ws_part);
     a.n_stiles = static_cast<int32_t>(nst);
     a.head = 1;
     a.T = temperature;

@@ -186,6 +186,20 @@ def test_qmatmul_residual_in_place(sdv, qtype):
     assert_close(host(h), yo, ab, "in-place residual")
 
 
+def test_one_workspace_serves_mixed_shapes(sdv):
+    """Calls of different shapes (different unit counts and k splits) share one workspace."""
+    M = 5
+    shapes = [(3 * 256, 320, 4), (640, 5120, 3), (96, 17408, 2), (4000, 1024, 1), (640, 5120, 3)]
+    ws = sdv.workspace(max(sdv.qmatmul_workspace_bytes(oracle.Q4_32, n, k) for n, k, _ in shapes))
+    for n, k, key in shapes:
+        blocks = sdgen.quantized_normal(oracle.Q4_32, sdgen.key(140, key), n, k)
+        q, s = acts(sdgen.key(141, k), M, k)
+        r = sdgen.normal(sdgen.key(142, n), (M, n))
+        y, _, _, _ = gpu_qmm(sdv, oracle.Q4_32, blocks, n, k, q, s, residual=r, ws=ws)
+        yo, ab = oracle.qmatmul(oracle.Q4_32, blocks, n, k, q, s, residual=r)
+        assert_close(y, yo, ab, f"shared workspace {n}x{k}")
+
+
 def test_requant_epilogue(sdv):
     """QKV-like: the last third of the columns is requantised in the epilogue.  The codes equal the
     standalone requantisation kernel applied to the same GPU outputs; the outputs match the oracle."""
