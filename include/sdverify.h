@@ -203,6 +203,83 @@ sd_status sd_accept_sample(const float *logits, int64_t vocab, int32_t K, const 
                            uint64_t seed, int64_t base_pos, int32_t *out_tokens, int32_t *out_count,
                            sd_stream_t stream);
 
+/*
+ * The whole verify pass in one persistent cooperative launch ("Inside OpenJet
+ * Engine", section "One GPU launch for a speculative cycle": one persistent
+ * kernel carries the cycle's phases with a software grid barrier between them).
+ *
+ * Per layer: RMSNorm + requant -> QKV (3H, columns [2H, 3H) requantised in the
+ * epilogue) -> O on those codes (+ residual into h) -> RMSNorm + requant ->
+ * gate|up (SiLU*mul requant epilogue) -> down (+ residual into h); then the final
+ * RMSNorm, the Q8_0 vocabulary head with argmax / statistics, and greedy
+ * acceptance (chain, or tree when parent != NULL).  Every phase runs the same
+ * device code as the single-operation calls above, so the pass produces the
+ * same bits as issuing those calls one by one.  Between phases the CTAs meet at
+ * a grid barrier (release/acquire on a counter in the plan, each wait bounded
+ * to 2 s, SD_ETIMEOUT in the status word on expiry); the weight stream never
+ * waits for it.
+ *
+ * sd_layer / sd_pass_desc: device pointers to repacked weights (gate_up repacked
+ * with SD_REPACK_PAIR_GATE_UP, 4-bit) and fp32 norm weights [hidden]; h [M][hidden]
+ * is the residual stream (input rows in, final hidden state out); qa/sa
+ * [M][hidden], qv/sv [M][hidden], qf/sf [M][ffn] (and [.../32] scales) are
+ * activation scratch; logits [M][vocab], argmax/row_max/row_sumexp [M];
+ * tokens = drafts [M-1] (chain) or node tokens [M] (tree); out_tokens [M],
+ * out_count [1].  workspace: >= sd_pass_workspace_bytes, zero-filled once.
+ * layers is a HOST array read only by sd_pass_prepare.
+ * sd_pass_prepare writes the phase table into `plan` (device, 256-byte aligned,
+ * >= sd_pass_plan_bytes(n_layers), synchronously) and fills `out`;
+ * sd_verify_pass launches it on `stream` (capturable in a CUDA graph).  Every
+ * GPU of the pool runs one CTA per SM; the launch fails with SD_ECUDA rather
+ * than wait if the GPU cannot hold them all at once.
+ */
+typedef struct {
+    const void *qkv, *o, *gate_up, *down;
+    const float *norm1, *norm2;
+} sd_layer;
+
+typedef struct {
+    int32_t n_layers;
+    int64_t hidden, ffn, vocab;
+    int32_t M;
+    int32_t wq; /* SD_Q4_32 */
+    float eps;
+    float temperature;
+    const sd_layer *layers;
+    const float *final_norm;
+    const void *head; /* Q8_0, repacked */
+    float *h;
+    int8_t *qa;
+    float *sa;
+    int8_t *qv;
+    float *sv;
+    int8_t *qf;
+    float *sf;
+    float *logits;
+    int32_t *argmax;
+    float *row_max;
+    float *row_sumexp;
+    const int32_t *tokens;
+    const int32_t *parent;
+    int32_t *out_tokens;
+    int32_t *out_count;
+    void *workspace;
+    size_t ws_bytes;
+} sd_pass_desc;
+
+typedef struct {
+    void *plan;
+    int32_t n_phases;
+    int32_t nt;
+    uint32_t smem_bytes;
+    int32_t grid;
+} sd_pass;
+
+size_t sd_pass_plan_bytes(int32_t n_layers);
+size_t sd_pass_workspace_bytes(int64_t hidden, int64_t ffn, int64_t vocab, int32_t wq);
+sd_status sd_pass_prepare(const sd_pass_desc *desc, void *plan, size_t plan_bytes, sd_pass *out);
+sd_status sd_verify_pass(const sd_pass *pass, sd_stream_t stream);
+
 /* Synchronises `stream`, returns and clears the current device's status word
  * (SD_OK, SD_ETIMEOUT or SD_EDEVICE); SD_ECUDA if synchronising failed. */
 sd_status sd_device_status(sd_stream_t stream);

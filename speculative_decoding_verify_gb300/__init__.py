@@ -30,6 +30,28 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: 
 _lib = None
 
 
+class SdLayer(ctypes.Structure):
+    _fields_ = [("qkv", ctypes.c_void_p), ("o", ctypes.c_void_p), ("gate_up", ctypes.c_void_p),
+                ("down", ctypes.c_void_p), ("norm1", ctypes.c_void_p), ("norm2", ctypes.c_void_p)]
+
+
+class SdPassDesc(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int32), ("hidden", ctypes.c_int64), ("ffn", ctypes.c_int64),
+                ("vocab", ctypes.c_int64), ("M", ctypes.c_int32), ("wq", ctypes.c_int32), ("eps", ctypes.c_float),
+                ("temperature", ctypes.c_float), ("layers", ctypes.POINTER(SdLayer)),
+                ("final_norm", ctypes.c_void_p), ("head", ctypes.c_void_p), ("h", ctypes.c_void_p),
+                ("qa", ctypes.c_void_p), ("sa", ctypes.c_void_p), ("qv", ctypes.c_void_p), ("sv", ctypes.c_void_p),
+                ("qf", ctypes.c_void_p), ("sf", ctypes.c_void_p), ("logits", ctypes.c_void_p),
+                ("argmax", ctypes.c_void_p), ("row_max", ctypes.c_void_p), ("row_sumexp", ctypes.c_void_p),
+                ("tokens", ctypes.c_void_p), ("parent", ctypes.c_void_p), ("out_tokens", ctypes.c_void_p),
+                ("out_count", ctypes.c_void_p), ("workspace", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t)]
+
+
+class SdPass(ctypes.Structure):
+    _fields_ = [("plan", ctypes.c_void_p), ("n_phases", ctypes.c_int32), ("nt", ctypes.c_int32),
+                ("smem_bytes", ctypes.c_uint32), ("grid", ctypes.c_int32)]
+
+
 class SdError(RuntimeError):
     def __init__(self, code: int, what: str):
         super().__init__(f"{what}: {STATUS.get(code, code)} ({code})")
@@ -64,6 +86,10 @@ def lib():
             "sd_debug_cexp": ([P, I64, P, P], I),
             "sd_debug_philox": ([U64, I64, I64, P, P], I),
             "sd_debug_wait_timeout": ([I64, P], I),
+            "sd_pass_plan_bytes": ([I32], SZ),
+            "sd_pass_workspace_bytes": ([I64, I64, I64, I32], SZ),
+            "sd_pass_prepare": ([ctypes.POINTER(SdPassDesc), P, SZ, ctypes.POINTER(SdPass)], I),
+            "sd_verify_pass": ([ctypes.POINTER(SdPass), P], I),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -176,6 +202,24 @@ def device_status() -> int:
 
 def set_pdl(enable: bool):
     lib().sd_set_pdl(1 if enable else 0)
+
+
+def pass_plan_bytes(n_layers: int) -> int:
+    return int(lib().sd_pass_plan_bytes(n_layers))
+
+
+def pass_workspace_bytes(hidden: int, ffn: int, vocab: int, wq: int = Q4_32) -> int:
+    return int(lib().sd_pass_workspace_bytes(hidden, ffn, vocab, wq))
+
+
+def pass_prepare(desc: SdPassDesc, plan: torch.Tensor) -> SdPass:
+    out = SdPass()
+    _check(lib().sd_pass_prepare(ctypes.byref(desc), _p(plan), plan.numel(), ctypes.byref(out)), "sd_pass_prepare")
+    return out
+
+
+def verify_pass(p: SdPass):
+    _check(lib().sd_verify_pass(ctypes.byref(p), _stream()), "sd_verify_pass")
 
 
 # ---------------------------------------------------------------------------

@@ -78,7 +78,19 @@ struct QmmArgs {
     int32_t n_stiles;
     int *status;
     uint32_t off_ring, off_act, off_meta, off_red, off_tmp;
+    uint32_t stage_stride;  // bytes between ring slots (>= SB * step_bytes)
+    // phase kind inside a pass: 0 matmul (qt, pair), 1 RMSNorm + requant, 2 greedy acceptance
+    int32_t kind, qt, pair;
+    const float *xin;       // RMSNorm input [M][K] (K = 32 KB)
+    const float *norm_w;    // RMSNorm weight [K]
+    float eps;
+    const int32_t *tokens;  // acceptance inputs / outputs
+    const int32_t *parent;
+    int32_t *out_tokens;
+    int32_t *out_count;
 };
+
+constexpr int KIND_MATMUL = 0, KIND_NORM = 1, KIND_ACCEPT = 2;
 
 // fetch-and-add with release (orders the CTA's prior writes, seen through a bar.sync) and acquire
 __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v) {
@@ -184,10 +196,10 @@ __device__ __forceinline__ void record_dots(const uint32_t (&a)[2][2][4], uint4 
 // activations, as two 32-bit words (pairs in k order).  `arow` nullptr: padding.
 __device__ __forceinline__ uint2 b_raw(const int8_t *arow, int c) {
     if (!arow) return make_uint2(0u, 0u);
-    const uint32_t *w = reinterpret_cast<const uint32_t *>(arow);
+    const unsigned *w = reinterpret_cast<const unsigned *>(arow);
     const int sh = 16 * (c & 1), j = c >> 1;
-    const uint32_t p0 = (w[j] >> sh) & 0xFFFFu, p1 = (w[2 + j] >> sh) & 0xFFFFu;
-    const uint32_t p2 = (w[4 + j] >> sh) & 0xFFFFu, p3 = (w[6 + j] >> sh) & 0xFFFFu;
+    const uint32_t p0 = (__ldcg(w + j) >> sh) & 0xFFFFu, p1 = (__ldcg(w + 2 + j) >> sh) & 0xFFFFu;
+    const uint32_t p2 = (__ldcg(w + 4 + j) >> sh) & 0xFFFFu, p3 = (__ldcg(w + 6 + j) >> sh) & 0xFFFFu;
     return make_uint2(p0 | (p1 << 16), p2 | (p3 << 16));
 }
 
@@ -216,7 +228,7 @@ template <int QT>
 __device__ __forceinline__ float dot_corr(const int8_t *arow) {
     if (!arow) return 0.0f;
     const uint4 *p = reinterpret_cast<const uint4 *>(arow);
-    const uint4 x0 = p[0], x1 = p[1];
+    const uint4 x0 = __ldcg(p), x1 = __ldcg(p + 1);
     int lo = 0, hi = 0;
     lo = dp4a(0x01010101, static_cast<int>(x0.x), lo);
     lo = dp4a(0x01010101, static_cast<int>(x0.y), lo);
@@ -250,7 +262,7 @@ __device__ __forceinline__ void epilogue(const QmmArgs &a, int u, int m, int lan
     } else {
         const int64_t n = static_cast<int64_t>(u) * 32 + lane;
         const bool ok = n < a.n_out;
-        if (ok && a.residual) v = __fadd_rn(v, a.residual[m * a.n_out + n]);
+        if (ok && a.residual) v = __fadd_rn(v, __ldcg(a.residual + m * a.n_out + n));
         if (ok && a.y) a.y[m * a.n_out + n] = v;
         if (a.epi == SD_EPI_REQUANT && static_cast<int64_t>(u) * 32 >= a.col0) {
             float d;
@@ -382,16 +394,92 @@ __device__ __forceinline__ void head_flush(const QmmArgs &a, int st, int n_done,
 }
 
 // ---------------------------------------------------------------------------
-// the kernel
+// per-CTA state and shared-memory regions
+// ---------------------------------------------------------------------------
+struct CtaShared {
+    int flag;
+    int st_cur, st_n;      // head: current statistics tile and tiles finished in it
+    volatile int abort;    // set by anyone whose bounded wait ran out
+    volatile int cabort;   // set by consumers only, read after a consumer barrier
+    float inv[16];         // RMSNorm phase: 1 / rms of each row
+};
+
+struct Smem {
+    uint64_t *full, *empty;
+    uint8_t *ring;
+    uint4 *bsm;   // B operands of the split: fp16 fragments [block][lane] (one position tile)
+    uint2 *bsm8;  // ... or raw int8 fragments [block][tile][lane] converted at use (two tiles)
+    float *meta;  // [block][tile][corr 8 | d_a 8]
+    float *red;   // per-warp partial sums [warp][position][row]; RMSNorm scratch
+};
+
+__device__ __forceinline__ Smem smem_regions(uint8_t *smem, const QmmArgs &a) {
+    Smem r;
+    r.full = reinterpret_cast<uint64_t *>(smem);
+    r.empty = r.full + a.NS;
+    r.ring = smem + a.off_ring;
+    r.bsm = reinterpret_cast<uint4 *>(smem + a.off_act);
+    r.bsm8 = reinterpret_cast<uint2 *>(smem + a.off_act);
+    r.meta = reinterpret_cast<float *>(smem + a.off_meta);
+    r.red = reinterpret_cast<float *>(smem + a.off_red);
+    return r;
+}
+
+__device__ __forceinline__ void cta_init(const Smem &sm, int NS, CtaShared &cs) {
+    for (int i = 0; i < NS; ++i) {
+        mbar_init(&sm.full[i], 1);
+        mbar_init(&sm.empty[i], NCW);
+    }
+    cs.abort = 0;
+    cs.cabort = 0;
+    cs.st_cur = -1;
+    cs.st_n = 0;
+    fence_barrier_init();
+}
+
+// ---------------------------------------------------------------------------
+// producer: stream this CTA's share of one matmul phase through the ring.
+// `it` counts stages over the whole launch (slot it % NS, phase parity it / NS).
+// ---------------------------------------------------------------------------
+__device__ inline void produce_phase(const QmmArgs &a, const Smem &sm, uint32_t &it, CtaShared &cs, uint64_t pol) {
+    const int64_t lo = static_cast<int64_t>(blockIdx.x) * a.W / a.G;
+    const int64_t hi = static_cast<int64_t>(blockIdx.x + 1) * a.W / a.G;
+    int64_t g = lo;
+    while (g < hi && !cs.abort) {
+        int s, u, j0, len;
+        decode_step(a, g, s, u, j0, len);
+        const int j1 = static_cast<int>(j0 + (hi - g) < len ? j0 + (hi - g) : len);
+        for (int jj = j0; jj < j1 && !cs.abort; jj += a.SB) {
+            const int n = j1 - jj < a.SB ? j1 - jj : a.SB;
+            const int stg = static_cast<int>(it % a.NS);
+            const uint32_t ph = (it / a.NS) & 1u;
+            if (!mbar_wait_bounded(&sm.empty[stg], ph ^ 1u, WAIT_NS, &cs.abort)) {
+                set_status(a.status, SD_ETIMEOUT);
+                cs.abort = 1;
+                break;
+            }
+            const uint32_t bytes = static_cast<uint32_t>(n) * a.step_bytes;
+            const uint8_t *src =
+                a.w + (static_cast<int64_t>(u) * a.KB + static_cast<int64_t>(s) * a.KBs + jj) * a.step_bytes;
+            mbar_arrive_expect_tx(&sm.full[stg], bytes);
+            bulk_g2s(sm.ring + static_cast<size_t>(stg) * a.stage_stride, src, bytes, &sm.full[stg], pol);
+            ++it;
+        }
+        g += j1 - j0;
+    }
+}
+
+// never leave with copies in flight: wait for the last issued stages
+__device__ inline void producer_drain(const Smem &sm, uint32_t it, int NS) {
+    const uint32_t first = it > static_cast<uint32_t>(NS) ? it - NS : 0u;
+    for (uint32_t k = first; k < it; ++k) mbar_wait_bounded(&sm.full[k % NS], (k / NS) & 1u, WAIT_NS);
+}
+
+// ---------------------------------------------------------------------------
+// consumers: one matmul phase (staging, stages, piece fixups, epilogues)
 // ---------------------------------------------------------------------------
 template <int QT, int PAIR, int NT>
-__global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
-    extern __shared__ __align__(1024) uint8_t smem[];
-    __shared__ int s_flag;
-    __shared__ int s_st_cur, s_st_n;  // head: current statistics tile and tiles finished in it
-    __shared__ volatile int s_abort;   // set by anyone whose bounded wait ran out
-    __shared__ volatile int s_cabort;  // set by consumers only, read after a consumer barrier
-
+__device__ inline void consume_phase(const QmmArgs &a, const Smem &sm, uint32_t &it, CtaShared &cs) {
     constexpr int REC = QT == SD_Q8_0 ? 1088 : 576;  // bytes of one 32-row record
     constexpr int CODE = QT == SD_Q8_0 ? 1024 : 512; // code bytes of a record
     constexpr int ROWS = PAIR ? 64 : 32;
@@ -399,75 +487,13 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
     const int M = a.M;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int lg = lane >> 2, lc = lane & 3;
-
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
-    uint64_t *empty = full + a.NS;
-    uint8_t *ring = smem + a.off_ring;
-    // B operands of the split: fp16 fragments [block][lane] (one position tile) or raw int8
-    // fragments [block][tile][lane] converted at use (two position tiles)
-    uint4 *bsm = reinterpret_cast<uint4 *>(smem + a.off_act);
-    uint2 *bsm8 = reinterpret_cast<uint2 *>(smem + a.off_act);
-    float *meta = reinterpret_cast<float *>(smem + a.off_meta);   // [block][ntile][corr 8 | d_a 8]
-    float *red = reinterpret_cast<float *>(smem + a.off_red);
+    uint4 *bsm = sm.bsm;
+    uint2 *bsm8 = sm.bsm8;
+    float *meta = sm.meta;
+    float *red = sm.red;
 
     const int64_t lo = static_cast<int64_t>(blockIdx.x) * a.W / a.G;
     const int64_t hi = static_cast<int64_t>(blockIdx.x + 1) * a.W / a.G;
-
-    if (tid == 0) {
-        for (int i = 0; i < a.NS; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], NCW);
-        }
-        s_abort = 0;
-        s_cabort = 0;
-        s_st_cur = -1;
-        s_st_n = 0;
-        fence_barrier_init();
-    }
-    __syncthreads();
-
-    if (warp == NCW) {
-        // ------------------------------ producer ------------------------------
-        pdl_launch_dependents();
-        if (lane == 0) {
-            const uint64_t pol = policy_evict_first();
-            uint32_t it = 0;
-            int64_t g = lo;
-            while (g < hi && !s_abort) {
-                int s, u, j0, len;
-                decode_step(a, g, s, u, j0, len);
-                int j1 = static_cast<int>(j0 + (hi - g) < len ? j0 + (hi - g) : len);
-                for (int jj = j0; jj < j1 && !s_abort; jj += a.SB) {
-                    int n = j1 - jj < a.SB ? j1 - jj : a.SB;
-                    int stg = static_cast<int>(it % a.NS);
-                    uint32_t ph = (it / a.NS) & 1u;
-                    if (!mbar_wait_bounded(&empty[stg], ph ^ 1u, WAIT_NS, &s_abort)) {
-                        set_status(a.status, SD_ETIMEOUT);
-                        s_abort = 1;
-                        break;
-                    }
-                    uint32_t bytes = static_cast<uint32_t>(n) * a.step_bytes;
-                    const uint8_t *src = a.w + (static_cast<int64_t>(u) * a.KB + static_cast<int64_t>(s) * a.KBs + jj) *
-                                                   a.step_bytes;
-                    mbar_arrive_expect_tx(&full[stg], bytes);
-                    bulk_g2s(ring + static_cast<size_t>(stg) * a.SB * a.step_bytes, src, bytes, &full[stg], pol);
-                    ++it;
-                }
-                g += j1 - j0;
-            }
-            // never leave with copies in flight: wait for the last issued stages
-            uint32_t first = it > static_cast<uint32_t>(a.NS) ? it - a.NS : 0u;
-            for (uint32_t k = first; k < it; ++k)
-                mbar_wait_bounded(&full[k % a.NS], (k / a.NS) & 1u, WAIT_NS);
-        }
-        return;
-    }
-
-    // ------------------------------ consumers ------------------------------
-    pdl_wait();
-    pdl_launch_dependents();
-
-    uint32_t it = 0;
     int cur_s = -1;
     int64_t g = lo;
     while (g < hi) {
@@ -508,7 +534,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
                 float *mp = meta + (jb * NT + nt) * 16;
                 const bool real = n < M;
                 mp[p] = dot_corr<QT>(real ? a.q + n * K + static_cast<int64_t>(b0 + jb) * 32 : nullptr);
-                mp[8 + p] = real ? a.sc[static_cast<int64_t>(n) * a.KB + b0 + jb] : 0.0f;
+                mp[8 + p] = real ? __ldcg(a.sc + static_cast<int64_t>(n) * a.KB + b0 + jb) : 0.0f;
             }
             named_bar_sync(1, NCW * 32);
             cur_s = s;
@@ -531,19 +557,18 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
             const int n = j1 - jj < a.SB ? j1 - jj : a.SB;
             const int stg = static_cast<int>(it % a.NS);
             const uint32_t ph = (it / a.NS) & 1u;
-            if (!mbar_wait_bounded(&full[stg], ph, WAIT_NS, &s_abort)) {
+            if (!mbar_wait_bounded(&sm.full[stg], ph, WAIT_NS, &cs.abort)) {
                 set_status(a.status, SD_ETIMEOUT);
-                s_abort = 1;
+                cs.abort = 1;
                 aborted = true;
                 break;
             }
-            const uint8_t *sbase = ring + static_cast<size_t>(stg) * a.SB * a.step_bytes;
-            // each warp takes steps warp and warp + NCW of the stage; for a gate|up pair the two
-            // halves of one step are the two records
-            constexpr int RPW = PAIR ? 2 : 2;  // records handled together per warp
-            const int r0 = warp, r1 = warp + NCW;
-            const int nrec = PAIR ? (r0 < n ? 2 : 0) : ((r0 < n) + (r1 < n));
-            if (nrec > 0) {
+            const uint8_t *sbase = sm.ring + static_cast<size_t>(stg) * a.stage_stride;
+            // per round each warp takes steps r0 and r0 + NCW (for a gate|up pair, step r0's two halves)
+            constexpr int RPW = 2;
+            for (int r0 = warp; r0 < n; r0 += (PAIR ? 1 : 2) * NCW) {
+                const int r1 = r0 + NCW;
+                const int nrec = PAIR ? 2 : (1 + (r1 < n));
                 const uint8_t *rp[RPW];
                 int jbr[RPW];
 #pragma unroll
@@ -613,12 +638,12 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[stg]);
+            if (lane == 0) mbar_arrive(&sm.empty[stg]);
             ++it;
         }
 
         // ---- finish the piece: add the 8 warps' partials in warp order ----
-        if (aborted) s_cabort = 1;
+        if (aborted) cs.cabort = 1;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -630,7 +655,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
                     if (PAIR) red[(warp * MT + m) * ROWS + 32 + row] = accu[PAIR ? nt : 0][t][i];
                 }
         named_bar_sync(1, NCW * 32);
-        if (s_cabort) return;  // uniform: written only before the barrier above
+        if (cs.cabort) return;  // uniform: written only before the barrier above
 
         const bool direct = (a.KS == 1) && (npieces(a, s, u) == 1);
         bool finish = direct;
@@ -648,15 +673,15 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
                 pp[m * ROWS + lane] = v;
                 if (PAIR) pp[m * ROWS + 32 + lane] = vu;
             }
-            named_bar_sync(1, NCW * 32);  // the partial sums above happen before thread 0's fence
+            named_bar_sync(1, NCW * 32);  // the partial sums above happen before thread 0's release
             if (tid == 0) {
                 int expected = 0;
                 for (int s2 = 0; s2 < a.KS; ++s2) expected += npieces(a, s2, u);
                 const unsigned old = atom_add_acq_rel(&a.cnt[u], 1u);
-                s_flag = (static_cast<int>(old) == expected - 1) ? 1 : 0;
+                cs.flag = (static_cast<int>(old) == expected - 1) ? 1 : 0;
             }
             named_bar_sync(1, NCW * 32);
-            finish = s_flag != 0;  // thread 0 fenced after its atomic; reads below bypass L1
+            finish = cs.flag != 0;  // thread 0 acquired with its atomic; reads below bypass L1
         }
 
         if (finish) {
@@ -698,21 +723,213 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
                 // count finished tiles per 1024-token statistics tile; one counter update per
                 // (CTA, statistics tile) run, issued when the run ends
                 const int st = u / (STAT_TILE / 32);
-                if (st != s_st_cur) {
-                    head_flush(a, s_st_cur, s_st_n, tid, lane, warp, s_flag);
+                if (st != cs.st_cur) {
+                    head_flush(a, cs.st_cur, cs.st_n, tid, lane, warp, cs.flag);
                     if (tid == 0) {
-                        s_st_cur = st;
-                        s_st_n = 0;
+                        cs.st_cur = st;
+                        cs.st_n = 0;
                     }
                     named_bar_sync(1, NCW * 32);
                 }
-                if (tid == 0) s_st_n += 1;
+                if (tid == 0) cs.st_n += 1;
             }
         }
-        named_bar_sync(1, NCW * 32);  // red[] and s_flag are reused by the next piece
+        named_bar_sync(1, NCW * 32);  // red[] and the flag are reused by the next piece
         g += j1 - j0;
     }
-    if (a.head) head_flush(a, s_st_cur, s_st_n, tid, lane, warp, s_flag);
+    if (a.head) {
+        head_flush(a, cs.st_cur, cs.st_n, tid, lane, warp, cs.flag);
+        if (tid == 0) {
+            cs.st_cur = -1;
+            cs.st_n = 0;
+        }
+        named_bar_sync(1, NCW * 32);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// consumers: RMSNorm + per-32 requantisation spread over the grid.  Every CTA
+// forms the rows' inverse RMS in the canonical order (256 strided partial sums,
+// pairwise tree), then requantises its share of the (row, block) items, one
+// warp per item -- the same operations as sd_rmsnorm_quant_acts.
+// ---------------------------------------------------------------------------
+__device__ inline void norm_phase(const QmmArgs &a, const Smem &sm, CtaShared &cs) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int M = a.M;
+    const int64_t K = static_cast<int64_t>(a.KB) * 32;
+    float *part = sm.red;  // [M][256]
+    for (int m = 0; m < M; ++m) {
+        const float *xr = a.xin + m * K;
+        float s = 0.0f;
+        for (int64_t i = tid; i < K; i += 256) {
+            const float x = __ldcg(xr + i);
+            s = __fadd_rn(s, __fmul_rn(x, x));
+        }
+        part[m * 256 + tid] = s;
+    }
+    named_bar_sync(1, NCW * 32);
+    for (int stride = 128; stride >= 1; stride >>= 1) {
+        if (tid < stride)
+            for (int m = 0; m < M; ++m) part[m * 256 + tid] = __fadd_rn(part[m * 256 + tid], part[m * 256 + tid + stride]);
+        named_bar_sync(1, NCW * 32);
+    }
+    if (tid < M) {
+        const float mean = __fdiv_rn(part[tid * 256], static_cast<float>(K));
+        cs.inv[tid] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, a.eps)));
+    }
+    named_bar_sync(1, NCW * 32);
+    const int64_t items = static_cast<int64_t>(M) * a.KB;
+    const int64_t i0 = static_cast<int64_t>(blockIdx.x) * items / gridDim.x;
+    const int64_t i1 = static_cast<int64_t>(blockIdx.x + 1) * items / gridDim.x;
+    for (int64_t it = i0 + warp; it < i1; it += NCW) {
+        const int m = static_cast<int>(it / a.KB);
+        const int64_t b = it - static_cast<int64_t>(m) * a.KB;
+        const float x = __ldcg(a.xin + m * K + b * 32 + lane);
+        const float y = __fmul_rn(__fmul_rn(x, cs.inv[m]), a.norm_w[b * 32 + lane]);
+        float d;
+        const int v = requant_lane(y, d);
+        a.q_next[m * K + b * 32 + lane] = static_cast<int8_t>(v);
+        if (lane == 0) a.s_next[m * a.KB + b] = d;
+    }
+}
+
+// greedy acceptance (chain when parent == nullptr, else a tree in BFS order); one thread
+__device__ inline void greedy_accept(const int32_t *argmax, const int32_t *tokens, const int32_t *parent, int M,
+                                     int32_t *out, int32_t *count) {
+    if (!parent) {
+        const int K = M - 1;
+        int n = 0;
+        while (n < K && __ldcg(tokens + n) == __ldcg(argmax + n)) {
+            out[n] = tokens[n];
+            ++n;
+        }
+        out[n] = __ldcg(argmax + n);
+        *count = n + 1;
+        return;
+    }
+    bool ok[16];
+    int depth[16];
+    ok[0] = true;
+    depth[0] = 0;
+    int best = 0;
+    for (int i = 1; i < M; ++i) {
+        const int p = parent[i];
+        ok[i] = false;
+        depth[i] = 0;
+        if (p < 0 || p >= i) continue;
+        depth[i] = depth[p] + 1;
+        ok[i] = ok[p] && tokens[i] == __ldcg(argmax + p);
+        if (ok[i] && depth[i] > depth[best]) best = i;
+    }
+    const int d = depth[best];
+    for (int i = best, j = d - 1; i != 0; i = parent[i], --j) out[j] = tokens[i];
+    out[d] = __ldcg(argmax + best);
+    *count = d + 1;
+}
+
+// ---------------------------------------------------------------------------
+// single-operation kernel (one matmul phase per launch)
+// ---------------------------------------------------------------------------
+template <int QT, int PAIR, int NT>
+__global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    __shared__ CtaShared cs;
+    const Smem sm = smem_regions(smem, a);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) cta_init(sm, a.NS, cs);
+    __syncthreads();
+    uint32_t it = 0;
+    if (warp == NCW) {
+        pdl_launch_dependents();
+        if (lane == 0) {
+            produce_phase(a, sm, it, cs, policy_evict_first());
+            producer_drain(sm, it, a.NS);
+        }
+        return;
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+    consume_phase<QT, PAIR, NT>(a, sm, it, cs);
+}
+
+// ---------------------------------------------------------------------------
+// persistent verify pass: every phase of the pass in one cooperative launch,
+// phases separated by a grid barrier (release / acquire on a global counter,
+// bounded wait).  The producer streams weights across phase boundaries.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+template <int NT>
+__global__ void __launch_bounds__(QMM_THREADS, 1)
+    pass_kernel(const QmmArgs *__restrict__ phases, int n_phases, uint32_t *barrier_ctr) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    __shared__ CtaShared cs;
+    __shared__ QmmArgs sa;  // the current phase, copied from global memory
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const QmmArgs &a0 = phases[0];
+    const Smem sm = smem_regions(smem, a0);
+    int *status = a0.status;
+    if (tid == 0) cta_init(sm, a0.NS, cs);
+    __syncthreads();
+    uint32_t it = 0;
+    if (warp == NCW) {
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            for (int p = 0; p < n_phases && !cs.abort; ++p)
+                if (phases[p].kind == KIND_MATMUL) produce_phase(phases[p], sm, it, cs, pol);
+            producer_drain(sm, it, a0.NS);
+        }
+        return;
+    }
+    for (int p = 0; p < n_phases; ++p) {
+        if (p > 0) {  // grid barrier: every CTA finished phase p - 1
+            if (tid == 0) {
+                const uint32_t target = static_cast<uint32_t>(p) * gridDim.x;
+                uint64_t t0 = gtimer_ns();
+                while (ld_acquire(barrier_ctr) < target) {
+                    if (cs.abort || gtimer_ns() - t0 > WAIT_NS) {
+                        set_status(status, SD_ETIMEOUT);
+                        cs.abort = 1;
+                        cs.cabort = 1;
+                        break;
+                    }
+                }
+            }
+        }
+        {  // copy the phase descriptor into shared memory
+            const uint32_t *src = reinterpret_cast<const uint32_t *>(phases + p);
+            uint32_t *dst = reinterpret_cast<uint32_t *>(&sa);
+            for (int i = tid; i < static_cast<int>(sizeof(QmmArgs) / 4); i += NCW * 32) dst[i] = src[i];
+        }
+        named_bar_sync(1, NCW * 32);
+        if (cs.cabort) return;
+        if (sa.kind == KIND_NORM) {
+            norm_phase(sa, sm, cs);
+        } else if (sa.kind == KIND_ACCEPT) {
+            if (blockIdx.x == 0 && tid == 0)
+                greedy_accept(sa.argmax, sa.tokens, sa.parent, sa.M, sa.out_tokens, sa.out_count);
+        } else if (sa.qt == SD_Q4_32 && sa.pair) {
+            consume_phase<SD_Q4_32, 1, NT>(sa, sm, it, cs);
+        } else if (sa.qt == SD_Q4_32) {
+            consume_phase<SD_Q4_32, 0, NT>(sa, sm, it, cs);
+        } else {
+            consume_phase<SD_Q8_0, 0, NT>(sa, sm, it, cs);
+        }
+        named_bar_sync(1, NCW * 32);
+        if (cs.cabort) {
+            cs.abort = 1;
+            return;
+        }
+        if (tid == 0) red_release_add(barrier_ctr, 1u);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -763,31 +980,38 @@ inline bool make_plan(int qtype, int64_t n_out, int64_t k_in, bool pair, bool he
     return true;
 }
 
-// shared-memory layout for NT 8-position tiles; returns total bytes
+// steps per stage (~18 KB stages): 32 records of 4-bit, 16 gate|up pairs, 16 Q8_0 records
+inline int stage_steps(int qtype, bool pair) { return pair ? 2 * NCW : (qtype == SD_Q8_0 ? 2 * NCW : 4 * NCW); }
+
+// Shared-memory layout for splits of up to `kbs` blocks, NT 8-position tiles, `rows` output
+// rows per unit (64 with a gate|up pair) and ring slots of `slot` bytes; returns total bytes.
+inline size_t layout_smem(int kbs, int NT, int rows, size_t slot, int &NS, uint32_t &off_ring, uint32_t &off_act,
+                          uint32_t &off_meta, uint32_t &off_red) {
+    const size_t act = static_cast<size_t>(kbs) * (NT == 1 ? 512 : 2 * 256);  // fp16 or raw int8 fragments
+    const size_t meta = static_cast<size_t>(kbs) * NT * 64;                  // corr + d_a per position
+    const size_t red = static_cast<size_t>(NCW) * 8 * NT * rows * 4;
+    const size_t fixed = 256 + act + meta + red + 3 * 128;
+    const size_t budget = 222 * 1024;
+    int ns = fixed + 2 * slot <= budget ? static_cast<int>((budget - fixed) / slot) : 2;
+    if (ns > 12) ns = 12;
+    NS = ns;
+    off_ring = 256;
+    off_act = static_cast<uint32_t>(align_up(off_ring + ns * slot, 128));
+    off_meta = static_cast<uint32_t>(align_up(off_act + act, 128));
+    off_red = static_cast<uint32_t>(align_up(off_meta + meta, 128));
+    return align_up(off_red + red, 128);
+}
+
+// single-operation layout
 inline size_t plan_smem(QmmPlan &p, int NT, bool pair, uint32_t &off_ring, uint32_t &off_act, uint32_t &off_meta,
                         uint32_t &off_red, uint32_t &off_tmp) {
-    const int rows = pair ? 64 : 32;
-    p.SB = pair ? NCW : 2 * NCW;  // two records per consumer warp per stage
-    const size_t stage = static_cast<size_t>(p.SB) * p.step_bytes;
-    const size_t act = static_cast<size_t>(p.KBs) * (NT == 1 ? 512 : 2 * 256);  // fp16 or raw int8 fragments
-    const size_t meta = static_cast<size_t>(p.KBs) * NT * 64;   // corr + d_a per position
-    const size_t red = static_cast<size_t>(NCW) * 8 * NT * rows * 4;
-    const size_t tmp = 0;
-    const size_t fixed = 256 + act + meta + red + tmp;
-    size_t ring = 96 * 1024;
-    if (ring < 4 * stage) ring = 4 * stage;
-    if (fixed + ring > 222 * 1024) ring = (222 * 1024 - fixed) / stage * stage;
-    if (ring < 2 * stage) ring = 2 * stage;
-    int ns = static_cast<int>(ring / stage);
-    if (ns > 12) ns = 12;
-    if (ns < 2) ns = 2;
+    p.SB = stage_steps(p.step_bytes == 1088 ? SD_Q8_0 : SD_Q4_32, pair);
+    int ns = 0;
+    const size_t total = layout_smem(p.KBs, NT, pair ? 64 : 32, static_cast<size_t>(p.SB) * p.step_bytes, ns, off_ring,
+                                     off_act, off_meta, off_red);
     p.NS = ns;
-    off_ring = 256;
-    off_act = static_cast<uint32_t>(align_up(off_ring + ns * stage, 128));
-    off_meta = static_cast<uint32_t>(align_up(off_act + act, 16));
-    off_red = static_cast<uint32_t>(align_up(off_meta + meta, 16));
-    off_tmp = static_cast<uint32_t>(align_up(off_red + red, 16));
-    return align_up(off_tmp + tmp, 128);
+    off_tmp = 0;
+    return total;
 }
 
 template <int QT, int PAIR, int NT>

@@ -17,6 +17,8 @@ cudaError_t qmm_dispatch<SD_Q4_32, 1>(QmmArgs a, QmmPlan &p, cudaStream_t s) {
     a.off_meta = o_meta;
     a.off_red = o_red;
     a.off_tmp = o_tmp;
+    a.stage_stride = static_cast<uint32_t>(p.SB) * p.step_bytes;
+    a.kind = KIND_MATMUL;
     return NT == 1 ? qmm_launch<SD_Q4_32, 1, 1>(a, smem, s) : qmm_launch<SD_Q4_32, 1, 2>(a, smem, s);
 }
 

@@ -13,8 +13,11 @@ from __future__ import annotations
 
 import torch
 
-from . import (EPI_NONE, EPI_REQUANT, EPI_SILU_MUL_REQUANT, Q4_32, Q8_0, accept_greedy, head_logits,
-               head_workspace_bytes, qmatmul_multipos, qmatmul_workspace_bytes, repack_weights, rmsnorm_quant_acts,
+import ctypes
+
+from . import (EPI_NONE, EPI_REQUANT, EPI_SILU_MUL_REQUANT, Q4_32, Q8_0, SdLayer, SdPassDesc, accept_greedy,
+               head_logits, head_workspace_bytes, pass_plan_bytes, pass_prepare, pass_workspace_bytes,
+               qmatmul_multipos, qmatmul_workspace_bytes, repack_weights, rmsnorm_quant_acts, verify_pass,
                workspace)
 
 
@@ -52,9 +55,10 @@ class VerifyStack:
                  qmatmul_workspace_bytes(wq, H, H, EPI_NONE),
                  qmatmul_workspace_bytes(wq, 2 * F, H, EPI_SILU_MUL_REQUANT),
                  qmatmul_workspace_bytes(wq, H, F, EPI_NONE),
-                 head_workspace_bytes(V, H))
+                 head_workspace_bytes(V, H), pass_workspace_bytes(H, F, V, wq))
         self.ws = workspace(ws, device)
         self.graph = None
+        self.fused = None
 
     # -- the pass -------------------------------------------------------------
     def layer(self, l: int):
@@ -84,6 +88,33 @@ class VerifyStack:
             self.layer(l)
         self.head()
         self.accept()
+
+    # -- the same pass as one persistent cooperative launch -----------------------
+    def prepare_fused(self, temperature: float = 1.0):
+        """Build the phase table of the one-launch pass over this stack's buffers."""
+        L = len(self.layers)
+        arr = (SdLayer * max(L, 1))()
+        for l in range(L):
+            w = self.layers[l]
+            n1, n2 = self.norms[l]
+            arr[l] = SdLayer(w["qkv"].data_ptr(), w["o"].data_ptr(), w["gate_up"].data_ptr(), w["down"].data_ptr(),
+                             n1.data_ptr(), n2.data_ptr())
+        self._layer_arr = arr
+        p = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+        d = SdPassDesc(L, self.H, self.F, self.V, self.M, self.wq, self.eps, temperature,
+                       ctypes.cast(arr, ctypes.POINTER(SdLayer)), p(self.final_norm), p(self.head_w), p(self.h),
+                       p(self.qa), p(self.sa), p(self.qv), p(self.sv), p(self.qf), p(self.sf), p(self.logits),
+                       p(self.argmax), p(self.row_max), p(self.row_sumexp), p(self.tokens), p(self.parent),
+                       p(self.out_tokens), p(self.out_count), p(self.ws), self.ws.numel())
+        self._plan = torch.zeros(pass_plan_bytes(L), dtype=torch.uint8, device=self.h.device)
+        self.fused = pass_prepare(d, self._plan)
+        return self.fused
+
+    def run_fused(self):
+        """One verify pass (layers, head, greedy acceptance) as a single cooperative launch."""
+        if self.fused is None:
+            self.prepare_fused()
+        verify_pass(self.fused)
 
     def capture(self):
         """Record run() as one CUDA graph (replayed by replay())."""
