@@ -6,10 +6,10 @@
 
 namespace sdv {
 
-// One status word per device: a module-scope device variable, so every GPU
-// that loads the library holds its own copy.  Host code reaches it through
-// cudaGetSymbolAddress, looked up once per device.
-static __device__ int g_status_word;
+// One status word per device (plus the location code of a timeout): a module-scope
+// device variable, so every GPU that loads the library holds its own copy.  Host
+// code reaches it through cudaGetSymbolAddress, looked up once per device.
+static __device__ int g_status_word[2];
 
 static std::mutex g_mu;
 static int *g_status_addr[64];
@@ -152,8 +152,8 @@ sd_status sd_device_status(sd_stream_t stream) {
     int v = 0;
     if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return SD_ECUDA;
     if (v != 0) {
-        int z = 0;
-        if (cudaMemcpy(p, &z, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return SD_ECUDA;
+        int z[2] = {0, 0};
+        if (cudaMemcpy(p, z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return SD_ECUDA;
     }
     return static_cast<sd_status>(v);
 }

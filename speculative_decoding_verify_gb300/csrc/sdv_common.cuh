@@ -129,8 +129,26 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// Named barrier over `nthreads` threads.  The non-.aligned form: callers may reach it from
+// code where a warp's lanes are not converged (after per-lane spin loops or lane-0 branches).
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+    __syncwarp();
+    asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier that also ORs a predicate over the participating threads: every thread gets
+// the same answer at the same point, so decisions taken on it stay uniform without a shared
+// flag that one thread might rewrite before a slower one has read it.
+__device__ __forceinline__ bool bar_any(int id, int nthreads, bool v) {
+    __syncwarp();
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbarrier.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
 }
 
 __device__ __forceinline__ void set_status(int *status, int code) {

@@ -36,7 +36,8 @@ constexpr int NCW = SDV_NCW;           // consumer warps
 constexpr int QMM_THREADS = (NCW + 1) * 32;
 constexpr int KB_SPLIT_MAX = 160;      // blocks per k-split
 constexpr int MPAD = 16;               // position stride of workspace partials
-constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s bound on any in-kernel wait
+constexpr uint64_t WAIT_NS = 2000000000ull;   // 2 s bound on any in-kernel wait
+constexpr uint64_t KERNEL_NS = 10000000000ull;  // 10 s bound on any launch's loops (self-check)
 constexpr int STAT_TILE = 1024;        // vocabulary tile of the softmax statistics
 constexpr int WS_UNIT_CNT = 32768;     // workspace counters: units (tiles / tile pairs) per call
 constexpr int WS_STAT_CNT = 2048;      // workspace counters: 1024-token statistics tiles
@@ -365,44 +366,50 @@ __device__ inline void head_final_fold(const QmmArgs &a, int lane, int warp) {
 
 // Adds `n_done` finished 32-row tiles to statistics tile `st`; the CTA that completes the tile
 // computes its statistics, and the CTA that completes the last tile folds them.  Called by all
-// consumer threads (bar.sync inside); the finished logits were written before the call.
-__device__ __forceinline__ void head_flush(const QmmArgs &a, int st, int n_done, int tid, int lane, int warp,
-                                           int &s_flag) {
+// consumer threads with the same arguments (barriers inside); the finished logits were written
+// before the call.
+__device__ __forceinline__ void head_flush(const QmmArgs &a, int st, int n_done, int tid, int lane, int warp) {
     if (st < 0 || n_done == 0) return;
-    named_bar_sync(1, NCW * 32);
+    named_bar_sync(1, NCW * 32);  // every thread's logits before thread 0's release
+    bool last = false;
     if (tid == 0) {
         const int tiles_in_st = (a.NU - st * (STAT_TILE / 32)) < (STAT_TILE / 32) ? (a.NU - st * (STAT_TILE / 32))
                                                                                    : (STAT_TILE / 32);
         const unsigned old = atom_add_acq_rel(&a.st_cnt[st], static_cast<uint32_t>(n_done));
-        s_flag = (static_cast<int>(old) + n_done == tiles_in_st) ? 1 : 0;
+        last = static_cast<int>(old) + n_done == tiles_in_st;
     }
-    named_bar_sync(1, NCW * 32);
-    if (!s_flag) return;
+    if (!bar_any(1, NCW * 32, last)) return;
     head_tile_stats(a, st, lane, warp);
-    named_bar_sync(1, NCW * 32);
+    named_bar_sync(1, NCW * 32);  // the tile's statistics before thread 0's release
+    bool fold = false;
     if (tid == 0) {
         a.st_cnt[st] = 0u;
         const unsigned old = atom_add_acq_rel(a.st_done, 1u);
-        s_flag = (static_cast<int>(old) == a.n_stiles - 1) ? 1 : 0;
+        fold = static_cast<int>(old) == a.n_stiles - 1;
     }
-    named_bar_sync(1, NCW * 32);
-    if (s_flag) {
-        head_final_fold(a, lane, warp);
-        if (tid == 0) *a.st_done = 0u;
-    }
-    named_bar_sync(1, NCW * 32);
+    if (!bar_any(1, NCW * 32, fold)) return;
+    head_final_fold(a, lane, warp);
+    if (tid == 0) *a.st_done = 0u;
 }
 
 // ---------------------------------------------------------------------------
 // per-CTA state and shared-memory regions
 // ---------------------------------------------------------------------------
+// Decisions the consumer threads must take together (abort, "last to arrive", "statistics tile
+// complete") travel through bar_any, never through a shared flag.
 struct CtaShared {
-    int flag;
-    int st_cur, st_n;      // head: current statistics tile and tiles finished in it
-    volatile int abort;    // set by anyone whose bounded wait ran out
-    volatile int cabort;   // set by consumers only, read after a consumer barrier
+    volatile int abort;    // set by anyone whose bounded wait ran out; polled by waits
     float inv[16];         // RMSNorm phase: 1 / rms of each row
+    uint64_t t0;           // launch start (globaltimer), for the launch-wide time bound
 };
+
+// Launch-wide self-check: past KERNEL_NS since the CTA started, record SD_ETIMEOUT and where
+// (status[1]: 1 producer, 2 consumer piece loop) and make the caller unwind.
+__device__ __forceinline__ bool out_of_time(const CtaShared &cs, int *status, int where) {
+    if (gtimer_ns() - cs.t0 <= KERNEL_NS) return false;
+    if (status && atomicCAS(status, 0, SD_ETIMEOUT) == 0) status[1] = where;
+    return true;
+}
 
 struct Smem {
     uint64_t *full, *empty;
@@ -431,9 +438,7 @@ __device__ __forceinline__ void cta_init(const Smem &sm, int NS, CtaShared &cs) 
         mbar_init(&sm.empty[i], NCW);
     }
     cs.abort = 0;
-    cs.cabort = 0;
-    cs.st_cur = -1;
-    cs.st_n = 0;
+    cs.t0 = gtimer_ns();
     fence_barrier_init();
 }
 
@@ -453,6 +458,10 @@ __device__ inline void produce_phase(const QmmArgs &a, const Smem &sm, uint32_t 
             const int n = j1 - jj < a.SB ? j1 - jj : a.SB;
             const int stg = static_cast<int>(it % a.NS);
             const uint32_t ph = (it / a.NS) & 1u;
+            if (out_of_time(cs, a.status, 1)) {
+                cs.abort = 1;
+                break;
+            }
             if (!mbar_wait_bounded(&sm.empty[stg], ph ^ 1u, WAIT_NS, &cs.abort)) {
                 set_status(a.status, SD_ETIMEOUT);
                 cs.abort = 1;
@@ -476,10 +485,12 @@ __device__ inline void producer_drain(const Smem &sm, uint32_t it, int NS) {
 }
 
 // ---------------------------------------------------------------------------
-// consumers: one matmul phase (staging, stages, piece fixups, epilogues)
+// consumers: one matmul phase (staging, stages, piece fixups, epilogues).
+// Returns false (the same on every consumer thread) when the phase was abandoned
+// after a bounded wait or the launch-wide time bound ran out.
 // ---------------------------------------------------------------------------
 template <int QT, int PAIR, int NT>
-__device__ inline void consume_phase(const QmmArgs &a, const Smem &sm, uint32_t &it, CtaShared &cs) {
+__device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t &it, CtaShared &cs) {
     constexpr int REC = QT == SD_Q8_0 ? 1088 : 576;  // bytes of one 32-row record
     constexpr int CODE = QT == SD_Q8_0 ? 1024 : 512; // code bytes of a record
     constexpr int ROWS = PAIR ? 64 : 32;
@@ -495,8 +506,15 @@ __device__ inline void consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
     const int64_t lo = static_cast<int64_t>(blockIdx.x) * a.W / a.G;
     const int64_t hi = static_cast<int64_t>(blockIdx.x + 1) * a.W / a.G;
     int cur_s = -1;
+    int st_cur = -1, st_n = 0;  // head: current statistics tile, tiles finished in it (same on all threads)
     int64_t g = lo;
     while (g < hi) {
+        // launch-wide self-check: thread 0 decides, the barrier hands the answer to all.  The
+        // barrier also ends every use of the previous piece's shared data (stages, red[], B).
+        if (bar_any(1, NCW * 32, tid == 0 && out_of_time(cs, a.status, 2))) {
+            cs.abort = 1;
+            return false;
+        }
         int s, u, j0, len;
         decode_step(a, g, s, u, j0, len);
         const int j1 = static_cast<int>(j0 + (hi - g) < len ? j0 + (hi - g) : len);
@@ -504,7 +522,6 @@ __device__ inline void consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
         if (s != cur_s) {
             // stage this split's activations straight from global memory: B operands (fp16 fragments,
             // or raw int8 for two position tiles) and per-(block, position) {corr, d_a}
-            named_bar_sync(1, NCW * 32);
             const int64_t K = static_cast<int64_t>(a.KB) * 32;
             const int b0 = s * a.KBs;
             const int nitems = len * NT * 32;
@@ -557,7 +574,9 @@ __device__ inline void consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
             const int n = j1 - jj < a.SB ? j1 - jj : a.SB;
             const int stg = static_cast<int>(it % a.NS);
             const uint32_t ph = (it / a.NS) & 1u;
-            if (!mbar_wait_bounded(&sm.full[stg], ph, WAIT_NS, &cs.abort)) {
+            const bool ready = mbar_wait_bounded(&sm.full[stg], ph, WAIT_NS, &cs.abort);
+            __syncwarp();  // lanes leave the wait one by one; mma.sync below needs the warp converged
+            if (!__all_sync(0xffffffffu, ready)) {
                 set_status(a.status, SD_ETIMEOUT);
                 cs.abort = 1;
                 aborted = true;
@@ -643,7 +662,6 @@ __device__ inline void consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
         }
 
         // ---- finish the piece: add the 8 warps' partials in warp order ----
-        if (aborted) cs.cabort = 1;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -654,8 +672,10 @@ __device__ inline void consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
                     red[(warp * MT + m) * ROWS + row] = acc[nt][t][i];
                     if (PAIR) red[(warp * MT + m) * ROWS + 32 + row] = accu[PAIR ? nt : 0][t][i];
                 }
-        named_bar_sync(1, NCW * 32);
-        if (cs.cabort) return;  // uniform: written only before the barrier above
+        if (bar_any(1, NCW * 32, aborted)) {
+            cs.abort = 1;
+            return false;
+        }
 
         const bool direct = (a.KS == 1) && (npieces(a, s, u) == 1);
         bool finish = direct;
@@ -674,14 +694,14 @@ __device__ inline void consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
                 if (PAIR) pp[m * ROWS + 32 + lane] = vu;
             }
             named_bar_sync(1, NCW * 32);  // the partial sums above happen before thread 0's release
+            bool last = false;
             if (tid == 0) {
                 int expected = 0;
                 for (int s2 = 0; s2 < a.KS; ++s2) expected += npieces(a, s2, u);
                 const unsigned old = atom_add_acq_rel(&a.cnt[u], 1u);
-                cs.flag = (static_cast<int>(old) == expected - 1) ? 1 : 0;
+                last = static_cast<int>(old) == expected - 1;
             }
-            named_bar_sync(1, NCW * 32);
-            finish = cs.flag != 0;  // thread 0 acquired with its atomic; reads below bypass L1
+            finish = bar_any(1, NCW * 32, last);  // thread 0 acquired with its atomic; reads below bypass L1
         }
 
         if (finish) {
@@ -723,28 +743,18 @@ __device__ inline void consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
                 // count finished tiles per 1024-token statistics tile; one counter update per
                 // (CTA, statistics tile) run, issued when the run ends
                 const int st = u / (STAT_TILE / 32);
-                if (st != cs.st_cur) {
-                    head_flush(a, cs.st_cur, cs.st_n, tid, lane, warp, cs.flag);
-                    if (tid == 0) {
-                        cs.st_cur = st;
-                        cs.st_n = 0;
-                    }
-                    named_bar_sync(1, NCW * 32);
+                if (st != st_cur) {
+                    head_flush(a, st_cur, st_n, tid, lane, warp);
+                    st_cur = st;
+                    st_n = 0;
                 }
-                if (tid == 0) cs.st_n += 1;
+                ++st_n;
             }
         }
-        named_bar_sync(1, NCW * 32);  // red[] and the flag are reused by the next piece
         g += j1 - j0;
     }
-    if (a.head) {
-        head_flush(a, cs.st_cur, cs.st_n, tid, lane, warp, cs.flag);
-        if (tid == 0) {
-            cs.st_cur = -1;
-            cs.st_n = 0;
-        }
-        named_bar_sync(1, NCW * 32);
-    }
+    if (a.head) head_flush(a, st_cur, st_n, tid, lane, warp);
+    return true;
 }
 
 // ---------------------------------------------------------------------------
@@ -849,7 +859,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
     }
     pdl_wait();
     pdl_launch_dependents();
-    consume_phase<QT, PAIR, NT>(a, sm, it, cs);
+    (void)consume_phase<QT, PAIR, NT>(a, sm, it, cs);
 }
 
 // ---------------------------------------------------------------------------
@@ -890,44 +900,42 @@ __global__ void __launch_bounds__(QMM_THREADS, 1)
         return;
     }
     for (int p = 0; p < n_phases; ++p) {
-        if (p > 0) {  // grid barrier: every CTA finished phase p - 1
-            if (tid == 0) {
-                const uint32_t target = static_cast<uint32_t>(p) * gridDim.x;
-                uint64_t t0 = gtimer_ns();
-                while (ld_acquire(barrier_ctr) < target) {
-                    if (cs.abort || gtimer_ns() - t0 > WAIT_NS) {
-                        set_status(status, SD_ETIMEOUT);
-                        cs.abort = 1;
-                        cs.cabort = 1;
-                        break;
-                    }
+        bool stop = false;
+        if (p > 0 && tid == 0) {  // grid barrier: every CTA finished phase p - 1
+            const uint32_t target = static_cast<uint32_t>(p) * gridDim.x;
+            const uint64_t t0 = gtimer_ns();
+            while (ld_acquire(barrier_ctr) < target) {
+                if (cs.abort || gtimer_ns() - t0 > WAIT_NS) {
+                    set_status(status, SD_ETIMEOUT);
+                    stop = true;
+                    break;
                 }
             }
         }
-        {  // copy the phase descriptor into shared memory
+        {  // copy the phase descriptor into shared memory (constant: may overlap the barrier wait)
             const uint32_t *src = reinterpret_cast<const uint32_t *>(phases + p);
             uint32_t *dst = reinterpret_cast<uint32_t *>(&sa);
             for (int i = tid; i < static_cast<int>(sizeof(QmmArgs) / 4); i += NCW * 32) dst[i] = src[i];
         }
-        named_bar_sync(1, NCW * 32);
-        if (cs.cabort) return;
+        if (bar_any(1, NCW * 32, stop)) {
+            cs.abort = 1;
+            return;
+        }
+        bool ok = true;
         if (sa.kind == KIND_NORM) {
             norm_phase(sa, sm, cs);
         } else if (sa.kind == KIND_ACCEPT) {
             if (blockIdx.x == 0 && tid == 0)
                 greedy_accept(sa.argmax, sa.tokens, sa.parent, sa.M, sa.out_tokens, sa.out_count);
         } else if (sa.qt == SD_Q4_32 && sa.pair) {
-            consume_phase<SD_Q4_32, 1, NT>(sa, sm, it, cs);
+            ok = consume_phase<SD_Q4_32, 1, NT>(sa, sm, it, cs);
         } else if (sa.qt == SD_Q4_32) {
-            consume_phase<SD_Q4_32, 0, NT>(sa, sm, it, cs);
+            ok = consume_phase<SD_Q4_32, 0, NT>(sa, sm, it, cs);
         } else {
-            consume_phase<SD_Q8_0, 0, NT>(sa, sm, it, cs);
+            ok = consume_phase<SD_Q8_0, 0, NT>(sa, sm, it, cs);
         }
-        named_bar_sync(1, NCW * 32);
-        if (cs.cabort) {
-            cs.abort = 1;
-            return;
-        }
+        if (!ok) return;  // uniform; cs.abort already stops the producer
+        named_bar_sync(1, NCW * 32);  // this CTA's writes of phase p before thread 0's release
         if (tid == 0) red_release_add(barrier_ctr, 1u);
     }
 }

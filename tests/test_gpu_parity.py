@@ -304,6 +304,29 @@ def test_head_batch_invariance(sdv):
         assert a1[0] == am[m] and r1[0] == rm[m] and z1[0] == rz[m]
 
 
+def test_head_repeated_calls_identical(sdv):
+    """Many back-to-back head calls at 16 positions (every consumer warp busy in the epilogue, so
+    the CTA's warps reach the statistics bookkeeping in varying order) return identical results."""
+    V, H, M = 4096, 512, 16
+    blocks = sdgen.quantized_normal(oracle.Q8_0, sdgen.key(125), V, H)
+    q, s = acts(sdgen.key(126), M, H)
+    w = sdv.repack_weights(oracle.Q8_0, cuda(blocks).reshape(-1), V, H)
+    ws = sdv.workspace(sdv.head_workspace_bytes(V, H))
+    qd, sd = cuda(q), cuda(s)
+    outs = []
+    for _ in range(40):
+        lg = torch.zeros((M, V), dtype=torch.float32, device="cuda")
+        am = torch.zeros(M, dtype=torch.int32, device="cuda")
+        rm = torch.zeros(M, dtype=torch.float32, device="cuda")
+        rz = torch.zeros(M, dtype=torch.float32, device="cuda")
+        sdv.head_logits(w, V, H, qd, sd, ws, lg, am, rm, rz, 1.0)
+        outs.append((lg, am, rm, rz))
+    status_ok()
+    for o in outs[1:]:
+        for x, y in zip(o, outs[0]):
+            assert torch.equal(x, y)
+
+
 # ---------------------------------------------------------------------------
 # acceptance: bit-exact when fed the oracle's logits
 # ---------------------------------------------------------------------------
