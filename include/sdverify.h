@@ -143,6 +143,36 @@ sd_status sd_qmatmul_multipos(int qtype, const void *w, int64_t n_out, int64_t k
                               size_t ws_bytes, sd_stream_t stream);
 
 /*
+ * The multi-position matmul without a caller-supplied workspace.  The papers
+ * have no counterpart: this is a convenience of this library, not a step of
+ * the method.
+ *
+ * For callers that cannot hand the library device memory: code that runs
+ * after a fixed start-up budget has been allocated and may not allocate
+ * again, or a host whose allocator the library must not touch.  Arguments and
+ * results are those of sd_qmatmul_multipos without `workspace`/`ws_bytes`;
+ * the stream-K counters and partial sums live instead in one static device
+ * array of SD_NOALLOC_SCRATCH_BYTES per device, inside this library.
+ *
+ * Allocates nothing: no cudaMalloc/cudaFree, no allocating library routine.
+ * The first call on each device looks up that device's scratch address (with
+ * the device current) and caches it; make that first call before any stream
+ * capture.  Every call clears the scratch's counter region on `stream` before
+ * its launch, so no state carries over between calls, including after
+ * SD_ETIMEOUT.  Calls whose workspace (sd_qmatmul_workspace_bytes) exceeds
+ * SD_NOALLOC_SCRATCH_BYTES are rejected with SD_EUNSUPPORTED before anything
+ * is launched (the 27B-shaped layer projections fit; a full-vocabulary head
+ * does not).  All calls share the one scratch array: calls that may overlap
+ * on the device (different streams, or several host threads) race on it and
+ * must be ordered by the caller.
+ */
+#define SD_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+sd_status sd_qmatmul_multipos_noalloc(int qtype, const void *w, int64_t n_out, int64_t k_in, const int8_t *q,
+                                      const float *scales, int32_t M, float *y, const float *residual,
+                                      uint32_t epilogue, int64_t requant_col0, int8_t *q_next, float *scales_next,
+                                      sd_stream_t stream);
+
+/*
  * Full-vocabulary output head with fused per-row argmax and softmax
  * statistics ("Inside OpenJet Engine", section "One GPU launch for a
  * speculative cycle": full-vocabulary output head + verification inside the

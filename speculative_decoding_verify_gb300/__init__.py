@@ -75,6 +75,7 @@ def lib():
             "sd_rmsnorm_quant_acts": ([P, I64, P, F, I32, I64, P, P, P], I),
             "sd_qmatmul_workspace_bytes": ([I, I64, I64, U32], SZ),
             "sd_qmatmul_multipos": ([I, P, I64, I64, P, P, I32, P, P, U32, I64, P, P, P, SZ, P], I),
+            "sd_qmatmul_multipos_noalloc": ([I, P, I64, I64, P, P, I32, P, P, U32, I64, P, P, P], I),
             "sd_head_workspace_bytes": ([I64, I64], SZ),
             "sd_head_logits": ([P, I64, I64, P, P, I32, F, P, P, P, P, P, SZ, P], I),
             "sd_accept_greedy": ([P, P, P, I32, P, P, P], I),
@@ -171,6 +172,17 @@ def qmatmul_multipos(qtype: int, w: torch.Tensor, n_out: int, k_in: int, q: torc
     _check(lib().sd_qmatmul_multipos(qtype, _p(w), n_out, k_in, _p(q), _p(scales), M, _p(y), _p(residual), epilogue,
                                      requant_col0, _p(q_next), _p(scales_next), _p(ws), ws.numel(), _stream()),
            "sd_qmatmul_multipos")
+
+
+def qmatmul_multipos_noalloc(qtype: int, w: torch.Tensor, n_out: int, k_in: int, q: torch.Tensor,
+                             scales: torch.Tensor, y: torch.Tensor | None = None, residual: torch.Tensor | None = None,
+                             epilogue: int = EPI_NONE, requant_col0: int = 0, q_next: torch.Tensor | None = None,
+                             scales_next: torch.Tensor | None = None):
+    """sd_qmatmul_multipos with the library's static scratch instead of a workspace (allocates nothing)."""
+    M = q.shape[0]
+    _check(lib().sd_qmatmul_multipos_noalloc(qtype, _p(w), n_out, k_in, _p(q), _p(scales), M, _p(y), _p(residual),
+                                             epilogue, requant_col0, _p(q_next), _p(scales_next), _stream()),
+           "sd_qmatmul_multipos_noalloc")
 
 
 def head_logits(w: torch.Tensor, vocab: int, hidden: int, q: torch.Tensor, scales: torch.Tensor, ws: torch.Tensor,
