@@ -101,10 +101,15 @@ sd_status sd_repack_weights(int qtype, const void *src_blocks, int64_t n_out, in
  *
  * x: fp32 [M][ldx] (row stride ldx >= K elements).  norm_w: fp32 [K], or NULL
  * for requantisation only.  Out: q int8 [M][K], scales fp32 [M][K/32].
- * Arithmetic (bit-exact contract): s = sum x^2 as 256 strided partials
- * (partial j over i = j mod 256, increasing i) folded by a pairwise tree at
- * strides 128..1; inv = 1/sqrt(s/K + eps) correctly rounded; y = (x*inv)*w;
- * per block d = amax/127, q = round-half-away(y/d) clamped to +-127 (0 if d=0).
+ * Arithmetic (bit-exact contract): s = sum x^2 as, per 32-element block, a
+ * pairwise tree over the block's rounded squares (strides 16, 8, 4, 2, 1),
+ * then a pairwise tree over the K/32 block sums zero-padded to a power of two
+ * of at least 256 slots; inv = 1/sqrt(s/K + eps) correctly rounded.  Codes of
+ * the normalised row y = x*inv*w are formed from t = x*w: per block c =
+ * amax|t|/127, q = round-half-away(t/c) clamped to +-127 (0 if c=0), scale
+ * d = inv*c (in exact arithmetic the requantisation of y, whose row factor
+ * cancels in the codes).  Without norm_w: c and q from x, d = c.  With norm_w,
+ * K/32 <= 2048 (else SD_EUNSUPPORTED).
  */
 sd_status sd_rmsnorm_quant_acts(const float *x, int64_t ldx, const float *norm_w, float eps, int32_t M,
                                 int64_t K, int8_t *q, float *scales, sd_stream_t stream);

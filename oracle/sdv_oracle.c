@@ -158,34 +158,47 @@ static void requant_row(const float *y, int64_t K, int8_t *q, float *scales) {
 
 /*
  * RMSNorm + requantisation of M rows (norm_w == NULL: requantisation only).
- * Sum of squares in the canonical order: 256 partial sums, partial j adding
- * x_i*x_i for i = j, j+256, j+512, ... in increasing i; then a pairwise tree
- * over the partials at strides 128, 64, ..., 1.  mean = s / K,
- * inv = 1 / sqrt(mean + eps) (correctly rounded division and square root),
- * y = (x * inv) * w (two rounded multiplies), then requantise.
+ * Sum of squares in the canonical order: for each 32-element block, a pairwise
+ * tree over its rounded squares x_i*x_i at strides 16, 8, 4, 2, 1 (t[j] +=
+ * t[j+s] for j < s); then the same pairwise tree over the K/32 block sums,
+ * zero-padded to a power of two of at least 256 slots.  mean = s / K,
+ * inv = 1 / sqrt(mean + eps) (correctly rounded division and square root).
+ * The normalised row is y = x * inv * w.  Its codes are formed from t = x * w
+ * (one rounded multiply): per block c = max|t| / 127 and q = round(t / c), the
+ * requantisation above applied to t; the block scale is d = inv * c (one
+ * rounded multiply).  In exact arithmetic this is the requantisation of y
+ * itself, since the positive row factor inv cancels in y / (max|y| / 127).
  */
 void oracle_rmsnorm_quant(const float *x, const float *norm_w, float eps, int M, int64_t K, int8_t *q, float *scales) {
-    float *y = (float *)malloc((size_t)K * sizeof(float));
+    float *t = (float *)malloc((size_t)K * sizeof(float));
     for (int m = 0; m < M; ++m) {
         const float *xr = x + (int64_t)m * K;
-        if (norm_w) {
-            float part[256];
-            for (int j = 0; j < 256; ++j) {
-                float s = 0.0f;
-                for (int64_t i = j; i < K; i += 256) s = s + xr[i] * xr[i];
-                part[j] = s;
-            }
-            for (int stride = 128; stride >= 1; stride >>= 1)
-                for (int j = 0; j < stride; ++j) part[j] = part[j] + part[j + stride];
-            float mean = part[0] / (float)K;
-            float inv = 1.0f / sqrtf(mean + eps);
-            for (int64_t i = 0; i < K; ++i) y[i] = (xr[i] * inv) * norm_w[i];
-        } else {
-            memcpy(y, xr, (size_t)K * sizeof(float));
+        float *sr = scales + (int64_t)m * (K / 32);
+        if (!norm_w) {
+            requant_row(xr, K, q + (int64_t)m * K, sr);
+            continue;
         }
-        requant_row(y, K, q + (int64_t)m * K, scales + (int64_t)m * (K / 32));
+        const int64_t KB = K / 32;
+        int64_t P = 256;
+        while (P < KB) P <<= 1;
+        float *part = (float *)calloc((size_t)P, sizeof(float));
+        for (int64_t b = 0; b < KB; ++b) {
+            float sq[32];
+            for (int i = 0; i < 32; ++i) sq[i] = xr[b * 32 + i] * xr[b * 32 + i];
+            for (int stride = 16; stride >= 1; stride >>= 1)
+                for (int j = 0; j < stride; ++j) sq[j] = sq[j] + sq[j + stride];
+            part[b] = sq[0];
+        }
+        for (int64_t stride = P / 2; stride >= 1; stride >>= 1)
+            for (int64_t j = 0; j < stride; ++j) part[j] = part[j] + part[j + stride];
+        float mean = part[0] / (float)K;
+        free(part);
+        float inv = 1.0f / sqrtf(mean + eps);
+        for (int64_t i = 0; i < K; ++i) t[i] = xr[i] * norm_w[i];
+        requant_row(t, K, q + (int64_t)m * K, sr);
+        for (int64_t b = 0; b < KB; ++b) sr[b] = inv * sr[b];
     }
-    free(y);
+    free(t);
 }
 
 /* ------------------------------------------------------------------ */

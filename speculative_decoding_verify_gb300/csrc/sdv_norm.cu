@@ -1,48 +1,64 @@
 // sdv_norm.cu - RMSNorm fused with per-32 int8 requantisation, and the small
 // test hooks (canonical exp, SiLU*mul requant, Philox, bounded-wait timeout).
-#include "sdv_common.cuh"
+#include "sdv_qmatmul.cuh"
 
 namespace sdv {
 
-// One CTA of 256 threads per row.  Sum of squares: thread j sums x_i^2 over
-// i = j mod 256 in increasing i, then a shared-memory pairwise tree at strides
-// 128..1; inv = 1/sqrt(s/K + eps) correctly rounded; y = (x*inv)*w; each warp
-// requantises 32-element blocks.
+// One CTA of 256 threads per row.  Sum of squares: per 32-element block a
+// pairwise tree over the block's squares (strides 16..1), then a pairwise tree
+// over the block sums zero-padded to a power of two (at least 256 slots);
+// inv = 1/sqrt(s/K + eps) correctly rounded.  Each warp requantises 32-element
+// blocks of t = x*w and scales them by inv: the requantisation of y = x*inv*w.  The matmul epilogues form the same block sums
+// where they finish a block of the residual stream, so the verify pass reaches
+// identical bits.
 __global__ void __launch_bounds__(256) rmsnorm_quant_kernel(const float *__restrict__ x, int64_t ldx,
                                                             const float *__restrict__ w, float eps, int64_t K,
                                                             int8_t *__restrict__ q, float *__restrict__ sc) {
-    __shared__ float part[256];
+    __shared__ float slots[NORM_MAX_KB];
     __shared__ float s_inv;
     pdl_wait();
     pdl_launch_dependents();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int m = blockIdx.x;
     const float *xr = x + static_cast<int64_t>(m) * ldx;
+    const int KB = static_cast<int>(K / 32);
     float inv = 1.0f;
     if (w) {
-        float s = 0.0f;
-        for (int64_t i = tid; i < K; i += 256) s = __fadd_rn(s, __fmul_rn(xr[i], xr[i]));
-        part[tid] = s;
+        int P = 256;
+        while (P < KB) P <<= 1;
+        for (int b = warp; b < P; b += 8) {
+            float t = 0.0f;
+            if (b < KB) {
+                const float v = xr[static_cast<int64_t>(b) * 32 + lane];
+                t = __fmul_rn(v, v);
+#pragma unroll
+                for (int s = 16; s >= 1; s >>= 1) {
+                    const float o = __shfl_down_sync(0xffffffffu, t, s);
+                    if (lane < s) t = __fadd_rn(t, o);
+                }
+            }
+            if (lane == 0) slots[b] = t;
+        }
         __syncthreads();
-        for (int stride = 128; stride >= 1; stride >>= 1) {
-            if (tid < stride) part[tid] = __fadd_rn(part[tid], part[tid + stride]);
+        for (int st = P / 2; st >= 1; st >>= 1) {
+            for (int j = tid; j < st; j += 256) slots[j] = __fadd_rn(slots[j], slots[j + st]);
             __syncthreads();
         }
         if (tid == 0) {
-            float mean = __fdiv_rn(part[0], static_cast<float>(K));
+            const float mean = __fdiv_rn(slots[0], static_cast<float>(K));
             s_inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
         }
         __syncthreads();
         inv = s_inv;
     }
-    const int64_t KB = K / 32;
+    // codes from t = x * w (the row factor inv cancels in t / (max|t| / 127)); scale inv * max|t| / 127
     for (int64_t b = warp; b < KB; b += 8) {
-        float y = xr[b * 32 + lane];
-        if (w) y = __fmul_rn(__fmul_rn(y, inv), w[b * 32 + lane]);
-        float d;
-        int v = requant_lane(y, d);
+        float t = xr[b * 32 + lane];
+        if (w) t = __fmul_rn(t, w[b * 32 + lane]);
+        float c;
+        const int v = requant_lane(t, c);
         q[static_cast<int64_t>(m) * K + b * 32 + lane] = static_cast<int8_t>(v);
-        if (lane == 0) sc[static_cast<int64_t>(m) * KB + b] = d;
+        if (lane == 0) sc[static_cast<int64_t>(m) * KB + b] = w ? __fmul_rn(inv, c) : c;
     }
 }
 
@@ -95,6 +111,7 @@ extern "C" {
 sd_status sd_rmsnorm_quant_acts(const float *x, int64_t ldx, const float *norm_w, float eps, int32_t M, int64_t K,
                                 int8_t *q, float *scales, sd_stream_t stream) {
     if (!x || !q || !scales || M < 1 || M > 65535 || K <= 0 || K % 32 || ldx < K) return SD_EINVAL;
+    if (norm_w && K / 32 > NORM_MAX_KB) return SD_EUNSUPPORTED;
     if (!aligned(x, 4) || !aligned(q, 16)) return SD_EINVAL;
     return launched(launch(rmsnorm_quant_kernel, dim3(M), dim3(256), 0, cs(stream), x, ldx, norm_w, eps, K, q,
                            scales));

@@ -1,9 +1,12 @@
 // sdv_pass.cu - the whole verify pass of a quantised projection stack as one
-// persistent cooperative launch: per layer RMSNorm -> QKV (V requantised in the
-// epilogue) -> O (+ residual) -> RMSNorm -> gate|up (SiLU*mul requant) -> down
-// (+ residual); then the final RMSNorm, the vocabulary head with fused argmax and
-// statistics, and greedy acceptance.  Every phase runs the same device code as
-// the single-operation entry points, so the pass equals them bit for bit.
+// persistent cooperative launch: the first RMSNorm; per layer QKV (V requantised
+// in the epilogue) -> O (+ residual; the next RMSNorm's codes in the epilogue)
+// -> gate|up (SiLU*mul requant) -> down (+ residual; the next RMSNorm's codes);
+// then the vocabulary head with fused argmax and statistics, and greedy
+// acceptance.  An RMSNorm's row factor 1/rms is applied where its codes are
+// staged by the next matmul, from block sums of squares the epilogues leave.
+// The arithmetic is that of the single-operation entry points, so the pass
+// equals them bit for bit.
 #include <vector>
 
 #include "sdv_qmatmul.cuh"
@@ -39,24 +42,65 @@ static cudaError_t pass_launch(const QmmArgs *phases, int n_phases, uint32_t *ct
 
 using namespace sdv;
 
+namespace sdv {
+
+// Workspace of the pass: the matmul counters and partial sums, the head's statistics, the
+// activation fragments feeding the QKV / gate|up / head (from the RMSNorm phases), the O
+// projection (from the QKV epilogue) and the down projection (from the SiLU epilogue), and the
+// per-block sums of squares of the residual stream.  Fragment regions are sized for M = 16.
+struct PassWs {
+    size_t part, stats, afa_frag, afa_meta, afv_frag, afv_meta, aff_frag, aff_meta, ss, total;
+};
+
+static bool pass_ws_layout(int64_t H, int64_t F, int64_t V, int wq, int sms, PassWs &L) {
+    QmmPlan p;
+    size_t part = 0;
+    const int64_t shapes[4][3] = {{3 * H, H, 0}, {H, H, 0}, {2 * F, H, 1}, {H, F, 0}};
+    for (auto &sh : shapes) {
+        if (!make_plan(wq, sh[0], sh[1], sh[2] != 0, false, sms, p)) return false;
+        part = p.ws_part > part ? p.ws_part : part;
+    }
+    if (!make_plan(SD_Q8_0, V, H, false, true, sms, p)) return false;
+    part = p.ws_part > part ? p.ws_part : part;
+    const size_t KBH = static_cast<size_t>(H / 32), KBF = static_cast<size_t>(F / 32);
+    const size_t fb = af_frag_bytes(16) > af_frag_bytes(8) ? af_frag_bytes(16) : af_frag_bytes(8);
+    const size_t mb = af_meta_bytes(16);
+    size_t off = WS_CNT_BYTES;
+    L.part = off;
+    off += part;
+    L.stats = off;
+    off += p.ws_stats;
+    L.afa_frag = off;
+    off += align_up(KBH * fb, 256);
+    L.afa_meta = off;
+    off += align_up(KBH * mb, 256);
+    L.afv_frag = off;
+    off += align_up(KBH * fb, 256);
+    L.afv_meta = off;
+    off += align_up(KBH * mb, 256);
+    L.aff_frag = off;
+    off += align_up(KBF * fb, 256);
+    L.aff_meta = off;
+    off += align_up(KBF * mb, 256);
+    L.ss = off;
+    off += align_up(16 * align_up(KBH, 4) * sizeof(float), 256);
+    L.total = off;
+    return true;
+}
+
+}  // namespace sdv
+
 extern "C" {
 
 size_t sd_pass_plan_bytes(int32_t n_layers) {
     if (n_layers < 0) return 0;
-    return sizeof(PassHeader) + static_cast<size_t>(6 * n_layers + 3) * sizeof(QmmArgs);
+    return sizeof(PassHeader) + static_cast<size_t>(4 * n_layers + 3) * sizeof(QmmArgs);
 }
 
 size_t sd_pass_workspace_bytes(int64_t hidden, int64_t ffn, int64_t vocab, int32_t wq) {
-    const int sms = num_sms();
-    size_t best = 0;
-    QmmPlan p;
-    const int64_t shapes[4][3] = {{3 * hidden, hidden, 0}, {hidden, hidden, 0}, {2 * ffn, hidden, 1}, {hidden, ffn, 0}};
-    for (auto &sh : shapes) {
-        if (!make_plan(wq, sh[0], sh[1], sh[2] != 0, false, sms, p)) return 0;
-        best = p.ws_total > best ? p.ws_total : best;
-    }
-    if (!make_plan(SD_Q8_0, vocab, hidden, false, true, sms, p)) return 0;
-    return p.ws_total > best ? p.ws_total : best;
+    if (hidden <= 0 || ffn <= 0 || vocab <= 0 || hidden % 64 || ffn % 32) return 0;
+    PassWs L;
+    return pass_ws_layout(hidden, ffn, vocab, wq, num_sms(), L) ? L.total : 0;
 }
 
 sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, sd_pass *out) {
@@ -65,7 +109,7 @@ sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, 
     const int64_t H = d->hidden, F = d->ffn, V = d->vocab;
     const int M = d->M;
     if (L < 0 || M < 1 || H <= 0 || F <= 0 || V <= 0 || H % 64 || F % 32 || !d->layers) return SD_EINVAL;
-    if (M > 16) return SD_EUNSUPPORTED;
+    if (M > 16 || H / 32 > PASS_NORM_MAX_KB) return SD_EUNSUPPORTED;
     if (d->wq != SD_Q4_32 && d->wq != SD_Q8_0) return SD_EINVAL;
     if (d->wq == SD_Q8_0) return SD_EUNSUPPORTED;  // the SiLU*mul epilogue needs the 4-bit gate|up pairing
     if (plan_bytes < sd_pass_plan_bytes(L)) return SD_EINVAL;
@@ -74,15 +118,21 @@ sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, 
         !d->workspace)
         return SD_EINVAL;
     if (M > 1 && !d->tokens) return SD_EINVAL;
-    if (!aligned(d->workspace, 256) || d->ws_bytes < sd_pass_workspace_bytes(H, F, V, d->wq)) return SD_EINVAL;
     if (!(d->temperature > 0.0f)) return SD_EINVAL;
     int *st = status_ptr();
     if (!st) return SD_ECUDA;
     const int sms = num_sms();
-    const int NT = M <= 8 ? 1 : 2;
+    PassWs W;
+    if (!pass_ws_layout(H, F, V, d->wq, sms, W)) return SD_EINVAL;
+    if (!aligned(d->workspace, 256) || d->ws_bytes < W.total) return SD_EINVAL;
+    const int NT = af_nt(M);
 
     std::vector<QmmArgs> ph;
+    ph.reserve(static_cast<size_t>(4 * L + 3));  // pointers returned by matmul() below stay valid
     uint8_t *ws = static_cast<uint8_t *>(d->workspace);
+    uint8_t *afa_f = ws + W.afa_frag, *afv_f = ws + W.afv_frag, *aff_f = ws + W.aff_frag;
+    float *afa_m = reinterpret_cast<float *>(ws + W.afa_meta), *afv_m = reinterpret_cast<float *>(ws + W.afv_meta),
+          *aff_m = reinterpret_cast<float *>(ws + W.aff_meta), *ssb = reinterpret_cast<float *>(ws + W.ss);
     auto base = [&](QmmArgs &a) {
         a = QmmArgs{};
         a.M = M;
@@ -90,14 +140,14 @@ sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, 
         a.cnt = reinterpret_cast<uint32_t *>(ws);
         a.st_cnt = a.cnt + WS_UNIT_CNT;
         a.st_done = a.st_cnt + WS_STAT_CNT;
-        a.part = reinterpret_cast<float *>(ws + WS_CNT_BYTES);
+        a.part = reinterpret_cast<float *>(ws + W.part);
     };
+    const int ss_ld = static_cast<int>(align_up(static_cast<size_t>(H / 32), 4));
     auto matmul = [&](int qt, const void *w, int64_t n, int64_t k, bool pair, const int8_t *q, const float *sc,
-                      float *y, const float *res, uint32_t epi, int64_t col0, int8_t *qn, float *sn,
-                      int64_t nq) -> bool {
+                      const uint8_t *af_f, const float *af_m) -> QmmArgs * {
         QmmPlan p;
-        if (!make_plan(qt, n, k, pair, false, sms, p) || p.G != sms) return false;
-        if (!w || !aligned(w, 16)) return false;
+        if (!make_plan(qt, n, k, pair, false, sms, p) || p.G != sms) return nullptr;
+        if (!w || !aligned(w, 16)) return nullptr;
         QmmArgs a;
         base(a);
         a.kind = KIND_MATMUL;
@@ -117,59 +167,89 @@ sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, 
         a.n_out = n;
         a.q = q;
         a.sc = sc;
-        a.y = y;
-        a.residual = res;
-        a.epi = epi;
-        a.col0 = col0;
-        a.q_next = qn;
-        a.s_next = sn;
-        a.nq = nq;
+        a.af_frag = af_f;
+        a.af_meta = af_m;
+        a.ss_ld = ss_ld;
+        a.eps = d->eps;
         ph.push_back(a);
-        return true;
+        return &ph.back();
     };
-    auto norm = [&](const float *x, const float *w, int64_t K, int8_t *q, float *s) {
+    // input: RMSNorm codes in AF_a, scaled by inv at staging (block sums of squares in ssb)
+    auto normed_input = [&](QmmArgs *a) {
+        a->af_norm = 1;
+        a->ss_in = ssb;
+        a->s_norm_out = d->sa;
+    };
+    // epilogue: residual add into h, block sums of squares, the next RMSNorm's codes into AF_a
+    auto residual_out = [&](QmmArgs *a, const float *next_norm, int next_qt) {
+        a->y = d->h;
+        a->residual = d->h;
+        a->ss = ssb;
+        a->norm_next = next_norm;
+        a->q_next = d->qa;
+        a->nq = H;
+        a->af_out_frag = afa_f;
+        a->af_out_meta = afa_m;
+        a->af_out_qt = next_qt;
+    };
+    {  // the first RMSNorm, on the input rows
         QmmArgs a;
         base(a);
         a.kind = KIND_NORM;
-        a.KB = static_cast<int32_t>(K / 32);
-        a.xin = x;
-        a.norm_w = w;
-        a.eps = d->eps;
-        a.q_next = q;
-        a.s_next = s;
+        a.KB = static_cast<int32_t>(H / 32);
+        a.xin = d->h;
+        a.norm_w = L > 0 ? d->layers[0].norm1 : d->final_norm;
+        a.ss = ssb;
+        a.ss_ld = ss_ld;
+        a.q_next = d->qa;
+        a.af_out_frag = afa_f;
+        a.af_out_meta = afa_m;
+        a.af_out_qt = L > 0 ? d->wq : SD_Q8_0;
+        if (!a.norm_w) return SD_EINVAL;
         ph.push_back(a);
-    };
+    }
     for (int l = 0; l < L; ++l) {
         const sd_layer &lw = d->layers[l];
         if (!lw.norm1 || !lw.norm2) return SD_EINVAL;
-        norm(d->h, lw.norm1, H, d->qa, d->sa);
-        if (!matmul(d->wq, lw.qkv, 3 * H, H, false, d->qa, d->sa, nullptr, nullptr, SD_EPI_REQUANT, 2 * H, d->qv, d->sv,
-                    H))
-            return SD_EINVAL;
-        if (!matmul(d->wq, lw.o, H, H, false, d->qv, d->sv, d->h, d->h, SD_EPI_NONE, 0, nullptr, nullptr, 0))
-            return SD_EINVAL;
-        norm(d->h, lw.norm2, H, d->qa, d->sa);
-        if (!matmul(d->wq, lw.gate_up, 2 * F, H, true, d->qa, d->sa, nullptr, nullptr, SD_EPI_SILU_MUL_REQUANT, 0,
-                    d->qf, d->sf, F))
-            return SD_EINVAL;
-        if (!matmul(d->wq, lw.down, H, F, false, d->qf, d->sf, d->h, d->h, SD_EPI_NONE, 0, nullptr, nullptr, 0))
-            return SD_EINVAL;
+        QmmArgs *a = matmul(d->wq, lw.qkv, 3 * H, H, false, d->qa, d->sa, afa_f, afa_m);
+        if (!a) return SD_EINVAL;
+        normed_input(a);
+        a->epi = SD_EPI_REQUANT;
+        a->col0 = 2 * H;
+        a->q_next = d->qv;
+        a->s_next = d->sv;
+        a->nq = H;
+        a->af_out_frag = afv_f;
+        a->af_out_meta = afv_m;
+        a->af_out_qt = d->wq;
+        if (!(a = matmul(d->wq, lw.o, H, H, false, d->qv, d->sv, afv_f, afv_m))) return SD_EINVAL;
+        residual_out(a, lw.norm2, d->wq);
+        if (!(a = matmul(d->wq, lw.gate_up, 2 * F, H, true, d->qa, d->sa, afa_f, afa_m))) return SD_EINVAL;
+        normed_input(a);
+        a->epi = SD_EPI_SILU_MUL_REQUANT;
+        a->q_next = d->qf;
+        a->s_next = d->sf;
+        a->nq = F;
+        a->af_out_frag = aff_f;
+        a->af_out_meta = aff_m;
+        a->af_out_qt = d->wq;
+        if (!(a = matmul(d->wq, lw.down, H, F, false, d->qf, d->sf, aff_f, aff_m))) return SD_EINVAL;
+        const bool lastl = l + 1 == L;
+        if (!lastl && !d->layers[l + 1].norm1) return SD_EINVAL;
+        residual_out(a, lastl ? d->final_norm : d->layers[l + 1].norm1, lastl ? SD_Q8_0 : d->wq);
     }
-    norm(d->h, d->final_norm, H, d->qa, d->sa);
-    if (!matmul(SD_Q8_0, d->head, V, H, false, d->qa, d->sa, d->logits, nullptr, SD_EPI_NONE, 0, nullptr, nullptr, 0))
-        return SD_EINVAL;
     {
-        QmmArgs &hd = ph.back();
-        const int64_t nst = (V + STAT_TILE - 1) / STAT_TILE;
-        QmmPlan p;
-        make_plan(SD_Q8_0, V, H, false, true, sms, p);
-        hd.head = 1;
-        hd.T = d->temperature;
-        hd.argmax = d->argmax;
-        hd.row_max = d->row_max;
-        hd.row_sumexp = d->row_sumexp;
-        hd.n_stiles = static_cast<int32_t>(nst);
-        hd.st_part = reinterpret_cast<float4 *>(ws + WS_CNT_BYTES + p.ws_part);
+        QmmArgs *hd = matmul(SD_Q8_0, d->head, V, H, false, d->qa, d->sa, afa_f, afa_m);
+        if (!hd) return SD_EINVAL;
+        normed_input(hd);
+        hd->y = d->logits;
+        hd->head = 1;
+        hd->T = d->temperature;
+        hd->argmax = d->argmax;
+        hd->row_max = d->row_max;
+        hd->row_sumexp = d->row_sumexp;
+        hd->n_stiles = static_cast<int32_t>((V + STAT_TILE - 1) / STAT_TILE);
+        hd->st_part = reinterpret_cast<float4 *>(ws + W.stats);
     }
     {
         QmmArgs a;
@@ -182,27 +262,19 @@ sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, 
         a.out_count = d->out_count;
         ph.push_back(a);
     }
-    // one shared-memory layout for every phase: the largest split, pair rows, the largest stage
+    // one shared-memory layout for every phase: the largest split, pair rows, the largest stage,
+    // and the RMSNorm scratch
     int kbs = 0;
     size_t slot = 0;
     for (const QmmArgs &a : ph)
         if (a.kind == KIND_MATMUL) {
             kbs = a.KBs > kbs ? a.KBs : kbs;
-            const size_t st = static_cast<size_t>(a.SB) * a.step_bytes;
-            slot = st > slot ? st : slot;
+            const size_t sz = static_cast<size_t>(a.SB) * a.step_bytes;
+            slot = sz > slot ? sz : slot;
         }
-    int NS = 0;
-    uint32_t o_ring, o_act, o_meta, o_red;
-    const size_t smem = layout_smem(kbs, NT, 64, slot, NS, o_ring, o_act, o_meta, o_red);
-    if (smem > 227 * 1024) return SD_EUNSUPPORTED;
-    for (QmmArgs &a : ph) {
-        a.NS = NS;
-        a.off_ring = o_ring;
-        a.off_act = o_act;
-        a.off_meta = o_meta;
-        a.off_red = o_red;
-        a.stage_stride = static_cast<uint32_t>(slot);
-    }
+    SmemLayout lay;
+    if (!layout_smem(kbs, M, 64, slot, static_cast<size_t>(M) * ss_ld * sizeof(float), lay)) return SD_EUNSUPPORTED;
+    for (QmmArgs &a : ph) apply_layout(a, lay, slot);
     PassHeader hdr = {};
     if (cudaMemcpy(plan, &hdr, sizeof(hdr), cudaMemcpyHostToDevice) != cudaSuccess) return SD_ECUDA;
     if (cudaMemcpy(static_cast<uint8_t *>(plan) + sizeof(PassHeader), ph.data(), ph.size() * sizeof(QmmArgs),
@@ -211,7 +283,7 @@ sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, 
     out->plan = plan;
     out->n_phases = static_cast<int32_t>(ph.size());
     out->nt = NT;
-    out->smem_bytes = static_cast<uint32_t>(smem);
+    out->smem_bytes = static_cast<uint32_t>(lay.total);
     out->grid = sms;
     return SD_OK;
 }

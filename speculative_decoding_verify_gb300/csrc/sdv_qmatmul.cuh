@@ -1,5 +1,6 @@
 // sdv_qmatmul.cuh - multi-position quantised matmul (one weight read serves
-// all M verify positions), with the requantising, SiLU*mul and head epilogues.
+// all M verify positions), with the requantising, SiLU*mul, residual and head
+// epilogues, and the persistent verify pass built from the same pieces.
 //
 // Work decomposition ("stream-K"): the weights of a matrix are 32-row tiles
 // (or gate|up tile pairs) x k-blocks.  The k range is cut into KS splits of at
@@ -12,36 +13,73 @@
 // All of this depends on (n_out, k_in, SM count) only, never on M, which
 // makes every output row bit-identical whatever the number of positions.
 //
-// Inside a CTA: warp 8 (one elected lane) streams records with TMA bulk copies
-// into a ring of shared-memory stages guarded by mbarriers; warps 0..7 consume
-// them.  Each record's exact int32 block dots come from mma.sync m16n8k16
-// (f16 operands, f32 accumulate): the weight codes enter as the fp16 values
-// 1024 + code (4-bit, one LOP3 per two values; codes in bits 4..7 of a byte
-// enter as 1024 + 16 code against activations pre-divided by 16) or 1152 + q
-// (Q8_0, one PRMT per two values), activations as exact fp16 integers, and the
-// accumulator starts at minus the offsets' contribution, so it ends at the
-// exact integer dot (every partial sum is an integer below 2^23).  Each lane
-// then adds d_w * d_a * dot for its 8 (row, position) results.  The 8 warps'
-// partials are added in warp order at the end of each piece.
+// Inside a CTA three roles run concurrently:
+//  * warp 8 (one elected lane) streams records with TMA bulk copies into a
+//    ring of shared-memory stages guarded by mbarriers;
+//  * warps 0..7 consume them.  Each record's exact int32 block dots come from
+//    mma.sync m16n8k16 (f16 operands, f32 accumulate): the weight codes enter
+//    as the fp16 values 1024 + code (4-bit, one LOP3 per two values; codes in
+//    bits 4..7 of a byte enter as 1024 + 16 code against activations divided
+//    by 16) or 1152 + q (Q8_0, one PRMT per two values), activations as exact
+//    fp16 integers, and the accumulator starts at minus the offsets'
+//    contribution, so it ends at the exact integer dot (every partial sum is
+//    an integer below 2^23).  Each lane then adds d_w * d_a * dot for its 8
+//    (row, position) results.  At the end of a piece each warp leaves its
+//    partial sums in a shared-memory slot and moves on;
+//  * warps 9..11 (the finishers, positions split between them) add the 8
+//    warps' partials of a piece in warp order, then run the stream-K fixup
+//    and the epilogue (residual, block sums of squares, requantisation into
+//    the next matmul's activation fragments, head statistics) while the
+//    consumers work on the next piece.
 #pragma once
 
 #include "sdv_common.cuh"
 
 namespace sdv {
 
-#ifndef SDV_NCW
-#define SDV_NCW 8
-#endif
-constexpr int NCW = SDV_NCW;           // consumer warps
-constexpr int QMM_THREADS = (NCW + 1) * 32;
+constexpr int NCW = 8;                       // consumer warps
+constexpr int NF = 3;                        // finisher warps
+constexpr int PRODUCER_WARP = NCW;           // streams the weights
+constexpr int FIN_WARP0 = NCW + 1;           // first finisher warp: reductions, fixups, epilogues
+constexpr int QMM_THREADS = (NCW + 1 + NF) * 32;
+constexpr int CONS_THREADS = NCW * 32;         // named barrier BAR_CONS: consumers
+constexpr int WORK_THREADS = (NCW + NF) * 32;  // named barrier BAR_WORK: consumers + finishers
+constexpr int FIN_THREADS = NF * 32;           // named barrier BAR_FIN: finishers
+constexpr int BAR_CONS = 1, BAR_WORK = 2, BAR_FIN = 3;
+constexpr int FIN_MPW = (16 + NF - 1) / NF;  // positions per finisher warp at most
 constexpr int KB_SPLIT_MAX = 160;      // blocks per k-split
 constexpr int MPAD = 16;               // position stride of workspace partials
-constexpr uint64_t WAIT_NS = 2000000000ull;   // 2 s bound on any in-kernel wait
+constexpr int MAX_NS = 12;             // ring stages (mbarrier header room)
+constexpr uint64_t WAIT_NS = 2000000000ull;     // 2 s bound on any in-kernel wait
 constexpr uint64_t KERNEL_NS = 10000000000ull;  // 10 s bound on any launch's loops (self-check)
 constexpr int STAT_TILE = 1024;        // vocabulary tile of the softmax statistics
 constexpr int WS_UNIT_CNT = 32768;     // workspace counters: units (tiles / tile pairs) per call
 constexpr int WS_STAT_CNT = 2048;      // workspace counters: 1024-token statistics tiles
 constexpr size_t WS_CNT_BYTES = 160 * 1024;  // >= (WS_UNIT_CNT + WS_STAT_CNT + 1) * 4, 256-aligned
+constexpr int NORM_MAX_KB = 2048;      // RMSNorm rows of at most 65536 elements
+constexpr int PASS_NORM_MAX_KB = 1024; // ... inside the verify pass (one warp's 1024-slot tree)
+
+// Shared-memory header: mbarriers at fixed offsets
+constexpr uint32_t HDR_FULL = 0, HDR_EMPTY = 8 * MAX_NS, HDR_ACT = 16 * MAX_NS, HDR_RFULL = HDR_ACT + 8,
+                   HDR_REMPTY = HDR_RFULL + 16, HDR_BYTES = 256;
+
+// ---------------------------------------------------------------------------
+// Activation fragments ("AF"): a matmul's int8 input laid out for its inner
+// loop, written by whoever produces the activations (the RMSNorm phase, the
+// requantising epilogues) and copied into shared memory with one bulk copy.
+// For K = 32 KB and M positions, NT = 1 (M <= 8) or 2:
+//   frag: per block M*4 entries, entry (m, c) at index (jb*M + m)*4 + c holding
+//     for position m the k values 2c, 2c+1 | 2c+8, 2c+9 | 16+2c, 17+2c |
+//     24+2c, 25+2c: NT = 1 as four fp16 pairs (uint4; for a 4-bit consumer
+//     the k+8 pairs divided by 16, exact), NT = 2 as eight raw bytes (uint2).
+//   meta: per block 8 NT pairs {corr, d_a} (float2), zero beyond M, where corr
+//     is minus the code offsets' contribution: 4-bit -(1032 S_lo + 72 S_hi)
+//     with S_lo / S_hi the sums of the codes at k % 16 < 8 / >= 8, Q8_0
+//     -1152 (S_lo + S_hi).
+// ---------------------------------------------------------------------------
+__host__ __device__ __forceinline__ int af_nt(int M) { return M <= 8 ? 1 : 2; }
+__host__ __device__ __forceinline__ uint32_t af_frag_bytes(int M) { return af_nt(M) == 1 ? 64u * M : 32u * M; }
+__host__ __device__ __forceinline__ uint32_t af_meta_bytes(int M) { return 64u * af_nt(M); }
 
 struct QmmArgs {
     const uint8_t *w;
@@ -55,16 +93,26 @@ struct QmmArgs {
     int32_t SB;          // steps per stage
     int32_t NS;          // stages
     uint32_t step_bytes; // bytes of one step
-    const int8_t *q;
+    const int8_t *q;     // int8 activations [M][K] + scales [M][KB] (staged directly when af_frag is null)
     const float *sc;
+    const uint8_t *af_frag;  // activation fragments of the input (bulk-copied when non-null)
+    const float *af_meta;
     int32_t M;
     float *y;
     const float *residual;
+    float *ss;           // residual epilogue: per-32-block sums of squares of y [M][n_out/32] (nullable)
     uint32_t epi;
     int64_t col0;
     int8_t *q_next;
     float *s_next;
     int64_t nq;          // row width of q_next
+    uint8_t *af_out_frag;  // requantising epilogues / RMSNorm: fragments of the next matmul (nullable)
+    float *af_out_meta;
+    int32_t af_out_qt;     // weight format of that matmul
+    const float *norm_next;  // residual epilogue: weight of the next RMSNorm; its codes go to q_next / af_out
+    int32_t af_norm;       // the input fragments hold RMSNorm codes: scales are max|x w| / 127, times inv here
+    int32_t ss_ld;         // row stride of the block sums of squares (a multiple of 4)
+    float *s_norm_out;     // scales inv * c of those codes [M][KB] (nullable)
     float *part;         // workspace partials [NU][KS][P][rows][MPAD]
     uint32_t *cnt;       // workspace counters [NU]
     // head statistics
@@ -78,12 +126,15 @@ struct QmmArgs {
     uint32_t *st_done;   // [1]
     int32_t n_stiles;
     int *status;
-    uint32_t off_ring, off_act, off_meta, off_red, off_tmp;
+    uint32_t off_ring, off_act, off_meta, off_red, off_ss;
     uint32_t stage_stride;  // bytes between ring slots (>= SB * step_bytes)
+    int32_t NRB;            // partial-sum slots between consumers and finisher (1 or 2)
+    int32_t rows_p;         // row stride of a slot (rows + 4: conflict-free stores)
     // phase kind inside a pass: 0 matmul (qt, pair), 1 RMSNorm + requant, 2 greedy acceptance
     int32_t kind, qt, pair;
     const float *xin;       // RMSNorm input [M][K] (K = 32 KB)
     const float *norm_w;    // RMSNorm weight [K]
+    const float *ss_in;     // block sums of squares [M][ss_ld] of the normalised input (af_norm)
     float eps;
     const int32_t *tokens;  // acceptance inputs / outputs
     const int32_t *parent;
@@ -93,7 +144,7 @@ struct QmmArgs {
 
 constexpr int KIND_MATMUL = 0, KIND_NORM = 1, KIND_ACCEPT = 2;
 
-// fetch-and-add with release (orders the CTA's prior writes, seen through a bar.sync) and acquire
+// fetch-and-add with release (orders the writes seen through a barrier) and acquire
 __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v) {
     uint32_t old;
     asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
@@ -244,7 +295,69 @@ __device__ __forceinline__ float dot_corr(const int8_t *arow) {
 }
 
 // ---------------------------------------------------------------------------
-// epilogue of one finished (unit, position): lane = row
+// activation fragments: writer
+// ---------------------------------------------------------------------------
+
+// two int8 values (or their sixteenths, exact) as an fp16 pair, the first in the low half
+__device__ __forceinline__ uint32_t pack_h2(int x0, int x1, float s) {
+    __half2 h = __floats2half2_rn(static_cast<float>(x0) * s, static_cast<float>(x1) * s);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_b4(int x0, int x1, int x2, int x3) {
+    return (static_cast<uint32_t>(x0) & 0xFFu) | ((static_cast<uint32_t>(x1) & 0xFFu) << 8) |
+           ((static_cast<uint32_t>(x2) & 0xFFu) << 16) | ((static_cast<uint32_t>(x3) & 0xFFu) << 24);
+}
+
+// Writes position m of block jb of an activation-fragment buffer (layout above) from one full
+// warp whose lane k holds the block's code v and whose scale is d.  qt: weight format of the
+// matmul that reads it.  Lanes 0..3 write the fragment entries, lane 0 the {corr, d} pair; the
+// writer of the last position also zeroes the pairs of the padding positions M .. 8 NT - 1.
+__device__ __forceinline__ void af_write(uint8_t *frag, float *meta, int M, int64_t jb, int m, int lane, int v,
+                                         float d, int qt) {
+    // S_lo + 65536 S_hi in one reduction; |S_lo| <= 16 * 127 < 32768 recovers both exactly
+    const int lo = (lane & 8) ? 0 : v;  // k % 16 < 8
+    int t = lo + (v - lo) * 65536;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    const int s_hi = (t + 32768) >> 16, s_lo = t - s_hi * 65536;
+    const float corr = static_cast<float>(qt == SD_Q4_32 ? -(1032 * s_lo + 72 * s_hi) : -1152 * (s_lo + s_hi));
+    const int c = lane & 3, k0 = 2 * c;
+    const int e0 = __shfl_sync(0xffffffffu, v, k0), e1 = __shfl_sync(0xffffffffu, v, k0 + 1);
+    const int e2 = __shfl_sync(0xffffffffu, v, k0 + 8), e3 = __shfl_sync(0xffffffffu, v, k0 + 9);
+    const int e4 = __shfl_sync(0xffffffffu, v, k0 + 16), e5 = __shfl_sync(0xffffffffu, v, k0 + 17);
+    const int e6 = __shfl_sync(0xffffffffu, v, k0 + 24), e7 = __shfl_sync(0xffffffffu, v, k0 + 25);
+    const int NT = af_nt(M);
+    if (lane < 4) {
+        const int64_t idx = (jb * M + m) * 4 + c;
+        if (NT == 1) {
+            const float hs = qt == SD_Q4_32 ? 0.0625f : 1.0f;
+            reinterpret_cast<uint4 *>(frag)[idx] =
+                make_uint4(pack_h2(e0, e1, 1.0f), pack_h2(e2, e3, hs), pack_h2(e4, e5, 1.0f), pack_h2(e6, e7, hs));
+        } else {
+            reinterpret_cast<uint2 *>(frag)[idx] = make_uint2(pack_b4(e0, e1, e2, e3), pack_b4(e4, e5, e6, e7));
+        }
+    }
+    if (lane == 0) {
+        float2 *mp = reinterpret_cast<float2 *>(meta) + jb * 8 * NT;
+        mp[m] = make_float2(corr, d);
+        if (m == M - 1)
+            for (int p = M; p < 8 * NT; ++p) mp[p] = make_float2(0.0f, 0.0f);
+    }
+}
+
+// pairwise tree over the 32 lanes (strides 16, 8, 4, 2, 1); lane 0 holds the sum
+__device__ __forceinline__ float tree32(float x, int lane) {
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) {
+        const float o = __shfl_down_sync(0xffffffffu, x, s);
+        if (lane < s) x = __fadd_rn(x, o);
+    }
+    return x;
+}
+
+// ---------------------------------------------------------------------------
+// epilogue of one finished (unit, position), run by the finisher warp: lane = row
 // ---------------------------------------------------------------------------
 template <int PAIR>
 __device__ __forceinline__ void epilogue(const QmmArgs &a, int u, int m, int lane, float v, float vu) {
@@ -255,42 +368,58 @@ __device__ __forceinline__ void epilogue(const QmmArgs &a, int u, int m, int lan
             a.y[m * a.n_out + n] = v;
             a.y[m * a.n_out + F + n] = vu;
         }
-        float h = silu_mul(v, vu);
+        const float h = silu_mul(v, vu);
         float d;
-        int code = requant_lane(h, d);
+        const int code = requant_lane(h, d);
         a.q_next[m * a.nq + n] = static_cast<int8_t>(code);
         if (lane == 0) a.s_next[m * (a.nq / 32) + u] = d;
+        if (a.af_out_frag) af_write(a.af_out_frag, a.af_out_meta, a.M, u, m, lane, code, d, a.af_out_qt);
     } else {
         const int64_t n = static_cast<int64_t>(u) * 32 + lane;
         const bool ok = n < a.n_out;
         if (ok && a.residual) v = __fadd_rn(v, __ldcg(a.residual + m * a.n_out + n));
         if (ok && a.y) a.y[m * a.n_out + n] = v;
+        if (a.ss) {  // n_out % 32 == 0 is required here
+            const float s = tree32(__fmul_rn(v, v), lane);
+            if (lane == 0) a.ss[m * a.ss_ld + u] = s;
+        }
+        if (a.norm_next) {  // codes of the next RMSNorm from t = v w; its scale waits for inv
+            float c;
+            const int code = requant_lane(__fmul_rn(v, __ldg(a.norm_next + n)), c);
+            a.q_next[m * a.nq + n] = static_cast<int8_t>(code);
+            af_write(a.af_out_frag, a.af_out_meta, a.M, u, m, lane, code, c, a.af_out_qt);
+        }
         if (a.epi == SD_EPI_REQUANT && static_cast<int64_t>(u) * 32 >= a.col0) {
             float d;
-            int code = requant_lane(ok ? v : 0.0f, d);  // n_out % 32 == 0 is required here
+            const int code = requant_lane(ok ? v : 0.0f, d);  // n_out % 32 == 0 is required here
             const int64_t c = n - a.col0;
             if (ok) a.q_next[m * a.nq + c] = static_cast<int8_t>(code);
             if (lane == 0) a.s_next[m * (a.nq / 32) + c / 32] = d;
+            if (a.af_out_frag)
+                af_write(a.af_out_frag, a.af_out_meta, a.M, (static_cast<int64_t>(u) * 32 - a.col0) / 32, m, lane, code,
+                         d, a.af_out_qt);
         }
     }
 }
 
-// Softmax statistics of one finished 1024-token tile st, then (last tile) the
-// per-row fold.  Called by all consumer threads after the tile's logits are
-// globally visible.  Warp w handles positions w, w+8, ...
-__device__ inline void head_tile_stats(const QmmArgs &a, int st, int lane, int warp) {
+// ---------------------------------------------------------------------------
+// head statistics (finisher warps; warp f takes positions f, f + NF, ...).  A
+// 1024-token tile's statistics are formed by the CTA that finishes its last
+// 32-row tile; the CTA that finishes the last statistics tile folds them per row.
+// ---------------------------------------------------------------------------
+__device__ inline void head_tile_stats(const QmmArgs &a, int st, int lane, int f) {
     const int64_t V = a.n_out;
-    for (int m = warp; m < a.M; m += NCW) {
+    for (int m = f; m < a.M; m += NF) {
         float v[32];
         float zmax = -__int_as_float(0x7f800000);
         float bl = -__int_as_float(0x7f800000);
         int bi = 0x7fffffff;
 #pragma unroll
         for (int r = 0; r < 32; ++r) {
-            int64_t e = static_cast<int64_t>(st) * STAT_TILE + lane + 32 * r;
+            const int64_t e = static_cast<int64_t>(st) * STAT_TILE + lane + 32 * r;
             float z = -__int_as_float(0x7f800000);
             if (e < V) {
-                float l = __ldcg(a.y + m * V + e);
+                const float l = __ldcg(a.y + m * V + e);
                 if (l > bl) {
                     bl = l;
                     bi = static_cast<int>(e);
@@ -303,8 +432,8 @@ __device__ inline void head_tile_stats(const QmmArgs &a, int st, int lane, int w
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) {
             zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, o));
-            float ol = __shfl_xor_sync(0xffffffffu, bl, o);
-            int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            const float ol = __shfl_xor_sync(0xffffffffu, bl, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
             if (ol > bl || (ol == bl && oi < bi)) {
                 bl = ol;
                 bi = oi;
@@ -312,23 +441,23 @@ __device__ inline void head_tile_stats(const QmmArgs &a, int st, int lane, int w
         }
 #pragma unroll
         for (int r = 0; r < 32; ++r) {
-            int64_t e = static_cast<int64_t>(st) * STAT_TILE + lane + 32 * r;
+            const int64_t e = static_cast<int64_t>(st) * STAT_TILE + lane + 32 * r;
             v[r] = e < V ? cexpf_canon(__fsub_rn(v[r], zmax)) : 0.0f;
         }
-        float s = tree1024_warp(v);
+        const float s = tree1024_warp(v);
         if (lane == 0) a.st_part[st * MPAD + m] = make_float4(zmax, s, __int_as_float(bi), bl);
     }
 }
 
-__device__ inline void head_final_fold(const QmmArgs &a, int lane, int warp) {
-    for (int m = warp; m < a.M; m += NCW) {
+__device__ inline void head_final_fold(const QmmArgs &a, int lane, int f) {
+    for (int m = f; m < a.M; m += NF) {
         float mx = -__int_as_float(0x7f800000);
         float bl = -__int_as_float(0x7f800000);
         int bi = 0x7fffffff;
         for (int t = lane; t < a.n_stiles; t += 32) {
-            float4 p = __ldcg(a.st_part + t * MPAD + m);
+            const float4 p = __ldcg(a.st_part + t * MPAD + m);
             mx = fmaxf(mx, p.x);
-            int pi = __float_as_int(p.z);
+            const int pi = __float_as_int(p.z);
             if (p.w > bl || (p.w == bl && pi < bi)) {
                 bl = p.w;
                 bi = pi;
@@ -337,8 +466,8 @@ __device__ inline void head_final_fold(const QmmArgs &a, int lane, int warp) {
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) {
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            float ol = __shfl_xor_sync(0xffffffffu, bl, o);
-            int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            const float ol = __shfl_xor_sync(0xffffffffu, bl, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
             if (ol > bl || (ol == bl && oi < bi)) {
                 bl = ol;
                 bi = oi;
@@ -347,13 +476,13 @@ __device__ inline void head_final_fold(const QmmArgs &a, int lane, int warp) {
         // Z = sequential fold over tiles of s_t * exp(m_t - m); the products in parallel
         float Z = 0.0f;
         for (int t0 = 0; t0 < a.n_stiles; t0 += 32) {
-            int t = t0 + lane;
+            const int t = t0 + lane;
             float e = 0.0f;
             if (t < a.n_stiles) {
-                float4 p = __ldcg(a.st_part + t * MPAD + m);
+                const float4 p = __ldcg(a.st_part + t * MPAD + m);
                 e = __fmul_rn(p.y, cexpf_canon(__fsub_rn(p.x, mx)));
             }
-            int nn = a.n_stiles - t0 < 32 ? a.n_stiles - t0 : 32;
+            const int nn = a.n_stiles - t0 < 32 ? a.n_stiles - t0 : 32;
             for (int j = 0; j < nn; ++j) Z = __fadd_rn(Z, __shfl_sync(0xffffffffu, e, j));
         }
         if (lane == 0) {
@@ -364,47 +493,43 @@ __device__ inline void head_final_fold(const QmmArgs &a, int lane, int warp) {
     }
 }
 
-// Adds `n_done` finished 32-row tiles to statistics tile `st`; the CTA that completes the tile
-// computes its statistics, and the CTA that completes the last tile folds them.  Called by all
-// consumer threads with the same arguments (barriers inside); the finished logits were written
-// before the call.
-__device__ __forceinline__ void head_flush(const QmmArgs &a, int st, int n_done, int tid, int lane, int warp) {
+// Adds `n_done` finished 32-row tiles to statistics tile `st`.  Called by every finisher warp
+// with the same arguments (barriers inside); the finished logits were written before the call.
+__device__ inline void head_flush(const QmmArgs &a, int st, int n_done, int lane, int f) {
     if (st < 0 || n_done == 0) return;
-    named_bar_sync(1, NCW * 32);  // every thread's logits before thread 0's release
+    named_bar_sync(BAR_FIN, FIN_THREADS);  // every finisher's logits before the release below
     bool last = false;
-    if (tid == 0) {
-        const int tiles_in_st = (a.NU - st * (STAT_TILE / 32)) < (STAT_TILE / 32) ? (a.NU - st * (STAT_TILE / 32))
-                                                                                   : (STAT_TILE / 32);
+    if (f == 0 && lane == 0) {
+        const int left = a.NU - st * (STAT_TILE / 32);
+        const int tiles_in_st = left < STAT_TILE / 32 ? left : STAT_TILE / 32;
         const unsigned old = atom_add_acq_rel(&a.st_cnt[st], static_cast<uint32_t>(n_done));
         last = static_cast<int>(old) + n_done == tiles_in_st;
     }
-    if (!bar_any(1, NCW * 32, last)) return;
-    head_tile_stats(a, st, lane, warp);
-    named_bar_sync(1, NCW * 32);  // the tile's statistics before thread 0's release
+    if (!bar_any(BAR_FIN, FIN_THREADS, last)) return;
+    head_tile_stats(a, st, lane, f);
+    named_bar_sync(BAR_FIN, FIN_THREADS);  // the tile's statistics before the release below
     bool fold = false;
-    if (tid == 0) {
+    if (f == 0 && lane == 0) {
         a.st_cnt[st] = 0u;
         const unsigned old = atom_add_acq_rel(a.st_done, 1u);
         fold = static_cast<int>(old) == a.n_stiles - 1;
     }
-    if (!bar_any(1, NCW * 32, fold)) return;
-    head_final_fold(a, lane, warp);
-    if (tid == 0) *a.st_done = 0u;
+    if (!bar_any(BAR_FIN, FIN_THREADS, fold)) return;
+    head_final_fold(a, lane, f);
+    if (f == 0 && lane == 0) *a.st_done = 0u;
 }
 
 // ---------------------------------------------------------------------------
 // per-CTA state and shared-memory regions
 // ---------------------------------------------------------------------------
-// Decisions the consumer threads must take together (abort, "last to arrive", "statistics tile
-// complete") travel through bar_any, never through a shared flag.
 struct CtaShared {
-    volatile int abort;    // set by anyone whose bounded wait ran out; polled by waits
+    volatile int abort;    // set by anyone whose bounded wait ran out; polled by every wait
     float inv[16];         // RMSNorm phase: 1 / rms of each row
     uint64_t t0;           // launch start (globaltimer), for the launch-wide time bound
 };
 
 // Launch-wide self-check: past KERNEL_NS since the CTA started, record SD_ETIMEOUT and where
-// (status[1]: 1 producer, 2 consumer piece loop) and make the caller unwind.
+// (status[1]: 1 producer, 2 consumer).
 __device__ __forceinline__ bool out_of_time(const CtaShared &cs, int *status, int where) {
     if (gtimer_ns() - cs.t0 <= KERNEL_NS) return false;
     if (status && atomicCAS(status, 0, SD_ETIMEOUT) == 0) status[1] = where;
@@ -412,23 +537,26 @@ __device__ __forceinline__ bool out_of_time(const CtaShared &cs, int *status, in
 }
 
 struct Smem {
-    uint64_t *full, *empty;
+    uint64_t *full, *empty, *act_bar, *rfull, *rempty;
     uint8_t *ring;
-    uint4 *bsm;   // B operands of the split: fp16 fragments [block][lane] (one position tile)
-    uint2 *bsm8;  // ... or raw int8 fragments [block][tile][lane] converted at use (two tiles)
-    float *meta;  // [block][tile][corr 8 | d_a 8]
-    float *red;   // per-warp partial sums [warp][position][row]; RMSNorm scratch
+    uint8_t *act;   // the split's activation fragments
+    float *meta;    // the split's {corr, d_a} pairs
+    float *red;     // partial-sum slots [NRB][warp][position][rows_p]
+    float *ss;      // block sums of squares of a normalised input [M][ss_ld]
 };
 
 __device__ __forceinline__ Smem smem_regions(uint8_t *smem, const QmmArgs &a) {
     Smem r;
-    r.full = reinterpret_cast<uint64_t *>(smem);
-    r.empty = r.full + a.NS;
+    r.full = reinterpret_cast<uint64_t *>(smem + HDR_FULL);
+    r.empty = reinterpret_cast<uint64_t *>(smem + HDR_EMPTY);
+    r.act_bar = reinterpret_cast<uint64_t *>(smem + HDR_ACT);
+    r.rfull = reinterpret_cast<uint64_t *>(smem + HDR_RFULL);
+    r.rempty = reinterpret_cast<uint64_t *>(smem + HDR_REMPTY);
     r.ring = smem + a.off_ring;
-    r.bsm = reinterpret_cast<uint4 *>(smem + a.off_act);
-    r.bsm8 = reinterpret_cast<uint2 *>(smem + a.off_act);
+    r.act = smem + a.off_act;
     r.meta = reinterpret_cast<float *>(smem + a.off_meta);
     r.red = reinterpret_cast<float *>(smem + a.off_red);
+    r.ss = reinterpret_cast<float *>(smem + a.off_ss);
     return r;
 }
 
@@ -436,6 +564,11 @@ __device__ __forceinline__ void cta_init(const Smem &sm, int NS, CtaShared &cs) 
     for (int i = 0; i < NS; ++i) {
         mbar_init(&sm.full[i], 1);
         mbar_init(&sm.empty[i], NCW);
+    }
+    mbar_init(sm.act_bar, 1);
+    for (int i = 0; i < 2; ++i) {
+        mbar_init(&sm.rfull[i], NCW);
+        mbar_init(&sm.rempty[i], NF);
     }
     cs.abort = 0;
     cs.t0 = gtimer_ns();
@@ -485,321 +618,455 @@ __device__ inline void producer_drain(const Smem &sm, uint32_t it, int NS) {
 }
 
 // ---------------------------------------------------------------------------
-// consumers: one matmul phase (staging, stages, piece fixups, epilogues).
-// Returns false (the same on every consumer thread) when the phase was abandoned
-// after a bounded wait or the launch-wide time bound ran out.
+// consumers: activations of one k-split into shared memory
+// ---------------------------------------------------------------------------
+
+// Bulk copy of the split's fragments and {corr, d_a} pairs (consumer thread 0).  The fragments
+// were written by generic stores of other CTAs, made visible by the grid barrier's acquire;
+// the proxy fence orders that acquire before the copy engine's reads.
+__device__ __forceinline__ void stage_issue(const QmmArgs &a, const Smem &sm, int s, int len) {
+    const int64_t b0 = static_cast<int64_t>(s) * a.KBs;
+    const uint32_t fb = af_frag_bytes(a.M), mb = af_meta_bytes(a.M);
+    const uint32_t nf = static_cast<uint32_t>(len) * fb, nm = static_cast<uint32_t>(len) * mb;
+    const uint32_t ns = a.af_norm ? static_cast<uint32_t>(a.M) * a.ss_ld * 4u : 0u;
+    fence_proxy_async_global();
+    mbar_arrive_expect_tx(sm.act_bar, nf + nm + ns);
+    bulk_g2s_l2keep(sm.act, a.af_frag + b0 * fb, nf, sm.act_bar);
+    bulk_g2s_l2keep(sm.meta, reinterpret_cast<const uint8_t *>(a.af_meta) + b0 * mb, nm, sm.act_bar);
+    if (ns) bulk_g2s_l2keep(sm.ss, a.ss_in, ns, sm.act_bar);
+}
+
+// Fragments holding RMSNorm codes: form each row's inverse RMS from its block sums of squares
+// (one warp per row: the pairwise tree over 1024 zero-padded slots, equal to the tree over the
+// row's own power of two), then scale the split's {corr, c} pairs to {corr, inv c} and, in the
+// CTA that owns the split's first step, write those scales out.  All consumer threads.
+__device__ inline void stage_norm_scales(const QmmArgs &a, const Smem &sm, CtaShared &cs, int s, int len, bool ok) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int M = a.M, NT = af_nt(M);
+    if (ok) {
+        for (int m = warp; m < M; m += NCW) {
+            float v[32];
+#pragma unroll
+            for (int r = 0; r < 32; ++r) {
+                const int slot = lane + 32 * r;
+                v[r] = slot < a.KB ? sm.ss[m * a.ss_ld + slot] : 0.0f;
+            }
+            const float sum = tree1024_warp(v);
+            if (lane == 0) {
+                const float mean = __fdiv_rn(sum, static_cast<float>(a.KB) * 32.0f);
+                cs.inv[m] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, a.eps)));
+            }
+        }
+    }
+    named_bar_sync(BAR_CONS, CONS_THREADS);
+    if (ok) {
+        const int b0 = s * a.KBs;
+        const bool writer = a.s_norm_out && static_cast<int>(blockIdx.x) == owner_of(a, unit_start(a, s, 0));
+        float2 *mp = reinterpret_cast<float2 *>(sm.meta);
+        for (int it = tid; it < len * M; it += CONS_THREADS) {
+            const int jb = it / M, m = it - jb * M;
+            const float d = __fmul_rn(cs.inv[m], mp[jb * 8 * NT + m].y);
+            mp[jb * 8 * NT + m].y = d;
+            if (writer) a.s_norm_out[static_cast<int64_t>(m) * a.KB + b0 + jb] = d;
+        }
+    }
+    named_bar_sync(BAR_CONS, CONS_THREADS);
+}
+
+// The same shared-memory contents formed from plain int8 rows and scales (all consumer threads).
+template <int QT>
+__device__ inline void stage_rows(const QmmArgs &a, const Smem &sm, int s, int len, int tid) {
+    const int M = a.M, NT = af_nt(M);
+    const int64_t K = static_cast<int64_t>(a.KB) * 32;
+    const int b0 = s * a.KBs;
+    const int nitems = len * M * 4;  // (block, position, c)
+    for (int base = tid; base < nitems; base += 4 * CONS_THREADS) {
+        uint2 raw[4];
+#pragma unroll
+        for (int u4 = 0; u4 < 4; ++u4) {
+            const int it = base + u4 * CONS_THREADS;
+            raw[u4] = make_uint2(0u, 0u);
+            if (it < nitems) {
+                const int jb = it / (M * 4), rem = it - jb * M * 4, m = rem >> 2, c = rem & 3;
+                raw[u4] = b_raw(a.q + m * K + static_cast<int64_t>(b0 + jb) * 32, c);
+            }
+        }
+#pragma unroll
+        for (int u4 = 0; u4 < 4; ++u4) {
+            const int it = base + u4 * CONS_THREADS;
+            if (it < nitems) {
+                if (NT == 1) reinterpret_cast<uint4 *>(sm.act)[it] = b_frag_from_raw<QT>(raw[u4]);
+                else reinterpret_cast<uint2 *>(sm.act)[it] = raw[u4];
+            }
+        }
+    }
+    const int P8 = 8 * NT;
+    for (int it = tid; it < len * P8; it += CONS_THREADS) {
+        const int jb = it / P8, m = it - jb * P8;
+        const bool real = m < M;
+        const float corr = dot_corr<QT>(real ? a.q + m * K + static_cast<int64_t>(b0 + jb) * 32 : nullptr);
+        const float da = real ? __ldcg(a.sc + static_cast<int64_t>(m) * a.KB + b0 + jb) : 0.0f;
+        reinterpret_cast<float2 *>(sm.meta)[it] = make_float2(corr, da);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// consumers: the records of one stage.  Warp w takes steps w, w + 8, ...;
+// acc[nt][t][i] holds row 16t + g + 8(i>>1), position 8nt + 2c + (i&1)
+// (accu: the up rows of a gate|up pair).
+// ---------------------------------------------------------------------------
+template <int QT, int PAIR, int NT, bool FULL>
+__device__ __forceinline__ void stage_compute(const uint8_t *sbase, int n, int jb0, const uint8_t *act,
+                                              const float *meta, int M, int warp, int lane, float (&acc)[NT][2][4],
+                                              float (&accu)[PAIR ? NT : 1][2][4]) {
+    constexpr int REC = QT == SD_Q8_0 ? 1088 : 576;   // bytes of one 32-row record
+    constexpr int CODE = QT == SD_Q8_0 ? 1024 : 512;  // code bytes of a record
+    constexpr int STEP = PAIR ? 2 * REC : REC;
+    constexpr int RPW = (PAIR || QT == SD_Q8_0) ? 2 : 4;  // steps per warp in a full stage
+    const int lg = lane >> 2, lc = lane & 3;
+    const uint4 *act4 = reinterpret_cast<const uint4 *>(act);
+    const uint2 *act2 = reinterpret_cast<const uint2 *>(act);
+    const float4 *meta4 = reinterpret_cast<const float4 *>(meta);
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+        const int r = warp + NCW * i;
+        if (!FULL && r >= n) break;
+        const uint8_t *rp = sbase + r * STEP;
+        const int jb = jb0 + r;
+        uint32_t af[2][2][4], afu[2][2][4];
+        float2 w01, w23, u01, u23;  // scales of rows g, g+8 and 16+g, 24+g
+        if (QT == SD_Q4_32) q4_frag(*reinterpret_cast<const uint4 *>(rp + lane * 16), af);
+        else q8_frag(*reinterpret_cast<const uint4 *>(rp + lane * 16), *reinterpret_cast<const uint4 *>(rp + 512 + lane * 16), af);
+        {
+            const uint2 sw = *reinterpret_cast<const uint2 *>(rp + CODE + lg * 8);
+            w01 = __half22float2(*reinterpret_cast<const __half2 *>(&sw.x));
+            w23 = __half22float2(*reinterpret_cast<const __half2 *>(&sw.y));
+        }
+        if (PAIR) {
+            q4_frag(*reinterpret_cast<const uint4 *>(rp + REC + lane * 16), afu);
+            const uint2 sw = *reinterpret_cast<const uint2 *>(rp + REC + CODE + lg * 8);
+            u01 = __half22float2(*reinterpret_cast<const __half2 *>(&sw.x));
+            u23 = __half22float2(*reinterpret_cast<const __half2 *>(&sw.y));
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            uint4 bf;
+            if (NT == 1) {
+                bf = lg < M ? act4[jb * 4 * M + lane] : make_uint4(0u, 0u, 0u, 0u);
+            } else {
+                const uint2 raw = 8 * nt + lg < M ? act2[jb * 4 * M + 32 * nt + lane] : make_uint2(0u, 0u);
+                bf = b_frag_from_raw<QT>(raw);
+            }
+            const float4 mt = meta4[(jb * NT + nt) * 4 + lc];  // corr(p), d_a(p), corr(p+1), d_a(p+1); p = 8nt+2c
+            const float2 corr = make_float2(mt.x, mt.z);
+            float d[2][4];
+            record_dots(af, bf, corr, d);
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const float2 w = t ? w23 : w01;
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    acc[nt][t][e] = __fmaf_rn(d[t][e], __fmul_rn((e >> 1) ? w.y : w.x, (e & 1) ? mt.w : mt.y),
+                                              acc[nt][t][e]);
+            }
+            if (PAIR) {
+                record_dots(afu, bf, corr, d);
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    const float2 w = t ? u23 : u01;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        accu[PAIR ? nt : 0][t][e] = __fmaf_rn(
+                            d[t][e], __fmul_rn((e >> 1) ? w.y : w.x, (e & 1) ? mt.w : mt.y), accu[PAIR ? nt : 0][t][e]);
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// consumers: one matmul phase.  `it` counts ring stages, `pk` pieces (their
+// partial-sum slots), `act_it` activation copies, all over the whole launch.
+// Returns false, the same on every consumer, when the phase was abandoned.
 // ---------------------------------------------------------------------------
 template <int QT, int PAIR, int NT>
-__device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t &it, CtaShared &cs) {
-    constexpr int REC = QT == SD_Q8_0 ? 1088 : 576;  // bytes of one 32-row record
-    constexpr int CODE = QT == SD_Q8_0 ? 1024 : 512; // code bytes of a record
+__device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t &it, uint32_t &pk, uint32_t &act_it,
+                                     CtaShared &cs) {
     constexpr int ROWS = PAIR ? 64 : 32;
-    constexpr int MT = 8 * NT;  // position slots
     const int M = a.M;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int lg = lane >> 2, lc = lane & 3;
-    uint4 *bsm = sm.bsm;
-    uint2 *bsm8 = sm.bsm8;
-    float *meta = sm.meta;
-    float *red = sm.red;
-
     const int64_t lo = static_cast<int64_t>(blockIdx.x) * a.W / a.G;
     const int64_t hi = static_cast<int64_t>(blockIdx.x + 1) * a.W / a.G;
     int cur_s = -1;
-    int st_cur = -1, st_n = 0;  // head: current statistics tile, tiles finished in it (same on all threads)
+    bool ok = true;         // this warp's waits have all succeeded
+    bool act_pending = false;  // thread 0: an activation copy may still be in flight
     int64_t g = lo;
     while (g < hi) {
-        // launch-wide self-check: thread 0 decides, the barrier hands the answer to all.  The
-        // barrier also ends every use of the previous piece's shared data (stages, red[], B).
-        if (bar_any(1, NCW * 32, tid == 0 && out_of_time(cs, a.status, 2))) {
-            cs.abort = 1;
-            return false;
-        }
         int s, u, j0, len;
         decode_step(a, g, s, u, j0, len);
         const int j1 = static_cast<int>(j0 + (hi - g) < len ? j0 + (hi - g) : len);
 
         if (s != cur_s) {
-            // stage this split's activations straight from global memory: B operands (fp16 fragments,
-            // or raw int8 for two position tiles) and per-(block, position) {corr, d_a}
-            const int64_t K = static_cast<int64_t>(a.KB) * 32;
-            const int b0 = s * a.KBs;
-            const int nitems = len * NT * 32;
-            for (int base = tid; base < nitems; base += 4 * NCW * 32) {
-                uint2 raw[4];
-#pragma unroll
-                for (int u4 = 0; u4 < 4; ++u4) {
-                    const int c = base + u4 * NCW * 32;
-                    raw[u4] = make_uint2(0u, 0u);
-                    if (c < nitems) {
-                        const int jb = c / (NT * 32), rem = c - jb * (NT * 32), nt = rem >> 5, l = rem & 31;
-                        const int n = nt * 8 + (l >> 2);
-                        raw[u4] = b_raw(n < M ? a.q + n * K + static_cast<int64_t>(b0 + jb) * 32 : nullptr, l & 3);
-                    }
-                }
-#pragma unroll
-                for (int u4 = 0; u4 < 4; ++u4) {
-                    const int c = base + u4 * NCW * 32;
-                    if (c < nitems) {
-                        if (NT == 1) bsm[c] = b_frag_from_raw<QT>(raw[u4]);
-                        else bsm8[c] = raw[u4];
-                    }
-                }
+            // every consumer is done with the previous split's activations; agree on aborts
+            if (bar_any(BAR_CONS, CONS_THREADS, !ok || cs.abort)) {
+                cs.abort = 1;
+                if (act_pending) mbar_wait_bounded(sm.act_bar, (act_it - 1) & 1u, WAIT_NS);
+                return false;
             }
-            for (int c = tid; c < len * MT; c += NCW * 32) {
-                const int jb = c / MT, n = c - jb * MT, nt = n >> 3, p = n & 7;
-                float *mp = meta + (jb * NT + nt) * 16;
-                const bool real = n < M;
-                mp[p] = dot_corr<QT>(real ? a.q + n * K + static_cast<int64_t>(b0 + jb) * 32 : nullptr);
-                mp[8 + p] = real ? __ldcg(a.sc + static_cast<int64_t>(n) * a.KB + b0 + jb) : 0.0f;
+            if (a.af_frag) {
+                if (tid == 0) {
+                    stage_issue(a, sm, s, len);
+                    act_pending = true;
+                }
+                const bool ready = mbar_wait_bounded(sm.act_bar, act_it & 1u, WAIT_NS, &cs.abort);
+                __syncwarp();
+                if (!__all_sync(0xffffffffu, ready)) {
+                    set_status(a.status, SD_ETIMEOUT);
+                    cs.abort = 1;
+                    ok = false;
+                } else if (tid == 0) {
+                    act_pending = false;
+                }
+                ++act_it;
+                if (a.af_norm) stage_norm_scales(a, sm, cs, s, len, ok);
+            } else {
+                stage_rows<QT>(a, sm, s, len, tid);
+                named_bar_sync(BAR_CONS, CONS_THREADS);
             }
-            named_bar_sync(1, NCW * 32);
             cur_s = s;
         }
 
-        // acc[nt][t][i]: row 16t + lg + 8(i>>1), position 8nt + 2lc + (i&1); accu: the up rows
         float acc[NT][2][4], accu[PAIR ? NT : 1][2][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int t = 0; t < 2; ++t)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    acc[nt][t][i] = 0.0f;
-                    if (PAIR) accu[PAIR ? nt : 0][t][i] = 0.0f;
+                for (int e = 0; e < 4; ++e) {
+                    acc[nt][t][e] = 0.0f;
+                    accu[PAIR ? nt : 0][t][e] = 0.0f;
                 }
 
-        bool aborted = false;
+        if (ok) {
+            int late = 0;
+            if (lane == 0) late = out_of_time(cs, a.status, 2) ? 1 : 0;
+            if (__shfl_sync(0xffffffffu, late, 0)) {
+                cs.abort = 1;
+                ok = false;
+            }
+        }
         for (int jj = j0; jj < j1; jj += a.SB) {
             const int n = j1 - jj < a.SB ? j1 - jj : a.SB;
             const int stg = static_cast<int>(it % a.NS);
             const uint32_t ph = (it / a.NS) & 1u;
+            ++it;
+            if (!ok) continue;
             const bool ready = mbar_wait_bounded(&sm.full[stg], ph, WAIT_NS, &cs.abort);
-            __syncwarp();  // lanes leave the wait one by one; mma.sync below needs the warp converged
+            __syncwarp();  // lanes leave the wait one by one; mma.sync needs the warp converged
             if (!__all_sync(0xffffffffu, ready)) {
                 set_status(a.status, SD_ETIMEOUT);
                 cs.abort = 1;
-                aborted = true;
-                break;
+                ok = false;
+                continue;
             }
             const uint8_t *sbase = sm.ring + static_cast<size_t>(stg) * a.stage_stride;
-            // per round each warp takes steps r0 and r0 + NCW (for a gate|up pair, step r0's two halves)
-            constexpr int RPW = 2;
-            for (int r0 = warp; r0 < n; r0 += (PAIR ? 1 : 2) * NCW) {
-                const int r1 = r0 + NCW;
-                const int nrec = PAIR ? 2 : (1 + (r1 < n));
-                const uint8_t *rp[RPW];
-                int jbr[RPW];
+            if (n == a.SB)
+                stage_compute<QT, PAIR, NT, true>(sbase, n, jj, sm.act, sm.meta, M, warp, lane, acc, accu);
+            else
+                stage_compute<QT, PAIR, NT, false>(sbase, n, jj, sm.act, sm.meta, M, warp, lane, acc, accu);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.empty[stg]);
+        }
+
+        // hand the piece's partial sums to the finisher
+        const uint32_t b = pk % static_cast<uint32_t>(a.NRB), use = pk / static_cast<uint32_t>(a.NRB);
+        ++pk;
+        if (ok) {
+            const bool ready = mbar_wait_bounded(&sm.rempty[b], (use & 1u) ^ 1u, WAIT_NS, &cs.abort);
+            __syncwarp();
+            if (!__all_sync(0xffffffffu, ready)) {
+                set_status(a.status, SD_ETIMEOUT);
+                cs.abort = 1;
+                ok = false;
+            }
+        }
+        if (ok) {
+            float *rb = sm.red + (static_cast<size_t>(b) * NCW + warp) * M * a.rows_p;
 #pragma unroll
-                for (int q = 0; q < RPW; ++q) {
-                    if (PAIR) {
-                        rp[q] = sbase + static_cast<size_t>(r0) * a.step_bytes + q * REC;
-                        jbr[q] = jj + r0;
-                    } else {
-                        rp[q] = sbase + static_cast<size_t>(q ? r1 : r0) * a.step_bytes;
-                        jbr[q] = jj + (q ? r1 : r0);
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int t = 0; t < 2; ++t)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int m = nt * 8 + 2 * lc + (e & 1), row = 16 * t + lg + 8 * (e >> 1);
+                        if (m < M) {
+                            rb[m * a.rows_p + row] = acc[nt][t][e];
+                            if (PAIR) rb[m * a.rows_p + 32 + row] = accu[PAIR ? nt : 0][t][e];
+                        }
                     }
-                }
-                uint32_t af[RPW][2][2][4];
-                float2 dwf[RPW][2];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.rfull[b]);
+        }
+        (void)ROWS;
+        g += j1 - j0;
+    }
+    if (tid == 0 && act_pending) mbar_wait_bounded(sm.act_bar, (act_it - 1) & 1u, WAIT_NS);
+    return ok && !cs.abort;
+}
+
+// ---------------------------------------------------------------------------
+// finisher warps: one matmul phase.  For each piece, in the consumers' order,
+// warp f takes positions f, f + NF, ...: add the 8 consumer warps' partial
+// sums (warp order), then finish the unit directly, or store the partial and,
+// if this CTA arrived last, add all partials in (split, piece) order and
+// finish it.  Returns false, the same on every finisher, when abandoned.
+// ---------------------------------------------------------------------------
+template <int PAIR>
+__device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &pk, CtaShared &cs, int f) {
+    constexpr int ROWS = PAIR ? 64 : 32;
+    const int M = a.M;
+    const int lane = threadIdx.x & 31;
+    const int64_t lo = static_cast<int64_t>(blockIdx.x) * a.W / a.G;
+    const int64_t hi = static_cast<int64_t>(blockIdx.x + 1) * a.W / a.G;
+    int st_cur = -1, st_n = 0;  // head: current statistics tile and tiles finished in it
+    bool ok = true;
+    int64_t g = lo;
+    while (g < hi) {
+        int s, u, j0, len;
+        decode_step(a, g, s, u, j0, len);
+        const int j1 = static_cast<int>(j0 + (hi - g) < len ? j0 + (hi - g) : len);
+        const uint32_t b = pk % static_cast<uint32_t>(a.NRB), use = pk / static_cast<uint32_t>(a.NRB);
+        ++pk;
+        g += j1 - j0;
+        const bool direct = (a.KS == 1) && (npieces(a, s, u) == 1);
+        if (ok) {
+            const bool ready = mbar_wait_bounded(&sm.rfull[b], use & 1u, WAIT_NS, &cs.abort);
+            __syncwarp();
+            if (!__all_sync(0xffffffffu, ready)) {
+                set_status(a.status, SD_ETIMEOUT);
+                cs.abort = 1;
+                ok = false;
+            }
+        }
+        // this warp's positions: the 8 consumer warps' partial sums, added in warp order
+        float v[FIN_MPW], vu[FIN_MPW];
+        if (ok) {
+            const float *rb = sm.red + static_cast<size_t>(b) * NCW * M * a.rows_p;
+            const size_t wstride = static_cast<size_t>(M) * a.rows_p;
 #pragma unroll
-                for (int q = 0; q < RPW; ++q) {
-                    if (q < nrec) {
-                        if (QT == SD_Q4_32) {
-                            q4_frag(*reinterpret_cast<const uint4 *>(rp[q] + lane * 16), af[q]);
-                        } else {
-                            q8_frag(*reinterpret_cast<const uint4 *>(rp[q] + lane * 16),
-                                    *reinterpret_cast<const uint4 *>(rp[q] + 512 + lane * 16), af[q]);
-                        }
-                        const uint2 sw = *reinterpret_cast<const uint2 *>(rp[q] + CODE + lg * 8);
-                        dwf[q][0] = __half22float2(*reinterpret_cast<const __half2 *>(&sw.x));  // rows g, g+8
-                        dwf[q][1] = __half22float2(*reinterpret_cast<const __half2 *>(&sw.y));  // rows 16+g, 24+g
-                    }
-                }
+            for (int i = 0; i < FIN_MPW; ++i) {
+                const int m = f + NF * i;
+                v[i] = vu[i] = 0.0f;
+                if (m < M) {
+                    v[i] = rb[m * a.rows_p + lane];
+                    if (PAIR) vu[i] = rb[m * a.rows_p + 32 + lane];
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    if (NT == 1 || nt * 8 < M) {
-                        float d[RPW][2][4];
-                        float2 da[RPW];
-#pragma unroll
-                        for (int q = 0; q < RPW; ++q) {
-                            if (q < nrec && (q == 0 || !PAIR)) {
-                                const int jb = jbr[q];
-                                const uint4 bf = NT == 1 ? bsm[jb * 32 + lane]
-                                                         : b_frag_from_raw<QT>(bsm8[(jb * NT + nt) * 32 + lane]);
-                                const float *mp = meta + (jb * NT + nt) * 16;
-                                const float2 corr = *reinterpret_cast<const float2 *>(mp + 2 * lc);
-                                da[q] = *reinterpret_cast<const float2 *>(mp + 8 + 2 * lc);
-                                record_dots(af[q], bf, corr, d[q]);
-                                if (PAIR) {  // the up half shares the step's activations
-                                    da[1] = da[0];
-                                    record_dots(af[1], bf, corr, d[1]);
-                                }
-                            }
-                        }
-#pragma unroll
-                        for (int q = 0; q < RPW; ++q) {
-                            if (q < nrec) {
-                                float (&ac)[2][4] = (PAIR && q == 1) ? accu[PAIR ? nt : 0] : acc[nt];
-#pragma unroll
-                                for (int t = 0; t < 2; ++t) {
-                                    const float w0 = t ? dwf[q][1].x : dwf[q][0].x;
-                                    const float w1 = t ? dwf[q][1].y : dwf[q][0].y;
-#pragma unroll
-                                    for (int i = 0; i < 4; ++i)
-                                        ac[t][i] = __fmaf_rn(d[q][t][i], __fmul_rn((i >> 1) ? w1 : w0,
-                                                                                   (i & 1) ? da[q].y : da[q].x),
-                                                             ac[t][i]);
-                                }
-                            }
-                        }
+                    for (int w2 = 1; w2 < NCW; ++w2) {
+                        v[i] = __fadd_rn(v[i], rb[w2 * wstride + m * a.rows_p + lane]);
+                        if (PAIR) vu[i] = __fadd_rn(vu[i], rb[w2 * wstride + m * a.rows_p + 32 + lane]);
                     }
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.empty[stg]);
-            ++it;
+            if (lane == 0) mbar_arrive(&sm.rempty[b]);  // the slot is free again
         }
-
-        // ---- finish the piece: add the 8 warps' partials in warp order ----
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int t = 0; t < 2; ++t)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int m = nt * 8 + 2 * lc + (i & 1), row = 16 * t + lg + 8 * (i >> 1);
-                    red[(warp * MT + m) * ROWS + row] = acc[nt][t][i];
-                    if (PAIR) red[(warp * MT + m) * ROWS + 32 + row] = accu[PAIR ? nt : 0][t][i];
-                }
-        if (bar_any(1, NCW * 32, aborted)) {
-            cs.abort = 1;
-            return false;
-        }
-
-        const bool direct = (a.KS == 1) && (npieces(a, s, u) == 1);
         bool finish = direct;
         if (!direct) {
-            const int piece = static_cast<int>(blockIdx.x) - owner_of(a, unit_start(a, s, u));
-            float *pp = a.part + ((static_cast<int64_t>(u) * a.KS + s) * a.P + piece) * (ROWS * MPAD);
-            for (int m = warp; m < M; m += NCW) {
-                float v = red[(0 * MT + m) * ROWS + lane];
-                float vu = PAIR ? red[(0 * MT + m) * ROWS + 32 + lane] : 0.0f;
+            if (ok) {
+                float *pp = a.part + ((static_cast<int64_t>(u) * a.KS + s) * a.P +
+                                      (static_cast<int>(blockIdx.x) - owner_of(a, unit_start(a, s, u)))) *
+                                         (ROWS * MPAD);
 #pragma unroll
-                for (int w2 = 1; w2 < NCW; ++w2) {
-                    v = __fadd_rn(v, red[(w2 * MT + m) * ROWS + lane]);
-                    if (PAIR) vu = __fadd_rn(vu, red[(w2 * MT + m) * ROWS + 32 + lane]);
+                for (int i = 0; i < FIN_MPW; ++i) {
+                    const int m = f + NF * i;
+                    if (m < M) {
+                        pp[m * ROWS + lane] = v[i];
+                        if (PAIR) pp[m * ROWS + 32 + lane] = vu[i];
+                    }
                 }
-                pp[m * ROWS + lane] = v;
-                if (PAIR) pp[m * ROWS + 32 + lane] = vu;
             }
-            named_bar_sync(1, NCW * 32);  // the partial sums above happen before thread 0's release
+            named_bar_sync(BAR_FIN, FIN_THREADS);  // every finisher's partial sums before the release
             bool last = false;
-            if (tid == 0) {
+            if (ok && f == 0 && lane == 0) {
                 int expected = 0;
                 for (int s2 = 0; s2 < a.KS; ++s2) expected += npieces(a, s2, u);
                 const unsigned old = atom_add_acq_rel(&a.cnt[u], 1u);
                 last = static_cast<int>(old) == expected - 1;
             }
-            finish = bar_any(1, NCW * 32, last);  // thread 0 acquired with its atomic; reads below bypass L1
-        }
-
-        if (finish) {
-            for (int m = warp; m < M; m += NCW) {
-                float v, vu = 0.0f;
-                if (direct) {
-                    v = red[(0 * MT + m) * ROWS + lane];
-                    if (PAIR) vu = red[(0 * MT + m) * ROWS + 32 + lane];
+            finish = bar_any(BAR_FIN, FIN_THREADS, last);  // the acquire above orders the loads below
+            if (finish && ok) {
 #pragma unroll
-                    for (int w2 = 1; w2 < NCW; ++w2) {
-                        v = __fadd_rn(v, red[(w2 * MT + m) * ROWS + lane]);
-                        if (PAIR) vu = __fadd_rn(vu, red[(w2 * MT + m) * ROWS + 32 + lane]);
-                    }
-                } else {
-                    v = 0.0f;
-                    bool first = true;
-                    for (int s2 = 0; s2 < a.KS; ++s2) {
-                        const int np = npieces(a, s2, u);
-                        for (int p2 = 0; p2 < np; ++p2) {
-                            const float *pp = a.part + ((static_cast<int64_t>(u) * a.KS + s2) * a.P + p2) * (ROWS * MPAD);
-                            float x = __ldcg(pp + m * ROWS + lane);
-                            float xu = PAIR ? __ldcg(pp + m * ROWS + 32 + lane) : 0.0f;
-                            if (first) {
-                                v = x;
-                                vu = xu;
-                                first = false;
-                            } else {
-                                v = __fadd_rn(v, x);
-                                if (PAIR) vu = __fadd_rn(vu, xu);
-                            }
+                for (int i = 0; i < FIN_MPW; ++i) v[i] = vu[i] = 0.0f;
+                bool first = true;
+                for (int s2 = 0; s2 < a.KS; ++s2) {
+                    const int np = npieces(a, s2, u);
+                    for (int p2 = 0; p2 < np; ++p2) {
+                        const float *q = a.part + ((static_cast<int64_t>(u) * a.KS + s2) * a.P + p2) * (ROWS * MPAD);
+                        float x[FIN_MPW], xu[FIN_MPW];
+#pragma unroll
+                        for (int i = 0; i < FIN_MPW; ++i) {  // all positions' loads in flight together
+                            const int m = f + NF * i;
+                            x[i] = m < M ? __ldcg(q + m * ROWS + lane) : 0.0f;
+                            xu[i] = (PAIR && m < M) ? __ldcg(q + m * ROWS + 32 + lane) : 0.0f;
                         }
+#pragma unroll
+                        for (int i = 0; i < FIN_MPW; ++i) {
+                            v[i] = first ? x[i] : __fadd_rn(v[i], x[i]);
+                            if (PAIR) vu[i] = first ? xu[i] : __fadd_rn(vu[i], xu[i]);
+                        }
+                        first = false;
                     }
                 }
-                epilogue<PAIR>(a, u, m, lane, v, vu);
-            }
-            if (!direct && tid == 0) a.cnt[u] = 0u;
-
-            if (a.head) {
-                // count finished tiles per 1024-token statistics tile; one counter update per
-                // (CTA, statistics tile) run, issued when the run ends
-                const int st = u / (STAT_TILE / 32);
-                if (st != st_cur) {
-                    head_flush(a, st_cur, st_n, tid, lane, warp);
-                    st_cur = st;
-                    st_n = 0;
-                }
-                ++st_n;
+                if (f == 0 && lane == 0) a.cnt[u] = 0u;
             }
         }
-        g += j1 - j0;
+        if (finish && ok) {
+#pragma unroll
+            for (int i = 0; i < FIN_MPW; ++i) {
+                const int m = f + NF * i;
+                if (m < M) epilogue<PAIR>(a, u, m, lane, v[i], vu[i]);
+            }
+        }
+        if (finish && a.head) {  // the same decisions on every finisher warp
+            const int st = u / (STAT_TILE / 32);
+            if (st != st_cur) {
+                head_flush(a, st_cur, st_n, lane, f);
+                st_cur = st;
+                st_n = 0;
+            }
+            ++st_n;
+        }
     }
-    if (a.head) head_flush(a, st_cur, st_n, tid, lane, warp);
-    return true;
+    if (a.head) head_flush(a, st_cur, st_n, lane, f);
+    return ok && !cs.abort;
 }
 
 // ---------------------------------------------------------------------------
-// consumers: RMSNorm + per-32 requantisation spread over the grid.  Every CTA
-// forms the rows' inverse RMS in the canonical order (256 strided partial sums,
-// pairwise tree), then requantises its share of the (row, block) items, one
-// warp per item -- the same operations as sd_rmsnorm_quant_acts.
+// consumers: the pass's first RMSNorm, on the input rows.  One warp per
+// 32-element block, all positions: the block's sum of squares (pairwise tree
+// over its squares) and its codes from t = x w (c = max|t| / 127), written as
+// int8 codes and as the next matmul's activation fragments holding {corr, c};
+// that matmul multiplies c by each row's inverse RMS when it stages them.
+// Later RMSNorms are formed the same way in the residual epilogues.
 // ---------------------------------------------------------------------------
-__device__ inline void norm_phase(const QmmArgs &a, const Smem &sm, CtaShared &cs) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int M = a.M;
-    const int64_t K = static_cast<int64_t>(a.KB) * 32;
-    float *part = sm.red;  // [M][256]
-    for (int m = 0; m < M; ++m) {
-        const float *xr = a.xin + m * K;
-        float s = 0.0f;
-        for (int64_t i = tid; i < K; i += 256) {
-            const float x = __ldcg(xr + i);
-            s = __fadd_rn(s, __fmul_rn(x, x));
+__device__ inline void norm_phase(const QmmArgs &a) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int M = a.M, KB = a.KB;
+    const int64_t K = static_cast<int64_t>(KB) * 32;
+    const int b0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * KB / gridDim.x);
+    const int b1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * KB / gridDim.x);
+    for (int b = b0 + warp; b < b1; b += NCW) {
+        for (int m = 0; m < M; ++m) {
+            const int64_t i = m * K + static_cast<int64_t>(b) * 32 + lane;
+            const float x = __ldcg(a.xin + i);
+            const float sq = tree32(__fmul_rn(x, x), lane);
+            if (lane == 0) a.ss[m * a.ss_ld + b] = sq;
+            float c;
+            const int v = requant_lane(__fmul_rn(x, a.norm_w[static_cast<int64_t>(b) * 32 + lane]), c);
+            a.q_next[i] = static_cast<int8_t>(v);
+            af_write(a.af_out_frag, a.af_out_meta, M, b, m, lane, v, c, a.af_out_qt);
         }
-        part[m * 256 + tid] = s;
-    }
-    named_bar_sync(1, NCW * 32);
-    for (int stride = 128; stride >= 1; stride >>= 1) {
-        if (tid < stride)
-            for (int m = 0; m < M; ++m) part[m * 256 + tid] = __fadd_rn(part[m * 256 + tid], part[m * 256 + tid + stride]);
-        named_bar_sync(1, NCW * 32);
-    }
-    if (tid < M) {
-        const float mean = __fdiv_rn(part[tid * 256], static_cast<float>(K));
-        cs.inv[tid] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, a.eps)));
-    }
-    named_bar_sync(1, NCW * 32);
-    const int64_t items = static_cast<int64_t>(M) * a.KB;
-    const int64_t i0 = static_cast<int64_t>(blockIdx.x) * items / gridDim.x;
-    const int64_t i1 = static_cast<int64_t>(blockIdx.x + 1) * items / gridDim.x;
-    for (int64_t it = i0 + warp; it < i1; it += NCW) {
-        const int m = static_cast<int>(it / a.KB);
-        const int64_t b = it - static_cast<int64_t>(m) * a.KB;
-        const float x = __ldcg(a.xin + m * K + b * 32 + lane);
-        const float y = __fmul_rn(__fmul_rn(x, cs.inv[m]), a.norm_w[b * 32 + lane]);
-        float d;
-        const int v = requant_lane(y, d);
-        a.q_next[m * K + b * 32 + lane] = static_cast<int8_t>(v);
-        if (lane == 0) a.s_next[m * a.KB + b] = d;
     }
 }
 
@@ -848,8 +1115,8 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) cta_init(sm, a.NS, cs);
     __syncthreads();
-    uint32_t it = 0;
-    if (warp == NCW) {
+    uint32_t it = 0, pk = 0, act_it = 0;
+    if (warp == PRODUCER_WARP) {
         pdl_launch_dependents();
         if (lane == 0) {
             produce_phase(a, sm, it, cs, policy_evict_first());
@@ -859,7 +1126,8 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
     }
     pdl_wait();
     pdl_launch_dependents();
-    (void)consume_phase<QT, PAIR, NT>(a, sm, it, cs);
+    if (warp >= FIN_WARP0) (void)finish_phase<PAIR>(a, sm, pk, cs, warp - FIN_WARP0);
+    else (void)consume_phase<QT, PAIR, NT>(a, sm, it, pk, act_it, cs);
 }
 
 // ---------------------------------------------------------------------------
@@ -889,8 +1157,8 @@ __global__ void __launch_bounds__(QMM_THREADS, 1)
     int *status = a0.status;
     if (tid == 0) cta_init(sm, a0.NS, cs);
     __syncthreads();
-    uint32_t it = 0;
-    if (warp == NCW) {
+    uint32_t it = 0, pk = 0, act_it = 0;
+    if (warp == PRODUCER_WARP) {
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
             for (int p = 0; p < n_phases && !cs.abort; ++p)
@@ -912,30 +1180,36 @@ __global__ void __launch_bounds__(QMM_THREADS, 1)
                 }
             }
         }
-        {  // copy the phase descriptor into shared memory (constant: may overlap the barrier wait)
+        if (warp < NCW) {  // copy the phase descriptor into shared memory (constant: may overlap the wait)
             const uint32_t *src = reinterpret_cast<const uint32_t *>(phases + p);
             uint32_t *dst = reinterpret_cast<uint32_t *>(&sa);
-            for (int i = tid; i < static_cast<int>(sizeof(QmmArgs) / 4); i += NCW * 32) dst[i] = src[i];
+            for (int i = tid; i < static_cast<int>(sizeof(QmmArgs) / 4); i += CONS_THREADS) dst[i] = src[i];
         }
-        if (bar_any(1, NCW * 32, stop)) {
+        if (bar_any(BAR_WORK, WORK_THREADS, stop)) {
             cs.abort = 1;
             return;
         }
         bool ok = true;
         if (sa.kind == KIND_NORM) {
-            norm_phase(sa, sm, cs);
+            if (warp < NCW) norm_phase(sa);
         } else if (sa.kind == KIND_ACCEPT) {
             if (blockIdx.x == 0 && tid == 0)
                 greedy_accept(sa.argmax, sa.tokens, sa.parent, sa.M, sa.out_tokens, sa.out_count);
+        } else if (warp >= FIN_WARP0) {
+            const int f = warp - FIN_WARP0;
+            ok = sa.pair ? finish_phase<1>(sa, sm, pk, cs, f) : finish_phase<0>(sa, sm, pk, cs, f);
         } else if (sa.qt == SD_Q4_32 && sa.pair) {
-            ok = consume_phase<SD_Q4_32, 1, NT>(sa, sm, it, cs);
+            ok = consume_phase<SD_Q4_32, 1, NT>(sa, sm, it, pk, act_it, cs);
         } else if (sa.qt == SD_Q4_32) {
-            ok = consume_phase<SD_Q4_32, 0, NT>(sa, sm, it, cs);
+            ok = consume_phase<SD_Q4_32, 0, NT>(sa, sm, it, pk, act_it, cs);
         } else {
-            ok = consume_phase<SD_Q8_0, 0, NT>(sa, sm, it, cs);
+            ok = consume_phase<SD_Q8_0, 0, NT>(sa, sm, it, pk, act_it, cs);
         }
-        if (!ok) return;  // uniform; cs.abort already stops the producer
-        named_bar_sync(1, NCW * 32);  // this CTA's writes of phase p before thread 0's release
+        // every write of phase p (consumers and finisher) before thread 0's release
+        if (bar_any(BAR_WORK, WORK_THREADS, !ok)) {
+            cs.abort = 1;
+            return;
+        }
         if (tid == 0) red_release_add(barrier_ctr, 1u);
     }
 }
@@ -944,7 +1218,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1)
 // host side: plan + launch
 // ---------------------------------------------------------------------------
 struct QmmPlan {
-    int32_t KB, NU, KS, KBs, KBlast, G, P, SB, NS;
+    int32_t KB, NU, KS, KBs, KBlast, G, P, SB, NS, NRB, rows_p;
     int64_t W;
     uint32_t step_bytes;
     size_t ws_part, ws_cnt, ws_stats, ws_total;
@@ -974,6 +1248,8 @@ inline bool make_plan(int qtype, int64_t n_out, int64_t k_in, bool pair, bool he
     p.step_bytes = static_cast<uint32_t>(rec * (pair ? 2 : 1));
     p.SB = 0;
     p.NS = 0;
+    p.NRB = 0;
+    p.rows_p = 0;
     const int rows = pair ? 64 : 32;
     // counters first, at fixed offsets shared by every call: units [0, WS_UNIT_CNT), statistics
     // tiles [WS_UNIT_CNT, WS_UNIT_CNT + WS_STAT_CNT), the statistics "done" counter after them.
@@ -991,35 +1267,47 @@ inline bool make_plan(int qtype, int64_t n_out, int64_t k_in, bool pair, bool he
 // steps per stage (~18 KB stages): 32 records of 4-bit, 16 gate|up pairs, 16 Q8_0 records
 inline int stage_steps(int qtype, bool pair) { return pair ? 2 * NCW : (qtype == SD_Q8_0 ? 2 * NCW : 4 * NCW); }
 
-// Shared-memory layout for splits of up to `kbs` blocks, NT 8-position tiles, `rows` output
-// rows per unit (64 with a gate|up pair) and ring slots of `slot` bytes; returns total bytes.
-inline size_t layout_smem(int kbs, int NT, int rows, size_t slot, int &NS, uint32_t &off_ring, uint32_t &off_act,
-                          uint32_t &off_meta, uint32_t &off_red) {
-    const size_t act = static_cast<size_t>(kbs) * (NT == 1 ? 512 : 2 * 256);  // fp16 or raw int8 fragments
-    const size_t meta = static_cast<size_t>(kbs) * NT * 64;                  // corr + d_a per position
-    const size_t red = static_cast<size_t>(NCW) * 8 * NT * rows * 4;
-    const size_t fixed = 256 + act + meta + red + 3 * 128;
+struct SmemLayout {
+    int NS, NRB, rows_p;
+    uint32_t off_ring, off_act, off_meta, off_red, off_ss;
+    size_t total;
+};
+
+
+// Shared memory for splits of up to `kbs` blocks, M positions, `rows` output rows per unit (64
+// with a gate|up pair), ring slots of `slot` bytes and `ss` bytes of block sums of squares.
+// Returns false when not even two ring stages fit.
+inline bool layout_smem(int kbs, int M, int rows, size_t slot, size_t ss, SmemLayout &L) {
+    const size_t act = static_cast<size_t>(kbs) * af_frag_bytes(M);
+    const size_t meta = static_cast<size_t>(kbs) * af_meta_bytes(M);
+    L.rows_p = rows + 4;
+    L.NRB = M <= 8 ? 2 : 1;
+    const size_t red = static_cast<size_t>(L.NRB) * NCW * M * L.rows_p * sizeof(float);
+    const size_t fixed = HDR_BYTES + act + meta + red + ss + 4 * 128;
     const size_t budget = 222 * 1024;
-    int ns = fixed + 2 * slot <= budget ? static_cast<int>((budget - fixed) / slot) : 2;
-    if (ns > 12) ns = 12;
-    NS = ns;
-    off_ring = 256;
-    off_act = static_cast<uint32_t>(align_up(off_ring + ns * slot, 128));
-    off_meta = static_cast<uint32_t>(align_up(off_act + act, 128));
-    off_red = static_cast<uint32_t>(align_up(off_meta + meta, 128));
-    return align_up(off_red + red, 128);
+    if (fixed + 2 * slot > budget) return false;
+    int ns = static_cast<int>((budget - fixed) / slot);
+    if (ns > MAX_NS) ns = MAX_NS;
+    L.NS = ns;
+    L.off_ring = HDR_BYTES;
+    L.off_act = static_cast<uint32_t>(align_up(L.off_ring + ns * slot, 128));
+    L.off_meta = static_cast<uint32_t>(align_up(L.off_act + act, 128));
+    L.off_red = static_cast<uint32_t>(align_up(L.off_meta + meta, 128));
+    L.off_ss = static_cast<uint32_t>(align_up(L.off_red + red, 128));
+    L.total = align_up(L.off_ss + ss, 128);
+    return true;
 }
 
-// single-operation layout
-inline size_t plan_smem(QmmPlan &p, int NT, bool pair, uint32_t &off_ring, uint32_t &off_act, uint32_t &off_meta,
-                        uint32_t &off_red, uint32_t &off_tmp) {
-    p.SB = stage_steps(p.step_bytes == 1088 ? SD_Q8_0 : SD_Q4_32, pair);
-    int ns = 0;
-    const size_t total = layout_smem(p.KBs, NT, pair ? 64 : 32, static_cast<size_t>(p.SB) * p.step_bytes, ns, off_ring,
-                                     off_act, off_meta, off_red);
-    p.NS = ns;
-    off_tmp = 0;
-    return total;
+inline void apply_layout(QmmArgs &a, const SmemLayout &L, size_t slot) {
+    a.NS = L.NS;
+    a.NRB = L.NRB;
+    a.rows_p = L.rows_p;
+    a.off_ring = L.off_ring;
+    a.off_act = L.off_act;
+    a.off_meta = L.off_meta;
+    a.off_red = L.off_red;
+    a.off_ss = L.off_ss;
+    a.stage_stride = static_cast<uint32_t>(slot);
 }
 
 template <int QT, int PAIR, int NT>
@@ -1030,8 +1318,24 @@ cudaError_t qmm_launch(QmmArgs a, size_t smem, cudaStream_t s) {
     return launch(k, dim3(a.G), dim3(QMM_THREADS), smem, s, a);
 }
 
-// dispatch on M: one 8-position tile for M <= 8, two above
+// Lays out shared memory for one single-operation call and launches it (one 8-position tile
+// for M <= 8, two above).  Returns cudaErrorInvalidValue when the layout does not fit.
 template <int QT, int PAIR>
-cudaError_t qmm_dispatch(QmmArgs a, QmmPlan &p, cudaStream_t s);
+cudaError_t qmm_dispatch(QmmArgs a, QmmPlan &p, cudaStream_t s) {  // instantiated in sdv_qmm_q4*.cu, sdv_qmm_q8.cu
+    p.SB = stage_steps(QT, PAIR != 0);
+    const size_t slot = static_cast<size_t>(p.SB) * p.step_bytes;
+    SmemLayout L;
+    if (!layout_smem(p.KBs, a.M, PAIR ? 64 : 32, slot, 0, L)) return cudaErrorInvalidValue;
+    a.SB = p.SB;
+    apply_layout(a, L, slot);
+    a.kind = KIND_MATMUL;
+    a.qt = QT;
+    a.pair = PAIR;
+    return af_nt(a.M) == 1 ? qmm_launch<QT, PAIR, 1>(a, L.total, s) : qmm_launch<QT, PAIR, 2>(a, L.total, s);
+}
+
+extern template cudaError_t qmm_dispatch<SD_Q4_32, 0>(QmmArgs, QmmPlan &, cudaStream_t);
+extern template cudaError_t qmm_dispatch<SD_Q4_32, 1>(QmmArgs, QmmPlan &, cudaStream_t);
+extern template cudaError_t qmm_dispatch<SD_Q8_0, 0>(QmmArgs, QmmPlan &, cudaStream_t);
 
 }  // namespace sdv
