@@ -166,8 +166,8 @@ sd_status sd_qmatmul_multipos(int qtype, const void *w, int64_t n_out, int64_t k
  * its launch, so no state carries over between calls, including after
  * SD_ETIMEOUT.  Calls whose workspace (sd_qmatmul_workspace_bytes) exceeds
  * SD_NOALLOC_SCRATCH_BYTES are rejected with SD_EUNSUPPORTED before anything
- * is launched (the 27B-shaped layer projections fit; a full-vocabulary head
- * does not).  All calls share the one scratch array: calls that may overlap
+ * is launched (every 27B-shaped projection fits; a 65536 x 17408 one does
+ * not).  All calls share the one scratch array: calls that may overlap
  * on the device (different streams, or several host threads) race on it and
  * must be ordered by the caller.
  */

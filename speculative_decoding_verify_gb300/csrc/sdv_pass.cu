@@ -161,6 +161,8 @@ sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, 
         a.W = p.W;
         a.G = p.G;
         a.P = p.P;
+        a.D = p.D;
+        a.R = p.R;
         a.step_bytes = p.step_bytes;
         a.SB = stage_steps(qt, pair);
         a.w = static_cast<const uint8_t *>(w);

@@ -2,16 +2,21 @@
 // all M verify positions), with the requantising, SiLU*mul, residual and head
 // epilogues, and the persistent verify pass built from the same pieces.
 //
-// Work decomposition ("stream-K"): the weights of a matrix are 32-row tiles
-// (or gate|up tile pairs) x k-blocks.  The k range is cut into KS splits of at
+// Work decomposition: the weights of a matrix are 32-row tiles (or gate|up
+// tile pairs; "units") x k-blocks.  The k range is cut into KS splits of at
 // most 160 blocks so the activations of one split fit in shared memory.  Steps
 // (one record of 32 rows x 32 weights, or a gate|up pair of records) are
-// ordered (split, unit, block) and every CTA of a grid of min(#SMs, steps)
-// CTAs takes one contiguous, equal share.  A unit whose steps all fall in one
-// CTA is finished directly; otherwise each CTA writes its partial sums to the
-// workspace and the last one to arrive adds them in (split, piece) order.
-// All of this depends on (n_out, k_in, SM count) only, never on M, which
-// makes every output row bit-identical whatever the number of positions.
+// shared out over a grid of min(#SMs, steps) CTAs in equal parts:
+//  * with one split and at least as many units as CTAs, each CTA takes D =
+//    NU / G whole units, and the R = NU - D G units left over are shared
+//    stream-K (each CTA a contiguous equal run of their unit-major steps); a
+//    CTA works its shared run first and its whole units last;
+//  * otherwise every step is shared stream-K in (split, unit, block) order.
+// A unit-split whose steps fall in one CTA is finished directly; otherwise
+// each CTA writes its partial sums to the workspace and the last one to
+// arrive adds them in (split, piece) order.  All of this depends on (n_out,
+// k_in, SM count) only, never on M, which makes every output row
+// bit-identical whatever the number of positions.
 //
 // Inside a CTA three roles run concurrently:
 //  * warp 8 (one elected lane) streams records with TMA bulk copies into a
@@ -90,6 +95,7 @@ struct QmmArgs {
     int64_t W;           // total steps
     int32_t G;           // CTAs
     int32_t P;           // max pieces per (unit, split)
+    int32_t D, R;        // whole units per CTA and units shared stream-K (D = 0: all shared)
     int32_t SB;          // steps per stage
     int32_t NS;          // stages
     uint32_t step_bytes; // bytes of one step
@@ -167,15 +173,75 @@ __device__ __forceinline__ int64_t unit_start(const QmmArgs &a, int s, int u) {
     return static_cast<int64_t>(a.NU) * a.KBs * s + static_cast<int64_t>(u) * len;
 }
 
-// CTA owning step x: largest c with floor(c W / G) <= x
-__device__ __forceinline__ int owner_of(const QmmArgs &a, int64_t x) {
-    return static_cast<int>(((x + 1) * a.G - 1) / a.W);
+// length of the shared stream-K step sequence
+__device__ __forceinline__ int64_t seq_len(const QmmArgs &a) { return a.D > 0 ? static_cast<int64_t>(a.R) * a.KB : a.W; }
+
+// CTA owning step x of the shared sequence: largest c with floor(c wseq / G) <= x
+__device__ __forceinline__ int seq_owner(const QmmArgs &a, int64_t wseq, int64_t x) {
+    return wseq > 0 ? static_cast<int>(((x + 1) * a.G - 1) / wseq) : 0;
 }
 
-__device__ __forceinline__ int npieces(const QmmArgs &a, int s, int u) {
-    int len = (s == a.KS - 1) ? a.KBlast : a.KBs;
-    int64_t st = unit_start(a, s, u);
-    return owner_of(a, st + len - 1) - owner_of(a, st) + 1;
+// CTAs sharing split s of unit u, and the first of them
+__device__ __forceinline__ void unit_split_owners(const QmmArgs &a, int s, int u, int &first, int &np) {
+    const int64_t wseq = seq_len(a);
+    int64_t st;
+    int len;
+    if (a.D > 0) {
+        st = static_cast<int64_t>(u) * a.KB;
+        len = a.KB;
+    } else {
+        st = unit_start(a, s, u);
+        len = (s == a.KS - 1) ? a.KBlast : a.KBs;
+    }
+    first = seq_owner(a, wseq, st);
+    np = seq_owner(a, wseq, st + len - 1) - first + 1;
+}
+
+// One piece of a CTA's work: blocks [j0, j1) of split s of unit u, shared by np CTAs from `first` on.
+struct Piece {
+    int s, u, j0, j1, first, np;
+};
+
+struct PieceIter {
+    int64_t g, hi;      // cursor in the shared step sequence
+    int d_next, d_end;  // whole units still to take
+};
+
+__device__ __forceinline__ void pieces_begin(const QmmArgs &a, PieceIter &it) {
+    const int64_t c = blockIdx.x, wseq = seq_len(a);
+    it.g = c * wseq / a.G;
+    it.hi = (c + 1) * wseq / a.G;
+    it.d_next = a.D > 0 ? a.R + static_cast<int>(c) * a.D : 0;
+    it.d_end = a.D > 0 ? it.d_next + a.D : 0;
+}
+
+// The next piece in processing order (shared run first, whole units last); false when done.
+__device__ __forceinline__ bool pieces_next(const QmmArgs &a, PieceIter &it, Piece &p) {
+    if (it.g < it.hi) {
+        int len;
+        if (a.D > 0) {
+            p.s = 0;
+            len = a.KB;
+            p.u = static_cast<int>(it.g / a.KB);
+            p.j0 = static_cast<int>(it.g - static_cast<int64_t>(p.u) * a.KB);
+        } else {
+            decode_step(a, it.g, p.s, p.u, p.j0, len);
+        }
+        p.j1 = static_cast<int>(p.j0 + (it.hi - it.g) < len ? p.j0 + (it.hi - it.g) : len);
+        it.g += p.j1 - p.j0;
+        unit_split_owners(a, p.s, p.u, p.first, p.np);
+        return true;
+    }
+    if (it.d_next < it.d_end) {
+        p.s = 0;
+        p.u = it.d_next++;
+        p.j0 = 0;
+        p.j1 = a.KB;
+        p.first = blockIdx.x;
+        p.np = 1;
+        return true;
+    }
+    return false;
 }
 
 // ---------------------------------------------------------------------------
@@ -360,7 +426,7 @@ __device__ __forceinline__ float tree32(float x, int lane) {
 // epilogue of one finished (unit, position), run by the finisher warp: lane = row
 // ---------------------------------------------------------------------------
 template <int PAIR>
-__device__ __forceinline__ void epilogue(const QmmArgs &a, int u, int m, int lane, float v, float vu) {
+__device__ __forceinline__ void epilogue(const QmmArgs &a, int u, int m, int lane, float v, float vu, float res, float nw) {
     if (PAIR) {
         const int64_t F = a.n_out / 2;
         const int64_t n = static_cast<int64_t>(u) * 32 + lane;  // F % 32 == 0 is required
@@ -377,7 +443,7 @@ __device__ __forceinline__ void epilogue(const QmmArgs &a, int u, int m, int lan
     } else {
         const int64_t n = static_cast<int64_t>(u) * 32 + lane;
         const bool ok = n < a.n_out;
-        if (ok && a.residual) v = __fadd_rn(v, __ldcg(a.residual + m * a.n_out + n));
+        if (ok && a.residual) v = __fadd_rn(v, res);
         if (ok && a.y) a.y[m * a.n_out + n] = v;
         if (a.ss) {  // n_out % 32 == 0 is required here
             const float s = tree32(__fmul_rn(v, v), lane);
@@ -385,7 +451,7 @@ __device__ __forceinline__ void epilogue(const QmmArgs &a, int u, int m, int lan
         }
         if (a.norm_next) {  // codes of the next RMSNorm from t = v w; its scale waits for inv
             float c;
-            const int code = requant_lane(__fmul_rn(v, __ldg(a.norm_next + n)), c);
+            const int code = requant_lane(__fmul_rn(v, nw), c);
             a.q_next[m * a.nq + n] = static_cast<int8_t>(code);
             af_write(a.af_out_frag, a.af_out_meta, a.M, u, m, lane, code, c, a.af_out_qt);
         }
@@ -580,14 +646,12 @@ __device__ __forceinline__ void cta_init(const Smem &sm, int NS, CtaShared &cs) 
 // `it` counts stages over the whole launch (slot it % NS, phase parity it / NS).
 // ---------------------------------------------------------------------------
 __device__ inline void produce_phase(const QmmArgs &a, const Smem &sm, uint32_t &it, CtaShared &cs, uint64_t pol) {
-    const int64_t lo = static_cast<int64_t>(blockIdx.x) * a.W / a.G;
-    const int64_t hi = static_cast<int64_t>(blockIdx.x + 1) * a.W / a.G;
-    int64_t g = lo;
-    while (g < hi && !cs.abort) {
-        int s, u, j0, len;
-        decode_step(a, g, s, u, j0, len);
-        const int j1 = static_cast<int>(j0 + (hi - g) < len ? j0 + (hi - g) : len);
-        for (int jj = j0; jj < j1 && !cs.abort; jj += a.SB) {
+    PieceIter pit;
+    pieces_begin(a, pit);
+    Piece pc;
+    while (!cs.abort && pieces_next(a, pit, pc)) {
+        const int s = pc.s, u = pc.u, j1 = pc.j1;
+        for (int jj = pc.j0; jj < j1 && !cs.abort; jj += a.SB) {
             const int n = j1 - jj < a.SB ? j1 - jj : a.SB;
             const int stg = static_cast<int>(it % a.NS);
             const uint32_t ph = (it / a.NS) & 1u;
@@ -607,7 +671,6 @@ __device__ inline void produce_phase(const QmmArgs &a, const Smem &sm, uint32_t 
             bulk_g2s(sm.ring + static_cast<size_t>(stg) * a.stage_stride, src, bytes, &sm.full[stg], pol);
             ++it;
         }
-        g += j1 - j0;
     }
 }
 
@@ -661,7 +724,10 @@ __device__ inline void stage_norm_scales(const QmmArgs &a, const Smem &sm, CtaSh
     named_bar_sync(BAR_CONS, CONS_THREADS);
     if (ok) {
         const int b0 = s * a.KBs;
-        const bool writer = a.s_norm_out && static_cast<int>(blockIdx.x) == owner_of(a, unit_start(a, s, 0));
+        // the CTA holding the split's first step: CTA 0 with one split (whole units or a shared run)
+        int first = 0, np = 1;
+        if (a.D == 0) unit_split_owners(a, s, 0, first, np);
+        const bool writer = a.s_norm_out && static_cast<int>(blockIdx.x) == first;
         float2 *mp = reinterpret_cast<float2 *>(sm.meta);
         for (int it = tid; it < len * M; it += CONS_THREADS) {
             const int jb = it / M, m = it - jb * M;
@@ -796,16 +862,15 @@ __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
     const int M = a.M;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int lg = lane >> 2, lc = lane & 3;
-    const int64_t lo = static_cast<int64_t>(blockIdx.x) * a.W / a.G;
-    const int64_t hi = static_cast<int64_t>(blockIdx.x + 1) * a.W / a.G;
     int cur_s = -1;
     bool ok = true;         // this warp's waits have all succeeded
     bool act_pending = false;  // thread 0: an activation copy may still be in flight
-    int64_t g = lo;
-    while (g < hi) {
-        int s, u, j0, len;
-        decode_step(a, g, s, u, j0, len);
-        const int j1 = static_cast<int>(j0 + (hi - g) < len ? j0 + (hi - g) : len);
+    PieceIter pit;
+    pieces_begin(a, pit);
+    Piece pc;
+    while (pieces_next(a, pit, pc)) {
+        const int s = pc.s, j0 = pc.j0, j1 = pc.j1;
+        const int len = (s == a.KS - 1) ? a.KBlast : a.KBs;
 
         if (s != cur_s) {
             // every consumer is done with the previous split's activations; agree on aborts
@@ -909,7 +974,6 @@ __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
             if (lane == 0) mbar_arrive(&sm.rfull[b]);
         }
         (void)ROWS;
-        g += j1 - j0;
     }
     if (tid == 0 && act_pending) mbar_wait_bounded(sm.act_bar, (act_it - 1) & 1u, WAIT_NS);
     return ok && !cs.abort;
@@ -927,19 +991,28 @@ __device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &
     constexpr int ROWS = PAIR ? 64 : 32;
     const int M = a.M;
     const int lane = threadIdx.x & 31;
-    const int64_t lo = static_cast<int64_t>(blockIdx.x) * a.W / a.G;
-    const int64_t hi = static_cast<int64_t>(blockIdx.x + 1) * a.W / a.G;
     int st_cur = -1, st_n = 0;  // head: current statistics tile and tiles finished in it
     bool ok = true;
-    int64_t g = lo;
-    while (g < hi) {
-        int s, u, j0, len;
-        decode_step(a, g, s, u, j0, len);
-        const int j1 = static_cast<int>(j0 + (hi - g) < len ? j0 + (hi - g) : len);
+    PieceIter pit;
+    pieces_begin(a, pit);
+    Piece pc;
+    while (pieces_next(a, pit, pc)) {
+        const int s = pc.s, u = pc.u;
         const uint32_t b = pk % static_cast<uint32_t>(a.NRB), use = pk / static_cast<uint32_t>(a.NRB);
         ++pk;
-        g += j1 - j0;
-        const bool direct = (a.KS == 1) && (npieces(a, s, u) == 1);
+        const bool direct = (a.KS == 1) && (pc.np == 1);
+        // values the epilogue will need, loaded before the wait: residual and next-norm weights
+        float res[FIN_MPW], nw = 0.0f;
+        if (!PAIR) {
+            const int64_t n = static_cast<int64_t>(u) * 32 + lane;
+            const bool nok = n < a.n_out;
+#pragma unroll
+            for (int i = 0; i < FIN_MPW; ++i) {
+                const int m = f + NF * i;
+                res[i] = (a.residual && nok && m < M) ? __ldcg(a.residual + m * a.n_out + n) : 0.0f;
+            }
+            if (a.norm_next && nok) nw = __ldg(a.norm_next + n);
+        }
         if (ok) {
             const bool ready = mbar_wait_bounded(&sm.rfull[b], use & 1u, WAIT_NS, &cs.abort);
             __syncwarp();
@@ -974,8 +1047,7 @@ __device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &
         bool finish = direct;
         if (!direct) {
             if (ok) {
-                float *pp = a.part + ((static_cast<int64_t>(u) * a.KS + s) * a.P +
-                                      (static_cast<int>(blockIdx.x) - owner_of(a, unit_start(a, s, u)))) *
+                float *pp = a.part + ((static_cast<int64_t>(u) * a.KS + s) * a.P + (static_cast<int>(blockIdx.x) - pc.first)) *
                                          (ROWS * MPAD);
 #pragma unroll
                 for (int i = 0; i < FIN_MPW; ++i) {
@@ -990,7 +1062,11 @@ __device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &
             bool last = false;
             if (ok && f == 0 && lane == 0) {
                 int expected = 0;
-                for (int s2 = 0; s2 < a.KS; ++s2) expected += npieces(a, s2, u);
+                for (int s2 = 0; s2 < a.KS; ++s2) {
+                    int f2, np2;
+                    unit_split_owners(a, s2, u, f2, np2);
+                    expected += np2;
+                }
                 const unsigned old = atom_add_acq_rel(&a.cnt[u], 1u);
                 last = static_cast<int>(old) == expected - 1;
             }
@@ -1000,7 +1076,8 @@ __device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &
                 for (int i = 0; i < FIN_MPW; ++i) v[i] = vu[i] = 0.0f;
                 bool first = true;
                 for (int s2 = 0; s2 < a.KS; ++s2) {
-                    const int np = npieces(a, s2, u);
+                    int f2, np;
+                    unit_split_owners(a, s2, u, f2, np);
                     for (int p2 = 0; p2 < np; ++p2) {
                         const float *q = a.part + ((static_cast<int64_t>(u) * a.KS + s2) * a.P + p2) * (ROWS * MPAD);
                         float x[FIN_MPW], xu[FIN_MPW];
@@ -1025,7 +1102,7 @@ __device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &
 #pragma unroll
             for (int i = 0; i < FIN_MPW; ++i) {
                 const int m = f + NF * i;
-                if (m < M) epilogue<PAIR>(a, u, m, lane, v[i], vu[i]);
+                if (m < M) epilogue<PAIR>(a, u, m, lane, v[i], vu[i], res[i], nw);
             }
         }
         if (finish && a.head) {  // the same decisions on every finisher warp
@@ -1218,7 +1295,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1)
 // host side: plan + launch
 // ---------------------------------------------------------------------------
 struct QmmPlan {
-    int32_t KB, NU, KS, KBs, KBlast, G, P, SB, NS, NRB, rows_p;
+    int32_t KB, NU, KS, KBs, KBlast, G, P, D, R, SB, NS, NRB, rows_p;
     int64_t W;
     uint32_t step_bytes;
     size_t ws_part, ws_cnt, ws_stats, ws_total;
@@ -1241,10 +1318,15 @@ inline bool make_plan(int qtype, int64_t n_out, int64_t k_in, bool pair, bool he
     p.KBlast = p.KB - p.KBs * (p.KS - 1);
     p.W = static_cast<int64_t>(p.NU) * (static_cast<int64_t>(p.KBs) * (p.KS - 1) + p.KBlast);
     p.G = static_cast<int32_t>(p.W < sms ? p.W : sms);
-    const int64_t qmin = p.W / p.G;
-    int64_t P = (static_cast<int64_t>(p.KBs) - 1) / qmin + 2;
+    // whole units per CTA when there is one split and at least one unit per CTA; the rest shared
+    p.D = (p.KS == 1 && p.NU >= p.G) ? p.NU / p.G : 0;
+    p.R = p.D > 0 ? p.NU - p.D * p.G : 0;
+    const int64_t wseq = p.D > 0 ? static_cast<int64_t>(p.R) * p.KB : p.W;
+    const int64_t qmin = wseq / p.G;
+    int64_t P = qmin > 0 ? (static_cast<int64_t>(p.KBs) - 1) / qmin + 2 : p.KBs;
     if (P > p.KBs) P = p.KBs;
     p.P = static_cast<int32_t>(P);
+    const int64_t shared_units = p.D > 0 ? p.R : p.NU;  // units that may need partial sums
     p.step_bytes = static_cast<uint32_t>(rec * (pair ? 2 : 1));
     p.SB = 0;
     p.NS = 0;
@@ -1258,7 +1340,7 @@ inline bool make_plan(int qtype, int64_t n_out, int64_t k_in, bool pair, bool he
     const int64_t nst = (n_out + STAT_TILE - 1) / STAT_TILE;
     if (head && nst > WS_STAT_CNT) return false;
     p.ws_cnt = WS_CNT_BYTES;
-    p.ws_part = align_up(static_cast<size_t>(p.NU) * p.KS * p.P * rows * MPAD * sizeof(float), 256);
+    p.ws_part = align_up(static_cast<size_t>(shared_units) * p.KS * p.P * rows * MPAD * sizeof(float), 256);
     p.ws_stats = head ? align_up(static_cast<size_t>(nst) * MPAD * sizeof(float4), 256) : 0;
     p.ws_total = p.ws_part + p.ws_cnt + p.ws_stats;
     return true;

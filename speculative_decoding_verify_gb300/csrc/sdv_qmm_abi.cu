@@ -54,6 +54,8 @@ static void fill_plan(QmmArgs &a, const QmmPlan &p) {
     a.W = p.W;
     a.G = p.G;
     a.P = p.P;
+    a.D = p.D;
+    a.R = p.R;
     a.step_bytes = p.step_bytes;
 }
 

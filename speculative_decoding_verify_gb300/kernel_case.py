@@ -4,8 +4,9 @@
 
 Cases: qkv (4-bit 5120->15360, requant epilogue), o (4-bit 5120->5120 + residual),
 gate_up (4-bit 5120->2x17408, SiLU*mul requant), down (4-bit 17408->5120 + residual),
-head (Q8_0 5120->151936 with argmax/statistics), rmsnorm (M x 5120).  Prints the
-mean event-timed duration per launch and the weight-stream GB/s.
+head (Q8_0 5120->151936 with argmax/statistics), rmsnorm (M x 5120), and pass:
+the one-launch verify pass over --layers 27B-shaped 4-bit layers plus the head.
+Prints the mean event-timed duration per launch and the weight-stream GB/s.
 """
 from __future__ import annotations
 
@@ -36,14 +37,36 @@ CASES = {
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--case", default="gate_up", choices=list(CASES) + ["rmsnorm"])
+    ap.add_argument("--case", default="gate_up", choices=list(CASES) + ["rmsnorm", "pass"])
+    ap.add_argument("--layers", type=int, default=4)
     ap.add_argument("--M", type=int, default=5)
     ap.add_argument("--reps", type=int, default=3)
     a = ap.parse_args()
     sdv.lib()
     M = a.M
     dev = "cuda"
-    if a.case == "rmsnorm":
+    if a.case == "pass":
+        from speculative_decoding_verify_gb300.verify_pass import VerifyStack, repack_matrix
+        spec = sdgen.StackSpec(layers=a.layers, hidden=H, ffn=F, vocab=V, seed=0)
+        layers, norms = [], []
+        for l in range(a.layers):
+            lw = {}
+            for name, n, k in spec.matrices():
+                blocks = sdgen.pinned_quantized_normal(spec.wq, spec.weight_key(l, name), n, k)
+                lw[name] = repack_matrix(spec.wq, blocks, n, k, pair=(name == "gate_up"), device=dev)
+            layers.append(lw)
+            norms.append(tuple(torch.from_numpy(x).to(dev) for x in spec.norms(l)))
+        hb = sdgen.pinned_quantized_normal(spec.head_q, spec.weight_key(0, "head"), V, H)
+        head = repack_matrix(spec.head_q, hb, V, H, device=dev)
+        stack = VerifyStack(layers, norms, torch.from_numpy(spec.final_norm()).to(dev), head, H, F, V, M)
+        h0 = torch.from_numpy(spec.hidden_in(M)).to(dev)
+        stack.prepare_fused()
+
+        def run():
+            stack.h.copy_(h0)
+            stack.run_fused()
+        nbytes = spec.weight_bytes()
+    elif a.case == "rmsnorm":
         x = torch.from_numpy(sdgen.normal(sdgen.key(9, 0), (M, H))).to(dev)
         w = torch.from_numpy(sdgen.norm_weight(sdgen.key(9, 1), H)).to(dev)
         q = torch.zeros((M, H), dtype=torch.int8, device=dev)

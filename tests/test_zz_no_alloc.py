@@ -75,13 +75,13 @@ def test_noalloc_equals_workspace_call_twice(sdv, n, k, epi, col0):
 
 
 def test_noalloc_rejects_calls_beyond_its_scratch(sdv):
-    V, H, M = 151936, 5120, 5
-    assert sdv.qmatmul_workspace_bytes(oracle.Q8_0, V, H, 0) > (4 << 20)  # SD_NOALLOC_SCRATCH_BYTES
-    q = torch.zeros((M, H), dtype=torch.int8, device="cuda")
-    s = torch.zeros((M, H // 32), dtype=torch.float32, device="cuda")
+    N, K, M = 65536, 17408, 5  # four k-splits of 2048 units: about 33 MB of partial sums
+    assert sdv.qmatmul_workspace_bytes(oracle.Q4_32, N, K, 0) > (4 << 20)  # SD_NOALLOC_SCRATCH_BYTES
+    q = torch.zeros((M, K), dtype=torch.int8, device="cuda")
+    s = torch.zeros((M, K // 32), dtype=torch.float32, device="cuda")
     w = torch.zeros(16, dtype=torch.uint8, device="cuda")  # never read: the call is refused first
-    y = torch.zeros((M, V), dtype=torch.float32, device="cuda")
-    rc = sdv.lib().sd_qmatmul_multipos_noalloc(oracle.Q8_0, sdv._p(w), V, H, sdv._p(q), sdv._p(s), M, sdv._p(y),
+    y = torch.zeros((M, 16), dtype=torch.float32, device="cuda")
+    rc = sdv.lib().sd_qmatmul_multipos_noalloc(oracle.Q4_32, sdv._p(w), N, K, sdv._p(q), sdv._p(s), M, sdv._p(y),
                                                None, 0, 0, None, None, sdv._stream())
     assert rc == 2  # SD_EUNSUPPORTED
     status_ok()
