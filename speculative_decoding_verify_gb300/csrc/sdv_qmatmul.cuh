@@ -65,8 +65,10 @@ constexpr int NORM_MAX_KB = 2048;      // RMSNorm rows of at most 65536 elements
 constexpr int PASS_NORM_MAX_KB = 1024; // ... inside the verify pass (one warp's 1024-slot tree)
 
 // Shared-memory header: mbarriers at fixed offsets
-constexpr uint32_t HDR_FULL = 0, HDR_EMPTY = 8 * MAX_NS, HDR_ACT = 16 * MAX_NS, HDR_RFULL = HDR_ACT + 8,
-                   HDR_REMPTY = HDR_RFULL + 16, HDR_BYTES = 256;
+constexpr uint32_t HDR_FULL = 0, HDR_EMPTY = 8 * MAX_NS, HDR_ACT = 16 * MAX_NS, HDR_AFREE = HDR_ACT + 8,
+                   HDR_RFULL = HDR_AFREE + 8, HDR_REMPTY = HDR_RFULL + 16, HDR_FING = HDR_REMPTY + 16,
+                   HDR_FINB = HDR_FING + 8, HDR_BYTES = 256;
+static_assert(HDR_FINB + 8 <= HDR_BYTES, "mbarrier header");
 
 // ---------------------------------------------------------------------------
 // Activation fragments ("AF"): a matmul's int8 input laid out for its inner
@@ -559,39 +561,24 @@ __device__ inline void head_final_fold(const QmmArgs &a, int lane, int f) {
     }
 }
 
-// Adds `n_done` finished 32-row tiles to statistics tile `st`.  Called by every finisher warp
-// with the same arguments (barriers inside); the finished logits were written before the call.
-__device__ inline void head_flush(const QmmArgs &a, int st, int n_done, int lane, int f) {
-    if (st < 0 || n_done == 0) return;
-    named_bar_sync(BAR_FIN, FIN_THREADS);  // every finisher's logits before the release below
-    bool last = false;
-    if (f == 0 && lane == 0) {
-        const int left = a.NU - st * (STAT_TILE / 32);
-        const int tiles_in_st = left < STAT_TILE / 32 ? left : STAT_TILE / 32;
-        const unsigned old = atom_add_acq_rel(&a.st_cnt[st], static_cast<uint32_t>(n_done));
-        last = static_cast<int>(old) + n_done == tiles_in_st;
-    }
-    if (!bar_any(BAR_FIN, FIN_THREADS, last)) return;
-    head_tile_stats(a, st, lane, f);
-    named_bar_sync(BAR_FIN, FIN_THREADS);  // the tile's statistics before the release below
-    bool fold = false;
-    if (f == 0 && lane == 0) {
-        a.st_cnt[st] = 0u;
-        const unsigned old = atom_add_acq_rel(a.st_done, 1u);
-        fold = static_cast<int>(old) == a.n_stiles - 1;
-    }
-    if (!bar_any(BAR_FIN, FIN_THREADS, fold)) return;
-    head_final_fold(a, lane, f);
-    if (f == 0 && lane == 0) *a.st_done = 0u;
-}
-
 // ---------------------------------------------------------------------------
 // per-CTA state and shared-memory regions
 // ---------------------------------------------------------------------------
+
+// One piece of a CTA's schedule as the producer publishes it (see produce_phase).
+struct QPiece {
+    int32_t s, u, j0, j1;
+    int32_t first, np;   // CTAs sharing this unit-split, from `first` on
+    int32_t expected;    // partial sums the unit waits for (all its splits)
+    int32_t last;        // the CTA's last piece of this phase
+};
+constexpr int PQ_N = 32;  // queue slots: more than the pieces between producer and finishers (NS + NRB + 2)
+
 struct CtaShared {
     volatile int abort;    // set by anyone whose bounded wait ran out; polled by every wait
-    float inv[16];         // RMSNorm phase: 1 / rms of each row
+    int fin_flag;          // finishers: warp 0's decision, published to the other finisher warps
     uint64_t t0;           // launch start (globaltimer), for the launch-wide time bound
+    QPiece pq[PQ_N];       // the schedule, piece k in slot k % PQ_N
 };
 
 // Launch-wide self-check: past KERNEL_NS since the CTA started, record SD_ETIMEOUT and where
@@ -603,7 +590,11 @@ __device__ __forceinline__ bool out_of_time(const CtaShared &cs, int *status, in
 }
 
 struct Smem {
-    uint64_t *full, *empty, *act_bar, *rfull, *rempty;
+    uint64_t *full, *empty;    // ring stages
+    uint64_t *act_bar;         // the split's activations have landed
+    uint64_t *act_free;        // every consumer warp is done with the previous split's activations
+    uint64_t *rfull, *rempty;  // partial-sum slots between consumers and finishers
+    uint64_t *fin_g, *fin_b;   // finisher rendezvous: gather at warp 0, broadcast back
     uint8_t *ring;
     uint8_t *act;   // the split's activation fragments
     float *meta;    // the split's {corr, d_a} pairs
@@ -616,8 +607,11 @@ __device__ __forceinline__ Smem smem_regions(uint8_t *smem, const QmmArgs &a) {
     r.full = reinterpret_cast<uint64_t *>(smem + HDR_FULL);
     r.empty = reinterpret_cast<uint64_t *>(smem + HDR_EMPTY);
     r.act_bar = reinterpret_cast<uint64_t *>(smem + HDR_ACT);
+    r.act_free = reinterpret_cast<uint64_t *>(smem + HDR_AFREE);
     r.rfull = reinterpret_cast<uint64_t *>(smem + HDR_RFULL);
     r.rempty = reinterpret_cast<uint64_t *>(smem + HDR_REMPTY);
+    r.fin_g = reinterpret_cast<uint64_t *>(smem + HDR_FING);
+    r.fin_b = reinterpret_cast<uint64_t *>(smem + HDR_FINB);
     r.ring = smem + a.off_ring;
     r.act = smem + a.off_act;
     r.meta = reinterpret_cast<float *>(smem + a.off_meta);
@@ -626,30 +620,72 @@ __device__ __forceinline__ Smem smem_regions(uint8_t *smem, const QmmArgs &a) {
     return r;
 }
 
-__device__ __forceinline__ void cta_init(const Smem &sm, int NS, CtaShared &cs) {
+// act_arrivals: 1 when activations arrive by bulk copy (plus its bytes), else every consumer thread
+__device__ __forceinline__ void cta_init(const Smem &sm, int NS, CtaShared &cs, uint32_t act_arrivals) {
     for (int i = 0; i < NS; ++i) {
         mbar_init(&sm.full[i], 1);
         mbar_init(&sm.empty[i], NCW);
     }
-    mbar_init(sm.act_bar, 1);
+    mbar_init(sm.act_bar, act_arrivals);
+    mbar_init(sm.act_free, NCW);
     for (int i = 0; i < 2; ++i) {
         mbar_init(&sm.rfull[i], NCW);
         mbar_init(&sm.rempty[i], NF);
     }
+    mbar_init(sm.fin_g, NF);
+    mbar_init(sm.fin_b, 1);
     cs.abort = 0;
     cs.t0 = gtimer_ns();
     fence_barrier_init();
 }
 
+// bounded wait by a whole warp: true when every lane saw the phase complete; on failure the
+// status records the timeout and every wait in the CTA gives up from then on
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, CtaShared &cs, int *status) {
+    const bool ready = mbar_wait_bounded(bar, parity, WAIT_NS, &cs.abort);
+    __syncwarp();  // lanes leave the wait one by one; warp-wide instructions follow
+    if (__all_sync(0xffffffffu, ready)) return true;
+    set_status(status, SD_ETIMEOUT);
+    cs.abort = 1;
+    return false;
+}
+
 // ---------------------------------------------------------------------------
-// producer: stream this CTA's share of one matmul phase through the ring.
-// `it` counts stages over the whole launch (slot it % NS, phase parity it / NS).
+// producer: stream this CTA's share of one matmul phase through the ring and
+// publish its schedule: piece k goes to queue slot k % PQ_N before the first
+// stage of that piece is armed, so a consumer that has waited for that stage
+// reads it (the stage's mbarrier orders the write).  `it` counts stages over
+// the whole launch (slot it % NS, phase parity it / NS), `npub` pieces.
 // ---------------------------------------------------------------------------
-__device__ inline void produce_phase(const QmmArgs &a, const Smem &sm, uint32_t &it, CtaShared &cs, uint64_t pol) {
+__device__ inline void produce_phase(const QmmArgs &a, const Smem &sm, uint32_t &it, uint32_t &npub, CtaShared &cs,
+                                     uint64_t pol) {
     PieceIter pit;
     pieces_begin(a, pit);
-    Piece pc;
-    while (!cs.abort && pieces_next(a, pit, pc)) {
+    Piece pc, nx;
+    bool have = pieces_next(a, pit, pc);
+    while (have && !cs.abort) {
+        const bool more = pieces_next(a, pit, nx);
+        {
+            QPiece &q = cs.pq[npub % PQ_N];
+            q.s = pc.s;
+            q.u = pc.u;
+            q.j0 = pc.j0;
+            q.j1 = pc.j1;
+            q.first = pc.first;
+            q.np = pc.np;
+            int expected = pc.np;
+            if (a.KS > 1) {  // a shared unit waits for the pieces of all its splits
+                expected = 0;
+                for (int s2 = 0; s2 < a.KS; ++s2) {
+                    int f2, np2;
+                    unit_split_owners(a, s2, pc.u, f2, np2);
+                    expected += np2;
+                }
+            }
+            q.expected = expected;
+            q.last = more ? 0 : 1;
+        }
+        ++npub;
         const int s = pc.s, u = pc.u, j1 = pc.j1;
         for (int jj = pc.j0; jj < j1 && !cs.abort; jj += a.SB) {
             const int n = j1 - jj < a.SB ? j1 - jj : a.SB;
@@ -671,6 +707,8 @@ __device__ inline void produce_phase(const QmmArgs &a, const Smem &sm, uint32_t 
             bulk_g2s(sm.ring + static_cast<size_t>(stg) * a.stage_stride, src, bytes, &sm.full[stg], pol);
             ++it;
         }
+        pc = nx;
+        have = more;
     }
 }
 
@@ -693,50 +731,11 @@ __device__ __forceinline__ void stage_issue(const QmmArgs &a, const Smem &sm, in
     const uint32_t nf = static_cast<uint32_t>(len) * fb, nm = static_cast<uint32_t>(len) * mb;
     const uint32_t ns = a.af_norm ? static_cast<uint32_t>(a.M) * a.ss_ld * 4u : 0u;
     fence_proxy_async_global();
+    fence_proxy_async_shared();
     mbar_arrive_expect_tx(sm.act_bar, nf + nm + ns);
     bulk_g2s_l2keep(sm.act, a.af_frag + b0 * fb, nf, sm.act_bar);
     bulk_g2s_l2keep(sm.meta, reinterpret_cast<const uint8_t *>(a.af_meta) + b0 * mb, nm, sm.act_bar);
     if (ns) bulk_g2s_l2keep(sm.ss, a.ss_in, ns, sm.act_bar);
-}
-
-// Fragments holding RMSNorm codes: form each row's inverse RMS from its block sums of squares
-// (one warp per row: the pairwise tree over 1024 zero-padded slots, equal to the tree over the
-// row's own power of two), then scale the split's {corr, c} pairs to {corr, inv c} and, in the
-// CTA that owns the split's first step, write those scales out.  All consumer threads.
-__device__ inline void stage_norm_scales(const QmmArgs &a, const Smem &sm, CtaShared &cs, int s, int len, bool ok) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int M = a.M, NT = af_nt(M);
-    if (ok) {
-        for (int m = warp; m < M; m += NCW) {
-            float v[32];
-#pragma unroll
-            for (int r = 0; r < 32; ++r) {
-                const int slot = lane + 32 * r;
-                v[r] = slot < a.KB ? sm.ss[m * a.ss_ld + slot] : 0.0f;
-            }
-            const float sum = tree1024_warp(v);
-            if (lane == 0) {
-                const float mean = __fdiv_rn(sum, static_cast<float>(a.KB) * 32.0f);
-                cs.inv[m] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, a.eps)));
-            }
-        }
-    }
-    named_bar_sync(BAR_CONS, CONS_THREADS);
-    if (ok) {
-        const int b0 = s * a.KBs;
-        // the CTA holding the split's first step: CTA 0 with one split (whole units or a shared run)
-        int first = 0, np = 1;
-        if (a.D == 0) unit_split_owners(a, s, 0, first, np);
-        const bool writer = a.s_norm_out && static_cast<int>(blockIdx.x) == first;
-        float2 *mp = reinterpret_cast<float2 *>(sm.meta);
-        for (int it = tid; it < len * M; it += CONS_THREADS) {
-            const int jb = it / M, m = it - jb * M;
-            const float d = __fmul_rn(cs.inv[m], mp[jb * 8 * NT + m].y);
-            mp[jb * 8 * NT + m].y = d;
-            if (writer) a.s_norm_out[static_cast<int64_t>(m) * a.KB + b0 + jb] = d;
-        }
-    }
-    named_bar_sync(BAR_CONS, CONS_THREADS);
 }
 
 // The same shared-memory contents formed from plain int8 rows and scales (all consumer threads).
@@ -776,6 +775,21 @@ __device__ inline void stage_rows(const QmmArgs &a, const Smem &sm, int s, int l
     }
 }
 
+// Inverse RMS of row m from its block sums of squares (whole warp; lane 0's result is broadcast):
+// the pairwise tree over 1024 zero-padded slots, equal to the tree over the row's own power of two.
+__device__ __forceinline__ float warp_row_inv(const QmmArgs &a, const Smem &sm, int m, int lane) {
+    float v[32];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+        const int slot = lane + 32 * r;
+        v[r] = slot < a.KB ? sm.ss[m * a.ss_ld + slot] : 0.0f;
+    }
+    const float sum = tree1024_warp(v);
+    const float mean = __fdiv_rn(sum, static_cast<float>(a.KB) * 32.0f);
+    const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, a.eps)));
+    return __shfl_sync(0xffffffffu, inv, 0);
+}
+
 // ---------------------------------------------------------------------------
 // consumers: the records of one stage.  Warp w takes steps w, w + 8, ...;
 // acc[nt][t][i] holds row 16t + g + 8(i>>1), position 8nt + 2c + (i&1)
@@ -783,8 +797,8 @@ __device__ inline void stage_rows(const QmmArgs &a, const Smem &sm, int s, int l
 // ---------------------------------------------------------------------------
 template <int QT, int PAIR, int NT, bool FULL>
 __device__ __forceinline__ void stage_compute(const uint8_t *sbase, int n, int jb0, const uint8_t *act,
-                                              const float *meta, int M, int warp, int lane, float (&acc)[NT][2][4],
-                                              float (&accu)[PAIR ? NT : 1][2][4]) {
+                                              const float *meta, int M, int warp, int lane, const float2 (&inv)[NT],
+                                              float (&acc)[NT][2][4], float (&accu)[PAIR ? NT : 1][2][4]) {
     constexpr int REC = QT == SD_Q8_0 ? 1088 : 576;   // bytes of one 32-row record
     constexpr int CODE = QT == SD_Q8_0 ? 1024 : 512;  // code bytes of a record
     constexpr int STEP = PAIR ? 2 * REC : REC;
@@ -825,6 +839,7 @@ __device__ __forceinline__ void stage_compute(const uint8_t *sbase, int n, int j
             }
             const float4 mt = meta4[(jb * NT + nt) * 4 + lc];  // corr(p), d_a(p), corr(p+1), d_a(p+1); p = 8nt+2c
             const float2 corr = make_float2(mt.x, mt.z);
+            const float da0 = __fmul_rn(inv[nt].x, mt.y), da1 = __fmul_rn(inv[nt].y, mt.w);  // exact when inv = 1
             float d[2][4];
             record_dots(af, bf, corr, d);
 #pragma unroll
@@ -832,7 +847,7 @@ __device__ __forceinline__ void stage_compute(const uint8_t *sbase, int n, int j
                 const float2 w = t ? w23 : w01;
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    acc[nt][t][e] = __fmaf_rn(d[t][e], __fmul_rn((e >> 1) ? w.y : w.x, (e & 1) ? mt.w : mt.y),
+                    acc[nt][t][e] = __fmaf_rn(d[t][e], __fmul_rn((e >> 1) ? w.y : w.x, (e & 1) ? da1 : da0),
                                               acc[nt][t][e]);
             }
             if (PAIR) {
@@ -843,7 +858,7 @@ __device__ __forceinline__ void stage_compute(const uint8_t *sbase, int n, int j
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
                         accu[PAIR ? nt : 0][t][e] = __fmaf_rn(
-                            d[t][e], __fmul_rn((e >> 1) ? w.y : w.x, (e & 1) ? mt.w : mt.y), accu[PAIR ? nt : 0][t][e]);
+                            d[t][e], __fmul_rn((e >> 1) ? w.y : w.x, (e & 1) ? da1 : da0), accu[PAIR ? nt : 0][t][e]);
                 }
             }
         }
@@ -852,52 +867,88 @@ __device__ __forceinline__ void stage_compute(const uint8_t *sbase, int n, int j
 
 // ---------------------------------------------------------------------------
 // consumers: one matmul phase.  `it` counts ring stages, `pk` pieces (their
-// partial-sum slots), `act_it` activation copies, all over the whole launch.
-// Returns false, the same on every consumer, when the phase was abandoned.
+// partial-sum slots and queue entries), `act_it` activation stagings, all over
+// the whole launch.  Every wait is bounded; a warp whose wait fails marks the
+// CTA aborted and leaves, and every other wait then gives up at once, so all
+// roles reach the phase-end barrier.  Returns false on an abandoned phase.
 // ---------------------------------------------------------------------------
 template <int QT, int PAIR, int NT>
 __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t &it, uint32_t &pk, uint32_t &act_it,
                                      CtaShared &cs) {
-    constexpr int ROWS = PAIR ? 64 : 32;
     const int M = a.M;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int lg = lane >> 2, lc = lane & 3;
     int cur_s = -1;
-    bool ok = true;         // this warp's waits have all succeeded
-    bool act_pending = false;  // thread 0: an activation copy may still be in flight
-    PieceIter pit;
-    pieces_begin(a, pit);
-    Piece pc;
-    while (pieces_next(a, pit, pc)) {
+    float2 inv[NT];  // RMSNorm row factors of this lane's positions 8nt + 2c, +1 (1 when not normalised)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) inv[nt] = make_float2(1.0f, 1.0f);
+    for (;;) {
+        if (out_of_time(cs, a.status, 2)) {  // launch-wide self-check (uniform per warp: lane values may differ)
+            cs.abort = 1;
+        }
+        // the next piece's descriptor rides with its first stage
+        const int stg0 = static_cast<int>(it % a.NS);
+        if (!warp_wait(&sm.full[stg0], (it / a.NS) & 1u, cs, a.status)) return false;
+        const QPiece pc = cs.pq[pk % PQ_N];
         const int s = pc.s, j0 = pc.j0, j1 = pc.j1;
-        const int len = (s == a.KS - 1) ? a.KBlast : a.KBs;
 
         if (s != cur_s) {
-            // every consumer is done with the previous split's activations; agree on aborts
-            if (bar_any(BAR_CONS, CONS_THREADS, !ok || cs.abort)) {
-                cs.abort = 1;
-                if (act_pending) mbar_wait_bounded(sm.act_bar, (act_it - 1) & 1u, WAIT_NS);
-                return false;
-            }
+            const int len = (s == a.KS - 1) ? a.KBlast : a.KBs;
+            if (cur_s >= 0 && lane == 0) mbar_arrive(sm.act_free);  // done with the previous split
             if (a.af_frag) {
+                bool issued = false;
                 if (tid == 0) {
-                    stage_issue(a, sm, s, len);
-                    act_pending = true;
+                    if (act_it > 0 && !mbar_wait_bounded(sm.act_free, (act_it - 1) & 1u, WAIT_NS, &cs.abort)) {
+                        set_status(a.status, SD_ETIMEOUT);
+                        cs.abort = 1;
+                    } else {
+                        stage_issue(a, sm, s, len);
+                        issued = true;
+                    }
                 }
-                const bool ready = mbar_wait_bounded(sm.act_bar, act_it & 1u, WAIT_NS, &cs.abort);
-                __syncwarp();
-                if (!__all_sync(0xffffffffu, ready)) {
-                    set_status(a.status, SD_ETIMEOUT);
-                    cs.abort = 1;
-                    ok = false;
-                } else if (tid == 0) {
-                    act_pending = false;
+                if (!warp_wait(sm.act_bar, act_it & 1u, cs, a.status)) {
+                    // a copy may still be landing: thread 0 waits for it before the CTA can end
+                    if (tid == 0 && issued) mbar_wait_bounded(sm.act_bar, act_it & 1u, WAIT_NS);
+                    return false;
                 }
-                ++act_it;
-                if (a.af_norm) stage_norm_scales(a, sm, cs, s, len, ok);
             } else {
+                if (act_it > 0 && !warp_wait(sm.act_free, (act_it - 1) & 1u, cs, a.status)) return false;
                 stage_rows<QT>(a, sm, s, len, tid);
-                named_bar_sync(BAR_CONS, CONS_THREADS);
+                mbar_arrive(sm.act_bar);  // every consumer thread: its share is written
+                if (!warp_wait(sm.act_bar, act_it & 1u, cs, a.status)) return false;
+            }
+            ++act_it;
+            if (a.af_norm) {
+                // this warp's own copy of the row factors (no cross-warp barrier), applied to the
+                // block scales as they are loaded: d_a = inv * max|x w| / 127, one rounding
+                float rinv[16];
+#pragma unroll
+                for (int m = 0; m < 16; ++m) rinv[m] = m < M ? warp_row_inv(a, sm, m, lane) : 1.0f;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int p0 = 8 * nt + 2 * lc;
+                    float x0 = 1.0f, x1 = 1.0f;
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) {
+                        x0 = m == p0 ? rinv[m] : x0;
+                        x1 = m == p0 + 1 ? rinv[m] : x1;
+                    }
+                    inv[nt] = make_float2(x0, x1);
+                }
+                // the CTA holding the split's first step writes the scales out (warp w: blocks w, w+8, ...)
+                int first = 0, np = 1;
+                if (a.D == 0) unit_split_owners(a, s, 0, first, np);
+                if (a.s_norm_out && static_cast<int>(blockIdx.x) == first) {
+                    const int b0 = s * a.KBs;
+                    const float2 *mp = reinterpret_cast<const float2 *>(sm.meta);
+                    for (int it2 = warp * 32 + lane; it2 < len * M; it2 += CONS_THREADS) {
+                        const int jb = it2 / M, m = it2 - jb * M;
+                        float r = 1.0f;
+#pragma unroll
+                        for (int mm = 0; mm < 16; ++mm) r = mm == m ? rinv[mm] : r;
+                        a.s_norm_out[static_cast<int64_t>(m) * a.KB + b0 + jb] = __fmul_rn(r, mp[jb * 8 * NT + m].y);
+                    }
+                }
             }
             cur_s = s;
         }
@@ -913,95 +964,115 @@ __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
                     accu[PAIR ? nt : 0][t][e] = 0.0f;
                 }
 
-        if (ok) {
-            int late = 0;
-            if (lane == 0) late = out_of_time(cs, a.status, 2) ? 1 : 0;
-            if (__shfl_sync(0xffffffffu, late, 0)) {
-                cs.abort = 1;
-                ok = false;
-            }
-        }
         for (int jj = j0; jj < j1; jj += a.SB) {
             const int n = j1 - jj < a.SB ? j1 - jj : a.SB;
             const int stg = static_cast<int>(it % a.NS);
             const uint32_t ph = (it / a.NS) & 1u;
             ++it;
-            if (!ok) continue;
-            const bool ready = mbar_wait_bounded(&sm.full[stg], ph, WAIT_NS, &cs.abort);
-            __syncwarp();  // lanes leave the wait one by one; mma.sync needs the warp converged
-            if (!__all_sync(0xffffffffu, ready)) {
-                set_status(a.status, SD_ETIMEOUT);
-                cs.abort = 1;
-                ok = false;
-                continue;
-            }
+            if (jj != j0 && !warp_wait(&sm.full[stg], ph, cs, a.status)) return false;
             const uint8_t *sbase = sm.ring + static_cast<size_t>(stg) * a.stage_stride;
             if (n == a.SB)
-                stage_compute<QT, PAIR, NT, true>(sbase, n, jj, sm.act, sm.meta, M, warp, lane, acc, accu);
+                stage_compute<QT, PAIR, NT, true>(sbase, n, jj, sm.act, sm.meta, M, warp, lane, inv, acc, accu);
             else
-                stage_compute<QT, PAIR, NT, false>(sbase, n, jj, sm.act, sm.meta, M, warp, lane, acc, accu);
+                stage_compute<QT, PAIR, NT, false>(sbase, n, jj, sm.act, sm.meta, M, warp, lane, inv, acc, accu);
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.empty[stg]);
         }
 
-        // hand the piece's partial sums to the finisher
+        // hand the piece's partial sums to the finishers
         const uint32_t b = pk % static_cast<uint32_t>(a.NRB), use = pk / static_cast<uint32_t>(a.NRB);
         ++pk;
-        if (ok) {
-            const bool ready = mbar_wait_bounded(&sm.rempty[b], (use & 1u) ^ 1u, WAIT_NS, &cs.abort);
-            __syncwarp();
-            if (!__all_sync(0xffffffffu, ready)) {
-                set_status(a.status, SD_ETIMEOUT);
-                cs.abort = 1;
-                ok = false;
-            }
-        }
-        if (ok) {
-            float *rb = sm.red + (static_cast<size_t>(b) * NCW + warp) * M * a.rows_p;
+        if (!warp_wait(&sm.rempty[b], (use & 1u) ^ 1u, cs, a.status)) return false;
+        float *rb = sm.red + (static_cast<size_t>(b) * NCW + warp) * M * a.rows_p;
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int t = 0; t < 2; ++t)
+            for (int t = 0; t < 2; ++t)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int m = nt * 8 + 2 * lc + (e & 1), row = 16 * t + lg + 8 * (e >> 1);
-                        if (m < M) {
-                            rb[m * a.rows_p + row] = acc[nt][t][e];
-                            if (PAIR) rb[m * a.rows_p + 32 + row] = accu[PAIR ? nt : 0][t][e];
-                        }
+                for (int e = 0; e < 4; ++e) {
+                    const int m = nt * 8 + 2 * lc + (e & 1), row = 16 * t + lg + 8 * (e >> 1);
+                    if (m < M) {
+                        rb[m * a.rows_p + row] = acc[nt][t][e];
+                        if (PAIR) rb[m * a.rows_p + 32 + row] = accu[PAIR ? nt : 0][t][e];
                     }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.rfull[b]);
-        }
-        (void)ROWS;
+                }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.rfull[b]);
+        if (pc.last) break;
     }
-    if (tid == 0 && act_pending) mbar_wait_bounded(sm.act_bar, (act_it - 1) & 1u, WAIT_NS);
-    return ok && !cs.abort;
+    if (lane == 0) mbar_arrive(sm.act_free);  // done with this phase's last split
+    return !cs.abort;
 }
 
 // ---------------------------------------------------------------------------
-// finisher warps: one matmul phase.  For each piece, in the consumers' order,
-// warp f takes positions f, f + NF, ...: add the 8 consumer warps' partial
-// sums (warp order), then finish the unit directly, or store the partial and,
-// if this CTA arrived last, add all partials in (split, piece) order and
-// finish it.  Returns false, the same on every finisher, when abandoned.
+// finisher warps (warp f takes positions f, f + NF, ...): rendezvous through
+// mbarriers (every wait bounded).  fin_sync: each finisher warp arrives;
+// warp 0 waits for all, lane 0 decides, and the decision reaches the others.
 // ---------------------------------------------------------------------------
+template <class Leader>
+__device__ __forceinline__ bool fin_sync(const Smem &sm, CtaShared &cs, uint32_t &fin_it, int f, int lane, int *status,
+                                         Leader leader) {
+    const uint32_t ph = fin_it & 1u;
+    ++fin_it;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sm.fin_g);
+    if (f == 0) {
+        if (!warp_wait(sm.fin_g, ph, cs, status)) return false;
+        int d = 0;
+        if (lane == 0) d = leader() ? 1 : 0;
+        if (lane == 0) {
+            cs.fin_flag = d;
+            mbar_arrive(sm.fin_b);
+        }
+        return __shfl_sync(0xffffffffu, d, 0) != 0;
+    }
+    if (!warp_wait(sm.fin_b, ph, cs, status)) return false;
+    return cs.fin_flag != 0;
+}
+
+// Adds `n_done` finished 32-row tiles to statistics tile `st`; the CTA that completes the tile
+// forms its statistics, the CTA that completes the last tile folds them.  Every finisher warp
+// calls it with the same arguments; the finished logits were written before the call.
+__device__ inline void head_flush(const QmmArgs &a, const Smem &sm, CtaShared &cs, uint32_t &fin_it, int st,
+                                  int n_done, int lane, int f) {
+    if (st < 0 || n_done == 0 || cs.abort) return;
+    const bool last = fin_sync(sm, cs, fin_it, f, lane, a.status, [&]() {
+        const int left = a.NU - st * (STAT_TILE / 32);
+        const int tiles_in_st = left < STAT_TILE / 32 ? left : STAT_TILE / 32;
+        const unsigned old = atom_add_acq_rel(&a.st_cnt[st], static_cast<uint32_t>(n_done));
+        return static_cast<int>(old) + n_done == tiles_in_st;
+    });
+    if (!last || cs.abort) return;
+    head_tile_stats(a, st, lane, f);
+    const bool fold = fin_sync(sm, cs, fin_it, f, lane, a.status, [&]() {
+        a.st_cnt[st] = 0u;
+        const unsigned old = atom_add_acq_rel(a.st_done, 1u);
+        return static_cast<int>(old) == a.n_stiles - 1;
+    });
+    if (!fold || cs.abort) return;
+    head_final_fold(a, lane, f);
+    if (f == 0 && lane == 0) *a.st_done = 0u;
+}
+
+// One matmul phase of the finisher warps.  For each piece, in the consumers' order: add the 8
+// consumer warps' partial sums (warp order), then finish the unit directly, or store the partial
+// and, if this CTA arrived last, add all partials in (split, piece) order and finish it.
 template <int PAIR>
-__device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &pk, CtaShared &cs, int f) {
+__device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &pk, uint32_t &fin_it, CtaShared &cs,
+                                    int f) {
     constexpr int ROWS = PAIR ? 64 : 32;
     const int M = a.M;
     const int lane = threadIdx.x & 31;
     int st_cur = -1, st_n = 0;  // head: current statistics tile and tiles finished in it
-    bool ok = true;
-    PieceIter pit;
-    pieces_begin(a, pit);
-    Piece pc;
-    while (pieces_next(a, pit, pc)) {
-        const int s = pc.s, u = pc.u;
+    for (;;) {
         const uint32_t b = pk % static_cast<uint32_t>(a.NRB), use = pk / static_cast<uint32_t>(a.NRB);
+        const uint32_t slot = pk % PQ_N;
         ++pk;
+        if (!warp_wait(&sm.rfull[b], use & 1u, cs, a.status)) return false;
+        const QPiece pc = cs.pq[slot];
+        const int s = pc.s, u = pc.u;
         const bool direct = (a.KS == 1) && (pc.np == 1);
-        // values the epilogue will need, loaded before the wait: residual and next-norm weights
+        // values the epilogue needs, in flight while the partial sums are added
         float res[FIN_MPW], nw = 0.0f;
         if (!PAIR) {
             const int64_t n = static_cast<int64_t>(u) * 32 + lane;
@@ -1013,18 +1084,9 @@ __device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &
             }
             if (a.norm_next && nok) nw = __ldg(a.norm_next + n);
         }
-        if (ok) {
-            const bool ready = mbar_wait_bounded(&sm.rfull[b], use & 1u, WAIT_NS, &cs.abort);
-            __syncwarp();
-            if (!__all_sync(0xffffffffu, ready)) {
-                set_status(a.status, SD_ETIMEOUT);
-                cs.abort = 1;
-                ok = false;
-            }
-        }
         // this warp's positions: the 8 consumer warps' partial sums, added in warp order
         float v[FIN_MPW], vu[FIN_MPW];
-        if (ok) {
+        {
             const float *rb = sm.red + static_cast<size_t>(b) * NCW * M * a.rows_p;
             const size_t wstride = static_cast<size_t>(M) * a.rows_p;
 #pragma unroll
@@ -1046,38 +1108,30 @@ __device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &
         }
         bool finish = direct;
         if (!direct) {
-            if (ok) {
-                float *pp = a.part + ((static_cast<int64_t>(u) * a.KS + s) * a.P + (static_cast<int>(blockIdx.x) - pc.first)) *
-                                         (ROWS * MPAD);
+            float *pp = a.part + ((static_cast<int64_t>(u) * a.KS + s) * a.P + (static_cast<int>(blockIdx.x) - pc.first)) *
+                                     (ROWS * MPAD);
 #pragma unroll
-                for (int i = 0; i < FIN_MPW; ++i) {
-                    const int m = f + NF * i;
-                    if (m < M) {
-                        pp[m * ROWS + lane] = v[i];
-                        if (PAIR) pp[m * ROWS + 32 + lane] = vu[i];
-                    }
+            for (int i = 0; i < FIN_MPW; ++i) {
+                const int m = f + NF * i;
+                if (m < M) {
+                    pp[m * ROWS + lane] = v[i];
+                    if (PAIR) pp[m * ROWS + 32 + lane] = vu[i];
                 }
             }
-            named_bar_sync(BAR_FIN, FIN_THREADS);  // every finisher's partial sums before the release
-            bool last = false;
-            if (ok && f == 0 && lane == 0) {
-                int expected = 0;
-                for (int s2 = 0; s2 < a.KS; ++s2) {
-                    int f2, np2;
-                    unit_split_owners(a, s2, u, f2, np2);
-                    expected += np2;
-                }
+            // every finisher's partial sums before the release in the counter update
+            finish = fin_sync(sm, cs, fin_it, f, lane, a.status, [&]() {
                 const unsigned old = atom_add_acq_rel(&a.cnt[u], 1u);
-                last = static_cast<int>(old) == expected - 1;
-            }
-            finish = bar_any(BAR_FIN, FIN_THREADS, last);  // the acquire above orders the loads below
-            if (finish && ok) {
+                return static_cast<int>(old) == pc.expected - 1;
+            });
+            if (cs.abort) return false;
+            if (finish) {  // the acquire in the counter update orders the loads below
 #pragma unroll
                 for (int i = 0; i < FIN_MPW; ++i) v[i] = vu[i] = 0.0f;
                 bool first = true;
                 for (int s2 = 0; s2 < a.KS; ++s2) {
                     int f2, np;
-                    unit_split_owners(a, s2, u, f2, np);
+                    if (a.KS == 1) np = pc.np;
+                    else unit_split_owners(a, s2, u, f2, np);
                     for (int p2 = 0; p2 < np; ++p2) {
                         const float *q = a.part + ((static_cast<int64_t>(u) * a.KS + s2) * a.P + p2) * (ROWS * MPAD);
                         float x[FIN_MPW], xu[FIN_MPW];
@@ -1098,7 +1152,7 @@ __device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &
                 if (f == 0 && lane == 0) a.cnt[u] = 0u;
             }
         }
-        if (finish && ok) {
+        if (finish) {
 #pragma unroll
             for (int i = 0; i < FIN_MPW; ++i) {
                 const int m = f + NF * i;
@@ -1108,15 +1162,16 @@ __device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &
         if (finish && a.head) {  // the same decisions on every finisher warp
             const int st = u / (STAT_TILE / 32);
             if (st != st_cur) {
-                head_flush(a, st_cur, st_n, lane, f);
+                head_flush(a, sm, cs, fin_it, st_cur, st_n, lane, f);
                 st_cur = st;
                 st_n = 0;
             }
             ++st_n;
         }
+        if (pc.last) break;
     }
-    if (a.head) head_flush(a, st_cur, st_n, lane, f);
-    return ok && !cs.abort;
+    if (a.head) head_flush(a, sm, cs, fin_it, st_cur, st_n, lane, f);
+    return !cs.abort;
 }
 
 // ---------------------------------------------------------------------------
@@ -1190,27 +1245,29 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
     __shared__ CtaShared cs;
     const Smem sm = smem_regions(smem, a);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0) cta_init(sm, a.NS, cs);
+    if (tid == 0) cta_init(sm, a.NS, cs, a.af_frag ? 1u : static_cast<uint32_t>(CONS_THREADS));
     __syncthreads();
-    uint32_t it = 0, pk = 0, act_it = 0;
+    uint32_t it = 0, pk = 0, act_it = 0, fin_it = 0;
     if (warp == PRODUCER_WARP) {
         pdl_launch_dependents();
         if (lane == 0) {
-            produce_phase(a, sm, it, cs, policy_evict_first());
+            uint32_t npub = 0;
+            produce_phase(a, sm, it, npub, cs, policy_evict_first());
             producer_drain(sm, it, a.NS);
         }
         return;
     }
     pdl_wait();
     pdl_launch_dependents();
-    if (warp >= FIN_WARP0) (void)finish_phase<PAIR>(a, sm, pk, cs, warp - FIN_WARP0);
+    if (warp >= FIN_WARP0) (void)finish_phase<PAIR>(a, sm, pk, fin_it, cs, warp - FIN_WARP0);
     else (void)consume_phase<QT, PAIR, NT>(a, sm, it, pk, act_it, cs);
 }
 
 // ---------------------------------------------------------------------------
 // persistent verify pass: every phase of the pass in one cooperative launch,
 // phases separated by a grid barrier (release / acquire on a global counter,
-// bounded wait).  The producer streams weights across phase boundaries.
+// bounded wait).  The producer streams weights, and publishes the schedule,
+// across phase boundaries.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
     uint32_t v;
@@ -1232,14 +1289,15 @@ __global__ void __launch_bounds__(QMM_THREADS, 1)
     const QmmArgs &a0 = phases[0];
     const Smem sm = smem_regions(smem, a0);
     int *status = a0.status;
-    if (tid == 0) cta_init(sm, a0.NS, cs);
+    if (tid == 0) cta_init(sm, a0.NS, cs, 1u);
     __syncthreads();
-    uint32_t it = 0, pk = 0, act_it = 0;
+    uint32_t it = 0, pk = 0, act_it = 0, fin_it = 0;
     if (warp == PRODUCER_WARP) {
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
+            uint32_t npub = 0;
             for (int p = 0; p < n_phases && !cs.abort; ++p)
-                if (phases[p].kind == KIND_MATMUL) produce_phase(phases[p], sm, it, cs, pol);
+                if (phases[p].kind == KIND_MATMUL) produce_phase(phases[p], sm, it, npub, cs, pol);
             producer_drain(sm, it, a0.NS);
         }
         return;
@@ -1274,7 +1332,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1)
                 greedy_accept(sa.argmax, sa.tokens, sa.parent, sa.M, sa.out_tokens, sa.out_count);
         } else if (warp >= FIN_WARP0) {
             const int f = warp - FIN_WARP0;
-            ok = sa.pair ? finish_phase<1>(sa, sm, pk, cs, f) : finish_phase<0>(sa, sm, pk, cs, f);
+            ok = sa.pair ? finish_phase<1>(sa, sm, pk, fin_it, cs, f) : finish_phase<0>(sa, sm, pk, fin_it, cs, f);
         } else if (sa.qt == SD_Q4_32 && sa.pair) {
             ok = consume_phase<SD_Q4_32, 1, NT>(sa, sm, it, pk, act_it, cs);
         } else if (sa.qt == SD_Q4_32) {
@@ -1282,7 +1340,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1)
         } else {
             ok = consume_phase<SD_Q8_0, 0, NT>(sa, sm, it, pk, act_it, cs);
         }
-        // every write of phase p (consumers and finisher) before thread 0's release
+        // every write of phase p (consumers and finishers) before thread 0's release
         if (bar_any(BAR_WORK, WORK_THREADS, !ok)) {
             cs.abort = 1;
             return;
