@@ -790,8 +790,11 @@ __device__ __forceinline__ float warp_row_inv(const QmmArgs &a, const Smem &sm, 
     return __shfl_sync(0xffffffffu, inv, 0);
 }
 
+// steps one call of stage_compute covers when full: 32 records of 4-bit, 16 gate|up pairs or Q8_0 records
+__host__ __device__ constexpr int sub_steps(int qtype, int pair) { return pair ? 2 * NCW : (qtype == SD_Q8_0 ? 2 * NCW : 4 * NCW); }
+
 // ---------------------------------------------------------------------------
-// consumers: the records of one stage.  Warp w takes steps w, w + 8, ...;
+// consumers: the records of one stage (sub-step).  Warp w takes steps w, w + 8, ...;
 // acc[nt][t][i] holds row 16t + g + 8(i>>1), position 8nt + 2c + (i&1)
 // (accu: the up rows of a gate|up pair).
 // ---------------------------------------------------------------------------
@@ -971,10 +974,17 @@ __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
             ++it;
             if (jj != j0 && !warp_wait(&sm.full[stg], ph, cs, a.status)) return false;
             const uint8_t *sbase = sm.ring + static_cast<size_t>(stg) * a.stage_stride;
-            if (n == a.SB)
-                stage_compute<QT, PAIR, NT, true>(sbase, n, jj, sm.act, sm.meta, M, warp, lane, inv, acc, accu);
-            else
-                stage_compute<QT, PAIR, NT, false>(sbase, n, jj, sm.act, sm.meta, M, warp, lane, inv, acc, accu);
+            constexpr int SUB = sub_steps(QT, PAIR);
+            constexpr int STEP = (QT == SD_Q8_0 ? 1088 : 576) * (PAIR ? 2 : 1);
+            for (int off = 0; off < n; off += SUB) {
+                const int nn = n - off < SUB ? n - off : SUB;
+                if (nn == SUB)
+                    stage_compute<QT, PAIR, NT, true>(sbase + off * STEP, nn, jj + off, sm.act, sm.meta, M, warp, lane,
+                                                      inv, acc, accu);
+                else
+                    stage_compute<QT, PAIR, NT, false>(sbase + off * STEP, nn, jj + off, sm.act, sm.meta, M, warp, lane,
+                                                       inv, acc, accu);
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.empty[stg]);
         }
@@ -1404,8 +1414,9 @@ inline bool make_plan(int qtype, int64_t n_out, int64_t k_in, bool pair, bool he
     return true;
 }
 
-// steps per stage (~18 KB stages): 32 records of 4-bit, 16 gate|up pairs, 16 Q8_0 records
-inline int stage_steps(int qtype, bool pair) { return pair ? 2 * NCW : (qtype == SD_Q8_0 ? 2 * NCW : 4 * NCW); }
+// steps per stage (~36 KB stages, one mbarrier wait per 64 records): 64 records of 4-bit, 32
+// gate|up pairs, 32 Q8_0 records.  The consumers take a stage in sub-steps of sub_steps().
+inline int stage_steps(int qtype, bool pair) { return pair ? 4 * NCW : (qtype == SD_Q8_0 ? 4 * NCW : 8 * NCW); }
 
 struct SmemLayout {
     int NS, NRB, rows_p;
