@@ -51,7 +51,7 @@ constexpr int CONS_THREADS = NCW * 32;         // named barrier BAR_CONS: consum
 constexpr int WORK_THREADS = (NCW + NF) * 32;  // named barrier BAR_WORK: consumers + finishers
 constexpr int FIN_THREADS = NF * 32;           // named barrier BAR_FIN: finishers
 constexpr int BAR_CONS = 1, BAR_WORK = 2, BAR_FIN = 3;
-constexpr int FIN_MPW = (16 + NF - 1) / NF;  // positions per finisher warp at most
+
 constexpr int KB_SPLIT_MAX = 160;      // blocks per k-split
 constexpr int MPAD = 16;               // position stride of workspace partials
 constexpr int MAX_NS = 12;             // ring stages (mbarrier header room)
@@ -775,16 +775,40 @@ __device__ inline void stage_rows(const QmmArgs &a, const Smem &sm, int s, int l
     }
 }
 
-// Inverse RMS of row m from its block sums of squares (whole warp; lane 0's result is broadcast):
-// the pairwise tree over 1024 zero-padded slots, equal to the tree over the row's own power of two.
+// Inverse RMS of row m from its block sums of squares (whole warp; the result is broadcast):
+// the pairwise tree over the zero-padded power of two of at least 256 slots.  Slots past
+// K/32 are zeros, so the tree over 256 slots (8 per lane) and the one over 1024 slots (32 per
+// lane) give the same sum when K/32 <= 256 (their extra levels add exact zeros).
 __device__ __forceinline__ float warp_row_inv(const QmmArgs &a, const Smem &sm, int m, int lane) {
-    float v[32];
+    const float *row = sm.ss + m * a.ss_ld;
+    float sum;
+    if (a.KB <= 256) {
+        float v[8];
 #pragma unroll
-    for (int r = 0; r < 32; ++r) {
-        const int slot = lane + 32 * r;
-        v[r] = slot < a.KB ? sm.ss[m * a.ss_ld + slot] : 0.0f;
+        for (int r = 0; r < 8; ++r) {
+            const int slot = lane + 32 * r;
+            v[r] = slot < a.KB ? row[slot] : 0.0f;
+        }
+#pragma unroll
+        for (int h = 4; h >= 1; h >>= 1)
+#pragma unroll
+            for (int r = 0; r < h; ++r) v[r] = __fadd_rn(v[r], v[r + h]);
+        float x = v[0];
+#pragma unroll
+        for (int st = 16; st >= 1; st >>= 1) {
+            const float o = __shfl_down_sync(0xffffffffu, x, st);
+            if (lane < st) x = __fadd_rn(x, o);
+        }
+        sum = x;
+    } else {
+        float v[32];
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+            const int slot = lane + 32 * r;
+            v[r] = slot < a.KB ? row[slot] : 0.0f;
+        }
+        sum = tree1024_warp(v);
     }
-    const float sum = tree1024_warp(v);
     const float mean = __fdiv_rn(sum, static_cast<float>(a.KB) * 32.0f);
     const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, a.eps)));
     return __shfl_sync(0xffffffffu, inv, 0);
@@ -1067,10 +1091,12 @@ __device__ inline void head_flush(const QmmArgs &a, const Smem &sm, CtaShared &c
 // One matmul phase of the finisher warps.  For each piece, in the consumers' order: add the 8
 // consumer warps' partial sums (warp order), then finish the unit directly, or store the partial
 // and, if this CTA arrived last, add all partials in (split, piece) order and finish it.
-template <int PAIR>
+template <int PAIR, int NT>
 __device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &pk, uint32_t &fin_it, CtaShared &cs,
                                     int f) {
     constexpr int ROWS = PAIR ? 64 : 32;
+    constexpr int FIN_MPW = (8 * NT + NF - 1) / NF;  // positions per finisher warp at most
+    constexpr int CH = 8;                            // partial sums loaded together
     const int M = a.M;
     const int lane = threadIdx.x & 31;
     int st_cur = -1, st_n = 0;  // head: current statistics tile and tiles finished in it
@@ -1142,21 +1168,31 @@ __device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &
                     int f2, np;
                     if (a.KS == 1) np = pc.np;
                     else unit_split_owners(a, s2, u, f2, np);
-                    for (int p2 = 0; p2 < np; ++p2) {
-                        const float *q = a.part + ((static_cast<int64_t>(u) * a.KS + s2) * a.P + p2) * (ROWS * MPAD);
-                        float x[FIN_MPW], xu[FIN_MPW];
+                    const float *qs = a.part + (static_cast<int64_t>(u) * a.KS + s2) * a.P * (ROWS * MPAD);
+                    for (int c0 = 0; c0 < np; c0 += CH) {
+                        // a chunk of pieces: every load in flight together, then added in piece order
+                        float x[CH][FIN_MPW], xu[CH][FIN_MPW];
 #pragma unroll
-                        for (int i = 0; i < FIN_MPW; ++i) {  // all positions' loads in flight together
-                            const int m = f + NF * i;
-                            x[i] = m < M ? __ldcg(q + m * ROWS + lane) : 0.0f;
-                            xu[i] = (PAIR && m < M) ? __ldcg(q + m * ROWS + 32 + lane) : 0.0f;
-                        }
+                        for (int c = 0; c < CH; ++c)
 #pragma unroll
-                        for (int i = 0; i < FIN_MPW; ++i) {
-                            v[i] = first ? x[i] : __fadd_rn(v[i], x[i]);
-                            if (PAIR) vu[i] = first ? xu[i] : __fadd_rn(vu[i], xu[i]);
+                            for (int i = 0; i < FIN_MPW; ++i) {
+                                const int m = f + NF * i;
+                                const bool in = c0 + c < np && m < M;
+                                const float *q = qs + static_cast<int64_t>(c0 + c) * (ROWS * MPAD) + m * ROWS + lane;
+                                x[c][i] = in ? __ldcg(q) : 0.0f;
+                                xu[c][i] = (PAIR && in) ? __ldcg(q + 32) : 0.0f;
+                            }
+#pragma unroll
+                        for (int c = 0; c < CH; ++c) {
+                            if (c0 + c < np) {
+#pragma unroll
+                                for (int i = 0; i < FIN_MPW; ++i) {
+                                    v[i] = first ? x[c][i] : __fadd_rn(v[i], x[c][i]);
+                                    if (PAIR) vu[i] = first ? xu[c][i] : __fadd_rn(vu[i], xu[c][i]);
+                                }
+                                first = false;
+                            }
                         }
-                        first = false;
                     }
                 }
                 if (f == 0 && lane == 0) a.cnt[u] = 0u;
@@ -1269,7 +1305,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
     }
     pdl_wait();
     pdl_launch_dependents();
-    if (warp >= FIN_WARP0) (void)finish_phase<PAIR>(a, sm, pk, fin_it, cs, warp - FIN_WARP0);
+    if (warp >= FIN_WARP0) (void)finish_phase<PAIR, NT>(a, sm, pk, fin_it, cs, warp - FIN_WARP0);
     else (void)consume_phase<QT, PAIR, NT>(a, sm, it, pk, act_it, cs);
 }
 
@@ -1342,7 +1378,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1)
                 greedy_accept(sa.argmax, sa.tokens, sa.parent, sa.M, sa.out_tokens, sa.out_count);
         } else if (warp >= FIN_WARP0) {
             const int f = warp - FIN_WARP0;
-            ok = sa.pair ? finish_phase<1>(sa, sm, pk, fin_it, cs, f) : finish_phase<0>(sa, sm, pk, fin_it, cs, f);
+            ok = sa.pair ? finish_phase<1, NT>(sa, sm, pk, fin_it, cs, f) : finish_phase<0, NT>(sa, sm, pk, fin_it, cs, f);
         } else if (sa.qt == SD_Q4_32 && sa.pair) {
             ok = consume_phase<SD_Q4_32, 1, NT>(sa, sm, it, pk, act_it, cs);
         } else if (sa.qt == SD_Q4_32) {
