@@ -94,7 +94,7 @@ extern "C" {
 
 size_t sd_pass_plan_bytes(int32_t n_layers) {
     if (n_layers < 0) return 0;
-    return sizeof(PassHeader) + static_cast<size_t>(4 * n_layers + 3) * sizeof(QmmArgs);
+    return sizeof(PassHeader) + static_cast<size_t>(5 * n_layers + 3) * sizeof(QmmArgs);
 }
 
 size_t sd_pass_workspace_bytes(int64_t hidden, int64_t ffn, int64_t vocab, int32_t wq) {
@@ -128,7 +128,7 @@ sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, 
     const int NT = af_nt(M);
 
     std::vector<QmmArgs> ph;
-    ph.reserve(static_cast<size_t>(4 * L + 3));  // pointers returned by matmul() below stay valid
+    ph.reserve(static_cast<size_t>(5 * L + 3));  // pointers returned by matmul() below stay valid
     uint8_t *ws = static_cast<uint8_t *>(d->workspace);
     uint8_t *afa_f = ws + W.afa_frag, *afv_f = ws + W.afv_frag, *aff_f = ws + W.aff_frag;
     float *afa_m = reinterpret_cast<float *>(ws + W.afa_meta), *afv_m = reinterpret_cast<float *>(ws + W.afv_meta),
@@ -239,6 +239,14 @@ sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, 
         const bool lastl = l + 1 == L;
         if (!lastl && !d->layers[l + 1].norm1) return SD_EINVAL;
         residual_out(a, lastl ? d->final_norm : d->layers[l + 1].norm1, lastl ? SD_Q8_0 : d->wq);
+        if (a->D == 0 && a->KS > 1) {
+            // every unit is shared across k-splits: store partial sums only and finish the units in a
+            // combine phase, an equal share per CTA, instead of wherever the last piece lands
+            a->defer = 1;
+            QmmArgs cmb = *a;
+            cmb.kind = KIND_COMBINE;
+            ph.push_back(cmb);
+        }
     }
     {
         QmmArgs *hd = matmul(SD_Q8_0, d->head, V, H, false, d->qa, d->sa, afa_f, afa_m);

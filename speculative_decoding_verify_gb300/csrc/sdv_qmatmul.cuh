@@ -54,7 +54,7 @@ constexpr int BAR_CONS = 1, BAR_WORK = 2, BAR_FIN = 3;
 
 constexpr int KB_SPLIT_MAX = 160;      // blocks per k-split
 constexpr int MPAD = 16;               // position stride of workspace partials
-constexpr int MAX_NS = 12;             // ring stages (mbarrier header room)
+constexpr int MAX_NS = 10;             // ring stages (mbarrier header room)
 constexpr uint64_t WAIT_NS = 2000000000ull;     // 2 s bound on any in-kernel wait
 constexpr uint64_t KERNEL_NS = 10000000000ull;  // 10 s bound on any launch's loops (self-check)
 constexpr int STAT_TILE = 1024;        // vocabulary tile of the softmax statistics
@@ -67,8 +67,8 @@ constexpr int PASS_NORM_MAX_KB = 1024; // ... inside the verify pass (one warp's
 // Shared-memory header: mbarriers at fixed offsets
 constexpr uint32_t HDR_FULL = 0, HDR_EMPTY = 8 * MAX_NS, HDR_ACT = 16 * MAX_NS, HDR_AFREE = HDR_ACT + 8,
                    HDR_RFULL = HDR_AFREE + 8, HDR_REMPTY = HDR_RFULL + 16, HDR_FING = HDR_REMPTY + 16,
-                   HDR_FINB = HDR_FING + 8, HDR_BYTES = 256;
-static_assert(HDR_FINB + 8 <= HDR_BYTES, "mbarrier header");
+                   HDR_FINB = HDR_FING + 8, HDR_INV = HDR_FINB + 8, HDR_BYTES = 256;
+static_assert(HDR_INV + 8 <= HDR_BYTES, "mbarrier header");
 
 // ---------------------------------------------------------------------------
 // Activation fragments ("AF"): a matmul's int8 input laid out for its inner
@@ -98,6 +98,7 @@ struct QmmArgs {
     int32_t G;           // CTAs
     int32_t P;           // max pieces per (unit, split)
     int32_t D, R;        // whole units per CTA and units shared stream-K (D = 0: all shared)
+    int32_t defer;       // partial sums only: a KIND_COMBINE phase adds them and runs the epilogue
     int32_t SB;          // steps per stage
     int32_t NS;          // stages
     uint32_t step_bytes; // bytes of one step
@@ -150,7 +151,7 @@ struct QmmArgs {
     int32_t *out_count;
 };
 
-constexpr int KIND_MATMUL = 0, KIND_NORM = 1, KIND_ACCEPT = 2;
+constexpr int KIND_MATMUL = 0, KIND_NORM = 1, KIND_ACCEPT = 2, KIND_COMBINE = 3;
 
 // fetch-and-add with release (orders the writes seen through a barrier) and acquire
 __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v) {
@@ -577,6 +578,7 @@ constexpr int PQ_N = 32;  // queue slots: more than the pieces between producer 
 struct CtaShared {
     volatile int abort;    // set by anyone whose bounded wait ran out; polled by every wait
     int fin_flag;          // finishers: warp 0's decision, published to the other finisher warps
+    float inv[16];         // RMSNorm row factors of the current normalised staging
     uint64_t t0;           // launch start (globaltimer), for the launch-wide time bound
     QPiece pq[PQ_N];       // the schedule, piece k in slot k % PQ_N
 };
@@ -595,6 +597,7 @@ struct Smem {
     uint64_t *act_free;        // every consumer warp is done with the previous split's activations
     uint64_t *rfull, *rempty;  // partial-sum slots between consumers and finishers
     uint64_t *fin_g, *fin_b;   // finisher rendezvous: gather at warp 0, broadcast back
+    uint64_t *inv_bar;         // the RMSNorm row factors of a staging are in CtaShared::inv
     uint8_t *ring;
     uint8_t *act;   // the split's activation fragments
     float *meta;    // the split's {corr, d_a} pairs
@@ -612,6 +615,7 @@ __device__ __forceinline__ Smem smem_regions(uint8_t *smem, const QmmArgs &a) {
     r.rempty = reinterpret_cast<uint64_t *>(smem + HDR_REMPTY);
     r.fin_g = reinterpret_cast<uint64_t *>(smem + HDR_FING);
     r.fin_b = reinterpret_cast<uint64_t *>(smem + HDR_FINB);
+    r.inv_bar = reinterpret_cast<uint64_t *>(smem + HDR_INV);
     r.ring = smem + a.off_ring;
     r.act = smem + a.off_act;
     r.meta = reinterpret_cast<float *>(smem + a.off_meta);
@@ -634,6 +638,7 @@ __device__ __forceinline__ void cta_init(const Smem &sm, int NS, CtaShared &cs, 
     }
     mbar_init(sm.fin_g, NF);
     mbar_init(sm.fin_b, 1);
+    mbar_init(sm.inv_bar, NCW);
     cs.abort = 0;
     cs.t0 = gtimer_ns();
     fence_barrier_init();
@@ -894,14 +899,14 @@ __device__ __forceinline__ void stage_compute(const uint8_t *sbase, int n, int j
 
 // ---------------------------------------------------------------------------
 // consumers: one matmul phase.  `it` counts ring stages, `pk` pieces (their
-// partial-sum slots and queue entries), `act_it` activation stagings, all over
-// the whole launch.  Every wait is bounded; a warp whose wait fails marks the
+// partial-sum slots and queue entries), `act_it` activation stagings and
+// `nrm_it` those of RMSNorm codes, all over the whole launch.  Every wait is bounded; a warp whose wait fails marks the
 // CTA aborted and leaves, and every other wait then gives up at once, so all
 // roles reach the phase-end barrier.  Returns false on an abandoned phase.
 // ---------------------------------------------------------------------------
 template <int QT, int PAIR, int NT>
 __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t &it, uint32_t &pk, uint32_t &act_it,
-                                     CtaShared &cs) {
+                                     uint32_t &nrm_it, CtaShared &cs) {
     const int M = a.M;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int lg = lane >> 2, lc = lane & 3;
@@ -946,21 +951,20 @@ __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
             }
             ++act_it;
             if (a.af_norm) {
-                // this warp's own copy of the row factors (no cross-warp barrier), applied to the
-                // block scales as they are loaded: d_a = inv * max|x w| / 127, one rounding
-                float rinv[16];
-#pragma unroll
-                for (int m = 0; m < 16; ++m) rinv[m] = m < M ? warp_row_inv(a, sm, m, lane) : 1.0f;
+                // the row factors, one warp per row (warp w: rows w, w + 8), published through
+                // inv_bar; applied to the block scales as they are loaded: d_a = inv * max|x w| / 127
+                for (int m = warp; m < M; m += NCW) {
+                    const float r = warp_row_inv(a, sm, m, lane);
+                    if (lane == 0) cs.inv[m] = r;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sm.inv_bar);
+                if (!warp_wait(sm.inv_bar, nrm_it & 1u, cs, a.status)) return false;
+                ++nrm_it;
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     const int p0 = 8 * nt + 2 * lc;
-                    float x0 = 1.0f, x1 = 1.0f;
-#pragma unroll
-                    for (int m = 0; m < 16; ++m) {
-                        x0 = m == p0 ? rinv[m] : x0;
-                        x1 = m == p0 + 1 ? rinv[m] : x1;
-                    }
-                    inv[nt] = make_float2(x0, x1);
+                    inv[nt] = make_float2(p0 < M ? cs.inv[p0] : 1.0f, p0 + 1 < M ? cs.inv[p0 + 1] : 1.0f);
                 }
                 // the CTA holding the split's first step writes the scales out (warp w: blocks w, w+8, ...)
                 int first = 0, np = 1;
@@ -970,10 +974,8 @@ __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
                     const float2 *mp = reinterpret_cast<const float2 *>(sm.meta);
                     for (int it2 = warp * 32 + lane; it2 < len * M; it2 += CONS_THREADS) {
                         const int jb = it2 / M, m = it2 - jb * M;
-                        float r = 1.0f;
-#pragma unroll
-                        for (int mm = 0; mm < 16; ++mm) r = mm == m ? rinv[mm] : r;
-                        a.s_norm_out[static_cast<int64_t>(m) * a.KB + b0 + jb] = __fmul_rn(r, mp[jb * 8 * NT + m].y);
+                        a.s_norm_out[static_cast<int64_t>(m) * a.KB + b0 + jb] =
+                            __fmul_rn(cs.inv[m], mp[jb * 8 * NT + m].y);
                     }
                 }
             }
@@ -1154,6 +1156,10 @@ __device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &
                     if (PAIR) pp[m * ROWS + 32 + lane] = vu[i];
                 }
             }
+            if (a.defer) {  // the combine phase after the grid barrier adds them up
+                if (pc.last) break;
+                continue;
+            }
             // every finisher's partial sums before the release in the counter update
             finish = fin_sync(sm, cs, fin_it, f, lane, a.status, [&]() {
                 const unsigned old = atom_add_acq_rel(&a.cnt[u], 1u);
@@ -1248,6 +1254,46 @@ __device__ inline void norm_phase(const QmmArgs &a) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// deferred fixup of a matmul whose units are all shared (several k-splits):
+// after the grid barrier every CTA finishes an equal share of the units.  Work
+// warp w (consumers and finishers, 0..10) takes (unit, position) items w,
+// w + 11, ...: the partial sums in (split, piece) order, then the epilogue.
+// ---------------------------------------------------------------------------
+__device__ inline void combine_phase(const QmmArgs &a, int widx) {
+    constexpr int ROWS = 32, CH = 8, NWW = NCW + NF;
+    const int lane = threadIdx.x & 31, M = a.M;
+    const int u0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * a.NU / gridDim.x);
+    const int u1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * a.NU / gridDim.x);
+    const int items = (u1 - u0) * M;
+    for (int i = widx; i < items; i += NWW) {
+        const int u = u0 + i / M, m = i - (i / M) * M;
+        const int64_t n = static_cast<int64_t>(u) * 32 + lane;
+        const bool nok = n < a.n_out;
+        const float res = (a.residual && nok) ? __ldcg(a.residual + m * a.n_out + n) : 0.0f;
+        const float nw = (a.norm_next && nok) ? __ldg(a.norm_next + n) : 0.0f;
+        float v = 0.0f;
+        bool first = true;
+        for (int s2 = 0; s2 < a.KS; ++s2) {
+            int f2, np;
+            unit_split_owners(a, s2, u, f2, np);
+            const float *qs = a.part + (static_cast<int64_t>(u) * a.KS + s2) * a.P * (ROWS * MPAD) + m * ROWS + lane;
+            for (int c0 = 0; c0 < np; c0 += CH) {
+                float x[CH];
+#pragma unroll
+                for (int c = 0; c < CH; ++c) x[c] = c0 + c < np ? __ldcg(qs + static_cast<int64_t>(c0 + c) * (ROWS * MPAD)) : 0.0f;
+#pragma unroll
+                for (int c = 0; c < CH; ++c)
+                    if (c0 + c < np) {
+                        v = first ? x[c] : __fadd_rn(v, x[c]);
+                        first = false;
+                    }
+            }
+        }
+        epilogue<0>(a, u, m, lane, v, 0.0f, res, nw);
+    }
+}
+
 // greedy acceptance (chain when parent == nullptr, else a tree in BFS order); one thread
 __device__ inline void greedy_accept(const int32_t *argmax, const int32_t *tokens, const int32_t *parent, int M,
                                      int32_t *out, int32_t *count) {
@@ -1293,7 +1339,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) cta_init(sm, a.NS, cs, a.af_frag ? 1u : static_cast<uint32_t>(CONS_THREADS));
     __syncthreads();
-    uint32_t it = 0, pk = 0, act_it = 0, fin_it = 0;
+    uint32_t it = 0, pk = 0, act_it = 0, nrm_it = 0, fin_it = 0;
     if (warp == PRODUCER_WARP) {
         pdl_launch_dependents();
         if (lane == 0) {
@@ -1306,7 +1352,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
     pdl_wait();
     pdl_launch_dependents();
     if (warp >= FIN_WARP0) (void)finish_phase<PAIR, NT>(a, sm, pk, fin_it, cs, warp - FIN_WARP0);
-    else (void)consume_phase<QT, PAIR, NT>(a, sm, it, pk, act_it, cs);
+    else (void)consume_phase<QT, PAIR, NT>(a, sm, it, pk, act_it, nrm_it, cs);
 }
 
 // ---------------------------------------------------------------------------
@@ -1337,7 +1383,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1)
     int *status = a0.status;
     if (tid == 0) cta_init(sm, a0.NS, cs, 1u);
     __syncthreads();
-    uint32_t it = 0, pk = 0, act_it = 0, fin_it = 0;
+    uint32_t it = 0, pk = 0, act_it = 0, nrm_it = 0, fin_it = 0;
     if (warp == PRODUCER_WARP) {
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
@@ -1376,15 +1422,17 @@ __global__ void __launch_bounds__(QMM_THREADS, 1)
         } else if (sa.kind == KIND_ACCEPT) {
             if (blockIdx.x == 0 && tid == 0)
                 greedy_accept(sa.argmax, sa.tokens, sa.parent, sa.M, sa.out_tokens, sa.out_count);
+        } else if (sa.kind == KIND_COMBINE) {
+            combine_phase(sa, warp < NCW ? warp : warp - 1);
         } else if (warp >= FIN_WARP0) {
             const int f = warp - FIN_WARP0;
             ok = sa.pair ? finish_phase<1, NT>(sa, sm, pk, fin_it, cs, f) : finish_phase<0, NT>(sa, sm, pk, fin_it, cs, f);
         } else if (sa.qt == SD_Q4_32 && sa.pair) {
-            ok = consume_phase<SD_Q4_32, 1, NT>(sa, sm, it, pk, act_it, cs);
+            ok = consume_phase<SD_Q4_32, 1, NT>(sa, sm, it, pk, act_it, nrm_it, cs);
         } else if (sa.qt == SD_Q4_32) {
-            ok = consume_phase<SD_Q4_32, 0, NT>(sa, sm, it, pk, act_it, cs);
+            ok = consume_phase<SD_Q4_32, 0, NT>(sa, sm, it, pk, act_it, nrm_it, cs);
         } else {
-            ok = consume_phase<SD_Q8_0, 0, NT>(sa, sm, it, pk, act_it, cs);
+            ok = consume_phase<SD_Q8_0, 0, NT>(sa, sm, it, pk, act_it, nrm_it, cs);
         }
         // every write of phase p (consumers and finishers) before thread 0's release
         if (bar_any(BAR_WORK, WORK_THREADS, !ok)) {
