@@ -94,7 +94,7 @@ extern "C" {
 
 size_t sd_pass_plan_bytes(int32_t n_layers) {
     if (n_layers < 0) return 0;
-    return sizeof(PassHeader) + static_cast<size_t>(5 * n_layers + 3) * sizeof(QmmArgs);
+    return sizeof(PassHeader) + static_cast<size_t>(5 * n_layers + 4) * sizeof(QmmArgs);
 }
 
 size_t sd_pass_workspace_bytes(int64_t hidden, int64_t ffn, int64_t vocab, int32_t wq) {
@@ -128,7 +128,7 @@ sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, 
     const int NT = af_nt(M);
 
     std::vector<QmmArgs> ph;
-    ph.reserve(static_cast<size_t>(5 * L + 3));  // pointers returned by matmul() below stay valid
+    ph.reserve(static_cast<size_t>(5 * L + 4));  // pointers returned by matmul() below stay valid
     uint8_t *ws = static_cast<uint8_t *>(d->workspace);
     uint8_t *afa_f = ws + W.afa_frag, *afv_f = ws + W.afv_frag, *aff_f = ws + W.aff_frag;
     float *afa_m = reinterpret_cast<float *>(ws + W.afa_meta), *afv_m = reinterpret_cast<float *>(ws + W.afv_meta),
@@ -260,11 +260,25 @@ sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, 
         hd->row_sumexp = d->row_sumexp;
         hd->n_stiles = static_cast<int32_t>((V + STAT_TILE - 1) / STAT_TILE);
         hd->st_part = reinterpret_cast<float4 *>(ws + W.stats);
+        // the statistics once the logits are complete: an even spread over the grid instead of
+        // wherever a tile's last rows land; the acceptance phase folds them
+        hd->defer_stats = 1;
+        QmmArgs hs = *hd;
+        hs.kind = KIND_HSTATS;
+        ph.push_back(hs);
     }
     {
+        const QmmArgs &hd = ph[ph.size() - 1];
         QmmArgs a;
         base(a);
         a.kind = KIND_ACCEPT;
+        a.defer_stats = 1;
+        a.T = hd.T;
+        a.n_out = hd.n_out;
+        a.n_stiles = hd.n_stiles;
+        a.st_part = hd.st_part;
+        a.row_max = hd.row_max;
+        a.row_sumexp = hd.row_sumexp;
         a.argmax = d->argmax;
         a.tokens = d->tokens;
         a.parent = d->parent;

@@ -99,6 +99,7 @@ struct QmmArgs {
     int32_t P;           // max pieces per (unit, split)
     int32_t D, R;        // whole units per CTA and units shared stream-K (D = 0: all shared)
     int32_t defer;       // partial sums only: a KIND_COMBINE phase adds them and runs the epilogue
+    int32_t defer_stats; // head: statistics formed by a KIND_HSTATS phase, folded by KIND_ACCEPT
     int32_t SB;          // steps per stage
     int32_t NS;          // stages
     uint32_t step_bytes; // bytes of one step
@@ -151,7 +152,7 @@ struct QmmArgs {
     int32_t *out_count;
 };
 
-constexpr int KIND_MATMUL = 0, KIND_NORM = 1, KIND_ACCEPT = 2, KIND_COMBINE = 3;
+constexpr int KIND_MATMUL = 0, KIND_NORM = 1, KIND_ACCEPT = 2, KIND_COMBINE = 3, KIND_HSTATS = 4;
 
 // fetch-and-add with release (orders the writes seen through a barrier) and acquire
 __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v) {
@@ -472,94 +473,105 @@ __device__ __forceinline__ void epilogue(const QmmArgs &a, int u, int m, int lan
 }
 
 // ---------------------------------------------------------------------------
-// head statistics (finisher warps; warp f takes positions f, f + NF, ...).  A
-// 1024-token tile's statistics are formed by the CTA that finishes its last
-// 32-row tile; the CTA that finishes the last statistics tile folds them per row.
+// head statistics.  Per operation: the finisher warps (warp f takes positions f, f + NF, ...) of
+// the CTA that finishes a 1024-token tile's last 32-row tile form its statistics; the CTA that
+// finishes the last statistics tile folds them per row.  In the pass: a statistics phase after
+// the logits are complete, (tile, position) items spread over every work warp of the grid, and
+// the fold at the start of the acceptance phase.
 // ---------------------------------------------------------------------------
-__device__ inline void head_tile_stats(const QmmArgs &a, int st, int lane, int f) {
+
+// Statistics of tile st for position m (one warp): max of z = l / T, the pairwise-tree sum of
+// exp(z - max) and the raw-logit argmax (lowest index on ties).
+__device__ inline void head_tile_stats_one(const QmmArgs &a, int st, int m, int lane) {
     const int64_t V = a.n_out;
-    for (int m = f; m < a.M; m += NF) {
-        float v[32];
-        float zmax = -__int_as_float(0x7f800000);
-        float bl = -__int_as_float(0x7f800000);
-        int bi = 0x7fffffff;
+    const bool unit_t = a.T == 1.0f;  // l / 1 is l exactly
+    float v[32];
+    float zmax = -__int_as_float(0x7f800000);
+    float bl = -__int_as_float(0x7f800000);
+    int bi = 0x7fffffff;
 #pragma unroll
-        for (int r = 0; r < 32; ++r) {
-            const int64_t e = static_cast<int64_t>(st) * STAT_TILE + lane + 32 * r;
-            float z = -__int_as_float(0x7f800000);
-            if (e < V) {
-                const float l = __ldcg(a.y + m * V + e);
-                if (l > bl) {
-                    bl = l;
-                    bi = static_cast<int>(e);
-                }
-                z = __fdiv_rn(l, a.T);
-                zmax = fmaxf(zmax, z);
+    for (int r = 0; r < 32; ++r) {
+        const int64_t e = static_cast<int64_t>(st) * STAT_TILE + lane + 32 * r;
+        float z = -__int_as_float(0x7f800000);
+        if (e < V) {
+            const float l = __ldcg(a.y + m * V + e);
+            if (l > bl) {
+                bl = l;
+                bi = static_cast<int>(e);
             }
-            v[r] = z;
+            z = unit_t ? l : __fdiv_rn(l, a.T);
+            zmax = fmaxf(zmax, z);
         }
+        v[r] = z;
+    }
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) {
-            zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, o));
-            const float ol = __shfl_xor_sync(0xffffffffu, bl, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ol > bl || (ol == bl && oi < bi)) {
-                bl = ol;
-                bi = oi;
-            }
+    for (int o = 16; o >= 1; o >>= 1) {
+        zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, o));
+        const float ol = __shfl_xor_sync(0xffffffffu, bl, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ol > bl || (ol == bl && oi < bi)) {
+            bl = ol;
+            bi = oi;
         }
+    }
 #pragma unroll
-        for (int r = 0; r < 32; ++r) {
-            const int64_t e = static_cast<int64_t>(st) * STAT_TILE + lane + 32 * r;
-            v[r] = e < V ? cexpf_canon(__fsub_rn(v[r], zmax)) : 0.0f;
+    for (int r = 0; r < 32; ++r) {
+        const int64_t e = static_cast<int64_t>(st) * STAT_TILE + lane + 32 * r;
+        v[r] = e < V ? cexpf_canon(__fsub_rn(v[r], zmax)) : 0.0f;
+    }
+    const float s = tree1024_warp(v);
+    if (lane == 0) a.st_part[st * MPAD + m] = make_float4(zmax, s, __int_as_float(bi), bl);
+}
+
+__device__ inline void head_tile_stats(const QmmArgs &a, int st, int lane, int f) {
+    for (int m = f; m < a.M; m += NF) head_tile_stats_one(a, st, m, lane);
+}
+
+// Fold of position m's tile statistics (one warp): argmax, row max and Z = the sequential fold
+// over tiles of s_t exp(m_t - max), the products formed in parallel.
+__device__ inline void head_final_fold_one(const QmmArgs &a, int m, int lane) {
+    float mx = -__int_as_float(0x7f800000);
+    float bl = -__int_as_float(0x7f800000);
+    int bi = 0x7fffffff;
+    for (int t = lane; t < a.n_stiles; t += 32) {
+        const float4 p = __ldcg(a.st_part + t * MPAD + m);
+        mx = fmaxf(mx, p.x);
+        const int pi = __float_as_int(p.z);
+        if (p.w > bl || (p.w == bl && pi < bi)) {
+            bl = p.w;
+            bi = pi;
         }
-        const float s = tree1024_warp(v);
-        if (lane == 0) a.st_part[st * MPAD + m] = make_float4(zmax, s, __int_as_float(bi), bl);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const float ol = __shfl_xor_sync(0xffffffffu, bl, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ol > bl || (ol == bl && oi < bi)) {
+            bl = ol;
+            bi = oi;
+        }
+    }
+    float Z = 0.0f;
+    for (int t0 = 0; t0 < a.n_stiles; t0 += 32) {
+        const int t = t0 + lane;
+        float e = 0.0f;
+        if (t < a.n_stiles) {
+            const float4 p = __ldcg(a.st_part + t * MPAD + m);
+            e = __fmul_rn(p.y, cexpf_canon(__fsub_rn(p.x, mx)));
+        }
+        const int nn = a.n_stiles - t0 < 32 ? a.n_stiles - t0 : 32;
+        for (int j = 0; j < nn; ++j) Z = __fadd_rn(Z, __shfl_sync(0xffffffffu, e, j));
+    }
+    if (lane == 0) {
+        a.argmax[m] = bi;
+        a.row_max[m] = mx;
+        a.row_sumexp[m] = Z;
     }
 }
 
 __device__ inline void head_final_fold(const QmmArgs &a, int lane, int f) {
-    for (int m = f; m < a.M; m += NF) {
-        float mx = -__int_as_float(0x7f800000);
-        float bl = -__int_as_float(0x7f800000);
-        int bi = 0x7fffffff;
-        for (int t = lane; t < a.n_stiles; t += 32) {
-            const float4 p = __ldcg(a.st_part + t * MPAD + m);
-            mx = fmaxf(mx, p.x);
-            const int pi = __float_as_int(p.z);
-            if (p.w > bl || (p.w == bl && pi < bi)) {
-                bl = p.w;
-                bi = pi;
-            }
-        }
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) {
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            const float ol = __shfl_xor_sync(0xffffffffu, bl, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ol > bl || (ol == bl && oi < bi)) {
-                bl = ol;
-                bi = oi;
-            }
-        }
-        // Z = sequential fold over tiles of s_t * exp(m_t - m); the products in parallel
-        float Z = 0.0f;
-        for (int t0 = 0; t0 < a.n_stiles; t0 += 32) {
-            const int t = t0 + lane;
-            float e = 0.0f;
-            if (t < a.n_stiles) {
-                const float4 p = __ldcg(a.st_part + t * MPAD + m);
-                e = __fmul_rn(p.y, cexpf_canon(__fsub_rn(p.x, mx)));
-            }
-            const int nn = a.n_stiles - t0 < 32 ? a.n_stiles - t0 : 32;
-            for (int j = 0; j < nn; ++j) Z = __fadd_rn(Z, __shfl_sync(0xffffffffu, e, j));
-        }
-        if (lane == 0) {
-            a.argmax[m] = bi;
-            a.row_max[m] = mx;
-            a.row_sumexp[m] = Z;
-        }
-    }
+    for (int m = f; m < a.M; m += NF) head_final_fold_one(a, m, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -897,6 +909,24 @@ __device__ __forceinline__ void stage_compute(const uint8_t *sbase, int n, int j
     }
 }
 
+// Thread 0, right after the grid barrier of a matmul phase whose activations arrive as fragments:
+// start the bulk copy of the CTA's first k-split at once (consume_phase then only waits for it).
+// Returns whether it issued the copy.
+__device__ inline bool pre_issue_staging(const QmmArgs &a, const Smem &sm, uint32_t act_it, CtaShared &cs) {
+    if (a.kind != KIND_MATMUL || !a.af_frag) return false;
+    PieceIter pit;
+    pieces_begin(a, pit);
+    Piece pc;
+    if (!pieces_next(a, pit, pc)) return false;
+    if (act_it > 0 && !mbar_wait_bounded(sm.act_free, (act_it - 1) & 1u, WAIT_NS, &cs.abort)) {
+        set_status(a.status, SD_ETIMEOUT);
+        cs.abort = 1;
+        return false;
+    }
+    stage_issue(a, sm, pc.s, (pc.s == a.KS - 1) ? a.KBlast : a.KBs);
+    return true;
+}
+
 // ---------------------------------------------------------------------------
 // consumers: one matmul phase.  `it` counts ring stages, `pk` pieces (their
 // partial-sum slots and queue entries), `act_it` activation stagings and
@@ -906,10 +936,15 @@ __device__ __forceinline__ void stage_compute(const uint8_t *sbase, int n, int j
 // ---------------------------------------------------------------------------
 template <int QT, int PAIR, int NT>
 __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t &it, uint32_t &pk, uint32_t &act_it,
-                                     uint32_t &nrm_it, CtaShared &cs) {
+                                     uint32_t &nrm_it, CtaShared &cs, bool pre_issued = false) {
     const int M = a.M;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int lg = lane >> 2, lc = lane & 3;
+    // descriptor fields the loops use, in registers (the descriptor may sit in shared memory, and
+    // every mbarrier operation below is a compiler memory barrier)
+    const int SB = a.SB, rows_p = a.rows_p;
+    const uint32_t NS = static_cast<uint32_t>(a.NS), NRB = static_cast<uint32_t>(a.NRB), sstride = a.stage_stride;
+    uint32_t stg = it % NS, sph = (it / NS) & 1u;  // ring slot and phase parity of stage `it`
     int cur_s = -1;
     float2 inv[NT];  // RMSNorm row factors of this lane's positions 8nt + 2c, +1 (1 when not normalised)
 #pragma unroll
@@ -919,8 +954,7 @@ __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
             cs.abort = 1;
         }
         // the next piece's descriptor rides with its first stage
-        const int stg0 = static_cast<int>(it % a.NS);
-        if (!warp_wait(&sm.full[stg0], (it / a.NS) & 1u, cs, a.status)) return false;
+        if (!warp_wait(&sm.full[stg], sph, cs, a.status)) return false;
         const QPiece pc = cs.pq[pk % PQ_N];
         const int s = pc.s, j0 = pc.j0, j1 = pc.j1;
 
@@ -928,8 +962,8 @@ __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
             const int len = (s == a.KS - 1) ? a.KBlast : a.KBs;
             if (cur_s >= 0 && lane == 0) mbar_arrive(sm.act_free);  // done with the previous split
             if (a.af_frag) {
-                bool issued = false;
-                if (tid == 0) {
+                bool issued = pre_issued && cur_s < 0;  // the phase's first copy, issued at the grid barrier
+                if (tid == 0 && !issued) {
                     if (act_it > 0 && !mbar_wait_bounded(sm.act_free, (act_it - 1) & 1u, WAIT_NS, &cs.abort)) {
                         set_status(a.status, SD_ETIMEOUT);
                         cs.abort = 1;
@@ -993,13 +1027,16 @@ __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
                     accu[PAIR ? nt : 0][t][e] = 0.0f;
                 }
 
-        for (int jj = j0; jj < j1; jj += a.SB) {
-            const int n = j1 - jj < a.SB ? j1 - jj : a.SB;
-            const int stg = static_cast<int>(it % a.NS);
-            const uint32_t ph = (it / a.NS) & 1u;
+        for (int jj = j0; jj < j1; jj += SB) {
+            const int n = j1 - jj < SB ? j1 - jj : SB;
+            if (jj != j0 && !warp_wait(&sm.full[stg], sph, cs, a.status)) return false;
+            const uint8_t *sbase = sm.ring + static_cast<size_t>(stg) * sstride;
+            const uint32_t done = stg;
             ++it;
-            if (jj != j0 && !warp_wait(&sm.full[stg], ph, cs, a.status)) return false;
-            const uint8_t *sbase = sm.ring + static_cast<size_t>(stg) * a.stage_stride;
+            if (++stg == NS) {
+                stg = 0;
+                sph ^= 1u;
+            }
             constexpr int SUB = sub_steps(QT, PAIR);
             constexpr int STEP = (QT == SD_Q8_0 ? 1088 : 576) * (PAIR ? 2 : 1);
             for (int off = 0; off < n; off += SUB) {
@@ -1012,14 +1049,14 @@ __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
                                                        inv, acc, accu);
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.empty[stg]);
+            if (lane == 0) mbar_arrive(&sm.empty[done]);
         }
 
         // hand the piece's partial sums to the finishers
-        const uint32_t b = pk % static_cast<uint32_t>(a.NRB), use = pk / static_cast<uint32_t>(a.NRB);
+        const uint32_t b = pk % NRB, use = pk / NRB;
         ++pk;
         if (!warp_wait(&sm.rempty[b], (use & 1u) ^ 1u, cs, a.status)) return false;
-        float *rb = sm.red + (static_cast<size_t>(b) * NCW + warp) * M * a.rows_p;
+        float *rb = sm.red + (static_cast<size_t>(b) * NCW + warp) * M * rows_p;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -1028,8 +1065,8 @@ __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
                 for (int e = 0; e < 4; ++e) {
                     const int m = nt * 8 + 2 * lc + (e & 1), row = 16 * t + lg + 8 * (e >> 1);
                     if (m < M) {
-                        rb[m * a.rows_p + row] = acc[nt][t][e];
-                        if (PAIR) rb[m * a.rows_p + 32 + row] = accu[PAIR ? nt : 0][t][e];
+                        rb[m * rows_p + row] = acc[nt][t][e];
+                        if (PAIR) rb[m * rows_p + 32 + row] = accu[PAIR ? nt : 0][t][e];
                     }
                 }
         __syncwarp();
@@ -1211,7 +1248,7 @@ __device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &
                 if (m < M) epilogue<PAIR>(a, u, m, lane, v[i], vu[i], res[i], nw);
             }
         }
-        if (finish && a.head) {  // the same decisions on every finisher warp
+        if (finish && a.head && !a.defer_stats) {  // the same decisions on every finisher warp
             const int st = u / (STAT_TILE / 32);
             if (st != st_cur) {
                 head_flush(a, sm, cs, fin_it, st_cur, st_n, lane, f);
@@ -1222,7 +1259,7 @@ __device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &
         }
         if (pc.last) break;
     }
-    if (a.head) head_flush(a, sm, cs, fin_it, st_cur, st_n, lane, f);
+    if (a.head && !a.defer_stats) head_flush(a, sm, cs, fin_it, st_cur, st_n, lane, f);
     return !cs.abort;
 }
 
@@ -1395,17 +1432,20 @@ __global__ void __launch_bounds__(QMM_THREADS, 1)
         return;
     }
     for (int p = 0; p < n_phases; ++p) {
-        bool stop = false;
-        if (p > 0 && tid == 0) {  // grid barrier: every CTA finished phase p - 1
-            const uint32_t target = static_cast<uint32_t>(p) * gridDim.x;
-            const uint64_t t0 = gtimer_ns();
-            while (ld_acquire(barrier_ctr) < target) {
-                if (cs.abort || gtimer_ns() - t0 > WAIT_NS) {
-                    set_status(status, SD_ETIMEOUT);
-                    stop = true;
-                    break;
+        bool stop = false, pre = false;
+        if (tid == 0) {
+            if (p > 0) {  // grid barrier: every CTA finished phase p - 1
+                const uint32_t target = static_cast<uint32_t>(p) * gridDim.x;
+                const uint64_t t0 = gtimer_ns();
+                while (ld_acquire(barrier_ctr) < target) {
+                    if (cs.abort || gtimer_ns() - t0 > WAIT_NS) {
+                        set_status(status, SD_ETIMEOUT);
+                        stop = true;
+                        break;
+                    }
                 }
             }
+            if (!stop) pre = pre_issue_staging(phases[p], sm, act_it, cs);
         }
         if (warp < NCW) {  // copy the phase descriptor into shared memory (constant: may overlap the wait)
             const uint32_t *src = reinterpret_cast<const uint32_t *>(phases + p);
@@ -1420,19 +1460,30 @@ __global__ void __launch_bounds__(QMM_THREADS, 1)
         if (sa.kind == KIND_NORM) {
             if (warp < NCW) norm_phase(sa);
         } else if (sa.kind == KIND_ACCEPT) {
-            if (blockIdx.x == 0 && tid == 0)
-                greedy_accept(sa.argmax, sa.tokens, sa.parent, sa.M, sa.out_tokens, sa.out_count);
+            if (blockIdx.x == 0) {  // the deferred fold (one warp per position), then the acceptance
+                if (sa.defer_stats) {
+                    for (int m = warp < NCW ? warp : warp - 1; m < sa.M; m += NCW + NF) head_final_fold_one(sa, m, lane);
+                    named_bar_sync(BAR_WORK, WORK_THREADS);
+                }
+                if (tid == 0) greedy_accept(sa.argmax, sa.tokens, sa.parent, sa.M, sa.out_tokens, sa.out_count);
+            }
         } else if (sa.kind == KIND_COMBINE) {
             combine_phase(sa, warp < NCW ? warp : warp - 1);
+        } else if (sa.kind == KIND_HSTATS) {  // (tile, position) items over every work warp of the grid
+            constexpr int NWW = NCW + NF;
+            const int n_items = sa.n_stiles * sa.M;
+            for (int i = static_cast<int>(blockIdx.x) * NWW + (warp < NCW ? warp : warp - 1); i < n_items;
+                 i += static_cast<int>(gridDim.x) * NWW)
+                head_tile_stats_one(sa, i / sa.M, i % sa.M, lane);
         } else if (warp >= FIN_WARP0) {
             const int f = warp - FIN_WARP0;
             ok = sa.pair ? finish_phase<1, NT>(sa, sm, pk, fin_it, cs, f) : finish_phase<0, NT>(sa, sm, pk, fin_it, cs, f);
         } else if (sa.qt == SD_Q4_32 && sa.pair) {
-            ok = consume_phase<SD_Q4_32, 1, NT>(sa, sm, it, pk, act_it, nrm_it, cs);
+            ok = consume_phase<SD_Q4_32, 1, NT>(sa, sm, it, pk, act_it, nrm_it, cs, pre);
         } else if (sa.qt == SD_Q4_32) {
-            ok = consume_phase<SD_Q4_32, 0, NT>(sa, sm, it, pk, act_it, nrm_it, cs);
+            ok = consume_phase<SD_Q4_32, 0, NT>(sa, sm, it, pk, act_it, nrm_it, cs, pre);
         } else {
-            ok = consume_phase<SD_Q8_0, 0, NT>(sa, sm, it, pk, act_it, nrm_it, cs);
+            ok = consume_phase<SD_Q8_0, 0, NT>(sa, sm, it, pk, act_it, nrm_it, cs, pre);
         }
         // every write of phase p (consumers and finishers) before thread 0's release
         if (bar_any(BAR_WORK, WORK_THREADS, !ok)) {
