@@ -489,19 +489,21 @@ __device__ inline void head_tile_stats_one(const QmmArgs &a, int st, int m, int 
     float zmax = -__int_as_float(0x7f800000);
     float bl = -__int_as_float(0x7f800000);
     int bi = 0x7fffffff;
+    // every load in flight before the first compare; -inf past the vocabulary changes nothing below
 #pragma unroll
     for (int r = 0; r < 32; ++r) {
         const int64_t e = static_cast<int64_t>(st) * STAT_TILE + lane + 32 * r;
-        float z = -__int_as_float(0x7f800000);
-        if (e < V) {
-            const float l = __ldcg(a.y + m * V + e);
-            if (l > bl) {
-                bl = l;
-                bi = static_cast<int>(e);
-            }
-            z = unit_t ? l : __fdiv_rn(l, a.T);
-            zmax = fmaxf(zmax, z);
+        v[r] = e < V ? __ldcg(a.y + m * V + e) : -__int_as_float(0x7f800000);
+    }
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+        const float l = v[r];
+        if (l > bl) {
+            bl = l;
+            bi = static_cast<int>(static_cast<int64_t>(st) * STAT_TILE + lane + 32 * r);
         }
+        const float z = unit_t ? l : __fdiv_rn(l, a.T);
+        zmax = fmaxf(zmax, z);
         v[r] = z;
     }
 #pragma unroll
@@ -533,6 +535,51 @@ __device__ inline void head_final_fold_one(const QmmArgs &a, int m, int lane) {
     float mx = -__int_as_float(0x7f800000);
     float bl = -__int_as_float(0x7f800000);
     int bi = 0x7fffffff;
+    if (a.n_stiles <= 256) {  // every tile's statistics in registers at once: one round of loads
+        float4 p[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int t = lane + 32 * k;
+            p[k] = t < a.n_stiles ? __ldcg(a.st_part + t * MPAD + m)
+                                  : make_float4(-__int_as_float(0x7f800000), 0.0f, __int_as_float(0x7fffffff),
+                                                -__int_as_float(0x7f800000));
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            mx = fmaxf(mx, p[k].x);
+            const int pi = __float_as_int(p[k].z);
+            if (p[k].w > bl || (p[k].w == bl && pi < bi)) {
+                bl = p[k].w;
+                bi = pi;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            const float ol = __shfl_xor_sync(0xffffffffu, bl, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ol > bl || (ol == bl && oi < bi)) {
+                bl = ol;
+                bi = oi;
+            }
+        }
+        float Z = 0.0f;  // sequential over tiles, as below
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int t0 = 32 * k;
+            if (t0 < a.n_stiles) {
+                const float e = t0 + lane < a.n_stiles ? __fmul_rn(p[k].y, cexpf_canon(__fsub_rn(p[k].x, mx))) : 0.0f;
+                const int nn = a.n_stiles - t0 < 32 ? a.n_stiles - t0 : 32;
+                for (int j = 0; j < nn; ++j) Z = __fadd_rn(Z, __shfl_sync(0xffffffffu, e, j));
+            }
+        }
+        if (lane == 0) {
+            a.argmax[m] = bi;
+            a.row_max[m] = mx;
+            a.row_sumexp[m] = Z;
+        }
+        return;
+    }
     for (int t = lane; t < a.n_stiles; t += 32) {
         const float4 p = __ldcg(a.st_part + t * MPAD + m);
         mx = fmaxf(mx, p.x);
@@ -1299,6 +1346,7 @@ __device__ inline void norm_phase(const QmmArgs &a) {
 // ---------------------------------------------------------------------------
 __device__ inline void combine_phase(const QmmArgs &a, int widx) {
     constexpr int ROWS = 32, CH = 8, NWW = NCW + NF;
+    constexpr int CKS = 8, CP = 4;  // splits and pieces per split held in registers at once
     const int lane = threadIdx.x & 31, M = a.M;
     const int u0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * a.NU / gridDim.x);
     const int u1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * a.NU / gridDim.x);
@@ -1311,6 +1359,32 @@ __device__ inline void combine_phase(const QmmArgs &a, int widx) {
         const float nw = (a.norm_next && nok) ? __ldg(a.norm_next + n) : 0.0f;
         float v = 0.0f;
         bool first = true;
+        if (a.KS <= CKS && a.P <= CP) {  // every partial sum of the unit in one round of loads
+            int np[CKS];
+            float x[CKS][CP];
+#pragma unroll
+            for (int s2 = 0; s2 < CKS; ++s2) {
+                int f2;
+                np[s2] = 0;
+                if (s2 < a.KS) unit_split_owners(a, s2, u, f2, np[s2]);
+            }
+#pragma unroll
+            for (int s2 = 0; s2 < CKS; ++s2) {
+                const float *qs = a.part + (static_cast<int64_t>(u) * a.KS + s2) * a.P * (ROWS * MPAD) + m * ROWS + lane;
+#pragma unroll
+                for (int c = 0; c < CP; ++c) x[s2][c] = c < np[s2] ? __ldcg(qs + c * (ROWS * MPAD)) : 0.0f;
+            }
+#pragma unroll
+            for (int s2 = 0; s2 < CKS; ++s2)
+#pragma unroll
+                for (int c = 0; c < CP; ++c)
+                    if (c < np[s2]) {  // (split, piece) order, as in the chunked walk below
+                        v = first ? x[s2][c] : __fadd_rn(v, x[s2][c]);
+                        first = false;
+                    }
+            epilogue<0>(a, u, m, lane, v, 0.0f, res, nw);
+            continue;
+        }
         for (int s2 = 0; s2 < a.KS; ++s2) {
             int f2, np;
             unit_split_owners(a, s2, u, f2, np);
@@ -1432,6 +1506,14 @@ __global__ void __launch_bounds__(QMM_THREADS, 1)
         return;
     }
     for (int p = 0; p < n_phases; ++p) {
+        // the phase descriptor into shared memory before the grid barrier: it is constant, and every
+        // work thread left the previous one at the phase-end barrier
+        if (warp < NCW) {
+            const uint32_t *src = reinterpret_cast<const uint32_t *>(phases + p);
+            uint32_t *dst = reinterpret_cast<uint32_t *>(&sa);
+            for (int i = tid; i < static_cast<int>(sizeof(QmmArgs) / 4); i += CONS_THREADS) dst[i] = src[i];
+            named_bar_sync(BAR_CONS, CONS_THREADS);
+        }
         bool stop = false, pre = false;
         if (tid == 0) {
             if (p > 0) {  // grid barrier: every CTA finished phase p - 1
@@ -1445,12 +1527,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1)
                     }
                 }
             }
-            if (!stop) pre = pre_issue_staging(phases[p], sm, act_it, cs);
-        }
-        if (warp < NCW) {  // copy the phase descriptor into shared memory (constant: may overlap the wait)
-            const uint32_t *src = reinterpret_cast<const uint32_t *>(phases + p);
-            uint32_t *dst = reinterpret_cast<uint32_t *>(&sa);
-            for (int i = tid; i < static_cast<int>(sizeof(QmmArgs) / 4); i += CONS_THREADS) dst[i] = src[i];
+            if (!stop) pre = pre_issue_staging(sa, sm, act_it, cs);
         }
         if (bar_any(BAR_WORK, WORK_THREADS, stop)) {
             cs.abort = 1;
@@ -1472,8 +1549,8 @@ __global__ void __launch_bounds__(QMM_THREADS, 1)
         } else if (sa.kind == KIND_HSTATS) {  // (tile, position) items over every work warp of the grid
             constexpr int NWW = NCW + NF;
             const int n_items = sa.n_stiles * sa.M;
-            for (int i = static_cast<int>(blockIdx.x) * NWW + (warp < NCW ? warp : warp - 1); i < n_items;
-                 i += static_cast<int>(gridDim.x) * NWW)
+            for (int i = (warp < NCW ? warp : warp - 1) * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x);
+                 i < n_items; i += static_cast<int>(gridDim.x) * NWW)
                 head_tile_stats_one(sa, i / sa.M, i % sa.M, lane);
         } else if (warp >= FIN_WARP0) {
             const int f = warp - FIN_WARP0;

@@ -6,11 +6,15 @@
 * The 5120 x 151936 Q8_0 head at K+1 = 5: logits, argmax and statistics against
   the oracle; greedy and rejection-sampling acceptance (general drafter and
   certainty drafter) bit-exact when fed the oracle's logits.
-* The 64-layer stack in the launch configuration the bench times (one CUDA
-  graph per pass): stage-wise parity on three layers with oracle inputs, every
-  row of the pass bit-equal to that row run alone, the chain/tree acceptance
-  rule on the pass's own argmax, and the free-running divergence from the
-  oracle's own 64-layer pass (reported; its float parity is unpinned).
+* The 64-layer stack as one CUDA graph of per-operation launches: stage-wise
+  parity on three layers with oracle inputs, every row of the pass bit-equal
+  to that row run alone, the chain/tree acceptance rule on the pass's own
+  argmax, and the free-running divergence from the oracle's own 64-layer pass
+  (reported; its float parity is unpinned).
+* The same stack as the one persistent launch the bench times (its deferred
+  down-projection combine and head-statistics phases exist only at these
+  widths): every output bit-equal to the per-operation pass, at M = 5 (chain)
+  and M = 16 (tree).
 """
 import numpy as np
 import pytest
@@ -315,3 +319,36 @@ def test_tree_pass_batch_invariant(sdv, stack_env):
         status_ok()
         assert np.array_equal(host(s1.logits).view(np.uint32), lg[m:m + 1].view(np.uint32))
         del s1
+
+
+@pytest.mark.parametrize("M", [5, 16])
+def test_stack_fused_pass_equals_per_op_pass(sdv, stack_env, M):
+    """The one-launch pass against the per-operation pass on the 64-layer stack: hidden rows, logits,
+    statistics, requantised activations and the accepted tokens, all bit-equal."""
+    spec = stack_env["spec"]
+    parent = cuda(sdgen.tree16(0)[0]) if M == 16 else None
+    h0 = cuda(spec.hidden_in(M)) if M == 5 else cuda(sdgen.normal(sdgen.key(6, 2), (M, H)))
+    a = stack_env["make"](M, parent)
+    a.h.copy_(h0)
+    a.run()
+    torch.cuda.synchronize()
+    am = host(a.argmax)
+    # drafts: the pass's own argmax for the first two, then a miss
+    tokens = np.array([am[i] if i < 2 else (am[i] + 1) % V for i in range(M)], np.int32)
+    if M == 16:
+        tokens = np.roll(tokens, 1)  # node i's draft is judged against its parent's argmax
+    a.tokens.copy_(cuda(tokens))
+    b = stack_env["make"](M, parent)
+    b.tokens.copy_(cuda(tokens))
+    a.h.copy_(h0)
+    a.run()
+    b.h.copy_(h0)
+    b.run_fused()
+    status_ok()
+    for name in ("h", "logits", "argmax", "row_max", "row_sumexp", "qa", "sa", "qv", "sv", "qf", "sf"):
+        x, y = getattr(a, name), getattr(b, name)
+        assert torch.equal(x.view(torch.int32) if x.dtype == torch.float32 else x,
+                           y.view(torch.int32) if y.dtype == torch.float32 else y), name
+    n = int(host(a.out_count)[0])
+    assert n >= 1 and int(host(b.out_count)[0]) == n
+    assert torch.equal(a.out_tokens[:n], b.out_tokens[:n])
