@@ -278,16 +278,27 @@ __device__ __forceinline__ void mma_acc(float (&d)[4], const uint32_t (&a)[4], u
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// (x & MASK) | magic as one three-input logic operation (lookup table 0xEA = (a & b) | c), the
+// mask as an immediate and the exponent bits in a register: the compiler left to itself splits
+// it in two, and this unpack is the integer pipe's largest load in the consumer loop
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t and_or(uint32_t x, uint32_t magic) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(x), "n"(MASK), "r"(magic));
+    return r;
+}
+
 // 4-bit codes of one lane -> fp16 pairs (1024 + code, or 1024 + 16 code in the k+8 halves)
 __device__ __forceinline__ void q4_frag(uint4 w, uint32_t (&a)[2][2][4]) {
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    const uint32_t magic = 0x64006400u;  // fp16 exponent of 1024 in both halves
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const uint32_t x = ws[j], y = x >> 8;
-        a[j >> 1][j & 1][0] = (x & 0x000F000Fu) | 0x64006400u;
-        a[j >> 1][j & 1][1] = (y & 0x000F000Fu) | 0x64006400u;
-        a[j >> 1][j & 1][2] = (x & 0x00F000F0u) | 0x64006400u;
-        a[j >> 1][j & 1][3] = (y & 0x00F000F0u) | 0x64006400u;
+        a[j >> 1][j & 1][0] = and_or<0x000F000Fu>(x, magic);
+        a[j >> 1][j & 1][1] = and_or<0x000F000Fu>(y, magic);
+        a[j >> 1][j & 1][2] = and_or<0x00F000F0u>(x, magic);
+        a[j >> 1][j & 1][3] = and_or<0x00F000F0u>(y, magic);
     }
 }
 
