@@ -56,7 +56,10 @@ constexpr int KB_SPLIT_MAX = 160;      // blocks per k-split
 constexpr int MPAD = 16;               // position stride of workspace partials
 constexpr int MAX_NS = 10;             // ring stages (mbarrier header room)
 constexpr uint64_t WAIT_NS = 2000000000ull;     // 2 s bound on any in-kernel wait
-constexpr uint64_t KERNEL_NS = 10000000000ull;  // 10 s bound on any launch's loops (self-check)
+// Bound on any launch's loops (self-check), in SM clock cycles: 10 s at 2.2 GHz, longer at lower
+// clocks.  Counted with the SM's cycle counter: reading the global timer costs far more, and
+// the check runs once per piece.
+constexpr long long KERNEL_CYCLES = 22000000000ll;
 constexpr int STAT_TILE = 1024;        // vocabulary tile of the softmax statistics
 constexpr int WS_UNIT_CNT = 32768;     // workspace counters: units (tiles / tile pairs) per call
 constexpr int WS_STAT_CNT = 2048;      // workspace counters: 1024-token statistics tiles
@@ -649,14 +652,14 @@ struct CtaShared {
     volatile int abort;    // set by anyone whose bounded wait ran out; polled by every wait
     int fin_flag;          // finishers: warp 0's decision, published to the other finisher warps
     float inv[16];         // RMSNorm row factors of the current normalised staging
-    uint64_t t0;           // launch start (globaltimer), for the launch-wide time bound
+    long long t0;          // launch start (SM cycle counter), for the launch-wide time bound
     QPiece pq[PQ_N];       // the schedule, piece k in slot k % PQ_N
 };
 
-// Launch-wide self-check: past KERNEL_NS since the CTA started, record SD_ETIMEOUT and where
+// Launch-wide self-check: past KERNEL_CYCLES since the CTA started, record SD_ETIMEOUT and where
 // (status[1]: 1 producer, 2 consumer).
 __device__ __forceinline__ bool out_of_time(const CtaShared &cs, int *status, int where) {
-    if (gtimer_ns() - cs.t0 <= KERNEL_NS) return false;
+    if (clock64() - cs.t0 <= KERNEL_CYCLES) return false;
     if (status && atomicCAS(status, 0, SD_ETIMEOUT) == 0) status[1] = where;
     return true;
 }
@@ -710,7 +713,7 @@ __device__ __forceinline__ void cta_init(const Smem &sm, int NS, CtaShared &cs, 
     mbar_init(sm.fin_b, 1);
     mbar_init(sm.inv_bar, NCW);
     cs.abort = 0;
-    cs.t0 = gtimer_ns();
+    cs.t0 = clock64();
     fence_barrier_init();
 }
 
@@ -1194,6 +1197,7 @@ __device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &
     constexpr int ROWS = PAIR ? 64 : 32;
     constexpr int FIN_MPW = (8 * NT + NF - 1) / NF;  // positions per finisher warp at most
     constexpr int CH = 8;                            // partial sums loaded together
+    constexpr int FKS = 8, FP = 4;                   // splits x pieces held at once when all splits share
     const int M = a.M;
     const int lane = threadIdx.x & 31;
     int st_cur = -1, st_n = 0;  // head: current statistics tile and tiles finished in it
@@ -1261,7 +1265,42 @@ __device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &
                 return static_cast<int>(old) == pc.expected - 1;
             });
             if (cs.abort) return false;
-            if (finish) {  // the acquire in the counter update orders the loads below
+            if (finish && !PAIR && a.KS > 1 && a.KS <= FKS && a.P <= FP) {
+                // every partial sum of the unit in one round of loads per position, added in
+                // (split, piece) order as in the chunked walk below
+                int npa[FKS];
+#pragma unroll
+                for (int s2 = 0; s2 < FKS; ++s2) {
+                    int f2;
+                    npa[s2] = 0;
+                    if (s2 < a.KS) unit_split_owners(a, s2, u, f2, npa[s2]);
+                }
+#pragma unroll
+                for (int i = 0; i < FIN_MPW; ++i) {
+                    const int m = f + NF * i;
+                    v[i] = 0.0f;
+                    if (m < M) {
+                        float x[FKS][FP];
+#pragma unroll
+                        for (int s2 = 0; s2 < FKS; ++s2) {
+                            const float *qs = a.part + (static_cast<int64_t>(u) * a.KS + s2) * a.P * (ROWS * MPAD) +
+                                              m * ROWS + lane;
+#pragma unroll
+                            for (int c = 0; c < FP; ++c) x[s2][c] = c < npa[s2] ? __ldcg(qs + c * (ROWS * MPAD)) : 0.0f;
+                        }
+                        bool first = true;
+#pragma unroll
+                        for (int s2 = 0; s2 < FKS; ++s2)
+#pragma unroll
+                            for (int c = 0; c < FP; ++c)
+                                if (c < npa[s2]) {
+                                    v[i] = first ? x[s2][c] : __fadd_rn(v[i], x[s2][c]);
+                                    first = false;
+                                }
+                    }
+                }
+                if (f == 0 && lane == 0) a.cnt[u] = 0u;
+            } else if (finish) {  // the acquire in the counter update orders the loads below
 #pragma unroll
                 for (int i = 0; i < FIN_MPW; ++i) v[i] = vu[i] = 0.0f;
                 bool first = true;
