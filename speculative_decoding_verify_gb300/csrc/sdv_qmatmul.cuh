@@ -752,7 +752,8 @@ __device__ inline void produce_phase(const QmmArgs &a, const Smem &sm, uint32_t 
             q.first = pc.first;
             q.np = pc.np;
             int expected = pc.np;
-            if (a.KS > 1) {  // a shared unit waits for the pieces of all its splits
+            if (a.KS > 1 && !a.defer) {  // a shared unit waits for the pieces of all its splits (unused
+                                         // when a combine phase adds them: the walk is costly)
                 expected = 0;
                 for (int s2 = 0; s2 < a.KS; ++s2) {
                     int f2, np2;
