@@ -247,7 +247,7 @@ sd_status sd_accept_sample(const float *logits, int64_t vocab, int32_t K, const 
  * epilogue) -> O on those codes (+ residual into h) -> RMSNorm + requant ->
  * gate|up (SiLU*mul requant epilogue) -> down (+ residual into h); then the final
  * RMSNorm, the Q8_0 vocabulary head with argmax / statistics, and greedy
- * acceptance (chain, or tree when parent != NULL).  Every phase runs the same
+ * acceptance (chain, or tree when parent != NULL) or rejection sampling (below).  Every phase runs the same
  * device code as the single-operation calls above, so the pass produces the
  * same bits as issuing those calls one by one.  Between phases the CTAs meet at
  * a grid barrier (release/acquire on a counter in the plan, each wait bounded
@@ -261,6 +261,11 @@ sd_status sd_accept_sample(const float *logits, int64_t vocab, int32_t K, const 
  * activation scratch; logits [M][vocab], argmax/row_max/row_sumexp [M];
  * tokens = drafts [M-1] (chain) or node tokens [M] (tree); out_tokens [M],
  * out_count [1].  workspace: >= sd_pass_workspace_bytes, zero-filled once.
+ * accept = SD_ACCEPT_SAMPLE replaces greedy acceptance by the rejection sampling of
+ * sd_accept_sample on the pass's own logits and statistics (drafts = tokens
+ * [M-1], K = M - 1, temperature, q_probs, seed, base_pos as there; chains only:
+ * parent must be NULL, else SD_EUNSUPPORTED); it produces the same tokens as the
+ * head followed by sd_accept_sample.
  * layers is a HOST array read only by sd_pass_prepare.
  * sd_pass_prepare writes the phase table into `plan` (device, 256-byte aligned,
  * >= sd_pass_plan_bytes(n_layers), synchronously) and fills `out`;
@@ -300,7 +305,13 @@ typedef struct {
     int32_t *out_count;
     void *workspace;
     size_t ws_bytes;
+    int32_t accept;        /* SD_ACCEPT_GREEDY (0) or SD_ACCEPT_SAMPLE (1) */
+    const float *q_probs;  /* SD_ACCEPT_SAMPLE: drafter probabilities [M-1][vocab], NULL = certainty drafter */
+    uint64_t seed;         /* SD_ACCEPT_SAMPLE: Philox key and position of the first draft */
+    int64_t base_pos;
 } sd_pass_desc;
+
+typedef enum { SD_ACCEPT_GREEDY = 0, SD_ACCEPT_SAMPLE = 1 } sd_accept_mode;
 
 typedef struct {
     void *plan;
@@ -308,6 +319,7 @@ typedef struct {
     int32_t nt;
     uint32_t smem_bytes;
     int32_t grid;
+    int32_t accept; /* the descriptor's acceptance mode */
 } sd_pass;
 
 size_t sd_pass_plan_bytes(int32_t n_layers);

@@ -44,12 +44,16 @@ class SdPassDesc(ctypes.Structure):
                 ("qf", ctypes.c_void_p), ("sf", ctypes.c_void_p), ("logits", ctypes.c_void_p),
                 ("argmax", ctypes.c_void_p), ("row_max", ctypes.c_void_p), ("row_sumexp", ctypes.c_void_p),
                 ("tokens", ctypes.c_void_p), ("parent", ctypes.c_void_p), ("out_tokens", ctypes.c_void_p),
-                ("out_count", ctypes.c_void_p), ("workspace", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t)]
+                ("out_count", ctypes.c_void_p), ("workspace", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t),
+                ("accept", ctypes.c_int32), ("q_probs", ctypes.c_void_p), ("seed", ctypes.c_uint64),
+                ("base_pos", ctypes.c_int64)]
+
+ACCEPT_GREEDY, ACCEPT_SAMPLE = 0, 1
 
 
 class SdPass(ctypes.Structure):
     _fields_ = [("plan", ctypes.c_void_p), ("n_phases", ctypes.c_int32), ("nt", ctypes.c_int32),
-                ("smem_bytes", ctypes.c_uint32), ("grid", ctypes.c_int32)]
+                ("smem_bytes", ctypes.c_uint32), ("grid", ctypes.c_int32), ("accept", ctypes.c_int32)]
 
 
 class SdError(RuntimeError):

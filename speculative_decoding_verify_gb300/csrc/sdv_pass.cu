@@ -2,8 +2,8 @@
 // persistent cooperative launch: the first RMSNorm; per layer QKV (V requantised
 // in the epilogue) -> O (+ residual; the next RMSNorm's codes in the epilogue)
 // -> gate|up (SiLU*mul requant) -> down (+ residual; the next RMSNorm's codes);
-// then the vocabulary head with fused argmax and statistics, and greedy
-// acceptance.  An RMSNorm's row factor 1/rms is applied where its codes are
+// then the vocabulary head with fused argmax and statistics, and greedy or
+// rejection-sampling acceptance.  An RMSNorm's row factor 1/rms is applied where its codes are
 // staged by the next matmul, from block sums of squares the epilogues leave.
 // The arithmetic is that of the single-operation entry points, so the pass
 // equals them bit for bit.
@@ -18,24 +18,11 @@ struct PassHeader {
     uint32_t pad[63];
 };
 
-static cudaError_t pass_launch(const QmmArgs *phases, int n_phases, uint32_t *ctr, int nt, size_t smem, int grid,
-                               cudaStream_t s) {
-    void (*k)(const QmmArgs *, int, uint32_t *) = nt == 1 ? pass_kernel<1> : pass_kernel<2>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    e = cudaMemsetAsync(ctr, 0, sizeof(uint32_t), s);
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(QMM_THREADS);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs resident, or the launch fails
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k, phases, n_phases, ctr);
+static cudaError_t pass_launch(const QmmArgs *phases, int n_phases, uint32_t *ctr, int nt, int sample, size_t smem,
+                               int grid, cudaStream_t s) {
+    if (sample) return pass_launch_sampling(phases, n_phases, ctr, nt, smem, grid, s);
+    return pass_launch_kernel(nt == 1 ? pass_kernel<1, false> : pass_kernel<2, false>, phases, n_phases, ctr, smem,
+                              grid, s);
 }
 
 }  // namespace sdv
@@ -119,6 +106,10 @@ sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, 
         return SD_EINVAL;
     if (M > 1 && !d->tokens) return SD_EINVAL;
     if (!(d->temperature > 0.0f)) return SD_EINVAL;
+    if (d->accept != SD_ACCEPT_GREEDY && d->accept != SD_ACCEPT_SAMPLE) return SD_EINVAL;
+    if (d->accept == SD_ACCEPT_SAMPLE &&
+        (d->parent || V > static_cast<int64_t>(MAX_TILES) * ATILE || !(d->temperature <= 3.0e38f)))
+        return SD_EUNSUPPORTED;  // sampling: chains only, the single-operation call's vocabulary limit
     int *st = status_ptr();
     if (!st) return SD_ECUDA;
     const int sms = num_sms();
@@ -284,6 +275,11 @@ sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, 
         a.parent = d->parent;
         a.out_tokens = d->out_tokens;
         a.out_count = d->out_count;
+        a.accept_mode = d->accept;
+        a.y = d->logits;
+        a.q_probs = d->q_probs;
+        a.seed = d->seed;
+        a.base_pos = d->base_pos;
         ph.push_back(a);
     }
     // one shared-memory layout for every phase: the largest split, pair rows, the largest stage,
@@ -298,6 +294,7 @@ sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, 
         }
     SmemLayout lay;
     if (!layout_smem(kbs, M, 64, slot, static_cast<size_t>(M) * ss_ld * sizeof(float), lay)) return SD_EUNSUPPORTED;
+    if (static_cast<size_t>(lay.NS) * slot < sizeof(SampleShared)) return SD_EUNSUPPORTED;  // the sampler's state
     for (QmmArgs &a : ph) apply_layout(a, lay, slot);
     PassHeader hdr = {};
     if (cudaMemcpy(plan, &hdr, sizeof(hdr), cudaMemcpyHostToDevice) != cudaSuccess) return SD_ECUDA;
@@ -309,15 +306,19 @@ sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, 
     out->nt = NT;
     out->smem_bytes = static_cast<uint32_t>(lay.total);
     out->grid = sms;
+    out->accept = d->accept;
     return SD_OK;
 }
 
 sd_status sd_verify_pass(const sd_pass *p, sd_stream_t stream) {
-    if (!p || !p->plan || p->n_phases < 1 || (p->nt != 1 && p->nt != 2) || p->grid < 1) return SD_EINVAL;
+    if (!p || !p->plan || p->n_phases < 1 || (p->nt != 1 && p->nt != 2) || p->grid < 1 ||
+        (p->accept != SD_ACCEPT_GREEDY && p->accept != SD_ACCEPT_SAMPLE))
+        return SD_EINVAL;
     uint8_t *plan = static_cast<uint8_t *>(p->plan);
     const QmmArgs *phases = reinterpret_cast<const QmmArgs *>(plan + sizeof(PassHeader));
     uint32_t *ctr = reinterpret_cast<uint32_t *>(plan);
-    return pass_launch(phases, p->n_phases, ctr, p->nt, p->smem_bytes, p->grid, reinterpret_cast<cudaStream_t>(stream)) ==
+    return pass_launch(phases, p->n_phases, ctr, p->nt, p->accept, p->smem_bytes, p->grid,
+                       reinterpret_cast<cudaStream_t>(stream)) ==
                    cudaSuccess
                ? SD_OK
                : SD_ECUDA;

@@ -39,6 +39,7 @@
 #pragma once
 
 #include "sdv_common.cuh"
+#include "sdv_sample.cuh"
 
 namespace sdv {
 
@@ -153,6 +154,10 @@ struct QmmArgs {
     const int32_t *parent;
     int32_t *out_tokens;
     int32_t *out_count;
+    int32_t accept_mode;    // acceptance: 0 greedy, 1 rejection sampling (chain)
+    const float *q_probs;   // sampling: drafter probabilities [M-1][n_out] (null: certainty drafter)
+    uint64_t seed;          // sampling: Philox key and first position
+    int64_t base_pos;
 };
 
 constexpr int KIND_MATMUL = 0, KIND_NORM = 1, KIND_ACCEPT = 2, KIND_COMBINE = 3, KIND_HSTATS = 4;
@@ -1533,7 +1538,29 @@ __device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-template <int NT>
+// Rejection-sampling acceptance by every work warp of one CTA (work-thread index wtid); `scratch`
+// (the weight ring, idle by then) holds the shared state.
+__device__ __forceinline__ void pass_sample_accept(const QmmArgs &sa, uint8_t *scratch, int wtid) {
+    SampleArgs g;
+    g.logits = sa.y;
+    g.V = sa.n_out;
+    g.K = sa.M - 1;
+    g.row_max = sa.row_max;
+    g.row_sumexp = sa.row_sumexp;
+    g.q = sa.q_probs;
+    g.drafts = sa.tokens;
+    g.T = sa.T;
+    g.seed = sa.seed;
+    g.base_pos = sa.base_pos;
+    g.out = sa.out_tokens;
+    g.count = sa.out_count;
+    sample_accept<WORK_THREADS>(g, *reinterpret_cast<SampleShared *>(scratch), wtid,
+                                []() { named_bar_sync(BAR_WORK, WORK_THREADS); });
+}
+
+// SAMPLE: the acceptance phase may run rejection sampling (a separate instantiation, so that the
+// greedy pass's code and register allocation stay those of the matmul loops alone)
+template <int NT, bool SAMPLE>
 __global__ void __launch_bounds__(QMM_THREADS, 1)
     pass_kernel(const QmmArgs *__restrict__ phases, int n_phases, uint32_t *barrier_ctr) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -1593,7 +1620,11 @@ __global__ void __launch_bounds__(QMM_THREADS, 1)
                     for (int m = warp < NCW ? warp : warp - 1; m < sa.M; m += NCW + NF) head_final_fold_one(sa, m, lane);
                     named_bar_sync(BAR_WORK, WORK_THREADS);
                 }
-                if (tid == 0) greedy_accept(sa.argmax, sa.tokens, sa.parent, sa.M, sa.out_tokens, sa.out_count);
+                if (SAMPLE && sa.accept_mode == 1) {
+                    if constexpr (SAMPLE) pass_sample_accept(sa, sm.ring, (warp < NCW ? warp : warp - 1) * 32 + lane);
+                } else if (tid == 0) {
+                    greedy_accept(sa.argmax, sa.tokens, sa.parent, sa.M, sa.out_tokens, sa.out_count);
+                }
             }
         } else if (sa.kind == KIND_COMBINE) {
             combine_phase(sa, warp < NCW ? warp : warp - 1);
@@ -1621,6 +1652,30 @@ __global__ void __launch_bounds__(QMM_THREADS, 1)
         if (tid == 0) red_release_add(barrier_ctr, 1u);
     }
 }
+
+// One cooperative launch of a pass kernel: every CTA resident at once, or the launch fails.
+inline cudaError_t pass_launch_kernel(void (*k)(const QmmArgs *, int, uint32_t *), const QmmArgs *phases,
+                                      int n_phases, uint32_t *ctr, size_t smem, int grid, cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    e = cudaMemsetAsync(ctr, 0, sizeof(uint32_t), s);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(QMM_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, phases, n_phases, ctr);
+}
+
+// the sampling instantiations, compiled in their own translation unit (sdv_pass_sample.cu)
+cudaError_t pass_launch_sampling(const QmmArgs *phases, int n_phases, uint32_t *ctr, int nt, size_t smem, int grid,
+                                 cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // host side: plan + launch

@@ -15,8 +15,8 @@ import torch
 
 import ctypes
 
-from . import (EPI_NONE, EPI_REQUANT, EPI_SILU_MUL_REQUANT, Q4_32, Q8_0, SdLayer, SdPassDesc, accept_greedy,
-               head_logits, head_workspace_bytes, pass_plan_bytes, pass_prepare, pass_workspace_bytes,
+from . import (ACCEPT_GREEDY, ACCEPT_SAMPLE, EPI_NONE, EPI_REQUANT, EPI_SILU_MUL_REQUANT, Q4_32, Q8_0, SdLayer,
+               SdPassDesc, accept_greedy, accept_sample, head_logits, head_workspace_bytes, pass_plan_bytes, pass_prepare, pass_workspace_bytes,
                qmatmul_multipos, qmatmul_workspace_bytes, repack_weights, rmsnorm_quant_acts, verify_pass,
                workspace)
 
@@ -82,6 +82,12 @@ class VerifyStack:
     def accept(self):
         accept_greedy(self.argmax, self.tokens, self.parent, self.M, self.out_tokens, self.out_count)
 
+    def accept_sampled(self, temperature: float, seed: int, base_pos: int = 0, q_probs=None):
+        """Rejection-sampling acceptance of the drafts self.tokens[:M-1] on this pass's logits and statistics."""
+        accept_sample(self.logits, self.M - 1, self.tokens if self.M > 1 else None, self.out_tokens, self.out_count,
+                      q_probs=q_probs, row_max=self.row_max, row_sumexp=self.row_sumexp, temperature=temperature,
+                      seed=seed, base_pos=base_pos)
+
     def run(self):
         """One verify pass over self.h (input hidden rows) and self.tokens (drafts)."""
         for l in range(len(self.layers)):
@@ -90,8 +96,12 @@ class VerifyStack:
         self.accept()
 
     # -- the same pass as one persistent cooperative launch -----------------------
-    def prepare_fused(self, temperature: float = 1.0):
-        """Build the phase table of the one-launch pass over this stack's buffers."""
+    def prepare_fused(self, temperature: float = 1.0, sample: bool = False, seed: int = 0, base_pos: int = 0,
+                      q_probs=None):
+        """Build the phase table of the one-launch pass over this stack's buffers; `sample` ends it with
+        rejection-sampling acceptance (temperature, seed, base_pos, q_probs as in accept_sample)
+        instead of greedy acceptance."""
+        self._q_probs = q_probs
         L = len(self.layers)
         arr = (SdLayer * max(L, 1))()
         for l in range(L):
@@ -105,13 +115,14 @@ class VerifyStack:
                        ctypes.cast(arr, ctypes.POINTER(SdLayer)), p(self.final_norm), p(self.head_w), p(self.h),
                        p(self.qa), p(self.sa), p(self.qv), p(self.sv), p(self.qf), p(self.sf), p(self.logits),
                        p(self.argmax), p(self.row_max), p(self.row_sumexp), p(self.tokens), p(self.parent),
-                       p(self.out_tokens), p(self.out_count), p(self.ws), self.ws.numel())
+                       p(self.out_tokens), p(self.out_count), p(self.ws), self.ws.numel(),
+                       ACCEPT_SAMPLE if sample else ACCEPT_GREEDY, p(q_probs), seed, base_pos)
         self._plan = torch.zeros(pass_plan_bytes(L), dtype=torch.uint8, device=self.h.device)
         self.fused = pass_prepare(d, self._plan)
         return self.fused
 
     def run_fused(self):
-        """One verify pass (layers, head, greedy acceptance) as a single cooperative launch."""
+        """One verify pass (layers, head, acceptance) as a single cooperative launch."""
         if self.fused is None:
             self.prepare_fused()
         verify_pass(self.fused)

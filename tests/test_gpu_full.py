@@ -14,7 +14,8 @@
 * The same stack as the one persistent launch the bench times (its deferred
   down-projection combine and head-statistics phases exist only at these
   widths): every output bit-equal to the per-operation pass, at M = 5 (chain)
-  and M = 16 (tree).
+  and M = 16 (tree), and with rejection-sampling acceptance (against the
+  per-operation pass + sd_accept_sample and the oracle's rule).
 """
 import numpy as np
 import pytest
@@ -352,3 +353,34 @@ def test_stack_fused_pass_equals_per_op_pass(sdv, stack_env, M):
     n = int(host(a.out_count)[0])
     assert n >= 1 and int(host(b.out_count)[0]) == n
     assert torch.equal(a.out_tokens[:n], b.out_tokens[:n])
+
+
+def test_stack_fused_pass_sampled_acceptance(sdv, stack_env):
+    """The 64-layer one-launch pass ending in rejection sampling (certainty drafter, T = 0.7) against
+    the per-operation pass followed by sd_accept_sample, and the oracle's rule on its logits."""
+    spec = stack_env["spec"]
+    M, T = 5, 0.7
+    h0 = cuda(spec.hidden_in(M))
+    a, b = stack_env["make"](M), stack_env["make"](M)
+    a.h.copy_(h0)
+    a.run()
+    torch.cuda.synchronize()
+    am = host(a.argmax)
+    drafts = np.array([am[0], am[1], (am[2] + 5) % V, am[3]], np.int32)
+    for st in (a, b):
+        st.h.copy_(h0)
+        st.tokens[:M - 1].copy_(cuda(drafts))
+    for l in range(spec.layers):
+        a.layer(l)
+    a.head(T)
+    a.accept_sampled(T, 77, 4096)
+    b.prepare_fused(temperature=T, sample=True, seed=77, base_pos=4096)
+    b.run_fused()
+    status_ok()
+    for name in ("logits", "row_max", "row_sumexp"):
+        x, y = getattr(a, name), getattr(b, name)
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32)), name
+    n = int(host(a.out_count)[0])
+    assert int(host(b.out_count)[0]) == n
+    assert torch.equal(a.out_tokens[:n], b.out_tokens[:n])
+    assert list(host(b.out_tokens)[:n]) == list(oracle.accept_sample(host(b.logits), None, drafts, T, 77, 4096))

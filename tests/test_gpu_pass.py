@@ -143,3 +143,55 @@ def test_fused_pass_rejects_bad_plans(sdv):
     bad = sdv.SdPass()
     bad.plan = None
     assert sdv.lib().sd_verify_pass(ctypes.byref(bad), None) == 1
+
+
+@pytest.mark.parametrize("certainty", [False, True])
+@pytest.mark.parametrize("M", [1, 5])
+def test_fused_pass_sampled_acceptance(sdv, M, certainty):
+    """The one-launch pass ending in rejection sampling against the per-operation pass followed by
+    sd_accept_sample (bit-equal tokens, logits and statistics), and against the oracle's rule on
+    the pass's own logits."""
+    env = small_stack(sdv, seed=3)
+    spec = env[0]
+    V, K, T = spec.vocab, M - 1, 0.8
+    h0 = cuda(spec.hidden_in(M))
+    probe = make(sdv, env, M)
+    probe.h.copy_(h0)
+    probe.run()
+    am = host(probe.argmax)
+    lg = host(probe.logits)
+    qp = None if certainty or K == 0 else np.stack(
+        [oracle.softmax_probs(lg[i] / T + sdgen.normal(sdgen.key(140, i), (V,))) for i in range(K)]).astype(np.float32)
+    qd = cuda(qp) if qp is not None else None
+    rng = np.random.default_rng(141)
+    a, b = make(sdv, env, M), make(sdv, env, M)
+    for t in range(6):
+        drafts = np.where(rng.random(K) < 0.6, am[:K], rng.integers(0, V, K)).astype(np.int32)
+        seed, base = 1000 + t, 17 * t
+        for st in (a, b):
+            st.h.copy_(h0)
+            if K:
+                st.tokens[:K].copy_(cuda(drafts))
+        for l in range(spec.layers):
+            a.layer(l)
+        a.head(T)
+        a.accept_sampled(T, seed, base, q_probs=qd)
+        b.prepare_fused(temperature=T, sample=True, seed=seed, base_pos=base, q_probs=qd)
+        b.run_fused()
+        status_ok()
+        for name in ("logits", "argmax", "row_max", "row_sumexp"):
+            assert same(getattr(a, name), getattr(b, name)), name
+        n = int(host(a.out_count)[0])
+        assert int(host(b.out_count)[0]) == n and n >= 1
+        assert torch.equal(a.out_tokens[:n], b.out_tokens[:n])
+        ref = oracle.accept_sample(host(b.logits), qp, drafts, T, seed, base)
+        assert list(host(b.out_tokens)[:n]) == list(ref), t
+
+
+def test_fused_pass_sampling_rejects_trees(sdv):
+    env = small_stack(sdv, L=1)
+    parent, _ = sdgen.tree16(0)
+    st = make(sdv, env, 16, cuda(parent))
+    with pytest.raises(sdv.SdError) as e:
+        st.prepare_fused(sample=True)
+    assert e.value.code == 2  # SD_EUNSUPPORTED
