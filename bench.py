@@ -266,7 +266,7 @@ def reference_arm(args, spec, M):
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic",
-            "config": {"workload": "config-4 verify pass weight stream (27B-shaped 4-bit stack + Q8_0 head), "
+            "config": {"workload": "verify pass weight stream (64-layer 27B-shaped 4-bit stack + Q8_0 head), "
                                    "sampled: 3584x5120 slice of one 4-bit projection per step", "M": M},
             "cpu_baseline": {"value": v, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
                              "sample": f"{args.steps} steps of a 3584x5120 4-bit projection at M={M}"},
@@ -478,7 +478,7 @@ def main():
     line = {"metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "int8", "data": "synthetic (seeded N(0,0.02) weights, N(0,1) hidden rows)",
-            "config": {"workload": "config-4 verify pass: 64-layer 27B-shaped 4-bit projection stack + 5120x151936 "
+            "config": {"workload": "verify pass: 64-layer 27B-shaped 4-bit projection stack + 5120x151936 "
                                    "Q8_0 head + greedy accept, K+1=5",
                        "M": M, "layers": spec.layers, "hidden": spec.hidden, "ffn": spec.ffn, "vocab": spec.vocab,
                        "weight_bytes_per_pass": wbytes, "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
