@@ -63,7 +63,7 @@ typedef enum { SD_Q8_0 = 0, SD_Q4_32 = 1 } sd_qtype;
 #define SD_EPI_SILU_MUL_REQUANT 2u  /* gate|up pair: h = silu(g) * u, requantised into q_next/scales_next */
 
 const char *sd_status_string(sd_status s);
-int sd_abi_version(void); /* 1 */
+int sd_abi_version(void); /* 2: sd_pass_desc and sd_pass carry the acceptance mode */
 
 /*
  * Load-time repack ("Inside OpenJet Engine", section "One GPU launch for a

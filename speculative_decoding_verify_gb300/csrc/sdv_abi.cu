@@ -140,7 +140,7 @@ const char *sd_status_string(sd_status s) {
     return "unknown status";
 }
 
-int sd_abi_version(void) { return 1; }
+int sd_abi_version(void) { return 2; }
 
 void sd_set_pdl(int enable) { g_pdl = enable ? 1 : 0; }
 

@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_status_strings_and_version(L):
-    assert L.sd_abi_version() == 1
+    assert L.sd_abi_version() == 2
     assert L.sd_status_string(0) == b"ok"
     assert L.sd_status_string(4) == b"device wait timed out"
 
@@ -78,3 +78,30 @@ def test_argument_checks_reject_without_launching(L):
     # rmsnorm: ldx < K
     assert L.sd_rmsnorm_quant_acts(p, 16, p, ctypes.c_float(1e-6), 5, 32, p, p, None) == 1
     assert L.sd_debug_wait_timeout(0, None) == 1
+
+
+def test_pass_structs_match_the_header(tmp_path):
+    """The binding's ctypes mirrors of sd_layer, sd_pass_desc and sd_pass have the C layout: every
+    field offset and the sizes, as gcc lays out the header."""
+    import shutil
+    import subprocess
+    import speculative_decoding_verify_gb300 as sdv
+    if shutil.which("gcc") is None:
+        pytest.skip("no gcc")
+    structs = {"sd_layer": sdv.SdLayer, "sd_pass_desc": sdv.SdPassDesc, "sd_pass": sdv.SdPass}
+    lines = ['#include <stdio.h>', '#include "sdverify.h"', "int main(void) {"]
+    for cname, py in structs.items():
+        lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
+        for f, _ in py._fields_:
+            lines.append(f'printf("{cname} {f} %zu\\n", offsetof({cname}, {f}));')
+    lines += ["return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    got = {tuple(l.split()[:2]): int(l.split()[2]) for l in out if l.strip()}
+    for cname, py in structs.items():
+        assert got[(cname, "size")] == ctypes.sizeof(py), cname
+        for f, _ in py._fields_:
+            assert got[(cname, f)] == getattr(py, f).offset, (cname, f)
