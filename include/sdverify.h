@@ -239,6 +239,25 @@ sd_status sd_accept_sample(const float *logits, int64_t vocab, int32_t K, const 
                            sd_stream_t stream);
 
 /*
+ * The same rule against a filtered target: the sampling knobs of "Inside
+ * OpenJet Engine" (API section: temperature, top-k up to 32, top-p), applied in
+ * this order (a reading; the page does not fix it).  Row i: z = l / T; the
+ * candidates are the top_k tokens by z (larger first, lower index among equal
+ * z); with e_c = cexp(z_c - z_first) in that order and S their sequential sum,
+ * the nucleus is the shortest prefix whose running sum reaches top_p * S, and
+ * the target is p'_c = e_c / (that running sum), 0 outside the nucleus.  The
+ * draft x is kept iff u * q(x) < p'(x); a rejection draws from
+ * max(0, p'_c - q(c)) over the nucleus in candidate order (p' if that is all
+ * zero), a full acceptance draws the bonus token from p' of row K, both by a
+ * sequential inverse CDF (the first c with w > 0 whose running sum exceeds
+ * u * W).  Uniforms, q_probs, drafts and outputs as in sd_accept_sample.
+ * 1 <= top_k <= 32, 0 < top_p <= 1, K <= 15; logits fp32 [K+1][vocab].
+ */
+sd_status sd_accept_sample_topk(const float *logits, int64_t vocab, int32_t K, const float *q_probs,
+                                const int32_t *drafts, float temperature, int32_t top_k, float top_p, uint64_t seed,
+                                int64_t base_pos, int32_t *out_tokens, int32_t *out_count, sd_stream_t stream);
+
+/*
  * The whole verify pass in one persistent cooperative launch ("Inside OpenJet
  * Engine", section "One GPU launch for a speculative cycle": one persistent
  * kernel carries the cycle's phases with a software grid barrier between them).

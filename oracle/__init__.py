@@ -17,6 +17,8 @@ page passage cited in the C source:
 * rejection sampling and the certainty drafter: "Speculative Decoding with
   Open-Weights Models", section "Mathematical Integrity: Rejection Sampling for
   LLMs", and "How Kinetic is fast", section "Why the output does not change";
+* the same against a top-k / top-p filtered target (the sampling knobs of
+  "Inside OpenJet Engine", API section; the filtering order is a reading);
 * Philox4x32-10: Salmon et al., SC'11.
 
 Parity status: every function here is pinned by a ``-m "not gpu"`` test in
@@ -84,6 +86,9 @@ def _get():
                 "oracle_accept_sample": ([_P, _I64, _I, _P, _P, _F, ctypes.c_uint64, _I64, _P], _I),
                 "oracle_accept_sample_trials": ([_P, _I64, _I, _P, _P, _F, ctypes.c_uint64, _I64, _I64, _P, _P],
                                                 None),
+                "oracle_filter_topk_topp": ([_P, _I64, _F, _I, _F, _P, _P], _I),
+                "oracle_accept_sample_topk_u": ([_P, _I64, _I, _P, _P, _F, _I, _F, _P, _P, _P], _I),
+                "oracle_accept_sample_topk": ([_P, _I64, _I, _P, _P, _F, _I, _F, ctypes.c_uint64, _I64, _P], _I),
             }
             for name, (args, res) in sig.items():
                 f = getattr(lib, name)
@@ -258,6 +263,47 @@ def accept_sample(logits, q_probs, drafts, T: float, seed: int, base_pos: int) -
     drafts, pd = _c(drafts, np.int32)
     out = np.empty(K + 1, dtype=np.int32)
     n = _get().oracle_accept_sample(pl, V, K, pq, pd, T, seed, base_pos, out.ctypes.data)
+    return out[:n].copy()
+
+
+def filter_topk_topp(logits_row, T: float, top_k: int, top_p: float):
+    """The filtered target of one row: (tokens, probabilities) of the nucleus in candidate order."""
+    l, pl = _c(np.asarray(logits_row).reshape(-1), np.float32)
+    tok = np.empty(64, dtype=np.int32)
+    prob = np.empty(64, dtype=np.float32)
+    n = _get().oracle_filter_topk_topp(pl, l.size, T, top_k, top_p, tok.ctypes.data, prob.ctypes.data)
+    return tok[:n].copy(), prob[:n].copy()
+
+
+def accept_sample_topk_u(logits, q_probs, drafts, T, top_k, top_p, u_acc, u_res) -> np.ndarray:
+    logits, pl = _c(logits, np.float32)
+    K1, V = logits.shape
+    K = K1 - 1
+    pq = None
+    if q_probs is not None:
+        q_probs, pq = _c(q_probs, np.float32)
+        assert q_probs.shape == (K, V)
+    drafts, pd = _c(drafts, np.int32)
+    ua, pua = _c(u_acc, np.float32)
+    ur, pur = _c(u_res, np.float32)
+    out = np.empty(K + 1, dtype=np.int32)
+    n = _get().oracle_accept_sample_topk_u(pl, V, K, pq, pd, T, top_k, top_p, pua, pur, out.ctypes.data)
+    return out[:n].copy()
+
+
+def accept_sample_topk(logits, q_probs, drafts, T: float, top_k: int, top_p: float, seed: int,
+                       base_pos: int) -> np.ndarray:
+    logits, pl = _c(logits, np.float32)
+    K1, V = logits.shape
+    K = K1 - 1
+    pq = None
+    if q_probs is not None:
+        q_probs, pq = _c(q_probs, np.float32)
+        assert q_probs.shape == (K, V)
+    drafts, pd = _c(drafts, np.int32)
+    out = np.empty(K + 1, dtype=np.int32)
+    n = _get().oracle_accept_sample_topk(pl, V, K, pq, pd, T, top_k, top_p, seed, base_pos, out.ctypes.data)
+    assert n > 0
     return out[:n].copy()
 
 

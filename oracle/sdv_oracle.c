@@ -517,3 +517,121 @@ void oracle_accept_sample_trials(const float *logits, int64_t V, int K, const fl
         counts[t] = oracle_accept_sample(logits, V, K, q_probs, drafts_per_trial + t * K, T, seed,
                                          base_pos + t * (K + 1), tokens + t * (K + 1));
 }
+
+/* ------------------------------------------------------------------ */
+/* Rejection sampling against a filtered target (the sampling knobs of  */
+/* "Inside OpenJet Engine", API section: temperature, top-k up to 32,   */
+/* top-p), read as follows.  Row i: z_j = l_j / T (then z + 0, so that  */
+/* -0 and +0 are one value); the candidates are the top_k tokens by z,  */
+/* larger z first and, among equal z, the lower token index first.     */
+/* With m = z of the first candidate, e_c = cexp(z_c - m) for the       */
+/* candidates in that order; S = their sequential sum; the nucleus is   */
+/* the shortest prefix of n candidates whose running sum reaches        */
+/* top_p * S (n >= 1); S' = the running sum over it; the target is      */
+/* p'_c = e_c / S' on the nucleus, 0 elsewhere.  The draft x is kept    */
+/* iff u_acc * q(x) < p'(x); on a rejection the token is drawn from     */
+/* w_c = max(0, p'_c - q(c)) over the nucleus in candidate order (q     */
+/* one-hot at x for a certainty drafter), on a full acceptance from p'  */
+/* of row K: W = sequential sum of w, target = u_res * W, the first     */
+/* candidate with w > 0 whose running sum exceeds it, else the last one */
+/* with w > 0; W not positive falls back to p'.                         */
+/* ------------------------------------------------------------------ */
+
+/* candidate j comes before candidate i: larger z, then lower index */
+static int cand_before(float zj, int64_t ij, float zi, int64_t ii) { return zj > zi || (zj == zi && ij < ii); }
+
+/* the filtered target of one row: writes up to top_k (token, p') pairs in candidate order; returns n */
+int oracle_filter_topk_topp(const float *l, int64_t V, float T, int top_k, float top_p, int32_t *tok, float *prob) {
+    int32_t ct[64];
+    float cz[64];
+    int nc = 0;
+    for (int64_t j = 0; j < V; ++j) {
+        float z = l[j] / T + 0.0f;
+        if (nc == top_k && !cand_before(z, j, cz[nc - 1], ct[nc - 1])) continue;
+        int pos = nc < top_k ? nc++ : nc - 1; /* insertion into the sorted list */
+        while (pos > 0 && cand_before(z, j, cz[pos - 1], ct[pos - 1])) {
+            cz[pos] = cz[pos - 1];
+            ct[pos] = ct[pos - 1];
+            --pos;
+        }
+        cz[pos] = z;
+        ct[pos] = (int32_t)j;
+    }
+    float e[64], S = 0.0f;
+    for (int c = 0; c < nc; ++c) {
+        e[c] = oracle_cexp(cz[c] - cz[0]);
+        S = S + e[c];
+    }
+    const float goal = top_p * S;
+    int n = 0;
+    float run = 0.0f;
+    while (n < nc) {
+        run = run + e[n];
+        ++n;
+        if (run >= goal) break;
+    }
+    for (int c = 0; c < n; ++c) {
+        tok[c] = ct[c];
+        prob[c] = e[c] / run;
+    }
+    return n;
+}
+
+/* inverse-CDF draw over n candidate weights in order; -1 if they sum to zero */
+static int draw_list(const float *w, int n, float u) {
+    float W = 0.0f;
+    for (int c = 0; c < n; ++c) W = W + w[c];
+    if (!(W > 0.0f)) return -1;
+    const float target = u * W;
+    float run = 0.0f;
+    int last = -1;
+    for (int c = 0; c < n; ++c) {
+        run = run + w[c];
+        if (w[c] > 0.0f) {
+            last = c;
+            if (run > target) return c;
+        }
+    }
+    return last;
+}
+
+int oracle_accept_sample_topk_u(const float *logits, int64_t V, int K, const float *q_probs, const int32_t *drafts,
+                                float T, int top_k, float top_p, const float *u_acc, const float *u_res, int32_t *out) {
+    int32_t tok[64];
+    float p[64], w[64];
+    int n = 0;
+    for (int i = 0; i <= K; ++i) {
+        const int nn = oracle_filter_topk_topp(logits + (int64_t)i * V, V, T, top_k, top_p, tok, p);
+        if (i == K) {
+            out[n++] = tok[draw_list(p, nn, u_res[i])];
+            break;
+        }
+        const int32_t x = drafts[i];
+        float px = 0.0f;
+        for (int c = 0; c < nn; ++c)
+            if (tok[c] == x) px = p[c];
+        const float qx = q_probs ? q_probs[(int64_t)i * V + x] : 1.0f;
+        if (u_acc[i] * qx < px) {
+            out[n++] = x;
+            continue;
+        }
+        for (int c = 0; c < nn; ++c) {
+            const float qc = q_probs ? q_probs[(int64_t)i * V + tok[c]] : (tok[c] == x ? 1.0f : 0.0f);
+            const float d = p[c] - qc;
+            w[c] = d > 0.0f ? d : 0.0f;
+        }
+        int c = draw_list(w, nn, u_res[i]);
+        if (c < 0) c = draw_list(p, nn, u_res[i]);
+        out[n++] = tok[c];
+        break;
+    }
+    return n;
+}
+
+int oracle_accept_sample_topk(const float *logits, int64_t V, int K, const float *q_probs, const int32_t *drafts,
+                              float T, int top_k, float top_p, uint64_t seed, int64_t base_pos, int32_t *out) {
+    float ua[64], ur[64];
+    if (K > 63 || top_k < 1 || top_k > 32) return -1;
+    for (int i = 0; i <= K; ++i) oracle_uniforms(seed, base_pos + i, &ua[i], &ur[i]);
+    return oracle_accept_sample_topk_u(logits, V, K, q_probs, drafts, T, top_k, top_p, ua, ur, out);
+}

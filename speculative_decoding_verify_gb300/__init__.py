@@ -84,6 +84,7 @@ def lib():
             "sd_head_logits": ([P, I64, I64, P, P, I32, F, P, P, P, P, P, SZ, P], I),
             "sd_accept_greedy": ([P, P, P, I32, P, P, P], I),
             "sd_accept_sample": ([P, I64, I32, P, P, P, P, F, U64, I64, P, P, P], I),
+            "sd_accept_sample_topk": ([P, I64, I32, P, P, F, I32, F, U64, I64, P, P, P], I),
             "sd_device_status": ([P], I),
             "sd_set_pdl": ([I], None),
             "sd_debug_block_dots": ([I, P, I64, I64, P, I32, P, P], I),
@@ -210,6 +211,15 @@ def accept_sample(logits: torch.Tensor, K: int, drafts: torch.Tensor | None, out
     _check(lib().sd_accept_sample(_p(logits), V, K, _p(row_max), _p(row_sumexp), _p(q_probs), _p(drafts),
                                   temperature, seed, base_pos, _p(out_tokens), _p(out_count), _stream()),
            "sd_accept_sample")
+
+
+def accept_sample_topk(logits: torch.Tensor, K: int, drafts: torch.Tensor | None, out_tokens: torch.Tensor,
+                       out_count: torch.Tensor, top_k: int, top_p: float = 1.0, q_probs: torch.Tensor | None = None,
+                       temperature: float = 1.0, seed: int = 0, base_pos: int = 0):
+    V = logits.shape[1]
+    _check(lib().sd_accept_sample_topk(_p(logits), V, K, _p(q_probs), _p(drafts), temperature, top_k, top_p, seed,
+                                       base_pos, _p(out_tokens), _p(out_count), _stream()),
+           "sd_accept_sample_topk")
 
 
 def device_status() -> int:

@@ -35,6 +35,13 @@ def test_library_exports_every_declared_symbol(L):
         assert hasattr(L, name), name
 
 
+def test_binding_types_every_declared_call(L):
+    """Each declared call has its argument types set in the binding (ctypes would otherwise pass
+    floats and 64-bit integers wrongly)."""
+    for name in declared_symbols():
+        assert getattr(L, name).argtypes is not None, name
+
+
 def test_status_strings_and_version(L):
     assert L.sd_abi_version() == 2
     assert L.sd_status_string(0) == b"ok"

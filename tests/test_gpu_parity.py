@@ -409,3 +409,68 @@ def test_bounded_wait_reports_timeout(sdv):
     sdv.debug_wait_timeout(2_000_000)  # 2 ms
     assert sdv.device_status() == 4    # SD_ETIMEOUT, and the word is cleared
     assert sdv.device_status() == 0
+
+
+# ---------------------------------------------------------------------------
+# rejection sampling against a top-k / top-p filtered target
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("certainty", [False, True])
+@pytest.mark.parametrize("top_k,top_p", [(1, 1.0), (5, 0.8), (20, 0.95), (32, 1.0), (32, 0.3)])
+def test_accept_sample_topk_bit_exact_small_vocab(sdv, certainty, top_k, top_p):
+    V, K = 64, 3
+    l = sdgen.normal(sdgen.key(150), (K + 1, V)) * 1.5
+    l[:, 7] = l[:, 9] = l.max(axis=1)  # ties at the top, broken by the lower index
+    qp = None if certainty else np.stack(
+        [oracle.softmax_probs(l[i] + sdgen.normal(sdgen.key(151, i), (V,))) for i in range(K)])
+    ld = cuda(l)
+    qd = cuda(qp) if qp is not None else None
+    rng = np.random.default_rng(152)
+    runs = []
+    for t in range(120):
+        am = np.argmax(l[:K], axis=1)
+        dr = np.where(rng.random(K) < 0.5, am, rng.integers(0, V, K)).astype(np.int32)
+        ot = torch.full((K + 1,), -7, dtype=torch.int32, device="cuda")
+        oc = torch.zeros(1, dtype=torch.int32, device="cuda")
+        sdv.accept_sample_topk(ld, K, cuda(dr), ot, oc, top_k, top_p, q_probs=qd, temperature=0.9, seed=31,
+                               base_pos=t * (K + 1))
+        runs.append((dr, ot, oc))
+    status_ok()
+    for t, (dr, ot, oc) in enumerate(runs):
+        ref = oracle.accept_sample_topk(l, qp, dr, 0.9, top_k, top_p, 31, t * (K + 1))
+        n = int(host(oc)[0])
+        assert list(host(ot)[:n]) == list(ref), t
+
+
+@pytest.mark.parametrize("certainty", [False, True])
+def test_accept_sample_topk_bit_exact_full_vocab(sdv, certainty):
+    V, K = 151936, 4
+    l = sdgen.normal(sdgen.key(153), (K + 1, V)) * 3
+    qp = None if certainty else np.stack(
+        [oracle.softmax_probs(l[i] + sdgen.normal(sdgen.key(154, i), (V,))) for i in range(K)])
+    ld = cuda(l)
+    qd = cuda(qp) if qp is not None else None
+    rng = np.random.default_rng(155)
+    for t in range(8):
+        # the drafts: a row's best token (likely kept), its second best, or a random one (rejected)
+        order = np.argsort(-l[:K], axis=1, kind="stable")
+        pick = rng.integers(0, 3, K)
+        dr = np.where(pick == 0, order[:, 0], np.where(pick == 1, order[:, 1], rng.integers(0, V, K))).astype(np.int32)
+        ot = torch.full((K + 1,), -7, dtype=torch.int32, device="cuda")
+        oc = torch.zeros(1, dtype=torch.int32, device="cuda")
+        sdv.accept_sample_topk(ld, K, cuda(dr), ot, oc, 20, 0.95, q_probs=qd, temperature=1.0, seed=9 + t,
+                               base_pos=500 * t)
+        ref = oracle.accept_sample_topk(l, qp, dr, 1.0, 20, 0.95, 9 + t, 500 * t)
+        status_ok()
+        n = int(host(oc)[0])
+        assert list(host(ot)[:n]) == list(ref), t
+
+
+def test_accept_sample_topk_argument_checks(sdv):
+    l = torch.zeros((2, 8), dtype=torch.float32, device="cuda")
+    d = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ot = torch.zeros(2, dtype=torch.int32, device="cuda")
+    oc = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for k, p in ((0, 1.0), (33, 1.0), (4, 0.0), (4, 1.5)):
+        with pytest.raises(sdv.SdError):
+            sdv.accept_sample_topk(l, 1, d, ot, oc, k, p)

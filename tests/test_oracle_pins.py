@@ -463,3 +463,97 @@ def test_rejection_sampling_monte_carlo_1e6(certainty):
         assert np.all(np.abs(freq - p) <= 3 * sigma + 1e-12), (freq - p) / sigma
         chi2 = (((freq - p) * N) ** 2 / (p * N)).sum()
         assert chi2 < 45  # 15 dof: p ~ 1e-4
+
+
+# ---------------------------------------------------------------------------
+# rejection sampling against a top-k / top-p filtered target
+# ---------------------------------------------------------------------------
+
+def test_filter_topk_topp_worked_example():
+    """z = (1, 3, 2, 3, -1): ties broken by index, closed-form probabilities, the nucleus cut."""
+    l = np.array([1.0, 3.0, 2.0, 3.0, -1.0], np.float32)
+    tok, p = oracle.filter_topk_topp(l, 1.0, 3, 1.0)
+    assert list(tok) == [1, 3, 2]
+    e = np.exp(np.array([0.0, 0.0, -1.0]))
+    np.testing.assert_allclose(p, e / e.sum(), rtol=4e-7)
+    tok, p = oracle.filter_topk_topp(l, 1.0, 3, 0.5)  # 1/2.37 < 0.5 <= 2/2.37: two candidates
+    assert list(tok) == [1, 3] and list(p) == [0.5, 0.5]
+    tok, p = oracle.filter_topk_topp(l, 1.0, 5, 1e-9)  # the nucleus is never empty
+    assert list(tok) == [1] and list(p) == [1.0]
+
+
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_filter_without_cuts_is_the_softmax(T):
+    V = 16
+    l = sdgen.normal(sdgen.key(60), (V,)) * 2
+    tok, p = oracle.filter_topk_topp(l, T, V, 1.0)
+    z = l.astype(np.float32) / np.float32(T)
+    assert list(tok) == list(np.lexsort((np.arange(V), -z)))
+    ref = np.exp(z.astype(np.float64) - z.max())
+    ref /= ref.sum()
+    np.testing.assert_allclose(p, ref[tok], rtol=1e-6)
+
+
+def test_filter_nucleus_is_the_shortest_prefix():
+    V = 64
+    l = sdgen.normal(sdgen.key(61), (V,)) * 3
+    for top_p in (0.3, 0.6, 0.9, 0.99):
+        tok, p = oracle.filter_topk_topp(l, 1.0, 32, top_p)
+        full_tok, full_p = oracle.filter_topk_topp(l, 1.0, 32, 1.0)
+        assert list(tok) == list(full_tok[:tok.size])
+        c = np.cumsum(full_p.astype(np.float64))
+        n = tok.size
+        assert c[n - 1] >= top_p - 1e-6 and (n == 1 or c[n - 2] < top_p + 1e-6)
+        np.testing.assert_allclose(p.sum(), 1.0, rtol=1e-6)
+
+
+def test_topk1_is_greedy_chain():
+    """With top_k = 1 the target is one-hot at the argmax, so any uniforms give the greedy chain rule."""
+    V, K = 64, 4
+    l = sdgen.normal(sdgen.key(62), (K + 1, V)) * 2
+    am = np.argmax(l, axis=1).astype(np.int32)
+    rng = np.random.default_rng(63)
+    for t in range(40):
+        drafts = np.where(rng.random(K) < 0.7, am[:K], rng.integers(0, V, K)).astype(np.int32)
+        q = oracle.softmax_probs(l[0] + 0.0)[None, :].repeat(K, 0) if t % 2 else None
+        got = oracle.accept_sample_topk(l, q, drafts, 1.0, 1, 1.0, seed=t, base_pos=100 * t)
+        assert list(got) == list(oracle.accept_greedy_chain(am, drafts)), t
+
+
+@pytest.mark.parametrize("certainty", [False, True])
+def test_filtered_rejection_sampling_exact_law(certainty):
+    """Emitted-token law of one verified draft, enumerated exactly over the uniforms, equals the
+    filtered target p' (top_k = 5, top_p = 0.8): the rejection-sampling guarantee for p'."""
+    V = 12
+    l = sdgen.normal(sdgen.key(64), (2, V)) * 1.5
+    tok, pk = oracle.filter_topk_topp(l[0], 1.0, 5, 0.8)
+    p = np.zeros(V)
+    p[tok] = pk
+    qrow = None if certainty else oracle.softmax_probs(l[0] + sdgen.normal(sdgen.key(65), (V,)))
+    qfull = None if certainty else qrow[None, :]
+    top = 1.0 - 2.0 ** -24
+    for x in (range(V) if certainty else [None]):
+        law = np.zeros(V)
+        for xd in ([x] if certainty else range(V)):
+            dr = np.array([xd], np.int32)
+            qx = 1.0 if certainty else float(qrow[xd])
+            acc = _grid_law(lambda u: len(oracle.accept_sample_topk_u(l, qfull, dr, 1.0, 5, 0.8, [u, 0.0],
+                                                                     [0.0, 0.0])) == 2)
+            pacc = acc.get(True, 0.0)
+            assert abs(pacc - min(1.0, p[xd] / qx)) <= 2.0 ** -23
+            weight = 1.0 if certainty else qx
+            law[xd] += weight * pacc
+            if pacc < 1.0:
+                res = _grid_law(lambda u: int(oracle.accept_sample_topk_u(l, qfull, dr, 1.0, 5, 0.8, [top, 0.0],
+                                                                          [u, 0.0])[0]))
+                qv = np.eye(V)[xd] if certainty else qrow.astype(np.float64)
+                w = np.maximum(0.0, p - qv)
+                r = w / w.sum() if w.sum() > 0 else p
+                for t, pr in res.items():
+                    assert abs(pr - r[t]) <= 2e-6
+                    law[t] += weight * (1 - pacc) * pr
+        if certainty:
+            # a certainty drafter's draft x: the law is p' whatever x is
+            assert np.all(np.abs(law - p) <= 4e-6), np.abs(law - p).max()
+    if not certainty:
+        assert np.all(np.abs(law - p) <= 4e-6), np.abs(law - p).max()
