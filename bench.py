@@ -275,6 +275,23 @@ def reference_arm(args, spec, M):
 
 
 # ---------------------------------------------------------------------------
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest of every rank's x: the job's time is that of its slowest replica (x itself when the
+    job has one rank)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rates(weight_bytes: int, M: int, ms: float, world: int):
+    """Whole-job rates of `world` replicas that each stream `weight_bytes` and verify M positions per
+    step of `ms` milliseconds (the slowest replica's): (GB/s, positions/s)."""
+    return weight_bytes / (ms * 1e-3) / 1e9 * world, M / (ms * 1e-3) * world
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -407,14 +424,10 @@ def main():
     kept = int(stack.out_count.cpu()[0])
     if sdv.device_status() != 0:
         raise RuntimeError("device status after the timed region")
-    if dist:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, device)
 
     wbytes = spec.weight_bytes()
-    gbs = wbytes / (ms * 1e-3) / 1e9 * world
-    pos_s = M / (ms * 1e-3) * world
+    gbs, pos_s = job_rates(wbytes, M, ms, world)
 
     # end to end through the ABI with host buffers: H2D of the input rows and drafts, the pass, D2H of the
     # accepted tokens and their count, every step
@@ -439,10 +452,7 @@ def main():
         e2e_step()
         torch.cuda.current_stream().synchronize()
     e2e_ms = (time.perf_counter() - t0) / e2e_steps * 1e3
-    if dist:
-        t = torch.tensor([e2e_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist, device)
     h2d = h_host.numel() * 4 + d_host.numel() * 4
     d2h = out_host.numel() * 4 + cnt_host.numel() * 4
 
