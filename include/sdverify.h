@@ -284,7 +284,7 @@ sd_status sd_accept_sample_topk(const float *logits, int64_t vocab, int32_t K, c
  * sd_accept_sample on the pass's own logits and statistics (drafts = tokens
  * [M-1], K = M - 1, temperature, q_probs, seed, base_pos as there; chains only:
  * parent must be NULL, else SD_EUNSUPPORTED); it produces the same tokens as the
- * head followed by sd_accept_sample.
+ * head followed by sd_accept_sample, or with top_k > 0 by sd_accept_sample_topk.
  * layers is a HOST array read only by sd_pass_prepare.
  * sd_pass_prepare writes the phase table into `plan` (device, 256-byte aligned,
  * >= sd_pass_plan_bytes(n_layers), synchronously) and fills `out`;
@@ -328,6 +328,8 @@ typedef struct {
     const float *q_probs;  /* SD_ACCEPT_SAMPLE: drafter probabilities [M-1][vocab], NULL = certainty drafter */
     uint64_t seed;         /* SD_ACCEPT_SAMPLE: Philox key and position of the first draft */
     int64_t base_pos;
+    int32_t top_k;         /* SD_ACCEPT_SAMPLE: 0 = unfiltered target (sd_accept_sample), 1..32 = */
+    float top_p;           /* the filtered target of sd_accept_sample_topk with top_p in (0, 1] */
 } sd_pass_desc;
 
 typedef enum { SD_ACCEPT_GREEDY = 0, SD_ACCEPT_SAMPLE = 1 } sd_accept_mode;

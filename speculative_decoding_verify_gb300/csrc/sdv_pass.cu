@@ -110,6 +110,9 @@ sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, 
     if (d->accept == SD_ACCEPT_SAMPLE &&
         (d->parent || V > static_cast<int64_t>(MAX_TILES) * ATILE || !(d->temperature <= 3.0e38f)))
         return SD_EUNSUPPORTED;  // sampling: chains only, the single-operation call's vocabulary limit
+    if (d->accept == SD_ACCEPT_SAMPLE && d->top_k != 0 &&
+        (d->top_k < 1 || d->top_k > TK_MAX || !(d->top_p > 0.0f) || d->top_p > 1.0f))
+        return SD_EINVAL;
     int *st = status_ptr();
     if (!st) return SD_ECUDA;
     const int sms = num_sms();
@@ -280,6 +283,8 @@ sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, 
         a.q_probs = d->q_probs;
         a.seed = d->seed;
         a.base_pos = d->base_pos;
+        a.top_k = d->top_k;
+        a.top_p = d->top_p;
         ph.push_back(a);
     }
     // one shared-memory layout for every phase: the largest split, pair rows, the largest stage,
@@ -294,7 +299,8 @@ sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, 
         }
     SmemLayout lay;
     if (!layout_smem(kbs, M, 64, slot, static_cast<size_t>(M) * ss_ld * sizeof(float), lay)) return SD_EUNSUPPORTED;
-    if (static_cast<size_t>(lay.NS) * slot < sizeof(SampleShared)) return SD_EUNSUPPORTED;  // the sampler's state
+    if (static_cast<size_t>(lay.NS) * slot < sizeof(SampleShared) || static_cast<size_t>(lay.NS) * slot < sizeof(TopkShared))
+        return SD_EUNSUPPORTED;  // the sampler's state
     for (QmmArgs &a : ph) apply_layout(a, lay, slot);
     PassHeader hdr = {};
     if (cudaMemcpy(plan, &hdr, sizeof(hdr), cudaMemcpyHostToDevice) != cudaSuccess) return SD_ECUDA;

@@ -40,6 +40,7 @@
 
 #include "sdv_common.cuh"
 #include "sdv_sample.cuh"
+#include "sdv_topk.cuh"
 
 namespace sdv {
 
@@ -158,6 +159,8 @@ struct QmmArgs {
     const float *q_probs;   // sampling: drafter probabilities [M-1][n_out] (null: certainty drafter)
     uint64_t seed;          // sampling: Philox key and first position
     int64_t base_pos;
+    int32_t top_k;          // sampling: 0 unfiltered, else the top-k / top-p filtered target
+    float top_p;
 };
 
 constexpr int KIND_MATMUL = 0, KIND_NORM = 1, KIND_ACCEPT = 2, KIND_COMBINE = 3, KIND_HSTATS = 4;
@@ -1560,6 +1563,25 @@ __device__ __forceinline__ void pass_sample_accept(const QmmArgs &sa, uint8_t *s
 
 // SAMPLE: the acceptance phase may run rejection sampling (a separate instantiation, so that the
 // greedy pass's code and register allocation stay those of the matmul loops alone)
+// The same against the top-k / top-p filtered target.
+__device__ __forceinline__ void pass_topk_accept(const QmmArgs &sa, uint8_t *scratch, int wtid) {
+    TopkArgs g;
+    g.logits = sa.y;
+    g.V = sa.n_out;
+    g.K = sa.M - 1;
+    g.q = sa.q_probs;
+    g.drafts = sa.tokens;
+    g.T = sa.T;
+    g.top_k = sa.top_k;
+    g.top_p = sa.top_p;
+    g.seed = sa.seed;
+    g.base_pos = sa.base_pos;
+    g.out = sa.out_tokens;
+    g.count = sa.out_count;
+    topk_accept<WORK_THREADS>(g, *reinterpret_cast<TopkShared *>(scratch), wtid,
+                              []() { named_bar_sync(BAR_WORK, WORK_THREADS); });
+}
+
 template <int NT, bool SAMPLE>
 __global__ void __launch_bounds__(QMM_THREADS, 1)
     pass_kernel(const QmmArgs *__restrict__ phases, int n_phases, uint32_t *barrier_ctr) {
@@ -1621,7 +1643,10 @@ __global__ void __launch_bounds__(QMM_THREADS, 1)
                     named_bar_sync(BAR_WORK, WORK_THREADS);
                 }
                 if (SAMPLE && sa.accept_mode == 1) {
-                    if constexpr (SAMPLE) pass_sample_accept(sa, sm.ring, (warp < NCW ? warp : warp - 1) * 32 + lane);
+                    if constexpr (SAMPLE) {
+                        if (sa.top_k > 0) pass_topk_accept(sa, sm.ring, (warp < NCW ? warp : warp - 1) * 32 + lane);
+                        else pass_sample_accept(sa, sm.ring, (warp < NCW ? warp : warp - 1) * 32 + lane);
+                    }
                 } else if (tid == 0) {
                     greedy_accept(sa.argmax, sa.tokens, sa.parent, sa.M, sa.out_tokens, sa.out_count);
                 }

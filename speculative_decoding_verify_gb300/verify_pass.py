@@ -16,7 +16,7 @@ import torch
 import ctypes
 
 from . import (ACCEPT_GREEDY, ACCEPT_SAMPLE, EPI_NONE, EPI_REQUANT, EPI_SILU_MUL_REQUANT, Q4_32, Q8_0, SdLayer,
-               SdPassDesc, accept_greedy, accept_sample, head_logits, head_workspace_bytes, pass_plan_bytes, pass_prepare, pass_workspace_bytes,
+               SdPassDesc, accept_greedy, accept_sample, accept_sample_topk, head_logits, head_workspace_bytes, pass_plan_bytes, pass_prepare, pass_workspace_bytes,
                qmatmul_multipos, qmatmul_workspace_bytes, repack_weights, rmsnorm_quant_acts, verify_pass,
                workspace)
 
@@ -82,9 +82,16 @@ class VerifyStack:
     def accept(self):
         accept_greedy(self.argmax, self.tokens, self.parent, self.M, self.out_tokens, self.out_count)
 
-    def accept_sampled(self, temperature: float, seed: int, base_pos: int = 0, q_probs=None):
-        """Rejection-sampling acceptance of the drafts self.tokens[:M-1] on this pass's logits and statistics."""
-        accept_sample(self.logits, self.M - 1, self.tokens if self.M > 1 else None, self.out_tokens, self.out_count,
+    def accept_sampled(self, temperature: float, seed: int, base_pos: int = 0, q_probs=None, top_k: int = 0,
+                       top_p: float = 1.0):
+        """Rejection-sampling acceptance of the drafts self.tokens[:M-1] on this pass's logits and statistics
+        (top_k > 0: against the top-k / top-p filtered target)."""
+        drafts = self.tokens if self.M > 1 else None
+        if top_k > 0:
+            accept_sample_topk(self.logits, self.M - 1, drafts, self.out_tokens, self.out_count, top_k, top_p,
+                               q_probs=q_probs, temperature=temperature, seed=seed, base_pos=base_pos)
+            return
+        accept_sample(self.logits, self.M - 1, drafts, self.out_tokens, self.out_count,
                       q_probs=q_probs, row_max=self.row_max, row_sumexp=self.row_sumexp, temperature=temperature,
                       seed=seed, base_pos=base_pos)
 
@@ -97,7 +104,7 @@ class VerifyStack:
 
     # -- the same pass as one persistent cooperative launch -----------------------
     def prepare_fused(self, temperature: float = 1.0, sample: bool = False, seed: int = 0, base_pos: int = 0,
-                      q_probs=None):
+                      q_probs=None, top_k: int = 0, top_p: float = 1.0):
         """Build the phase table of the one-launch pass over this stack's buffers; `sample` ends it with
         rejection-sampling acceptance (temperature, seed, base_pos, q_probs as in accept_sample)
         instead of greedy acceptance."""
@@ -116,7 +123,7 @@ class VerifyStack:
                        p(self.qa), p(self.sa), p(self.qv), p(self.sv), p(self.qf), p(self.sf), p(self.logits),
                        p(self.argmax), p(self.row_max), p(self.row_sumexp), p(self.tokens), p(self.parent),
                        p(self.out_tokens), p(self.out_count), p(self.ws), self.ws.numel(),
-                       ACCEPT_SAMPLE if sample else ACCEPT_GREEDY, p(q_probs), seed, base_pos)
+                       ACCEPT_SAMPLE if sample else ACCEPT_GREEDY, p(q_probs), seed, base_pos, top_k, top_p)
         self._plan = torch.zeros(pass_plan_bytes(L), dtype=torch.uint8, device=self.h.device)
         self.fused = pass_prepare(d, self._plan)
         return self.fused

@@ -384,3 +384,32 @@ def test_stack_fused_pass_sampled_acceptance(sdv, stack_env):
     assert int(host(b.out_count)[0]) == n
     assert torch.equal(a.out_tokens[:n], b.out_tokens[:n])
     assert list(host(b.out_tokens)[:n]) == list(oracle.accept_sample(host(b.logits), None, drafts, T, 77, 4096))
+
+
+def test_stack_fused_pass_filtered_sampling(sdv, stack_env):
+    """The 64-layer one-launch pass with top_k = 20, top_p = 0.95 (T = 1) against the oracle's rule on
+    its own logits and the per-operation pass + sd_accept_sample_topk."""
+    spec = stack_env["spec"]
+    M = 5
+    h0 = cuda(spec.hidden_in(M))
+    a, b = stack_env["make"](M), stack_env["make"](M)
+    a.h.copy_(h0)
+    a.run()
+    torch.cuda.synchronize()
+    am = host(a.argmax)
+    drafts = np.array([am[0], am[1], am[2], (am[3] + 9) % V], np.int32)
+    for st in (a, b):
+        st.h.copy_(h0)
+        st.tokens[:M - 1].copy_(cuda(drafts))
+    for l in range(spec.layers):
+        a.layer(l)
+    a.head(1.0)
+    a.accept_sampled(1.0, 123, 77, top_k=20, top_p=0.95)
+    b.prepare_fused(temperature=1.0, sample=True, seed=123, base_pos=77, top_k=20, top_p=0.95)
+    b.run_fused()
+    status_ok()
+    n = int(host(a.out_count)[0])
+    assert int(host(b.out_count)[0]) == n
+    assert torch.equal(a.out_tokens[:n], b.out_tokens[:n])
+    assert list(host(b.out_tokens)[:n]) == list(oracle.accept_sample_topk(host(b.logits), None, drafts, 1.0, 20, 0.95,
+                                                                        123, 77))

@@ -195,3 +195,44 @@ def test_fused_pass_sampling_rejects_trees(sdv):
     with pytest.raises(sdv.SdError) as e:
         st.prepare_fused(sample=True)
     assert e.value.code == 2  # SD_EUNSUPPORTED
+
+
+@pytest.mark.parametrize("top_k,top_p,certainty", [(1, 1.0, True), (20, 0.95, False), (32, 0.6, True)])
+def test_fused_pass_filtered_sampling(sdv, top_k, top_p, certainty):
+    """The one-launch pass ending in rejection sampling against the top-k / top-p filtered target,
+    against the per-operation pass + sd_accept_sample_topk and the oracle's rule on its logits."""
+    env = small_stack(sdv, seed=4)
+    spec = env[0]
+    M, V, T = 5, spec.vocab, 0.9
+    K = M - 1
+    h0 = cuda(spec.hidden_in(M))
+    probe = make(sdv, env, M)
+    probe.h.copy_(h0)
+    probe.run()
+    am, lg = host(probe.argmax), host(probe.logits)
+    qp = None if certainty else np.stack(
+        [oracle.softmax_probs(lg[i] / T + sdgen.normal(sdgen.key(142, i), (V,))) for i in range(K)]).astype(np.float32)
+    qd = cuda(qp) if qp is not None else None
+    rng = np.random.default_rng(143)
+    a, b = make(sdv, env, M), make(sdv, env, M)
+    for t in range(5):
+        drafts = np.where(rng.random(K) < 0.7, am[:K], rng.integers(0, V, K)).astype(np.int32)
+        seed, base = 2000 + t, 11 * t
+        for st in (a, b):
+            st.h.copy_(h0)
+            st.tokens[:K].copy_(cuda(drafts))
+        for l in range(spec.layers):
+            a.layer(l)
+        a.head(T)
+        a.accept_sampled(T, seed, base, q_probs=qd, top_k=top_k, top_p=top_p)
+        b.prepare_fused(temperature=T, sample=True, seed=seed, base_pos=base, q_probs=qd, top_k=top_k, top_p=top_p)
+        b.run_fused()
+        status_ok()
+        assert same(a.logits, b.logits)
+        n = int(host(a.out_count)[0])
+        assert int(host(b.out_count)[0]) == n and n >= 1
+        assert torch.equal(a.out_tokens[:n], b.out_tokens[:n])
+        ref = oracle.accept_sample_topk(host(b.logits), qp, drafts, T, top_k, top_p, seed, base)
+        assert list(host(b.out_tokens)[:n]) == list(ref), t
+        if top_k == 1:  # the greedy chain rule on the pass's argmax
+            assert list(ref) == list(oracle.accept_greedy_chain(host(b.argmax), drafts))
