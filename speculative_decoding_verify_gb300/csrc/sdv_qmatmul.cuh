@@ -145,7 +145,8 @@ struct QmmArgs {
     uint32_t stage_stride;  // bytes between ring slots (>= SB * step_bytes)
     int32_t NRB;            // partial-sum slots between consumers and finisher (1 or 2)
     int32_t rows_p;         // row stride of a slot (rows + 4: conflict-free stores)
-    // phase kind inside a pass: 0 matmul (qt, pair), 1 RMSNorm + requant, 2 greedy acceptance
+    // phase kind inside a pass: KIND_MATMUL (qt, pair), KIND_NORM (RMSNorm + requant), KIND_ACCEPT
+    // (statistics fold, then greedy or sampled acceptance), KIND_COMBINE, KIND_HSTATS
     int32_t kind, qt, pair;
     const float *xin;       // RMSNorm input [M][K] (K = 32 KB)
     const float *norm_w;    // RMSNorm weight [K]
