@@ -474,3 +474,21 @@ def test_accept_sample_topk_argument_checks(sdv):
     for k, p in ((0, 1.0), (33, 1.0), (4, 0.0), (4, 1.5)):
         with pytest.raises(sdv.SdError):
             sdv.accept_sample_topk(l, 1, d, ot, oc, k, p)
+
+
+@pytest.mark.parametrize("K", [0, 2])
+def test_accept_sample_topk_vocab_smaller_than_k(sdv, K):
+    """top_k = 32 over an 8-token vocabulary: every token is a candidate; K = 0 draws the bonus token only."""
+    V = 8
+    l = sdgen.normal(sdgen.key(156), (K + 1, V)) * 2
+    ld = cuda(l)
+    rng = np.random.default_rng(157)
+    for t in range(40):
+        dr = rng.integers(0, V, K).astype(np.int32)
+        ot = torch.full((K + 1,), -7, dtype=torch.int32, device="cuda")
+        oc = torch.zeros(1, dtype=torch.int32, device="cuda")
+        sdv.accept_sample_topk(ld, K, cuda(dr) if K else None, ot, oc, 32, 0.5, temperature=1.3, seed=t, base_pos=3 * t)
+        ref = oracle.accept_sample_topk(l, None, dr, 1.3, 32, 0.5, t, 3 * t)
+        status_ok()
+        n = int(host(oc)[0])
+        assert list(host(ot)[:n]) == list(ref), t
