@@ -374,6 +374,15 @@ sd_status sd_debug_philox(uint64_t seed, int64_t pos, int64_t n, uint32_t *out, 
  * device: every wait inside the verify kernels is bounded the same way (2 s). */
 sd_status sd_debug_wait_timeout(int64_t limit_ns, sd_stream_t stream);
 
+/* The matmul's work partition, replayed on the host with the same code the
+ * kernels walk: for each of the `sms` CTAs its pieces in order, as rows of 8
+ * int32 {cta, split, unit, j0, j1, first owner, owners, last}; plus the plan
+ * {KB, NU, KS, KBs, KBlast, G, P, D, R} in plan[9].  Returns the number of
+ * pieces, -1 for a shape the matmul rejects, -2 when cap rows are too few.
+ * No GPU is needed. */
+int64_t sd_debug_schedule(int qtype, int64_t n_out, int64_t k_in, int32_t pair, int32_t head, int32_t sms,
+                          int32_t *plan, int32_t *rows, int64_t cap);
+
 #ifdef __cplusplus
 }
 #endif

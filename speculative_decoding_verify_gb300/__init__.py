@@ -92,6 +92,7 @@ def lib():
             "sd_debug_cexp": ([P, I64, P, P], I),
             "sd_debug_philox": ([U64, I64, I64, P, P], I),
             "sd_debug_wait_timeout": ([I64, P], I),
+            "sd_debug_schedule": ([I, I64, I64, I32, I32, I32, P, P, I64], I64),
             "sd_pass_plan_bytes": ([I32], SZ),
             "sd_pass_workspace_bytes": ([I64, I64, I64, I32], SZ),
             "sd_pass_prepare": ([ctypes.POINTER(SdPassDesc), P, SZ, ctypes.POINTER(SdPass)], I),

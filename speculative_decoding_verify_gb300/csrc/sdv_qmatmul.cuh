@@ -173,7 +173,7 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v) {
     return old;
 }
 
-__device__ __forceinline__ void decode_step(const QmmArgs &a, int64_t g, int &s, int &u, int &j, int &len) {
+__host__ __device__ __forceinline__ void decode_step(const QmmArgs &a, int64_t g, int &s, int &u, int &j, int &len) {
     int64_t per = static_cast<int64_t>(a.NU) * a.KBs;
     int64_t ss = g / per;
     if (ss > a.KS - 1) ss = a.KS - 1;
@@ -184,21 +184,21 @@ __device__ __forceinline__ void decode_step(const QmmArgs &a, int64_t g, int &s,
     j = static_cast<int>(rem - static_cast<int64_t>(u) * len);
 }
 
-__device__ __forceinline__ int64_t unit_start(const QmmArgs &a, int s, int u) {
+__host__ __device__ __forceinline__ int64_t unit_start(const QmmArgs &a, int s, int u) {
     int len = (s == a.KS - 1) ? a.KBlast : a.KBs;
     return static_cast<int64_t>(a.NU) * a.KBs * s + static_cast<int64_t>(u) * len;
 }
 
 // length of the shared stream-K step sequence
-__device__ __forceinline__ int64_t seq_len(const QmmArgs &a) { return a.D > 0 ? static_cast<int64_t>(a.R) * a.KB : a.W; }
+__host__ __device__ __forceinline__ int64_t seq_len(const QmmArgs &a) { return a.D > 0 ? static_cast<int64_t>(a.R) * a.KB : a.W; }
 
 // CTA owning step x of the shared sequence: largest c with floor(c wseq / G) <= x
-__device__ __forceinline__ int seq_owner(const QmmArgs &a, int64_t wseq, int64_t x) {
+__host__ __device__ __forceinline__ int seq_owner(const QmmArgs &a, int64_t wseq, int64_t x) {
     return wseq > 0 ? static_cast<int>(((x + 1) * a.G - 1) / wseq) : 0;
 }
 
 // CTAs sharing split s of unit u, and the first of them
-__device__ __forceinline__ void unit_split_owners(const QmmArgs &a, int s, int u, int &first, int &np) {
+__host__ __device__ __forceinline__ void unit_split_owners(const QmmArgs &a, int s, int u, int &first, int &np) {
     const int64_t wseq = seq_len(a);
     int64_t st;
     int len;
@@ -221,18 +221,25 @@ struct Piece {
 struct PieceIter {
     int64_t g, hi;      // cursor in the shared step sequence
     int d_next, d_end;  // whole units still to take
+    int cta;            // the CTA walking this schedule
 };
 
-__device__ __forceinline__ void pieces_begin(const QmmArgs &a, PieceIter &it) {
-    const int64_t c = blockIdx.x, wseq = seq_len(a);
+// The schedule of CTA `cta` (host and device: the host replays it to check the partition).
+__host__ __device__ __forceinline__ void pieces_begin_cta(const QmmArgs &a, PieceIter &it, int cta) {
+    const int64_t c = cta, wseq = seq_len(a);
+    it.cta = cta;
     it.g = c * wseq / a.G;
     it.hi = (c + 1) * wseq / a.G;
     it.d_next = a.D > 0 ? a.R + static_cast<int>(c) * a.D : 0;
     it.d_end = a.D > 0 ? it.d_next + a.D : 0;
 }
 
+__device__ __forceinline__ void pieces_begin(const QmmArgs &a, PieceIter &it) {
+    pieces_begin_cta(a, it, static_cast<int>(blockIdx.x));
+}
+
 // The next piece in processing order (shared run first, whole units last); false when done.
-__device__ __forceinline__ bool pieces_next(const QmmArgs &a, PieceIter &it, Piece &p) {
+__host__ __device__ __forceinline__ bool pieces_next(const QmmArgs &a, PieceIter &it, Piece &p) {
     if (it.g < it.hi) {
         int len;
         if (a.D > 0) {
@@ -253,7 +260,7 @@ __device__ __forceinline__ bool pieces_next(const QmmArgs &a, PieceIter &it, Pie
         p.u = it.d_next++;
         p.j0 = 0;
         p.j1 = a.KB;
-        p.first = blockIdx.x;
+        p.first = it.cta;
         p.np = 1;
         return true;
     }

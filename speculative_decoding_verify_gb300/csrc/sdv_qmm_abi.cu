@@ -65,6 +65,41 @@ using namespace sdv;
 
 extern "C" {
 
+int64_t sd_debug_schedule(int qtype, int64_t n_out, int64_t k_in, int32_t pair, int32_t head, int32_t sms,
+                          int32_t *plan, int32_t *rows, int64_t cap) {
+    if ((qtype != SD_Q8_0 && qtype != SD_Q4_32) || sms < 1 || !plan) return -1;
+    QmmPlan p;
+    if (!make_plan(qtype, n_out, k_in, pair != 0, head != 0, sms, p)) return -1;
+    QmmArgs a = {};
+    fill_plan(a, p);
+    const int32_t fields[9] = {p.KB, p.NU, p.KS, p.KBs, p.KBlast, p.G, p.P, p.D, p.R};
+    for (int i = 0; i < 9; ++i) plan[i] = fields[i];
+    int64_t n = 0;
+    for (int c = 0; c < p.G; ++c) {
+        PieceIter it;
+        pieces_begin_cta(a, it, c);
+        Piece pc, nx;
+        bool have = pieces_next(a, it, pc);
+        while (have) {
+            const bool more = pieces_next(a, it, nx);
+            if (n >= cap || !rows) return -2;
+            int32_t *r = rows + 8 * n;
+            r[0] = c;
+            r[1] = pc.s;
+            r[2] = pc.u;
+            r[3] = pc.j0;
+            r[4] = pc.j1;
+            r[5] = pc.first;
+            r[6] = pc.np;
+            r[7] = more ? 0 : 1;
+            ++n;
+            pc = nx;
+            have = more;
+        }
+    }
+    return n;
+}
+
 size_t sd_qmatmul_workspace_bytes(int qtype, int64_t n_out, int64_t k_in, uint32_t epilogue) {
     if (qtype != SD_Q8_0 && qtype != SD_Q4_32) return 0;
     QmmPlan p;
