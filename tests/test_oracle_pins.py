@@ -557,3 +557,35 @@ def test_filtered_rejection_sampling_exact_law(certainty):
             assert np.all(np.abs(law - p) <= 4e-6), np.abs(law - p).max()
     if not certainty:
         assert np.all(np.abs(law - p) <= 4e-6), np.abs(law - p).max()
+
+
+def test_filter_candidates_match_a_stable_sort_with_many_ties():
+    """Integer-valued logits (many exact ties, -0 and +0 among them): the candidate order is a stable
+    sort of z descending, for every top_k, and the probabilities follow the closed form."""
+    rng = np.random.default_rng(66)
+    for trial in range(30):
+        V = int(rng.integers(1, 200))
+        l = rng.integers(-4, 5, V).astype(np.float32)
+        l[rng.random(V) < 0.1] = -0.0
+        T = float(rng.choice([1.0, 0.5, 2.0]))
+        z = (l / np.float32(T) + np.float32(0.0)).astype(np.float32)
+        order = np.lexsort((np.arange(V), -z))
+        for k in (1, 2, 7, 32):
+            tok, p = oracle.filter_topk_topp(l, T, k, 1.0)
+            kk = min(k, V)
+            assert list(tok) == list(order[:tok.size]), (trial, k)
+            # the nucleus at top_p = 1: the shortest prefix whose fp32 running sum reaches the total
+            # (a tail too small to move the sum is left out; its mass is below 2^-24 of the total)
+            e32 = [oracle.cexp(float(z[i] - z[order[0]])) for i in order[:kk]]
+            S = np.float32(0.0)
+            for x in e32:
+                S = np.float32(S + np.float32(x))
+            run, n = np.float32(0.0), 0
+            while n < kk:
+                run = np.float32(run + np.float32(e32[n]))
+                n += 1
+                if run >= S:
+                    break
+            assert tok.size == n, (trial, k)
+            e = np.exp(z[tok].astype(np.float64) - z[tok[0]])
+            np.testing.assert_allclose(p, e / e.sum(), rtol=2e-6)
