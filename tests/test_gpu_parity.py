@@ -492,3 +492,24 @@ def test_accept_sample_topk_vocab_smaller_than_k(sdv, K):
         status_ok()
         n = int(host(oc)[0])
         assert list(host(ot)[:n]) == list(ref), t
+
+
+def test_accept_sample_topk_many_ties(sdv):
+    """Integer-valued logits with many exact ties and signed zeros: candidates, nucleus and draws
+    bit-exact against the oracle."""
+    rng = np.random.default_rng(158)
+    for trial in range(24):
+        V, K = int(rng.integers(1, 3000)), int(rng.integers(0, 4))
+        l = rng.integers(-4, 5, (K + 1, V)).astype(np.float32)
+        l[rng.random((K + 1, V)) < 0.1] = -0.0
+        T = float(rng.choice([1.0, 0.5, 2.0]))
+        k, p = int(rng.choice([1, 3, 20, 32])), float(rng.choice([1.0, 0.9, 0.5]))
+        dr = rng.integers(0, V, K).astype(np.int32)
+        ot = torch.full((K + 1,), -7, dtype=torch.int32, device="cuda")
+        oc = torch.zeros(1, dtype=torch.int32, device="cuda")
+        sdv.accept_sample_topk(cuda(l), K, cuda(dr) if K else None, ot, oc, k, p, temperature=T, seed=trial,
+                               base_pos=7 * trial)
+        ref = oracle.accept_sample_topk(l, None, dr, T, k, p, trial, 7 * trial)
+        status_ok()
+        n = int(host(oc)[0])
+        assert list(host(ot)[:n]) == list(ref), trial
