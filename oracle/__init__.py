@@ -89,6 +89,8 @@ def _get():
                 "oracle_filter_topk_topp": ([_P, _I64, _F, _I, _F, _P, _P], _I),
                 "oracle_accept_sample_topk_u": ([_P, _I64, _I, _P, _P, _F, _I, _F, _P, _P, _P], _I),
                 "oracle_accept_sample_topk": ([_P, _I64, _I, _P, _P, _F, _I, _F, ctypes.c_uint64, _I64, _P], _I),
+                "oracle_shortlist_copy": ([_P, _I64, _I64, _P, _P, _P], None),
+                "oracle_shortlist_argmax": ([_P, _P, _P, _I64, _I64, _P, _P, _I, _P, _P], None),
             }
             for name, (args, res) in sig.items():
                 f = getattr(lib, name)
@@ -305,6 +307,30 @@ def accept_sample_topk(logits, q_probs, drafts, T: float, top_k: int, top_p: flo
     n = _get().oracle_accept_sample_topk(pl, V, K, pq, pd, T, top_k, top_p, seed, base_pos, out.ctypes.data)
     assert n > 0
     return out[:n].copy()
+
+
+def shortlist_copy(q8_blocks, N: int, K: int):
+    """4-bit copy of a Q8_0 matrix with its row error bounds and row norms: (q4 blocks, bound, wnorm)."""
+    w, pw = _c(np.asarray(q8_blocks).reshape(-1), np.uint8)
+    q4 = np.zeros(N * (K // 32) * 18, dtype=np.uint8)
+    bound = np.empty(N, dtype=np.float32)
+    wnorm = np.empty(N, dtype=np.float32)
+    _get().oracle_shortlist_copy(pw, N, K, q4.ctypes.data, bound.ctypes.data, wnorm.ctypes.data)
+    return q4, bound, wnorm
+
+
+def shortlist_argmax(q4_blocks, bound, q8_blocks, N: int, K: int, q, scales):
+    """Argmax per position through the shortlist (fp64 scores) and the count of rows scored exactly."""
+    w4, p4 = _c(np.asarray(q4_blocks).reshape(-1), np.uint8)
+    bd, pb = _c(bound, np.float32)
+    w8, p8 = _c(np.asarray(q8_blocks).reshape(-1), np.uint8)
+    q, pq = _c(q, np.int8)
+    sc, ps = _c(scales, np.float32)
+    M = q.shape[0]
+    am = np.empty(M, dtype=np.int32)
+    nc = np.empty(M, dtype=np.int64)
+    _get().oracle_shortlist_argmax(p4, pb, p8, N, K, pq, ps, M, am.ctypes.data, nc.ctypes.data)
+    return am, nc
 
 
 def accept_sample_trials(logits, q_probs, drafts_per_trial, T: float, seed: int, base_pos: int):

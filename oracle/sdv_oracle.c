@@ -635,3 +635,127 @@ int oracle_accept_sample_topk(const float *logits, int64_t V, int K, const float
     for (int i = 0; i <= K; ++i) oracle_uniforms(seed, base_pos + i, &ua[i], &ur[i]);
     return oracle_accept_sample_topk_u(logits, V, K, q_probs, drafts, T, top_k, top_p, ua, ur, out);
 }
+
+/* ------------------------------------------------------------------ */
+/* Shortlist head ("Inside OpenJet Engine", section "Shortlist"): a     */
+/* smaller copy of the output layer with a proven bound on every row's  */
+/* error scores all rows; the best-looking rows are scored exactly,     */
+/* which gives a floor, and only rows whose bound reaches the floor are */
+/* scored exactly.  Reading: the copy is the 32-weight 4-bit format     */
+/* (d = amax / 7.5 rounded to fp16, code = 8 + round-half-away(w / d)   */
+/* clamped to [0, 15]) of the Q8_0 head's dequantised weights; the      */
+/* bound of row r is E_r = ||w8_r - w4_r||_2 (Cauchy-Schwarz: the copy  */
+/* score is within E_r ||a||_2 of the exact one, a the dequantised      */
+/* activation row); the floor is F = max_r (s_r - E_r ||a||), s the     */
+/* copy scores, and the candidates are the rows with s_r + E_r ||a|| >= F. */
+/* Exact scores and the argmax (lowest index among equal maxima) are    */
+/* taken over the candidates only.                                      */
+/* ------------------------------------------------------------------ */
+
+/* IEEE binary32 -> binary16, round to nearest even (finite, |x| < 65520) */
+static uint16_t f32_to_f16_rne_oracle(float x) {
+    uint16_t sign = x < 0.0f ? 0x8000u : 0u;
+    double a = fabs((double)x);
+    if (a == 0.0) return sign;
+    int e;
+    (void)frexp(a, &e);                 /* a = f 2^e, f in [0.5, 1): unit exponent e - 1 */
+    int ue = e - 1;
+    if (ue < -14) ue = -14;             /* subnormal spacing 2^-24 */
+    double q = ldexp(a, 10 - ue);       /* the significand in units of the last place */
+    double r = floor(q);
+    double frac = q - r;
+    if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;
+    double v = ldexp(r, ue - 10);       /* rounded value */
+    (void)frexp(v, &e);
+    ue = e - 1;
+    if (v < ldexp(1.0, -14)) return (uint16_t)(sign | (uint16_t)ldexp(v, 24));   /* subnormal */
+    uint16_t mant = (uint16_t)(ldexp(v, 10 - ue) - 1024.0);
+    return (uint16_t)(sign | (uint16_t)((ue + 15) << 10) | mant);
+}
+
+static float round_half_away_f(float x) { return x < 0.0f ? -floorf(-x + 0.5f) : floorf(x + 0.5f); }
+
+/* the 4-bit copy of a Q8_0 matrix [N][K/32], its row bounds E_r and row norms ||w8_r||_2 */
+void oracle_shortlist_copy(const uint8_t *q8, int64_t N, int64_t K, uint8_t *q4, float *bound, float *wnorm) {
+    int64_t KB = K / 32;
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; ++n) {
+        double e2 = 0.0, w2 = 0.0;
+        for (int64_t b = 0; b < KB; ++b) {
+            const uint8_t *blk = q8 + (n * KB + b) * 34;
+            uint8_t *out = q4 + (n * KB + b) * 18;
+            float w[32], amax = 0.0f;
+            for (int i = 0; i < 32; ++i) {
+                w[i] = block_scale(blk) * (float)block_wq(0, blk, i);
+                if (fabsf(w[i]) > amax) amax = fabsf(w[i]);
+            }
+            uint16_t d16 = f32_to_f16_rne_oracle(amax / 7.5f);
+            float d = oracle_f16_to_f32(d16);
+            out[0] = (uint8_t)(d16 & 0xFF);
+            out[1] = (uint8_t)(d16 >> 8);
+            memset(out + 2, 0, 16);
+            for (int i = 0; i < 32; ++i) {
+                int c = 8;
+                if (d > 0.0f) {
+                    float t = round_half_away_f(w[i] / d) + 8.0f;
+                    c = t < 0.0f ? 0 : (t > 15.0f ? 15 : (int)t);
+                }
+                out[2 + (i & 15)] |= (uint8_t)(i < 16 ? c : c << 4);
+                double err = (double)w[i] - (double)d * (double)(c - 8);
+                e2 += err * err;
+                w2 += (double)w[i] * (double)w[i];
+            }
+        }
+        bound[n] = nextafterf((float)sqrt(e2), INFINITY);
+        wnorm[n] = nextafterf((float)sqrt(w2), INFINITY);
+    }
+}
+
+/* exact fp64 score of row n at position m (the definition the shortlist must reproduce) */
+static double exact_score(int qtype, const uint8_t *w, int64_t n, int64_t K, const int8_t *q, const float *scales, int m) {
+    int64_t KB = K / 32;
+    int bb = block_bytes(qtype);
+    double acc = 0.0;
+    for (int64_t b = 0; b < KB; ++b) {
+        const uint8_t *blk = w + (n * KB + b) * bb;
+        acc += (double)block_scale(blk) * (double)scales[(int64_t)m * KB + b] *
+               (double)block_dot(qtype, blk, q + (int64_t)m * K + b * 32);
+    }
+    return acc;
+}
+
+/* shortlist argmax per position; ncand[m] = candidate rows scored exactly.  Scores in fp64. */
+void oracle_shortlist_argmax(const uint8_t *q4, const float *bound, const uint8_t *q8, int64_t N, int64_t K,
+                             const int8_t *q, const float *scales, int M, int32_t *argmax, int64_t *ncand) {
+    int64_t KB = K / 32;
+    double *s = (double *)malloc((size_t)N * sizeof(double));
+    for (int m = 0; m < M; ++m) {
+        double a2 = 0.0;
+        for (int64_t b = 0; b < KB; ++b) {
+            double d = scales[(int64_t)m * KB + b];
+            for (int i = 0; i < 32; ++i) {
+                double v = d * q[(int64_t)m * K + b * 32 + i];
+                a2 += v * v;
+            }
+        }
+        const double an = sqrt(a2);
+#pragma omp parallel for schedule(static)
+        for (int64_t n = 0; n < N; ++n) s[n] = exact_score(1, q4, n, K, q, scales, m);
+        double F = -INFINITY;
+        for (int64_t n = 0; n < N; ++n) {
+            double lo = s[n] - (double)bound[n] * an;
+            if (lo > F) F = lo;
+        }
+        int64_t best = -1, nc = 0;
+        double bv = -INFINITY;
+        for (int64_t n = 0; n < N; ++n) {
+            if (s[n] + (double)bound[n] * an < F) continue;
+            ++nc;
+            double e = exact_score(0, q8, n, K, q, scales, m);
+            if (e > bv) { bv = e; best = n; }
+        }
+        argmax[m] = (int32_t)best;
+        ncand[m] = nc;
+    }
+    free(s);
+}

@@ -589,3 +589,136 @@ def test_filter_candidates_match_a_stable_sort_with_many_ties():
             assert tok.size == n, (trial, k)
             e = np.exp(z[tok].astype(np.float64) - z[tok[0]])
             np.testing.assert_allclose(p, e / e.sum(), rtol=2e-6)
+
+
+# ---------------------------------------------------------------------------
+# shortlist head: 4-bit copy with per-row error bounds, exact argmax over the candidates
+# ---------------------------------------------------------------------------
+
+def _shortlist_case(seed, N=4096, K=1024, M=3):
+    w8 = sdgen.quantized_normal(oracle.Q8_0, sdgen.key(seed, 1), N, K)
+    x = sdgen.normal(sdgen.key(seed, 2), (M, K))
+    q, s = oracle.rmsnorm_quant(x, None)
+    return w8, q, s
+
+
+def _exact_scores(w8, N, K, q, s):
+    dots = oracle.block_dots(oracle.Q8_0, w8, N, K, q).astype(np.float64)  # [M][N][KB]
+    d = oracle.dequant(oracle.Q8_0, w8, N, K).reshape(N, K // 32, 32)
+    dw = np.array([[oracle.f16_to_f32(int(v)) for v in row] for row in
+                   np.asarray(w8).reshape(N, K // 32, 34)[:, :, :2].copy().view(np.uint16)[:, :, 0]])
+    del d
+    return (dots * dw[None] * s.astype(np.float64)[:, None, :]).sum(axis=2)
+
+
+def test_shortlist_copy_error_is_half_a_step_and_bounded():
+    N, K = 256, 512
+    w8 = sdgen.quantized_normal(oracle.Q8_0, sdgen.key(70), N, K)
+    q4, bound, wnorm = oracle.shortlist_copy(w8, N, K)
+    a = oracle.dequant(oracle.Q8_0, w8, N, K).astype(np.float64)
+    b = oracle.dequant(oracle.Q4_32, q4, N, K).astype(np.float64)
+    d4 = np.asarray(q4).reshape(N, K // 32, 18)[:, :, :2].copy().view(np.uint16)[:, :, 0]
+    step = np.vectorize(lambda h: oracle.f16_to_f32(int(h)))(d4).astype(np.float64)
+    # d = amax / 7.5 in fp32, rounded to fp16 to nearest even (numpy's conversion)
+    amax = np.abs(oracle.dequant(oracle.Q8_0, w8, N, K).reshape(N, K // 32, 32)).max(axis=2).astype(np.float32)
+    assert np.array_equal(d4, (amax / np.float32(7.5)).astype(np.float16).view(np.uint16))
+    err = (a - b).reshape(N, K // 32, 32)
+    # half a step, plus the fp16 rounding of d at the clamped extreme: |w| <= amax <= 7.5 d (1 + 2^-10)
+    assert np.all(np.abs(err) <= 0.5 * step[:, :, None] + 7.5 * step[:, :, None] * 2.0 ** -10)
+    e = np.sqrt((err.reshape(N, K) ** 2).sum(axis=1))
+    assert np.all(bound >= e) and np.all(bound <= e * (1 + 1e-6) + 1e-30)
+    assert np.allclose(wnorm, np.sqrt((a ** 2).sum(axis=1)), rtol=1e-6)
+
+
+def test_shortlist_bound_holds_for_every_row():
+    N, K, M = 2048, 1024, 3
+    w8, q, s = _shortlist_case(71, N, K, M)
+    q4, bound, _ = oracle.shortlist_copy(w8, N, K)
+    exact = _exact_scores(w8, N, K, q, s)
+    dots4 = oracle.block_dots(oracle.Q4_32, q4, N, K, q).astype(np.float64)
+    d4 = np.asarray(q4).reshape(N, K // 32, 18)[:, :, :2].copy().view(np.uint16)[:, :, 0]
+    dw4 = np.vectorize(lambda h: oracle.f16_to_f32(int(h)))(d4).astype(np.float64)
+    copy = (dots4 * dw4[None] * s.astype(np.float64)[:, None, :]).sum(axis=2)
+    an = np.sqrt(((q.astype(np.float64).reshape(M, K // 32, 32) * s[:, :, None]) ** 2).sum(axis=(1, 2)))
+    assert np.all(np.abs(exact - copy) <= bound[None, :] * an[:, None] * (1 + 1e-9))
+
+
+def test_shortlist_argmax_is_the_full_argmax_with_ties():
+    N, K, M = 4096, 1024, 3
+    w8, q, s = _shortlist_case(72, N, K, M)
+    exact = _exact_scores(w8, N, K, q, s)
+    # a duplicate of position 0's best row at a lower index: equal scores, the lower index must win
+    top = int(np.argmax(exact[0]))
+    rows = np.asarray(w8).reshape(N, -1).copy()
+    dup = 5 if top != 5 else 6
+    rows[dup] = rows[top]
+    w8 = rows.reshape(-1)
+    exact = _exact_scores(w8, N, K, q, s)
+    q4, bound, _ = oracle.shortlist_copy(w8, N, K)
+    am, nc = oracle.shortlist_argmax(q4, bound, w8, N, K, q, s)
+    ref = [int(np.flatnonzero(exact[m] == exact[m].max())[0]) for m in range(M)]
+    assert list(am) == ref and am[0] == min(dup, top)
+    assert np.all(nc >= 1)
+
+
+def test_shortlist_scores_few_rows_when_the_winner_stands_out():
+    """Random rows leave every row within the worst-case bound of the best (the bound grows like
+    ||err|| ||a||, the spread of random scores like their root-mean-square), so nothing is skipped;
+    a row aligned with the activations, as in a peaked output distribution, lets the shortlist skip
+    almost all of them."""
+    N, K, M = 4096, 1024, 2
+    w8, q, s = _shortlist_case(73, N, K, M)
+    a = (q.astype(np.float64).reshape(M, K // 32, 32) * s[:, :, None]).reshape(M, K)
+    # rows 100 and 2000 follow positions 0 and 1's activations (requantised as Q8_0 blocks)
+    planted = {0: 100, 1: 2000}
+    rows = np.asarray(w8).reshape(N, -1).copy()
+    for m, r in planted.items():
+        blk = sdgen.quantize(oracle.Q8_0, (a[m] / np.abs(a[m]).max() * 0.1).astype(np.float32)[None, :])
+        rows[r] = np.asarray(blk).reshape(-1)
+    w8 = rows.reshape(-1)
+    q4, bound, _ = oracle.shortlist_copy(w8, N, K)
+    am, nc = oracle.shortlist_argmax(q4, bound, w8, N, K, q, s)
+    exact = _exact_scores(w8, N, K, q, s)
+    assert list(am) == [int(np.argmax(exact[m])) for m in range(M)] == [100, 2000]
+    assert np.all(nc <= N // 100), nc
+
+
+def test_shortlist_finds_the_exact_winner_when_the_copy_ranks_it_second():
+    """Two rows whose 4-bit copies are equal byte for byte, the lower-index one a single int8 step
+    worse in exact arithmetic: the copy alone would pick the lower index, the exact scores of the
+    candidates must pick the other."""
+    N, K, M = 1024, 512, 1
+    w8, q, s = _shortlist_case(74, N, K, M)
+    exact = _exact_scores(w8, N, K, q, s)
+    top = int(np.argmax(exact[0]))
+    lo = 3 if top != 3 else 4
+    rows = np.asarray(w8).reshape(N, K // 32, 34).copy()
+    a = q.astype(np.int64).reshape(K)
+    copy_top = np.asarray(oracle.shortlist_copy(rows[top].reshape(-1), 1, K)[0]).copy()
+    done = False
+    for b in range(K // 32):
+        v = rows[top, b, 2:].view(np.int8).astype(np.int64)
+        for j in range(32):
+            aj = a[b * 32 + j]
+            if aj == 0 or abs(v[j]) == np.abs(v).max():
+                continue
+            w = v.copy()
+            w[j] -= 1 if aj > 0 else -1
+            if abs(w[j]) >= np.abs(v).max():
+                continue
+            cand = rows[top].copy()
+            cand[b, 2:] = w.astype(np.int8).view(np.uint8)
+            if np.array_equal(np.asarray(oracle.shortlist_copy(cand.reshape(-1), 1, K)[0]), copy_top):
+                rows[lo] = cand
+                done = True
+                break
+        if done:
+            break
+    assert done
+    w8 = rows.reshape(-1)
+    exact = _exact_scores(w8, N, K, q, s)
+    q4, bound, _ = oracle.shortlist_copy(w8, N, K)
+    assert np.array_equal(np.asarray(q4).reshape(N, -1)[lo], np.asarray(q4).reshape(N, -1)[top])
+    assert exact[0, lo] < exact[0, top] == exact[0].max()
+    am, nc = oracle.shortlist_argmax(q4, bound, w8, N, K, q, s)
+    assert int(am[0]) == top and nc[0] >= 2
