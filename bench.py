@@ -129,12 +129,16 @@ def build_stack(spec, M, device, timings):
                        head_q=spec.head_q, device=device)
 
 
+# The translation units of pass_kernel and the headers they include.
+PASS_KERNEL_SOURCES = ("sdv_common.cuh", "sdv_pass.cu", "sdv_pass_sample.cu", "sdv_qmatmul.cuh", "sdv_sample.cuh",
+                       "sdv_topk.cuh")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     d = os.path.join(ROOT, "speculative_decoding_verify_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
-        if f.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(d, f), "rb").read())
+    for f in PASS_KERNEL_SOURCES:
+        h.update(open(os.path.join(d, f), "rb").read())
     return h.hexdigest()[:16]
 
 

@@ -673,8 +673,6 @@ static uint16_t f32_to_f16_rne_oracle(float x) {
     return (uint16_t)(sign | (uint16_t)((ue + 15) << 10) | mant);
 }
 
-static float round_half_away_f(float x) { return x < 0.0f ? -floorf(-x + 0.5f) : floorf(x + 0.5f); }
-
 /* the 4-bit copy of a Q8_0 matrix [N][K/32], its row bounds E_r and row norms ||w8_r||_2 */
 void oracle_shortlist_copy(const uint8_t *q8, int64_t N, int64_t K, uint8_t *q4, float *bound, float *wnorm) {
     int64_t KB = K / 32;
@@ -697,7 +695,7 @@ void oracle_shortlist_copy(const uint8_t *q8, int64_t N, int64_t K, uint8_t *q4,
             for (int i = 0; i < 32; ++i) {
                 int c = 8;
                 if (d > 0.0f) {
-                    float t = round_half_away_f(w[i] / d) + 8.0f;
+                    float t = roundf(w[i] / d) + 8.0f;   /* C99 roundf: halves away from zero */
                     c = t < 0.0f ? 0 : (t > 15.0f ? 15 : (int)t);
                 }
                 out[2 + (i & 15)] |= (uint8_t)(i < 16 ? c : c << 4);

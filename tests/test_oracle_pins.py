@@ -622,6 +622,15 @@ def test_shortlist_copy_error_is_half_a_step_and_bounded():
     # d = amax / 7.5 in fp32, rounded to fp16 to nearest even (numpy's conversion)
     amax = np.abs(oracle.dequant(oracle.Q8_0, w8, N, K).reshape(N, K // 32, 32)).max(axis=2).astype(np.float32)
     assert np.array_equal(d4, (amax / np.float32(7.5)).astype(np.float16).view(np.uint16))
+    # codes: 8 + round-half-away(w / d) of the fp32 quotient, clamped to [0, 15] (8 where d == 0)
+    d32 = step.astype(np.float32)[:, :, None]
+    wq = a.astype(np.float32).reshape(N, K // 32, 32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        t = (wq / d32).astype(np.float64)
+    want = np.where(d32 > 0, np.clip(np.sign(t) * np.floor(np.abs(t) + 0.5) + 8, 0, 15), 8).astype(np.uint8)
+    nib = np.asarray(q4).reshape(N, K // 32, 18)[:, :, 2:]
+    got = np.concatenate([nib & 15, nib >> 4], axis=2)
+    assert np.array_equal(got, want)
     err = (a - b).reshape(N, K // 32, 32)
     # half a step, plus the fp16 rounding of d at the clamped extreme: |w| <= amax <= 7.5 d (1 + 2^-10)
     assert np.all(np.abs(err) <= 0.5 * step[:, :, None] + 7.5 * step[:, :, None] * 2.0 ** -10)
