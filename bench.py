@@ -296,6 +296,97 @@ def job_rates(weight_bytes: int, M: int, ms: float, world: int):
     return weight_bytes / (ms * 1e-3) / 1e9 * world, M / (ms * 1e-3) * world
 
 
+def shortlist_bench(args, local):
+    """The exact shortlist head against the full Q8_0 head on the 5120 x 151936 head over M positions:
+    device time per call (CUDA events, one stream, the 826 MB head and its 438 MB copy far above L2),
+    rows scored exactly, and whether both give the same argmax.  Two heads: random rows (N(0, 0.02),
+    the bound prunes nothing) and the same head with one row per position aligned with that
+    position's activations (a peaked output distribution, where the bound prunes nearly every row).
+    Prints one JSON line."""
+    import numpy as np
+    import torch
+
+    import sdgen
+    from speculative_decoding_verify_gb300 import build as b
+    b.build()
+    sdgen.build()
+    import speculative_decoding_verify_gb300 as sdv
+
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    spec = sdgen.StackSpec(layers=0)
+    N, K, M = spec.vocab, spec.hidden, args.M
+    KB = K // 32
+    hb_host = sdgen.pinned_quantized_normal(spec.head_q, spec.weight_key(0, "head"), N, K)
+    hb = hb_host.to(dev).reshape(-1)
+    x = torch.from_numpy(spec.hidden_in(M)).to(dev)
+    q = torch.empty((M, K), dtype=torch.int8, device=dev)
+    sc = torch.empty((M, KB), dtype=torch.float32, device=dev)
+    sdv.rmsnorm_quant_acts(x, None, q, sc)
+    torch.cuda.synchronize()
+
+    def plant():
+        """Rows 151935, 0, 77777, ... follow positions 0, 1, 2, ...: their activations / max * 0.1."""
+        a = (q.cpu().numpy().astype(np.float64).reshape(M, KB, 32) * sc.cpu().numpy()[:, :, None]).reshape(M, K)
+        rows = [(151935 + 77777 * m) % N for m in range(M)]
+        for m, r in enumerate(rows):
+            blk = sdgen.quantize(spec.head_q, (a[m] / np.abs(a[m]).max() * 0.1).astype(np.float32)[None, :])
+            hb[r * KB * 34:(r + 1) * KB * 34].copy_(torch.from_numpy(np.ascontiguousarray(blk).reshape(-1)))
+        torch.cuda.synchronize()
+        return rows
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        if sdv.device_status() != 0:
+            raise RuntimeError("device status after the timed calls")
+        return e0.elapsed_time(e1) / args.steps
+
+    cases = {}
+    for case in ("random", "peaked"):
+        planted = plant() if case == "peaked" else None
+        head = sdv.repack_weights(spec.head_q, hb, N, K)
+        copy, bound, wnorm = sdv.shortlist_build(hb, N, K)
+        cw = sdv.repack_weights(sdv.Q4_32, copy, N, K)
+        del copy
+        ws_h = sdv.workspace(sdv.head_workspace_bytes(N, K), device=dev)
+        ws_s = sdv.workspace(sdv.shortlist_workspace_bytes(N, K), device=dev)
+        logits = torch.empty((M, N), dtype=torch.float32, device=dev)
+        am_h = torch.empty(M, dtype=torch.int32, device=dev)
+        rmax = torch.empty(M, dtype=torch.float32, device=dev)
+        rsum = torch.empty(M, dtype=torch.float32, device=dev)
+        am_s = torch.empty(M, dtype=torch.int32, device=dev)
+        nc = torch.empty(M, dtype=torch.int32, device=dev)
+        full_ms = timed(lambda: sdv.head_logits(head, N, K, q, sc, ws_h, logits, am_h, rmax, rsum))
+        short_ms = timed(lambda: sdv.head_shortlist(cw, bound, wnorm, hb, N, K, q, sc, ws_s, am_s, nc))
+        cases[case] = {"full_head_ms": round(full_ms, 4), "shortlist_ms": round(short_ms, 4),
+                       "speedup": round(full_ms / short_ms, 3), "rows_scored_exactly": nc.cpu().tolist(),
+                       "argmax_shortlist": am_s.cpu().tolist(), "argmax_full_head_fp32": am_h.cpu().tolist(),
+                       "planted_rows": planted}
+        del head, cw, ws_h, ws_s, logits
+        torch.cuda.empty_cache()
+        log(f"shortlist {case}: full head {full_ms:.4f} ms, shortlist {short_ms:.4f} ms, "
+            f"rows scored exactly {cases[case]['rows_scored_exactly']}")
+    head_bytes = N * KB * 34
+    copy_bytes = N * KB * 18
+    print(json.dumps({
+        "metric": "exact greedy head: ms per call, shortlist vs full Q8_0 head", "unit": "ms",
+        "value": cases["peaked"]["shortlist_ms"], "higher_is_better": False, "steps": args.steps,
+        "warmup": args.warmup, "n_gpus": 1, "dtype": "int8 dot / fp32 copy scores / fp64 exact scores",
+        "data": "synthetic", "config": {"workload": f"Q8_0 head {N}x{K}, M={M}",
+                                        "l2": "inputs larger than L2 (head 826 MB, copy 438 MB)"},
+        "algorithmic_bytes": {"full_head": head_bytes, "shortlist_copy": copy_bytes + 8 * N,
+                              "per_exact_row": KB * 34},
+        "cases": cases}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -310,6 +401,8 @@ def main():
                     help="time only the one-launch pass (no per-operation graph, no eager per-kernel breakdown)")
     ap.add_argument("--mode", default="fused", choices=["fused", "graph"],
                     help="fused: the whole pass as one persistent launch; graph: one CUDA graph of per-op launches")
+    ap.add_argument("--shortlist", action="store_true",
+                    help="instead of the pass: time the exact shortlist head against the full head (own JSON line)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -324,6 +417,9 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             reference_arm(args, spec, M)
+        return
+    if args.shortlist:
+        shortlist_bench(args, local)
         return
 
     import numpy as np

@@ -198,6 +198,43 @@ sd_status sd_head_logits(const void *w, int64_t vocab, int64_t hidden, const int
                          float *row_sumexp, void *workspace, size_t ws_bytes, sd_stream_t stream);
 
 /*
+ * Exact shortlist head for greedy verification ("Inside OpenJet Engine",
+ * section "Shortlist": a cheaper copy of the output layer with a proven bound
+ * on each row's error scores every row, the best guaranteed score becomes a
+ * floor, and only rows whose bound reaches the floor are scored exactly).
+ *
+ * sd_shortlist_build (load time): head_blocks is the Q8_0 head in GGUF order
+ * [vocab][hidden/32] (device, 16-byte aligned).  Writes copy_blocks, the
+ * SD_Q4_32 copy in GGUF order (vocab * hidden/32 * 18 bytes): per block d =
+ * amax|w|/7.5 rounded to fp16 (nearest even; held at 65504 if larger), code =
+ * 8 + round-half-away(w/d) clamped to [0, 15] (8 if d = 0); bound[r] >=
+ * ||w8_r - w4_r||_2 and wnorm[r] >= ||w8_r||_2 (fp32, rounded up) of the
+ * dequantised rows.  Repack copy_blocks with sd_repack_weights(SD_Q4_32, ...,
+ * flags 0) for sd_head_shortlist.  Weights must be finite.
+ *
+ * sd_head_shortlist (verify time): copy_w the repacked copy, bound / wnorm
+ * from the build, head_blocks the GGUF-order Q8_0 head; q int8 [M][hidden],
+ * scales fp32 [M][hidden/32] as for sd_head_logits; 1 <= M <= 16.  argmax
+ * int32 [M] receives, per position, the row maximising the exact score
+ *   e_r = sum over blocks b, in order, of (d_w[r,b] * d_a[b]) * dot_b(r)
+ * in fp64 (one rounding per product and per addition; lowest index among
+ * equal maxima) -- the argmax of the exact head, whatever the copy says.
+ * n_cand int32 [M] (or NULL) receives how many rows were scored exactly.
+ * Device-side: a position with no candidate (non-finite inputs only) records
+ * SD_EDEVICE in the status word and gets argmax -1.  workspace: ws_bytes >=
+ * sd_shortlist_workspace_bytes(vocab, hidden), zero-filled by the caller once
+ * (it holds the copy matmul's counters, which every call returns to zero).
+ * Errors: SD_EINVAL on null/misaligned pointers or bad sizes; SD_EUNSUPPORTED
+ * for M > 16 or hidden/32 * M > 12288.
+ */
+sd_status sd_shortlist_build(const void *head_blocks, int64_t vocab, int64_t hidden, void *copy_blocks, float *bound,
+                             float *wnorm, sd_stream_t stream);
+size_t sd_shortlist_workspace_bytes(int64_t vocab, int64_t hidden);
+sd_status sd_head_shortlist(const void *copy_w, const float *bound, const float *wnorm, const void *head_blocks,
+                            int64_t vocab, int64_t hidden, const int8_t *q, const float *scales, int32_t M,
+                            int32_t *argmax, int32_t *n_cand, void *workspace, size_t ws_bytes, sd_stream_t stream);
+
+/*
  * Greedy acceptance ("How Kinetic is fast", section "Why the output does not
  * change": keep a guess only when it is the model's top token; section
  * "RAD-1": tree drafts, each row seeing only its own path).

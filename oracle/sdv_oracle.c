@@ -687,7 +687,9 @@ void oracle_shortlist_copy(const uint8_t *q8, int64_t N, int64_t K, uint8_t *q4,
                 w[i] = block_scale(blk) * (float)block_wq(0, blk, i);
                 if (fabsf(w[i]) > amax) amax = fabsf(w[i]);
             }
-            uint16_t d16 = f32_to_f16_rne_oracle(amax / 7.5f);
+            /* a scale beyond the largest half (65504) is held there: the copy stays finite */
+            const float dq = amax / 7.5f;
+            uint16_t d16 = dq < 65520.0f ? f32_to_f16_rne_oracle(dq) : (uint16_t)0x7BFF;
             float d = oracle_f16_to_f32(d16);
             out[0] = (uint8_t)(d16 & 0xFF);
             out[1] = (uint8_t)(d16 >> 8);

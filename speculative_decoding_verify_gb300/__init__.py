@@ -82,6 +82,9 @@ def lib():
             "sd_qmatmul_multipos_noalloc": ([I, P, I64, I64, P, P, I32, P, P, U32, I64, P, P, P], I),
             "sd_head_workspace_bytes": ([I64, I64], SZ),
             "sd_head_logits": ([P, I64, I64, P, P, I32, F, P, P, P, P, P, SZ, P], I),
+            "sd_shortlist_build": ([P, I64, I64, P, P, P, P], I),
+            "sd_shortlist_workspace_bytes": ([I64, I64], SZ),
+            "sd_head_shortlist": ([P, P, P, P, I64, I64, P, P, I32, P, P, P, SZ, P], I),
             "sd_accept_greedy": ([P, P, P, I32, P, P, P], I),
             "sd_accept_sample": ([P, I64, I32, P, P, P, P, F, U64, I64, P, P, P], I),
             "sd_accept_sample_topk": ([P, I64, I32, P, P, F, I32, F, U64, I64, P, P, P], I),
@@ -197,6 +200,31 @@ def head_logits(w: torch.Tensor, vocab: int, hidden: int, q: torch.Tensor, scale
     M = q.shape[0]
     _check(lib().sd_head_logits(_p(w), vocab, hidden, _p(q), _p(scales), M, temperature, _p(logits), _p(argmax),
                                 _p(row_max), _p(row_sumexp), _p(ws), ws.numel(), _stream()), "sd_head_logits")
+
+
+def shortlist_build(head_blocks: torch.Tensor, vocab: int, hidden: int):
+    """4-bit copy of a GGUF-order Q8_0 head with its row error bounds and row norms:
+    (copy blocks in GGUF order, bound fp32 [vocab], wnorm fp32 [vocab])."""
+    dev = head_blocks.device
+    copy = torch.empty(vocab * (hidden // 32) * 18, dtype=torch.uint8, device=dev)
+    bound = torch.empty(vocab, dtype=torch.float32, device=dev)
+    wnorm = torch.empty(vocab, dtype=torch.float32, device=dev)
+    _check(lib().sd_shortlist_build(_p(head_blocks), vocab, hidden, _p(copy), _p(bound), _p(wnorm), _stream()),
+           "sd_shortlist_build")
+    return copy, bound, wnorm
+
+
+def shortlist_workspace_bytes(vocab: int, hidden: int) -> int:
+    return int(lib().sd_shortlist_workspace_bytes(vocab, hidden))
+
+
+def head_shortlist(copy_w: torch.Tensor, bound: torch.Tensor, wnorm: torch.Tensor, head_blocks: torch.Tensor,
+                   vocab: int, hidden: int, q: torch.Tensor, scales: torch.Tensor, ws: torch.Tensor,
+                   argmax: torch.Tensor, n_cand: torch.Tensor | None = None):
+    M = q.shape[0]
+    _check(lib().sd_head_shortlist(_p(copy_w), _p(bound), _p(wnorm), _p(head_blocks), vocab, hidden, _p(q),
+                                   _p(scales), M, _p(argmax), _p(n_cand), _p(ws), ws.numel(), _stream()),
+           "sd_head_shortlist")
 
 
 def accept_greedy(argmax: torch.Tensor, tokens: torch.Tensor | None, parent: torch.Tensor | None, M: int,

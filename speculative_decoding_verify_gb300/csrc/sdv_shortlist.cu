@@ -1,0 +1,414 @@
+// sdv_shortlist.cu - exact shortlist head for greedy verification ("Inside OpenJet Engine",
+// section "Shortlist"): a cheaper copy of the output layer, with a proven bound on each row's
+// error, scores every row; the best guaranteed score (the floor) rules out every row whose bound
+// cannot reach it; the remaining rows are scored exactly, and the argmax over them is the argmax
+// of the exact head.
+//
+// The copy is the 32-weight 4-bit format of the Q8_0 head's dequantised rows (d = amax / 7.5
+// rounded to fp16, code = 8 + round-half-away(w / d) clamped to [0, 15]).  Row r carries
+// E_r >= ||w8_r - w4_r||_2 and W_r >= ||w8_r||_2, both rounded up.  With a the dequantised
+// activation row of one position, its norm rounded up as A, and s_r the copy score the 4-bit
+// matmul computes in fp32:
+//   |exact_r - s_r| <= B_r = (E_r + gamma (2 W_r + E_r)) A
+// (Cauchy-Schwarz for the copy's error; gamma covers the fp32 rounding of the copy score, whose
+// terms add up to at most ||w4_r|| ||a|| <= (W_r + E_r) A, and the fp64 rounding of the exact
+// score).  The floor is F = max_r (s_r - B_r) and row r is a candidate iff s_r + B_r >= F; every
+// bound operation rounds towards the safe side, so the row of the exact maximum is always a
+// candidate.  Exact scores are sums over the row's 32-blocks, in block order, of
+// (d_w d_a) * dot in fp64 -- the same arithmetic as the oracle's definition, so the argmax (lowest
+// index among equal maxima) is the exact one bit for bit.
+#include "sdv_common.cuh"
+
+namespace sdv {
+
+constexpr int SL_THREADS = 256;
+constexpr int SL_WARPS = SL_THREADS / 32;
+constexpr int SL_MAXM = 16;
+constexpr size_t SL_EXACT_SMEM_CAP = 96 * 1024;  // per CTA: two CTAs of the exact kernel per SM
+
+struct SlBest {
+    double v;     // best exact score (-inf: none)
+    int32_t idx;  // its row (-1: none)
+    int32_t cnt;  // candidate rows scored
+};
+
+struct ShortlistArgs {
+    const float *scores;  // copy scores [M][N]
+    const float *bound;   // E_r [N]
+    const float *wnorm;   // W_r [N]
+    const uint8_t *w8;    // the Q8_0 head, GGUF-order blocks [N][KB]
+    const int8_t *q;      // activations [M][K]
+    const float *sc;      // activation scales [M][KB]
+    int64_t N, KB;
+    int32_t M;
+    int32_t G;              // CTAs of the floor and exact kernels
+    int64_t rows_per_cta;   // multiple of 32
+    double gamma;
+    double *an;             // [SL_MAXM] activation norms (rounded up), written by the floor kernel
+    double *floor_part;     // [G][SL_MAXM]
+    SlBest *best_part;      // [G][SL_MAXM]
+    int32_t *argmax;        // [M]
+    int32_t *n_cand;        // [M] or nullptr
+    int *status;
+};
+
+// ---------------------------------------------------------------------------
+// load time: the copy, E_r and W_r (one warp per row, lanes over the row's blocks)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ double warp_sum_ru(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = __dadd_ru(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__global__ void __launch_bounds__(SL_THREADS) shortlist_build_kernel(const uint8_t *src, int64_t N, int64_t KB,
+                                                                     uint8_t *dst, float *bound, float *wnorm) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int lane = static_cast<int>(threadIdx.x) & 31;
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * SL_WARPS;
+    for (int64_t r = static_cast<int64_t>(blockIdx.x) * SL_WARPS + threadIdx.x / 32; r < N; r += nwarps) {
+        double e2 = 0.0, w2 = 0.0;  // sums of non-negative terms, every operation rounded up
+        for (int64_t b = lane; b < KB; b += 32) {
+            // a Q8_0 block starts on an even byte: read it as 17 halfwords
+            const uint16_t *blk = reinterpret_cast<const uint16_t *>(src + (r * KB + b) * 34);
+            const float d8 = __half2float(__ushort_as_half(blk[0]));
+            float w[32];
+            float amax = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const uint16_t v = blk[1 + j];
+                w[2 * j] = d8 * static_cast<float>(static_cast<int8_t>(v & 0xFF));  // exact: 11 x 8 bits
+                w[2 * j + 1] = d8 * static_cast<float>(static_cast<int8_t>(v >> 8));
+                amax = fmaxf(amax, fmaxf(fabsf(w[2 * j]), fabsf(w[2 * j + 1])));
+            }
+            // d = amax / 7.5 to fp16 (nearest even), held at the largest finite half if it overflows
+            const float dq = amax / 7.5f;
+            const __half dh = dq < 65520.0f ? __float2half_rn(dq) : __ushort_as_half(static_cast<uint16_t>(0x7BFF));
+            const float d = __half2float(dh);
+            int c[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                int ci = 8;
+                if (d > 0.0f) {
+                    const float t = roundf(w[i] / d) + 8.0f;  // roundf: halves away from zero
+                    ci = t < 0.0f ? 0 : (t > 15.0f ? 15 : static_cast<int>(t));
+                }
+                c[i] = ci;
+                // w and d (c - 8) carry at most 18 significant bits a few binades apart: the
+                // difference is exact in fp64
+                const double err = static_cast<double>(w[i]) - static_cast<double>(d) * static_cast<double>(ci - 8);
+                e2 = __dadd_ru(e2, __dmul_ru(err, err));
+                w2 = __dadd_ru(w2, __dmul_ru(static_cast<double>(w[i]), static_cast<double>(w[i])));
+            }
+            uint16_t *out = reinterpret_cast<uint16_t *>(dst + (r * KB + b) * 18);
+            out[0] = __half_as_ushort(dh);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t lo = static_cast<uint32_t>(c[2 * j] | (c[2 * j + 16] << 4));
+                const uint32_t hi = static_cast<uint32_t>(c[2 * j + 1] | (c[2 * j + 17] << 4));
+                out[1 + j] = static_cast<uint16_t>(lo | (hi << 8));
+            }
+        }
+        e2 = warp_sum_ru(e2);
+        w2 = warp_sum_ru(w2);
+        if (lane == 0) {
+            bound[r] = __double2float_ru(__dsqrt_ru(e2));
+            wnorm[r] = __double2float_ru(__dsqrt_ru(w2));
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// verify time
+// ---------------------------------------------------------------------------
+
+// B_r for one position, rounded up
+__device__ __forceinline__ double row_bound(const ShortlistArgs &a, int64_t r, double an) {
+    const double E = static_cast<double>(a.bound[r]);
+    const double W = static_cast<double>(a.wnorm[r]);
+    const double c = __dadd_ru(E, __dmul_ru(a.gamma, __dadd_ru(__dmul_ru(2.0, W), E)));
+    return __dmul_ru(c, an);
+}
+
+__device__ __forceinline__ double block_max(double v, double *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmax(v, __shfl_xor_sync(0xffffffffu, v, o));
+    const int warp = static_cast<int>(threadIdx.x) / 32, lane = static_cast<int>(threadIdx.x) & 31;
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    double m = red[0];
+#pragma unroll
+    for (int w = 1; w < SL_WARPS; ++w) m = fmax(m, red[w]);
+    return m;
+}
+
+// ||a_m||_2 of every position, rounded up (the same value in every CTA)
+__device__ void act_norms(const ShortlistArgs &a, double *an, double *red) {
+    const int64_t K = a.KB * 32;
+    const int warp = static_cast<int>(threadIdx.x) / 32, lane = static_cast<int>(threadIdx.x) & 31;
+    for (int m = 0; m < a.M; ++m) {
+        double t = 0.0;
+        for (int64_t i = threadIdx.x; i < K; i += SL_THREADS) {
+            // fp32 scale x int8 code: exact in fp64
+            const double v = static_cast<double>(a.sc[m * a.KB + i / 32]) * static_cast<double>(a.q[m * K + i]);
+            t = __dadd_ru(t, __dmul_ru(v, v));
+        }
+        t = warp_sum_ru(t);
+        __syncthreads();
+        if (lane == 0) red[warp] = t;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            double s = 0.0;
+            for (int w = 0; w < SL_WARPS; ++w) s = __dadd_ru(s, red[w]);
+            an[m] = __dsqrt_ru(s);
+        }
+    }
+    __syncthreads();
+}
+
+// the floor: per CTA, max over its rows of s_r - B_r (rounded down), per position
+__global__ void __launch_bounds__(SL_THREADS) shortlist_floor_kernel(const ShortlistArgs a) {
+    __shared__ double an[SL_MAXM];
+    __shared__ double red[SL_WARPS];
+    pdl_wait();
+    pdl_launch_dependents();
+    act_norms(a, an, red);
+    if (blockIdx.x == 0 && static_cast<int>(threadIdx.x) < a.M) a.an[threadIdx.x] = an[threadIdx.x];
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * a.rows_per_cta;
+    const int64_t r1 = min(a.N, r0 + a.rows_per_cta);
+    for (int m = 0; m < a.M; ++m) {
+        double mx = -INFINITY;
+        for (int64_t r = r0 + threadIdx.x; r < r1; r += SL_THREADS)
+            mx = fmax(mx, __dsub_rd(static_cast<double>(a.scores[m * a.N + r]), row_bound(a, r, an[m])));
+        mx = block_max(mx, red);
+        if (threadIdx.x == 0) a.floor_part[blockIdx.x * SL_MAXM + m] = mx;
+    }
+}
+
+// candidates and their exact scores; per CTA the best row per position and the candidate count
+__global__ void __launch_bounds__(SL_THREADS) shortlist_exact_kernel(const ShortlistArgs a) {
+    extern __shared__ double prod[];  // [warps][KB][M] block products of the row in hand
+    __shared__ double F[SL_MAXM], an[SL_MAXM];
+    __shared__ SlBest wb[SL_WARPS][SL_MAXM];
+    pdl_wait();
+    pdl_launch_dependents();
+    const int nw = static_cast<int>(blockDim.x) / 32;
+    const int warp = static_cast<int>(threadIdx.x) / 32, lane = static_cast<int>(threadIdx.x) & 31;
+    const int M = a.M;
+    const int64_t K = a.KB * 32;
+    if (static_cast<int>(threadIdx.x) < M) {
+        double f = -INFINITY;
+        for (int c = 0; c < a.G; ++c) f = fmax(f, a.floor_part[c * SL_MAXM + threadIdx.x]);
+        F[threadIdx.x] = f;
+        an[threadIdx.x] = a.an[threadIdx.x];
+    }
+    __syncthreads();
+    double bv = -INFINITY;  // lane m keeps position m's best
+    int32_t bi = -1, cnt = 0;
+    double *p = prod + static_cast<size_t>(warp) * a.KB * M;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * a.rows_per_cta;
+    const int64_t r1 = min(a.N, r0 + a.rows_per_cta);
+    for (int64_t g = r0 + 32 * warp; g < r1; g += 32 * nw) {
+        const int64_t r = g + lane;
+        uint32_t cm = 0;  // positions for which this lane's row is a candidate
+        if (r < r1) {
+            for (int m = 0; m < M; ++m) {
+                const double hi = __dadd_ru(static_cast<double>(a.scores[m * a.N + r]), row_bound(a, r, an[m]));
+                if (hi >= F[m]) cm |= 1u << m;
+            }
+        }
+        uint32_t rows = __ballot_sync(0xffffffffu, cm != 0);
+        while (rows) {
+            const int l = __ffs(static_cast<int>(rows)) - 1;
+            rows &= rows - 1;
+            const int64_t rr = g + l;
+            const uint32_t pm = __shfl_sync(0xffffffffu, cm, l);
+            for (int64_t b = lane; b < a.KB; b += 32) {
+                const uint16_t *blk = reinterpret_cast<const uint16_t *>(a.w8 + (rr * a.KB + b) * 34);
+                const double dw = static_cast<double>(__half2float(__ushort_as_half(blk[0])));
+                int wv[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    wv[j] = static_cast<int>(static_cast<uint32_t>(blk[1 + 2 * j]) |
+                                             (static_cast<uint32_t>(blk[2 + 2 * j]) << 16));
+                for (int m = 0; m < M; ++m) {
+                    if (!((pm >> m) & 1u)) continue;
+                    const int4 *qa = reinterpret_cast<const int4 *>(a.q + m * K + b * 32);
+                    const int4 q0 = qa[0], q1 = qa[1];
+                    int dot = dp4a(wv[0], q0.x, 0);
+                    dot = dp4a(wv[1], q0.y, dot);
+                    dot = dp4a(wv[2], q0.z, dot);
+                    dot = dp4a(wv[3], q0.w, dot);
+                    dot = dp4a(wv[4], q1.x, dot);
+                    dot = dp4a(wv[5], q1.y, dot);
+                    dot = dp4a(wv[6], q1.z, dot);
+                    dot = dp4a(wv[7], q1.w, dot);
+                    // (d_w d_a) is exact in fp64; one rounding for the product with the dot
+                    p[b * M + m] = dw * static_cast<double>(a.sc[m * a.KB + b]) * static_cast<double>(dot);
+                }
+            }
+            __syncwarp();
+            if (lane < M && ((pm >> lane) & 1u)) {
+                double acc = 0.0;
+                for (int64_t b = 0; b < a.KB; ++b) acc += p[b * M + lane];  // block order
+                ++cnt;
+                if (acc > bv || (acc == bv && rr < bi)) {
+                    bv = acc;
+                    bi = static_cast<int32_t>(rr);
+                }
+            }
+            __syncwarp();
+        }
+    }
+    if (lane < M) wb[warp][lane] = SlBest{bv, bi, cnt};
+    __syncthreads();
+    if (static_cast<int>(threadIdx.x) < M) {
+        SlBest best{-INFINITY, -1, 0};
+        for (int w = 0; w < nw; ++w) {
+            const SlBest x = wb[w][threadIdx.x];
+            best.cnt += x.cnt;
+            if (x.idx >= 0 && (best.idx < 0 || x.v > best.v || (x.v == best.v && x.idx < best.idx))) {
+                best.v = x.v;
+                best.idx = x.idx;
+            }
+        }
+        a.best_part[blockIdx.x * SL_MAXM + threadIdx.x] = best;
+    }
+}
+
+// the argmax over the CTAs' bests (lowest index among equal maxima) and the candidate counts
+__global__ void __launch_bounds__(32) shortlist_fold_kernel(const ShortlistArgs a) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int m = static_cast<int>(threadIdx.x);
+    if (m >= a.M) return;
+    SlBest best{-INFINITY, -1, 0};
+    for (int c = 0; c < a.G; ++c) {
+        const SlBest x = a.best_part[c * SL_MAXM + m];
+        best.cnt += x.cnt;
+        if (x.idx >= 0 && (best.idx < 0 || x.v > best.v || (x.v == best.v && x.idx < best.idx))) {
+            best.v = x.v;
+            best.idx = x.idx;
+        }
+    }
+    // with finite inputs the row of the exact maximum is always a candidate
+    if (best.idx < 0) set_status(a.status, SD_EDEVICE);
+    a.argmax[m] = best.idx;
+    if (a.n_cand) a.n_cand[m] = best.cnt;
+}
+
+struct SlLayout {
+    size_t mm, scores, an, floor_part, best_part, total;
+    int G;
+    int64_t rows_per_cta;
+};
+
+static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+static bool sl_layout(int64_t vocab, int64_t hidden, SlLayout &L) {
+    if (vocab < 1 || vocab > (int64_t(1) << 31) - 1 || hidden <= 0 || hidden % 32) return false;
+    const size_t mm = sd_qmatmul_workspace_bytes(SD_Q4_32, vocab, hidden, SD_EPI_NONE);
+    if (mm == 0) return false;
+    L.G = num_sms();
+    if (L.G < 1) return false;
+    L.rows_per_cta = ((vocab + L.G - 1) / L.G + 31) / 32 * 32;
+    L.mm = 0;
+    L.scores = align256(mm);
+    L.an = align256(L.scores + sizeof(float) * SL_MAXM * static_cast<size_t>(vocab));
+    L.floor_part = align256(L.an + sizeof(double) * SL_MAXM);
+    L.best_part = align256(L.floor_part + sizeof(double) * SL_MAXM * L.G);
+    L.total = align256(L.best_part + sizeof(SlBest) * SL_MAXM * L.G);
+    return true;
+}
+
+}  // namespace sdv
+
+using namespace sdv;
+
+extern "C" {
+
+sd_status sd_shortlist_build(const void *head_blocks, int64_t vocab, int64_t hidden, void *copy_blocks, float *bound,
+                             float *wnorm, sd_stream_t stream) {
+    if (!head_blocks || !copy_blocks || !bound || !wnorm) return SD_EINVAL;
+    if (!aligned(head_blocks, 16) || !aligned(copy_blocks, 16) || !aligned(bound, 4) || !aligned(wnorm, 4))
+        return SD_EINVAL;
+    if (vocab < 1 || vocab > (int64_t(1) << 31) - 1 || hidden <= 0 || hidden % 32) return SD_EINVAL;
+    const int sms = num_sms();
+    if (sms < 1) return SD_ECUDA;
+    const int64_t need = (vocab + SL_WARPS - 1) / SL_WARPS;
+    const int grid = static_cast<int>(need < int64_t(sms) * 8 ? need : int64_t(sms) * 8);
+    return launch(shortlist_build_kernel, dim3(grid), dim3(SL_THREADS), 0, reinterpret_cast<cudaStream_t>(stream),
+                  static_cast<const uint8_t *>(head_blocks), vocab, hidden / 32, static_cast<uint8_t *>(copy_blocks),
+                  bound, wnorm) == cudaSuccess
+               ? SD_OK
+               : SD_ECUDA;
+}
+
+size_t sd_shortlist_workspace_bytes(int64_t vocab, int64_t hidden) {
+    SlLayout L;
+    return sl_layout(vocab, hidden, L) ? L.total : 0;
+}
+
+sd_status sd_head_shortlist(const void *copy_w, const float *bound, const float *wnorm, const void *head_blocks,
+                            int64_t vocab, int64_t hidden, const int8_t *q, const float *scales, int32_t M,
+                            int32_t *argmax, int32_t *n_cand, void *workspace, size_t ws_bytes, sd_stream_t stream) {
+    if (M < 1) return SD_EINVAL;
+    if (M > SL_MAXM) return SD_EUNSUPPORTED;
+    if (!copy_w || !bound || !wnorm || !head_blocks || !q || !scales || !argmax || !workspace) return SD_EINVAL;
+    if (!aligned(copy_w, 16) || !aligned(head_blocks, 16) || !aligned(q, 16) || !aligned(scales, 4) ||
+        !aligned(bound, 4) || !aligned(wnorm, 4) || !aligned(argmax, 4) || (n_cand && !aligned(n_cand, 4)) ||
+        !aligned(workspace, 256))
+        return SD_EINVAL;
+    SlLayout L;
+    if (!sl_layout(vocab, hidden, L)) return SD_EINVAL;
+    if (ws_bytes < L.total) return SD_EINVAL;
+    const int64_t KB = hidden / 32;
+    // the exact kernel keeps one row's block products per warp in shared memory
+    const size_t per_warp = sizeof(double) * static_cast<size_t>(KB) * static_cast<size_t>(M);
+    int nw = static_cast<int>(SL_EXACT_SMEM_CAP / per_warp);
+    if (nw > SL_WARPS) nw = SL_WARPS;
+    if (nw < 1) return SD_EUNSUPPORTED;
+    const size_t smem = per_warp * nw;
+    int *st = status_ptr();
+    if (!st) return SD_ECUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    float *scores = reinterpret_cast<float *>(ws + L.scores);
+    // copy scores of every row: the multi-position matmul over the 4-bit copy
+    const sd_status rc = sd_qmatmul_multipos(SD_Q4_32, copy_w, vocab, hidden, q, scales, M, scores, nullptr,
+                                             SD_EPI_NONE, 0, nullptr, nullptr, ws + L.mm, L.scores, stream);
+    if (rc != SD_OK) return rc;
+    ShortlistArgs a = {};
+    a.scores = scores;
+    a.bound = bound;
+    a.wnorm = wnorm;
+    a.w8 = static_cast<const uint8_t *>(head_blocks);
+    a.q = q;
+    a.sc = scales;
+    a.N = vocab;
+    a.KB = KB;
+    a.M = M;
+    a.G = L.G;
+    a.rows_per_cta = L.rows_per_cta;
+    // fp32 copy score: at most KB + 64 rounding steps on any term's path, each <= 2^-24 relative,
+    // taken twice over; the fp64 exact score's rounding is far below it
+    a.gamma = static_cast<double>(KB + 64) * 0x1p-23;
+    a.an = reinterpret_cast<double *>(ws + L.an);
+    a.floor_part = reinterpret_cast<double *>(ws + L.floor_part);
+    a.best_part = reinterpret_cast<SlBest *>(ws + L.best_part);
+    a.argmax = argmax;
+    a.n_cand = n_cand;
+    a.status = st;
+    if (launch(shortlist_floor_kernel, dim3(L.G), dim3(SL_THREADS), 0, s, a) != cudaSuccess) return SD_ECUDA;
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(shortlist_exact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+        return SD_ECUDA;
+    if (launch(shortlist_exact_kernel, dim3(L.G), dim3(32 * nw), smem, s, a) != cudaSuccess) return SD_ECUDA;
+    return launch(shortlist_fold_kernel, dim3(1), dim3(32), 0, s, a) == cudaSuccess ? SD_OK : SD_ECUDA;
+}
+
+}  // extern "C"

@@ -85,6 +85,14 @@ def test_argument_checks_reject_without_launching(L):
     # rmsnorm: ldx < K
     assert L.sd_rmsnorm_quant_acts(p, 16, p, ctypes.c_float(1e-6), 5, 32, p, p, None) == 1
     assert L.sd_debug_wait_timeout(0, None) == 1
+    # shortlist: misaligned head, hidden % 32, M out of range, missing argmax
+    assert L.sd_shortlist_build(mis, 4096, 1024, p, p, p, None) == 1
+    assert L.sd_shortlist_build(p, 4096, 1000, p, p, p, None) == 1
+    assert L.sd_shortlist_build(p, 0, 1024, p, p, p, None) == 1
+    assert L.sd_head_shortlist(p, p, p, p, 4096, 1024, p, p, 17, p, None, p, 1 << 24, None) == 2
+    assert L.sd_head_shortlist(p, p, p, p, 4096, 1024, p, p, 0, p, None, p, 1 << 24, None) == 1
+    assert L.sd_head_shortlist(p, p, p, mis, 4096, 1024, p, p, 5, p, None, p, 1 << 24, None) == 1
+    assert L.sd_head_shortlist(p, p, p, p, 4096, 1024, p, p, 5, None, None, p, 1 << 24, None) == 1
 
 
 def test_pass_structs_match_the_header(tmp_path):
