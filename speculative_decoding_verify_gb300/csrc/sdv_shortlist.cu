@@ -13,10 +13,11 @@
 // (Cauchy-Schwarz for the copy's error; gamma covers the fp32 rounding of the copy score, whose
 // terms add up to at most ||w4_r|| ||a|| <= (W_r + E_r) A, and the fp64 rounding of the exact
 // score).  The floor is F = max_r (s_r - B_r) and row r is a candidate iff s_r + B_r >= F; every
-// bound operation rounds towards the safe side, so the row of the exact maximum is always a
-// candidate.  Exact scores are sums over the row's 32-blocks, in block order, of
-// (d_w d_a) * dot in fp64 -- the same arithmetic as the oracle's definition, so the argmax (lowest
-// index among equal maxima) is the exact one bit for bit.
+// bound operation is an fp32 operation rounded towards the safe side (A, B_r and s_r + B_r up,
+// s_r - B_r down), so the row of the exact maximum is always a candidate.  Exact scores are sums
+// over the row's 32-blocks, in block order, of (d_w d_a) * dot in fp64 -- the same arithmetic as
+// the oracle's definition, so the argmax (lowest index among equal maxima) is the exact one bit
+// for bit.
 #include "sdv_common.cuh"
 
 namespace sdv {
@@ -43,10 +44,10 @@ struct ShortlistArgs {
     int32_t M;
     int32_t G;              // CTAs of the floor and exact kernels
     int64_t rows_per_cta;   // multiple of 32
-    double gamma;
-    double *an;             // [SL_MAXM] activation norms (rounded up), written by the floor kernel
-    double *floor_part;     // [G][SL_MAXM]
-    SlBest *best_part;      // [G][SL_MAXM]
+    float gamma;
+    float *an;              // [SL_MAXM] activation norms (rounded up), written by the floor kernel
+    float *floor_part;      // [SL_MAXM][G]
+    SlBest *best_part;      // [SL_MAXM][G]
     int32_t *argmax;        // [M]
     int32_t *n_cand;        // [M] or nullptr
     int *status;
@@ -124,74 +125,98 @@ __global__ void __launch_bounds__(SL_THREADS) shortlist_build_kernel(const uint8
 // verify time
 // ---------------------------------------------------------------------------
 
-// B_r for one position, rounded up
-__device__ __forceinline__ double row_bound(const ShortlistArgs &a, int64_t r, double an) {
-    const double E = static_cast<double>(a.bound[r]);
-    const double W = static_cast<double>(a.wnorm[r]);
-    const double c = __dadd_ru(E, __dmul_ru(a.gamma, __dadd_ru(__dmul_ru(2.0, W), E)));
-    return __dmul_ru(c, an);
+// C_r = E_r + gamma (2 W_r + E_r), rounded up; B_r = C_r A for a position with norm A
+__device__ __forceinline__ float row_coef(const ShortlistArgs &a, int64_t r) {
+    const float E = a.bound[r], W = a.wnorm[r];
+    return __fadd_ru(E, __fmul_ru(a.gamma, __fadd_ru(__fmul_ru(2.0f, W), E)));
 }
 
-__device__ __forceinline__ double block_max(double v, double *red) {
+__device__ __forceinline__ float warp_sum_ru_f(float v) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmax(v, __shfl_xor_sync(0xffffffffu, v, o));
+    for (int o = 16; o > 0; o >>= 1) v = __fadd_ru(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_max_f(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// ||a_m||_2 of every position, rounded up: per block d_a^2 times the exact integer sum of squared
+// codes, summed with upward rounding (the same value in every CTA).  One warp per position.
+__device__ void act_norms(const ShortlistArgs &a, float *an) {
     const int warp = static_cast<int>(threadIdx.x) / 32, lane = static_cast<int>(threadIdx.x) & 31;
-    __syncthreads();
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    double m = red[0];
-#pragma unroll
-    for (int w = 1; w < SL_WARPS; ++w) m = fmax(m, red[w]);
-    return m;
-}
-
-// ||a_m||_2 of every position, rounded up (the same value in every CTA)
-__device__ void act_norms(const ShortlistArgs &a, double *an, double *red) {
     const int64_t K = a.KB * 32;
-    const int warp = static_cast<int>(threadIdx.x) / 32, lane = static_cast<int>(threadIdx.x) & 31;
-    for (int m = 0; m < a.M; ++m) {
-        double t = 0.0;
-        for (int64_t i = threadIdx.x; i < K; i += SL_THREADS) {
-            // fp32 scale x int8 code: exact in fp64
-            const double v = static_cast<double>(a.sc[m * a.KB + i / 32]) * static_cast<double>(a.q[m * K + i]);
-            t = __dadd_ru(t, __dmul_ru(v, v));
+    for (int m = warp; m < a.M; m += SL_WARPS) {
+        float t = 0.0f;
+        for (int64_t b = lane; b < a.KB; b += 32) {
+            const int4 *qa = reinterpret_cast<const int4 *>(a.q + m * K + b * 32);
+            const int4 q0 = qa[0], q1 = qa[1];
+            int s2 = dp4a(q0.x, q0.x, 0);
+            s2 = dp4a(q0.y, q0.y, s2);
+            s2 = dp4a(q0.z, q0.z, s2);
+            s2 = dp4a(q0.w, q0.w, s2);
+            s2 = dp4a(q1.x, q1.x, s2);
+            s2 = dp4a(q1.y, q1.y, s2);
+            s2 = dp4a(q1.z, q1.z, s2);
+            s2 = dp4a(q1.w, q1.w, s2);  // <= 32 * 127^2: exact in fp32
+            const float d = a.sc[m * a.KB + b];
+            t = __fadd_ru(t, __fmul_ru(__fmul_ru(d, d), static_cast<float>(s2)));
         }
-        t = warp_sum_ru(t);
-        __syncthreads();
-        if (lane == 0) red[warp] = t;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            double s = 0.0;
-            for (int w = 0; w < SL_WARPS; ++w) s = __dadd_ru(s, red[w]);
-            an[m] = __dsqrt_ru(s);
-        }
+        t = warp_sum_ru_f(t);
+        if (lane == 0) an[m] = __fsqrt_ru(t);
     }
     __syncthreads();
 }
 
 // the floor: per CTA, max over its rows of s_r - B_r (rounded down), per position
 __global__ void __launch_bounds__(SL_THREADS) shortlist_floor_kernel(const ShortlistArgs a) {
-    __shared__ double an[SL_MAXM];
-    __shared__ double red[SL_WARPS];
+    __shared__ float an[SL_MAXM];
+    __shared__ float red[SL_MAXM][SL_WARPS];
     pdl_wait();
     pdl_launch_dependents();
-    act_norms(a, an, red);
+    act_norms(a, an);
     if (blockIdx.x == 0 && static_cast<int>(threadIdx.x) < a.M) a.an[threadIdx.x] = an[threadIdx.x];
+    const int warp = static_cast<int>(threadIdx.x) / 32, lane = static_cast<int>(threadIdx.x) & 31;
     const int64_t r0 = static_cast<int64_t>(blockIdx.x) * a.rows_per_cta;
     const int64_t r1 = min(a.N, r0 + a.rows_per_cta);
-    for (int m = 0; m < a.M; ++m) {
-        double mx = -INFINITY;
-        for (int64_t r = r0 + threadIdx.x; r < r1; r += SL_THREADS)
-            mx = fmax(mx, __dsub_rd(static_cast<double>(a.scores[m * a.N + r]), row_bound(a, r, an[m])));
-        mx = block_max(mx, red);
-        if (threadIdx.x == 0) a.floor_part[blockIdx.x * SL_MAXM + m] = mx;
+    float mx[SL_MAXM];
+#pragma unroll
+    for (int m = 0; m < SL_MAXM; ++m) mx[m] = -INFINITY;
+    for (int64_t r = r0 + threadIdx.x; r < r1; r += SL_THREADS) {
+        const float c = row_coef(a, r);
+#pragma unroll
+        for (int m = 0; m < SL_MAXM; ++m)
+            if (m < a.M) mx[m] = fmaxf(mx[m], __fsub_rd(a.scores[m * a.N + r], __fmul_ru(c, an[m])));
+    }
+#pragma unroll
+    for (int m = 0; m < SL_MAXM; ++m) {
+        if (m >= a.M) break;
+        const float v = warp_max_f(mx[m]);
+        if (lane == 0) red[m][warp] = v;
+    }
+    __syncthreads();
+    if (static_cast<int>(threadIdx.x) < a.M) {
+        float v = red[threadIdx.x][0];
+#pragma unroll
+        for (int w = 1; w < SL_WARPS; ++w) v = fmaxf(v, red[threadIdx.x][w]);
+        a.floor_part[threadIdx.x * a.G + blockIdx.x] = v;
+    }
+}
+
+// (value, index) of the better of two: larger value, lower index among equal values; idx < 0 = none
+__device__ __forceinline__ void better(double &v, int32_t &i, double v2, int32_t i2) {
+    if (i2 >= 0 && (i < 0 || v2 > v || (v2 == v && i2 < i))) {
+        v = v2;
+        i = i2;
     }
 }
 
 // candidates and their exact scores; per CTA the best row per position and the candidate count
 __global__ void __launch_bounds__(SL_THREADS) shortlist_exact_kernel(const ShortlistArgs a) {
     extern __shared__ double prod[];  // [warps][KB][M] block products of the row in hand
-    __shared__ double F[SL_MAXM], an[SL_MAXM];
+    __shared__ float F[SL_MAXM], an[SL_MAXM];
     __shared__ SlBest wb[SL_WARPS][SL_MAXM];
     pdl_wait();
     pdl_launch_dependents();
@@ -199,11 +224,14 @@ __global__ void __launch_bounds__(SL_THREADS) shortlist_exact_kernel(const Short
     const int warp = static_cast<int>(threadIdx.x) / 32, lane = static_cast<int>(threadIdx.x) & 31;
     const int M = a.M;
     const int64_t K = a.KB * 32;
-    if (static_cast<int>(threadIdx.x) < M) {
-        double f = -INFINITY;
-        for (int c = 0; c < a.G; ++c) f = fmax(f, a.floor_part[c * SL_MAXM + threadIdx.x]);
-        F[threadIdx.x] = f;
-        an[threadIdx.x] = a.an[threadIdx.x];
+    for (int m = warp; m < M; m += nw) {  // the floor of position m: one warp over the CTAs' maxima
+        float f = -INFINITY;
+        for (int c = lane; c < a.G; c += 32) f = fmaxf(f, a.floor_part[m * a.G + c]);
+        f = warp_max_f(f);
+        if (lane == 0) {
+            F[m] = f;
+            an[m] = a.an[m];
+        }
     }
     __syncthreads();
     double bv = -INFINITY;  // lane m keeps position m's best
@@ -215,10 +243,9 @@ __global__ void __launch_bounds__(SL_THREADS) shortlist_exact_kernel(const Short
         const int64_t r = g + lane;
         uint32_t cm = 0;  // positions for which this lane's row is a candidate
         if (r < r1) {
-            for (int m = 0; m < M; ++m) {
-                const double hi = __dadd_ru(static_cast<double>(a.scores[m * a.N + r]), row_bound(a, r, an[m]));
-                if (hi >= F[m]) cm |= 1u << m;
-            }
+            const float c = row_coef(a, r);
+            for (int m = 0; m < M; ++m)
+                if (__fadd_ru(a.scores[m * a.N + r], __fmul_ru(c, an[m])) >= F[m]) cm |= 1u << m;
         }
         uint32_t rows = __ballot_sync(0xffffffffu, cm != 0);
         while (rows) {
@@ -255,10 +282,7 @@ __global__ void __launch_bounds__(SL_THREADS) shortlist_exact_kernel(const Short
                 double acc = 0.0;
                 for (int64_t b = 0; b < a.KB; ++b) acc += p[b * M + lane];  // block order
                 ++cnt;
-                if (acc > bv || (acc == bv && rr < bi)) {
-                    bv = acc;
-                    bi = static_cast<int32_t>(rr);
-                }
+                better(bv, bi, acc, static_cast<int32_t>(rr));
             }
             __syncwarp();
         }
@@ -270,34 +294,38 @@ __global__ void __launch_bounds__(SL_THREADS) shortlist_exact_kernel(const Short
         for (int w = 0; w < nw; ++w) {
             const SlBest x = wb[w][threadIdx.x];
             best.cnt += x.cnt;
-            if (x.idx >= 0 && (best.idx < 0 || x.v > best.v || (x.v == best.v && x.idx < best.idx))) {
-                best.v = x.v;
-                best.idx = x.idx;
-            }
+            better(best.v, best.idx, x.v, x.idx);
         }
-        a.best_part[blockIdx.x * SL_MAXM + threadIdx.x] = best;
+        a.best_part[threadIdx.x * a.G + blockIdx.x] = best;
     }
 }
 
-// the argmax over the CTAs' bests (lowest index among equal maxima) and the candidate counts
-__global__ void __launch_bounds__(32) shortlist_fold_kernel(const ShortlistArgs a) {
+// the argmax over the CTAs' bests (lowest index among equal maxima) and the candidate counts:
+// one warp per position, lanes over the CTAs
+__global__ void __launch_bounds__(32 * SL_MAXM) shortlist_fold_kernel(const ShortlistArgs a) {
     pdl_wait();
     pdl_launch_dependents();
-    const int m = static_cast<int>(threadIdx.x);
+    const int m = static_cast<int>(threadIdx.x) / 32, lane = static_cast<int>(threadIdx.x) & 31;
     if (m >= a.M) return;
-    SlBest best{-INFINITY, -1, 0};
-    for (int c = 0; c < a.G; ++c) {
-        const SlBest x = a.best_part[c * SL_MAXM + m];
-        best.cnt += x.cnt;
-        if (x.idx >= 0 && (best.idx < 0 || x.v > best.v || (x.v == best.v && x.idx < best.idx))) {
-            best.v = x.v;
-            best.idx = x.idx;
-        }
+    double v = -INFINITY;
+    int32_t i = -1, cnt = 0;
+    for (int c = lane; c < a.G; c += 32) {
+        const SlBest x = a.best_part[m * a.G + c];
+        cnt += x.cnt;
+        better(v, i, x.v, x.idx);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const double v2 = __shfl_xor_sync(0xffffffffu, v, o);
+        const int32_t i2 = __shfl_xor_sync(0xffffffffu, i, o);
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+        better(v, i, v2, i2);
+    }
+    if (lane != 0) return;
     // with finite inputs the row of the exact maximum is always a candidate
-    if (best.idx < 0) set_status(a.status, SD_EDEVICE);
-    a.argmax[m] = best.idx;
-    if (a.n_cand) a.n_cand[m] = best.cnt;
+    if (i < 0) set_status(a.status, SD_EDEVICE);
+    a.argmax[m] = i;
+    if (a.n_cand) a.n_cand[m] = cnt;
 }
 
 struct SlLayout {
@@ -318,8 +346,8 @@ static bool sl_layout(int64_t vocab, int64_t hidden, SlLayout &L) {
     L.mm = 0;
     L.scores = align256(mm);
     L.an = align256(L.scores + sizeof(float) * SL_MAXM * static_cast<size_t>(vocab));
-    L.floor_part = align256(L.an + sizeof(double) * SL_MAXM);
-    L.best_part = align256(L.floor_part + sizeof(double) * SL_MAXM * L.G);
+    L.floor_part = align256(L.an + sizeof(float) * SL_MAXM);
+    L.best_part = align256(L.floor_part + sizeof(float) * SL_MAXM * L.G);
     L.total = align256(L.best_part + sizeof(SlBest) * SL_MAXM * L.G);
     return true;
 }
@@ -395,9 +423,9 @@ sd_status sd_head_shortlist(const void *copy_w, const float *bound, const float 
     a.rows_per_cta = L.rows_per_cta;
     // fp32 copy score: at most KB + 64 rounding steps on any term's path, each <= 2^-24 relative,
     // taken twice over; the fp64 exact score's rounding is far below it
-    a.gamma = static_cast<double>(KB + 64) * 0x1p-23;
-    a.an = reinterpret_cast<double *>(ws + L.an);
-    a.floor_part = reinterpret_cast<double *>(ws + L.floor_part);
+    a.gamma = static_cast<float>(KB + 64) * 0x1p-23f;
+    a.an = reinterpret_cast<float *>(ws + L.an);
+    a.floor_part = reinterpret_cast<float *>(ws + L.floor_part);
     a.best_part = reinterpret_cast<SlBest *>(ws + L.best_part);
     a.argmax = argmax;
     a.n_cand = n_cand;
@@ -408,7 +436,7 @@ sd_status sd_head_shortlist(const void *copy_w, const float *bound, const float 
                              static_cast<int>(smem)) != cudaSuccess)
         return SD_ECUDA;
     if (launch(shortlist_exact_kernel, dim3(L.G), dim3(32 * nw), smem, s, a) != cudaSuccess) return SD_ECUDA;
-    return launch(shortlist_fold_kernel, dim3(1), dim3(32), 0, s, a) == cudaSuccess ? SD_OK : SD_ECUDA;
+    return launch(shortlist_fold_kernel, dim3(1), dim3(32 * M), 0, s, a) == cudaSuccess ? SD_OK : SD_ECUDA;
 }
 
 }  // extern "C"
