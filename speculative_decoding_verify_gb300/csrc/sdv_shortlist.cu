@@ -26,6 +26,9 @@ constexpr int SL_THREADS = 256;
 constexpr int SL_WARPS = SL_THREADS / 32;
 constexpr int SL_MAXM = 16;
 constexpr size_t SL_EXACT_SMEM_CAP = 96 * 1024;  // per CTA: two CTAs of the exact kernel per SM
+// CTAs per SM of the floor and exact kernels: about one row per thread on a 152k vocabulary, so
+// every thread issues its loads at once instead of walking a slice
+constexpr int SL_CTAS_PER_SM = 4;
 
 struct SlBest {
     double v;     // best exact score (-inf: none)
@@ -171,7 +174,7 @@ __device__ void act_norms(const ShortlistArgs &a, float *an) {
 }
 
 // the floor: per CTA, max over its rows of s_r - B_r (rounded down), per position
-__global__ void __launch_bounds__(SL_THREADS) shortlist_floor_kernel(const ShortlistArgs a) {
+__global__ void __launch_bounds__(SL_THREADS, SL_CTAS_PER_SM) shortlist_floor_kernel(const ShortlistArgs a) {
     __shared__ float an[SL_MAXM];
     __shared__ float red[SL_MAXM][SL_WARPS];
     pdl_wait();
@@ -340,8 +343,9 @@ static bool sl_layout(int64_t vocab, int64_t hidden, SlLayout &L) {
     if (vocab < 1 || vocab > (int64_t(1) << 31) - 1 || hidden <= 0 || hidden % 32) return false;
     const size_t mm = sd_qmatmul_workspace_bytes(SD_Q4_32, vocab, hidden, SD_EPI_NONE);
     if (mm == 0) return false;
-    L.G = num_sms();
-    if (L.G < 1) return false;
+    const int sms = num_sms();
+    if (sms < 1) return false;
+    L.G = sms * SL_CTAS_PER_SM;
     L.rows_per_cta = ((vocab + L.G - 1) / L.G + 31) / 32 * 32;
     L.mm = 0;
     L.scores = align256(mm);
