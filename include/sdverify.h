@@ -223,7 +223,8 @@ sd_status sd_head_logits(const void *w, int64_t vocab, int64_t hidden, const int
  * Device-side: a position with no candidate (non-finite inputs only) records
  * SD_EDEVICE in the status word and gets argmax -1.  workspace: ws_bytes >=
  * sd_shortlist_workspace_bytes(vocab, hidden), zero-filled by the caller once
- * (it holds the copy matmul's counters, which every call returns to zero).
+ * (it holds counters, the copy matmul's among them, that every call returns
+ * to zero).
  * Errors: SD_EINVAL on null/misaligned pointers or bad sizes; SD_EUNSUPPORTED
  * for M > 16 or hidden/32 * M > 12288.
  */

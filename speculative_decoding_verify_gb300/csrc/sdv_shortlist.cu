@@ -50,7 +50,9 @@ struct ShortlistArgs {
     float gamma;
     float *an;              // [SL_MAXM] activation norms (rounded up), written by the floor kernel
     float *floor_part;      // [SL_MAXM][G]
+    float *F;               // [SL_MAXM] floors, written by the floor kernel's last CTA
     SlBest *best_part;      // [SL_MAXM][G]
+    uint32_t *ticket;       // [2] CTAs done (floor, exact); zero between calls
     int32_t *argmax;        // [M]
     int32_t *n_cand;        // [M] or nullptr
     int *status;
@@ -173,10 +175,29 @@ __device__ void act_norms(const ShortlistArgs &a, float *an) {
     __syncthreads();
 }
 
-// the floor: per CTA, max over its rows of s_r - B_r (rounded down), per position
+// Whether this CTA is the grid's last to finish its part.  Every thread fences its stores of
+// partial results before the CTA takes its ticket; the last CTA fences again before reading the
+// others' partials and puts the counter back to zero for the next call.  Nothing waits.
+__device__ __forceinline__ bool last_cta(uint32_t *ticket, int *flag) {
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const bool last = atomicAdd(ticket, 1u) == gridDim.x - 1;
+        if (last) atomicExch(ticket, 0u);
+        *flag = last ? 1 : 0;
+    }
+    __syncthreads();
+    const bool last = *flag != 0;
+    if (last) __threadfence();
+    return last;
+}
+
+// the floor: per CTA, max over its rows of s_r - B_r (rounded down), per position; the last CTA
+// reduces the CTAs' maxima to the floor of each position
 __global__ void __launch_bounds__(SL_THREADS, SL_CTAS_PER_SM) shortlist_floor_kernel(const ShortlistArgs a) {
     __shared__ float an[SL_MAXM];
     __shared__ float red[SL_MAXM][SL_WARPS];
+    __shared__ int is_last;
     pdl_wait();
     pdl_launch_dependents();
     act_norms(a, an);
@@ -206,6 +227,13 @@ __global__ void __launch_bounds__(SL_THREADS, SL_CTAS_PER_SM) shortlist_floor_ke
         for (int w = 1; w < SL_WARPS; ++w) v = fmaxf(v, red[threadIdx.x][w]);
         a.floor_part[threadIdx.x * a.G + blockIdx.x] = v;
     }
+    if (!last_cta(a.ticket, &is_last)) return;
+    for (int m = warp; m < a.M; m += SL_WARPS) {
+        float f = -INFINITY;
+        for (int c = lane; c < a.G; c += 32) f = fmaxf(f, __ldcg(a.floor_part + m * a.G + c));
+        f = warp_max_f(f);
+        if (lane == 0) a.F[m] = f;
+    }
 }
 
 // (value, index) of the better of two: larger value, lower index among equal values; idx < 0 = none
@@ -221,20 +249,16 @@ __global__ void __launch_bounds__(SL_THREADS) shortlist_exact_kernel(const Short
     extern __shared__ double prod[];  // [warps][KB][M] block products of the row in hand
     __shared__ float F[SL_MAXM], an[SL_MAXM];
     __shared__ SlBest wb[SL_WARPS][SL_MAXM];
+    __shared__ int is_last;
     pdl_wait();
     pdl_launch_dependents();
     const int nw = static_cast<int>(blockDim.x) / 32;
     const int warp = static_cast<int>(threadIdx.x) / 32, lane = static_cast<int>(threadIdx.x) & 31;
     const int M = a.M;
     const int64_t K = a.KB * 32;
-    for (int m = warp; m < M; m += nw) {  // the floor of position m: one warp over the CTAs' maxima
-        float f = -INFINITY;
-        for (int c = lane; c < a.G; c += 32) f = fmaxf(f, a.floor_part[m * a.G + c]);
-        f = warp_max_f(f);
-        if (lane == 0) {
-            F[m] = f;
-            an[m] = a.an[m];
-        }
+    if (static_cast<int>(threadIdx.x) < M) {
+        F[threadIdx.x] = a.F[threadIdx.x];
+        an[threadIdx.x] = a.an[threadIdx.x];
     }
     __syncthreads();
     double bv = -INFINITY;  // lane m keeps position m's best
@@ -301,38 +325,36 @@ __global__ void __launch_bounds__(SL_THREADS) shortlist_exact_kernel(const Short
         }
         a.best_part[threadIdx.x * a.G + blockIdx.x] = best;
     }
-}
-
-// the argmax over the CTAs' bests (lowest index among equal maxima) and the candidate counts:
-// one warp per position, lanes over the CTAs
-__global__ void __launch_bounds__(32 * SL_MAXM) shortlist_fold_kernel(const ShortlistArgs a) {
-    pdl_wait();
-    pdl_launch_dependents();
-    const int m = static_cast<int>(threadIdx.x) / 32, lane = static_cast<int>(threadIdx.x) & 31;
-    if (m >= a.M) return;
-    double v = -INFINITY;
-    int32_t i = -1, cnt = 0;
-    for (int c = lane; c < a.G; c += 32) {
-        const SlBest x = a.best_part[m * a.G + c];
-        cnt += x.cnt;
-        better(v, i, x.v, x.idx);
-    }
+    // the last CTA: the argmax over the CTAs' bests (lowest index among equal maxima) and the
+    // candidate counts, one warp per position
+    if (!last_cta(a.ticket + 1, &is_last)) return;
+    for (int m = warp; m < M; m += nw) {
+        double v = -INFINITY;
+        int32_t i = -1, n = 0;
+        for (int c = lane; c < a.G; c += 32) {
+            const SlBest *x = a.best_part + m * a.G + c;
+            const int2 ic = __ldcg(reinterpret_cast<const int2 *>(&x->idx));
+            n += ic.y;
+            better(v, i, __ldcg(&x->v), ic.x);
+        }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const double v2 = __shfl_xor_sync(0xffffffffu, v, o);
-        const int32_t i2 = __shfl_xor_sync(0xffffffffu, i, o);
-        cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-        better(v, i, v2, i2);
+        for (int o = 16; o > 0; o >>= 1) {
+            const double v2 = __shfl_xor_sync(0xffffffffu, v, o);
+            const int32_t i2 = __shfl_xor_sync(0xffffffffu, i, o);
+            n += __shfl_xor_sync(0xffffffffu, n, o);
+            better(v, i, v2, i2);
+        }
+        if (lane == 0) {
+            // with finite inputs the row of the exact maximum is always a candidate
+            if (i < 0) set_status(a.status, SD_EDEVICE);
+            a.argmax[m] = i;
+            if (a.n_cand) a.n_cand[m] = n;
+        }
     }
-    if (lane != 0) return;
-    // with finite inputs the row of the exact maximum is always a candidate
-    if (i < 0) set_status(a.status, SD_EDEVICE);
-    a.argmax[m] = i;
-    if (a.n_cand) a.n_cand[m] = cnt;
 }
 
 struct SlLayout {
-    size_t mm, scores, an, floor_part, best_part, total;
+    size_t mm, scores, an, F, ticket, floor_part, best_part, total;
     int G;
     int64_t rows_per_cta;
 };
@@ -350,7 +372,9 @@ static bool sl_layout(int64_t vocab, int64_t hidden, SlLayout &L) {
     L.mm = 0;
     L.scores = align256(mm);
     L.an = align256(L.scores + sizeof(float) * SL_MAXM * static_cast<size_t>(vocab));
-    L.floor_part = align256(L.an + sizeof(float) * SL_MAXM);
+    L.F = align256(L.an + sizeof(float) * SL_MAXM);
+    L.ticket = align256(L.F + sizeof(float) * SL_MAXM);
+    L.floor_part = align256(L.ticket + sizeof(uint32_t) * 2);
     L.best_part = align256(L.floor_part + sizeof(float) * SL_MAXM * L.G);
     L.total = align256(L.best_part + sizeof(SlBest) * SL_MAXM * L.G);
     return true;
@@ -430,7 +454,9 @@ sd_status sd_head_shortlist(const void *copy_w, const float *bound, const float 
     a.gamma = static_cast<float>(KB + 64) * 0x1p-23f;
     a.an = reinterpret_cast<float *>(ws + L.an);
     a.floor_part = reinterpret_cast<float *>(ws + L.floor_part);
+    a.F = reinterpret_cast<float *>(ws + L.F);
     a.best_part = reinterpret_cast<SlBest *>(ws + L.best_part);
+    a.ticket = reinterpret_cast<uint32_t *>(ws + L.ticket);
     a.argmax = argmax;
     a.n_cand = n_cand;
     a.status = st;
@@ -439,8 +465,7 @@ sd_status sd_head_shortlist(const void *copy_w, const float *bound, const float 
         cudaFuncSetAttribute(shortlist_exact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
         return SD_ECUDA;
-    if (launch(shortlist_exact_kernel, dim3(L.G), dim3(32 * nw), smem, s, a) != cudaSuccess) return SD_ECUDA;
-    return launch(shortlist_fold_kernel, dim3(1), dim3(32 * M), 0, s, a) == cudaSuccess ? SD_OK : SD_ECUDA;
+    return launch(shortlist_exact_kernel, dim3(L.G), dim3(32 * nw), smem, s, a) == cudaSuccess ? SD_OK : SD_ECUDA;
 }
 
 }  // extern "C"
