@@ -19,7 +19,14 @@ page passage cited in the C source:
   LLMs", and "How Kinetic is fast", section "Why the output does not change";
 * the same against a top-k / top-p filtered target (the sampling knobs of
   "Inside OpenJet Engine", API section; the filtering order is a reading);
-* Philox4x32-10: Salmon et al., SC'11.
+* Philox4x32-10: Salmon et al., SC'11;
+* the 4-bit shortlist copy and its exact argmax: "Inside OpenJet Engine",
+  section "Shortlist";
+* decode attention over the K+1 positions with a tree mask, the fp16 KV append
+  and the in-place commit of the accepted path: "Inside OpenJet Engine",
+  section "Cheap drafting, careful state management"; "How Kinetic is fast",
+  section "Where the guesses come from"; "Speculative Decoding with
+  Open-Weights Models", section "KV Cache Synchronization".
 
 Parity status: every function here is pinned by a ``-m "not gpu"`` test in
 ``tests/test_oracle_pins.py`` against something other than itself.  The
@@ -90,6 +97,10 @@ def _get():
                 "oracle_accept_sample_topk_u": ([_P, _I64, _I, _P, _P, _F, _I, _F, _P, _P, _P], _I),
                 "oracle_accept_sample_topk": ([_P, _I64, _I, _P, _P, _F, _I, _F, ctypes.c_uint64, _I64, _P], _I),
                 "oracle_shortlist_copy": ([_P, _I64, _I64, _P, _P, _P], None),
+                "oracle_f32_to_f16": ([_P, _I64, _P], None),
+                "oracle_kv_append": ([_P, _P, _I, _I, _I, _P, _P, _I64, _I64], None),
+                "oracle_attn_decode": ([_P, _P, _P, _I, _I, _I, _I, _I64, _I64, _P, _P], None),
+                "oracle_kv_commit": ([_P, _P, _I, _I, _I64, _I64, _P, _I], None),
                 "oracle_shortlist_argmax": ([_P, _P, _P, _I64, _I64, _P, _P, _I, _P, _P], None),
             }
             for name, (args, res) in sig.items():
@@ -331,6 +342,49 @@ def shortlist_argmax(q4_blocks, bound, q8_blocks, N: int, K: int, q, scales):
     nc = np.empty(M, dtype=np.int64)
     _get().oracle_shortlist_argmax(p4, pb, p8, N, K, pq, ps, M, am.ctypes.data, nc.ctypes.data)
     return am, nc
+
+
+def f32_to_f16(x) -> np.ndarray:
+    """fp32 -> fp16 bits (uint16), nearest even."""
+    x, px = _c(x, np.float32)
+    out = np.empty(x.shape, dtype=np.uint16)
+    _get().oracle_f32_to_f16(px, x.size, out.ctypes.data)
+    return out
+
+
+def kv_append(k_new, v_new, k_cache, v_cache, L: int):
+    """Write fp32 [M][H_kv][D] rows into slots [L, L+M) of the fp16-bit caches [H_kv][S_max][D] (in place)."""
+    k_new, pk = _c(k_new, np.float32)
+    v_new, pv = _c(v_new, np.float32)
+    M, H_kv, D = k_new.shape
+    assert k_cache.dtype == np.uint16 and k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    S_max = k_cache.shape[1]
+    assert L + M <= S_max
+    _get().oracle_kv_append(pk, pv, M, H_kv, D, k_cache.ctypes.data, v_cache.ctypes.data, S_max, L)
+
+
+def attn_decode(q, k_cache, v_cache, L: int, parent=None) -> np.ndarray:
+    """q fp32 [M][H][D]; caches fp16 bits [H_kv][S_max][D] with L committed + M new rows.  fp64 [M][H][D]."""
+    q, pq = _c(q, np.float32)
+    M, H, D = q.shape
+    k_cache, pk = _c(k_cache, np.uint16)
+    v_cache, pv = _c(v_cache, np.uint16)
+    H_kv, S_max, D2 = k_cache.shape
+    assert D2 == D and H % H_kv == 0 and L + M <= S_max
+    pp = None
+    if parent is not None:
+        parent, pp = _c(parent, np.int32)
+    out = np.empty((M, H, D), dtype=np.float64)
+    _get().oracle_attn_decode(pq, pk, pv, M, H, H_kv, D, S_max, L, pp, out.ctypes.data)
+    return out
+
+
+def kv_commit(k_cache, v_cache, L: int, path):
+    """Move the accepted path's rows to slots [L, L+n) (in place)."""
+    path, pp = _c(path, np.int32)
+    H_kv, S_max, D = k_cache.shape
+    assert k_cache.dtype == np.uint16 and k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    _get().oracle_kv_commit(k_cache.ctypes.data, v_cache.ctypes.data, H_kv, D, S_max, L, pp, path.size)
 
 
 def accept_sample_trials(logits, q_probs, drafts_per_trial, T: float, seed: int, base_pos: int):

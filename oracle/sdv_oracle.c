@@ -652,11 +652,13 @@ int oracle_accept_sample_topk(const float *logits, int64_t V, int K, const float
 /* taken over the candidates only.                                      */
 /* ------------------------------------------------------------------ */
 
-/* IEEE binary32 -> binary16, round to nearest even (finite, |x| < 65520) */
+/* IEEE binary32 -> binary16, round to nearest even; |x| >= 65520 gives infinity */
 static uint16_t f32_to_f16_rne_oracle(float x) {
-    uint16_t sign = x < 0.0f ? 0x8000u : 0u;
+    if (x != x) return 0x7E00u;
+    uint16_t sign = signbit(x) ? 0x8000u : 0u;
     double a = fabs((double)x);
     if (a == 0.0) return sign;
+    if (a >= 65520.0) return (uint16_t)(sign | 0x7C00u);
     int e;
     (void)frexp(a, &e);                 /* a = f 2^e, f in [0.5, 1): unit exponent e - 1 */
     int ue = e - 1;
@@ -758,4 +760,101 @@ void oracle_shortlist_argmax(const uint8_t *q4, const float *bound, const uint8_
         ncand[m] = nc;
     }
     free(s);
+}
+
+/* ------------------------------------------------------------------ */
+/* Decode attention over the K+1 verified positions ("Inside OpenJet    */
+/* Engine", section "Cheap drafting, careful state management": split-K */
+/* flash decoding of full-attention layers with fp16 K/V and fp32       */
+/* accumulation; "How Kinetic is fast", section "Where the guesses come */
+/* from": each row of a draft tree sees only its own path; "Speculative */
+/* Decoding with Open-Weights Models", section "KV Cache                */
+/* Synchronization": rejected                                           */
+/* entries are dropped in place).  Reading: the cache holds, per KV     */
+/* head, fp16 K and V rows [S_max][D]; the M new positions are appended */
+/* at slots L..L+M-1 (fp32 -> fp16, nearest even); query row (i, h)     */
+/* sees every committed slot and the new slot L+j iff j is i itself or  */
+/* an ancestor of i (chain: j <= i); query head h reads KV head         */
+/* h / (H / H_kv); out = sum_j softmax_j(q.k_j / sqrt(D)) v_j.  The     */
+/* oracle takes all of it in fp64 from the fp16 values, with no split.  */
+/* After acceptance the n entries of the accepted path move to slots    */
+/* L..L+n-1 (in path order) and the cache length becomes L+n.           */
+/* ------------------------------------------------------------------ */
+
+void oracle_f32_to_f16(const float *x, int64_t n, uint16_t *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = f32_to_f16_rne_oracle(x[i]);
+}
+
+/* k_new, v_new fp32 [M][H_kv][D] -> cache slots [L, L+M) of [H_kv][S_max][D] */
+void oracle_kv_append(const float *k_new, const float *v_new, int M, int H_kv, int D, uint16_t *k_cache,
+                      uint16_t *v_cache, int64_t S_max, int64_t L) {
+    for (int i = 0; i < M; ++i)
+        for (int h = 0; h < H_kv; ++h)
+            for (int d = 0; d < D; ++d) {
+                const int64_t src = ((int64_t)i * H_kv + h) * D + d;
+                const int64_t dst = ((int64_t)h * S_max + L + i) * D + d;
+                k_cache[dst] = f32_to_f16_rne_oracle(k_new[src]);
+                v_cache[dst] = f32_to_f16_rne_oracle(v_new[src]);
+            }
+}
+
+/* whether new position j is on the path of new position i (parent NULL: a chain) */
+static int on_path(const int32_t *parent, int i, int j) {
+    if (!parent) return j <= i;
+    for (int a = i; a >= 0; a = parent[a])
+        if (a == j) return 1;
+    return 0;
+}
+
+/* q fp32 [M][H][D]; caches fp16 bits [H_kv][S_max][D] holding L + M rows per head;
+   out fp64 [M][H][D] */
+void oracle_attn_decode(const float *q, const uint16_t *k_cache, const uint16_t *v_cache, int M, int H, int H_kv,
+                        int D, int64_t S_max, int64_t L, const int32_t *parent, double *out) {
+    const int g = H / H_kv;
+    const int64_t NK = L + M;
+#pragma omp parallel for schedule(static)
+    for (int r = 0; r < M * H; ++r) {
+        const int i = r / H, h = r % H, kh = h / g;
+        const float *qr = q + (int64_t)r * D;
+        double *o = out + (int64_t)r * D;
+        double *sc = (double *)malloc((size_t)NK * sizeof(double));
+        double mx = -INFINITY;
+        for (int64_t j = 0; j < NK; ++j) {
+            if (j >= L && !on_path(parent, i, (int)(j - L))) {
+                sc[j] = -INFINITY;
+                continue;
+            }
+            const uint16_t *kr = k_cache + ((int64_t)kh * S_max + j) * D;
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d) dot += (double)qr[d] * (double)oracle_f16_to_f32(kr[d]);
+            sc[j] = dot / sqrt((double)D);
+            if (sc[j] > mx) mx = sc[j];
+        }
+        double den = 0.0;
+        for (int d = 0; d < D; ++d) o[d] = 0.0;
+        for (int64_t j = 0; j < NK; ++j) {
+            if (sc[j] == -INFINITY) continue;
+            const double p = exp(sc[j] - mx);
+            den += p;
+            const uint16_t *vr = v_cache + ((int64_t)kh * S_max + j) * D;
+            for (int d = 0; d < D; ++d) o[d] += p * (double)oracle_f16_to_f32(vr[d]);
+        }
+        for (int d = 0; d < D; ++d) o[d] /= den;
+        free(sc);
+    }
+}
+
+/* keep the accepted path: slot L+path[t] -> slot L+t for t < n (path increasing, so each move
+   reads a slot no earlier move has written) */
+void oracle_kv_commit(uint16_t *k_cache, uint16_t *v_cache, int H_kv, int D, int64_t S_max, int64_t L,
+                      const int32_t *path, int n) {
+    for (int t = 0; t < n; ++t) {
+        if (path[t] == t) continue;
+        for (int h = 0; h < H_kv; ++h) {
+            const int64_t src = ((int64_t)h * S_max + L + path[t]) * D;
+            const int64_t dst = ((int64_t)h * S_max + L + t) * D;
+            memcpy(k_cache + dst, k_cache + src, (size_t)D * sizeof(uint16_t));
+            memcpy(v_cache + dst, v_cache + src, (size_t)D * sizeof(uint16_t));
+        }
+    }
 }

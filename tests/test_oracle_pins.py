@@ -731,3 +731,140 @@ def test_shortlist_finds_the_exact_winner_when_the_copy_ranks_it_second():
     assert exact[0, lo] < exact[0, top] == exact[0].max()
     am, nc = oracle.shortlist_argmax(q4, bound, w8, N, K, q, s)
     assert int(am[0]) == top and nc[0] >= 2
+
+
+# ---------------------------------------------------------------------------
+# decode attention over the K+1 positions, fp16 KV append, commit of the accepted path
+# ---------------------------------------------------------------------------
+
+def _f16(a):
+    return np.asarray(a, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def _caches(H_kv, S_max, D):
+    return np.zeros((H_kv, S_max, D), dtype=np.uint16), np.zeros((H_kv, S_max, D), dtype=np.uint16)
+
+
+def test_f16_conversion_is_numpys_nearest_even():
+    x = np.concatenate([sdgen.normal(sdgen.key(90), (4096,)) * s for s in (1e-6, 1e-3, 1.0, 300.0, 3e4)])
+    x = np.concatenate([x, np.float32([65504.0, 65519.0, 65520.0, -7e4, 2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -26,
+                                       0.0, -0.0, np.inf])])
+    with np.errstate(over="ignore"):
+        want = x.astype(np.float32).astype(np.float16).view(np.uint16)
+    assert np.array_equal(oracle.f32_to_f16(x), want)
+
+
+def test_attention_one_hot_keys_closed_form():
+    """Keys alpha e_j, query beta e_2: score alpha beta / sqrt(D) at key 2, 0 elsewhere, so the
+    output is (e^s v_2 + sum_{j != 2} v_j) / (e^s + n - 1); the scale 1/sqrt(D) is what is pinned."""
+    H_kv, D, L, M = 1, 64, 12, 1
+    kc, vc = _caches(H_kv, 32, D)
+    alpha, beta = 2.0, 3.0
+    for j in range(L + M):
+        kc[0, j] = _f16(alpha * np.eye(D)[j])
+        vc[0, j] = _f16(np.full(D, float(j)))
+    q = np.zeros((M, 1, D), np.float32)
+    q[0, 0, 2] = beta
+    out = oracle.attn_decode(q, kc, vc, L)
+    s = alpha * beta / np.sqrt(D)
+    n = L + M
+    want = (np.exp(s) * 2.0 + (sum(range(n)) - 2.0)) / (np.exp(s) + n - 1)
+    np.testing.assert_allclose(out[0, 0], want, rtol=1e-13)
+
+
+def test_attention_chain_and_tree_masks_count_the_visible_keys():
+    """Equal keys: the output is the mean of the visible values.  Value of slot j is j, so the
+    mean names the visible set: committed 0..L-1 plus the path of position i."""
+    H_kv, D, L, M = 1, 32, 7, 5
+    kc, vc = _caches(H_kv, 16, D)
+    for j in range(L + M):
+        kc[0, j] = _f16(np.full(D, 0.5))
+        vc[0, j] = _f16(np.full(D, float(j)))
+    q = sdgen.normal(sdgen.key(91), (M, 1, D))
+    chain = oracle.attn_decode(q, kc, vc, L)
+    for i in range(M):
+        vis = list(range(L)) + [L + j for j in range(i + 1)]
+        np.testing.assert_allclose(chain[i, 0], np.mean(vis), rtol=1e-13)
+    parent = np.array([-1, 0, 0, 1, 2], np.int32)  # node 3 under 1, node 4 under 2
+    tree = oracle.attn_decode(q, kc, vc, L, parent)
+    paths = {0: [0], 1: [0, 1], 2: [0, 2], 3: [0, 1, 3], 4: [0, 2, 4]}
+    for i in range(M):
+        vis = list(range(L)) + [L + j for j in paths[i]]
+        np.testing.assert_allclose(tree[i, 0], np.mean(vis), rtol=1e-13)
+
+
+def test_attention_grouped_heads_read_their_kv_head():
+    """H = 3 H_kv: query head h reads KV head h // 3 (constant values per KV head)."""
+    H_kv, H, D, L, M = 2, 6, 32, 9, 3
+    kc, vc = _caches(H_kv, 16, D)
+    rng = sdgen.normal(sdgen.key(92), (H_kv, L + M, D))
+    for h in range(H_kv):
+        kc[h, :L + M] = _f16(rng[h])
+        vc[h, :L + M] = _f16(np.full((L + M, D), 10.0 * (h + 1)))
+    q = sdgen.normal(sdgen.key(92, 1), (M, H, D))
+    out = oracle.attn_decode(q, kc, vc, L)
+    for h in range(H):
+        np.testing.assert_allclose(out[:, h], 10.0 * (h // 3 + 1), rtol=1e-13)
+
+
+def test_attention_matches_a_dense_softmax_with_explicit_mask():
+    """Brute force by matrices: S = Q K^T / sqrt(D) + mask, softmax rows, times V (numpy, fp64)."""
+    H_kv, H, D, L, M = 2, 4, 64, 40, 5
+    S_max = 64
+    kc, vc = _caches(H_kv, S_max, D)
+    kc[:, :L] = _f16(sdgen.normal(sdgen.key(93), (H_kv, L, D)))
+    vc[:, :L] = _f16(sdgen.normal(sdgen.key(93, 1), (H_kv, L, D)))
+    k_new = sdgen.normal(sdgen.key(93, 2), (M, H_kv, D))
+    v_new = sdgen.normal(sdgen.key(93, 3), (M, H_kv, D))
+    oracle.kv_append(k_new, v_new, kc, vc, L)
+    assert np.array_equal(kc[:, L:L + M], _f16(k_new.transpose(1, 0, 2)))
+    q = sdgen.normal(sdgen.key(93, 4), (M, H, D)) * 2.0
+    parent = np.array([-1, 0, 1, 0, 3], np.int32)
+    out = oracle.attn_decode(q, kc, vc, L, parent)
+    Kf = kc.view(np.float16).astype(np.float64)
+    Vf = vc.view(np.float16).astype(np.float64)
+    anc = [[0], [0, 1], [0, 1, 2], [0, 3], [0, 3, 4]]
+    for h in range(H):
+        kh = h // (H // H_kv)
+        S = q[:, h].astype(np.float64) @ Kf[kh, :L + M].T / np.sqrt(D)
+        mask = np.full((M, L + M), -np.inf)
+        mask[:, :L] = 0
+        for i in range(M):
+            mask[i, [L + j for j in anc[i]]] = 0
+        P = np.exp(S + mask - (S + mask).max(axis=1, keepdims=True))
+        P /= P.sum(axis=1, keepdims=True)
+        np.testing.assert_allclose(out[:, h], P @ Vf[kh, :L + M], rtol=1e-12, atol=1e-14)
+
+
+def test_commit_then_chain_equals_tree_attention():
+    """Attention of tree node i before the commit equals chain attention of the last position
+    after the commit of i's path: the commit keeps exactly the path's entries, in order."""
+    H_kv, H, D, L, M = 2, 2, 32, 20, 6
+    kc, vc = _caches(H_kv, 32, D)
+    kc[:, :L + M] = _f16(sdgen.normal(sdgen.key(94), (H_kv, L + M, D)))
+    vc[:, :L + M] = _f16(sdgen.normal(sdgen.key(94, 1), (H_kv, L + M, D)))
+    q = sdgen.normal(sdgen.key(94, 2), (M, H, D))
+    parent = np.array([-1, 0, 0, 2, 2, 3], np.int32)
+    tree = oracle.attn_decode(q, kc, vc, L, parent)
+    path = np.array([0, 2, 3, 5], np.int32)   # node 5's path
+    kc2, vc2 = kc.copy(), vc.copy()
+    oracle.kv_commit(kc2, vc2, L, path)
+    n = path.size
+    assert np.array_equal(kc2[:, L:L + n], kc[:, L + path]) and np.array_equal(vc2[:, :L], vc[:, :L])
+    # chain over the committed n entries: query rows 0..n-1 take the path's queries
+    qc = q[path]
+    chain = oracle.attn_decode(qc, kc2[:, :L + n].copy(), vc2[:, :L + n].copy(), L)
+    np.testing.assert_allclose(chain[n - 1], tree[5], rtol=1e-13)
+    np.testing.assert_allclose(chain[1], tree[2], rtol=1e-13)
+
+
+def test_attention_is_stable_for_large_scores():
+    """A key scoring 1e4 above the rest takes all the weight (no overflow in the softmax)."""
+    H_kv, D, L, M = 1, 32, 30, 1
+    kc, vc = _caches(H_kv, 32, D)
+    kc[0, :L + M] = _f16(np.ones((L + M, D)) * 0.01)
+    kc[0, 17] = _f16(np.ones(D) * 100.0)
+    vc[0, :L + M] = _f16(sdgen.normal(sdgen.key(95), (L + M, D)))
+    q = np.full((M, 1, D), 20.0, np.float32)
+    out = oracle.attn_decode(q, kc, vc, L)
+    np.testing.assert_allclose(out[0, 0], vc[0, 17].view(np.float16).astype(np.float64), rtol=1e-12)
