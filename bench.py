@@ -390,6 +390,65 @@ def shortlist_bench(args, local):
         "cases": cases}))
 
 
+def attention_bench(args, local):
+    """Decode attention of one 27B-shaped layer (40 heads of 128, one KV head per query head) over
+    the K+1 positions at contexts of 4096 and 32768 rows: device time per call (CUDA events), the
+    fp16 K and V rows read once per call as the algorithmic bytes, against the measured copy peak.
+    Prints one JSON line."""
+    import numpy as np
+    import torch
+
+    import sdgen
+    from speculative_decoding_verify_gb300 import build as b
+    b.build()
+    sdgen.build()
+    import speculative_decoding_verify_gb300 as sdv
+
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    H_kv = H = 40
+    D, M = 128, args.M
+    peak, peak_kind = measured_peaks()
+    cases = {}
+    for L in (4096, 32768):
+        S_max = L + M
+        kc = torch.from_numpy(sdgen.normal(sdgen.key(6, L), (H_kv, S_max, D)).astype(np.float16)).to(dev)
+        vc = torch.from_numpy(sdgen.normal(sdgen.key(6, L + 1), (H_kv, S_max, D)).astype(np.float16)).to(dev)
+        q = torch.from_numpy(sdgen.normal(sdgen.key(6, L + 2), (M, H, D))).to(dev)
+        out = torch.empty((M, H, D), dtype=torch.float32, device=dev)
+        ws = sdv.workspace(sdv.attn_workspace_bytes(M, H, H_kv, D, L), device=dev)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # larger than L2
+        for _ in range(args.warmup):
+            sdv.attn_decode(q, kc, vc, L, out, ws)
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(args.steps):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            sdv.attn_decode(q, kc, vc, L, out, ws)
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        if sdv.device_status() != 0:
+            raise RuntimeError("device status after the timed calls")
+        ms = float(np.median(times))
+        nbytes = 2 * H_kv * (L + M) * D * 2
+        gbs = nbytes / ms / 1e6
+        cases[str(L)] = {"ms": round(ms, 4), "kv_bytes": nbytes, "GB/s": round(gbs, 1),
+                         "frac_of_peak": round(gbs / peak, 3)}
+        log(f"attention L={L}: {ms:.4f} ms, {gbs:.0f} GB/s ({gbs / peak:.1%} of the {peak_kind} copy peak)")
+        del kc, vc, flush
+        torch.cuda.empty_cache()
+    print(json.dumps({
+        "metric": "decode attention over K+1 positions: KV GB/s per call", "unit": "GB/s",
+        "value": cases["32768"]["GB/s"], "higher_is_better": True, "steps": args.steps, "warmup": args.warmup,
+        "n_gpus": 1, "dtype": "fp16 K/V, fp32 arithmetic", "data": "synthetic",
+        "config": {"workload": f"attention 40x128 heads, M={M}, contexts 4096 and 32768",
+                   "l2": "a 256 MB buffer written between timed calls"},
+        "peak_gbs": peak, "peak_kind": peak_kind, "cases": cases}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -404,6 +463,8 @@ def main():
                     help="time only the one-launch pass (no per-operation graph, no eager per-kernel breakdown)")
     ap.add_argument("--mode", default="fused", choices=["fused", "graph"],
                     help="fused: the whole pass as one persistent launch; graph: one CUDA graph of per-op launches")
+    ap.add_argument("--attention", action="store_true",
+                    help="instead of the pass: time the decode attention over the K+1 positions (own JSON line)")
     ap.add_argument("--shortlist", action="store_true",
                     help="instead of the pass: time the exact shortlist head against the full head (own JSON line)")
     args = ap.parse_args()
@@ -423,6 +484,9 @@ def main():
         return
     if args.shortlist:
         shortlist_bench(args, local)
+        return
+    if args.attention:
+        attention_bench(args, local)
         return
 
     import numpy as np

@@ -228,6 +228,49 @@ sd_status sd_head_logits(const void *w, int64_t vocab, int64_t hidden, const int
  * Errors: SD_EINVAL on null/misaligned pointers or bad sizes; SD_EUNSUPPORTED
  * for M > 16 or hidden/32 * M > 12288.
  */
+/*
+ * Decode attention over the K+1 verified positions ("Inside OpenJet Engine",
+ * section "Cheap drafting, careful state management": split-K flash decoding
+ * of full-attention layers, fp16 K/V, fp32 accumulation; "How Kinetic is
+ * fast", section "Where the guesses come from": each row of a draft tree sees
+ * only its own path; "Speculative Decoding with Open-Weights Models", section
+ * "KV Cache Synchronization": rejected entries are dropped in place).
+ *
+ * Cache layout (per layer, caller-owned, 16-byte aligned): k_cache and
+ * v_cache fp16 [H_kv][S_max][D]; rows [0, L) are committed, rows [L, L+M)
+ * hold the M = K+1 new positions.
+ *
+ * sd_kv_append: k_new, v_new fp32 [M][H_kv][D] -> rows [L, L+M), rounded to
+ * fp16 (nearest even).  Requires S_max >= L + M.
+ *
+ * sd_attn_decode: q fp32 [M][H][D] (H a multiple of H_kv; query head h reads
+ * KV head h / (H/H_kv)); parent int32 [M] (device) with parent[0] = -1 and
+ * parent[i] < i for a draft tree, or NULL for a chain.  out fp32 [M][H][D]:
+ *   out[i][h] = sum_j softmax_j(q[i][h] . k_j / sqrt(D)) v_j
+ * over the committed rows and the new rows L+j with j on i's path (j = i or
+ * an ancestor; chain: j <= i).  fp32 arithmetic from the fp16 cache; keys
+ * split into chunks, one partial (max, sum, output) per chunk, then combined.
+ * D = 64 or 128, 1 <= M <= 16 (else SD_EUNSUPPORTED).  workspace: ws_bytes >=
+ * sd_attn_workspace_bytes(M, H, H_kv, D, L), no initialisation needed.  A
+ * parent array that is not a tree (parent[i] >= i) records SD_EDEVICE.
+ *
+ * sd_kv_commit: after acceptance, keep the accepted entries: *count (device,
+ * the accepted token count n, 1 <= n <= M) rows; path int32 [M] (device)
+ * lists the accepted tree nodes in increasing order (node 0 first), and row
+ * L+path[t] moves to row L+t for t < n, in place.  path NULL: a chain, whose
+ * first n rows are already in place (nothing is launched).  The cache length
+ * becomes L+n.  A count or path out of range records SD_EDEVICE and moves
+ * nothing.  D <= 256.
+ */
+size_t sd_attn_workspace_bytes(int32_t M, int32_t H, int32_t H_kv, int32_t D, int64_t L);
+sd_status sd_kv_append(const float *k_new, const float *v_new, int32_t M, int32_t H_kv, int32_t D, void *k_cache,
+                       void *v_cache, int64_t S_max, int64_t L, sd_stream_t stream);
+sd_status sd_attn_decode(const float *q, const void *k_cache, const void *v_cache, int32_t M, int32_t H, int32_t H_kv,
+                         int32_t D, int64_t S_max, int64_t L, const int32_t *parent, float *out, void *workspace,
+                         size_t ws_bytes, sd_stream_t stream);
+sd_status sd_kv_commit(void *k_cache, void *v_cache, int32_t H_kv, int32_t D, int64_t S_max, int64_t L, int32_t M,
+                       const int32_t *path, const int32_t *count, sd_stream_t stream);
+
 sd_status sd_shortlist_build(const void *head_blocks, int64_t vocab, int64_t hidden, void *copy_blocks, float *bound,
                              float *wnorm, sd_stream_t stream);
 size_t sd_shortlist_workspace_bytes(int64_t vocab, int64_t hidden);

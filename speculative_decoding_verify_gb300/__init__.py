@@ -82,6 +82,10 @@ def lib():
             "sd_qmatmul_multipos_noalloc": ([I, P, I64, I64, P, P, I32, P, P, U32, I64, P, P, P], I),
             "sd_head_workspace_bytes": ([I64, I64], SZ),
             "sd_head_logits": ([P, I64, I64, P, P, I32, F, P, P, P, P, P, SZ, P], I),
+            "sd_attn_workspace_bytes": ([I32, I32, I32, I32, I64], SZ),
+            "sd_kv_append": ([P, P, I32, I32, I32, P, P, I64, I64, P], I),
+            "sd_attn_decode": ([P, P, P, I32, I32, I32, I32, I64, I64, P, P, P, SZ, P], I),
+            "sd_kv_commit": ([P, P, I32, I32, I64, I64, I32, P, P, P], I),
             "sd_shortlist_build": ([P, I64, I64, P, P, P, P], I),
             "sd_shortlist_workspace_bytes": ([I64, I64], SZ),
             "sd_head_shortlist": ([P, P, P, P, I64, I64, P, P, I32, P, P, P, SZ, P], I),
@@ -200,6 +204,34 @@ def head_logits(w: torch.Tensor, vocab: int, hidden: int, q: torch.Tensor, scale
     M = q.shape[0]
     _check(lib().sd_head_logits(_p(w), vocab, hidden, _p(q), _p(scales), M, temperature, _p(logits), _p(argmax),
                                 _p(row_max), _p(row_sumexp), _p(ws), ws.numel(), _stream()), "sd_head_logits")
+
+
+def attn_workspace_bytes(M: int, H: int, H_kv: int, D: int, L: int) -> int:
+    return int(lib().sd_attn_workspace_bytes(M, H, H_kv, D, L))
+
+
+def kv_append(k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, L: int):
+    """k_new, v_new fp32 [M][H_kv][D] -> rows [L, L+M) of the fp16 caches [H_kv][S_max][D]."""
+    M, H_kv, D = k_new.shape
+    _check(lib().sd_kv_append(_p(k_new), _p(v_new), M, H_kv, D, _p(k_cache), _p(v_cache), k_cache.shape[1], L,
+                              _stream()), "sd_kv_append")
+
+
+def attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, L: int, out: torch.Tensor,
+                ws: torch.Tensor, parent: torch.Tensor | None = None):
+    """q fp32 [M][H][D] over the fp16 caches [H_kv][S_max][D] (L committed rows + M new) -> out [M][H][D]."""
+    M, H, D = q.shape
+    H_kv, S_max, _ = k_cache.shape
+    _check(lib().sd_attn_decode(_p(q), _p(k_cache), _p(v_cache), M, H, H_kv, D, S_max, L, _p(parent), _p(out),
+                                _p(ws), ws.numel(), _stream()), "sd_attn_decode")
+
+
+def kv_commit(k_cache: torch.Tensor, v_cache: torch.Tensor, L: int, M: int, count: torch.Tensor,
+              path: torch.Tensor | None = None):
+    """Keep the accepted path's rows (count[0] of them) at rows [L, L+count)."""
+    H_kv, S_max, D = k_cache.shape
+    _check(lib().sd_kv_commit(_p(k_cache), _p(v_cache), H_kv, D, S_max, L, M, _p(path), _p(count), _stream()),
+           "sd_kv_commit")
 
 
 def shortlist_build(head_blocks: torch.Tensor, vocab: int, hidden: int):

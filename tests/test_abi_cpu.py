@@ -85,6 +85,14 @@ def test_argument_checks_reject_without_launching(L):
     # rmsnorm: ldx < K
     assert L.sd_rmsnorm_quant_acts(p, 16, p, ctypes.c_float(1e-6), 5, 32, p, p, None) == 1
     assert L.sd_debug_wait_timeout(0, None) == 1
+    # attention: S_max too small, unsupported D or M, misaligned q; commit without a count
+    assert L.sd_kv_append(p, p, 5, 8, 128, p, p, 100, 96, None) == 1
+    assert L.sd_attn_decode(p, p, p, 5, 8, 8, 96, 1000, 10, None, p, p, 1 << 20, None) == 2
+    assert L.sd_attn_decode(p, p, p, 17, 8, 8, 128, 1000, 10, None, p, p, 1 << 20, None) == 2
+    assert L.sd_attn_decode(p, p, p, 5, 12, 8, 128, 1000, 10, None, p, p, 1 << 20, None) == 1
+    assert L.sd_attn_decode(mis, p, p, 5, 8, 8, 128, 1000, 10, None, p, p, 1 << 20, None) == 1
+    assert L.sd_kv_commit(p, p, 8, 128, 1000, 10, 5, p, None, None) == 1
+    assert L.sd_kv_commit(p, p, 8, 512, 1000, 10, 5, p, p, None) == 1
     # shortlist: misaligned head, hidden % 32, M out of range, missing argmax
     assert L.sd_shortlist_build(mis, 4096, 1024, p, p, p, None) == 1
     assert L.sd_shortlist_build(p, 4096, 1000, p, p, p, None) == 1
