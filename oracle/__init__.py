@@ -435,3 +435,41 @@ def head(h: np.ndarray, final_norm: np.ndarray, head_w: np.ndarray, vocab: int, 
     logits, _ = qmatmul(head_q, head_w, vocab, hidden, q, s)
     m, z, a = softmax_stats(logits, T)
     return logits, a, m, z
+
+
+# ---------------------------------------------------------------------------
+# adaptive draft depth (plain Python: a few integers per cycle)
+# ---------------------------------------------------------------------------
+
+def depth_policy(k_max: int, max_pause: int, cycles):
+    """Drafts per cycle under the adaptive-depth reading: "Inside OpenJet Engine", section "Cheap
+    drafting, careful state management" (a configured depth is cut by one for the cycle after a
+    rejection) and "How Kinetic is fast", section "Where the guesses come from" (draft length
+    follows recent drafts; after drafts that miss outright, drafting pauses for longer and
+    longer).
+
+    cycles: the accepted-draft count of each cycle, in order (ignored for a cycle that drafted
+    nothing).  Returns the depth used by each cycle, starting at k_max:
+      all drafts accepted        -> next depth k_max, miss count 0
+      some but not all accepted  -> next depth max(1, k_max - 1), miss count 0
+      none accepted (a miss)     -> miss count + 1, then min(max_pause, 2^(misses - 1)) cycles
+                                    without drafts (none if max_pause is 0), then depth
+                                    max(1, k_max - 1)
+    """
+    reduced = max(1, k_max - 1)
+    k, pause, misses = k_max, 0, 0
+    used = []
+    for acc in cycles:
+        used.append(k)
+        if k == 0:
+            pause = max(0, pause - 1)
+            k = 0 if pause > 0 else reduced
+        elif acc == k:
+            misses, k = 0, k_max
+        elif acc > 0:
+            misses, k = 0, reduced
+        else:
+            misses = min(misses + 1, 31)
+            pause = min(max_pause, 2 ** (misses - 1))
+            k = 0 if pause > 0 else reduced
+    return used

@@ -868,3 +868,34 @@ def test_attention_is_stable_for_large_scores():
     q = np.full((M, 1, D), 20.0, np.float32)
     out = oracle.attn_decode(q, kc, vc, L)
     np.testing.assert_allclose(out[0, 0], vc[0, 17].view(np.float16).astype(np.float64), rtol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# adaptive draft depth
+# ---------------------------------------------------------------------------
+
+def test_depth_cut_by_one_for_the_cycle_after_a_rejection():
+    """A configured depth of four runs three drafts in the cycle after a rejection, and four again
+    after that cycle's drafts are all accepted."""
+    assert oracle.depth_policy(4, 64, [4, 2, 3, 4]) == [4, 4, 3, 4]
+    # a rejection at 4 (1 of 4), all 3 of the cut cycle accepted -> 4 again, and so on
+    assert oracle.depth_policy(4, 64, [1, 3, 1, 3, 3]) == [4, 3, 4, 3, 4]
+    # rejections in a row keep the cut depth
+    assert oracle.depth_policy(4, 64, [2, 1, 2, 3]) == [4, 3, 3, 3]
+    assert oracle.depth_policy(1, 64, [0, 0, 1]) == [1, 0, 1]
+
+
+def test_outright_misses_pause_drafting_for_longer_and_longer():
+    """Misses in a row: pauses of 1, 2, 4, 8 cycles; each resumption drafts at the cut depth."""
+    used = oracle.depth_policy(4, 64, [0] * 40)
+    drafted = [i for i, k in enumerate(used) if k > 0]
+    gaps = [b - a - 1 for a, b in zip(drafted, drafted[1:])]
+    assert gaps[:4] == [1, 2, 4, 8]
+    assert all(used[i] == 3 for i in drafted[1:])
+    # a hit resets the streak (the miss after it pauses 1 cycle, not 4); paused cycles accept nothing
+    assert oracle.depth_policy(4, 64, [0, 0, 0, 0, 0, 2, 0, 0, 0]) == [4, 0, 3, 0, 0, 3, 3, 0, 3]
+    # the cap holds
+    used = oracle.depth_policy(2, 3, [0] * 30)
+    drafted = [i for i, k in enumerate(used) if k > 0]
+    assert max(b - a - 1 for a, b in zip(drafted, drafted[1:])) == 3
+    assert oracle.depth_policy(4, 0, [0, 0, 2]) == [4, 3, 3]
