@@ -262,6 +262,37 @@ sd_status sd_head_logits(const void *w, int64_t vocab, int64_t hidden, const int
  * becomes L+n.  A count or path out of range records SD_EDEVICE and moves
  * nothing.  D <= 256.
  */
+/*
+ * Adaptive draft depth, host only ("Inside OpenJet Engine", section "Cheap
+ * drafting, careful state management": a configured depth is cut by one for
+ * the cycle after a rejection; "How Kinetic is fast", section "Where the
+ * guesses come from": draft length follows recent drafts, and outright misses
+ * pause drafting for longer and longer).
+ *
+ * The state lives in caller memory (HOST pointer); nothing touches a device.
+ * sd_depth_init: k_max drafts per cycle (1..15), max_pause >= 0 cycles;
+ * k_next = k_max.  Run the next cycle with k_next drafts (0: plain decoding,
+ * M = 1), then call sd_depth_update with the number of drafts accepted:
+ *   all k_next accepted      -> k_next = k_max, miss count 0
+ *   some, not all            -> k_next = max(1, k_max - 1), miss count 0
+ *   none (an outright miss)  -> miss count + 1; pause_left =
+ *                               min(max_pause, 2^(misses - 1)) cycles with
+ *                               k_next = 0 (none if max_pause is 0), then
+ *                               k_next = max(1, k_max - 1)
+ *   a cycle with k_next = 0  -> pause_left - 1 (accepted is ignored)
+ * Errors: SD_EINVAL on a null or uninitialised state, or accepted outside
+ * [0, k_next].
+ */
+typedef struct {
+    int32_t k_max;      /* configured depth */
+    int32_t max_pause;  /* longest pause, in cycles */
+    int32_t k_next;     /* drafts for the next cycle; 0 = no drafting */
+    int32_t pause_left; /* cycles without drafts still to run */
+    int32_t misses;     /* outright misses in a row */
+} sd_depth_state;
+sd_status sd_depth_init(sd_depth_state *s, int32_t k_max, int32_t max_pause);
+sd_status sd_depth_update(sd_depth_state *s, int32_t accepted);
+
 size_t sd_attn_workspace_bytes(int32_t M, int32_t H, int32_t H_kv, int32_t D, int64_t L);
 sd_status sd_kv_append(const float *k_new, const float *v_new, int32_t M, int32_t H_kv, int32_t D, void *k_cache,
                        void *v_cache, int64_t S_max, int64_t L, sd_stream_t stream);

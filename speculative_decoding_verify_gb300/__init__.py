@@ -56,6 +56,11 @@ class SdPass(ctypes.Structure):
                 ("smem_bytes", ctypes.c_uint32), ("grid", ctypes.c_int32), ("accept", ctypes.c_int32)]
 
 
+class SdDepthState(ctypes.Structure):
+    _fields_ = [("k_max", ctypes.c_int32), ("max_pause", ctypes.c_int32), ("k_next", ctypes.c_int32),
+                ("pause_left", ctypes.c_int32), ("misses", ctypes.c_int32)]
+
+
 class SdError(RuntimeError):
     def __init__(self, code: int, what: str):
         super().__init__(f"{what}: {STATUS.get(code, code)} ({code})")
@@ -82,6 +87,8 @@ def lib():
             "sd_qmatmul_multipos_noalloc": ([I, P, I64, I64, P, P, I32, P, P, U32, I64, P, P, P], I),
             "sd_head_workspace_bytes": ([I64, I64], SZ),
             "sd_head_logits": ([P, I64, I64, P, P, I32, F, P, P, P, P, P, SZ, P], I),
+            "sd_depth_init": ([ctypes.POINTER(SdDepthState), I32, I32], I),
+            "sd_depth_update": ([ctypes.POINTER(SdDepthState), I32], I),
             "sd_attn_workspace_bytes": ([I32, I32, I32, I32, I64], SZ),
             "sd_kv_append": ([P, P, I32, I32, I32, P, P, I64, I64, P], I),
             "sd_attn_decode": ([P, P, P, I32, I32, I32, I32, I64, I64, P, P, P, SZ, P], I),
@@ -204,6 +211,23 @@ def head_logits(w: torch.Tensor, vocab: int, hidden: int, q: torch.Tensor, scale
     M = q.shape[0]
     _check(lib().sd_head_logits(_p(w), vocab, hidden, _p(q), _p(scales), M, temperature, _p(logits), _p(argmax),
                                 _p(row_max), _p(row_sumexp), _p(ws), ws.numel(), _stream()), "sd_head_logits")
+
+
+class DepthPolicy:
+    """Adaptive draft depth (host only): ``k`` is the number of drafts to run this cycle (0: plain
+    decoding); call ``update(accepted)`` after the cycle."""
+
+    def __init__(self, k_max: int, max_pause: int = 64):
+        self.state = SdDepthState()
+        _check(lib().sd_depth_init(ctypes.byref(self.state), k_max, max_pause), "sd_depth_init")
+
+    @property
+    def k(self) -> int:
+        return int(self.state.k_next)
+
+    def update(self, accepted: int) -> int:
+        _check(lib().sd_depth_update(ctypes.byref(self.state), accepted), "sd_depth_update")
+        return self.k
 
 
 def attn_workspace_bytes(M: int, H: int, H_kv: int, D: int, L: int) -> int:

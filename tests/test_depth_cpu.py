@@ -1,0 +1,58 @@
+"""The library's adaptive draft depth (sd_depth_init / sd_depth_update, host code in
+libsdverify.so) against the oracle's, step for step, on seeded acceptance sequences, plus its
+argument checks.  No GPU: the state machine runs on the host."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+import sdgen
+
+
+@pytest.fixture(scope="module")
+def sdv():
+    from speculative_decoding_verify_gb300 import build as b
+    b.build()
+    import speculative_decoding_verify_gb300 as m
+    m.lib()
+    return m
+
+
+def drive(sdv, k_max, max_pause, hit_rate, n, seed):
+    """Run n cycles; each drafted token is accepted with probability hit_rate until the first
+    rejection.  Returns the depths used and the accepted counts fed back."""
+    u = sdgen.u32(sdgen.key(9, seed), n * 16).reshape(n, 16) / 2.0 ** 32
+    pol = sdv.DepthPolicy(k_max, max_pause)
+    used, accs = [], []
+    for c in range(n):
+        k = pol.k
+        acc = 0
+        while acc < k and u[c, acc] < hit_rate:
+            acc += 1
+        used.append(k)
+        accs.append(acc)
+        pol.update(acc)
+    return used, accs
+
+
+@pytest.mark.parametrize("k_max,max_pause,hit_rate", [(4, 64, 0.7), (4, 64, 0.2), (1, 8, 0.5), (15, 3, 0.9),
+                                                      (3, 0, 0.3), (7, 64, 0.02)])
+def test_depth_matches_oracle(sdv, k_max, max_pause, hit_rate):
+    used, accs = drive(sdv, k_max, max_pause, hit_rate, 400, k_max * 100 + max_pause)
+    assert used == oracle.depth_policy(k_max, max_pause, accs)
+    assert all(0 <= k <= k_max for k in used)
+
+
+def test_depth_argument_checks(sdv):
+    L = sdv.lib()
+    st = sdv.SdDepthState()
+    assert L.sd_depth_init(ctypes.byref(st), 0, 4) == 1
+    assert L.sd_depth_init(ctypes.byref(st), 16, 4) == 1
+    assert L.sd_depth_init(ctypes.byref(st), 4, -1) == 1
+    assert L.sd_depth_init(None, 4, 4) == 1
+    assert L.sd_depth_init(ctypes.byref(st), 4, 4) == 0 and st.k_next == 4
+    assert L.sd_depth_update(ctypes.byref(st), 5) == 1     # more accepted than drafted
+    assert L.sd_depth_update(ctypes.byref(st), -1) == 1
+    assert st.k_next == 4                                   # a rejected call changes nothing
+    assert L.sd_depth_update(ctypes.byref(st), 2) == 0 and st.k_next == 3
