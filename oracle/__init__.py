@@ -98,6 +98,9 @@ def _get():
                 "oracle_accept_sample_topk": ([_P, _I64, _I, _P, _P, _F, _I, _F, ctypes.c_uint64, _I64, _P], _I),
                 "oracle_shortlist_copy": ([_P, _I64, _I64, _P, _P, _P], None),
                 "oracle_f32_to_f16": ([_P, _I64, _P], None),
+                "oracle_kq_block_bytes": ([_I], _I),
+                "oracle_kq_dequant": ([_I, _P, _I64, _P], None),
+                "oracle_kq_matmul": ([_I, _P, _I64, _I64, _P, _P, _I, _P], None),
                 "oracle_kv_append": ([_P, _P, _I, _I, _I, _P, _P, _I64, _I64], None),
                 "oracle_attn_decode": ([_P, _P, _P, _I, _I, _I, _I, _I64, _I64, _P, _P], None),
                 "oracle_kv_commit": ([_P, _P, _I, _I, _I64, _I64, _P, _I], None),
@@ -342,6 +345,30 @@ def shortlist_argmax(q4_blocks, bound, q8_blocks, N: int, K: int, q, scales):
     nc = np.empty(M, dtype=np.int64)
     _get().oracle_shortlist_argmax(p4, pb, p8, N, K, pq, ps, M, am.ctypes.data, nc.ctypes.data)
     return am, nc
+
+
+Q4_K, Q6_K = 2, 3   # 256-weight K-quant super-blocks (144 and 210 bytes)
+
+
+def kq_dequant(qtype: int, blocks, n_out: int, k_in: int) -> np.ndarray:
+    """K-quant super-blocks [n_out][k_in/256] -> fp32 [n_out][k_in]."""
+    blocks, p = _c(np.asarray(blocks).reshape(-1), np.uint8)
+    bb = _get().oracle_kq_block_bytes(qtype)
+    assert k_in % 256 == 0 and blocks.size == n_out * (k_in // 256) * bb
+    out = np.empty((n_out, k_in), dtype=np.float32)
+    _get().oracle_kq_dequant(qtype, p, n_out * (k_in // 256), out.ctypes.data)
+    return out
+
+
+def kq_matmul(qtype: int, blocks, n_out: int, k_in: int, q, scales) -> np.ndarray:
+    """fp64 [M][n_out]: per 32-weight block, the integer dots times the scales (factored form)."""
+    blocks, pw = _c(np.asarray(blocks).reshape(-1), np.uint8)
+    q, pq = _c(q, np.int8)
+    sc, ps = _c(scales, np.float32)
+    M = q.shape[0]
+    y = np.empty((M, n_out), dtype=np.float64)
+    _get().oracle_kq_matmul(qtype, pw, n_out, k_in, pq, ps, M, y.ctypes.data)
+    return y
 
 
 def f32_to_f16(x) -> np.ndarray:

@@ -858,3 +858,118 @@ void oracle_kv_commit(uint16_t *k_cache, uint16_t *v_cache, int H_kv, int D, int
         }
     }
 }
+
+/* ------------------------------------------------------------------ */
+/* K-quant formats of the pages' model files (Q4_K_M = Q4_K weights    */
+/* with some Q6_K tensors: "Inside OpenJet Engine", section "One GPU    */
+/* launch for a speculative cycle" repacks Q6_K; "How Kinetic is fast"  */
+/* and "Speculative Decoding with Open-Weights Models" run Q4_K_M).     */
+/* The pages print no block layout; the layouts below restate the GGUF  */
+/* K-quant formats.  Both hold 256 weights per super-block.             */
+/*  Q4_K (144 B): fp16 d, fp16 dmin, 12 bytes of 6-bit scale/min pairs  */
+/*   for eight 32-weight sub-blocks, 128 bytes of 4-bit codes.  Pair s:  */
+/*   s < 4: scale = b[s] & 63, min = b[s+4] & 63; s >= 4: scale =        */
+/*   (b[s+4] & 15) | (b[s-4] >> 6) << 4, min = (b[s+4] >> 4) |          */
+/*   (b[s] >> 6) << 4.  Codes: 64-weight chunk c uses bytes 32c..32c+31, */
+/*   low nibbles for its first 32 weights, high nibbles for the next 32. */
+/*   Weight = d * scale * code - dmin * min.                            */
+/*  Q6_K (210 B): 128 bytes ql (low 4 bits), 64 bytes qh (high 2 bits), */
+/*   16 int8 scales, fp16 d.  Weight i of half n = i / 128, r = i % 128, */
+/*   l = r % 32, k = r / 32: low bits from ql[64n + l + 32 (k & 1)],    */
+/*   the low nibble for k < 2 and the high nibble for k >= 2; high bits */
+/*   (qh[32n + l] >> 2k) & 3; code = low | high << 4, minus 32.         */
+/*   Weight = d * scales[i / 16] * code.                                */
+/* With int8 activations per 32-block (q, d_a) the matmul adds, per     */
+/* 32-weight activation block, d_a * (d sc dot(code, q) - dmin m sum q) */
+/* (Q4_K) or d_a d (sc_lo dot_lo + sc_hi dot_hi) over its two 16-weight */
+/* halves (Q6_K): integer dots, then the scales, in fp64.               */
+/* ------------------------------------------------------------------ */
+
+enum { OQ4_K = 2, OQ6_K = 3 };
+
+int oracle_kq_block_bytes(int qtype) { return qtype == OQ4_K ? 144 : (qtype == OQ6_K ? 210 : 0); }
+
+static void q4k_scale_min(const uint8_t *b, int s, int *sc, int *mn) {
+    if (s < 4) {
+        *sc = b[s] & 63;
+        *mn = b[s + 4] & 63;
+    } else {
+        *sc = (b[s + 4] & 15) | ((b[s - 4] >> 6) << 4);
+        *mn = (b[s + 4] >> 4) | ((b[s] >> 6) << 4);
+    }
+}
+
+/* code of weight i (0..255) of a super-block */
+static int kq_code(int qtype, const uint8_t *blk, int i) {
+    if (qtype == OQ4_K) {
+        const int c = i / 64, r = i % 64;
+        const uint8_t byte = blk[16 + 32 * c + (r % 32)];
+        return r < 32 ? (byte & 15) : (byte >> 4);
+    }
+    const int n = i / 128, r = i % 128, l = r % 32, k = r / 32;
+    const uint8_t lo = blk[64 * n + l + 32 * (k & 1)];
+    const int low = k < 2 ? (lo & 15) : (lo >> 4);
+    const int high = (blk[128 + 32 * n + l] >> (2 * k)) & 3;
+    return (low | (high << 4)) - 32;
+}
+
+/* dequantised weights of nblk super-blocks, fp32 */
+void oracle_kq_dequant(int qtype, const uint8_t *blocks, int64_t nblk, float *out) {
+    const int bb = oracle_kq_block_bytes(qtype);
+    for (int64_t n = 0; n < nblk; ++n) {
+        const uint8_t *blk = blocks + n * bb;
+        for (int i = 0; i < 256; ++i) {
+            double v;
+            if (qtype == OQ4_K) {
+                const double d = oracle_f16_to_f32((uint16_t)(blk[0] | (blk[1] << 8)));
+                const double dmin = oracle_f16_to_f32((uint16_t)(blk[2] | (blk[3] << 8)));
+                int sc, mn;
+                q4k_scale_min(blk + 4, i / 32, &sc, &mn);
+                v = d * sc * kq_code(qtype, blk, i) - dmin * mn;
+            } else {
+                const double d = oracle_f16_to_f32((uint16_t)(blk[208] | (blk[209] << 8)));
+                v = d * (int8_t)blk[192 + i / 16] * kq_code(qtype, blk, i);
+            }
+            out[n * 256 + i] = (float)v;
+        }
+    }
+}
+
+/* y[m][n] (fp64) = sum over 32-blocks of the factored integer form; w [n_out][k_in/256] blocks,
+   q int8 [M][k_in], scales fp32 [M][k_in/32] */
+void oracle_kq_matmul(int qtype, const uint8_t *w, int64_t n_out, int64_t k_in, const int8_t *q,
+                      const float *scales, int M, double *y) {
+    const int bb = oracle_kq_block_bytes(qtype);
+    const int64_t SB = k_in / 256, KB = k_in / 32;
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < n_out; ++n) {
+        for (int m = 0; m < M; ++m) {
+            double acc = 0.0;
+            for (int64_t b = 0; b < KB; ++b) {
+                const uint8_t *blk = w + (n * SB + b / 8) * bb;
+                const int s = (int)(b % 8);  /* 32-weight sub-block within the super-block */
+                const int8_t *qa = q + (int64_t)m * k_in + b * 32;
+                const double da = scales[(int64_t)m * KB + b];
+                if (qtype == OQ4_K) {
+                    int64_t dot = 0, sum = 0;
+                    for (int i = 0; i < 32; ++i) {
+                        dot += (int64_t)kq_code(qtype, blk, 32 * s + i) * qa[i];
+                        sum += qa[i];
+                    }
+                    int sc, mn;
+                    q4k_scale_min(blk + 4, s, &sc, &mn);
+                    const double d = oracle_f16_to_f32((uint16_t)(blk[0] | (blk[1] << 8)));
+                    const double dmin = oracle_f16_to_f32((uint16_t)(blk[2] | (blk[3] << 8)));
+                    acc += da * (d * sc * (double)dot - dmin * mn * (double)sum);
+                } else {
+                    int64_t lo = 0, hi = 0;
+                    for (int i = 0; i < 16; ++i) lo += (int64_t)kq_code(qtype, blk, 32 * s + i) * qa[i];
+                    for (int i = 16; i < 32; ++i) hi += (int64_t)kq_code(qtype, blk, 32 * s + i) * qa[i];
+                    const double d = oracle_f16_to_f32((uint16_t)(blk[208] | (blk[209] << 8)));
+                    acc += da * d * ((int8_t)blk[192 + 2 * s] * (double)lo + (int8_t)blk[192 + 2 * s + 1] * (double)hi);
+                }
+            }
+            y[(int64_t)m * n_out + n] = acc;
+        }
+    }
+}

@@ -210,3 +210,24 @@ def tree16(k: int):
     for i in range(1, 16):
         depth[i] = depth[parent[i]] + 1
     return np.array(parent, dtype=np.int32), np.array(depth, dtype=np.int32)
+
+
+KQ_BLOCK_BYTES = {2: 144, 3: 210}   # Q4_K, Q6_K super-blocks of 256 weights
+
+
+def random_kq_blocks(qtype: int, k: int, n_out: int, k_in: int, d_scale: float = 1e-3) -> np.ndarray:
+    """Seeded K-quant super-blocks [n_out][k_in/256]: random code and scale bytes (every byte
+    pattern is a valid block), with the fp16 scale fields set to finite values in
+    [d_scale, 2 d_scale)."""
+    assert k_in % 256 == 0
+    bb = KQ_BLOCK_BYTES[qtype]
+    nblk = n_out * (k_in // 256)
+    raw = u32(k, (nblk * bb + 3) // 4).view(np.uint8)[:nblk * bb].reshape(nblk, bb).copy()
+    d = (d_scale * (1.0 + u32(key(k, 1), 2 * nblk).astype(np.float64) / 2.0 ** 32)).astype(np.float16)
+    d = d.view(np.uint8).reshape(nblk, 2, 2)
+    if qtype == 2:
+        raw[:, 0:2] = d[:, 0]
+        raw[:, 2:4] = d[:, 1]
+    else:
+        raw[:, 208:210] = d[:, 0]
+    return raw.reshape(n_out, -1)

@@ -899,3 +899,78 @@ def test_outright_misses_pause_drafting_for_longer_and_longer():
     drafted = [i for i, k in enumerate(used) if k > 0]
     assert max(b - a - 1 for a, b in zip(drafted, drafted[1:])) == 3
     assert oracle.depth_policy(4, 0, [0, 0, 2]) == [4, 3, 3]
+
+
+# ---------------------------------------------------------------------------
+# K-quant formats (Q4_K, Q6_K): layouts pinned by packing known fields, the matmul by the
+# dense product of the dequantised weights
+# ---------------------------------------------------------------------------
+
+def _pack_q4k(d, dmin, sc, mn, codes):
+    """One Q4_K super-block from its fields: sc, mn 6-bit [8]; codes 4-bit [256]."""
+    b = np.zeros(144, np.uint8)
+    b[0:2] = np.frombuffer(np.float16(d).tobytes(), np.uint8)
+    b[2:4] = np.frombuffer(np.float16(dmin).tobytes(), np.uint8)
+    s = np.zeros(12, np.int64)
+    for j in range(4):
+        s[j] = sc[j] | ((sc[j + 4] >> 4) << 6)          # scale j, top bits of scale j+4
+        s[j + 4] = mn[j] | ((mn[j + 4] >> 4) << 6)      # min j, top bits of min j+4
+        s[j + 8] = (sc[j + 4] & 15) | ((mn[j + 4] & 15) << 4)
+    b[4:16] = s
+    for c in range(4):
+        lo, hi = codes[64 * c:64 * c + 32], codes[64 * c + 32:64 * c + 64]
+        b[16 + 32 * c:48 + 32 * c] = np.asarray(lo) | (np.asarray(hi) << 4)
+    return b
+
+
+def _pack_q6k(d, scales, codes):
+    """One Q6_K super-block: scales int8 [16]; codes 6-bit unsigned [256] (weight = code - 32)."""
+    b = np.zeros(210, np.uint8)
+    codes = np.asarray(codes, np.int64)
+    for n in range(2):
+        for l in range(32):
+            q = [codes[128 * n + 32 * k + l] for k in range(4)]
+            b[64 * n + l] = (q[0] & 15) | ((q[2] & 15) << 4)
+            b[64 * n + l + 32] = (q[1] & 15) | ((q[3] & 15) << 4)
+            b[128 + 32 * n + l] = (q[0] >> 4) | ((q[1] >> 4) << 2) | ((q[2] >> 4) << 4) | ((q[3] >> 4) << 6)
+    b[192:208] = np.asarray(scales, np.int8).view(np.uint8)
+    b[208:210] = np.frombuffer(np.float16(d).tobytes(), np.uint8)
+    return b
+
+
+def test_q4k_layout_from_known_fields():
+    u = sdgen.u32(sdgen.key(96), 8 + 8 + 256)
+    sc, mn, codes = u[:8] % 64, u[8:16] % 64, u[16:] % 16
+    b = _pack_q4k(0.5, 0.25, sc, mn, codes)
+    w = oracle.kq_dequant(oracle.Q4_K, b, 1, 256)[0]
+    want = 0.5 * np.repeat(sc, 32) * codes - 0.25 * np.repeat(mn, 32)
+    assert np.array_equal(w, want.astype(np.float32))
+    # every 6-bit field reaches its top value
+    b = _pack_q4k(1.0, 1.0, [63] * 8, [63] * 8, [15] * 256)
+    assert np.all(oracle.kq_dequant(oracle.Q4_K, b, 1, 256) == 63 * 15 - 63)
+
+
+def test_q6k_layout_from_known_fields():
+    u = sdgen.u32(sdgen.key(97), 16 + 256)
+    scales = (u[:16] % 256).astype(np.int64) - 128
+    codes = u[16:] % 64
+    b = _pack_q6k(0.125, scales, codes)
+    w = oracle.kq_dequant(oracle.Q6_K, b, 1, 256)[0]
+    want = 0.125 * np.repeat(scales, 16) * (codes.astype(np.int64) - 32)
+    assert np.array_equal(w, want.astype(np.float32))
+
+
+@pytest.mark.parametrize("qtype", [2, 3])
+def test_kq_matmul_factored_form_equals_dense_product(qtype):
+    """The per-block integer form (Q4_K: d sc dot - dmin m sum) against the fp64 product of the
+    dequantised weights with the dequantised activations."""
+    N, K, M = 96, 1024, 5
+    w = sdgen.random_kq_blocks(qtype, sdgen.key(98, qtype), N, K)
+    q, s = oracle.rmsnorm_quant(sdgen.normal(sdgen.key(98, 9), (M, K)), None)
+    y = oracle.kq_matmul(qtype, w, N, K, q, s)
+    W = oracle.kq_dequant(qtype, w, N, K).astype(np.float64)
+    A = (q.astype(np.float64).reshape(M, K // 32, 32) * s[:, :, None]).reshape(M, K)
+    ref = A @ W.T
+    absb = np.abs(A) @ np.abs(W).T
+    # the dequantised weights are fp32 roundings of the exact values (at most 2^-24 relative)
+    assert np.all(np.abs(y - ref) <= 2.0 ** -23 * absb + 1e-300)
