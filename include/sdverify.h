@@ -198,7 +198,7 @@ sd_status sd_head_logits(const void *w, int64_t vocab, int64_t hidden, const int
                          float *row_sumexp, void *workspace, size_t ws_bytes, sd_stream_t stream);
 
 /*
- * Exact shortlist head for greedy verification ("Inside OpenJet Engine",
+ * Exact shortlist head for greedy verification ("How Kinetic is fast",
  * section "Shortlist": a cheaper copy of the output layer with a proven bound
  * on each row's error scores every row, the best guaranteed score becomes a
  * floor, and only rows whose bound reaches the floor are scored exactly).

@@ -20,18 +20,25 @@ page passage cited in the C source:
 * the same against a top-k / top-p filtered target (the sampling knobs of
   "Inside OpenJet Engine", API section; the filtering order is a reading);
 * Philox4x32-10: Salmon et al., SC'11;
-* the 4-bit shortlist copy and its exact argmax: "Inside OpenJet Engine",
+* the 4-bit shortlist copy and its exact argmax: "How Kinetic is fast",
   section "Shortlist";
 * decode attention over the K+1 positions with a tree mask, the fp16 KV append
   and the in-place commit of the accepted path: "Inside OpenJet Engine",
   section "Cheap drafting, careful state management"; "How Kinetic is fast",
   section "Where the guesses come from"; "Speculative Decoding with
-  Open-Weights Models", section "KV Cache Synchronization".
+  Open-Weights Models", section "KV Cache Synchronization";
+* the adaptive draft depth: "Inside OpenJet Engine", section "Cheap drafting,
+  careful state management", and "How Kinetic is fast", section "Where the
+  guesses come from";
+* Q4_K / Q6_K super-blocks and their matmul: the GGUF K-quant formats the
+  pages' model files use (no page prints a block).
 
 Parity status: every function here is pinned by a ``-m "not gpu"`` test in
 ``tests/test_oracle_pins.py`` against something other than itself.  The
 free-running 64-layer stack composition (``stack_pass``) is pinned only through
-its stages; its end-to-end float output is "parity unpinned".
+its stages; its end-to-end float output is "parity unpinned".  The K-quant
+decoders are pinned to their stated layout, but their agreement with real GGUF
+files is "parity unpinned" (no model file is available).
 """
 from __future__ import annotations
 

@@ -637,7 +637,7 @@ int oracle_accept_sample_topk(const float *logits, int64_t V, int K, const float
 }
 
 /* ------------------------------------------------------------------ */
-/* Shortlist head ("Inside OpenJet Engine", section "Shortlist"): a     */
+/* Shortlist head ("How Kinetic is fast", section "Shortlist"): a       */
 /* smaller copy of the output layer with a proven bound on every row's  */
 /* error scores all rows; the best-looking rows are scored exactly,     */
 /* which gives a floor, and only rows whose bound reaches the floor are */

@@ -1,4 +1,4 @@
-// sdv_shortlist.cu - exact shortlist head for greedy verification ("Inside OpenJet Engine",
+// sdv_shortlist.cu - exact shortlist head for greedy verification ("How Kinetic is fast",
 // section "Shortlist"): a cheaper copy of the output layer, with a proven bound on each row's
 // error, scores every row; the best guaranteed score (the floor) rules out every row whose bound
 // cannot reach it; the remaining rows are scored exactly, and the argmax over them is the argmax

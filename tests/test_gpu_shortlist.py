@@ -1,4 +1,4 @@
-"""GPU parity of the exact shortlist head ("Inside OpenJet Engine", section "Shortlist"):
+"""GPU parity of the exact shortlist head ("How Kinetic is fast", section "Shortlist"):
 sd_shortlist_build against the oracle's copy (bytes bit-exact, bounds valid and tight), and
 sd_head_shortlist's argmax against the oracle's (bit-exact: both take the exact scores in fp64 in
 block order), on random heads where the bound prunes nothing, on heads with one row per position
