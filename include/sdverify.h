@@ -234,7 +234,8 @@ sd_status sd_head_logits(const void *w, int64_t vocab, int64_t hidden, const int
  * of full-attention layers, fp16 K/V, fp32 accumulation; "How Kinetic is
  * fast", section "Where the guesses come from": each row of a draft tree sees
  * only its own path; "Speculative Decoding with Open-Weights Models", section
- * "KV Cache Synchronization": rejected entries are dropped in place).
+ * "Engineering the Architecture: KV Cache Synchronization": rejected entries
+ * are dropped in place).
  *
  * Cache layout (per layer, caller-owned, 16-byte aligned): k_cache and
  * v_cache fp16 [H_kv][S_max][D]; rows [0, L) are committed, rows [L, L+M)

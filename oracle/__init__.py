@@ -26,7 +26,8 @@ page passage cited in the C source:
   and the in-place commit of the accepted path: "Inside OpenJet Engine",
   section "Cheap drafting, careful state management"; "How Kinetic is fast",
   section "Where the guesses come from"; "Speculative Decoding with
-  Open-Weights Models", section "KV Cache Synchronization";
+  Open-Weights Models", section "Engineering the Architecture: KV Cache
+  Synchronization";
 * the adaptive draft depth: "Inside OpenJet Engine", section "Cheap drafting,
   careful state management", and "How Kinetic is fast", section "Where the
   guesses come from";

@@ -768,8 +768,8 @@ void oracle_shortlist_argmax(const uint8_t *q4, const float *bound, const uint8_
 /* flash decoding of full-attention layers with fp16 K/V and fp32       */
 /* accumulation; "How Kinetic is fast", section "Where the guesses come */
 /* from": each row of a draft tree sees only its own path; "Speculative */
-/* Decoding with Open-Weights Models", section "KV Cache                */
-/* Synchronization": rejected                                           */
+/* Decoding with Open-Weights Models", section "Engineering the       */
+/* Architecture: KV Cache Synchronization": rejected                   */
 /* entries are dropped in place).  Reading: the cache holds, per KV     */
 /* head, fp16 K and V rows [S_max][D]; the M new positions are appended */
 /* at slots L..L+M-1 (fp32 -> fp16, nearest even); query row (i, h)     */

@@ -2,8 +2,8 @@
 // Engine", section "Cheap drafting, careful state management": split-K flash decoding of the
 // full-attention layers, fp16 K/V with fp32 accumulation; "How Kinetic is fast", section "Where
 // the guesses come from": each row of a draft tree sees only its own path; "Speculative Decoding
-// with Open-Weights Models", section "KV Cache Synchronization": rejected entries are dropped in
-// place).
+// with Open-Weights Models", section "Engineering the Architecture: KV Cache Synchronization":
+// rejected entries are dropped in place).
 //
 // Cache: per KV head, fp16 K and V rows [S_max][D]; L committed rows, then the M new positions.
 // Query row (i, h) sees every committed row and new row j iff j is on i's path; query head h
