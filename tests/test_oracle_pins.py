@@ -974,3 +974,35 @@ def test_kq_matmul_factored_form_equals_dense_product(qtype):
     absb = np.abs(A) @ np.abs(W).T
     # the dequantised weights are fp32 roundings of the exact values (at most 2^-24 relative)
     assert np.all(np.abs(y - ref) <= 2.0 ** -23 * absb + 1e-300)
+
+
+def test_kq_matmul_reduces_to_the_32_weight_formats():
+    """Q4_K with every scale 1, min 8 and dmin = d is Q4_32 (d (code - 8)); Q6_K with every scale 1
+    is Q8_0 with codes in [-32, 31].  Same weights, so the same matmul as the brute-force-pinned
+    32-weight path, whose fp64 sums come back rounded to fp32: equal to the fp32 rounding of the
+    K-quant path's fp64 sums (one rounding step either way at a rounding boundary)."""
+    N, K, M = 24, 512, 3
+    q, s = oracle.rmsnorm_quant(sdgen.normal(sdgen.key(99, 1), (M, K)), None)
+    u = sdgen.u32(sdgen.key(99, 2), N * K)
+    d = np.float16(0.0123)
+    # 4-bit
+    codes4 = (u % 16).reshape(N, K // 256, 256)
+    q4k = np.stack([np.concatenate([_pack_q4k(d, d, [1] * 8, [8] * 8, codes4[n, j]) for j in range(K // 256)])
+                    for n in range(N)])
+    q432 = np.zeros((N, K // 32, 18), np.uint8)
+    q432[:, :, 0:2] = np.frombuffer(d.tobytes(), np.uint8)
+    c = codes4.reshape(N, K // 32, 32)
+    q432[:, :, 2:] = c[:, :, :16] | (c[:, :, 16:] << 4)
+    y_k = oracle.kq_matmul(oracle.Q4_K, q4k, N, K, q, s)
+    y_32, _ = oracle.qmatmul(oracle.Q4_32, q432.reshape(-1), N, K, q, s)
+    assert np.all(np.abs(y_k.astype(np.float32) - y_32) <= np.spacing(np.abs(y_32)))
+    # 6-bit
+    codes6 = (u // 16 % 64).reshape(N, K // 256, 256)
+    q6k = np.stack([np.concatenate([_pack_q6k(d, [1] * 16, codes6[n, j]) for j in range(K // 256)])
+                    for n in range(N)])
+    q80 = np.zeros((N, K // 32, 34), np.uint8)
+    q80[:, :, 0:2] = np.frombuffer(d.tobytes(), np.uint8)
+    q80[:, :, 2:] = (codes6.reshape(N, K // 32, 32).astype(np.int64) - 32).astype(np.int8).view(np.uint8)
+    y_k = oracle.kq_matmul(oracle.Q6_K, q6k, N, K, q, s)
+    y_8, _ = oracle.qmatmul(oracle.Q8_0, q80.reshape(-1), N, K, q, s)
+    assert np.all(np.abs(y_k.astype(np.float32) - y_8) <= np.spacing(np.abs(y_8)))
