@@ -252,7 +252,9 @@ sd_status sd_head_logits(const void *w, int64_t vocab, int64_t hidden, const int
  * an ancestor; chain: j <= i).  fp32 arithmetic from the fp16 cache; keys
  * split into chunks, one partial (max, sum, output) per chunk, then combined.
  * D = 64 or 128, 1 <= M <= 16 (else SD_EUNSUPPORTED).  workspace: ws_bytes >=
- * sd_attn_workspace_bytes(M, H, H_kv, D, L), no initialisation needed.  A
+ * sd_attn_workspace_bytes(M, H, H_kv, D, L), no initialisation needed; the
+ * size for the longest context serves every shorter one (the number of key
+ * chunks is capped by the SM count, not the context).  A
  * parent array that is not a tree (parent[i] >= i) records SD_EDEVICE.
  *
  * sd_kv_commit: after acceptance, keep the accepted entries: *count (device,
