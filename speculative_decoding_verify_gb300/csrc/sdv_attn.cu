@@ -338,8 +338,9 @@ static bool attn_plan(int32_t M, int32_t H, int32_t H_kv, int32_t D, int64_t L, 
     int64_t cp = (NP + want - 1) / want;
     if (cp < AT_MIN_CHUNK_PAIRS) cp = AT_MIN_CHUNK_PAIRS;
     p.chunk_pairs = cp;
-    p.S = static_cast<int32_t>((NP + cp - 1) / cp);
-    const size_t nrow = static_cast<size_t>(H_kv) * p.QG * p.S * AT_TQ;
+    p.S = static_cast<int32_t>((NP + cp - 1) / cp);  // <= want, whatever the context
+    // partials sized for `want` chunks, so one workspace serves every context length
+    const size_t nrow = static_cast<size_t>(H_kv) * p.QG * static_cast<size_t>(want) * AT_TQ;
     p.off_o = (nrow * 2 * sizeof(float) + 255) & ~static_cast<size_t>(255);
     p.total = p.off_o + ((nrow * D * sizeof(float) + 255) & ~static_cast<size_t>(255));
     return true;
