@@ -107,6 +107,7 @@ def _get():
                 "oracle_shortlist_copy": ([_P, _I64, _I64, _P, _P, _P], None),
                 "oracle_f32_to_f16": ([_P, _I64, _P], None),
                 "oracle_kq_block_bytes": ([_I], _I),
+                "oracle_accept_greedy_tree_path": ([_P, _P, _P, _I, _P], _I),
                 "oracle_kq_dequant": ([_I, _P, _I64, _P], None),
                 "oracle_kq_matmul": ([_I, _P, _I64, _I64, _P, _P, _I, _P], None),
                 "oracle_kv_append": ([_P, _P, _I, _I, _I, _P, _P, _I64, _I64], None),
@@ -237,6 +238,17 @@ def accept_greedy_tree(argmax: np.ndarray, tokens: np.ndarray, parent: np.ndarra
     M = tokens.size
     out = np.empty(M, dtype=np.int32)
     n = _get().oracle_accept_greedy_tree(pa, pt, pp, M, out.ctypes.data)
+    return out[:n].copy()
+
+
+def accept_greedy_tree_path(argmax: np.ndarray, tokens: np.ndarray, parent: np.ndarray) -> np.ndarray:
+    """Node indices of the accepted path (root first) under the greedy tree rule."""
+    argmax, pa = _c(argmax, np.int32)
+    tokens, pt = _c(tokens, np.int32)
+    parent, pp = _c(parent, np.int32)
+    M = tokens.size
+    out = np.empty(M, dtype=np.int32)
+    n = _get().oracle_accept_greedy_tree_path(pa, pt, pp, M, out.ctypes.data)
     return out[:n].copy()
 
 

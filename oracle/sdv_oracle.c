@@ -973,3 +973,25 @@ void oracle_kq_matmul(int qtype, const uint8_t *w, int64_t n_out, int64_t k_in, 
         }
     }
 }
+
+/* The accepted path of the greedy tree rule above as node indices, root first: the nodes whose
+   K/V rows the cache keeps ("Speculative Decoding with Open-Weights Models", section
+   "Engineering the Architecture: KV Cache Synchronization").  Returns the node count. */
+int oracle_accept_greedy_tree_path(const int32_t *argmax, const int32_t *tokens, const int32_t *parent, int M,
+                                   int32_t *path) {
+    int *ok = (int *)calloc((size_t)M, sizeof(int)), *depth = (int *)calloc((size_t)M, sizeof(int));
+    ok[0] = 1;
+    int best = 0;
+    for (int i = 1; i < M; ++i) {
+        const int p = parent[i];
+        if (p < 0 || p >= i) continue;
+        depth[i] = depth[p] + 1;
+        ok[i] = ok[p] && tokens[i] == argmax[p];
+        if (ok[i] && depth[i] > depth[best]) best = i;
+    }
+    const int d = depth[best];
+    for (int i = best, j = d; j >= 0; i = parent[i], --j) path[j] = i;
+    free(ok);
+    free(depth);
+    return d + 1;
+}

@@ -1006,3 +1006,20 @@ def test_kq_matmul_reduces_to_the_32_weight_formats():
     y_k = oracle.kq_matmul(oracle.Q6_K, q6k, N, K, q, s)
     y_8, _ = oracle.qmatmul(oracle.Q8_0, q80.reshape(-1), N, K, q, s)
     assert np.all(np.abs(y_k.astype(np.float32) - y_8) <= np.spacing(np.abs(y_8)))
+
+
+def test_tree_path_names_the_accepted_tokens():
+    """The accepted path's nodes carry exactly the tokens the pinned tree rule emits (the last
+    emitted token is the argmax after the path's end), on random trees with repeated tokens."""
+    u = sdgen.u32(sdgen.key(100), 200 * 64)
+    for t in range(200):
+        M = 2 + t % 15
+        r = u[t * 64:(t + 1) * 64]
+        parent = np.array([-1] + [int(r[i] % i) for i in range(1, M)], np.int32)
+        argmax = (r[16:16 + M] % 3).astype(np.int32)        # three tokens: many matches and ties
+        tokens = (r[32:32 + M] % 3).astype(np.int32)
+        path = oracle.accept_greedy_tree_path(argmax, tokens, parent)
+        out = oracle.accept_greedy_tree(argmax, tokens, parent)
+        assert path[0] == 0 and len(path) == len(out)
+        assert all(parent[path[i]] == path[i - 1] for i in range(1, len(path)))
+        assert list(tokens[path[1:]]) + [argmax[path[-1]]] == list(out)
