@@ -296,6 +296,17 @@ typedef struct {
 sd_status sd_depth_init(sd_depth_state *s, int32_t k_max, int32_t max_pause);
 sd_status sd_depth_update(sd_depth_state *s, int32_t accepted);
 
+/*
+ * The accepted path of a greedy draft tree as node indices (HOST pointers,
+ * no device work): the rule of sd_accept_greedy with a parent array, path
+ * int32 [M] receives the accepted nodes root first (node 0, then each
+ * accepted draft down to the deepest, lowest index among equals).  Returns
+ * the node count n (the accepted token count sd_accept_greedy reports), or -1
+ * for null pointers, M outside 1..16, parent[0] != -1 or parent[i] not in
+ * [0, i).  Copy path to the device for sd_kv_commit.
+ */
+int32_t sd_tree_path(const int32_t *argmax, const int32_t *tokens, const int32_t *parent, int32_t M, int32_t *path);
+
 size_t sd_attn_workspace_bytes(int32_t M, int32_t H, int32_t H_kv, int32_t D, int64_t L);
 sd_status sd_kv_append(const float *k_new, const float *v_new, int32_t M, int32_t H_kv, int32_t D, void *k_cache,
                        void *v_cache, int64_t S_max, int64_t L, sd_stream_t stream);

@@ -87,6 +87,7 @@ def lib():
             "sd_qmatmul_multipos_noalloc": ([I, P, I64, I64, P, P, I32, P, P, U32, I64, P, P, P], I),
             "sd_head_workspace_bytes": ([I64, I64], SZ),
             "sd_head_logits": ([P, I64, I64, P, P, I32, F, P, P, P, P, P, SZ, P], I),
+            "sd_tree_path": ([P, P, P, I32, P], I32),
             "sd_depth_init": ([ctypes.POINTER(SdDepthState), I32, I32], I),
             "sd_depth_update": ([ctypes.POINTER(SdDepthState), I32], I),
             "sd_attn_workspace_bytes": ([I32, I32, I32, I32, I64], SZ),
@@ -211,6 +212,19 @@ def head_logits(w: torch.Tensor, vocab: int, hidden: int, q: torch.Tensor, scale
     M = q.shape[0]
     _check(lib().sd_head_logits(_p(w), vocab, hidden, _p(q), _p(scales), M, temperature, _p(logits), _p(argmax),
                                 _p(row_max), _p(row_sumexp), _p(ws), ws.numel(), _stream()), "sd_head_logits")
+
+
+def tree_path(argmax, tokens, parent):
+    """Accepted nodes of a greedy draft tree, root first (host int32 arrays in, numpy out)."""
+    import numpy as np
+    a = np.ascontiguousarray(argmax, dtype=np.int32)
+    t = np.ascontiguousarray(tokens, dtype=np.int32)
+    p = np.ascontiguousarray(parent, dtype=np.int32)
+    out = np.empty(t.size, dtype=np.int32)
+    n = lib().sd_tree_path(a.ctypes.data, t.ctypes.data, p.ctypes.data, t.size, out.ctypes.data)
+    if n < 0:
+        raise SdError(1, "sd_tree_path")
+    return out[:n].copy()
 
 
 class DepthPolicy:

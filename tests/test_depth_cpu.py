@@ -1,6 +1,7 @@
-"""The library's adaptive draft depth (sd_depth_init / sd_depth_update, host code in
-libsdverify.so) against the oracle's, step for step, on seeded acceptance sequences, plus its
-argument checks.  No GPU: the state machine runs on the host."""
+"""The library's host-side cycle helpers (host code in libsdverify.so) against the oracle: the
+adaptive draft depth (sd_depth_init / sd_depth_update) step for step on seeded acceptance
+sequences, and the accepted tree path (sd_tree_path) on seeded random trees, plus their argument
+checks.  No GPU: both run on the host."""
 import ctypes
 
 import numpy as np
@@ -56,3 +57,24 @@ def test_depth_argument_checks(sdv):
     assert L.sd_depth_update(ctypes.byref(st), -1) == 1
     assert st.k_next == 4                                   # a rejected call changes nothing
     assert L.sd_depth_update(ctypes.byref(st), 2) == 0 and st.k_next == 3
+
+
+def test_tree_path_matches_oracle(sdv):
+    u = sdgen.u32(sdgen.key(101), 300 * 64)
+    for t in range(300):
+        M = 1 + t % 16
+        r = u[t * 64:(t + 1) * 64]
+        parent = np.array([-1] + [int(r[i] % i) for i in range(1, M)], np.int32)
+        argmax = (r[16:16 + M] % 3).astype(np.int32)
+        tokens = (r[32:32 + M] % 3).astype(np.int32)
+        assert list(sdv.tree_path(argmax, tokens, parent)) == list(
+            oracle.accept_greedy_tree_path(argmax, tokens, parent))
+
+
+def test_tree_path_rejects_malformed_trees(sdv):
+    with pytest.raises(sdv.SdError):
+        sdv.tree_path([0, 0], [0, 0], [-1, 1])      # a node as its own parent
+    with pytest.raises(sdv.SdError):
+        sdv.tree_path([0, 0], [0, 0], [0, 0])       # no root
+    with pytest.raises(sdv.SdError):
+        sdv.tree_path([0] * 17, [0] * 17, [-1] + list(range(16)))
