@@ -217,9 +217,13 @@ def head_logits(w: torch.Tensor, vocab: int, hidden: int, q: torch.Tensor, scale
 def tree_path(argmax, tokens, parent):
     """Accepted nodes of a greedy draft tree, root first (host int32 arrays in, numpy out)."""
     import numpy as np
-    a = np.ascontiguousarray(argmax, dtype=np.int32)
-    t = np.ascontiguousarray(tokens, dtype=np.int32)
-    p = np.ascontiguousarray(parent, dtype=np.int32)
+    a = np.ascontiguousarray(argmax, dtype=np.int32).reshape(-1)
+    t = np.ascontiguousarray(tokens, dtype=np.int32).reshape(-1)
+    p = np.ascontiguousarray(parent, dtype=np.int32).reshape(-1)
+    # sd_tree_path reads M entries of each array: refuse mismatched lengths before the call
+    if not (a.size == t.size == p.size) or not 1 <= t.size <= 16:
+        raise SdError(1, f"sd_tree_path: argmax, tokens and parent need one equal length in 1..16 "
+                         f"(got {a.size}, {t.size}, {p.size})")
     out = np.empty(t.size, dtype=np.int32)
     n = lib().sd_tree_path(a.ctypes.data, t.ctypes.data, p.ctypes.data, t.size, out.ctypes.data)
     if n < 0:

@@ -4,6 +4,7 @@ describing the run and an e2e block with no host-device bytes; under torchrun on
 prints.  Runs on the CPU in a few seconds."""
 import json
 import os
+import socket
 import subprocess
 import sys
 
@@ -32,10 +33,17 @@ def test_reference_arm_line():
     assert "workload" in d["config"]
 
 
+def free_port() -> int:
+    """A port the kernel hands out as free right now (bound to port 0, then released)."""
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
 def test_reference_arm_under_two_ranks_prints_once():
     env = os.environ.copy()
     env["MASTER_ADDR"] = "127.0.0.1"
     lines = run(["-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2", "--master-addr", "127.0.0.1",
-                 "--master-port", "29631", "bench.py", "--impl", "reference", "--gpus", "2", "--steps", "1",
+                 "--master-port", str(free_port()), "bench.py", "--impl", "reference", "--gpus", "2", "--steps", "1",
                  "--warmup", "3"], env=env)
     assert len(lines) == 1 and lines[0]["impl"] == "reference"

@@ -78,3 +78,13 @@ def test_tree_path_rejects_malformed_trees(sdv):
         sdv.tree_path([0, 0], [0, 0], [0, 0])       # no root
     with pytest.raises(sdv.SdError):
         sdv.tree_path([0] * 17, [0] * 17, [-1] + list(range(16)))
+
+
+def test_tree_path_rejects_arrays_of_unequal_length(sdv):
+    """The C call reads M entries of each array: shorter argmax or parent arrays are refused on the host."""
+    with pytest.raises(sdv.SdError):
+        sdv.tree_path([0], [0, 0, 0], [-1, 0, 0])   # argmax shorter than tokens
+    with pytest.raises(sdv.SdError):
+        sdv.tree_path([0, 0, 0], [0, 0, 0], [-1, 0])  # parent shorter than tokens
+    with pytest.raises(sdv.SdError):
+        sdv.tree_path([], [], [])                     # empty tree

@@ -291,35 +291,56 @@ def test_stack_pass_batch_invariant_and_accept(sdv, stack_env):
 
 
 def test_tree_pass_batch_invariant(sdv, stack_env):
-    """A 16-node draft tree evaluated as M = 16 rows: each row's logits bit-equal that row alone; the
-    accepted path follows the tree rule on the pass's argmax."""
+    """The 16-node draft tree (root, binary tree of depth 3, one spine node) as M = 16 rows through the
+    64-layer stack and head.  Tree tokens are uniform over the vocabulary except along the path
+    0 -> 1 -> 3 -> 7 -> 15, which follows the ORACLE's argmax chain of its own 64-layer pass.
+    Checks: every one of the 16 rows' logits bit-equal that row run alone (M = 1); the pass's
+    acceptance equals the tree rule on the pass's own argmax; and sd_accept_greedy fed the oracle's
+    argmax accepts exactly what the oracle's tree rule accepts (the whole path plus its bonus)."""
     spec = stack_env["spec"]
     parent, depth = sdgen.tree16(0)
     M = 16
     emb = sdgen.normal(sdgen.key(6, 0), (M, H))
+    # the oracle's own 64-layer pass over the 16 rows: its argmax chain lays out the accepted path
+    h = emb.copy()
+    for l in range(spec.layers):
+        wts = {name: spec.weights(l, name) for name, _, _ in spec.matrices()}
+        n1, n2 = spec.norms(l)
+        h = oracle.stack_layer(h, wts, n1, n2, H, F, spec.wq)
+    _, ao, _, _ = oracle.head(h, spec.final_norm(), spec.head(), V, H)
+    tokens = sdgen.uniform_tokens(sdgen.key(6, 1), M, V)
+    path = (1, 3, 7, 15)
+    for child in path:
+        tokens[child] = ao[parent[child]]
+    tokens = tokens.astype(np.int32)
+    ref = oracle.accept_greedy_tree(ao, tokens, parent)
+    assert list(ref) == [tokens[c] for c in path] + [ao[15]]
+
     st = stack_env["make"](M, parent=cuda(parent))
     hin = cuda(emb)
-    st.h.copy_(hin)
-    st.run()
-    torch.cuda.synchronize()
-    am = host(st.argmax)
-    # tokens uniform over the vocabulary except along the path 0 -> 1 -> 3 -> 7 -> 15, which follows the argmax
-    tokens = sdgen.uniform_tokens(sdgen.key(6, 1), M, V)
-    for child in (1, 3, 7, 15):
-        tokens[child] = am[parent[child]]
-    st.tokens.copy_(cuda(tokens.astype(np.int32)))
+    st.tokens.copy_(cuda(tokens))
     run_graph(st, hin)
     status_ok()
-    lg = host(st.logits)
+    lg, am = host(st.logits), host(st.argmax)
     n = int(host(st.out_count)[0])
-    kept = list(host(st.out_tokens)[:n])
-    assert kept == [tokens[1], tokens[3], tokens[7], tokens[15], am[15]]
-    for m in (0, 3, 7, 15):
-        s1 = stack_env["make"](1)
+    assert list(host(st.out_tokens)[:n]) == list(oracle.accept_greedy_tree(am, tokens, parent))
+    print(f"\ntree pass vs oracle argmax: {int((am == ao).sum())}/{M} rows agree")
+
+    # config-5 acceptance, integer work fed the oracle's argmax: bit-exact against the oracle's rule
+    ot = torch.full((M,), -1, dtype=torch.int32, device="cuda")
+    oc = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sdv.accept_greedy(cuda(ao.astype(np.int32)), cuda(tokens), cuda(parent), M, ot, oc)
+    status_ok()
+    assert list(host(ot)[:int(host(oc)[0])]) == list(ref)
+
+    # every row of the M = 16 pass bit-equal to that row alone (one M = 1 stack, reused)
+    s1 = stack_env["make"](1)
+    for m in range(M):
         run_graph(s1, hin[m:m + 1])
         status_ok()
-        assert np.array_equal(host(s1.logits).view(np.uint32), lg[m:m + 1].view(np.uint32))
-        del s1
+        assert np.array_equal(host(s1.logits).view(np.uint32), lg[m:m + 1].view(np.uint32)), m
+        assert int(host(s1.argmax)[0]) == am[m]
+    del s1
 
 
 @pytest.mark.parametrize("M", [5, 16])

@@ -179,6 +179,51 @@ def test_rmsnorm_constant_row_closed_form():
     assert np.all(np.abs(deq - closed.reshape(1, K // 32, 32)) <= s[..., None] * (0.5 + 1e-5))
 
 
+@pytest.mark.parametrize("c", [0.5, -4.0, 2.0 ** -20])
+def test_rmsnorm_power_of_two_row_normalises_to_w_exactly(c):
+    """Closed form with every step exact: a constant row x = c = +-2^k with eps = 0 has mean square
+    c^2 (exact partial sums), inv = 1/|c| (a power of two), so the normalised row is sign(c) w
+    exactly; its block scales are exactly fl(max|w| / 127) and its codes the requantisation of
+    sign(c) w.  A wrong divisor of the mean, a missing square root or a misplaced row factor
+    changes the scales."""
+    K = 5120
+    x = np.full((2, K), c, dtype=np.float32)
+    w = sdgen.norm_weight(sdgen.key(5, 1), K)
+    q, s = oracle.rmsnorm_quant(x, w, 0.0)
+    yn = (np.sign(c) * w).astype(np.float32)
+    qr, sr = oracle.rmsnorm_quant(np.vstack([yn, yn]), None)  # requantisation alone of sign(c) w
+    d = (np.abs(w.reshape(K // 32, 32)).max(axis=1) / np.float32(127.0)).astype(np.float32)
+    assert np.array_equal(s[0], d) and np.array_equal(s[1], d)
+    assert np.array_equal(sr[0], d)
+    assert np.array_equal(q, qr)
+    assert np.all(np.abs(q.reshape(2, K // 32, 32)).max(axis=2) == 127)
+
+
+def test_rmsnorm_codes_equal_the_plain_definition_except_at_ties():
+    """Reading R4 forms the codes from t = x w and the scale as inv max|t| / 127; the plain
+    definition requantises y = (x inv) w.  On the bench's input rows at the RMSNorm sites of the
+    oracle's own pass: live on the first four layers, and from the stored statistics of all 129
+    sites of the 64-layer stack (tests/golden/make_rmsnorm_ties.py, which calls only the oracle).
+    Every code that differs differs by one step and sits within TIE of a half-integer of the plain
+    quotient; scales agree within 4 fp32 ulps (the two orders' few roundings)."""
+    import json
+    import os
+
+    from _rmsnorm_ties import TIE, compare_site, stack_sites
+    spec = sdgen.StackSpec()
+    live = [dict(compare_site(x, w, sdgen.EPS), site=n) for n, x, w in stack_sites(spec, 5, 4)]
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "rmsnorm_ties_27b_stack_m5.json")))
+    sites = g["sites"]
+    assert len(sites) == 2 * spec.layers + 1 and g["tie_band"] == TIE
+    assert live == sites[:len(live)]  # the stored statistics are those of the current oracle
+    for r in live + sites:
+        assert r["max_step"] <= 1, r
+        assert r["max_tie_distance_of_differing"] <= TIE, r
+        assert r["max_scale_ulps"] <= 4.0, r
+    assert g["total_differing"] == sum(r["differing"] for r in sites)
+    assert g["tie_rate"] < 1e-5
+
+
 @pytest.mark.parametrize("K", [1024, 5120, 17408])
 def test_rmsnorm_quant_vs_float64_definition(K):
     M = 3
