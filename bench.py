@@ -244,7 +244,8 @@ def oracle_sample(spec, M, budget_s=12.0, max_layers=64):
             break
     return {"value": nbytes / t_total / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"{layers} layer(s) of the 64-layer stack at M={M} (all four 4-bit matrices, "
-                      f"{nbytes / 1e6:.0f} MB of weights), {t_total:.1f} s"}
+                      f"{nbytes / 1e6:.0f} MB of weights, {nbytes / spec.weight_bytes():.1%} of the pass's bytes; "
+                      f"the Q8_0 head is not in the sample), {t_total:.1f} s"}
 
 
 def reference_arm(args, spec, M):
@@ -449,6 +450,120 @@ def attention_bench(args, local):
         "peak_gbs": peak, "peak_kind": peak_kind, "cases": cases}))
 
 
+def write_trace(path, stack, h_dev, sdv):
+    """One traced pass (the same launch as the timed one, with per-phase stamps) -> .npz with the SM id
+    of each CTA, the stamps [phase][cta][6] relative to the earliest stamp, and each phase's kind."""
+    import numpy as np
+    import torch
+
+    p = stack.fused
+    n = sdv.pass_trace_bytes(p) // 8
+    tr = torch.zeros(n, dtype=torch.int64, device=h_dev.device)
+    stack.h.copy_(h_dev)
+    sdv.verify_pass_traced(p, tr)
+    torch.cuda.synchronize()
+    t = tr.cpu().numpy()
+    G, P = p.grid, p.n_phases
+    smid = t[:G].copy()
+    raw = t[G:G + P * G * 9].reshape(P, G, 9)
+    st = raw[:, :, :6].astype(np.float64)
+    t0 = st[st > 0].min()
+    st = np.where(st > 0, st - t0, np.nan)
+    np.savez(path, smid=smid, stamps=st, cycles=raw[:, :, 6:].astype(np.float64))
+    log(f"trace: {P} phases x {G} CTAs written to {path}")
+
+
+CASES = ("qkv", "o", "gate_up", "down", "head", "rmsnorm", "pass")
+
+
+def case_bench(args, local):
+    """One kernel on one seeded layer-sized case, for profiling: qkv (4-bit 5120->15360, V requant
+    epilogue), o (4-bit 5120->5120 + residual), gate_up (4-bit 5120->2x17408, SiLU*mul requant),
+    down (4-bit 17408->5120 + residual), head (Q8_0 5120->151936 with argmax and statistics),
+    rmsnorm (M x 5120), or pass (the one-launch pass over --layers layers plus the head).  Runs
+    --steps launches after one untimed launch and prints one line: mean event-timed duration per
+    launch and weight-stream GB/s."""
+    import numpy as np
+    import torch
+
+    import sdgen
+    from speculative_decoding_verify_gb300 import build as b
+    b.build()
+    sdgen.build()
+    import speculative_decoding_verify_gb300 as sdv
+
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    H, F, V = sdgen.HIDDEN, sdgen.FFN, sdgen.VOCAB
+    M = args.M
+    mats = {"qkv": (sdv.Q4_32, 3 * H, H, sdv.EPI_REQUANT), "o": (sdv.Q4_32, H, H, sdv.EPI_NONE),
+            "gate_up": (sdv.Q4_32, 2 * F, H, sdv.EPI_SILU_MUL_REQUANT), "down": (sdv.Q4_32, H, F, sdv.EPI_NONE),
+            "head": (sdv.Q8_0, V, H, None)}
+    if args.case == "pass":
+        spec = sdgen.StackSpec(layers=args.layers)
+        stack = build_stack(spec, M, dev, {})
+        h0 = torch.from_numpy(spec.hidden_in(M)).to(dev)
+        stack.prepare_fused()
+
+        def run():
+            stack.h.copy_(h0)
+            stack.run_fused()
+        nbytes = spec.weight_bytes()
+    elif args.case == "rmsnorm":
+        x = torch.from_numpy(sdgen.normal(sdgen.key(9, 0), (M, H))).to(dev)
+        w = torch.from_numpy(sdgen.norm_weight(sdgen.key(9, 1), H)).to(dev)
+        q = torch.zeros((M, H), dtype=torch.int8, device=dev)
+        sc = torch.zeros((M, H // 32), dtype=torch.float32, device=dev)
+        run = lambda: sdv.rmsnorm_quant_acts(x, w, q, sc)  # noqa: E731
+        nbytes = 0
+    else:
+        qtype, n, k, epi = mats[args.case]
+        blocks = sdgen.pinned_quantized_normal(qtype, sdgen.key(9, 2, n, k), n, k)
+        w = sdv.repack_weights(qtype, blocks.to(dev).reshape(-1), n, k, pair=(epi == sdv.EPI_SILU_MUL_REQUANT))
+        xq = torch.from_numpy(sdgen.normal(sdgen.key(9, 3), (M, k))).to(dev)
+        q = torch.zeros((M, k), dtype=torch.int8, device=dev)
+        sc = torch.zeros((M, k // 32), dtype=torch.float32, device=dev)
+        sdv.rmsnorm_quant_acts(xq, None, q, sc)
+        nbytes = n * (k // 32) * sdv.BLOCK_BYTES[qtype]
+        y = torch.zeros((M, n), dtype=torch.float32, device=dev)
+        if args.case == "head":
+            ws = sdv.workspace(sdv.head_workspace_bytes(n, k), dev)
+            am = torch.zeros(M, dtype=torch.int32, device=dev)
+            rm = torch.zeros(M, dtype=torch.float32, device=dev)
+            rz = torch.zeros(M, dtype=torch.float32, device=dev)
+            run = lambda: sdv.head_logits(w, n, k, q, sc, ws, y, am, rm, rz)  # noqa: E731
+        else:
+            ws = sdv.workspace(sdv.qmatmul_workspace_bytes(qtype, n, k, epi), dev)
+            if epi == sdv.EPI_REQUANT:
+                qn = torch.zeros((M, n - 2 * H), dtype=torch.int8, device=dev)
+                sn = torch.zeros((M, (n - 2 * H) // 32), dtype=torch.float32, device=dev)
+                run = lambda: sdv.qmatmul_multipos(qtype, w, n, k, q, sc, ws, y=y, epilogue=epi,  # noqa: E731
+                                                   requant_col0=2 * H, q_next=qn, scales_next=sn)
+            elif epi == sdv.EPI_SILU_MUL_REQUANT:
+                qn = torch.zeros((M, n // 2), dtype=torch.int8, device=dev)
+                sn = torch.zeros((M, n // 64), dtype=torch.float32, device=dev)
+                run = lambda: sdv.qmatmul_multipos(qtype, w, n, k, q, sc, ws, epilogue=epi,  # noqa: E731
+                                                   q_next=qn, scales_next=sn)
+            else:
+                run = lambda: sdv.qmatmul_multipos(qtype, w, n, k, q, sc, ws, y=y, residual=y)  # noqa: E731
+    torch.cuda.synchronize()
+    run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    st = sdv.device_status()
+    gbs = nbytes / (ms * 1e-3) / 1e9 if nbytes else 0.0
+    print(f"case={args.case} M={M} launches={args.steps} ms_per_launch={ms:.4f} weight_bytes={nbytes} "
+          f"GB/s={gbs:.1f} status={st}", flush=True)
+    if st != 0:
+        raise SystemExit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -467,6 +582,11 @@ def main():
                     help="instead of the pass: time the decode attention over the K+1 positions (own JSON line)")
     ap.add_argument("--shortlist", action="store_true",
                     help="instead of the pass: time the exact shortlist head against the full head (own JSON line)")
+    ap.add_argument("--trace", default=None, metavar="FILE",
+                    help="after the timed region, run one traced pass and write its per-phase, per-CTA "
+                         "global-timer stamps (numpy .npz) to FILE")
+    ap.add_argument("--case", default=None, choices=CASES,
+                    help="instead of the pass: run one kernel on one layer-sized case --steps times, for profiling")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -481,6 +601,9 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             reference_arm(args, spec, M)
+        return
+    if args.case:
+        case_bench(args, local)
         return
     if args.shortlist:
         shortlist_bench(args, local)
@@ -622,6 +745,9 @@ def main():
     e2e_ms = max_over_ranks(e2e_ms, dist, device)
     h2d = h_host.numel() * 4 + d_host.numel() * 4
     d2h = out_host.numel() * 4 + cnt_host.numel() * 4
+
+    if args.trace and rank == 0:
+        write_trace(args.trace, stack, h_dev, sdv)
 
     # per-kernel durations of the per-operation pipeline (one eagerly launched pass, events between launches)
     prof = None

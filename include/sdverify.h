@@ -474,6 +474,22 @@ size_t sd_pass_workspace_bytes(int64_t hidden, int64_t ffn, int64_t vocab, int32
 sd_status sd_pass_prepare(const sd_pass_desc *desc, void *plan, size_t plan_bytes, sd_pass *out);
 sd_status sd_verify_pass(const sd_pass *pass, sd_stream_t stream);
 
+/* Tracing (no counterpart on the pages; a profiling aid, since a persistent
+ * launch hides its phases from host-side tools): the same pass as
+ * sd_verify_pass, plus global-timer stamps (nanoseconds) written into `trace`
+ * (device, 8-byte aligned, >= sd_pass_trace_bytes(pass) bytes, caller-owned).
+ * Layout, uint64: trace[c] = SM id of CTA c for c < grid; then for phase p and
+ * CTA c 9 values at grid + (p * grid + c) * 9.  Global-timer stamps: the phase
+ * begins (grid barrier passed), the consumers hold their first activations
+ * (matmul phases), the consumers leave the phase, the phase ends, and the
+ * producer starts and finishes issuing the phase's weight copies (matmul
+ * phases).  Then SM cycles one consumer warp spent in the phase waiting for
+ * weight stages, computing records, and handing partial sums on.  Values a
+ * phase does not reach are left as they were.  Results equal sd_verify_pass's.
+ * SD_EINVAL for a null, misaligned or short buffer. */
+size_t sd_pass_trace_bytes(const sd_pass *pass);
+sd_status sd_verify_pass_traced(const sd_pass *pass, uint64_t *trace, size_t trace_bytes, sd_stream_t stream);
+
 /* Synchronises `stream`, returns and clears the current device's status word
  * (SD_OK, SD_ETIMEOUT or SD_EDEVICE); SD_ECUDA if synchronising failed. */
 sd_status sd_device_status(sd_stream_t stream);

@@ -112,6 +112,8 @@ def lib():
             "sd_pass_workspace_bytes": ([I64, I64, I64, I32], SZ),
             "sd_pass_prepare": ([ctypes.POINTER(SdPassDesc), P, SZ, ctypes.POINTER(SdPass)], I),
             "sd_verify_pass": ([ctypes.POINTER(SdPass), P], I),
+            "sd_pass_trace_bytes": ([ctypes.POINTER(SdPass)], ctypes.c_size_t),
+            "sd_verify_pass_traced": ([ctypes.POINTER(SdPass), P, ctypes.c_size_t, P], I),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -349,6 +351,17 @@ def pass_prepare(desc: SdPassDesc, plan: torch.Tensor) -> SdPass:
 
 def verify_pass(p: SdPass):
     _check(lib().sd_verify_pass(ctypes.byref(p), _stream()), "sd_verify_pass")
+
+
+def pass_trace_bytes(p: SdPass) -> int:
+    return int(lib().sd_pass_trace_bytes(ctypes.byref(p)))
+
+
+def verify_pass_traced(p: SdPass, trace: torch.Tensor):
+    """sd_verify_pass with per-phase global-timer stamps into `trace` (int64 CUDA tensor of at least
+    pass_trace_bytes(p) bytes): SM ids of the grid's CTAs, then 6 stamps per (phase, CTA)."""
+    _check(lib().sd_verify_pass_traced(ctypes.byref(p), _p(trace), trace.numel() * trace.element_size(), _stream()),
+           "sd_verify_pass_traced")
 
 
 # ---------------------------------------------------------------------------

@@ -18,11 +18,11 @@ struct PassHeader {
     uint32_t pad[63];
 };
 
-static cudaError_t pass_launch(const QmmArgs *phases, int n_phases, uint32_t *ctr, int nt, int sample, size_t smem,
-                               int grid, cudaStream_t s) {
-    if (sample) return pass_launch_sampling(phases, n_phases, ctr, nt, smem, grid, s);
-    return pass_launch_kernel(nt == 1 ? pass_kernel<1, false> : pass_kernel<2, false>, phases, n_phases, ctr, smem,
-                              grid, s);
+static cudaError_t pass_launch(const QmmArgs *phases, int n_phases, uint32_t *ctr, uint64_t *trace, int nt,
+                               int sample, size_t smem, int grid, cudaStream_t s) {
+    if (sample) return pass_launch_sampling(phases, n_phases, ctr, trace, nt, smem, grid, s);
+    return pass_launch_kernel(nt == 1 ? pass_kernel<1, false> : pass_kernel<2, false>, phases, n_phases, ctr, trace,
+                              smem, grid, s);
 }
 
 }  // namespace sdv
@@ -316,18 +316,30 @@ sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, 
     return SD_OK;
 }
 
-sd_status sd_verify_pass(const sd_pass *p, sd_stream_t stream) {
+static sd_status verify_pass_launch(const sd_pass *p, uint64_t *trace, sd_stream_t stream) {
     if (!p || !p->plan || p->n_phases < 1 || (p->nt != 1 && p->nt != 2) || p->grid < 1 ||
         (p->accept != SD_ACCEPT_GREEDY && p->accept != SD_ACCEPT_SAMPLE))
         return SD_EINVAL;
     uint8_t *plan = static_cast<uint8_t *>(p->plan);
     const QmmArgs *phases = reinterpret_cast<const QmmArgs *>(plan + sizeof(PassHeader));
     uint32_t *ctr = reinterpret_cast<uint32_t *>(plan);
-    return pass_launch(phases, p->n_phases, ctr, p->nt, p->accept, p->smem_bytes, p->grid,
-                       reinterpret_cast<cudaStream_t>(stream)) ==
-                   cudaSuccess
+    return pass_launch(phases, p->n_phases, ctr, trace, p->nt, p->accept, p->smem_bytes, p->grid,
+                       reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? SD_OK
                : SD_ECUDA;
+}
+
+sd_status sd_verify_pass(const sd_pass *p, sd_stream_t stream) { return verify_pass_launch(p, nullptr, stream); }
+
+size_t sd_pass_trace_bytes(const sd_pass *p) {
+    if (!p || p->n_phases < 1 || p->grid < 1) return 0;
+    return (static_cast<size_t>(p->grid) + static_cast<size_t>(p->n_phases) * p->grid * TR_SLOTS) * sizeof(uint64_t);
+}
+
+sd_status sd_verify_pass_traced(const sd_pass *p, uint64_t *trace, size_t trace_bytes, sd_stream_t stream) {
+    if (!trace || !aligned(trace, 8) || trace_bytes < sd_pass_trace_bytes(p) || sd_pass_trace_bytes(p) == 0)
+        return SD_EINVAL;
+    return verify_pass_launch(p, trace, stream);
 }
 
 }  // extern "C"

@@ -4,10 +4,10 @@
 
 namespace sdv {
 
-cudaError_t pass_launch_sampling(const QmmArgs *phases, int n_phases, uint32_t *ctr, int nt, size_t smem, int grid,
-                                 cudaStream_t s) {
-    return pass_launch_kernel(nt == 1 ? pass_kernel<1, true> : pass_kernel<2, true>, phases, n_phases, ctr, smem,
-                              grid, s);
+cudaError_t pass_launch_sampling(const QmmArgs *phases, int n_phases, uint32_t *ctr, uint64_t *trace, int nt,
+                                 size_t smem, int grid, cudaStream_t s) {
+    return pass_launch_kernel(nt == 1 ? pass_kernel<1, true> : pass_kernel<2, true>, phases, n_phases, ctr, trace,
+                              smem, grid, s);
 }
 
 }  // namespace sdv

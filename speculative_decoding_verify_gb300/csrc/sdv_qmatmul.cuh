@@ -166,6 +166,15 @@ struct QmmArgs {
 
 constexpr int KIND_MATMUL = 0, KIND_NORM = 1, KIND_ACCEPT = 2, KIND_COMBINE = 3, KIND_HSTATS = 4;
 
+// Optional per-phase trace of the one-launch pass: after the SM ids of the G CTAs, TR_SLOTS values per
+// (phase, CTA).  Global-timer nanoseconds: the phase begins (grid barrier passed), the consumers hold
+// their first activations, the consumers leave the phase, the phase ends (every role done), and the
+// producer starts and finishes issuing the phase's weight copies.  SM cycles spent by consumer warp 0
+// in the phase: waiting for weight stages, computing records, and handing partial sums to the
+// finishers (waiting for a free slot included).
+constexpr int TR_START = 0, TR_ACT = 1, TR_CONS_END = 2, TR_END = 3, TR_PROD_FIRST = 4, TR_PROD_LAST = 5,
+              TR_CYC_WAIT = 6, TR_CYC_COMP = 7, TR_CYC_HAND = 8, TR_SLOTS = 9;
+
 // fetch-and-add with release (orders the writes seen through a barrier) and acquire
 __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v) {
     uint32_t old;
@@ -752,7 +761,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, CtaSha
 // the whole launch (slot it % NS, phase parity it / NS), `npub` pieces.
 // ---------------------------------------------------------------------------
 __device__ inline void produce_phase(const QmmArgs &a, const Smem &sm, uint32_t &it, uint32_t &npub, CtaShared &cs,
-                                     uint64_t pol) {
+                                     uint64_t pol, uint64_t *tslot = nullptr) {
+    if (tslot) tslot[TR_PROD_FIRST] = gtimer_ns();
     PieceIter pit;
     pieces_begin(a, pit);
     Piece pc, nx;
@@ -805,6 +815,7 @@ __device__ inline void produce_phase(const QmmArgs &a, const Smem &sm, uint32_t 
         pc = nx;
         have = more;
     }
+    if (tslot) tslot[TR_PROD_LAST] = gtimer_ns();
 }
 
 // never leave with copies in flight: wait for the last issued stages
@@ -1014,7 +1025,8 @@ __device__ inline bool pre_issue_staging(const QmmArgs &a, const Smem &sm, uint3
 // ---------------------------------------------------------------------------
 template <int QT, int PAIR, int NT>
 __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t &it, uint32_t &pk, uint32_t &act_it,
-                                     uint32_t &nrm_it, CtaShared &cs, bool pre_issued = false) {
+                                     uint32_t &nrm_it, CtaShared &cs, bool pre_issued = false,
+                                     uint64_t *tslot = nullptr) {
     const int M = a.M;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int lg = lane >> 2, lc = lane & 3;
@@ -1024,6 +1036,8 @@ __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
     const uint32_t NS = static_cast<uint32_t>(a.NS), NRB = static_cast<uint32_t>(a.NRB), sstride = a.stage_stride;
     uint32_t stg = it % NS, sph = (it / NS) & 1u;  // ring slot and phase parity of stage `it`
     int cur_s = -1;
+    const bool tr = tslot != nullptr && threadIdx.x == 0;  // consumer warp 0 keeps the cycle accounts
+    long long c_wait = 0, c_comp = 0, c_hand = 0, c0 = 0;
     float2 inv[NT];  // RMSNorm row factors of this lane's positions 8nt + 2c, +1 (1 when not normalised)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) inv[nt] = make_float2(1.0f, 1.0f);
@@ -1032,7 +1046,9 @@ __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
             cs.abort = 1;
         }
         // the next piece's descriptor rides with its first stage
+        if (tr) c0 = clock64();
         if (!warp_wait(&sm.full[stg], sph, cs, a.status)) return false;
+        if (tr) c_wait += clock64() - c0;
         const QPiece pc = cs.pq[pk % PQ_N];
         const int s = pc.s, j0 = pc.j0, j1 = pc.j1;
 
@@ -1062,6 +1078,7 @@ __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
                 if (!warp_wait(sm.act_bar, act_it & 1u, cs, a.status)) return false;
             }
             ++act_it;
+            if (tslot && cur_s < 0 && threadIdx.x == 0) tslot[TR_ACT] = gtimer_ns();
             if (a.af_norm) {
                 // the row factors, one warp per row (warp w: rows w, w + 8), published through
                 // inv_bar; applied to the block scales as they are loaded: d_a = inv * max|x w| / 127
@@ -1107,7 +1124,13 @@ __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
 
         for (int jj = j0; jj < j1; jj += SB) {
             const int n = j1 - jj < SB ? j1 - jj : SB;
+            if (tr) c0 = clock64();
             if (jj != j0 && !warp_wait(&sm.full[stg], sph, cs, a.status)) return false;
+            if (tr) {
+                const long long c1 = clock64();
+                c_wait += c1 - c0;
+                c0 = c1;
+            }
             const uint8_t *sbase = sm.ring + static_cast<size_t>(stg) * sstride;
             const uint32_t done = stg;
             ++it;
@@ -1128,9 +1151,11 @@ __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.empty[done]);
+            if (tr) c_comp += clock64() - c0;
         }
 
         // hand the piece's partial sums to the finishers
+        if (tr) c0 = clock64();
         const uint32_t b = pk % NRB, use = pk / NRB;
         ++pk;
         if (!warp_wait(&sm.rempty[b], (use & 1u) ^ 1u, cs, a.status)) return false;
@@ -1149,9 +1174,16 @@ __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
                 }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.rfull[b]);
+        if (tr) c_hand += clock64() - c0;
         if (pc.last) break;
     }
     if (lane == 0) mbar_arrive(sm.act_free);  // done with this phase's last split
+    if (tr) {
+        tslot[TR_CONS_END] = gtimer_ns();
+        tslot[TR_CYC_WAIT] = static_cast<uint64_t>(c_wait);
+        tslot[TR_CYC_COMP] = static_cast<uint64_t>(c_comp);
+        tslot[TR_CYC_HAND] = static_cast<uint64_t>(c_hand);
+    }
     return !cs.abort;
 }
 
@@ -1592,7 +1624,7 @@ __device__ __forceinline__ void pass_topk_accept(const QmmArgs &sa, uint8_t *scr
 
 template <int NT, bool SAMPLE>
 __global__ void __launch_bounds__(QMM_THREADS, 1)
-    pass_kernel(const QmmArgs *__restrict__ phases, int n_phases, uint32_t *barrier_ctr) {
+    pass_kernel(const QmmArgs *__restrict__ phases, int n_phases, uint32_t *barrier_ctr, uint64_t *trace) {
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ CtaShared cs;
     __shared__ QmmArgs sa;  // the current phase, copied from global memory
@@ -1603,12 +1635,22 @@ __global__ void __launch_bounds__(QMM_THREADS, 1)
     if (tid == 0) cta_init(sm, a0.NS, cs, 1u);
     __syncthreads();
     uint32_t it = 0, pk = 0, act_it = 0, nrm_it = 0, fin_it = 0;
+    const int G = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
+    // this CTA's stamps of phase p (nullptr when not tracing)
+    auto tslot = [&](int p) -> uint64_t * {
+        return trace ? trace + G + (static_cast<int64_t>(p) * G + cta) * TR_SLOTS : nullptr;
+    };
+    if (trace && tid == 0) {
+        uint32_t smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        trace[cta] = smid;
+    }
     if (warp == PRODUCER_WARP) {
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
             uint32_t npub = 0;
             for (int p = 0; p < n_phases && !cs.abort; ++p)
-                if (phases[p].kind == KIND_MATMUL) produce_phase(phases[p], sm, it, npub, cs, pol);
+                if (phases[p].kind == KIND_MATMUL) produce_phase(phases[p], sm, it, npub, cs, pol, tslot(p));
             producer_drain(sm, it, a0.NS);
         }
         return;
@@ -1636,6 +1678,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1)
                 }
             }
             if (!stop) pre = pre_issue_staging(sa, sm, act_it, cs);
+            if (trace) tslot(p)[TR_START] = gtimer_ns();
         }
         if (bar_any(BAR_WORK, WORK_THREADS, stop)) {
             cs.abort = 1;
@@ -1671,24 +1714,28 @@ __global__ void __launch_bounds__(QMM_THREADS, 1)
             const int f = warp - FIN_WARP0;
             ok = sa.pair ? finish_phase<1, NT>(sa, sm, pk, fin_it, cs, f) : finish_phase<0, NT>(sa, sm, pk, fin_it, cs, f);
         } else if (sa.qt == SD_Q4_32 && sa.pair) {
-            ok = consume_phase<SD_Q4_32, 1, NT>(sa, sm, it, pk, act_it, nrm_it, cs, pre);
+            ok = consume_phase<SD_Q4_32, 1, NT>(sa, sm, it, pk, act_it, nrm_it, cs, pre, tslot(p));
         } else if (sa.qt == SD_Q4_32) {
-            ok = consume_phase<SD_Q4_32, 0, NT>(sa, sm, it, pk, act_it, nrm_it, cs, pre);
+            ok = consume_phase<SD_Q4_32, 0, NT>(sa, sm, it, pk, act_it, nrm_it, cs, pre, tslot(p));
         } else {
-            ok = consume_phase<SD_Q8_0, 0, NT>(sa, sm, it, pk, act_it, nrm_it, cs, pre);
+            ok = consume_phase<SD_Q8_0, 0, NT>(sa, sm, it, pk, act_it, nrm_it, cs, pre, tslot(p));
         }
         // every write of phase p (consumers and finishers) before thread 0's release
         if (bar_any(BAR_WORK, WORK_THREADS, !ok)) {
             cs.abort = 1;
             return;
         }
-        if (tid == 0) red_release_add(barrier_ctr, 1u);
+        if (tid == 0) {
+            if (trace) tslot(p)[TR_END] = gtimer_ns();
+            red_release_add(barrier_ctr, 1u);
+        }
     }
 }
 
 // One cooperative launch of a pass kernel: every CTA resident at once, or the launch fails.
-inline cudaError_t pass_launch_kernel(void (*k)(const QmmArgs *, int, uint32_t *), const QmmArgs *phases,
-                                      int n_phases, uint32_t *ctr, size_t smem, int grid, cudaStream_t s) {
+inline cudaError_t pass_launch_kernel(void (*k)(const QmmArgs *, int, uint32_t *, uint64_t *), const QmmArgs *phases,
+                                      int n_phases, uint32_t *ctr, uint64_t *trace, size_t smem, int grid,
+                                      cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     e = cudaMemsetAsync(ctr, 0, sizeof(uint32_t), s);
@@ -1703,12 +1750,12 @@ inline cudaError_t pass_launch_kernel(void (*k)(const QmmArgs *, int, uint32_t *
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k, phases, n_phases, ctr);
+    return cudaLaunchKernelEx(&cfg, k, phases, n_phases, ctr, trace);
 }
 
 // the sampling instantiations, compiled in their own translation unit (sdv_pass_sample.cu)
-cudaError_t pass_launch_sampling(const QmmArgs *phases, int n_phases, uint32_t *ctr, int nt, size_t smem, int grid,
-                                 cudaStream_t s);
+cudaError_t pass_launch_sampling(const QmmArgs *phases, int n_phases, uint32_t *ctr, uint64_t *trace, int nt,
+                                 size_t smem, int grid, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // host side: plan + launch
