@@ -212,6 +212,7 @@ sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, 
         normed_input(a);
         a->epi = SD_EPI_REQUANT;
         a->col0 = 2 * H;
+        if (a->NU % 3 == 0) a->ilv3 = a->NU / 3;  // V tiles spread over the CTAs, V first
         a->q_next = d->qv;
         a->s_next = d->sv;
         a->nq = H;

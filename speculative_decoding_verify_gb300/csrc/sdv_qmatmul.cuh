@@ -162,6 +162,7 @@ struct QmmArgs {
     int64_t base_pos;
     int32_t top_k;          // sampling: 0 unfiltered, else the top-k / top-p filtered target
     float top_p;
+    int32_t ilv3;           // 0, or NU / 3: units taken in threes from the three thirds of the rows (see phys_unit)
 };
 
 constexpr int KIND_MATMUL = 0, KIND_NORM = 1, KIND_ACCEPT = 2, KIND_COMBINE = 3, KIND_HSTATS = 4;
@@ -180,6 +181,16 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v) {
     uint32_t old;
     asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
     return old;
+}
+
+// Row tile (32 rows, or a gate|up tile pair) of schedule unit u.  The identity, except for a matmul whose
+// requantising epilogue covers the last third of its rows only (the V columns of a fused QKV
+// projection): there units are taken in threes, one tile from each third, the requantised one first,
+// so every CTA finishes an equal share of requantised tiles and its last unit has no epilogue work.
+__host__ __device__ __forceinline__ int phys_unit(const QmmArgs &a, int u) {
+    if (!a.ilv3) return u;
+    const int r = u % 3, q = u / 3;
+    return (r == 0 ? 2 : r - 1) * a.ilv3 + q;
 }
 
 __host__ __device__ __forceinline__ void decode_step(const QmmArgs &a, int64_t g, int &s, int &u, int &j, int &len) {
@@ -807,7 +818,8 @@ __device__ inline void produce_phase(const QmmArgs &a, const Smem &sm, uint32_t 
             }
             const uint32_t bytes = static_cast<uint32_t>(n) * a.step_bytes;
             const uint8_t *src =
-                a.w + (static_cast<int64_t>(u) * a.KB + static_cast<int64_t>(s) * a.KBs + jj) * a.step_bytes;
+                a.w + (static_cast<int64_t>(phys_unit(a, u)) * a.KB + static_cast<int64_t>(s) * a.KBs + jj) *
+                          a.step_bytes;
             mbar_arrive_expect_tx(&sm.full[stg], bytes);
             bulk_g2s(sm.ring + static_cast<size_t>(stg) * a.stage_stride, src, bytes, &sm.full[stg], pol);
             ++it;
@@ -920,6 +932,16 @@ __device__ __forceinline__ float warp_row_inv(const QmmArgs &a, const Smem &sm, 
     return __shfl_sync(0xffffffffu, inv, 0);
 }
 
+// The four fp16 row scales of a lane's group (rows g, g+8, 16+g, 24+g) as pairs (w, w), ready to
+// multiply a lane's two positions at once.
+__device__ __forceinline__ void row_scale_pairs(uint2 sw, float2 (&wr)[4]) {
+    const __half2 h01 = *reinterpret_cast<const __half2 *>(&sw.x), h23 = *reinterpret_cast<const __half2 *>(&sw.y);
+    wr[0] = __half22float2(__low2half2(h01));
+    wr[1] = __half22float2(__high2half2(h01));
+    wr[2] = __half22float2(__low2half2(h23));
+    wr[3] = __half22float2(__high2half2(h23));
+}
+
 // steps one call of stage_compute covers when full: 32 records of 4-bit, 16 gate|up pairs or Q8_0 records
 __host__ __device__ constexpr int sub_steps(int qtype, int pair) { return pair ? 2 * NCW : (qtype == SD_Q8_0 ? 2 * NCW : 4 * NCW); }
 
@@ -947,52 +969,54 @@ __device__ __forceinline__ void stage_compute(const uint8_t *sbase, int n, int j
         const uint8_t *rp = sbase + r * STEP;
         const int jb = jb0 + r;
         uint32_t af[2][2][4], afu[2][2][4];
-        float2 w01, w23, u01, u23;  // scales of rows g, g+8 and 16+g, 24+g
+        float2 wr[4], ur[4];  // scales of rows g, g+8, 16+g, 24+g, each as a pair (w, w)
         if (QT == SD_Q4_32) q4_frag(*reinterpret_cast<const uint4 *>(rp + lane * 16), af);
         else q8_frag(*reinterpret_cast<const uint4 *>(rp + lane * 16), *reinterpret_cast<const uint4 *>(rp + 512 + lane * 16), af);
-        {
-            const uint2 sw = *reinterpret_cast<const uint2 *>(rp + CODE + lg * 8);
-            w01 = __half22float2(*reinterpret_cast<const __half2 *>(&sw.x));
-            w23 = __half22float2(*reinterpret_cast<const __half2 *>(&sw.y));
-        }
+        row_scale_pairs(*reinterpret_cast<const uint2 *>(rp + CODE + lg * 8), wr);
         if (PAIR) {
             q4_frag(*reinterpret_cast<const uint4 *>(rp + REC + lane * 16), afu);
-            const uint2 sw = *reinterpret_cast<const uint2 *>(rp + REC + CODE + lg * 8);
-            u01 = __half22float2(*reinterpret_cast<const __half2 *>(&sw.x));
-            u23 = __half22float2(*reinterpret_cast<const __half2 *>(&sw.y));
+            row_scale_pairs(*reinterpret_cast<const uint2 *>(rp + REC + CODE + lg * 8), ur);
         }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             uint4 bf;
             if (NT == 1) {
-                bf = lg < M ? act4[jb * 4 * M + lane] : make_uint4(0u, 0u, 0u, 0u);
+                // lanes of padding positions (lg >= M) read whatever fragment follows in shared memory
+                // (the next block's, or the {corr, d_a} pairs after the last block): their columns of the
+                // product are never stored
+                bf = act4[jb * 4 * M + lane];
             } else {
                 const uint2 raw = 8 * nt + lg < M ? act2[jb * 4 * M + 32 * nt + lane] : make_uint2(0u, 0u);
                 bf = b_frag_from_raw<QT>(raw);
             }
             const float4 mt = meta4[(jb * NT + nt) * 4 + lc];  // corr(p), d_a(p), corr(p+1), d_a(p+1); p = 8nt+2c
             const float2 corr = make_float2(mt.x, mt.z);
-            const float da0 = __fmul_rn(inv[nt].x, mt.y), da1 = __fmul_rn(inv[nt].y, mt.w);  // exact when inv = 1
+            const float2 da = fmul2_rn(inv[nt], make_float2(mt.y, mt.w));  // exact when inv = 1
             float d[2][4];
             record_dots(af, bf, corr, d);
+            // acc(row, p), acc(row, p+1) += dot * (w_row * d_a): two fp32 roundings per element, as pairs
 #pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                const float2 w = t ? w23 : w01;
+            for (int t = 0; t < 2; ++t)
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    acc[nt][t][e] = __fmaf_rn(d[t][e], __fmul_rn((e >> 1) ? w.y : w.x, (e & 1) ? da1 : da0),
-                                              acc[nt][t][e]);
-            }
+                for (int h = 0; h < 2; ++h) {
+                    const float2 r = ffma2_rn(make_float2(d[t][2 * h], d[t][2 * h + 1]), fmul2_rn(wr[2 * t + h], da),
+                                              make_float2(acc[nt][t][2 * h], acc[nt][t][2 * h + 1]));
+                    acc[nt][t][2 * h] = r.x;
+                    acc[nt][t][2 * h + 1] = r.y;
+                }
             if (PAIR) {
                 record_dots(afu, bf, corr, d);
 #pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    const float2 w = t ? u23 : u01;
+                for (int t = 0; t < 2; ++t)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        accu[PAIR ? nt : 0][t][e] = __fmaf_rn(
-                            d[t][e], __fmul_rn((e >> 1) ? w.y : w.x, (e & 1) ? da1 : da0), accu[PAIR ? nt : 0][t][e]);
-                }
+                    for (int h = 0; h < 2; ++h) {
+                        float(&au)[2][4] = accu[PAIR ? nt : 0];
+                        const float2 r = ffma2_rn(make_float2(d[t][2 * h], d[t][2 * h + 1]),
+                                                  fmul2_rn(ur[2 * t + h], da),
+                                                  make_float2(au[t][2 * h], au[t][2 * h + 1]));
+                        au[t][2 * h] = r.x;
+                        au[t][2 * h + 1] = r.y;
+                    }
             }
         }
     }
@@ -1260,8 +1284,9 @@ __device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &
         const bool direct = (a.KS == 1) && (pc.np == 1);
         // values the epilogue needs, in flight while the partial sums are added
         float res[FIN_MPW], nw = 0.0f;
+        const int up = phys_unit(a, u);  // the row tile of this unit
         if (!PAIR) {
-            const int64_t n = static_cast<int64_t>(u) * 32 + lane;
+            const int64_t n = static_cast<int64_t>(up) * 32 + lane;
             const bool nok = n < a.n_out;
 #pragma unroll
             for (int i = 0; i < FIN_MPW; ++i) {
@@ -1391,11 +1416,11 @@ __device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &
 #pragma unroll
             for (int i = 0; i < FIN_MPW; ++i) {
                 const int m = f + NF * i;
-                if (m < M) epilogue<PAIR>(a, u, m, lane, v[i], vu[i], res[i], nw);
+                if (m < M) epilogue<PAIR>(a, up, m, lane, v[i], vu[i], res[i], nw);
             }
         }
         if (finish && a.head && !a.defer_stats) {  // the same decisions on every finisher warp
-            const int st = u / (STAT_TILE / 32);
+            const int st = up / (STAT_TILE / 32);
             if (st != st_cur) {
                 head_flush(a, sm, cs, fin_it, st_cur, st_n, lane, f);
                 st_cur = st;
@@ -1451,8 +1476,8 @@ __device__ inline void combine_phase(const QmmArgs &a, int widx) {
     const int u1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * a.NU / gridDim.x);
     const int items = (u1 - u0) * M;
     for (int i = widx; i < items; i += NWW) {
-        const int u = u0 + i / M, m = i - (i / M) * M;
-        const int64_t n = static_cast<int64_t>(u) * 32 + lane;
+        const int u = u0 + i / M, m = i - (i / M) * M, up = phys_unit(a, u);
+        const int64_t n = static_cast<int64_t>(up) * 32 + lane;
         const bool nok = n < a.n_out;
         const float res = (a.residual && nok) ? __ldcg(a.residual + m * a.n_out + n) : 0.0f;
         const float nw = (a.norm_next && nok) ? __ldg(a.norm_next + n) : 0.0f;
@@ -1481,7 +1506,7 @@ __device__ inline void combine_phase(const QmmArgs &a, int widx) {
                         v = first ? x[s2][c] : __fadd_rn(v, x[s2][c]);
                         first = false;
                     }
-            epilogue<0>(a, u, m, lane, v, 0.0f, res, nw);
+            epilogue<0>(a, up, m, lane, v, 0.0f, res, nw);
             continue;
         }
         for (int s2 = 0; s2 < a.KS; ++s2) {
@@ -1500,7 +1525,7 @@ __device__ inline void combine_phase(const QmmArgs &a, int widx) {
                     }
             }
         }
-        epilogue<0>(a, u, m, lane, v, 0.0f, res, nw);
+        epilogue<0>(a, up, m, lane, v, 0.0f, res, nw);
     }
 }
 

@@ -159,6 +159,8 @@ sd_status sd_qmatmul_multipos(int qtype, const void *w, int64_t n_out, int64_t k
     a.q_next = q_next;
     a.s_next = scales_next;
     a.nq = nq;
+    // requantised columns = the last third of the rows in whole 32-row tiles: interleave the thirds
+    if (epilogue == SD_EPI_REQUANT && p.NU % 3 == 0 && 3 * requant_col0 == 2 * n_out) a.ilv3 = p.NU / 3;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     a.cnt = reinterpret_cast<uint32_t *>(ws);
     a.part = reinterpret_cast<float *>(ws + p.ws_cnt);

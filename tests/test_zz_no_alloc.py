@@ -78,7 +78,9 @@ def test_noalloc_equals_workspace_call_twice(sdv, n, k, epi, col0):
 
 
 def test_noalloc_rejects_calls_beyond_its_scratch(sdv):
-    N, K, M = 65536, 17408, 5  # four k-splits of 2048 units: about 33 MB of partial sums
+    # fewer 32-row units than SMs and thirteen k-splits: every unit is shared across CTAs, whose
+    # partial sums (several MB) do not fit the static scratch
+    N, K, M = 4800, 65536, 5
     assert sdv.qmatmul_workspace_bytes(oracle.Q4_32, N, K, 0) > (4 << 20)  # SD_NOALLOC_SCRATCH_BYTES
     q = torch.zeros((M, K), dtype=torch.int8, device="cuda")
     s = torch.zeros((M, K // 32), dtype=torch.float32, device="cuda")
