@@ -29,6 +29,22 @@
  *              element j in its low nibble and element j+16 in its high
  *              nibble; value d*(code-8); 18 bytes per block.
  * A weight matrix is [n_out rows][k_in/32 blocks] of such blocks.
+ * K-quant super-blocks of 256 weights (the GGUF K formats of the Q4_K_M model
+ * files the pages run: "Inside OpenJet Engine", section "One GPU launch for a
+ * speculative cycle", and "How Kinetic is fast", opening section); a matrix is
+ * [n_out rows][k_in/256 super-blocks], n_out % 32 == 0, k_in % 256 == 0:
+ *  - SD_Q4_K (144 B): fp16 d, fp16 dmin, 12 bytes of eight 6-bit (scale,
+ *              min) pairs (pair s < 4: scale = b[s] & 63, min = b[s+4] & 63;
+ *              s >= 4: scale = (b[s+4] & 15) | (b[s-4] >> 6) << 4, min =
+ *              (b[s+4] >> 4) | (b[s] >> 6) << 4), 128 bytes of 4-bit codes
+ *              (byte 32c + l holds weight 64c + l in its low nibble and 64c +
+ *              32 + l in its high one); weight = d scale_s code - dmin min_s
+ *              for the 32-weight sub-block s.
+ *  - SD_Q6_K (210 B): 128 bytes of low code nibbles, 64 bytes of high 2-bit
+ *              pairs, 16 int8 scales, fp16 d; weight i (n = i/128, r = i%128,
+ *              l = r%32, k = r/32): low = byte 64n + l + 32(k&1), its low
+ *              nibble for k < 2 else its high one; high = (byte 128 + 32n + l
+ *              >> 2k) & 3; weight = d scale[i/16] (low | high << 4 - 32).
  */
 #ifndef SDVERIFY_H
 #define SDVERIFY_H
@@ -52,7 +68,7 @@ typedef enum {
     SD_EDEVICE = 5        /* a device-side check failed (from sd_device_status) */
 } sd_status;
 
-typedef enum { SD_Q8_0 = 0, SD_Q4_32 = 1 } sd_qtype;
+typedef enum { SD_Q8_0 = 0, SD_Q4_32 = 1, SD_Q4_K = 2, SD_Q6_K = 3 } sd_qtype;
 
 /* Repack flags */
 #define SD_REPACK_PAIR_GATE_UP 1u /* rows [0,F) are gate and [F,2F) are up; store them pairwise */
@@ -86,7 +102,25 @@ int sd_abi_version(void); /* 2: sd_pass_desc and sd_pass carry the acceptance mo
  * With SD_REPACK_PAIR_GATE_UP (n_out = 2F) the record of gate tile j is
  * followed by the record of up tile j, pairs ordered (j, b).  Values are
  * unchanged; only their places move.
- * Errors: SD_EINVAL on null/misaligned pointers, k_in % 32 != 0, odd n_out
+ * K-quants: per (tile, super-block) one super-record of the 32 rows' 256
+ * weights, ordered (tile, super-block); 32-weight sub-block s's codes sit in
+ * the fragment order above.
+ *   SD_Q4_K (4736 B): eight 512-B code planes (sub-block s at 512 s, as
+ *     SD_Q4_32); at 4096 + 64 s + 8 g the bytes scale of rows g, g+8, 16+g,
+ *     24+g then min of the same rows (sub-block s); at 4608 + 16 g the fp16
+ *     (d, dmin) of rows g, g+8, 16+g, 24+g.  The 6-bit fields are stored as
+ *     bytes: 32 B per 32 x 256 weights more than the file (2.8 %).
+ *   SD_Q6_K (6720 B, the file's bytes): per sub-block s at 768 s, 512 B of low
+ *     nibbles (as SD_Q4_32) and 256 B of high bits, 8 B per lane: word h
+ *     covers code words 2h, 2h+1; for code word 2h the two high bits of its
+ *     nibbles 0, 4, 2, 6, 1, 5, 3, 7 sit at bits 4, 20, 6, 22, 8, 24, 10, 26;
+ *     for code word 2h+1 at bits 0, 16, 12, 28, 2, 18, 14, 30; at 6144 + 64 s
+ *     + 8 g the int8 scales of rows g, g+8, 16+g, 24+g for weights 0-15 then
+ *     16-31 of sub-block s; at 6656 + 8 g the fp16 d of rows g, g+8, 16+g, 24+g.
+ *   With SD_REPACK_PAIR_GATE_UP (SD_Q4_K only) the gate super-record of tile
+ *   j is followed by the up super-record of tile j.
+ * Errors: SD_EINVAL on null/misaligned pointers, k_in % 32 != 0 (K-quants:
+ * k_in % 256 != 0 or n_out % 32 != 0; the pair flag with SD_Q6_K), odd n_out
  * with the pair flag, or dst_bytes too small.
  */
 size_t sd_repacked_bytes(int qtype, int64_t n_out, int64_t k_in, uint32_t flags);

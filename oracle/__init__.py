@@ -109,7 +109,7 @@ def _get():
                 "oracle_kq_block_bytes": ([_I], _I),
                 "oracle_accept_greedy_tree_path": ([_P, _P, _P, _I, _P], _I),
                 "oracle_kq_dequant": ([_I, _P, _I64, _P], None),
-                "oracle_kq_matmul": ([_I, _P, _I64, _I64, _P, _P, _I, _P], None),
+                "oracle_kq_matmul": ([_I, _P, _I64, _I64, _P, _P, _I, _P, _P], None),
                 "oracle_kv_append": ([_P, _P, _I, _I, _I, _P, _P, _I64, _I64], None),
                 "oracle_attn_decode": ([_P, _P, _P, _I, _I, _I, _I, _I64, _I64, _P, _P], None),
                 "oracle_kv_commit": ([_P, _P, _I, _I, _I64, _I64, _P, _I], None),
@@ -380,15 +380,17 @@ def kq_dequant(qtype: int, blocks, n_out: int, k_in: int) -> np.ndarray:
     return out
 
 
-def kq_matmul(qtype: int, blocks, n_out: int, k_in: int, q, scales) -> np.ndarray:
-    """fp64 [M][n_out]: per 32-weight block, the integer dots times the scales (factored form)."""
+def kq_matmul(qtype: int, blocks, n_out: int, k_in: int, q, scales, with_bound: bool = False):
+    """fp64 [M][n_out]: per 32-weight block, the integer dots times the scales (factored form).
+    with_bound: also the absolute sum of the same terms [M][n_out] (the tolerance scale, reading R5)."""
     blocks, pw = _c(np.asarray(blocks).reshape(-1), np.uint8)
     q, pq = _c(q, np.int8)
     sc, ps = _c(scales, np.float32)
     M = q.shape[0]
     y = np.empty((M, n_out), dtype=np.float64)
-    _get().oracle_kq_matmul(qtype, pw, n_out, k_in, pq, ps, M, y.ctypes.data)
-    return y
+    ab = np.empty((M, n_out), dtype=np.float64)
+    _get().oracle_kq_matmul(qtype, pw, n_out, k_in, pq, ps, M, y.ctypes.data, ab.ctypes.data)
+    return (y, ab) if with_bound else y
 
 
 def f32_to_f16(x) -> np.ndarray:

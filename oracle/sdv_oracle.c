@@ -936,15 +936,17 @@ void oracle_kq_dequant(int qtype, const uint8_t *blocks, int64_t nblk, float *ou
 }
 
 /* y[m][n] (fp64) = sum over 32-blocks of the factored integer form; w [n_out][k_in/256] blocks,
-   q int8 [M][k_in], scales fp32 [M][k_in/32] */
+   q int8 [M][k_in], scales fp32 [M][k_in/32].  absb (nullable) receives the absolute sum of the same
+   terms (Q4_K: |d_a| (|d sc dot| + |dmin m sum|); Q6_K: |d_a d| (|sc_lo dot_lo| + |sc_hi dot_hi|)), the
+   scale of the rounding error any order of evaluating them in fp32 can make (tolerance reading R5). */
 void oracle_kq_matmul(int qtype, const uint8_t *w, int64_t n_out, int64_t k_in, const int8_t *q,
-                      const float *scales, int M, double *y) {
+                      const float *scales, int M, double *y, double *absb) {
     const int bb = oracle_kq_block_bytes(qtype);
     const int64_t SB = k_in / 256, KB = k_in / 32;
 #pragma omp parallel for schedule(static)
     for (int64_t n = 0; n < n_out; ++n) {
         for (int m = 0; m < M; ++m) {
-            double acc = 0.0;
+            double acc = 0.0, ab = 0.0;
             for (int64_t b = 0; b < KB; ++b) {
                 const uint8_t *blk = w + (n * SB + b / 8) * bb;
                 const int s = (int)(b % 8);  /* 32-weight sub-block within the super-block */
@@ -961,15 +963,19 @@ void oracle_kq_matmul(int qtype, const uint8_t *w, int64_t n_out, int64_t k_in, 
                     const double d = oracle_f16_to_f32((uint16_t)(blk[0] | (blk[1] << 8)));
                     const double dmin = oracle_f16_to_f32((uint16_t)(blk[2] | (blk[3] << 8)));
                     acc += da * (d * sc * (double)dot - dmin * mn * (double)sum);
+                    ab += fabs(da) * (fabs(d * sc * (double)dot) + fabs(dmin * mn * (double)sum));
                 } else {
                     int64_t lo = 0, hi = 0;
                     for (int i = 0; i < 16; ++i) lo += (int64_t)kq_code(qtype, blk, 32 * s + i) * qa[i];
                     for (int i = 16; i < 32; ++i) hi += (int64_t)kq_code(qtype, blk, 32 * s + i) * qa[i];
                     const double d = oracle_f16_to_f32((uint16_t)(blk[208] | (blk[209] << 8)));
                     acc += da * d * ((int8_t)blk[192 + 2 * s] * (double)lo + (int8_t)blk[192 + 2 * s + 1] * (double)hi);
+                    ab += fabs(da * d) * (fabs((int8_t)blk[192 + 2 * s] * (double)lo) +
+                                          fabs((int8_t)blk[192 + 2 * s + 1] * (double)hi));
                 }
             }
             y[(int64_t)m * n_out + n] = acc;
+            if (absb) absb[(int64_t)m * n_out + n] = ab;
         }
     }
 }

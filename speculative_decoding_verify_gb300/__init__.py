@@ -18,7 +18,10 @@ LIB_PATH = os.path.join(HERE, "libsdverify.so")
 
 Q8_0 = 0
 Q4_32 = 1
+Q4_K = 2
+Q6_K = 3
 BLOCK_BYTES = {Q8_0: 34, Q4_32: 18}
+SUPER_BLOCK_BYTES = {Q4_K: 144, Q6_K: 210}  # K-quant super-blocks of 256 weights
 REPACK_PAIR_GATE_UP = 1
 EPI_NONE = 0
 EPI_REQUANT = 1

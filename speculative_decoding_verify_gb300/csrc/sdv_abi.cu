@@ -122,6 +122,126 @@ __global__ void repack_kernel(int qtype, const uint8_t *__restrict__ src, int64_
     }
 }
 
+// ---------------------------------------------------------------------------
+// K-quant super-blocks (256 weights) -> super-records of 32 rows (values unchanged)
+// ---------------------------------------------------------------------------
+
+// code of weight i (0..255) of a Q4_K super-block: 128 code bytes from byte 16, byte 32c + l holding
+// weight 64c + l (low nibble) and 64c + 32 + l (high nibble)
+__device__ __forceinline__ int q4k_code(const uint8_t *blk, int i) {
+    const int c = i >> 6, r = i & 63;
+    const uint8_t b = blk[16 + 32 * c + (r & 31)];
+    return r < 32 ? (b & 15) : (b >> 4);
+}
+
+// 6-bit (scale, min) of sub-block s from the 12 packed bytes at blk + 4
+__device__ __forceinline__ void q4k_scale_min_dev(const uint8_t *blk, int s, int &sc, int &mn) {
+    const uint8_t *b = blk + 4;
+    if (s < 4) {
+        sc = b[s] & 63;
+        mn = b[s + 4] & 63;
+    } else {
+        sc = (b[s + 4] & 15) | ((b[s - 4] >> 6) << 4);
+        mn = (b[s + 4] >> 4) | ((b[s] >> 6) << 4);
+    }
+}
+
+// unsigned 6-bit code (0..63) of weight i of a Q6_K super-block: low nibble from the first 128 bytes,
+// two high bits from the next 64
+__device__ __forceinline__ int q6k_code(const uint8_t *blk, int i) {
+    const int n = i >> 7, r = i & 127, l = r & 31, k = r >> 5;
+    const uint8_t lo = blk[64 * n + l + 32 * (k & 1)];
+    const int low = k < 2 ? (lo & 15) : (lo >> 4);
+    const int high = (blk[128 + 32 * n + l] >> (2 * k)) & 3;
+    return low | (high << 4);
+}
+
+// Where the two high bits of nibble `nib` of code word 2h+e of a lane go in the lane's high-bit word h.
+__device__ __forceinline__ int q6k_hi_pos(int e, int nib) {
+    // nibbles 0..7 -> bit positions; e = 0: 4, 8, 6, 10, 20, 24, 22, 26; e = 1: 0, 2, 12, 14, 16, 18, 28, 30
+    const int p0[8] = {4, 8, 6, 10, 20, 24, 22, 26}, p1[8] = {0, 2, 12, 14, 16, 18, 28, 30};
+    return e ? p1[nib] : p0[nib];
+}
+
+// One thread per (super-record, lane): the lane's code words of the eight sub-blocks and, for lanes
+// with c == 0, its row group's scales and super-block factors.
+__global__ void repack_kq_kernel(int qtype, const uint8_t *__restrict__ src, int64_t SBK, int pair, int64_t F,
+                                 uint8_t *__restrict__ dst, int64_t n_sr) {
+    const int bb = qtype == SD_Q4_K ? 144 : 210;
+    const int srb = qtype == SD_Q4_K ? 4736 : 6720;
+    const int64_t total = n_sr * 32;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t sr = i >> 5;
+        const int lane = static_cast<int>(i & 31), g = lane >> 2, c = lane & 3;
+        int64_t row0, j;
+        if (pair) {
+            const int64_t pr = sr >> 1, half = sr & 1, tp = pr / SBK;
+            j = pr - tp * SBK;
+            row0 = tp * 32 + half * F;
+        } else {
+            const int64_t tile = sr / SBK;
+            j = sr - tile * SBK;
+            row0 = tile * 32;
+        }
+        auto blk = [&](int rr) -> const uint8_t * { return src + ((row0 + rr) * SBK + j) * bb; };
+        uint8_t *d = dst + sr * srb;
+        const int rows[4] = {g, g + 8, 16 + g, 24 + g};
+        for (int s = 0; s < 8; ++s) {
+            uint32_t words[4], hiw[2] = {0u, 0u};
+            for (int jw = 0; jw < 4; ++jw) {
+                const int t = jw >> 1, sk = jw & 1;
+                uint32_t wv = 0;
+                for (int nib = 0; nib < 8; ++nib) {
+                    const int rr = 16 * t + g + ((nib & 2) ? 8 : 0);
+                    const int kk = 32 * s + 16 * sk + 2 * c + ((nib & 1) ? 8 : 0) + (nib >> 2);
+                    if (qtype == SD_Q4_K) {
+                        wv |= static_cast<uint32_t>(q4k_code(blk(rr), kk)) << (4 * nib);
+                    } else {
+                        const int code = q6k_code(blk(rr), kk);
+                        wv |= static_cast<uint32_t>(code & 15) << (4 * nib);
+                        hiw[jw >> 1] |= static_cast<uint32_t>(code >> 4) << q6k_hi_pos(jw & 1, nib);
+                    }
+                }
+                words[jw] = wv;
+            }
+            const int plane = qtype == SD_Q4_K ? 512 : 768;
+            uint8_t *o = d + s * plane + lane * 16;
+            for (int jw = 0; jw < 4; ++jw)
+                for (int e = 0; e < 4; ++e) o[4 * jw + e] = static_cast<uint8_t>(words[jw] >> (8 * e));
+            if (qtype == SD_Q6_K) {
+                uint8_t *oh = d + s * plane + 512 + lane * 8;
+                for (int h = 0; h < 2; ++h)
+                    for (int e = 0; e < 4; ++e) oh[4 * h + e] = static_cast<uint8_t>(hiw[h] >> (8 * e));
+            }
+            if (c == 0) {
+                for (int e = 0; e < 4; ++e) {
+                    const uint8_t *bl = blk(rows[e]);
+                    if (qtype == SD_Q4_K) {
+                        int sc, mn;
+                        q4k_scale_min_dev(bl, s, sc, mn);
+                        d[4096 + 64 * s + 8 * g + e] = static_cast<uint8_t>(sc);
+                        d[4096 + 64 * s + 8 * g + 4 + e] = static_cast<uint8_t>(mn);
+                    } else {
+                        d[6144 + 64 * s + 8 * g + e] = bl[192 + 2 * s];
+                        d[6144 + 64 * s + 8 * g + 4 + e] = bl[192 + 2 * s + 1];
+                    }
+                }
+            }
+        }
+        if (c == 0) {
+            for (int e = 0; e < 4; ++e) {
+                const uint8_t *bl = blk(rows[e]);
+                if (qtype == SD_Q4_K) {
+                    for (int q = 0; q < 4; ++q) d[4608 + 16 * g + 4 * e + q] = bl[q];  // d, dmin
+                } else {
+                    d[6656 + 8 * g + 2 * e] = bl[208];
+                    d[6656 + 8 * g + 2 * e + 1] = bl[209];
+                }
+            }
+        }
+    }
+}
+
 }  // namespace sdv
 
 using namespace sdv;
@@ -159,6 +279,14 @@ sd_status sd_device_status(sd_stream_t stream) {
 }
 
 size_t sd_repacked_bytes(int qtype, int64_t n_out, int64_t k_in, uint32_t flags) {
+    if (qtype == SD_Q4_K || qtype == SD_Q6_K) {
+        if (n_out <= 0 || k_in <= 0 || k_in % 256 || n_out % 32) return 0;
+        const int64_t srb = qtype == SD_Q4_K ? 4736 : 6720;
+        if (flags & SD_REPACK_PAIR_GATE_UP) {
+            if (qtype != SD_Q4_K || n_out % 64) return 0;
+        }
+        return static_cast<size_t>(n_out / 32 * (k_in / 256) * srb);
+    }
     if ((qtype != SD_Q8_0 && qtype != SD_Q4_32) || n_out <= 0 || k_in <= 0 || k_in % 32) return 0;
     int64_t KB = k_in / 32;
     int64_t rec = qtype == SD_Q8_0 ? 1088 : 576;
@@ -175,6 +303,15 @@ sd_status sd_repack_weights(int qtype, const void *src_blocks, int64_t n_out, in
                             size_t dst_bytes, sd_stream_t stream) {
     size_t need = sd_repacked_bytes(qtype, n_out, k_in, flags);
     if (!need || !src_blocks || !dst || !aligned(dst, 16) || dst_bytes < need) return SD_EINVAL;
+    if (qtype == SD_Q4_K || qtype == SD_Q6_K) {
+        const int64_t n_sr = static_cast<int64_t>(need) / (qtype == SD_Q4_K ? 4736 : 6720);
+        const int64_t threads = n_sr * 32;
+        const int grid = static_cast<int>(threads / 256 + 1 < 65536 ? threads / 256 + 1 : 65536);
+        repack_kq_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+            qtype, static_cast<const uint8_t *>(src_blocks), k_in / 256, (flags & SD_REPACK_PAIR_GATE_UP) ? 1 : 0,
+            n_out / 2, static_cast<uint8_t *>(dst), n_sr);
+        return cudaGetLastError() == cudaSuccess ? SD_OK : SD_ECUDA;
+    }
     int64_t KB = k_in / 32;
     int64_t rec = qtype == SD_Q8_0 ? 1088 : 576;
     int64_t n_records = static_cast<int64_t>(need) / rec;

@@ -129,6 +129,7 @@ sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, 
           *aff_m = reinterpret_cast<float *>(ws + W.aff_meta), *ssb = reinterpret_cast<float *>(ws + W.ss);
     auto base = [&](QmmArgs &a) {
         a = QmmArgs{};
+        a.GR = 1;
         a.M = M;
         a.status = st;
         a.cnt = reinterpret_cast<uint32_t *>(ws);
@@ -147,6 +148,7 @@ sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, 
         a.kind = KIND_MATMUL;
         a.qt = qt;
         a.pair = pair ? 1 : 0;
+        a.GR = p.GR;
         a.KB = p.KB;
         a.NU = p.NU;
         a.KS = p.KS;

@@ -93,6 +93,19 @@ __host__ __device__ __forceinline__ int af_nt(int M) { return M <= 8 ? 1 : 2; }
 __host__ __device__ __forceinline__ uint32_t af_frag_bytes(int M) { return af_nt(M) == 1 ? 64u * M : 32u * M; }
 __host__ __device__ __forceinline__ uint32_t af_meta_bytes(int M) { return 64u * af_nt(M); }
 
+// K-quant consumers (SD_Q4_K, SD_Q6_K) read a wider {c0, c1, d_a, S} per (block, position): Q4_K the
+// offset correction of the raw code dot in c0 and the code sum S of the activations (for the minima);
+// Q6_K the corrections of the block's two 16-weight halves in c0, c1.  128 NT bytes per block.
+__host__ __device__ constexpr bool is_kq(int qt) { return qt == SD_Q4_K || qt == SD_Q6_K; }
+__host__ __device__ __forceinline__ uint32_t af_meta_bytes_q(int M, int qt) {
+    return (is_kq(qt) ? 128u : 64u) * af_nt(M);
+}
+// bytes of one 32-weight step of a matrix (a K-quant super-record holds eight)
+__host__ __device__ constexpr int step_bytes_q(int qt) {
+    return qt == SD_Q8_0 ? 1088 : (qt == SD_Q4_K ? 592 : (qt == SD_Q6_K ? 840 : 576));
+}
+constexpr int Q4K_SR = 4736, Q6K_SR = 6720;  // super-record bytes (32 rows x 256 weights)
+
 struct QmmArgs {
     const uint8_t *w;
     int64_t n_out;       // output columns (2F for a gate|up pair)
@@ -163,6 +176,8 @@ struct QmmArgs {
     int32_t top_k;          // sampling: 0 unfiltered, else the top-k / top-p filtered target
     float top_p;
     int32_t ilv3;           // 0, or NU / 3: units taken in threes from the three thirds of the rows (see phys_unit)
+    int32_t GR;             // schedule granule in blocks: every piece and split boundary is a multiple (8 for the
+                            // 256-weight K-quant super-blocks, else 1)
 };
 
 constexpr int KIND_MATMUL = 0, KIND_NORM = 1, KIND_ACCEPT = 2, KIND_COMBINE = 3, KIND_HSTATS = 4;
@@ -212,9 +227,11 @@ __host__ __device__ __forceinline__ int64_t unit_start(const QmmArgs &a, int s, 
 // length of the shared stream-K step sequence
 __host__ __device__ __forceinline__ int64_t seq_len(const QmmArgs &a) { return a.D > 0 ? static_cast<int64_t>(a.R) * a.KB : a.W; }
 
-// CTA owning step x of the shared sequence: largest c with floor(c wseq / G) <= x
+// CTA owning step x of the shared sequence: the CTAs' runs start at floor(c wq / G) granules (wq =
+// wseq / GR granules in all), so the owner is the largest c with floor(c wq / G) <= floor(x / GR)
 __host__ __device__ __forceinline__ int seq_owner(const QmmArgs &a, int64_t wseq, int64_t x) {
-    return wseq > 0 ? static_cast<int>(((x + 1) * a.G - 1) / wseq) : 0;
+    const int64_t wq = wseq / a.GR;
+    return wq > 0 ? static_cast<int>(((x / a.GR + 1) * a.G - 1) / wq) : 0;
 }
 
 // CTAs sharing split s of unit u, and the first of them
@@ -246,10 +263,10 @@ struct PieceIter {
 
 // The schedule of CTA `cta` (host and device: the host replays it to check the partition).
 __host__ __device__ __forceinline__ void pieces_begin_cta(const QmmArgs &a, PieceIter &it, int cta) {
-    const int64_t c = cta, wseq = seq_len(a);
+    const int64_t c = cta, wq = seq_len(a) / a.GR;
     it.cta = cta;
-    it.g = c * wseq / a.G;
-    it.hi = (c + 1) * wseq / a.G;
+    it.g = c * wq / a.G * a.GR;
+    it.hi = (c + 1) * wq / a.G * a.GR;
     it.d_next = a.D > 0 ? a.R + static_cast<int>(c) * a.D : 0;
     it.d_end = a.D > 0 ? it.d_next + a.D : 0;
 }
@@ -353,6 +370,39 @@ __device__ __forceinline__ void q8_frag(uint4 p0, uint4 p1, uint32_t (&a)[2][2][
     }
 }
 
+// t | (h & MASK) as one three-input logic operation (lookup table 0xF8 = a | (b & c)), the mask as an immediate
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t or_masked(uint32_t t, uint32_t h) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xF8;" : "=r"(r) : "r"(t), "n"(MASK), "r"(h));
+    return r;
+}
+
+// Q6_K codes of one lane -> fp16 pairs 1024 + code (code = low nibble | two high bits << 4, 0..63), or
+// 1024 + 16 code in the k+8 halves: the low nibbles are placed as the 4-bit format's, and high-bit word
+// h holds the high bits of code words 2h (at 4..11, 20..27) and 2h+1 (at 0..3, 12..19, 28..31) where
+// one shift brings each register's pair under the masks 0x00300030 / 0x03000300.
+__device__ __forceinline__ void q6_frag(uint4 lo, uint2 hi, uint32_t (&a)[2][2][4]) {
+    const uint32_t ws[4] = {lo.x, lo.y, lo.z, lo.w};
+    const uint32_t magic = 0x64006400u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t x = ws[j], y = x >> 8, H = (j >> 1) ? hi.y : hi.x;
+        const uint32_t ha0 = (j & 1) ? H << 4 : H, ha1 = (j & 1) ? H >> 8 : H >> 2;
+        const uint32_t hb0 = (j & 1) ? H << 6 : H, hb1 = (j & 1) ? H >> 6 : H >> 2;
+        a[j >> 1][j & 1][0] = or_masked<0x00300030u>(and_or<0x000F000Fu>(x, magic), ha0);
+        a[j >> 1][j & 1][1] = or_masked<0x00300030u>(and_or<0x000F000Fu>(y, magic), ha1);
+        a[j >> 1][j & 1][2] = or_masked<0x03000300u>(and_or<0x00F000F0u>(x, magic), hb0);
+        a[j >> 1][j & 1][3] = or_masked<0x03000300u>(and_or<0x00F000F0u>(y, magic), hb1);
+    }
+}
+
+// unsigned byte e of x as an exact float (the byte in the mantissa of 2^23)
+__device__ __forceinline__ float ubyte_f(uint32_t x, int e) {
+    return __int_as_float(static_cast<int>(__byte_perm(x, 0x4B000000u, 0x7440u | static_cast<uint32_t>(e)))) -
+           8388608.0f;
+}
+
 // the two row tiles' exact dots of one record against one 8-position tile:
 // d[t][i] = dot(row 16t + g + 8(i>>1), position 2c + (i&1))
 __device__ __forceinline__ void record_dots(const uint32_t (&a)[2][2][4], uint4 bf, float2 corr, float (&d)[2][4]) {
@@ -388,7 +438,7 @@ __device__ __forceinline__ uint32_t i8pair_to_h2(uint32_t x, bool div16) {
 // the k+8 halves divided by 16 for the 4-bit format
 template <int QT>
 __device__ __forceinline__ uint4 b_frag_from_raw(uint2 r) {
-    const bool d = QT == SD_Q4_32;
+    const bool d = QT != SD_Q8_0;  // the 4-bit and K-quant formats take the k+8 halves as sixteenths
     return make_uint4(i8pair_to_h2(r.x, false), i8pair_to_h2(r.x >> 16, d), i8pair_to_h2(r.y, false),
                       i8pair_to_h2(r.y >> 16, d));
 }
@@ -412,6 +462,19 @@ __device__ __forceinline__ float dot_corr(const int8_t *arow) {
     hi = dp4a(0x01010101, static_cast<int>(x1.w), hi);
     const int v = QT == SD_Q4_32 ? -(1032 * lo + 72 * hi) : -1152 * (lo + hi);
     return static_cast<float>(v);
+}
+
+// {c0, c1, d_a, S} of a K-quant consumer from the activation code sums of the block's quarters (k 0-7,
+// 8-15, 16-23, 24-31; the fragments carry the 8-15 and 24-31 codes as sixteenths).  Q4_K: c0 removes the
+// fp16 offsets 1024 and 64 so the dot is sum code * a; S = sum a.  Q6_K: per 16-weight half, c removes
+// the offsets and the code bias 32 (1056 = 1024 + 32, 96 = 64 + 32).  Exact integers below 2^24.
+template <int QT>
+__device__ __forceinline__ float4 kq_meta(const int (&s4)[4], float da) {
+    if (QT == SD_Q4_K)
+        return make_float4(static_cast<float>(-(1024 * (s4[0] + s4[2]) + 64 * (s4[1] + s4[3]))), 0.0f, da,
+                           static_cast<float>(s4[0] + s4[1] + s4[2] + s4[3]));
+    return make_float4(static_cast<float>(-(1056 * s4[0] + 96 * s4[1])), static_cast<float>(-(1056 * s4[2] + 96 * s4[3])),
+                       da, 0.0f);
 }
 
 // ---------------------------------------------------------------------------
@@ -845,7 +908,7 @@ __device__ inline void producer_drain(const Smem &sm, uint32_t it, int NS) {
 // the proxy fence orders that acquire before the copy engine's reads.
 __device__ __forceinline__ void stage_issue(const QmmArgs &a, const Smem &sm, int s, int len) {
     const int64_t b0 = static_cast<int64_t>(s) * a.KBs;
-    const uint32_t fb = af_frag_bytes(a.M), mb = af_meta_bytes(a.M);
+    const uint32_t fb = af_frag_bytes(a.M), mb = af_meta_bytes_q(a.M, a.qt);
     const uint32_t nf = static_cast<uint32_t>(len) * fb, nm = static_cast<uint32_t>(len) * mb;
     const uint32_t ns = a.af_norm ? static_cast<uint32_t>(a.M) * a.ss_ld * 4u : 0u;
     fence_proxy_async_global();
@@ -887,9 +950,23 @@ __device__ inline void stage_rows(const QmmArgs &a, const Smem &sm, int s, int l
     for (int it = tid; it < len * P8; it += CONS_THREADS) {
         const int jb = it / P8, m = it - jb * P8;
         const bool real = m < M;
-        const float corr = dot_corr<QT>(real ? a.q + m * K + static_cast<int64_t>(b0 + jb) * 32 : nullptr);
         const float da = real ? __ldcg(a.sc + static_cast<int64_t>(m) * a.KB + b0 + jb) : 0.0f;
-        reinterpret_cast<float2 *>(sm.meta)[it] = make_float2(corr, da);
+        if constexpr (is_kq(QT)) {
+            // the activations' code sums over k 0-7, 8-15, 16-23, 24-31 of the block
+            int s4[4] = {0, 0, 0, 0};
+            if (real) {
+                const uint4 *p = reinterpret_cast<const uint4 *>(a.q + m * K + static_cast<int64_t>(b0 + jb) * 32);
+                const uint4 x0 = __ldcg(p), x1 = __ldcg(p + 1);
+                s4[0] = dp4a(0x01010101, static_cast<int>(x0.y), dp4a(0x01010101, static_cast<int>(x0.x), 0));
+                s4[1] = dp4a(0x01010101, static_cast<int>(x0.w), dp4a(0x01010101, static_cast<int>(x0.z), 0));
+                s4[2] = dp4a(0x01010101, static_cast<int>(x1.y), dp4a(0x01010101, static_cast<int>(x1.x), 0));
+                s4[3] = dp4a(0x01010101, static_cast<int>(x1.w), dp4a(0x01010101, static_cast<int>(x1.z), 0));
+            }
+            reinterpret_cast<float4 *>(sm.meta)[it] = kq_meta<QT>(s4, da);
+        } else {
+            const float corr = dot_corr<QT>(real ? a.q + m * K + static_cast<int64_t>(b0 + jb) * 32 : nullptr);
+            reinterpret_cast<float2 *>(sm.meta)[it] = make_float2(corr, da);
+        }
     }
 }
 
@@ -1017,6 +1094,120 @@ __device__ __forceinline__ void stage_compute(const uint8_t *sbase, int n, int j
                         au[t][2 * h] = r.x;
                         au[t][2 * h + 1] = r.y;
                     }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// consumers, K-quant formats: the records of one sub-step.  Steps come in whole super-records (eight
+// 32-weight sub-blocks of 32 rows); record r = warp + 8i of a sub-step is sub-block `warp` of
+// super-record i, so each warp always takes the same sub-block.  Accumulators as stage_compute's.
+//  Q4_K: dot = sum code * a exactly (the activations' {c0} removes the code offset); per (row,
+//    position) acc += d_a (d sc dot - dmin m S), S the activations' code sum.
+//  Q6_K: the two 16-weight halves' dots (code - 32) a separately (corrections c0, c1); acc += (d d_a)
+//    (sc_lo dot_lo + sc_hi dot_hi), whose integer part is exact below 2^24.
+// ---------------------------------------------------------------------------
+template <int QT, int PAIR, int NT, bool FULL>
+__device__ __forceinline__ void stage_compute_kq(const uint8_t *sbase, int n, int jb0, const uint8_t *act,
+                                                 const float *meta, int M, int warp, int lane,
+                                                 const float2 (&inv)[NT], float (&acc)[NT][2][4],
+                                                 float (&accu)[PAIR ? NT : 1][2][4]) {
+    constexpr int SR = QT == SD_Q4_K ? Q4K_SR : Q6K_SR;
+    constexpr int PSR = PAIR ? 2 * SR : SR;           // a gate|up pair of super-records
+    constexpr int RPW = PAIR ? 2 : 4;                 // records per warp in a full sub-step
+    const int lg = lane >> 2, lc = lane & 3;
+    const uint4 *act4 = reinterpret_cast<const uint4 *>(act);
+    const uint2 *act2 = reinterpret_cast<const uint2 *>(act);
+    const float4 *meta4 = reinterpret_cast<const float4 *>(meta);
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+        const int r = warp + NCW * i;
+        if (!FULL && r >= n) break;
+        const int jb = jb0 + r;
+#pragma unroll
+        for (int half = 0; half < (PAIR ? 2 : 1); ++half) {
+            const uint8_t *srp = sbase + i * PSR + half * SR;
+            uint32_t af[2][2][4];
+            float f1[4], f2[4];  // per row g, g+8, 16+g, 24+g: Q4_K d sc, dmin m; Q6_K sc_lo, sc_hi
+            float dq[4];         // Q6_K: d per row
+            if (QT == SD_Q4_K) {
+                q4_frag(*reinterpret_cast<const uint4 *>(srp + warp * 512 + lane * 16), af);
+                const uint2 scm = *reinterpret_cast<const uint2 *>(srp + 4096 + 64 * warp + 8 * lg);
+                const uint4 dd = *reinterpret_cast<const uint4 *>(srp + 4608 + 16 * lg);
+                const uint32_t dw[4] = {dd.x, dd.y, dd.z, dd.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 dm = __half22float2(*reinterpret_cast<const __half2 *>(&dw[e]));  // d, dmin
+                    f1[e] = __fmul_rn(dm.x, ubyte_f(scm.x, e));  // exact: 11 x 6 bits
+                    f2[e] = __fmul_rn(dm.y, ubyte_f(scm.y, e));
+                }
+            } else {
+                q6_frag(*reinterpret_cast<const uint4 *>(srp + warp * 768 + lane * 16),
+                        *reinterpret_cast<const uint2 *>(srp + warp * 768 + 512 + lane * 8), af);
+                const uint2 scb = *reinterpret_cast<const uint2 *>(srp + 6144 + 64 * warp + 8 * lg);
+                const uint2 dh = *reinterpret_cast<const uint2 *>(srp + 6656 + 8 * lg);
+                const float2 d01 = __half22float2(*reinterpret_cast<const __half2 *>(&dh.x));
+                const float2 d23 = __half22float2(*reinterpret_cast<const __half2 *>(&dh.y));
+                dq[0] = d01.x;
+                dq[1] = d01.y;
+                dq[2] = d23.x;
+                dq[3] = d23.y;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    f1[e] = ubyte_f(scb.x ^ 0x80808080u, e) - 128.0f;  // int8 scales, exact
+                    f2[e] = ubyte_f(scb.y ^ 0x80808080u, e) - 128.0f;
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                uint4 bf;
+                if (NT == 1) {
+                    bf = act4[jb * 4 * M + lane];  // padding lanes read neighbouring fragments; never stored
+                } else {
+                    const uint2 raw = 8 * nt + lg < M ? act2[jb * 4 * M + 32 * nt + lane] : make_uint2(0u, 0u);
+                    bf = b_frag_from_raw<QT>(raw);
+                }
+                const float4 m0 = meta4[(jb * NT + nt) * 8 + 2 * lc], m1 = meta4[(jb * NT + nt) * 8 + 2 * lc + 1];
+                const float2 da = fmul2_rn(inv[nt], make_float2(m0.z, m1.z));
+                float(&ac)[2][4] = half ? accu[PAIR ? nt : 0] : acc[nt];
+                if (QT == SD_Q4_K) {
+                    float d[2][4];
+                    record_dots(af, bf, make_float2(m0.x, m1.x), d);
+                    const float2 ns = make_float2(-m0.w, -m1.w);
+#pragma unroll
+                    for (int t = 0; t < 2; ++t)
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int e = 2 * t + h;
+                            const float2 v = ffma2_rn(make_float2(d[t][2 * h], d[t][2 * h + 1]),
+                                                      make_float2(f1[e], f1[e]), fmul2_rn(ns, make_float2(f2[e], f2[e])));
+                            const float2 r2 = ffma2_rn(v, da, make_float2(ac[t][2 * h], ac[t][2 * h + 1]));
+                            ac[t][2 * h] = r2.x;
+                            ac[t][2 * h + 1] = r2.y;
+                        }
+                } else {
+                    float dl[2][4], dh2[2][4];
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        mma_init(dl[t], af[t][0], bf.x, bf.y, m0.x, m1.x);
+                        mma_init(dh2[t], af[t][1], bf.z, bf.w, m0.y, m1.y);
+                    }
+#pragma unroll
+                    for (int t = 0; t < 2; ++t)
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int e = 2 * t + h;
+                            const float2 v = ffma2_rn(make_float2(dh2[t][2 * h], dh2[t][2 * h + 1]),
+                                                      make_float2(f2[e], f2[e]),
+                                                      fmul2_rn(make_float2(dl[t][2 * h], dl[t][2 * h + 1]),
+                                                               make_float2(f1[e], f1[e])));
+                            const float2 r2 = ffma2_rn(v, fmul2_rn(make_float2(dq[e], dq[e]), da),
+                                                       make_float2(ac[t][2 * h], ac[t][2 * h + 1]));
+                            ac[t][2 * h] = r2.x;
+                            ac[t][2 * h + 1] = r2.y;
+                        }
+                }
             }
         }
     }
@@ -1163,15 +1354,24 @@ __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
                 sph ^= 1u;
             }
             constexpr int SUB = sub_steps(QT, PAIR);
-            constexpr int STEP = (QT == SD_Q8_0 ? 1088 : 576) * (PAIR ? 2 : 1);
+            constexpr int STEP = step_bytes_q(QT) * (PAIR ? 2 : 1);
             for (int off = 0; off < n; off += SUB) {
                 const int nn = n - off < SUB ? n - off : SUB;
-                if (nn == SUB)
-                    stage_compute<QT, PAIR, NT, true>(sbase + off * STEP, nn, jj + off, sm.act, sm.meta, M, warp, lane,
-                                                      inv, acc, accu);
-                else
-                    stage_compute<QT, PAIR, NT, false>(sbase + off * STEP, nn, jj + off, sm.act, sm.meta, M, warp, lane,
-                                                       inv, acc, accu);
+                if constexpr (is_kq(QT)) {
+                    if (nn == SUB)
+                        stage_compute_kq<QT, PAIR, NT, true>(sbase + off * STEP, nn, jj + off, sm.act, sm.meta, M,
+                                                             warp, lane, inv, acc, accu);
+                    else
+                        stage_compute_kq<QT, PAIR, NT, false>(sbase + off * STEP, nn, jj + off, sm.act, sm.meta, M,
+                                                              warp, lane, inv, acc, accu);
+                } else {
+                    if (nn == SUB)
+                        stage_compute<QT, PAIR, NT, true>(sbase + off * STEP, nn, jj + off, sm.act, sm.meta, M, warp,
+                                                          lane, inv, acc, accu);
+                    else
+                        stage_compute<QT, PAIR, NT, false>(sbase + off * STEP, nn, jj + off, sm.act, sm.meta, M, warp,
+                                                           lane, inv, acc, accu);
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.empty[done]);
@@ -1786,7 +1986,7 @@ cudaError_t pass_launch_sampling(const QmmArgs *phases, int n_phases, uint32_t *
 // host side: plan + launch
 // ---------------------------------------------------------------------------
 struct QmmPlan {
-    int32_t KB, NU, KS, KBs, KBlast, G, P, D, R, SB, NS, NRB, rows_p;
+    int32_t KB, NU, KS, KBs, KBlast, G, P, D, R, SB, NS, NRB, rows_p, GR;
     int64_t W;
     uint32_t step_bytes;
     size_t ws_part, ws_cnt, ws_stats, ws_total;
@@ -1796,7 +1996,10 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 inline bool make_plan(int qtype, int64_t n_out, int64_t k_in, bool pair, bool head, int sms, QmmPlan &p) {
     if (k_in <= 0 || k_in % 32 || n_out <= 0) return false;
-    const int rec = qtype == SD_Q8_0 ? 1088 : 576;
+    const int GR = is_kq(qtype) ? 8 : 1;  // K-quants: pieces never split a 256-weight super-block
+    if (GR > 1 && (k_in % 256 || n_out % 32)) return false;
+    const int rec = step_bytes_q(qtype);
+    p.GR = GR;
     p.KB = static_cast<int32_t>(k_in / 32);
     if (pair) {
         if (n_out % 64) return false;
@@ -1805,17 +2008,18 @@ inline bool make_plan(int qtype, int64_t n_out, int64_t k_in, bool pair, bool he
         p.NU = static_cast<int32_t>((n_out + 31) / 32);
     }
     p.KS = (p.KB + KB_SPLIT_MAX - 1) / KB_SPLIT_MAX;
-    p.KBs = (p.KB + p.KS - 1) / p.KS;
+    p.KBs = ((p.KB + p.KS - 1) / p.KS + GR - 1) / GR * GR;
+    p.KS = (p.KB + p.KBs - 1) / p.KBs;
     p.KBlast = p.KB - p.KBs * (p.KS - 1);
     p.W = static_cast<int64_t>(p.NU) * (static_cast<int64_t>(p.KBs) * (p.KS - 1) + p.KBlast);
-    p.G = static_cast<int32_t>(p.W < sms ? p.W : sms);
+    p.G = static_cast<int32_t>(p.W / GR < sms ? p.W / GR : sms);
     // whole units per CTA when there is one split and at least one unit per CTA; the rest shared
     p.D = (p.KS == 1 && p.NU >= p.G) ? p.NU / p.G : 0;
     p.R = p.D > 0 ? p.NU - p.D * p.G : 0;
     const int64_t wseq = p.D > 0 ? static_cast<int64_t>(p.R) * p.KB : p.W;
-    const int64_t qmin = wseq / p.G;
-    int64_t P = qmin > 0 ? (static_cast<int64_t>(p.KBs) - 1) / qmin + 2 : p.KBs;
-    if (P > p.KBs) P = p.KBs;
+    const int64_t qmin = wseq / GR / p.G * GR;  // the shortest run, a whole number of granules
+    int64_t P = qmin > 0 ? (static_cast<int64_t>(p.KBs) - 1) / qmin + 2 : p.KBs / GR;
+    if (P > p.KBs / GR) P = p.KBs / GR;
     p.P = static_cast<int32_t>(P);
     const int64_t shared_units = p.D > 0 ? p.R : p.NU;  // units that may need partial sums
     p.step_bytes = static_cast<uint32_t>(rec * (pair ? 2 : 1));
@@ -1839,7 +2043,10 @@ inline bool make_plan(int qtype, int64_t n_out, int64_t k_in, bool pair, bool he
 
 // steps per stage (~36 KB stages, one mbarrier wait per 64 records): 64 records of 4-bit, 32
 // gate|up pairs, 32 Q8_0 records.  The consumers take a stage in sub-steps of sub_steps().
-inline int stage_steps(int qtype, bool pair) { return pair ? 4 * NCW : (qtype == SD_Q8_0 ? 4 * NCW : 8 * NCW); }
+inline int stage_steps(int qtype, bool pair) {
+    if (qtype == SD_Q6_K) return 4 * NCW;  // 4 super-records, 26.9 KB
+    return pair ? 4 * NCW : (qtype == SD_Q8_0 ? 4 * NCW : 8 * NCW);
+}
 
 struct SmemLayout {
     int NS, NRB, rows_p;
@@ -1851,9 +2058,9 @@ struct SmemLayout {
 // Shared memory for splits of up to `kbs` blocks, M positions, `rows` output rows per unit (64
 // with a gate|up pair), ring slots of `slot` bytes and `ss` bytes of block sums of squares.
 // Returns false when not even two ring stages fit.
-inline bool layout_smem(int kbs, int M, int rows, size_t slot, size_t ss, SmemLayout &L) {
+inline bool layout_smem(int kbs, int M, int rows, size_t slot, size_t ss, SmemLayout &L, int meta_qt = SD_Q4_32) {
     const size_t act = static_cast<size_t>(kbs) * af_frag_bytes(M);
-    const size_t meta = static_cast<size_t>(kbs) * af_meta_bytes(M);
+    const size_t meta = static_cast<size_t>(kbs) * af_meta_bytes_q(M, meta_qt);
     L.rows_p = rows + 4;
     L.NRB = M <= 8 ? 2 : 1;
     const size_t red = static_cast<size_t>(L.NRB) * NCW * M * L.rows_p * sizeof(float);
@@ -1899,7 +2106,7 @@ cudaError_t qmm_dispatch(QmmArgs a, QmmPlan &p, cudaStream_t s) {  // instantiat
     p.SB = stage_steps(QT, PAIR != 0);
     const size_t slot = static_cast<size_t>(p.SB) * p.step_bytes;
     SmemLayout L;
-    if (!layout_smem(p.KBs, a.M, PAIR ? 64 : 32, slot, 0, L)) return cudaErrorInvalidValue;
+    if (!layout_smem(p.KBs, a.M, PAIR ? 64 : 32, slot, 0, L, QT)) return cudaErrorInvalidValue;
     a.SB = p.SB;
     apply_layout(a, L, slot);
     a.kind = KIND_MATMUL;
@@ -1911,5 +2118,8 @@ cudaError_t qmm_dispatch(QmmArgs a, QmmPlan &p, cudaStream_t s) {  // instantiat
 extern template cudaError_t qmm_dispatch<SD_Q4_32, 0>(QmmArgs, QmmPlan &, cudaStream_t);
 extern template cudaError_t qmm_dispatch<SD_Q4_32, 1>(QmmArgs, QmmPlan &, cudaStream_t);
 extern template cudaError_t qmm_dispatch<SD_Q8_0, 0>(QmmArgs, QmmPlan &, cudaStream_t);
+extern template cudaError_t qmm_dispatch<SD_Q4_K, 0>(QmmArgs, QmmPlan &, cudaStream_t);
+extern template cudaError_t qmm_dispatch<SD_Q4_K, 1>(QmmArgs, QmmPlan &, cudaStream_t);
+extern template cudaError_t qmm_dispatch<SD_Q6_K, 0>(QmmArgs, QmmPlan &, cudaStream_t);
 
 }  // namespace sdv

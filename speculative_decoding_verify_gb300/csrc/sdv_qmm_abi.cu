@@ -42,10 +42,15 @@ static inline cudaStream_t cs(sd_stream_t s) { return reinterpret_cast<cudaStrea
 
 static cudaError_t dispatch(int qtype, bool pair, QmmArgs &a, QmmPlan &p, cudaStream_t s) {
     if (qtype == SD_Q4_32) return pair ? qmm_dispatch<SD_Q4_32, 1>(a, p, s) : qmm_dispatch<SD_Q4_32, 0>(a, p, s);
+    if (qtype == SD_Q4_K) return pair ? qmm_dispatch<SD_Q4_K, 1>(a, p, s) : qmm_dispatch<SD_Q4_K, 0>(a, p, s);
+    if (qtype == SD_Q6_K) return qmm_dispatch<SD_Q6_K, 0>(a, p, s);
     return qmm_dispatch<SD_Q8_0, 0>(a, p, s);
 }
 
+static bool known_qtype(int q) { return q == SD_Q8_0 || q == SD_Q4_32 || q == SD_Q4_K || q == SD_Q6_K; }
+
 static void fill_plan(QmmArgs &a, const QmmPlan &p) {
+    a.GR = p.GR;
     a.KB = p.KB;
     a.NU = p.NU;
     a.KS = p.KS;
@@ -67,7 +72,7 @@ extern "C" {
 
 int64_t sd_debug_schedule(int qtype, int64_t n_out, int64_t k_in, int32_t pair, int32_t head, int32_t sms,
                           int32_t *plan, int32_t *rows, int64_t cap) {
-    if ((qtype != SD_Q8_0 && qtype != SD_Q4_32) || sms < 1 || !plan) return -1;
+    if (!known_qtype(qtype) || sms < 1 || !plan) return -1;
     QmmPlan p;
     if (!make_plan(qtype, n_out, k_in, pair != 0, head != 0, sms, p)) return -1;
     QmmArgs a = {};
@@ -101,7 +106,7 @@ int64_t sd_debug_schedule(int qtype, int64_t n_out, int64_t k_in, int32_t pair, 
 }
 
 size_t sd_qmatmul_workspace_bytes(int qtype, int64_t n_out, int64_t k_in, uint32_t epilogue) {
-    if (qtype != SD_Q8_0 && qtype != SD_Q4_32) return 0;
+    if (!known_qtype(qtype)) return 0;
     QmmPlan p;
     if (!make_plan(qtype, n_out, k_in, epilogue == SD_EPI_SILU_MUL_REQUANT, false, num_sms(), p)) return 0;
     return p.ws_total;
@@ -117,12 +122,13 @@ sd_status sd_qmatmul_multipos(int qtype, const void *w, int64_t n_out, int64_t k
                               const float *scales, int32_t M, float *y, const float *residual, uint32_t epilogue,
                               int64_t requant_col0, int8_t *q_next, float *scales_next, void *workspace,
                               size_t ws_bytes, sd_stream_t stream) {
-    if (qtype != SD_Q8_0 && qtype != SD_Q4_32) return SD_EINVAL;
+    if (!known_qtype(qtype)) return SD_EINVAL;
     if (M < 1) return SD_EINVAL;
     if (M > 16) return SD_EUNSUPPORTED;
     if (!w || !q || !scales || !workspace) return SD_EINVAL;
     if (!aligned(w, 16) || !aligned(q, 16) || !aligned(scales, 4) || !aligned(workspace, 256)) return SD_EINVAL;
     if (k_in <= 0 || k_in % 32 || n_out <= 0) return SD_EINVAL;
+    if ((qtype == SD_Q4_K || qtype == SD_Q6_K) && (k_in % 256 || n_out % 32)) return SD_EINVAL;
     const bool pair = epilogue == SD_EPI_SILU_MUL_REQUANT;
     int64_t nq = 0;
     if (epilogue == SD_EPI_NONE) {
@@ -133,7 +139,7 @@ sd_status sd_qmatmul_multipos(int qtype, const void *w, int64_t n_out, int64_t k
             return SD_EINVAL;
         nq = n_out - requant_col0;
     } else if (pair) {
-        if (qtype != SD_Q4_32) return SD_EUNSUPPORTED;
+        if (qtype != SD_Q4_32 && qtype != SD_Q4_K) return SD_EUNSUPPORTED;
         if (!q_next || !scales_next || residual || n_out % 64) return SD_EINVAL;
         nq = n_out / 2;
     } else {

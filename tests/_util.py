@@ -95,3 +95,87 @@ def status_ok():
     torch.cuda.synchronize()
     st = sdv.device_status()
     assert st == 0, f"device status {st}"
+
+
+def unpack_kq_repacked(qtype, buf, n_out, k_in, pair=False):
+    """Inverse of the documented K-quant super-record layout -> GGUF super-blocks [n_out][k_in/256 * bb]
+    (Q4_K 144 B: d, dmin, 12 packed (scale, min) bytes, 128 code bytes; Q6_K 210 B: 128 low-nibble
+    bytes, 64 high-bit bytes, 16 int8 scales, d).  Codes: sub-block s plane, lane l = 4g + c, word j =
+    2t+s' holds nibble i at (row 16t+g+8[i&2], weight 32s + 16s'+2c+8[i&1]+(i>>2)); Q6_K high bits of
+    word j at the documented positions of the lane's high-bit word j//2."""
+    buf = np.asarray(buf, dtype=np.uint8)
+    SBK = k_in // 256
+    q4 = qtype == oracle.Q4_K
+    srb, bb, plane = (4736, 144, 512) if q4 else (6720, 210, 768)
+    halves = 2 if pair else 1
+    rows_per = n_out // 2 if pair else n_out
+    nt = rows_per // 32
+    sr = buf.reshape(nt, SBK, halves, srb)
+    code = np.zeros((nt, halves, 32, SBK, 256), dtype=np.int32)  # unsigned codes (Q6_K: 0..63)
+    p0 = [4, 8, 6, 10, 20, 24, 22, 26]
+    p1 = [0, 2, 12, 14, 16, 18, 28, 30]
+
+    def u32(a):
+        a = a.astype(np.uint32)
+        return a[..., 0] | (a[..., 1] << 8) | (a[..., 2] << 16) | (a[..., 3] << 24)
+
+    for s in range(8):
+        for lane in range(32):
+            g, c = lane >> 2, lane & 3
+            base = s * plane + lane * 16
+            words = u32(sr[..., base:base + 16].reshape(nt, SBK, halves, 4, 4))
+            if not q4:
+                hb = s * plane + 512 + lane * 8
+                hw = u32(sr[..., hb:hb + 8].reshape(nt, SBK, halves, 2, 4))
+            for j in range(4):
+                t, sk = j >> 1, j & 1
+                for i in range(8):
+                    row = 16 * t + g + (8 if i & 2 else 0)
+                    k = 32 * s + 16 * sk + 2 * c + (8 if i & 1 else 0) + (i >> 2)
+                    v = (words[..., j] >> (4 * i)) & 0xF
+                    if not q4:
+                        pos = (p1 if j & 1 else p0)[i]
+                        v = v | (((hw[..., j >> 1] >> pos) & 3) << 4)
+                    code[:, :, row, :, k] = v.transpose(0, 2, 1)
+    out = np.zeros((nt, halves, 32, SBK, bb), dtype=np.uint8)
+    for g in range(8):
+        for e, row in enumerate((g, g + 8, 16 + g, 24 + g)):
+            if q4:
+                sc = np.stack([sr[..., 4096 + 64 * s + 8 * g + e] for s in range(8)], -1).astype(np.int32)
+                mn = np.stack([sr[..., 4096 + 64 * s + 8 * g + 4 + e] for s in range(8)], -1).astype(np.int32)
+                b = np.zeros(sc.shape[:-1] + (12,), dtype=np.int32)
+                for s in range(4):
+                    b[..., s] = (sc[..., s] & 63) | ((sc[..., s + 4] >> 4) << 6)
+                    b[..., s + 4] = (mn[..., s] & 63) | ((mn[..., s + 4] >> 4) << 6)
+                    b[..., s + 8] = (sc[..., s + 4] & 15) | ((mn[..., s + 4] & 15) << 4)
+                dd = sr[..., 4608 + 16 * g + 4 * e:4608 + 16 * g + 4 * e + 4]
+                out[:, :, row, :, 0:4] = dd.transpose(0, 2, 1, 3)
+                out[:, :, row, :, 4:16] = b.astype(np.uint8).transpose(0, 2, 1, 3)
+            else:
+                scs = np.stack([sr[..., 6144 + 64 * s + 8 * g + 4 * h + e] for s in range(8) for h in range(2)], -1)
+                out[:, :, row, :, 192:208] = scs.transpose(0, 2, 1, 3)
+                out[:, :, row, :, 208:210] = sr[..., 6656 + 8 * g + 2 * e:6656 + 8 * g + 2 * e + 2].transpose(0, 2, 1, 3)
+    # codes into the file's order
+    i = np.arange(256)
+    if q4:
+        cidx, r = i // 64, i % 64
+        byte = 16 + 32 * cidx + (r % 32)
+        for hi in (0, 1):
+            sel = (r >= 32) == bool(hi)
+            vals = code[..., sel] << (4 * hi)
+            out[..., byte[sel]] |= vals.astype(np.uint8)
+    else:
+        n_, r = i // 128, i % 128
+        l, kq = r % 32, r // 32
+        lo_byte = 64 * n_ + l + 32 * (kq & 1)
+        hi_byte = 128 + 32 * n_ + l
+        for sel_k in range(4):
+            sel = kq == sel_k
+            lo = code[..., sel] & 15
+            out[..., lo_byte[sel]] |= (lo << (4 if sel_k >= 2 else 0)).astype(np.uint8)
+            out[..., hi_byte[sel]] |= ((code[..., sel] >> 4) << (2 * sel_k)).astype(np.uint8)
+    o = out.reshape(nt, halves, 32, SBK * bb)
+    res = np.zeros((n_out, SBK * bb), dtype=np.uint8)
+    for h in range(halves):
+        res[h * rows_per:(h + 1) * rows_per] = o[:, h].reshape(rows_per, SBK * bb)
+    return res

@@ -1068,3 +1068,27 @@ def test_tree_path_names_the_accepted_tokens():
         assert path[0] == 0 and len(path) == len(out)
         assert all(parent[path[i]] == path[i - 1] for i in range(1, len(path)))
         assert list(tokens[path[1:]]) + [argmax[path[-1]]] == list(out)
+
+
+@pytest.mark.parametrize("qtype", [oracle.Q4_K, oracle.Q6_K])
+def test_kq_matmul_bound_is_the_absolute_sum(qtype):
+    """The tolerance scale returned with the K-quant product is the absolute sum of its terms: at least
+    |y| everywhere, and equal to y when every weight and activation is non-negative (no cancellation).
+    Q4_K with zero minima and Q6_K with codes >= 32 and positive scales make every term >= 0."""
+    N, K, M = 8, 512, 3
+    w = sdgen.random_kq_blocks(qtype, sdgen.key(190, qtype), N, K).reshape(N, K // 256, -1)
+    q, s = oracle.rmsnorm_quant(np.abs(sdgen.normal(sdgen.key(191), (M, K))), None)
+    y, ab = oracle.kq_matmul(qtype, w, N, K, q, s, with_bound=True)
+    assert np.all(ab >= np.abs(y) * (1 - 1e-12))
+    w2 = w.copy()
+    if qtype == oracle.Q4_K:
+        w2[..., 4:16] &= 0x3F                    # sub-blocks 0-3: minima 0 (bytes 4-7: scales, 8-11: minima)
+        w2[..., 8:12] = 0
+        w2[..., 12:16] &= 0x0F                   # sub-blocks 4-7: minima 0
+        w2[..., 4:8] &= 0x3F                     # and the high bits of the minima of 4-7
+    else:
+        w2[..., 128:192] = 0xAA                  # high bits 2 for every code: codes 32..47
+        w2[..., 192:208] = 5                     # positive scales
+    y2, ab2 = oracle.kq_matmul(qtype, w2, N, K, q, s, with_bound=True)
+    assert np.all(y2 >= 0)
+    assert np.allclose(ab2, y2, rtol=1e-12, atol=0)

@@ -7,7 +7,7 @@ import ctypes
 import numpy as np
 import pytest
 
-Q8_0, Q4_32 = 0, 1
+Q8_0, Q4_32, Q4_K, Q6_K = 0, 1, 2, 3
 
 
 @pytest.fixture(scope="module")
@@ -35,6 +35,9 @@ SHAPES = [
     (Q4_32, 512, 512, False, False), (Q8_0, 33, 64, False, False), (Q4_32, 1024, 1024, True, False),
     (Q4_32, 640, 17408, False, False), (Q8_0, 4096, 1024, False, True), (Q4_32, 65536, 17408, False, False),
     (Q4_32, 32, 32, False, False), (Q8_0, 100, 2048, False, False),
+    # K-quant super-blocks: every piece a whole number of 256-weight super-blocks
+    (Q4_K, 3 * 5120, 5120, False, False), (Q4_K, 2 * 17408, 5120, True, False), (Q6_K, 5120, 17408, False, False),
+    (Q4_K, 32, 256, False, False), (Q6_K, 640, 17408, False, False), (Q4_K, 4800, 2560, False, False),
 ]
 
 
@@ -48,9 +51,12 @@ def test_partition_covers_every_step_once(L, qtype, n_out, k_in, pair, head, sms
     seen = {}
     owners = {}
     work = np.zeros(G, np.int64)
+    gr = 8 if qtype in (Q4_K, Q6_K) else 1
+    assert KBs % gr == 0 and KBlast % gr == 0
     for cta, s, u, j0, j1, first, np_, last in rows:
         ln = KBlast if s == KS - 1 else KBs
         assert 0 <= s < KS and 0 <= u < NU and 0 <= j0 < j1 <= ln  # never crosses a unit-split
+        assert j0 % gr == 0 and j1 % gr == 0                       # nor a K-quant super-block
         assert first <= cta < first + np_
         key = (s, u)
         owners.setdefault(key, set()).add(int(cta))
@@ -71,7 +77,7 @@ def test_partition_covers_every_step_once(L, qtype, n_out, k_in, pair, head, sms
     W = KB * NU
     assert work.sum() == W
     # balance: the shared steps split evenly, whole units in equal numbers
-    assert work.max() - work.min() <= (KB if p["D"] > 0 else 1) + 1
+    assert work.max() - work.min() <= (KB if p["D"] > 0 else gr) + gr
     # every CTA has work, and its last piece is the one flagged last
     ctas = rows[:, 0]
     assert set(ctas.tolist()) == set(range(G))
