@@ -79,7 +79,7 @@ typedef enum { SD_Q8_0 = 0, SD_Q4_32 = 1, SD_Q4_K = 2, SD_Q6_K = 3 } sd_qtype;
 #define SD_EPI_SILU_MUL_REQUANT 2u  /* gate|up pair: h = silu(g) * u, requantised into q_next/scales_next */
 
 const char *sd_status_string(sd_status s);
-int sd_abi_version(void); /* 2: sd_pass_desc and sd_pass carry the acceptance mode */
+int sd_abi_version(void); /* 3: sd_pass_desc carries the down projections' format, sd_pass the K-quant flag */
 
 /*
  * Load-time repack ("Inside OpenJet Engine", section "One GPU launch for a
@@ -433,8 +433,11 @@ sd_status sd_accept_sample_topk(const float *logits, int64_t vocab, int32_t K, c
  * to 2 s, SD_ETIMEOUT in the status word on expiry); the weight stream never
  * waits for it.
  *
- * sd_layer / sd_pass_desc: device pointers to repacked weights (gate_up repacked
- * with SD_REPACK_PAIR_GATE_UP, 4-bit) and fp32 norm weights [hidden]; h [M][hidden]
+ * sd_layer / sd_pass_desc: device pointers to repacked weights in format wq
+ * (SD_Q4_32 or SD_Q4_K; gate_up repacked with SD_REPACK_PAIR_GATE_UP; down in
+ * wq_down) and fp32 norm weights [hidden]; the head is Q8_0.  K-quant stacks
+ * (hidden and ffn multiples of 256) take greedy acceptance only
+ * (SD_EUNSUPPORTED otherwise).  h [M][hidden]
  * is the residual stream (input rows in, final hidden state out); qa/sa
  * [M][hidden], qv/sv [M][hidden], qf/sf [M][ffn] (and [.../32] scales) are
  * activation scratch; logits [M][vocab], argmax/row_max/row_sumexp [M];
@@ -490,6 +493,8 @@ typedef struct {
     int64_t base_pos;
     int32_t top_k;         /* SD_ACCEPT_SAMPLE: 0 = unfiltered target (sd_accept_sample), 1..32 = */
     float top_p;           /* the filtered target of sd_accept_sample_topk with top_p in (0, 1] */
+    int32_t wq_down;       /* format of the down projections: 0 = wq; SD_Q6_K with wq = SD_Q4_K (the */
+                           /* Q4_K_M recipe: Q4_K projections, Q6_K down projections) */
 } sd_pass_desc;
 
 typedef enum { SD_ACCEPT_GREEDY = 0, SD_ACCEPT_SAMPLE = 1 } sd_accept_mode;
@@ -501,6 +506,7 @@ typedef struct {
     uint32_t smem_bytes;
     int32_t grid;
     int32_t accept; /* the descriptor's acceptance mode */
+    int32_t kq;     /* 1 when the stack's weights are K-quants */
 } sd_pass;
 
 size_t sd_pass_plan_bytes(int32_t n_layers);

@@ -49,14 +49,16 @@ class SdPassDesc(ctypes.Structure):
                 ("tokens", ctypes.c_void_p), ("parent", ctypes.c_void_p), ("out_tokens", ctypes.c_void_p),
                 ("out_count", ctypes.c_void_p), ("workspace", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t),
                 ("accept", ctypes.c_int32), ("q_probs", ctypes.c_void_p), ("seed", ctypes.c_uint64),
-                ("base_pos", ctypes.c_int64), ("top_k", ctypes.c_int32), ("top_p", ctypes.c_float)]
+                ("base_pos", ctypes.c_int64), ("top_k", ctypes.c_int32), ("top_p", ctypes.c_float),
+                ("wq_down", ctypes.c_int32)]
 
 ACCEPT_GREEDY, ACCEPT_SAMPLE = 0, 1
 
 
 class SdPass(ctypes.Structure):
     _fields_ = [("plan", ctypes.c_void_p), ("n_phases", ctypes.c_int32), ("nt", ctypes.c_int32),
-                ("smem_bytes", ctypes.c_uint32), ("grid", ctypes.c_int32), ("accept", ctypes.c_int32)]
+                ("smem_bytes", ctypes.c_uint32), ("grid", ctypes.c_int32), ("accept", ctypes.c_int32),
+                ("kq", ctypes.c_int32)]
 
 
 class SdDepthState(ctypes.Structure):

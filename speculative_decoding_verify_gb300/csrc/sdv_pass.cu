@@ -19,7 +19,8 @@ struct PassHeader {
 };
 
 static cudaError_t pass_launch(const QmmArgs *phases, int n_phases, uint32_t *ctr, uint64_t *trace, int nt,
-                               int sample, size_t smem, int grid, cudaStream_t s) {
+                               int sample, int kq, size_t smem, int grid, cudaStream_t s) {
+    if (kq) return pass_launch_kq(phases, n_phases, ctr, trace, nt, smem, grid, s);
     if (sample) return pass_launch_sampling(phases, n_phases, ctr, trace, nt, smem, grid, s);
     return pass_launch_kernel(nt == 1 ? pass_kernel<1, false> : pass_kernel<2, false>, phases, n_phases, ctr, trace,
                               smem, grid, s);
@@ -44,6 +45,7 @@ static bool pass_ws_layout(int64_t H, int64_t F, int64_t V, int wq, int sms, Pas
     size_t part = 0;
     const int64_t shapes[4][3] = {{3 * H, H, 0}, {H, H, 0}, {2 * F, H, 1}, {H, F, 0}};
     for (auto &sh : shapes) {
+        // a K-quant stack's down projection may be Q6_K: the plan (and so the partial sums) is the same
         if (!make_plan(wq, sh[0], sh[1], sh[2] != 0, false, sms, p)) return false;
         part = p.ws_part > part ? p.ws_part : part;
     }
@@ -51,7 +53,7 @@ static bool pass_ws_layout(int64_t H, int64_t F, int64_t V, int wq, int sms, Pas
     part = p.ws_part > part ? p.ws_part : part;
     const size_t KBH = static_cast<size_t>(H / 32), KBF = static_cast<size_t>(F / 32);
     const size_t fb = af_frag_bytes(16) > af_frag_bytes(8) ? af_frag_bytes(16) : af_frag_bytes(8);
-    const size_t mb = af_meta_bytes(16);
+    const size_t mb = af_meta_bytes_q(16, is_kq(wq) ? SD_Q4_K : SD_Q4_32);
     size_t off = WS_CNT_BYTES;
     L.part = off;
     off += part;
@@ -97,8 +99,13 @@ sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, 
     const int M = d->M;
     if (L < 0 || M < 1 || H <= 0 || F <= 0 || V <= 0 || H % 64 || F % 32 || !d->layers) return SD_EINVAL;
     if (M > 16 || H / 32 > PASS_NORM_MAX_KB) return SD_EUNSUPPORTED;
-    if (d->wq != SD_Q4_32 && d->wq != SD_Q8_0) return SD_EINVAL;
-    if (d->wq == SD_Q8_0) return SD_EUNSUPPORTED;  // the SiLU*mul epilogue needs the 4-bit gate|up pairing
+    if (d->wq != SD_Q4_32 && d->wq != SD_Q8_0 && d->wq != SD_Q4_K && d->wq != SD_Q6_K) return SD_EINVAL;
+    if (d->wq == SD_Q8_0 || d->wq == SD_Q6_K) return SD_EUNSUPPORTED;  // the SiLU*mul epilogue needs a paired format
+    const int wqd = d->wq_down == 0 ? d->wq : d->wq_down;  // the down projections' format
+    if (wqd != d->wq && !(d->wq == SD_Q4_K && wqd == SD_Q6_K)) return SD_EUNSUPPORTED;
+    const bool kq = is_kq(d->wq);
+    if (kq && (H % 256 || F % 256)) return SD_EINVAL;
+    if (kq && d->accept != SD_ACCEPT_GREEDY) return SD_EUNSUPPORTED;
     if (plan_bytes < sd_pass_plan_bytes(L)) return SD_EINVAL;
     if (!d->h || !d->qa || !d->sa || !d->qv || !d->sv || !d->qf || !d->sf || !d->final_norm || !d->head ||
         !d->logits || !d->argmax || !d->row_max || !d->row_sumexp || !d->out_tokens || !d->out_count ||
@@ -141,7 +148,7 @@ sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, 
     auto matmul = [&](int qt, const void *w, int64_t n, int64_t k, bool pair, const int8_t *q, const float *sc,
                       const uint8_t *af_f, const float *af_m) -> QmmArgs * {
         QmmPlan p;
-        if (!make_plan(qt, n, k, pair, false, sms, p) || p.G != sms) return nullptr;
+        if (!make_plan(qt, n, k, pair, false, sms, p)) return nullptr;  // CTAs past p.G sit the phase out
         if (!w || !aligned(w, 16)) return nullptr;
         QmmArgs a;
         base(a);
@@ -231,8 +238,8 @@ sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, 
         a->nq = F;
         a->af_out_frag = aff_f;
         a->af_out_meta = aff_m;
-        a->af_out_qt = d->wq;
-        if (!(a = matmul(d->wq, lw.down, H, F, false, d->qf, d->sf, aff_f, aff_m))) return SD_EINVAL;
+        a->af_out_qt = wqd;
+        if (!(a = matmul(wqd, lw.down, H, F, false, d->qf, d->sf, aff_f, aff_m))) return SD_EINVAL;
         const bool lastl = l + 1 == L;
         if (!lastl && !d->layers[l + 1].norm1) return SD_EINVAL;
         residual_out(a, lastl ? d->final_norm : d->layers[l + 1].norm1, lastl ? SD_Q8_0 : d->wq);
@@ -301,7 +308,9 @@ sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, 
             slot = sz > slot ? sz : slot;
         }
     SmemLayout lay;
-    if (!layout_smem(kbs, M, 64, slot, static_cast<size_t>(M) * ss_ld * sizeof(float), lay)) return SD_EUNSUPPORTED;
+    if (!layout_smem(kbs, M, 64, slot, static_cast<size_t>(M) * ss_ld * sizeof(float), lay,
+                     kq ? SD_Q4_K : SD_Q4_32))
+        return SD_EUNSUPPORTED;
     if (static_cast<size_t>(lay.NS) * slot < sizeof(SampleShared) || static_cast<size_t>(lay.NS) * slot < sizeof(TopkShared))
         return SD_EUNSUPPORTED;  // the sampler's state
     for (QmmArgs &a : ph) apply_layout(a, lay, slot);
@@ -316,6 +325,7 @@ sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, 
     out->smem_bytes = static_cast<uint32_t>(lay.total);
     out->grid = sms;
     out->accept = d->accept;
+    out->kq = kq ? 1 : 0;
     return SD_OK;
 }
 
@@ -326,7 +336,7 @@ static sd_status verify_pass_launch(const sd_pass *p, uint64_t *trace, sd_stream
     uint8_t *plan = static_cast<uint8_t *>(p->plan);
     const QmmArgs *phases = reinterpret_cast<const QmmArgs *>(plan + sizeof(PassHeader));
     uint32_t *ctr = reinterpret_cast<uint32_t *>(plan);
-    return pass_launch(phases, p->n_phases, ctr, trace, p->nt, p->accept, p->smem_bytes, p->grid,
+    return pass_launch(phases, p->n_phases, ctr, trace, p->nt, p->accept, p->kq, p->smem_bytes, p->grid,
                        reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? SD_OK
                : SD_ECUDA;

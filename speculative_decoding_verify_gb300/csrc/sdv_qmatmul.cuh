@@ -265,6 +265,11 @@ struct PieceIter {
 __host__ __device__ __forceinline__ void pieces_begin_cta(const QmmArgs &a, PieceIter &it, int cta) {
     const int64_t c = cta, wq = seq_len(a) / a.GR;
     it.cta = cta;
+    if (cta >= a.G) {  // a matmul with fewer granules of work than the grid has CTAs: none for this one
+        it.g = it.hi = 0;
+        it.d_next = it.d_end = 0;
+        return;
+    }
     it.g = c * wq / a.G * a.GR;
     it.hi = (c + 1) * wq / a.G * a.GR;
     it.d_next = a.D > 0 ? a.R + static_cast<int>(c) * a.D : 0;
@@ -514,12 +519,27 @@ __device__ __forceinline__ void af_write(uint8_t *frag, float *meta, int M, int6
     if (lane < 4) {
         const int64_t idx = (jb * M + m) * 4 + c;
         if (NT == 1) {
-            const float hs = qt == SD_Q4_32 ? 0.0625f : 1.0f;
+            const float hs = qt != SD_Q8_0 ? 0.0625f : 1.0f;  // 4-bit and K-quant consumers: k+8 halves / 16
             reinterpret_cast<uint4 *>(frag)[idx] =
                 make_uint4(pack_h2(e0, e1, 1.0f), pack_h2(e2, e3, hs), pack_h2(e4, e5, 1.0f), pack_h2(e6, e7, hs));
         } else {
             reinterpret_cast<uint2 *>(frag)[idx] = make_uint2(pack_b4(e0, e1, e2, e3), pack_b4(e4, e5, e6, e7));
         }
+    }
+    if (is_kq(qt)) {  // {c0, c1, d, S} from the code sums of the block's four 8-weight quarters
+        int x = v;
+        x += __shfl_xor_sync(0xffffffffu, x, 1);
+        x += __shfl_xor_sync(0xffffffffu, x, 2);
+        x += __shfl_xor_sync(0xffffffffu, x, 4);
+        const int s4[4] = {__shfl_sync(0xffffffffu, x, 0), __shfl_sync(0xffffffffu, x, 8),
+                           __shfl_sync(0xffffffffu, x, 16), __shfl_sync(0xffffffffu, x, 24)};
+        if (lane == 0) {
+            float4 *mp = reinterpret_cast<float4 *>(meta) + jb * 8 * NT;
+            mp[m] = qt == SD_Q4_K ? kq_meta<SD_Q4_K>(s4, d) : kq_meta<SD_Q6_K>(s4, d);
+            if (m == M - 1)
+                for (int p = M; p < 8 * NT; ++p) mp[p] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+        return;
     }
     if (lane == 0) {
         float2 *mp = reinterpret_cast<float2 *>(meta) + jb * 8 * NT;
@@ -1242,6 +1262,7 @@ template <int QT, int PAIR, int NT>
 __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t &it, uint32_t &pk, uint32_t &act_it,
                                      uint32_t &nrm_it, CtaShared &cs, bool pre_issued = false,
                                      uint64_t *tslot = nullptr) {
+    if (static_cast<int>(blockIdx.x) >= a.G) return true;  // no work for this CTA in this phase
     const int M = a.M;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int lg = lane >> 2, lc = lane & 3;
@@ -1471,6 +1492,7 @@ __device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &
     constexpr int FIN_MPW = (8 * NT + NF - 1) / NF;  // positions per finisher warp at most
     constexpr int CH = 8;                            // partial sums loaded together
     constexpr int FKS = 8, FP = 4;                   // splits x pieces held at once when all splits share
+    if (static_cast<int>(blockIdx.x) >= a.G) return true;  // no work for this CTA in this phase
     const int M = a.M;
     const int lane = threadIdx.x & 31;
     int st_cur = -1, st_n = 0;  // head: current statistics tile and tiles finished in it
@@ -1847,7 +1869,9 @@ __device__ __forceinline__ void pass_topk_accept(const QmmArgs &sa, uint8_t *scr
                               []() { named_bar_sync(BAR_WORK, WORK_THREADS); });
 }
 
-template <int NT, bool SAMPLE>
+// KQ: the stack's projections are K-quants (Q4_K, Q6_K) instead of the 32-weight 4-bit format; a separate
+// instantiation, so each pass carries the consumer loops of its own formats only
+template <int NT, bool SAMPLE, bool KQ = false>
 __global__ void __launch_bounds__(QMM_THREADS, 1)
     pass_kernel(const QmmArgs *__restrict__ phases, int n_phases, uint32_t *barrier_ctr, uint64_t *trace) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -1938,10 +1962,16 @@ __global__ void __launch_bounds__(QMM_THREADS, 1)
         } else if (warp >= FIN_WARP0) {
             const int f = warp - FIN_WARP0;
             ok = sa.pair ? finish_phase<1, NT>(sa, sm, pk, fin_it, cs, f) : finish_phase<0, NT>(sa, sm, pk, fin_it, cs, f);
-        } else if (sa.qt == SD_Q4_32 && sa.pair) {
-            ok = consume_phase<SD_Q4_32, 1, NT>(sa, sm, it, pk, act_it, nrm_it, cs, pre, tslot(p));
-        } else if (sa.qt == SD_Q4_32) {
-            ok = consume_phase<SD_Q4_32, 0, NT>(sa, sm, it, pk, act_it, nrm_it, cs, pre, tslot(p));
+        } else if (KQ && sa.qt == SD_Q4_K && sa.pair) {
+            if constexpr (KQ) ok = consume_phase<SD_Q4_K, 1, NT>(sa, sm, it, pk, act_it, nrm_it, cs, pre, tslot(p));
+        } else if (KQ && sa.qt == SD_Q4_K) {
+            if constexpr (KQ) ok = consume_phase<SD_Q4_K, 0, NT>(sa, sm, it, pk, act_it, nrm_it, cs, pre, tslot(p));
+        } else if (KQ && sa.qt == SD_Q6_K) {
+            if constexpr (KQ) ok = consume_phase<SD_Q6_K, 0, NT>(sa, sm, it, pk, act_it, nrm_it, cs, pre, tslot(p));
+        } else if (!KQ && sa.qt == SD_Q4_32 && sa.pair) {
+            if constexpr (!KQ) ok = consume_phase<SD_Q4_32, 1, NT>(sa, sm, it, pk, act_it, nrm_it, cs, pre, tslot(p));
+        } else if (!KQ && sa.qt == SD_Q4_32) {
+            if constexpr (!KQ) ok = consume_phase<SD_Q4_32, 0, NT>(sa, sm, it, pk, act_it, nrm_it, cs, pre, tslot(p));
         } else {
             ok = consume_phase<SD_Q8_0, 0, NT>(sa, sm, it, pk, act_it, nrm_it, cs, pre, tslot(p));
         }
@@ -1981,6 +2011,9 @@ inline cudaError_t pass_launch_kernel(void (*k)(const QmmArgs *, int, uint32_t *
 // the sampling instantiations, compiled in their own translation unit (sdv_pass_sample.cu)
 cudaError_t pass_launch_sampling(const QmmArgs *phases, int n_phases, uint32_t *ctr, uint64_t *trace, int nt,
                                  size_t smem, int grid, cudaStream_t s);
+// the K-quant instantiations (greedy acceptance), in sdv_pass_kq.cu
+cudaError_t pass_launch_kq(const QmmArgs *phases, int n_phases, uint32_t *ctr, uint64_t *trace, int nt, size_t smem,
+                           int grid, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // host side: plan + launch

@@ -26,12 +26,14 @@ class VerifyStack:
 
     def __init__(self, layers, norms, final_norm, head_w, hidden: int, ffn: int, vocab: int, M: int,
                  wq: int = Q4_32, head_q: int = Q8_0, eps: float = 1e-6, tree_parent: torch.Tensor | None = None,
-                 device="cuda"):
+                 device="cuda", wq_down: int | None = None):
         """layers: list of dicts {qkv, o, gate_up, down} of REPACKED uint8 CUDA tensors (gate_up repacked with
-        the gate|up pairing).  norms: list of (norm1, norm2) fp32 CUDA tensors [hidden]."""
+        the gate|up pairing).  norms: list of (norm1, norm2) fp32 CUDA tensors [hidden].  wq: format of the
+        projections (Q4_32 or Q4_K); wq_down: of the down projections (default wq; Q6_K with Q4_K)."""
         assert head_q == Q8_0
         self.layers, self.norms, self.final_norm, self.head_w = layers, norms, final_norm, head_w
         self.H, self.F, self.V, self.M, self.wq, self.eps = hidden, ffn, vocab, M, wq, eps
+        self.wq_down = wq if wq_down is None else wq_down
         H, F, V = hidden, ffn, vocab
         f32 = dict(dtype=torch.float32, device=device)
         i8 = dict(dtype=torch.int8, device=device)
@@ -54,7 +56,7 @@ class VerifyStack:
         ws = max(qmatmul_workspace_bytes(wq, 3 * H, H, EPI_REQUANT),
                  qmatmul_workspace_bytes(wq, H, H, EPI_NONE),
                  qmatmul_workspace_bytes(wq, 2 * F, H, EPI_SILU_MUL_REQUANT),
-                 qmatmul_workspace_bytes(wq, H, F, EPI_NONE),
+                 qmatmul_workspace_bytes(self.wq_down, H, F, EPI_NONE),
                  head_workspace_bytes(V, H), pass_workspace_bytes(H, F, V, wq))
         self.ws = workspace(ws, device)
         self.graph = None
@@ -72,7 +74,7 @@ class VerifyStack:
         rmsnorm_quant_acts(self.h, n2, self.qa, self.sa, self.eps)
         qmatmul_multipos(wq, w["gate_up"], 2 * F, H, self.qa, self.sa, self.ws, epilogue=EPI_SILU_MUL_REQUANT,
                          q_next=self.qf, scales_next=self.sf)
-        qmatmul_multipos(wq, w["down"], H, F, self.qf, self.sf, self.ws, y=self.h, residual=self.h)
+        qmatmul_multipos(self.wq_down, w["down"], H, F, self.qf, self.sf, self.ws, y=self.h, residual=self.h)
 
     def head(self, temperature: float = 1.0):
         rmsnorm_quant_acts(self.h, self.final_norm, self.qa, self.sa, self.eps)
@@ -123,7 +125,8 @@ class VerifyStack:
                        p(self.qa), p(self.sa), p(self.qv), p(self.sv), p(self.qf), p(self.sf), p(self.logits),
                        p(self.argmax), p(self.row_max), p(self.row_sumexp), p(self.tokens), p(self.parent),
                        p(self.out_tokens), p(self.out_count), p(self.ws), self.ws.numel(),
-                       ACCEPT_SAMPLE if sample else ACCEPT_GREEDY, p(q_probs), seed, base_pos, top_k, top_p)
+                       ACCEPT_SAMPLE if sample else ACCEPT_GREEDY, p(q_probs), seed, base_pos, top_k, top_p,
+                       0 if self.wq_down == self.wq else self.wq_down)
         self._plan = torch.zeros(pass_plan_bytes(L), dtype=torch.uint8, device=self.h.device)
         self.fused = pass_prepare(d, self._plan)
         return self.fused

@@ -131,3 +131,73 @@ def test_kq_epilogues(sdv):
                                         torch.from_numpy(np.ascontiguousarray(gu[:, F:])).cuda())
     status_ok()
     assert torch.equal(gq, qf) and torch.equal(gs, sf)
+
+
+# ---------------------------------------------------------------------------
+# the one-launch pass over a K-quant stack (Q4_K projections, Q6_K down projections, Q8_0 head)
+# ---------------------------------------------------------------------------
+
+def kq_stack(sdv, L=3, H=512, F=1024, V=4096):
+    from speculative_decoding_verify_gb300.verify_pass import repack_matrix
+    spec = sdgen.StackSpec(layers=L, hidden=H, ffn=F, vocab=V, seed=3)
+    layers, norms = [], []
+    for l in range(L):
+        lw = {}
+        for name, n, k in spec.matrices():
+            qt = Q6_K if name == "down" else Q4_K
+            # small super-block scales keep weights near the 0.02 of the other stacks
+            b = sdgen.random_kq_blocks(qt, sdgen.key(184, l, n, k), n, k, d_scale=2e-5)
+            lw[name] = repack_matrix(qt, b, n, k, pair=(name == "gate_up"))
+        layers.append(lw)
+        n1, n2 = spec.norms(l)
+        norms.append((cuda(n1), cuda(n2)))
+    head = repack_matrix(spec.head_q, spec.head(), V, H)
+    return spec, layers, norms, head
+
+
+def kq_make(env, M, parent=None):
+    from speculative_decoding_verify_gb300.verify_pass import VerifyStack
+    spec, layers, norms, head = env
+    return VerifyStack(layers, norms, cuda(spec.final_norm()), head, spec.hidden, spec.ffn, spec.vocab, M,
+                       wq=Q4_K, wq_down=Q6_K, tree_parent=parent)
+
+
+@pytest.mark.parametrize("M", [1, 5, 16])
+def test_kq_fused_pass_equals_pipeline(sdv, M):
+    """The K-quant pass as one launch against the same calls issued one by one: hidden rows, logits,
+    statistics, every requantised activation and the accepted tokens, bit for bit (chain; a tree at
+    M = 16)."""
+    env = kq_stack(sdv)
+    spec = env[0]
+    parent = cuda(sdgen.tree16(0)[0]) if M == 16 else None
+    h0 = cuda(sdgen.normal(sdgen.key(185, M), (M, spec.hidden)))
+    a, b = kq_make(env, M, parent), kq_make(env, M, parent)
+    a.h.copy_(h0)
+    a.run()
+    torch.cuda.synchronize()
+    am = host(a.argmax)
+    tokens = np.array([am[i] if i < 2 else (am[i] + 1) % spec.vocab for i in range(M)], np.int32)
+    if M == 16:
+        tokens = np.roll(tokens, 1)
+    for st in (a, b):
+        st.h.copy_(h0)
+        st.tokens[:M].copy_(cuda(tokens))
+    a.run()
+    b.run_fused()
+    status_ok()
+    assert b.fused.kq == 1
+    for name in ("h", "logits", "argmax", "row_max", "row_sumexp", "qa", "sa", "qv", "sv", "qf", "sf"):
+        x, y = getattr(a, name), getattr(b, name)
+        assert torch.equal(x.view(torch.int32) if x.dtype == torch.float32 else x,
+                           y.view(torch.int32) if y.dtype == torch.float32 else y), name
+    assert np.isfinite(host(b.logits)).all()
+    n = int(host(a.out_count)[0])
+    assert n >= 1 and int(host(b.out_count)[0]) == n
+    assert torch.equal(a.out_tokens[:n], b.out_tokens[:n])
+
+
+def test_kq_pass_rejects_sampling_and_bad_widths(sdv):
+    env = kq_stack(sdv, L=1)
+    st = kq_make(env, 5)
+    with pytest.raises(sdv.SdError):
+        st.prepare_fused(sample=True)
