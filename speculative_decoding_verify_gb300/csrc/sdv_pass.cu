@@ -137,6 +137,7 @@ sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, 
     auto base = [&](QmmArgs &a) {
         a = QmmArgs{};
         a.GR = 1;
+        a.GRS = 0;
         a.M = M;
         a.status = st;
         a.cnt = reinterpret_cast<uint32_t *>(ws);
@@ -156,6 +157,7 @@ sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, 
         a.qt = qt;
         a.pair = pair ? 1 : 0;
         a.GR = p.GR;
+        a.GRS = p.GRS;
         a.KB = p.KB;
         a.NU = p.NU;
         a.KS = p.KS;

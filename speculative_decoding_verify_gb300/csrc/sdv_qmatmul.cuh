@@ -178,6 +178,7 @@ struct QmmArgs {
     int32_t ilv3;           // 0, or NU / 3: units taken in threes from the three thirds of the rows (see phys_unit)
     int32_t GR;             // schedule granule in blocks: every piece and split boundary is a multiple (8 for the
                             // 256-weight K-quant super-blocks, else 1)
+    int32_t GRS;            // log2 GR (the schedule walk shifts instead of dividing: it runs at every phase start)
 };
 
 constexpr int KIND_MATMUL = 0, KIND_NORM = 1, KIND_ACCEPT = 2, KIND_COMBINE = 3, KIND_HSTATS = 4;
@@ -230,8 +231,8 @@ __host__ __device__ __forceinline__ int64_t seq_len(const QmmArgs &a) { return a
 // CTA owning step x of the shared sequence: the CTAs' runs start at floor(c wq / G) granules (wq =
 // wseq / GR granules in all), so the owner is the largest c with floor(c wq / G) <= floor(x / GR)
 __host__ __device__ __forceinline__ int seq_owner(const QmmArgs &a, int64_t wseq, int64_t x) {
-    const int64_t wq = wseq / a.GR;
-    return wq > 0 ? static_cast<int>(((x / a.GR + 1) * a.G - 1) / wq) : 0;
+    const int64_t wq = wseq >> a.GRS;
+    return wq > 0 ? static_cast<int>((((x >> a.GRS) + 1) * a.G - 1) / wq) : 0;
 }
 
 // CTAs sharing split s of unit u, and the first of them
@@ -263,15 +264,15 @@ struct PieceIter {
 
 // The schedule of CTA `cta` (host and device: the host replays it to check the partition).
 __host__ __device__ __forceinline__ void pieces_begin_cta(const QmmArgs &a, PieceIter &it, int cta) {
-    const int64_t c = cta, wq = seq_len(a) / a.GR;
+    const int64_t c = cta, wq = seq_len(a) >> a.GRS;
     it.cta = cta;
     if (cta >= a.G) {  // a matmul with fewer granules of work than the grid has CTAs: none for this one
         it.g = it.hi = 0;
         it.d_next = it.d_end = 0;
         return;
     }
-    it.g = c * wq / a.G * a.GR;
-    it.hi = (c + 1) * wq / a.G * a.GR;
+    it.g = (c * wq / a.G) << a.GRS;
+    it.hi = ((c + 1) * wq / a.G) << a.GRS;
     it.d_next = a.D > 0 ? a.R + static_cast<int>(c) * a.D : 0;
     it.d_end = a.D > 0 ? it.d_next + a.D : 0;
 }
@@ -501,6 +502,7 @@ __device__ __forceinline__ uint32_t pack_b4(int x0, int x1, int x2, int x3) {
 // warp whose lane k holds the block's code v and whose scale is d.  qt: weight format of the
 // matmul that reads it.  Lanes 0..3 write the fragment entries, lane 0 the {corr, d} pair; the
 // writer of the last position also zeroes the pairs of the padding positions M .. 8 NT - 1.
+template <bool KQ = false>
 __device__ __forceinline__ void af_write(uint8_t *frag, float *meta, int M, int64_t jb, int m, int lane, int v,
                                          float d, int qt) {
     // S_lo + 65536 S_hi in one reduction; |S_lo| <= 16 * 127 < 32768 recovers both exactly
@@ -526,7 +528,7 @@ __device__ __forceinline__ void af_write(uint8_t *frag, float *meta, int M, int6
             reinterpret_cast<uint2 *>(frag)[idx] = make_uint2(pack_b4(e0, e1, e2, e3), pack_b4(e4, e5, e6, e7));
         }
     }
-    if (is_kq(qt)) {  // {c0, c1, d, S} from the code sums of the block's four 8-weight quarters
+    if (KQ && is_kq(qt)) {  // {c0, c1, d, S} from the code sums of the block's four 8-weight quarters
         int x = v;
         x += __shfl_xor_sync(0xffffffffu, x, 1);
         x += __shfl_xor_sync(0xffffffffu, x, 2);
@@ -562,7 +564,7 @@ __device__ __forceinline__ float tree32(float x, int lane) {
 // ---------------------------------------------------------------------------
 // epilogue of one finished (unit, position), run by the finisher warp: lane = row
 // ---------------------------------------------------------------------------
-template <int PAIR>
+template <int PAIR, bool KQ = false>
 __device__ __forceinline__ void epilogue(const QmmArgs &a, int u, int m, int lane, float v, float vu, float res, float nw) {
     if (PAIR) {
         const int64_t F = a.n_out / 2;
@@ -576,7 +578,7 @@ __device__ __forceinline__ void epilogue(const QmmArgs &a, int u, int m, int lan
         const int code = requant_lane(h, d);
         a.q_next[m * a.nq + n] = static_cast<int8_t>(code);
         if (lane == 0) a.s_next[m * (a.nq / 32) + u] = d;
-        if (a.af_out_frag) af_write(a.af_out_frag, a.af_out_meta, a.M, u, m, lane, code, d, a.af_out_qt);
+        if (a.af_out_frag) af_write<KQ>(a.af_out_frag, a.af_out_meta, a.M, u, m, lane, code, d, a.af_out_qt);
     } else {
         const int64_t n = static_cast<int64_t>(u) * 32 + lane;
         const bool ok = n < a.n_out;
@@ -590,7 +592,7 @@ __device__ __forceinline__ void epilogue(const QmmArgs &a, int u, int m, int lan
             float c;
             const int code = requant_lane(__fmul_rn(v, nw), c);
             a.q_next[m * a.nq + n] = static_cast<int8_t>(code);
-            af_write(a.af_out_frag, a.af_out_meta, a.M, u, m, lane, code, c, a.af_out_qt);
+            af_write<KQ>(a.af_out_frag, a.af_out_meta, a.M, u, m, lane, code, c, a.af_out_qt);
         }
         if (a.epi == SD_EPI_REQUANT && static_cast<int64_t>(u) * 32 >= a.col0) {
             float d;
@@ -599,7 +601,7 @@ __device__ __forceinline__ void epilogue(const QmmArgs &a, int u, int m, int lan
             if (ok) a.q_next[m * a.nq + c] = static_cast<int8_t>(code);
             if (lane == 0) a.s_next[m * (a.nq / 32) + c / 32] = d;
             if (a.af_out_frag)
-                af_write(a.af_out_frag, a.af_out_meta, a.M, (static_cast<int64_t>(u) * 32 - a.col0) / 32, m, lane, code,
+                af_write<KQ>(a.af_out_frag, a.af_out_meta, a.M, (static_cast<int64_t>(u) * 32 - a.col0) / 32, m, lane, code,
                          d, a.af_out_qt);
         }
     }
@@ -1485,7 +1487,7 @@ __device__ inline void head_flush(const QmmArgs &a, const Smem &sm, CtaShared &c
 // One matmul phase of the finisher warps.  For each piece, in the consumers' order: add the 8
 // consumer warps' partial sums (warp order), then finish the unit directly, or store the partial
 // and, if this CTA arrived last, add all partials in (split, piece) order and finish it.
-template <int PAIR, int NT>
+template <int PAIR, int NT, bool KQ = false>
 __device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &pk, uint32_t &fin_it, CtaShared &cs,
                                     int f) {
     constexpr int ROWS = PAIR ? 64 : 32;
@@ -1638,7 +1640,7 @@ __device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &
 #pragma unroll
             for (int i = 0; i < FIN_MPW; ++i) {
                 const int m = f + NF * i;
-                if (m < M) epilogue<PAIR>(a, up, m, lane, v[i], vu[i], res[i], nw);
+                if (m < M) epilogue<PAIR, KQ>(a, up, m, lane, v[i], vu[i], res[i], nw);
             }
         }
         if (finish && a.head && !a.defer_stats) {  // the same decisions on every finisher warp
@@ -1664,6 +1666,7 @@ __device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &
 // that matmul multiplies c by each row's inverse RMS when it stages them.
 // Later RMSNorms are formed the same way in the residual epilogues.
 // ---------------------------------------------------------------------------
+template <bool KQ = false>
 __device__ inline void norm_phase(const QmmArgs &a) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int M = a.M, KB = a.KB;
@@ -1679,7 +1682,7 @@ __device__ inline void norm_phase(const QmmArgs &a) {
             float c;
             const int v = requant_lane(__fmul_rn(x, a.norm_w[static_cast<int64_t>(b) * 32 + lane]), c);
             a.q_next[i] = static_cast<int8_t>(v);
-            af_write(a.af_out_frag, a.af_out_meta, M, b, m, lane, v, c, a.af_out_qt);
+            af_write<KQ>(a.af_out_frag, a.af_out_meta, M, b, m, lane, v, c, a.af_out_qt);
         }
     }
 }
@@ -1690,6 +1693,7 @@ __device__ inline void norm_phase(const QmmArgs &a) {
 // warp w (consumers and finishers, 0..10) takes (unit, position) items w,
 // w + 11, ...: the partial sums in (split, piece) order, then the epilogue.
 // ---------------------------------------------------------------------------
+template <bool KQ = false>
 __device__ inline void combine_phase(const QmmArgs &a, int widx) {
     constexpr int ROWS = 32, CH = 8, NWW = NCW + NF;
     constexpr int CKS = 8, CP = 4;  // splits and pieces per split held in registers at once
@@ -1728,7 +1732,7 @@ __device__ inline void combine_phase(const QmmArgs &a, int widx) {
                         v = first ? x[s2][c] : __fadd_rn(v, x[s2][c]);
                         first = false;
                     }
-            epilogue<0>(a, up, m, lane, v, 0.0f, res, nw);
+            epilogue<0, KQ>(a, up, m, lane, v, 0.0f, res, nw);
             continue;
         }
         for (int s2 = 0; s2 < a.KS; ++s2) {
@@ -1747,7 +1751,7 @@ __device__ inline void combine_phase(const QmmArgs &a, int widx) {
                     }
             }
         }
-        epilogue<0>(a, up, m, lane, v, 0.0f, res, nw);
+        epilogue<0, KQ>(a, up, m, lane, v, 0.0f, res, nw);
     }
 }
 
@@ -1935,7 +1939,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1)
         }
         bool ok = true;
         if (sa.kind == KIND_NORM) {
-            if (warp < NCW) norm_phase(sa);
+            if (warp < NCW) norm_phase<KQ>(sa);
         } else if (sa.kind == KIND_ACCEPT) {
             if (blockIdx.x == 0) {  // the deferred fold (one warp per position), then the acceptance
                 if (sa.defer_stats) {
@@ -1952,7 +1956,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1)
                 }
             }
         } else if (sa.kind == KIND_COMBINE) {
-            combine_phase(sa, warp < NCW ? warp : warp - 1);
+            combine_phase<KQ>(sa, warp < NCW ? warp : warp - 1);
         } else if (sa.kind == KIND_HSTATS) {  // (tile, position) items over every work warp of the grid
             constexpr int NWW = NCW + NF;
             const int n_items = sa.n_stiles * sa.M;
@@ -1961,7 +1965,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1)
                 head_tile_stats_one(sa, i / sa.M, i % sa.M, lane);
         } else if (warp >= FIN_WARP0) {
             const int f = warp - FIN_WARP0;
-            ok = sa.pair ? finish_phase<1, NT>(sa, sm, pk, fin_it, cs, f) : finish_phase<0, NT>(sa, sm, pk, fin_it, cs, f);
+            ok = sa.pair ? finish_phase<1, NT, KQ>(sa, sm, pk, fin_it, cs, f) : finish_phase<0, NT, KQ>(sa, sm, pk, fin_it, cs, f);
         } else if (KQ && sa.qt == SD_Q4_K && sa.pair) {
             if constexpr (KQ) ok = consume_phase<SD_Q4_K, 1, NT>(sa, sm, it, pk, act_it, nrm_it, cs, pre, tslot(p));
         } else if (KQ && sa.qt == SD_Q4_K) {
@@ -2019,7 +2023,7 @@ cudaError_t pass_launch_kq(const QmmArgs *phases, int n_phases, uint32_t *ctr, u
 // host side: plan + launch
 // ---------------------------------------------------------------------------
 struct QmmPlan {
-    int32_t KB, NU, KS, KBs, KBlast, G, P, D, R, SB, NS, NRB, rows_p, GR;
+    int32_t KB, NU, KS, KBs, KBlast, G, P, D, R, SB, NS, NRB, rows_p, GR, GRS;
     int64_t W;
     uint32_t step_bytes;
     size_t ws_part, ws_cnt, ws_stats, ws_total;
@@ -2033,6 +2037,7 @@ inline bool make_plan(int qtype, int64_t n_out, int64_t k_in, bool pair, bool he
     if (GR > 1 && (k_in % 256 || n_out % 32)) return false;
     const int rec = step_bytes_q(qtype);
     p.GR = GR;
+    p.GRS = GR == 8 ? 3 : 0;
     p.KB = static_cast<int32_t>(k_in / 32);
     if (pair) {
         if (n_out % 64) return false;

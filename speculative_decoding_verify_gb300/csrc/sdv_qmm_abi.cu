@@ -51,6 +51,7 @@ static bool known_qtype(int q) { return q == SD_Q8_0 || q == SD_Q4_32 || q == SD
 
 static void fill_plan(QmmArgs &a, const QmmPlan &p) {
     a.GR = p.GR;
+    a.GRS = p.GRS;
     a.KB = p.KB;
     a.NU = p.NU;
     a.KS = p.KS;
