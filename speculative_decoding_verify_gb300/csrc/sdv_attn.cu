@@ -10,19 +10,21 @@
 // reads KV head h / (H / H_kv); out = softmax(q k^T / sqrt(D)) v.
 //
 // The context is read once per KV head for all its query rows (M positions x the heads of the
-// group, up to 8 per CTA).  It is HBM-bound (about M/2 fp32 multiply-adds per cache byte at
-// M = 5), so it runs on the CUDA cores in fp32: a warp takes two keys per step, 16 lanes per key
-// with D/16 elements each for q.k (reduced by shuffles), then all 32 lanes with D/32 elements
-// each for the running p v; the next pair's K and V are loaded before the current pair is used.
-// The keys are split into chunks, one CTA of 4 warps per (chunk, query group, KV head); each CTA
-// leaves an unnormalised (max, sum, o) per row and a second kernel combines the chunks.
-// Scores are kept in log2 units (q is scaled by log2(e)/sqrt(D) once) and exponentials are exp2f.
+// group, up to 8 per CTA): the keys are split into chunks, one CTA per (chunk, query group, KV
+// head) streaming its K and V rows through shared memory (attn_tc_kernel below: fp16 tensor-core
+// products with fp32 accumulation); each CTA leaves an unnormalised (max, sum, o) per row and a
+// second kernel combines the chunks.  Scores are kept in log2 units (q is scaled by
+// log2(e)/sqrt(D) once) and exponentials are exp2f.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "sdv_common.cuh"
 
 namespace sdv {
 
 constexpr int AT_TQ = 8;     // query rows per CTA
-constexpr int AT_WARPS = 4;  // warps per attention CTA
 constexpr int AT_MIN_CHUNK_PAIRS = 32;
 constexpr float AT_NEG = -3.402823466e38f;  // running-max start: finite, below every score
 
@@ -58,177 +60,298 @@ __device__ __forceinline__ uint32_t path_mask(const AttnArgs &a, int i) {
     return m;
 }
 
+// ---------------------------------------------------------------------------
+// Tensor-core partial attention.  One CTA per (key chunk, query group of 8 rows, KV head): a producer
+// thread streams the chunk's K and V rows (fp16, as cached) into a ring of shared-memory stages of
+// AT_KT keys with tensor copies (TMA; tiles of AT_KT rows x 64 halves, 128-byte swizzled so the
+// fragment loads are free of bank conflicts; rows past the last key arrive as zeros); four
+// consumer warps each take 16 keys of a stage:
+//   S^T = K Q^T on mma m16n8k16 (keys x rows, fp32 accumulation), with q split into an fp16 high
+//   part and an fp16 remainder (two mma into the same accumulator), each row pre-scaled by a power
+//   of two so neither part is subnormal; scores in exp2 units;
+//   online softmax per row (running max and sum in fp32, masked keys at -inf);
+//   O^T += V^T P^T on the same mma, P split the same way (scaled by 2^14), its fragments moved from
+//   the score layout to the operand layout by register transposes (movmatrix).
+// Each warp keeps its own (max, sum, O) per row; the CTA merges its warps at the end and leaves one
+// partial per row for the combine kernel.
+// ---------------------------------------------------------------------------
+constexpr int AT_KT = 64;          // keys per stage (16 per consumer warp)
+constexpr int AT_NST = 2;          // ring stages (three CTAs per SM)
+constexpr int AT_CW = 4;           // consumer warps
+constexpr float AT_PS = 16384.0f;  // P scaling into the fp16 operand (a power of two: exact)
+
 template <int D>
-struct KvLane {
-    static constexpr int DL = D / 16;  // q.k elements per lane (16 lanes per key)
-    static constexpr int DV = D / 32;  // p v elements per lane
+struct AtLayout {
+    static constexpr int TILE = AT_KT * 128;              // one tensor tile: AT_KT rows x 64 halves
+    static constexpr int NB = D / 64;                     // tiles across a row
+    static constexpr int STAGE = 2 * NB * TILE;           // K tiles then V tiles
+    static constexpr int RING = AT_NST * STAGE;
+    static constexpr int BARS = RING;                     // full[AT_NST], empty[AT_NST], abort flag
+    static constexpr int TOTAL = 1024 + RING + 16 * AT_NST + 16;  // + room to align the ring to 1024 B
+    static_assert(AT_CW * AT_TQ * (D + 2) * 4 <= RING, "the warps' states fit in the ring");
 };
 
-template <int DL>
-__device__ __forceinline__ void load_k(const __half *row, int hl, float (&kf)[DL]) {
-    if constexpr (DL == 8) {
-        const uint4 r = __ldg(reinterpret_cast<const uint4 *>(row + hl * 8));
-        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[e]));
-            kf[2 * e] = f.x;
-            kf[2 * e + 1] = f.y;
-        }
-    } else {
-        const uint2 r = __ldg(reinterpret_cast<const uint2 *>(row + hl * 4));
-        const uint32_t w[2] = {r.x, r.y};
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[e]));
-            kf[2 * e] = f.x;
-            kf[2 * e + 1] = f.y;
-        }
-    }
+// byte offset, inside a stage's K or V tiles, of the 16-byte chunk holding halves d .. d+7 of row r
+// (the 128-byte swizzle: chunk j of a 128-byte row r sits at chunk j ^ (r & 7))
+template <int D>
+__device__ __forceinline__ uint32_t at_off(int r, int d) {
+    return static_cast<uint32_t>((d >> 6) * AtLayout<D>::TILE + r * 128 + ((((d & 63) >> 3) ^ (r & 7)) << 4));
 }
 
-template <int DV>
-__device__ __forceinline__ void load_v(const __half *row, int lane, float (&vf)[DV]) {
-    if constexpr (DV == 4) {
-        const uint2 r = __ldg(reinterpret_cast<const uint2 *>(row + lane * 4));
-        const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&r.x));
-        const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&r.y));
-        vf[0] = f0.x;
-        vf[1] = f0.y;
-        vf[2] = f1.x;
-        vf[3] = f1.y;
-    } else {
-        const uint32_t r = __ldg(reinterpret_cast<const unsigned int *>(row + lane * 2));
-        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&r));
-        vf[0] = f.x;
-        vf[1] = f.y;
-    }
+// one tile of a cache viewed as [H_kv][NK][D] halves (x = d, y = key, z = KV head)
+__device__ __forceinline__ void tma_3d(void *dst, const CUtensorMap *tm, int x, int y, int z, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+__device__ __forceinline__ void hmma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// (x0, x1) as an fp16 pair plus the fp16 pair of what that leaves over
+__device__ __forceinline__ void split_h2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    const __half2 h = __floats2half2_rn(x0, x1);
+    const float2 hf = __half22float2(h);
+    const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
 template <int D>
-__global__ void __launch_bounds__(32 * AT_WARPS) attn_partial_kernel(const AttnArgs a) {
-    constexpr int DL = KvLane<D>::DL, DV = KvLane<D>::DV;
-    __shared__ float sm_m[AT_WARPS][AT_TQ], sm_l[AT_WARPS][AT_TQ];
-    __shared__ float sm_o[AT_WARPS][AT_TQ][D];
+__global__ void __launch_bounds__(32 * (AT_CW + 1)) attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmk,
+                                                                   const __grid_constant__ CUtensorMap tmv) {
+    using LY = AtLayout<D>;
+    constexpr int KS = D / 16;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);  // the swizzle wants 1024 B
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + LY::BARS);
+    uint64_t *empty = full + AT_NST;
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + LY::BARS + 16 * AT_NST);
+    const int sc = blockIdx.x, qg = blockIdx.y, kh = blockIdx.z;
+    const int warp = static_cast<int>(threadIdx.x) >> 5, lane = static_cast<int>(threadIdx.x) & 31;
+    const int g = lane >> 2, c = lane & 3;
+    const int rows = a.M * a.g;
+    const int64_t k0 = static_cast<int64_t>(sc) * a.chunk_pairs * 2;  // the chunk's keys [k0, k1)
+    const int64_t k1 = min(a.NK, k0 + a.chunk_pairs * 2);
+    const int nst = k1 > k0 ? static_cast<int>((k1 - k0 + AT_KT - 1) / AT_KT) : 0;
+
+    // every row of a tile holds finite values (cache rows below NK, zeros past it): masked keys weigh
+    // their V rows by exactly 0
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < AT_NST; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], AT_CW);
+        }
+        *abort = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
     pdl_wait();
     pdl_launch_dependents();
-    const int sc = blockIdx.x, qg = blockIdx.y, kh = blockIdx.z;
-    const int warp = static_cast<int>(threadIdx.x) / 32, lane = static_cast<int>(threadIdx.x) & 31;
-    const int half = lane >> 4, hl = lane & 15;
-    const int rows = a.M * a.g;
 
-    float qr[AT_TQ][DL];
-    uint32_t vis[AT_TQ];
+    float m0 = AT_NEG, m1 = AT_NEG, l0 = 0.0f, l1 = 0.0f;  // rows 2c, 2c+1 of this warp
+    float o[KS][4];                                         // O^T: d = 16 dt + g (+8), rows 2c, 2c+1
 #pragma unroll
-    for (int t = 0; t < AT_TQ; ++t) {
-        const int tg = qg * AT_TQ + t;
-        vis[t] = 0;
+    for (int dt = 0; dt < KS; ++dt)
 #pragma unroll
-        for (int e = 0; e < DL; ++e) qr[t][e] = 0.0f;
-        if (tg < rows) {
-            const int i = tg / a.g, h = kh * a.g + tg % a.g;
-            const float *qp = a.q + (static_cast<int64_t>(i) * a.H + h) * D + hl * DL;
-#pragma unroll
-            for (int e = 0; e < DL; ++e) qr[t][e] = qp[e] * a.qscale;
-            vis[t] = path_mask(a, i);
-        }
-    }
+        for (int e = 0; e < 4; ++e) o[dt][e] = 0.0f;
 
-    float m[AT_TQ], l[AT_TQ], o[AT_TQ][DV];
+    if (warp == AT_CW) {  // producer: one thread issues the stage's tensor copies
+        if (lane == 0) {
+            int issued = 0;
+            for (int i = 0; i < nst; ++i) {
+                const int slot = i % AT_NST;
+                if (i >= AT_NST && !mbar_wait_bounded(&empty[slot], ((i / AT_NST) - 1) & 1u, 2000000000ull, abort)) {
+                    set_status(a.status, SD_ETIMEOUT);
+                    *abort = 1;
+                    break;
+                }
+                const int y = static_cast<int>(k0) + i * AT_KT;
+                mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(LY::STAGE));  // zero-filled rows count too
+                uint8_t *st = smem + slot * LY::STAGE;
 #pragma unroll
-    for (int t = 0; t < AT_TQ; ++t) {
-        m[t] = AT_NEG;
-        l[t] = 0.0f;
-#pragma unroll
-        for (int e = 0; e < DV; ++e) o[t][e] = 0.0f;
-    }
-
-    const int64_t NP = (a.NK + 1) / 2;
-    const int64_t p_end = min(NP, (static_cast<int64_t>(sc) + 1) * a.chunk_pairs);
-    const __half *kbase = a.kc + static_cast<int64_t>(kh) * a.S_max * D;
-    const __half *vbase = a.vc + static_cast<int64_t>(kh) * a.S_max * D;
-    int64_t p = static_cast<int64_t>(sc) * a.chunk_pairs + warp;
-
-    // registers of the pair in hand and of the next one
-    float kf[DL], vA[DV], vB[DV];
-    auto fetch = [&](int64_t pp, float (&k_)[DL], float (&va)[DV], float (&vb)[DV]) {
-        const int64_t jA = 2 * pp, jB = jA + 1, jm = jA + half;
-        if (jm < a.NK) {
-            load_k<DL>(kbase + jm * D, hl, k_);
-        } else {
-#pragma unroll
-            for (int e = 0; e < DL; ++e) k_[e] = 0.0f;
+                for (int b = 0; b < LY::NB; ++b) {
+                    tma_3d(st + b * LY::TILE, &tmk, 64 * b, y, kh, &full[slot]);
+                    tma_3d(st + (LY::NB + b) * LY::TILE, &tmv, 64 * b, y, kh, &full[slot]);
+                }
+                ++issued;
+            }
+            // never leave with copies in flight
+            for (int i = issued > AT_NST ? issued - AT_NST : 0; i < issued; ++i)
+                mbar_wait_bounded(&full[i % AT_NST], (i / AT_NST) & 1u, 2000000000ull);
         }
-        load_v<DV>(vbase + jA * D, lane, va);
-        if (jB < a.NK) {
-            load_v<DV>(vbase + jB * D, lane, vb);
-        } else {
+        __syncwarp();
+    } else {
+        // B fragments of query row g (high and low fp16 parts), scaled by 2^(11-e) for max |q| in [2^(e-1), 2^e)
+        uint32_t qh[KS][2], ql[KS][2];
+        float rsc = 0.0f;  // the scale back, 2^(e-11), of row g
+        {
+            const int tg = qg * AT_TQ + g;
+            const bool real = tg < rows;
+            const int i = real ? tg / a.g : 0, h = real ? kh * a.g + tg % a.g : 0;
+            const float *qp = a.q + (static_cast<int64_t>(i) * a.H + h) * D;
+            float qv[KS][4];
+            float mx = 0.0f;
 #pragma unroll
-            for (int e = 0; e < DV; ++e) vb[e] = 0.0f;
-        }
-    };
-    if (p < p_end) fetch(p, kf, vA, vB);
-    while (p < p_end) {
-        const int64_t pn = p + AT_WARPS;
-        float kn[DL], vAn[DV], vBn[DV];
-        if (pn < p_end) fetch(pn, kn, vAn, vBn);
-        const int64_t jA = 2 * p, jB = jA + 1;
+            for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
-        for (int t = 0; t < AT_TQ; ++t) {
-            float s = 0.0f;
+                for (int e = 0; e < 4; ++e) {
+                    const int d = 16 * ks + 2 * c + (e & 1) + 8 * (e >> 1);
+                    qv[ks][e] = real ? __fmul_rn(qp[d], a.qscale) : 0.0f;
+                    mx = fmaxf(mx, fabsf(qv[ks][e]));
+                }
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            int ex = 0;
+            if (mx > 0.0f) (void)frexpf(mx, &ex);
+            const float up = ldexpf(1.0f, 11 - ex);
+            rsc = mx > 0.0f ? ldexpf(1.0f, ex - 11) : 0.0f;
 #pragma unroll
-            for (int e = 0; e < DL; ++e) s = fmaf(qr[t][e], kf[e], s);
-#pragma unroll
-            for (int off = 8; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-            const float so = __shfl_xor_sync(0xffffffffu, s, 16);
-            float sA = half ? so : s, sB = half ? s : so;
-            if (jA >= a.L && !((vis[t] >> static_cast<int>(jA - a.L)) & 1u)) sA = -INFINITY;
-            if (jB >= a.NK || (jB >= a.L && !((vis[t] >> static_cast<int>(jB - a.L)) & 1u))) sB = -INFINITY;
-            const float mn = fmaxf(m[t], fmaxf(sA, sB));
-            const float alpha = exp2f(m[t] - mn);
-            const float pA = exp2f(sA - mn), pB = exp2f(sB - mn);
-            l[t] = fmaf(l[t], alpha, pA + pB);
-            m[t] = mn;
-#pragma unroll
-            for (int e = 0; e < DV; ++e) o[t][e] = fmaf(pB, vB[e], fmaf(pA, vA[e], o[t][e] * alpha));
-        }
-        if (pn < p_end) {
-#pragma unroll
-            for (int e = 0; e < DL; ++e) kf[e] = kn[e];
-#pragma unroll
-            for (int e = 0; e < DV; ++e) {
-                vA[e] = vAn[e];
-                vB[e] = vBn[e];
+            for (int ks = 0; ks < KS; ++ks) {
+                split_h2(qv[ks][0] * up, qv[ks][1] * up, qh[ks][0], ql[ks][0]);
+                split_h2(qv[ks][2] * up, qv[ks][3] * up, qh[ks][1], ql[ks][1]);
             }
         }
-        p = pn;
-    }
-
-    // the CTA's warps into one (max, sum, o) per row
+        // rows 2c and 2c+1 of the score fragments: scale back, visibility, validity
+        const float rs0 = __shfl_sync(0xffffffffu, rsc, 8 * c), rs1 = __shfl_sync(0xffffffffu, rsc, 8 * c + 4);
+        uint32_t vis0 = 0, vis1 = 0;
+        const int t0r = qg * AT_TQ + 2 * c;
+        const bool ok0 = t0r < rows, ok1 = t0r + 1 < rows;
+        if (ok0) vis0 = path_mask(a, t0r / a.g);
+        if (ok1) vis1 = path_mask(a, (t0r + 1) / a.g);
+        const uint32_t sbase = smem_u32(smem);
+        // ldmatrix row addresses of this lane: the K tiles (keys x d) and, transposed, the V tiles
+        const int kr = 16 * warp + (lane & 7) + ((lane >> 3) & 1) * 8, kd = (lane >> 4) * 8;
+        const int vr = 16 * warp + (lane & 7) + (lane >> 4) * 8, vd = ((lane >> 3) & 1) * 8;
+        constexpr uint32_t VOFF = LY::NB * LY::TILE;  // the V tiles after the K tiles
+        for (int i = 0; i < nst; ++i) {
+            const int slot = i % AT_NST;
+            const bool ready = mbar_wait_bounded(&full[slot], (i / AT_NST) & 1u, 2000000000ull, abort);
+            if (!__all_sync(0xffffffffu, ready)) {
+                if (lane == 0) {
+                    set_status(a.status, SD_ETIMEOUT);
+                    *abort = 1;
+                }
+                break;
+            }
+            const uint32_t st = sbase + slot * LY::STAGE;
+            // four independent accumulator chains (high / low part x even / odd k step), then summed
+            float sa[4][4] = {};
 #pragma unroll
-    for (int t = 0; t < AT_TQ; ++t) {
-        if (lane == 0) {
-            sm_m[warp][t] = m[t];
-            sm_l[warp][t] = l[t];
+            for (int ks = 0; ks < KS; ++ks) {
+                uint32_t ka[4];
+                ldsm_x4(st + at_off<D>(kr, 16 * ks + kd), ka);
+                hmma(sa[ks & 1], ka, qh[ks][0], qh[ks][1]);
+                hmma(sa[2 + (ks & 1)], ka, ql[ks][0], ql[ks][1]);
+            }
+            float s[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s[e] = (sa[0][e] + sa[1][e]) + (sa[2][e] + sa[3][e]);
+            // s0, s1: key 16w + g, rows 2c, 2c+1; s2, s3: key 16w + g + 8
+            const int64_t ja = k0 + static_cast<int64_t>(i) * AT_KT + 16 * warp + g, jb = ja + 8;
+            const bool va0 = ok0 && ja < k1 && (ja < a.L || ((vis0 >> static_cast<int>(ja - a.L)) & 1u));
+            const bool va1 = ok1 && ja < k1 && (ja < a.L || ((vis1 >> static_cast<int>(ja - a.L)) & 1u));
+            const bool vb0 = ok0 && jb < k1 && (jb < a.L || ((vis0 >> static_cast<int>(jb - a.L)) & 1u));
+            const bool vb1 = ok1 && jb < k1 && (jb < a.L || ((vis1 >> static_cast<int>(jb - a.L)) & 1u));
+            s[0] = va0 ? s[0] * rs0 : -INFINITY;
+            s[1] = va1 ? s[1] * rs1 : -INFINITY;
+            s[2] = vb0 ? s[2] * rs0 : -INFINITY;
+            s[3] = vb1 ? s[3] * rs1 : -INFINITY;
+            float x0 = fmaxf(s[0], s[2]), x1 = fmaxf(s[1], s[3]);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
+                x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
+            }
+            const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+            const float al0 = exp2f(m0 - n0), al1 = exp2f(m1 - n1);
+            const float p0 = exp2f(s[0] - n0), p1 = exp2f(s[1] - n1), p2 = exp2f(s[2] - n0), p3 = exp2f(s[3] - n1);
+            float r0 = p0 + p2, r1 = p1 + p3;
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                r0 += __shfl_xor_sync(0xffffffffu, r0, off);
+                r1 += __shfl_xor_sync(0xffffffffu, r1, off);
+            }
+            l0 = fmaf(l0, al0, r0);
+            l1 = fmaf(l1, al1, r1);
+            m0 = n0;
+            m1 = n1;
+#pragma unroll
+            for (int dt = 0; dt < KS; ++dt) {
+                o[dt][0] *= al0;
+                o[dt][1] *= al1;
+                o[dt][2] *= al0;
+                o[dt][3] *= al1;
+            }
+            // P^T (keys x rows) as the B operand, high and low fp16 parts
+            uint32_t ph01, pl01, ph23, pl23;
+            split_h2(p0 * AT_PS, p1 * AT_PS, ph01, pl01);
+            split_h2(p2 * AT_PS, p3 * AT_PS, ph23, pl23);
+            const uint32_t bh0 = movm_t(ph01), bh1 = movm_t(ph23), bl0 = movm_t(pl01), bl1 = movm_t(pl23);
+#pragma unroll
+            for (int dt = 0; dt < KS; ++dt) {
+                uint32_t va[4];
+                ldsm_x4_t(st + VOFF + at_off<D>(vr, 16 * dt + vd), va);
+                hmma(o[dt], va, bh0, bh1);
+                hmma(o[dt], va, bl0, bl1);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+        }
+    }
+    __syncthreads();  // every consumer past its loop and every copy landed: the ring is free
+    float *sm_m = reinterpret_cast<float *>(smem), *sm_l = sm_m + AT_CW * AT_TQ, *sm_o = sm_l + AT_CW * AT_TQ;
+    if (warp < AT_CW) {
+        if (g == 0) {
+            sm_m[warp * AT_TQ + 2 * c] = m0;
+            sm_m[warp * AT_TQ + 2 * c + 1] = m1;
+            sm_l[warp * AT_TQ + 2 * c] = l0;
+            sm_l[warp * AT_TQ + 2 * c + 1] = l1;
         }
 #pragma unroll
-        for (int e = 0; e < DV; ++e) sm_o[warp][t][lane * DV + e] = o[t][e];
+        for (int dt = 0; dt < KS; ++dt) {
+            float *ow = sm_o + static_cast<size_t>(warp) * AT_TQ * D;
+            ow[(2 * c) * D + 16 * dt + g] = o[dt][0];
+            ow[(2 * c + 1) * D + 16 * dt + g] = o[dt][1];
+            ow[(2 * c) * D + 16 * dt + g + 8] = o[dt][2];
+            ow[(2 * c + 1) * D + 16 * dt + g + 8] = o[dt][3];
+        }
     }
     __syncthreads();
     const int64_t base = ((static_cast<int64_t>(kh) * a.QG + qg) * a.S + sc) * AT_TQ;
-    for (int idx = threadIdx.x; idx < AT_TQ * D; idx += 32 * AT_WARPS) {
+    for (int idx = threadIdx.x; idx < AT_TQ * D; idx += blockDim.x) {
         const int t = idx / D, d = idx % D;
-        float mx = sm_m[0][t];
+        float mx = sm_m[t];
 #pragma unroll
-        for (int w = 1; w < AT_WARPS; ++w) mx = fmaxf(mx, sm_m[w][t]);
+        for (int w = 1; w < AT_CW; ++w) mx = fmaxf(mx, sm_m[w * AT_TQ + t]);
         float ov = 0.0f, lv = 0.0f;
 #pragma unroll
-        for (int w = 0; w < AT_WARPS; ++w) {
-            const float f = exp2f(sm_m[w][t] - mx);
-            ov = fmaf(sm_o[w][t][d], f, ov);
-            lv = fmaf(sm_l[w][t], f, lv);
+        for (int w = 0; w < AT_CW; ++w) {
+            const float f = exp2f(sm_m[w * AT_TQ + t] - mx);
+            ov = fmaf(sm_o[(static_cast<size_t>(w) * AT_TQ + t) * D + d], f, ov);
+            lv = fmaf(sm_l[w * AT_TQ + t], f, lv);
         }
-        a.part_o[(base + t) * D + d] = ov;
+        a.part_o[(base + t) * D + d] = ov * (1.0f / AT_PS);
         if (d == 0) {
             a.part_ml[(base + t) * 2] = mx;
             a.part_ml[(base + t) * 2 + 1] = lv;
@@ -239,7 +362,7 @@ __global__ void __launch_bounds__(32 * AT_WARPS) attn_partial_kernel(const AttnA
 // combine the chunks of one (KV head, query group): one warp per query row, lanes over d
 template <int D>
 __global__ void __launch_bounds__(32 * AT_TQ) attn_combine_kernel(const AttnArgs a) {
-    constexpr int DV = KvLane<D>::DV;
+    constexpr int DV = D / 32;  // elements per lane
     pdl_wait();
     pdl_launch_dependents();
     const int qg = blockIdx.x, kh = blockIdx.y;
@@ -332,10 +455,12 @@ static bool attn_plan(int32_t M, int32_t H, int32_t H_kv, int32_t D, int64_t L, 
     const int64_t rows = static_cast<int64_t>(M) * (H / H_kv);
     p.QG = static_cast<int32_t>((rows + AT_TQ - 1) / AT_TQ);
     const int64_t NP = (L + M + 1) / 2;
-    // about 4 CTAs (16 warps) per SM over all (chunk, query group, KV head)
+    // three CTAs per SM over all (chunk, query group, KV head), in one wave; chunks of whole stages
     const int64_t per = static_cast<int64_t>(p.QG) * H_kv;
-    const int64_t want = (4 * static_cast<int64_t>(sms) + per - 1) / per;
+    int64_t want = 3 * static_cast<int64_t>(sms) / per;
+    if (want < 1) want = 1;
     int64_t cp = (NP + want - 1) / want;
+    cp = (cp + AT_KT / 2 - 1) / (AT_KT / 2) * (AT_KT / 2);
     if (cp < AT_MIN_CHUNK_PAIRS) cp = AT_MIN_CHUNK_PAIRS;
     p.chunk_pairs = cp;
     p.S = static_cast<int32_t>((NP + cp - 1) / cp);  // <= want, whatever the context
@@ -344,6 +469,36 @@ static bool attn_plan(int32_t M, int32_t H, int32_t H_kv, int32_t D, int64_t L, 
     p.off_o = (nrow * 2 * sizeof(float) + 255) & ~static_cast<size_t>(255);
     p.total = p.off_o + ((nrow * D * sizeof(float) + 255) & ~static_cast<size_t>(255));
     return true;
+}
+
+// The driver's tensor-map encoder, looked up once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// A cache [H_kv][S_max][D] fp16 seen as [H_kv][NK][D]: tiles of AT_KT keys x 64 halves, 128-byte
+// swizzle, zeros past key NK.
+bool cache_map(CUtensorMap *tm, const void *base, int D, int64_t NK, int64_t S_max, int H_kv) {
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(NK),
+                                static_cast<cuuint64_t>(H_kv)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(S_max) * D * 2};
+    const cuuint32_t box[3] = {64, AT_KT, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace sdv
@@ -381,9 +536,13 @@ sd_status sd_attn_decode(const float *q, const void *k_cache, const void *v_cach
     if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
         !aligned(workspace, 256))
         return SD_EINVAL;
+    if (L + M > INT32_MAX - AT_KT) return SD_EUNSUPPORTED;  // tensor-copy coordinates are 32-bit
     AttnPlan p;
     if (!attn_plan(M, H, H_kv, D, L, p)) return SD_EINVAL;
     if (ws_bytes < p.total) return SD_EINVAL;
+    CUtensorMap tmk, tmv;
+    if (!cache_map(&tmk, k_cache, D, L + M, S_max, H_kv) || !cache_map(&tmv, v_cache, D, L + M, S_max, H_kv))
+        return SD_ECUDA;
     int *st = status_ptr();
     if (!st) return SD_ECUDA;
     AttnArgs a = {};
@@ -411,10 +570,16 @@ sd_status sd_attn_decode(const float *q, const void *k_cache, const void *v_cach
     const dim3 grid(p.S, p.QG, H_kv);
     cudaError_t e;
     if (D == 128) {
-        e = launch(attn_partial_kernel<128>, grid, dim3(32 * AT_WARPS), 0, s, a);
+        e = cudaFuncSetAttribute(attn_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 AtLayout<128>::TOTAL);
+        if (e == cudaSuccess)
+            e = launch(attn_tc_kernel<128>, grid, dim3(32 * (AT_CW + 1)), AtLayout<128>::TOTAL, s, a, tmk, tmv);
         if (e == cudaSuccess) e = launch(attn_combine_kernel<128>, dim3(p.QG, H_kv), dim3(32 * AT_TQ), 0, s, a);
     } else {
-        e = launch(attn_partial_kernel<64>, grid, dim3(32 * AT_WARPS), 0, s, a);
+        e = cudaFuncSetAttribute(attn_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 AtLayout<64>::TOTAL);
+        if (e == cudaSuccess)
+            e = launch(attn_tc_kernel<64>, grid, dim3(32 * (AT_CW + 1)), AtLayout<64>::TOTAL, s, a, tmk, tmv);
         if (e == cudaSuccess) e = launch(attn_combine_kernel<64>, dim3(p.QG, H_kv), dim3(32 * AT_TQ), 0, s, a);
     }
     return e == cudaSuccess ? SD_OK : SD_ECUDA;
