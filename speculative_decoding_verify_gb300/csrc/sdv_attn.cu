@@ -359,10 +359,29 @@ __global__ void __launch_bounds__(32 * (AT_CW + 1)) attn_tc_kernel(const AttnArg
     }
 }
 
-// combine the chunks of one (KV head, query group): one warp per query row, lanes over d
+// combine the chunks of one (KV head, query group): one warp per query row, lanes over d.  Each lane
+// holds the weight of one chunk (32 chunks at a time) and the warp walks them with the loads of
+// several chunks in flight.
+template <int DV>
+struct VecF;
+template <>
+struct VecF<2> {
+    using T = float2;
+    static __device__ __forceinline__ float at(const T &v, int e) { return e == 0 ? v.x : v.y; }
+};
+template <>
+struct VecF<4> {
+    using T = float4;
+    static __device__ __forceinline__ float at(const T &v, int e) {
+        return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+    }
+};
+
 template <int D>
-__global__ void __launch_bounds__(32 * AT_TQ) attn_combine_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(32 * AT_TQ, 1) attn_combine_kernel(const AttnArgs a) {
     constexpr int DV = D / 32;  // elements per lane
+    using V = typename VecF<DV>::T;
+    static_assert(D % 64 == 0, "two or four floats per lane");
     pdl_wait();
     pdl_launch_dependents();
     const int qg = blockIdx.x, kh = blockIdx.y;
@@ -378,13 +397,24 @@ __global__ void __launch_bounds__(32 * AT_TQ) attn_combine_kernel(const AttnArgs
     float lv = 0.0f, ov[DV];
 #pragma unroll
     for (int e = 0; e < DV; ++e) ov[e] = 0.0f;
-    for (int s = 0; s < a.S; ++s) {
-        const int64_t r = (base + s) * AT_TQ + t;
-        const float f = exp2f(a.part_ml[r * 2] - mx);
-        lv = fmaf(a.part_ml[r * 2 + 1], f, lv);
+    for (int s0 = 0; s0 < a.S; s0 += 32) {
+        float f = 0.0f;
+        if (s0 + lane < a.S) {
+            const int64_t r = (base + s0 + lane) * AT_TQ + t;
+            f = exp2f(a.part_ml[r * 2] - mx);
+            lv = fmaf(a.part_ml[r * 2 + 1], f, lv);
+        }
+        const int n = min(32, a.S - s0);
+#pragma unroll 8
+        for (int j = 0; j < n; ++j) {
+            const float fj = __shfl_sync(0xffffffffu, f, j);
+            const V v = *reinterpret_cast<const V *>(a.part_o + ((base + s0 + j) * AT_TQ + t) * D + lane * DV);
 #pragma unroll
-        for (int e = 0; e < DV; ++e) ov[e] = fmaf(a.part_o[r * D + lane * DV + e], f, ov[e]);
+            for (int e = 0; e < DV; ++e) ov[e] = fmaf(VecF<DV>::at(v, e), fj, ov[e]);
+        }
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lv += __shfl_xor_sync(0xffffffffu, lv, off);
     float *op = a.out + (static_cast<int64_t>(i) * a.H + h) * D + lane * DV;
 #pragma unroll
     for (int e = 0; e < DV; ++e) op[e] = ov[e] / lv;
