@@ -79,7 +79,8 @@ typedef enum { SD_Q8_0 = 0, SD_Q4_32 = 1, SD_Q4_K = 2, SD_Q6_K = 3 } sd_qtype;
 #define SD_EPI_SILU_MUL_REQUANT 2u  /* gate|up pair: h = silu(g) * u, requantised into q_next/scales_next */
 
 const char *sd_status_string(sd_status s);
-int sd_abi_version(void); /* 3: sd_pass_desc carries the down projections' format, sd_pass the K-quant flag */
+int sd_abi_version(void); /* 4: sd_device_status_site and sd_build_flags; 3: sd_pass_desc carries the down
+                           projections' format, sd_pass the K-quant flag */
 
 /*
  * Load-time repack ("Inside OpenJet Engine", section "One GPU launch for a
@@ -533,6 +534,22 @@ sd_status sd_verify_pass_traced(const sd_pass *pass, uint64_t *trace, size_t tra
 /* Synchronises `stream`, returns and clears the current device's status word
  * (SD_OK, SD_ETIMEOUT or SD_EDEVICE); SD_ECUDA if synchronising failed. */
 sd_status sd_device_status(sd_stream_t stream);
+
+/* The same, also returning where the condition was recorded: *site (HOST
+ * pointer) = 1 the launch-wide time bound ran out in a producer, 2 in a
+ * consumer; >= 100 a bounds check of the debug build failed (the site numbers
+ * are listed with the checks in the kernels' sources); 0 otherwise.  SD_EINVAL
+ * if site is NULL. */
+sd_status sd_device_status_site(sd_stream_t stream, int32_t *site);
+
+/* Build variant: SD_BUILD_DEBUG_BOUNDS set when the library was compiled with
+ * SD_DEBUG_BOUNDS: every index the matmul kernels (per call and inside the
+ * one-launch pass) compute for a global access or a weight, activation or
+ * partial-sum copy is checked against the extent the call's shapes imply; a
+ * failed check records SD_EDEVICE with its site and skips the access.  The
+ * release build compiles the checks away. */
+#define SD_BUILD_DEBUG_BOUNDS 1
+int32_t sd_build_flags(void);
 
 /* Programmatic dependent launch on (1, default) or off (0) for later launches. */
 void sd_set_pdl(int enable);

@@ -14,7 +14,9 @@ import os
 import torch
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libsdverify.so")
+# SDV_DEBUG_BOUNDS=1 selects the bounds-checked build of the same sources (build.build(debug_bounds=True))
+DEBUG_BOUNDS = os.environ.get("SDV_DEBUG_BOUNDS", "") == "1"
+LIB_PATH = os.path.join(HERE, "libsdverify_dbg.so" if DEBUG_BOUNDS else "libsdverify.so")
 
 Q8_0 = 0
 Q4_32 = 1
@@ -95,6 +97,8 @@ def lib():
             "sd_tree_path": ([P, P, P, I32, P], I32),
             "sd_depth_init": ([ctypes.POINTER(SdDepthState), I32, I32], I),
             "sd_depth_update": ([ctypes.POINTER(SdDepthState), I32], I),
+            "sd_device_status_site": ([P, ctypes.POINTER(I32)], I),
+            "sd_build_flags": ([], I32),
             "sd_attn_workspace_bytes": ([I32, I32, I32, I32, I64], SZ),
             "sd_kv_append": ([P, P, I32, I32, I32, P, P, I64, I64, P], I),
             "sd_attn_decode": ([P, P, P, I32, I32, I32, I32, I64, I64, P, P, P, SZ, P], I),
@@ -334,6 +338,18 @@ def accept_sample_topk(logits: torch.Tensor, K: int, drafts: torch.Tensor | None
 
 def device_status() -> int:
     return int(lib().sd_device_status(_stream()))
+
+
+def device_status_site() -> tuple[int, int]:
+    """(status, site): the status word and where it was recorded (0 none, 1/2 a time bound,
+    >= 100 a bounds check of the debug build); both cleared."""
+    site = ctypes.c_int32(0)
+    st = int(lib().sd_device_status_site(_stream(), ctypes.byref(site)))
+    return st, int(site.value)
+
+
+def build_flags() -> int:
+    return int(lib().sd_build_flags())
 
 
 def set_pdl(enable: bool):

@@ -19,6 +19,9 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libsdverify.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
+# the bounds-checked variant (SD_DEBUG_BOUNDS), loaded by the package when SDV_DEBUG_BOUNDS=1
+LIB_DBG = os.path.join(HERE, "libsdverify_dbg.so")
+BUILD_DIR_DBG = os.path.join(ROOT, "_build_dbg")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -40,11 +43,17 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_log: str | None = None) -> str:
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_log: str | None = None,
+          debug_bounds: bool | None = None) -> str:
+    """Build the library (default: the variant the package loads, the bounds-checked one when
+    SDV_DEBUG_BOUNDS=1) and return its path."""
+    if debug_bounds is None:
+        debug_bounds = os.environ.get("SDV_DEBUG_BOUNDS", "") == "1"
+    build_dir, lib = (BUILD_DIR_DBG, LIB_DBG) if debug_bounds else (BUILD_DIR, LIB)
+    os.makedirs(build_dir, exist_ok=True)
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cuh")]
     headers.append(os.path.join(ROOT, "include", "sdverify.h"))
-    stamp = os.path.join(BUILD_DIR, "flags.txt")
+    stamp = os.path.join(build_dir, "flags.txt")
     want = os.environ.get("SDV_NVCC_FLAGS", "")
     if not os.path.exists(stamp) or open(stamp).read() != want:
         force = True
@@ -57,10 +66,12 @@ def build(force: bool = False, verbose: bool = False, ptxas_log: str | None = No
         flags += ["-Xptxas", "-v"]
     extra = os.environ.get("SDV_NVCC_FLAGS", "").split()
     flags += extra
+    if debug_bounds:
+        flags += ["-DSD_DEBUG_BOUNDS"]
     objs = []
     jobs = []
     for s in srcs:
-        o = os.path.join(BUILD_DIR, os.path.basename(s)[:-3] + ".o")
+        o = os.path.join(build_dir, os.path.basename(s)[:-3] + ".o")
         objs.append(o)
         if force or _stale(o, [s] + headers):
             jobs.append((s, o))
@@ -84,14 +95,14 @@ def build(force: bool = False, verbose: bool = False, ptxas_log: str | None = No
     if ptxas_log and logs:
         with open(ptxas_log, "w") as f:
             f.write("\n".join(logs))
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or jobs or _stale(lib, objs):
+        tmp = lib + f".tmp{os.getpid()}"
         cmd = [nvcc(), "-shared", "-o", tmp] + objs + ARCH + ["-lcudart"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
@@ -100,5 +111,6 @@ if __name__ == "__main__":
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--ptxas-log", default=None)
+    ap.add_argument("--debug-bounds", action="store_true", help="the bounds-checked variant")
     a = ap.parse_args()
-    print(build(force=a.force, verbose=True, ptxas_log=a.ptxas_log))
+    print(build(force=a.force, verbose=True, ptxas_log=a.ptxas_log, debug_bounds=a.debug_bounds or None))

@@ -1,6 +1,8 @@
 // sdv_abi.cu - status word, device queries, load-time repack, RMSNorm +
 // requantisation, and the test hooks of the verify-pass library.
 #include <mutex>
+#include <set>
+#include <utility>
 
 #include "sdv_common.cuh"
 
@@ -47,6 +49,25 @@ int num_sms() {
 }
 
 bool pdl_enabled() { return g_pdl != 0; }
+
+cudaError_t allow_max_dynamic_smem(const void *kernel) {
+    const int d = cur_dev();
+    if (d < 0) return cudaErrorInvalidDevice;
+    static std::mutex mu;
+    static std::set<std::pair<const void *, int>> done;
+    std::lock_guard<std::mutex> lk(mu);
+    if (done.count({kernel, d})) return cudaSuccess;
+    int optin = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d);
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa{};
+    e = cudaFuncGetAttributes(&fa, kernel);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             optin - static_cast<int>(fa.sharedSizeBytes));
+    if (e == cudaSuccess) done.insert({kernel, d});
+    return e;
+}
 
 // ---------------------------------------------------------------------------
 // load-time repack: GGUF blocks -> 32-row tile records (values unchanged)
@@ -260,9 +281,34 @@ const char *sd_status_string(sd_status s) {
     return "unknown status";
 }
 
-int sd_abi_version(void) { return 3; }
+int sd_abi_version(void) { return 4; }
 
 void sd_set_pdl(int enable) { g_pdl = enable ? 1 : 0; }
+
+sd_status sd_device_status_site(sd_stream_t stream, int32_t *site) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!site) return SD_EINVAL;
+    *site = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SD_ECUDA;
+    int *p = status_ptr();
+    if (!p) return SD_ECUDA;
+    int v[2] = {0, 0};
+    if (cudaMemcpy(v, p, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return SD_ECUDA;
+    if (v[0] != 0 || v[1] != 0) {
+        int z[2] = {0, 0};
+        if (cudaMemcpy(p, z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return SD_ECUDA;
+    }
+    *site = v[1];
+    return static_cast<sd_status>(v[0]);
+}
+
+int32_t sd_build_flags(void) {
+#ifdef SD_DEBUG_BOUNDS
+    return SD_BUILD_DEBUG_BOUNDS;
+#else
+    return 0;
+#endif
+}
 
 sd_status sd_device_status(sd_stream_t stream) {
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -301,6 +347,7 @@ size_t sd_repacked_bytes(int qtype, int64_t n_out, int64_t k_in, uint32_t flags)
 
 sd_status sd_repack_weights(int qtype, const void *src_blocks, int64_t n_out, int64_t k_in, uint32_t flags, void *dst,
                             size_t dst_bytes, sd_stream_t stream) {
+    SD_NVTX("sd_repack_weights");
     size_t need = sd_repacked_bytes(qtype, n_out, k_in, flags);
     if (!need || !src_blocks || !dst || !aligned(dst, 16) || dst_bytes < need) return SD_EINVAL;
     if (qtype == SD_Q4_K || qtype == SD_Q6_K) {

@@ -66,6 +66,7 @@ extern "C" {
 
 sd_status sd_accept_greedy(const int32_t *argmax, const int32_t *tokens, const int32_t *parent, int32_t M,
                            int32_t *out_tokens, int32_t *out_count, sd_stream_t stream) {
+    SD_NVTX("sd_accept_greedy");
     if (!argmax || !out_tokens || !out_count || M < 1 || M > 16) return SD_EINVAL;
     if (M > 1 && !tokens) return SD_EINVAL;
     return launch(accept_greedy_kernel, dim3(1), dim3(32), 0, cs_(stream), argmax, tokens, parent, static_cast<int>(M),
@@ -78,6 +79,7 @@ sd_status sd_accept_sample(const float *logits, int64_t vocab, int32_t K, const 
                            const float *row_sumexp, const float *q_probs, const int32_t *drafts, float temperature,
                            uint64_t seed, int64_t base_pos, int32_t *out_tokens, int32_t *out_count,
                            sd_stream_t stream) {
+    SD_NVTX("sd_accept_sample");
     if (!logits || !out_tokens || !out_count || K < 0 || K > 15) return SD_EINVAL;
     if (K > 0 && !drafts) return SD_EINVAL;
     if (vocab < 1 || vocab > static_cast<int64_t>(MAX_TILES) * ATILE) return SD_EINVAL;

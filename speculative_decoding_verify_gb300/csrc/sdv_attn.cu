@@ -544,6 +544,7 @@ size_t sd_attn_workspace_bytes(int32_t M, int32_t H, int32_t H_kv, int32_t D, in
 
 sd_status sd_kv_append(const float *k_new, const float *v_new, int32_t M, int32_t H_kv, int32_t D, void *k_cache,
                        void *v_cache, int64_t S_max, int64_t L, sd_stream_t stream) {
+    SD_NVTX("sd_kv_append");
     if (!k_new || !v_new || !k_cache || !v_cache) return SD_EINVAL;
     if (M < 1 || M > 16 || H_kv < 1 || D < 1 || L < 0 || S_max < L + M) return SD_EINVAL;
     if (!aligned(k_new, 4) || !aligned(v_new, 4) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
@@ -560,6 +561,7 @@ sd_status sd_kv_append(const float *k_new, const float *v_new, int32_t M, int32_
 sd_status sd_attn_decode(const float *q, const void *k_cache, const void *v_cache, int32_t M, int32_t H,
                          int32_t H_kv, int32_t D, int64_t S_max, int64_t L, const int32_t *parent, float *out,
                          void *workspace, size_t ws_bytes, sd_stream_t stream) {
+    SD_NVTX("sd_attn_decode");
     if (!q || !k_cache || !v_cache || !out || !workspace) return SD_EINVAL;
     if (M < 1 || H_kv < 1 || H < H_kv || H % H_kv || L < 0 || S_max < L + M) return SD_EINVAL;
     if (M > 16 || (D != 64 && D != 128)) return SD_EUNSUPPORTED;
@@ -600,14 +602,12 @@ sd_status sd_attn_decode(const float *q, const void *k_cache, const void *v_cach
     const dim3 grid(p.S, p.QG, H_kv);
     cudaError_t e;
     if (D == 128) {
-        e = cudaFuncSetAttribute(attn_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 AtLayout<128>::TOTAL);
+        e = allow_max_dynamic_smem(attn_tc_kernel<128>);
         if (e == cudaSuccess)
             e = launch(attn_tc_kernel<128>, grid, dim3(32 * (AT_CW + 1)), AtLayout<128>::TOTAL, s, a, tmk, tmv);
         if (e == cudaSuccess) e = launch(attn_combine_kernel<128>, dim3(p.QG, H_kv), dim3(32 * AT_TQ), 0, s, a);
     } else {
-        e = cudaFuncSetAttribute(attn_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 AtLayout<64>::TOTAL);
+        e = allow_max_dynamic_smem(attn_tc_kernel<64>);
         if (e == cudaSuccess)
             e = launch(attn_tc_kernel<64>, grid, dim3(32 * (AT_CW + 1)), AtLayout<64>::TOTAL, s, a, tmk, tmv);
         if (e == cudaSuccess) e = launch(attn_combine_kernel<64>, dim3(p.QG, H_kv), dim3(32 * AT_TQ), 0, s, a);
@@ -617,6 +617,7 @@ sd_status sd_attn_decode(const float *q, const void *k_cache, const void *v_cach
 
 sd_status sd_kv_commit(void *k_cache, void *v_cache, int32_t H_kv, int32_t D, int64_t S_max, int64_t L, int32_t M,
                        const int32_t *path, const int32_t *count, sd_stream_t stream) {
+    SD_NVTX("sd_kv_commit");
     if (!k_cache || !v_cache || !count) return SD_EINVAL;
     if (H_kv < 1 || D < 1 || D > KC_MAXD || M < 1 || M > 16 || L < 0 || S_max < L + M) return SD_EINVAL;
     if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return SD_EINVAL;

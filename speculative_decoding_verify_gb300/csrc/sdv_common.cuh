@@ -3,11 +3,23 @@
 
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include "sdverify.h"
 
 namespace sdv {
+
+// An NVTX range around one library call (host side): a profiler's timeline shows each call, named as
+// in the C ABI, over the kernels it enqueues.  Without a profiler attached a push / pop costs a
+// test of a function pointer.
+struct NvtxScope {
+    explicit NvtxScope(const char *name) { nvtxRangePushA(name); }
+    ~NvtxScope() { nvtxRangePop(); }
+    NvtxScope(const NvtxScope &) = delete;
+    NvtxScope &operator=(const NvtxScope &) = delete;
+};
+#define SD_NVTX(name) ::sdv::NvtxScope sd_nvtx_scope_(name)
 
 // ---------------------------------------------------------------------------
 // host-side plumbing
@@ -20,6 +32,15 @@ int *status_ptr();
 int num_sms();
 // Whether launches carry the programmatic-stream-serialisation attribute.
 bool pdl_enabled();
+// Raise a kernel's dynamic shared-memory limit to everything the device lets one block have, once
+// per (kernel, device).  The limit is a property of the function, not of a launch: set per call to
+// that call's size, it would be lowered by a smaller call after a larger one had been captured into
+// a graph, and any later re-launch of the larger node with the function's current limit would fail.
+cudaError_t allow_max_dynamic_smem(const void *kernel);
+template <typename... KArgs>
+cudaError_t allow_max_dynamic_smem(void (*kernel)(KArgs...)) {
+    return allow_max_dynamic_smem(reinterpret_cast<const void *>(kernel));
+}
 
 inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -168,6 +189,19 @@ __device__ __forceinline__ bool bar_any(int id, int nthreads, bool v) {
 __device__ __forceinline__ void set_status(int *status, int code) {
     if (status) atomicCAS(status, 0, code);
 }
+
+// Bounds checks of the debug build (compiled with SD_DEBUG_BOUNDS): a failed check records
+// SD_EDEVICE with the site's number (>= 100) in the status word's second entry, and the caller skips
+// the access.  The release build compiles every check to `true`, so the condition is never evaluated.
+__device__ __forceinline__ bool bounds_check(bool ok, int *status, int site) {
+    if (!ok && status && atomicCAS(status, 0, SD_EDEVICE) == 0) status[1] = site;
+    return ok;
+}
+#ifdef SD_DEBUG_BOUNDS
+#define SD_INB(cond, status, site) (::sdv::bounds_check((cond), (status), (site)))
+#else
+#define SD_INB(cond, status, site) (true)
+#endif
 
 __device__ __forceinline__ int dp4a(int a, int b, int c) { return __dp4a(a, b, c); }
 

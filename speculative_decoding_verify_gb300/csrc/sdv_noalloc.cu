@@ -33,6 +33,7 @@ extern "C" sd_status sd_qmatmul_multipos_noalloc(int qtype, const void *w, int64
                                                  const int8_t *q, const float *scales, int32_t M, float *y,
                                                  const float *residual, uint32_t epilogue, int64_t requant_col0,
                                                  int8_t *q_next, float *scales_next, sd_stream_t stream) {
+    SD_NVTX("sd_qmatmul_multipos_noalloc");
     const size_t need = sd_qmatmul_workspace_bytes(qtype, n_out, k_in, epilogue);
     if (need == 0) return SD_EINVAL;
     if (need > SD_NOALLOC_SCRATCH_BYTES) return SD_EUNSUPPORTED;

@@ -110,6 +110,7 @@ extern "C" {
 
 sd_status sd_rmsnorm_quant_acts(const float *x, int64_t ldx, const float *norm_w, float eps, int32_t M, int64_t K,
                                 int8_t *q, float *scales, sd_stream_t stream) {
+    SD_NVTX("sd_rmsnorm_quant_acts");
     if (!x || !q || !scales || M < 1 || M > 65535 || K <= 0 || K % 32 || ldx < K) return SD_EINVAL;
     if (norm_w && K / 32 > NORM_MAX_KB) return SD_EUNSUPPORTED;
     if (!aligned(x, 4) || !aligned(q, 16)) return SD_EINVAL;

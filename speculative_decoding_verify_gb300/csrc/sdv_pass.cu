@@ -344,7 +344,10 @@ static sd_status verify_pass_launch(const sd_pass *p, uint64_t *trace, sd_stream
                : SD_ECUDA;
 }
 
-sd_status sd_verify_pass(const sd_pass *p, sd_stream_t stream) { return verify_pass_launch(p, nullptr, stream); }
+sd_status sd_verify_pass(const sd_pass *p, sd_stream_t stream) {
+    SD_NVTX("sd_verify_pass");
+    return verify_pass_launch(p, nullptr, stream);
+}
 
 size_t sd_pass_trace_bytes(const sd_pass *p) {
     if (!p || p->n_phases < 1 || p->grid < 1) return 0;
@@ -352,6 +355,7 @@ size_t sd_pass_trace_bytes(const sd_pass *p) {
 }
 
 sd_status sd_verify_pass_traced(const sd_pass *p, uint64_t *trace, size_t trace_bytes, sd_stream_t stream) {
+    SD_NVTX("sd_verify_pass_traced");
     if (!trace || !aligned(trace, 8) || trace_bytes < sd_pass_trace_bytes(p) || sd_pass_trace_bytes(p) == 0)
         return SD_EINVAL;
     return verify_pass_launch(p, trace, stream);

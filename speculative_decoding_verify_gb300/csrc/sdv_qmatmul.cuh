@@ -566,6 +566,10 @@ __device__ __forceinline__ float tree32(float x, int lane) {
 // ---------------------------------------------------------------------------
 template <int PAIR, bool KQ = false>
 __device__ __forceinline__ void epilogue(const QmmArgs &a, int u, int m, int lane, float v, float vu, float res, float nw) {
+    // site 106: a position of the call and a row tile of the output
+    if (!SD_INB(m >= 0 && m < a.M && u >= 0 && static_cast<int64_t>(u) * 32 < (PAIR ? a.n_out / 2 : a.n_out), a.status,
+                106))
+        return;
     if (PAIR) {
         const int64_t F = a.n_out / 2;
         const int64_t n = static_cast<int64_t>(u) * 32 + lane;  // F % 32 == 0 is required
@@ -657,7 +661,9 @@ __device__ inline void head_tile_stats_one(const QmmArgs &a, int st, int m, int 
         v[r] = e < V ? cexpf_canon(__fsub_rn(v[r], zmax)) : 0.0f;
     }
     const float s = tree1024_warp(v);
-    if (lane == 0) a.st_part[st * MPAD + m] = make_float4(zmax, s, __int_as_float(bi), bl);
+    // site 107: a statistics tile of the vocabulary and a position of the call
+    if (lane == 0 && SD_INB(st >= 0 && st < a.n_stiles && m >= 0 && m < a.M, a.status, 107))
+        a.st_part[st * MPAD + m] = make_float4(zmax, s, __int_as_float(bi), bl);
 }
 
 __device__ inline void head_tile_stats(const QmmArgs &a, int st, int lane, int f) {
@@ -905,6 +911,13 @@ __device__ inline void produce_phase(const QmmArgs &a, const Smem &sm, uint32_t 
             const uint8_t *src =
                 a.w + (static_cast<int64_t>(phys_unit(a, u)) * a.KB + static_cast<int64_t>(s) * a.KBs + jj) *
                           a.step_bytes;
+            // site 101: the copy stays inside its unit's k range and its ring stage
+            if (!SD_INB(phys_unit(a, u) >= 0 && phys_unit(a, u) < a.NU && s >= 0 && s < a.KS && jj >= 0 &&
+                            static_cast<int64_t>(s) * a.KBs + jj + n <= a.KB && bytes <= a.stage_stride,
+                        a.status, 101)) {
+                cs.abort = 1;
+                break;
+            }
             mbar_arrive_expect_tx(&sm.full[stg], bytes);
             bulk_g2s(sm.ring + static_cast<size_t>(stg) * a.stage_stride, src, bytes, &sm.full[stg], pol);
             ++it;
@@ -933,6 +946,9 @@ __device__ __forceinline__ void stage_issue(const QmmArgs &a, const Smem &sm, in
     const uint32_t fb = af_frag_bytes(a.M), mb = af_meta_bytes_q(a.M, a.qt);
     const uint32_t nf = static_cast<uint32_t>(len) * fb, nm = static_cast<uint32_t>(len) * mb;
     const uint32_t ns = a.af_norm ? static_cast<uint32_t>(a.M) * a.ss_ld * 4u : 0u;
+    // site 102: the split's blocks lie inside the input and fit the activation region (sized for KBs);
+    // a skipped copy leaves the consumers' wait to run out
+    if (!SD_INB(s >= 0 && s < a.KS && len >= 0 && len <= a.KBs && b0 + len <= a.KB, a.status, 102)) return;
     fence_proxy_async_global();
     fence_proxy_async_shared();
     mbar_arrive_expect_tx(sm.act_bar, nf + nm + ns);
@@ -1543,8 +1559,14 @@ __device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &
         }
         bool finish = direct;
         if (!direct) {
-            float *pp = a.part + ((static_cast<int64_t>(u) * a.KS + s) * a.P + (static_cast<int>(blockIdx.x) - pc.first)) *
-                                     (ROWS * MPAD);
+            // site 103: this CTA's partial-sum slot of (unit, split) exists
+            const int slot_c = static_cast<int>(blockIdx.x) - pc.first;
+            if (!SD_INB(u >= 0 && u < a.NU && s >= 0 && s < a.KS && slot_c >= 0 && slot_c < a.P && pc.np <= a.P, a.status,
+                        103)) {
+                cs.abort = 1;
+                return false;
+            }
+            float *pp = a.part + ((static_cast<int64_t>(u) * a.KS + s) * a.P + slot_c) * (ROWS * MPAD);
 #pragma unroll
             for (int i = 0; i < FIN_MPW; ++i) {
                 const int m = f + NF * i;
@@ -1559,6 +1581,9 @@ __device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &
             }
             // every finisher's partial sums before the release in the counter update
             finish = fin_sync(sm, cs, fin_it, f, lane, a.status, [&]() {
+                // site 104: one counter per unit, inside the workspace's counter region
+                if (!SD_INB(u < WS_UNIT_CNT && pc.expected >= 1 && pc.expected <= a.KS * a.P, a.status, 104))
+                    return false;
                 const unsigned old = atom_add_acq_rel(&a.cnt[u], 1u);
                 return static_cast<int>(old) == pc.expected - 1;
             });
@@ -1572,6 +1597,7 @@ __device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &
                     int f2;
                     npa[s2] = 0;
                     if (s2 < a.KS) unit_split_owners(a, s2, u, f2, npa[s2]);
+                    if (!SD_INB(npa[s2] >= 0 && npa[s2] <= a.P, a.status, 105)) npa[s2] = 0;
                 }
 #pragma unroll
                 for (int i = 0; i < FIN_MPW; ++i) {
@@ -1606,6 +1632,7 @@ __device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &
                     int f2, np;
                     if (a.KS == 1) np = pc.np;
                     else unit_split_owners(a, s2, u, f2, np);
+                    if (!SD_INB(np >= 0 && np <= a.P, a.status, 105)) np = 0;  // site 105: pieces per split
                     const float *qs = a.part + (static_cast<int64_t>(u) * a.KS + s2) * a.P * (ROWS * MPAD);
                     for (int c0 = 0; c0 < np; c0 += CH) {
                         // a chunk of pieces: every load in flight together, then added in piece order
@@ -1717,6 +1744,7 @@ __device__ inline void combine_phase(const QmmArgs &a, int widx) {
                 int f2;
                 np[s2] = 0;
                 if (s2 < a.KS) unit_split_owners(a, s2, u, f2, np[s2]);
+                if (!SD_INB(np[s2] >= 0 && np[s2] <= a.P, a.status, 108)) np[s2] = 0;  // site 108: pieces per split
             }
 #pragma unroll
             for (int s2 = 0; s2 < CKS; ++s2) {
@@ -1738,6 +1766,7 @@ __device__ inline void combine_phase(const QmmArgs &a, int widx) {
         for (int s2 = 0; s2 < a.KS; ++s2) {
             int f2, np;
             unit_split_owners(a, s2, u, f2, np);
+            if (!SD_INB(np >= 0 && np <= a.P, a.status, 108)) np = 0;
             const float *qs = a.part + (static_cast<int64_t>(u) * a.KS + s2) * a.P * (ROWS * MPAD) + m * ROWS + lane;
             for (int c0 = 0; c0 < np; c0 += CH) {
                 float x[CH];
@@ -1995,7 +2024,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1)
 inline cudaError_t pass_launch_kernel(void (*k)(const QmmArgs *, int, uint32_t *, uint64_t *), const QmmArgs *phases,
                                       int n_phases, uint32_t *ctr, uint64_t *trace, size_t smem, int grid,
                                       cudaStream_t s) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaError_t e = allow_max_dynamic_smem(k);
     if (e != cudaSuccess) return e;
     e = cudaMemsetAsync(ctr, 0, sizeof(uint32_t), s);
     if (e != cudaSuccess) return e;
@@ -2132,7 +2161,7 @@ inline void apply_layout(QmmArgs &a, const SmemLayout &L, size_t slot) {
 template <int QT, int PAIR, int NT>
 cudaError_t qmm_launch(QmmArgs a, size_t smem, cudaStream_t s) {
     auto k = qmm_kernel<QT, PAIR, NT>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaError_t e = allow_max_dynamic_smem(k);
     if (e != cudaSuccess) return e;
     return launch(k, dim3(a.G), dim3(QMM_THREADS), smem, s, a);
 }

@@ -123,6 +123,7 @@ sd_status sd_qmatmul_multipos(int qtype, const void *w, int64_t n_out, int64_t k
                               const float *scales, int32_t M, float *y, const float *residual, uint32_t epilogue,
                               int64_t requant_col0, int8_t *q_next, float *scales_next, void *workspace,
                               size_t ws_bytes, sd_stream_t stream) {
+    SD_NVTX("sd_qmatmul_multipos");
     if (!known_qtype(qtype)) return SD_EINVAL;
     if (M < 1) return SD_EINVAL;
     if (M > 16) return SD_EUNSUPPORTED;
@@ -178,6 +179,7 @@ sd_status sd_qmatmul_multipos(int qtype, const void *w, int64_t n_out, int64_t k
 sd_status sd_head_logits(const void *w, int64_t vocab, int64_t hidden, const int8_t *q, const float *scales, int32_t M,
                          float temperature, float *logits, int32_t *argmax, float *row_max, float *row_sumexp,
                          void *workspace, size_t ws_bytes, sd_stream_t stream) {
+    SD_NVTX("sd_head_logits");
     if (M < 1) return SD_EINVAL;
     if (M > 16) return SD_EUNSUPPORTED;
     if (!w || !q || !scales || !logits || !argmax || !row_max || !row_sumexp || !workspace) return SD_EINVAL;

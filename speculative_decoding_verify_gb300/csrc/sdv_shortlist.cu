@@ -388,6 +388,7 @@ extern "C" {
 
 sd_status sd_shortlist_build(const void *head_blocks, int64_t vocab, int64_t hidden, void *copy_blocks, float *bound,
                              float *wnorm, sd_stream_t stream) {
+    SD_NVTX("sd_shortlist_build");
     if (!head_blocks || !copy_blocks || !bound || !wnorm) return SD_EINVAL;
     if (!aligned(head_blocks, 16) || !aligned(copy_blocks, 16) || !aligned(bound, 4) || !aligned(wnorm, 4))
         return SD_EINVAL;
@@ -411,6 +412,7 @@ size_t sd_shortlist_workspace_bytes(int64_t vocab, int64_t hidden) {
 sd_status sd_head_shortlist(const void *copy_w, const float *bound, const float *wnorm, const void *head_blocks,
                             int64_t vocab, int64_t hidden, const int8_t *q, const float *scales, int32_t M,
                             int32_t *argmax, int32_t *n_cand, void *workspace, size_t ws_bytes, sd_stream_t stream) {
+    SD_NVTX("sd_head_shortlist");
     if (M < 1) return SD_EINVAL;
     if (M > SL_MAXM) return SD_EUNSUPPORTED;
     if (!copy_w || !bound || !wnorm || !head_blocks || !q || !scales || !argmax || !workspace) return SD_EINVAL;
@@ -461,10 +463,7 @@ sd_status sd_head_shortlist(const void *copy_w, const float *bound, const float 
     a.n_cand = n_cand;
     a.status = st;
     if (launch(shortlist_floor_kernel, dim3(L.G), dim3(SL_THREADS), 0, s, a) != cudaSuccess) return SD_ECUDA;
-    if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(shortlist_exact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-        return SD_ECUDA;
+    if (allow_max_dynamic_smem(shortlist_exact_kernel) != cudaSuccess) return SD_ECUDA;
     return launch(shortlist_exact_kernel, dim3(L.G), dim3(32 * nw), smem, s, a) == cudaSuccess ? SD_OK : SD_ECUDA;
 }
 

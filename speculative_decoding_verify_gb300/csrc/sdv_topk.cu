@@ -22,6 +22,7 @@ extern "C" {
 sd_status sd_accept_sample_topk(const float *logits, int64_t vocab, int32_t K, const float *q_probs,
                                 const int32_t *drafts, float temperature, int32_t top_k, float top_p, uint64_t seed,
                                 int64_t base_pos, int32_t *out_tokens, int32_t *out_count, sd_stream_t stream) {
+    SD_NVTX("sd_accept_sample_topk");
     if (!logits || !out_tokens || !out_count || K < 0 || K > 15) return SD_EINVAL;
     if (K > 0 && !drafts) return SD_EINVAL;
     if (vocab < 1 || vocab > (int64_t(1) << 31) - 1) return SD_EINVAL;

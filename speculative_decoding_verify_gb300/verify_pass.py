@@ -98,11 +98,19 @@ class VerifyStack:
                       seed=seed, base_pos=base_pos)
 
     def run(self):
-        """One verify pass over self.h (input hidden rows) and self.tokens (drafts)."""
+        """One verify pass over self.h (input hidden rows) and self.tokens (drafts); an NVTX range per
+        layer, for the head and for the acceptance (each library call inside has its own)."""
+        nvtx = torch.cuda.nvtx
         for l in range(len(self.layers)):
+            nvtx.range_push(f"layer {l}")
             self.layer(l)
+            nvtx.range_pop()
+        nvtx.range_push("head")
         self.head()
+        nvtx.range_pop()
+        nvtx.range_push("accept")
         self.accept()
+        nvtx.range_pop()
 
     # -- the same pass as one persistent cooperative launch -----------------------
     def prepare_fused(self, temperature: float = 1.0, sample: bool = False, seed: int = 0, base_pos: int = 0,

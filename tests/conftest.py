@@ -25,3 +25,18 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+@pytest.fixture(autouse=True)
+def _bounds_checked_build(request):
+    """Under SDV_DEBUG_BOUNDS=1 (the bounds-checked library): after every GPU test that loaded the
+    library, no bounds check may have failed (site numbers >= 100 in the status word)."""
+    yield
+    if os.environ.get("SDV_DEBUG_BOUNDS") != "1" or "gpu" not in request.keywords:
+        return
+    import speculative_decoding_verify_gb300 as m
+    if m._lib is None:
+        return
+    assert m.build_flags() & 1, "SDV_DEBUG_BOUNDS=1 but the loaded library is the release build"
+    st, site = m.device_status_site()
+    assert site < 100, f"bounds check failed at site {site} (status {st})"
