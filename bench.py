@@ -29,6 +29,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "weight-stream GB/s (% of HBM peak) per verify pass at K+1=5; verified pos/s"
+METRIC_TREE = "weight-stream GB/s (% of HBM peak) per tree verify pass at M=16; verified pos/s"
 NOMINAL_HBM_GBS = 8000.0
 
 
@@ -102,7 +103,7 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # model construction
 # ---------------------------------------------------------------------------
-def build_stack(spec, M, device, timings):
+def build_stack(spec, M, device, timings, tree_parent=None):
     import numpy as np
     import torch
 
@@ -126,7 +127,7 @@ def build_stack(spec, M, device, timings):
     fn = torch.from_numpy(spec.final_norm()).to(device)
     timings["build_s"] = time.time() - t0
     return VerifyStack(layers, norms, fn, head, spec.hidden, spec.ffn, spec.vocab, M, wq=spec.wq,
-                       head_q=spec.head_q, device=device)
+                       head_q=spec.head_q, device=device, tree_parent=tree_parent)
 
 
 # The translation units of pass_kernel and the headers they include.
@@ -720,6 +721,86 @@ def case_bench(args, local):
         raise SystemExit(1)
 
 
+SKINNY_SHAPES = (("QKV/O-like 5120x5120", 5120, 5120), ("FFN up/gate 5120->17408", 17408, 5120),
+                 ("FFN down 17408->5120", 5120, 17408))
+
+
+def skinny_bench(args, local):
+    """Layer-sized skinny matmuls: each shape x M in {1, 2, 3, 5, 8} x {Q8_0, 4-bit}, one
+    sd_qmatmul_multipos call per step over activations formed by the fused RMSNorm + int8 requant
+    (weight 1 + N(0, 0.1), eps 1e-6) of N(0, 1) rows.  The weights rotate over copies totalling at
+    least 1 GB, so no call finds its matrix in L2.  Device time of back-to-back calls (CUDA events
+    around the loop).  Prints one JSON line: the aggregate weight-stream GB/s over all cases, and
+    each case."""
+    import numpy as np
+    import torch
+
+    import sdgen
+    from speculative_decoding_verify_gb300 import build as b
+    b.build()
+    sdgen.build()
+    import speculative_decoding_verify_gb300 as sdv
+    from speculative_decoding_verify_gb300.verify_pass import repack_matrix
+
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    peak, peak_kind = measured_peaks()
+    rotate_bytes = 1 << 30
+    cases = []
+    tot_bytes, tot_ms = 0, 0.0
+    for qt, qname in ((sdv.Q8_0, "Q8_0"), (sdv.Q4_32, "4-bit")):
+        for sname, n, k in SKINNY_SHAPES:
+            blocks = sdgen.pinned_quantized_normal(qt, sdgen.key(21, qt, n, k), n, k)
+            w0 = repack_matrix(qt, blocks, n, k, device=dev)
+            nbytes = n * (k // 32) * sdv.BLOCK_BYTES[qt]
+            copies = [w0] + [w0.clone() for _ in range(max(1, -(-rotate_bytes // w0.numel())) - 1)]
+            ws = sdv.workspace(sdv.qmatmul_workspace_bytes(qt, n, k), device=dev)
+            nw = torch.from_numpy(sdgen.norm_weight(sdgen.key(22, k), k)).to(dev)
+            for M in (1, 2, 3, 5, 8):
+                x = torch.from_numpy(sdgen.normal(sdgen.key(23, k, M), (M, k))).to(dev)
+                q = torch.empty((M, k), dtype=torch.int8, device=dev)
+                sc = torch.empty((M, k // 32), dtype=torch.float32, device=dev)
+                sdv.rmsnorm_quant_acts(x, nw, q, sc, eps=1e-6)
+                y = torch.empty((M, n), dtype=torch.float32, device=dev)
+                for i in range(args.warmup):
+                    sdv.qmatmul_multipos(qt, copies[i % len(copies)], n, k, q, sc, ws, y=y)
+                torch.cuda.synchronize()
+                reps = max(args.steps, 2 * len(copies))
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for i in range(reps):
+                    sdv.qmatmul_multipos(qt, copies[i % len(copies)], n, k, q, sc, ws, y=y)
+                e1.record()
+                torch.cuda.synchronize()
+                if sdv.device_status() != 0:
+                    raise RuntimeError(f"device status after {qname} {sname} M={M}")
+                ms = e0.elapsed_time(e1) / reps
+                gbs = nbytes / (ms * 1e-3) / 1e9
+                cases.append({"format": qname, "shape": sname, "n_out": n, "k_in": k, "M": M,
+                              "weight_bytes": nbytes, "us_per_call": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
+                              "frac_of_peak": round(gbs / peak, 3), "copies": len(copies)})
+                tot_bytes += nbytes
+                tot_ms += ms
+                log(f"{qname} {sname} M={M}: {ms * 1e3:.1f} us, {gbs:.0f} GB/s ({gbs / peak:.1%})")
+            del copies, w0, ws
+            torch.cuda.empty_cache()
+    agg = tot_bytes / (tot_ms * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": "weight-stream GB/s of layer-sized skinny matmuls (aggregate over shapes x M x formats)",
+        "value": agg, "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8 activations, Q8_0 / 4-bit codes",
+        "data": "synthetic (seeded N(0,0.02) weights, N(0,1) rows through RMSNorm + requant)",
+        "config": {"workload": "layer-sized skinny matmuls: 5120x5120, 5120->17408, 17408->5120 in Q8_0 and 4-bit, "
+                               "M in {1,2,3,5,8}, one sd_qmatmul_multipos call per step",
+                   "l2": "weights rotated over copies of at least 1 GB per shape (larger than L2)"},
+        "roofline": {"bound": "hbm", "kernel": "qmm_kernel (multi-position matmul, one launch per call)",
+                     "achieved": agg, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": agg / peak,
+                     "traffic": None, "algorithmic_bytes_per_launch": "each case's weight_bytes",
+                     "avg_launch_ms": tot_ms / len(cases)},
+        "gpu_launches": sum(max(args.steps, 2 * c["copies"]) for c in cases),
+        "cases": cases}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -743,6 +824,9 @@ def main():
     ap.add_argument("--trace", default=None, metavar="FILE",
                     help="after the timed region, run one traced pass and write its per-phase, per-CTA "
                          "global-timer stamps (numpy .npz) to FILE")
+    ap.add_argument("--config", type=int, default=4, choices=(2, 4, 5),
+                    help="2: layer-sized skinny matmuls (own JSON line); 4: the 64-layer verify pass at K+1=5 "
+                         "(default); 5: the same stack verifying a 16-node draft tree (M=16)")
     ap.add_argument("--case", default=None, choices=CASES,
                     help="instead of the pass: run one kernel on one layer-sized case --steps times, for profiling")
     args = ap.parse_args()
@@ -772,6 +856,12 @@ def main():
     if args.attention:
         attention_bench(args, local)
         return
+    if args.config == 2:
+        skinny_bench(args, local)
+        return
+    tree = args.config == 5
+    if tree:
+        M = args.M = 16
 
     import numpy as np
     import torch
@@ -796,10 +886,13 @@ def main():
 
     timings = {}
     log(f"[rank {rank}] building the {spec.layers}-layer stack ({spec.weight_bytes() / 1e9:.2f} GB of weights)")
-    stack = build_stack(spec, M, device, timings)
+    parent_np = sdgen.tree16(0)[0] if tree else None
+    stack = build_stack(spec, M, device, timings,
+                        tree_parent=torch.from_numpy(parent_np).to(device) if tree else None)
     h0 = torch.from_numpy(spec.hidden_in(M)).to(device)
 
-    # drafts: the target's argmax with probability 0.75 per position, else uniform (from an untimed pass)
+    # drafts: the target's argmax with probability 0.75 per position, else uniform (from an untimed pass);
+    # a tree: uniform tokens except along the path 0-1-3-7-15, which follows the argmax chain
     stack.h.copy_(h0)
     if args.fused_only:
         stack.run_fused()
@@ -807,8 +900,13 @@ def main():
         stack.run()
     torch.cuda.synchronize()
     am = stack.argmax.cpu().numpy()
-    drafts = sdgen.drafts_p(sdgen.key(4, 7), am[:M - 1], spec.vocab)
-    stack.tokens[:M - 1].copy_(torch.from_numpy(drafts))
+    if tree:
+        drafts = sdgen.uniform_tokens(sdgen.key(4, 8), M, spec.vocab).astype(np.int32)
+        for child in (1, 3, 7, 15):
+            drafts[child] = am[parent_np[child]]
+    else:
+        drafts = sdgen.drafts_p(sdgen.key(4, 7), am[:M - 1], spec.vocab)
+    stack.tokens[:len(drafts)].copy_(torch.from_numpy(drafts))
     if sdv.device_status() != 0:
         raise RuntimeError("device status after the first pass")
 
@@ -890,7 +988,7 @@ def main():
 
     def e2e_step():
         h_dev.copy_(h_host, non_blocking=True)
-        stack.tokens[:M - 1].copy_(d_host, non_blocking=True)
+        stack.tokens[:d_host.numel()].copy_(d_host, non_blocking=True)
         graph.replay()
         out_host.copy_(stack.out_tokens, non_blocking=True)
         cnt_host.copy_(stack.out_count, non_blocking=True)
@@ -939,11 +1037,15 @@ def main():
         roof["per_op_pipeline_eager"] = {k: {"launches": v["launches"], "ms": round(v["ms"], 4),
                                              "share": round(v["ms"] / prof_total, 4)} for k, v in prof.items()}
 
-    line = {"metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+    line = {"metric": METRIC_TREE if tree else METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "int8", "data": "synthetic (seeded N(0,0.02) weights, N(0,1) hidden rows)",
-            "config": {"workload": "verify pass: 64-layer 27B-shaped 4-bit projection stack + 5120x151936 "
-                                   "Q8_0 head + greedy accept, K+1=5",
+            "config": {"workload": ("tree verify pass: 16-node draft tree (root, binary depth 3, one spine node) "
+                                    "as M=16 rows through the 64-layer 27B-shaped 4-bit stack + 5120x151936 Q8_0 "
+                                    "head + greedy tree accept") if tree else
+                                   ("verify pass: 64-layer 27B-shaped 4-bit projection stack + 5120x151936 "
+                                    "Q8_0 head + greedy accept, K+1=5"),
                        "M": M, "layers": spec.layers, "hidden": spec.hidden, "ffn": spec.ffn, "vocab": spec.vocab,
                        "weight_bytes_per_pass": wbytes, "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                        "l2": "inputs larger than L2: 14.2 GB of weights streamed per step vs 129 MB L2",

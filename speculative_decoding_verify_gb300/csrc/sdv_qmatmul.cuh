@@ -179,6 +179,7 @@ struct QmmArgs {
     int32_t GR;             // schedule granule in blocks: every piece and split boundary is a multiple (8 for the
                             // 256-weight K-quant super-blocks, else 1)
     int32_t GRS;            // log2 GR (the schedule walk shifts instead of dividing: it runs at every phase start)
+    int32_t af_build;       // single-operation calls: act_frag_kernel forms af_frag / af_meta from q / sc first
 };
 
 constexpr int KIND_MATMUL = 0, KIND_NORM = 1, KIND_ACCEPT = 2, KIND_COMBINE = 3, KIND_HSTATS = 4;
@@ -1819,6 +1820,53 @@ __device__ inline void greedy_accept(const int32_t *argmax, const int32_t *token
 }
 
 // ---------------------------------------------------------------------------
+// single-operation calls: the activation fragments and {corr, d_a} records of plain int8 rows, for
+// the whole k range, formed once per call into the workspace (the same bytes stage_rows forms in
+// shared memory), so that each CTA stages a split with one bulk copy instead of latency-bound row
+// loads.  Items (block, position, c) of the fragments, then (block, position slot) of the records.
+// ---------------------------------------------------------------------------
+template <int QT>
+__global__ void __launch_bounds__(256) act_frag_kernel(const QmmArgs a) {
+    pdl_wait();
+    pdl_launch_dependents();  // the matmul's producer may start streaming weights
+    const int M = a.M, NT = af_nt(M), P8 = 8 * NT;
+    const int64_t K = static_cast<int64_t>(a.KB) * 32;
+    const int64_t nfrag = static_cast<int64_t>(a.KB) * M * 4, nmeta = static_cast<int64_t>(a.KB) * P8;
+    uint8_t *frag = const_cast<uint8_t *>(a.af_frag);
+    float *meta = const_cast<float *>(a.af_meta);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t it = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; it < nfrag + nmeta; it += stride) {
+        if (it < nfrag) {
+            const int64_t jb = it / (M * 4);
+            const int rem = static_cast<int>(it - jb * M * 4), m = rem >> 2, c = rem & 3;
+            const uint2 raw = b_raw(a.q + m * K + jb * 32, c);
+            if (NT == 1) reinterpret_cast<uint4 *>(frag)[it] = b_frag_from_raw<QT>(raw);
+            else reinterpret_cast<uint2 *>(frag)[it] = raw;
+        } else {
+            const int64_t i2 = it - nfrag, jb = i2 / P8;
+            const int m = static_cast<int>(i2 - jb * P8);
+            const bool real = m < M;
+            const float da = real ? __ldg(a.sc + static_cast<int64_t>(m) * a.KB + jb) : 0.0f;
+            if constexpr (is_kq(QT)) {
+                int s4[4] = {0, 0, 0, 0};
+                if (real) {
+                    const uint4 *p = reinterpret_cast<const uint4 *>(a.q + m * K + jb * 32);
+                    const uint4 x0 = __ldg(p), x1 = __ldg(p + 1);
+                    s4[0] = dp4a(0x01010101, static_cast<int>(x0.y), dp4a(0x01010101, static_cast<int>(x0.x), 0));
+                    s4[1] = dp4a(0x01010101, static_cast<int>(x0.w), dp4a(0x01010101, static_cast<int>(x0.z), 0));
+                    s4[2] = dp4a(0x01010101, static_cast<int>(x1.y), dp4a(0x01010101, static_cast<int>(x1.x), 0));
+                    s4[3] = dp4a(0x01010101, static_cast<int>(x1.w), dp4a(0x01010101, static_cast<int>(x1.z), 0));
+                }
+                reinterpret_cast<float4 *>(meta)[i2] = kq_meta<QT>(s4, da);
+            } else {
+                const float corr = dot_corr<QT>(real ? a.q + m * K + jb * 32 : nullptr);
+                reinterpret_cast<float2 *>(meta)[i2] = make_float2(corr, da);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // single-operation kernel (one matmul phase per launch)
 // ---------------------------------------------------------------------------
 template <int QT, int PAIR, int NT>
@@ -1841,8 +1889,22 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
     }
     pdl_wait();
     pdl_launch_dependents();
-    if (warp >= FIN_WARP0) (void)finish_phase<PAIR, NT>(a, sm, pk, fin_it, cs, warp - FIN_WARP0);
-    else (void)consume_phase<QT, PAIR, NT>(a, sm, it, pk, act_it, nrm_it, cs);
+    if (warp >= FIN_WARP0) {
+        (void)finish_phase<PAIR, NT>(a, sm, pk, fin_it, cs, warp - FIN_WARP0);
+    } else {
+        // the first split's activations are copied while the first weight stage is still in flight
+        const bool pre = tid == 0 && pre_issue_staging(a, sm, act_it, cs);
+        (void)consume_phase<QT, PAIR, NT>(a, sm, it, pk, act_it, nrm_it, cs, pre);
+    }
+}
+
+// Single-operation calls with several k-splits: the matmul leaves every unit's partial sums, and this
+// launch adds them in (split, piece) order and runs the epilogue, each CTA an equal share of the units
+// (the one-launch pass's combine phase, as its own launch).
+static __global__ void __launch_bounds__(WORK_THREADS) qmm_combine_kernel(const QmmArgs a) {
+    pdl_wait();
+    pdl_launch_dependents();
+    combine_phase<false>(a, static_cast<int>(threadIdx.x) >> 5);
 }
 
 // ---------------------------------------------------------------------------
@@ -2055,8 +2117,19 @@ struct QmmPlan {
     int32_t KB, NU, KS, KBs, KBlast, G, P, D, R, SB, NS, NRB, rows_p, GR, GRS;
     int64_t W;
     uint32_t step_bytes;
-    size_t ws_part, ws_cnt, ws_stats, ws_total;
+    size_t ws_part, ws_cnt, ws_stats, ws_act, ws_total;
 };
+
+// Workspace bytes per k block of the activation fragments and {corr, d_a} records a single-operation
+// call forms (the largest over M = 1..16).
+inline size_t af_ws_bytes_per_block(int qtype) {
+    size_t mx = 0;
+    for (int M = 1; M <= 16; ++M) {
+        const size_t b = af_frag_bytes(M) + af_meta_bytes_q(M, qtype);
+        mx = b > mx ? b : mx;
+    }
+    return mx;
+}
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -2104,7 +2177,8 @@ inline bool make_plan(int qtype, int64_t n_out, int64_t k_in, bool pair, bool he
     p.ws_cnt = WS_CNT_BYTES;
     p.ws_part = align_up(static_cast<size_t>(shared_units) * p.KS * p.P * rows * MPAD * sizeof(float), 256);
     p.ws_stats = head ? align_up(static_cast<size_t>(nst) * MPAD * sizeof(float4), 256) : 0;
-    p.ws_total = p.ws_part + p.ws_cnt + p.ws_stats;
+    p.ws_act = align_up(static_cast<size_t>(p.KB) * af_ws_bytes_per_block(qtype), 256);
+    p.ws_total = p.ws_part + p.ws_cnt + p.ws_stats + p.ws_act;
     return true;
 }
 
@@ -2179,7 +2253,20 @@ cudaError_t qmm_dispatch(QmmArgs a, QmmPlan &p, cudaStream_t s) {  // instantiat
     a.kind = KIND_MATMUL;
     a.qt = QT;
     a.pair = PAIR;
-    return af_nt(a.M) == 1 ? qmm_launch<QT, PAIR, 1>(a, L.total, s) : qmm_launch<QT, PAIR, 2>(a, L.total, s);
+    if (a.af_build) {
+        const int64_t items = static_cast<int64_t>(a.KB) * (4 * a.M + 8 * af_nt(a.M));
+        const int64_t blocks = (items + 255) / 256;
+        const cudaError_t e = launch(act_frag_kernel<QT>, dim3(static_cast<unsigned>(blocks < 1024 ? blocks : 1024)),
+                                     dim3(256), 0, s, a);
+        if (e != cudaSuccess) return e;
+    }
+    // several k-splits (no gate|up pairing, not the head): the partial sums are added by a second launch
+    // spread over the grid rather than by the last split to finish each unit, whose fixups would run
+    // one after another on the finisher warps
+    a.defer = (!PAIR && !a.head && a.KS > 1) ? 1 : 0;
+    cudaError_t e = af_nt(a.M) == 1 ? qmm_launch<QT, PAIR, 1>(a, L.total, s) : qmm_launch<QT, PAIR, 2>(a, L.total, s);
+    if (e == cudaSuccess && a.defer) e = launch(qmm_combine_kernel, dim3(a.G), dim3(WORK_THREADS), 0, s, a);
+    return e;
 }
 
 extern template cudaError_t qmm_dispatch<SD_Q4_32, 0>(QmmArgs, QmmPlan &, cudaStream_t);

@@ -47,6 +47,14 @@ static cudaError_t dispatch(int qtype, bool pair, QmmArgs &a, QmmPlan &p, cudaSt
     return qmm_dispatch<SD_Q8_0, 0>(a, p, s);
 }
 
+// The call's activation fragments and records go to the workspace's last region (act_frag_kernel).
+static void set_af_build(QmmArgs &a, const QmmPlan &p, uint8_t *ws) {
+    uint8_t *act = ws + p.ws_cnt + p.ws_part + p.ws_stats;
+    a.af_frag = act;
+    a.af_meta = reinterpret_cast<const float *>(act + static_cast<size_t>(p.KB) * af_frag_bytes(a.M));
+    a.af_build = 1;
+}
+
 static bool known_qtype(int q) { return q == SD_Q8_0 || q == SD_Q4_32 || q == SD_Q4_K || q == SD_Q6_K; }
 
 static void fill_plan(QmmArgs &a, const QmmPlan &p) {
@@ -172,6 +180,7 @@ sd_status sd_qmatmul_multipos(int qtype, const void *w, int64_t n_out, int64_t k
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     a.cnt = reinterpret_cast<uint32_t *>(ws);
     a.part = reinterpret_cast<float *>(ws + p.ws_cnt);
+    set_af_build(a, p, ws);
     a.status = st;
     return dispatch(qtype, pair, a, p, cs(stream)) == cudaSuccess ? SD_OK : SD_ECUDA;
 }
@@ -207,6 +216,7 @@ sd_status sd_head_logits(const void *w, int64_t vocab, int64_t hidden, const int
     a.part = reinterpret_cast<float *>(ws + p.ws_cnt);
     const int64_t nst = (vocab + STAT_TILE - 1) / STAT_TILE;
     a.st_part = reinterpret_cast<float4 *>(ws + p.ws_cnt + p.ws_part);
+    set_af_build(a, p, ws);
     a.n_stiles = static_cast<int32_t>(nst);
     a.head = 1;
     a.T = temperature;
