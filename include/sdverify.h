@@ -79,7 +79,8 @@ typedef enum { SD_Q8_0 = 0, SD_Q4_32 = 1, SD_Q4_K = 2, SD_Q6_K = 3 } sd_qtype;
 #define SD_EPI_SILU_MUL_REQUANT 2u  /* gate|up pair: h = silu(g) * u, requantised into q_next/scales_next */
 
 const char *sd_status_string(sd_status s);
-int sd_abi_version(void); /* 4: sd_device_status_site and sd_build_flags; 3: sd_pass_desc carries the down
+int sd_abi_version(void); /* 5: sd_head_shortlist takes the repacked head and returns sd_head_logits' argmax;
+                           4: sd_device_status_site and sd_build_flags; 3: sd_pass_desc carries the down
                            projections' format, sd_pass the K-quant flag */
 
 /*
@@ -248,20 +249,25 @@ sd_status sd_head_logits(const void *w, int64_t vocab, int64_t hidden, const int
  * flags 0) for sd_head_shortlist.  Weights must be finite.
  *
  * sd_head_shortlist (verify time): copy_w the repacked copy, bound / wnorm
- * from the build, head_blocks the GGUF-order Q8_0 head; q int8 [M][hidden],
- * scales fp32 [M][hidden/32] as for sd_head_logits; 1 <= M <= 16.  argmax
- * int32 [M] receives, per position, the row maximising the exact score
- *   e_r = sum over blocks b, in order, of (d_w[r,b] * d_a[b]) * dot_b(r)
- * in fp64 (one rounding per product and per addition; lowest index among
- * equal maxima) -- the argmax of the exact head, whatever the copy says.
- * n_cand int32 [M] (or NULL) receives how many rows were scored exactly.
+ * from the build, head_w the REPACKED Q8_0 head (as for sd_head_logits); q
+ * int8 [M][hidden], scales fp32 [M][hidden/32] as for sd_head_logits;
+ * 1 <= M <= 16.  argmax int32 [M] receives, per position, sd_head_logits'
+ * argmax on the same inputs, bit for bit: the row of the largest fp32 logit
+ * of the head's own matmul (lowest index among equal maxima).  The copy's
+ * scores and bounds rule rows out; the 32-row tiles holding the remaining
+ * candidates are scored by the head's matmul restricted to them (same plan,
+ * same arithmetic as sd_head_logits).  n_cand int32 [M] (or NULL) receives
+ * the candidate count per position (vocab in full mode).  Full mode: when the
+ * previous call's candidates filled more than a quarter of the tiles, the call
+ * skips the copy and scores every tile (the full head plus a few empty
+ * launches), trying the shortlist again every 16th call.
  * Device-side: a position with no candidate (non-finite inputs only) records
  * SD_EDEVICE in the status word and gets argmax -1.  workspace: ws_bytes >=
  * sd_shortlist_workspace_bytes(vocab, hidden), zero-filled by the caller once
- * (it holds counters, the copy matmul's among them, that every call returns
- * to zero).
+ * and kept between calls (it holds counters that every call returns to zero,
+ * and the mode state).
  * Errors: SD_EINVAL on null/misaligned pointers or bad sizes; SD_EUNSUPPORTED
- * for M > 16 or hidden/32 * M > 12288.
+ * for M > 16.
  */
 /*
  * Decode attention over the K+1 verified positions ("Inside OpenJet Engine",
@@ -354,7 +360,7 @@ sd_status sd_kv_commit(void *k_cache, void *v_cache, int32_t H_kv, int32_t D, in
 sd_status sd_shortlist_build(const void *head_blocks, int64_t vocab, int64_t hidden, void *copy_blocks, float *bound,
                              float *wnorm, sd_stream_t stream);
 size_t sd_shortlist_workspace_bytes(int64_t vocab, int64_t hidden);
-sd_status sd_head_shortlist(const void *copy_w, const float *bound, const float *wnorm, const void *head_blocks,
+sd_status sd_head_shortlist(const void *copy_w, const float *bound, const float *wnorm, const void *head_w,
                             int64_t vocab, int64_t hidden, const int8_t *q, const float *scales, int32_t M,
                             int32_t *argmax, int32_t *n_cand, void *workspace, size_t ws_bytes, sd_stream_t stream);
 

@@ -303,11 +303,12 @@ def shortlist_workspace_bytes(vocab: int, hidden: int) -> int:
     return int(lib().sd_shortlist_workspace_bytes(vocab, hidden))
 
 
-def head_shortlist(copy_w: torch.Tensor, bound: torch.Tensor, wnorm: torch.Tensor, head_blocks: torch.Tensor,
+def head_shortlist(copy_w: torch.Tensor, bound: torch.Tensor, wnorm: torch.Tensor, head_w: torch.Tensor,
                    vocab: int, hidden: int, q: torch.Tensor, scales: torch.Tensor, ws: torch.Tensor,
                    argmax: torch.Tensor, n_cand: torch.Tensor | None = None):
+    """argmax = sd_head_logits' argmax on the repacked Q8_0 head head_w; ws zero-filled once and kept."""
     M = q.shape[0]
-    _check(lib().sd_head_shortlist(_p(copy_w), _p(bound), _p(wnorm), _p(head_blocks), vocab, hidden, _p(q),
+    _check(lib().sd_head_shortlist(_p(copy_w), _p(bound), _p(wnorm), _p(head_w), vocab, hidden, _p(q),
                                    _p(scales), M, _p(argmax), _p(n_cand), _p(ws), ws.numel(), _stream()),
            "sd_head_shortlist")
 

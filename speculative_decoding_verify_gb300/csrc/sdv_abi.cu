@@ -281,7 +281,7 @@ const char *sd_status_string(sd_status s) {
     return "unknown status";
 }
 
-int sd_abi_version(void) { return 4; }
+int sd_abi_version(void) { return 5; }
 
 void sd_set_pdl(int enable) { g_pdl = enable ? 1 : 0; }
 

@@ -32,6 +32,16 @@ int *status_ptr();
 int num_sms();
 // Whether launches carry the programmatic-stream-serialisation attribute.
 bool pdl_enabled();
+// sd_qmatmul_multipos restricted by a previous launch on the stream: only the row tiles set in
+// unit_mask (bit per 32-row tile; null: all) are computed, and nothing at all if *skip_if != 0
+// (null: always).  af_pre / af_meta_pre (nullable): the activation fragments and records of q / scales
+// in this format's layout, formed by an earlier launch (else the call forms them).  Outputs of a
+// computed tile equal the unrestricted call's bit for bit.
+sd_status qmatmul_restricted(int qtype, const void *w, int64_t n_out, int64_t k_in, const int8_t *q,
+                             const float *scales, int32_t M, float *y, const float *residual, uint32_t epilogue,
+                             int64_t requant_col0, int8_t *q_next, float *scales_next, void *workspace,
+                             size_t ws_bytes, const uint32_t *unit_mask, const int *skip_if, const uint8_t *af_pre,
+                             const float *af_meta_pre, sd_stream_t stream);
 // Raise a kernel's dynamic shared-memory limit to everything the device lets one block have, once
 // per (kernel, device).  The limit is a property of the function, not of a launch: set per call to
 // that call's size, it would be lowered by a smaller call after a larger one had been captured into

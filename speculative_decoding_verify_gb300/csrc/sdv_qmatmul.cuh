@@ -180,6 +180,9 @@ struct QmmArgs {
                             // 256-weight K-quant super-blocks, else 1)
     int32_t GRS;            // log2 GR (the schedule walk shifts instead of dividing: it runs at every phase start)
     int32_t af_build;       // single-operation calls: act_frag_kernel forms af_frag / af_meta from q / sc first
+    // single-operation calls whose work a previous launch decides (read after griddepcontrol.wait):
+    const uint32_t *unit_mask;  // bit per row tile: only set tiles are computed (null: all)
+    const int *skip_if;         // non-zero: the call does nothing (null: always runs)
 };
 
 constexpr int KIND_MATMUL = 0, KIND_NORM = 1, KIND_ACCEPT = 2, KIND_COMBINE = 3, KIND_HSTATS = 4;
@@ -261,12 +264,16 @@ struct PieceIter {
     int64_t g, hi;      // cursor in the shared step sequence
     int d_next, d_end;  // whole units still to take
     int cta;            // the CTA walking this schedule
+    int mw;             // restricted calls: index of the unit-mask word in mbits (-1: none loaded)
+    uint32_t mbits;
 };
 
 // The schedule of CTA `cta` (host and device: the host replays it to check the partition).
 __host__ __device__ __forceinline__ void pieces_begin_cta(const QmmArgs &a, PieceIter &it, int cta) {
     const int64_t c = cta, wq = seq_len(a) >> a.GRS;
     it.cta = cta;
+    it.mw = -1;
+    it.mbits = 0;
     if (cta >= a.G) {  // a matmul with fewer granules of work than the grid has CTAs: none for this one
         it.g = it.hi = 0;
         it.d_next = it.d_end = 0;
@@ -280,6 +287,18 @@ __host__ __device__ __forceinline__ void pieces_begin_cta(const QmmArgs &a, Piec
 
 __device__ __forceinline__ void pieces_begin(const QmmArgs &a, PieceIter &it) {
     pieces_begin_cta(a, it, static_cast<int>(blockIdx.x));
+}
+
+// Unit u is computed in this call (a call restricted to a set of row tiles reads them from unit_mask;
+// the walk's units mostly increase, so one mask word is loaded per 32 units, not one per piece).
+__device__ __forceinline__ bool unit_on(const QmmArgs &a, int u, PieceIter &it) {
+    if (!a.unit_mask) return true;
+    const int pu = phys_unit(a, u);
+    if ((pu >> 5) != it.mw) {
+        it.mw = pu >> 5;
+        it.mbits = __ldcg(a.unit_mask + it.mw);
+    }
+    return ((it.mbits >> (pu & 31)) & 1u) != 0u;
 }
 
 // The next piece in processing order (shared run first, whole units last); false when done.
@@ -309,6 +328,24 @@ __host__ __device__ __forceinline__ bool pieces_next(const QmmArgs &a, PieceIter
         return true;
     }
     return false;
+}
+
+// The next piece of a unit this call computes.
+__device__ __forceinline__ bool pieces_next_on(const QmmArgs &a, PieceIter &it, Piece &p) {
+    while (pieces_next(a, it, p))
+        if (unit_on(a, p.u, it)) return true;
+    return false;
+}
+
+// Whether this CTA has any piece in this phase (past the grid's CTAs, or every piece of a restricted
+// call in units it leaves out: none; the roles then sit the phase out).
+__device__ inline bool cta_has_work(const QmmArgs &a) {
+    if (static_cast<int>(blockIdx.x) >= a.G) return false;
+    if (!a.unit_mask) return true;
+    PieceIter it;
+    pieces_begin(a, it);
+    Piece p;
+    return pieces_next_on(a, it, p);
 }
 
 // ---------------------------------------------------------------------------
@@ -869,9 +906,9 @@ __device__ inline void produce_phase(const QmmArgs &a, const Smem &sm, uint32_t 
     PieceIter pit;
     pieces_begin(a, pit);
     Piece pc, nx;
-    bool have = pieces_next(a, pit, pc);
+    bool have = pieces_next_on(a, pit, pc);
     while (have && !cs.abort) {
-        const bool more = pieces_next(a, pit, nx);
+        const bool more = pieces_next_on(a, pit, nx);
         {
             QPiece &q = cs.pq[npub % PQ_N];
             q.s = pc.s;
@@ -1260,7 +1297,7 @@ __device__ inline bool pre_issue_staging(const QmmArgs &a, const Smem &sm, uint3
     PieceIter pit;
     pieces_begin(a, pit);
     Piece pc;
-    if (!pieces_next(a, pit, pc)) return false;
+    if (!pieces_next_on(a, pit, pc)) return false;
     if (act_it > 0 && !mbar_wait_bounded(sm.act_free, (act_it - 1) & 1u, WAIT_NS, &cs.abort)) {
         set_status(a.status, SD_ETIMEOUT);
         cs.abort = 1;
@@ -1281,7 +1318,7 @@ template <int QT, int PAIR, int NT>
 __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t &it, uint32_t &pk, uint32_t &act_it,
                                      uint32_t &nrm_it, CtaShared &cs, bool pre_issued = false,
                                      uint64_t *tslot = nullptr) {
-    if (static_cast<int>(blockIdx.x) >= a.G) return true;  // no work for this CTA in this phase
+    if (!cta_has_work(a)) return true;  // no work for this CTA in this phase
     const int M = a.M;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int lg = lane >> 2, lc = lane & 3;
@@ -1511,7 +1548,7 @@ __device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &
     constexpr int FIN_MPW = (8 * NT + NF - 1) / NF;  // positions per finisher warp at most
     constexpr int CH = 8;                            // partial sums loaded together
     constexpr int FKS = 8, FP = 4;                   // splits x pieces held at once when all splits share
-    if (static_cast<int>(blockIdx.x) >= a.G) return true;  // no work for this CTA in this phase
+    if (!cta_has_work(a)) return true;  // no work for this CTA in this phase
     const int M = a.M;
     const int lane = threadIdx.x & 31;
     int st_cur = -1, st_n = 0;  // head: current statistics tile and tiles finished in it
@@ -1826,31 +1863,27 @@ __device__ inline void greedy_accept(const int32_t *argmax, const int32_t *token
 // loads.  Items (block, position, c) of the fragments, then (block, position slot) of the records.
 // ---------------------------------------------------------------------------
 template <int QT>
-__global__ void __launch_bounds__(256) act_frag_kernel(const QmmArgs a) {
-    pdl_wait();
-    pdl_launch_dependents();  // the matmul's producer may start streaming weights
-    const int M = a.M, NT = af_nt(M), P8 = 8 * NT;
-    const int64_t K = static_cast<int64_t>(a.KB) * 32;
-    const int64_t nfrag = static_cast<int64_t>(a.KB) * M * 4, nmeta = static_cast<int64_t>(a.KB) * P8;
-    uint8_t *frag = const_cast<uint8_t *>(a.af_frag);
-    float *meta = const_cast<float *>(a.af_meta);
+__device__ inline void act_frag_build(const int8_t *q, const float *sc, int M, int KB, uint8_t *frag, float *meta) {
+    const int NT = af_nt(M), P8 = 8 * NT;
+    const int64_t K = static_cast<int64_t>(KB) * 32;
+    const int64_t nfrag = static_cast<int64_t>(KB) * M * 4, nmeta = static_cast<int64_t>(KB) * P8;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t it = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; it < nfrag + nmeta; it += stride) {
         if (it < nfrag) {
             const int64_t jb = it / (M * 4);
             const int rem = static_cast<int>(it - jb * M * 4), m = rem >> 2, c = rem & 3;
-            const uint2 raw = b_raw(a.q + m * K + jb * 32, c);
+            const uint2 raw = b_raw(q + m * K + jb * 32, c);
             if (NT == 1) reinterpret_cast<uint4 *>(frag)[it] = b_frag_from_raw<QT>(raw);
             else reinterpret_cast<uint2 *>(frag)[it] = raw;
         } else {
             const int64_t i2 = it - nfrag, jb = i2 / P8;
             const int m = static_cast<int>(i2 - jb * P8);
             const bool real = m < M;
-            const float da = real ? __ldg(a.sc + static_cast<int64_t>(m) * a.KB + jb) : 0.0f;
+            const float da = real ? __ldg(sc + static_cast<int64_t>(m) * KB + jb) : 0.0f;
             if constexpr (is_kq(QT)) {
                 int s4[4] = {0, 0, 0, 0};
                 if (real) {
-                    const uint4 *p = reinterpret_cast<const uint4 *>(a.q + m * K + jb * 32);
+                    const uint4 *p = reinterpret_cast<const uint4 *>(q + m * K + jb * 32);
                     const uint4 x0 = __ldg(p), x1 = __ldg(p + 1);
                     s4[0] = dp4a(0x01010101, static_cast<int>(x0.y), dp4a(0x01010101, static_cast<int>(x0.x), 0));
                     s4[1] = dp4a(0x01010101, static_cast<int>(x0.w), dp4a(0x01010101, static_cast<int>(x0.z), 0));
@@ -1859,11 +1892,19 @@ __global__ void __launch_bounds__(256) act_frag_kernel(const QmmArgs a) {
                 }
                 reinterpret_cast<float4 *>(meta)[i2] = kq_meta<QT>(s4, da);
             } else {
-                const float corr = dot_corr<QT>(real ? a.q + m * K + jb * 32 : nullptr);
+                const float corr = dot_corr<QT>(real ? q + m * K + jb * 32 : nullptr);
                 reinterpret_cast<float2 *>(meta)[i2] = make_float2(corr, da);
             }
         }
     }
+}
+
+template <int QT>
+__global__ void __launch_bounds__(256) act_frag_kernel(const QmmArgs a) {
+    pdl_wait();
+    pdl_launch_dependents();  // the matmul's producer may start streaming weights
+    if (a.skip_if && *reinterpret_cast<const volatile int *>(a.skip_if) != 0) return;
+    act_frag_build<QT>(a.q, a.sc, a.M, a.KB, const_cast<uint8_t *>(a.af_frag), const_cast<float *>(a.af_meta));
 }
 
 // ---------------------------------------------------------------------------
@@ -1877,6 +1918,13 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) cta_init(sm, a.NS, cs, a.af_frag ? 1u : static_cast<uint32_t>(CONS_THREADS));
     __syncthreads();
+    if (a.skip_if || a.unit_mask) {  // written by the previous launch: every role waits for it
+        pdl_wait();
+        if (a.skip_if && *reinterpret_cast<const volatile int *>(a.skip_if) != 0) {
+            pdl_launch_dependents();
+            return;
+        }
+    }
     uint32_t it = 0, pk = 0, act_it = 0, nrm_it = 0, fin_it = 0;
     if (warp == PRODUCER_WARP) {
         pdl_launch_dependents();

@@ -132,6 +132,19 @@ sd_status sd_qmatmul_multipos(int qtype, const void *w, int64_t n_out, int64_t k
                               int64_t requant_col0, int8_t *q_next, float *scales_next, void *workspace,
                               size_t ws_bytes, sd_stream_t stream) {
     SD_NVTX("sd_qmatmul_multipos");
+    return sdv::qmatmul_restricted(qtype, w, n_out, k_in, q, scales, M, y, residual, epilogue, requant_col0, q_next,
+                                   scales_next, workspace, ws_bytes, nullptr, nullptr, nullptr, nullptr, stream);
+}
+
+}  // extern "C"
+
+namespace sdv {
+
+sd_status qmatmul_restricted(int qtype, const void *w, int64_t n_out, int64_t k_in, const int8_t *q,
+                             const float *scales, int32_t M, float *y, const float *residual, uint32_t epilogue,
+                             int64_t requant_col0, int8_t *q_next, float *scales_next, void *workspace,
+                             size_t ws_bytes, const uint32_t *unit_mask, const int *skip_if, const uint8_t *af_pre,
+                             const float *af_meta_pre, sd_stream_t stream) {
     if (!known_qtype(qtype)) return SD_EINVAL;
     if (M < 1) return SD_EINVAL;
     if (M > 16) return SD_EUNSUPPORTED;
@@ -181,9 +194,20 @@ sd_status sd_qmatmul_multipos(int qtype, const void *w, int64_t n_out, int64_t k
     a.cnt = reinterpret_cast<uint32_t *>(ws);
     a.part = reinterpret_cast<float *>(ws + p.ws_cnt);
     set_af_build(a, p, ws);
+    if (af_pre) {
+        a.af_frag = af_pre;
+        a.af_meta = af_meta_pre;
+        a.af_build = 0;
+    }
+    a.unit_mask = unit_mask;
+    a.skip_if = skip_if;
     a.status = st;
     return dispatch(qtype, pair, a, p, cs(stream)) == cudaSuccess ? SD_OK : SD_ECUDA;
 }
+
+}  // namespace sdv
+
+extern "C" {
 
 sd_status sd_head_logits(const void *w, int64_t vocab, int64_t hidden, const int8_t *q, const float *scales, int32_t M,
                          float temperature, float *logits, int32_t *argmax, float *row_max, float *row_sumexp,

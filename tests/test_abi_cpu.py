@@ -43,7 +43,7 @@ def test_binding_types_every_declared_call(L):
 
 
 def test_status_strings_and_version(L):
-    assert L.sd_abi_version() == 4
+    assert L.sd_abi_version() == 5
     assert L.sd_status_string(0) == b"ok"
     assert L.sd_status_string(4) == b"device wait timed out"
 
