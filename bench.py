@@ -802,6 +802,26 @@ def skinny_bench(args, local):
         "cases": cases}), flush=True)
 
 
+def run_probe(name, extra):
+    """Build probes/<name> for sm_103a into _build/probes and run it; its table goes to stdout."""
+    import subprocess
+
+    from speculative_decoding_verify_gb300 import build as b
+    src = os.path.join(ROOT, "probes", {"consumer": "consumer_loop_probe.cu", "tcgen05": "tcgen05_probe.cu"}[name])
+    out_dir = os.path.join(ROOT, "_build", "probes")
+    os.makedirs(out_dir, exist_ok=True)
+    exe = os.path.join(out_dir, name)
+    cmd = [b.nvcc(), "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-I",
+           os.path.join(ROOT, "include"), "-I", os.path.join(ROOT, "speculative_decoding_verify_gb300", "csrc"), src,
+           "-o", exe]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise SystemExit(f"probe build failed:\n{r.stderr[-3000:]}")
+    r = subprocess.run([exe] + list(extra))
+    if r.returncode != 0:
+        raise SystemExit(r.returncode)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -828,6 +848,9 @@ def main():
     ap.add_argument("--config", type=int, default=4, choices=(2, 4, 5),
                     help="2: layer-sized skinny matmuls (own JSON line); 4: the 64-layer verify pass at K+1=5 "
                          "(default); 5: the same stack verifying a 16-node draft tree (M=16)")
+    ap.add_argument("--probe", default=None, choices=("consumer", "tcgen05"),
+                    help="instead of the pass: build and run a design microbenchmark from probes/ (prints its table)")
+    ap.add_argument("--probe-args", default="400", help="arguments of the probe program (consumer: iterations [filter])")
     ap.add_argument("--case", default=None, choices=CASES,
                     help="instead of the pass: run one kernel on one layer-sized case --steps times, for profiling")
     args = ap.parse_args()
@@ -844,6 +867,9 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             reference_arm(args, spec, M)
+        return
+    if args.probe:
+        run_probe(args.probe, args.probe_args.split())
         return
     if args.case:
         case_bench(args, local)
