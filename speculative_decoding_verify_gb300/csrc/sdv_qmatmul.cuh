@@ -1307,6 +1307,13 @@ __device__ inline bool pre_issue_staging(const QmmArgs &a, const Smem &sm, uint3
     return true;
 }
 
+// The CTA's last piece of a phase, when it is a whole tile finished here (one split, one piece) and no
+// statistics are formed inline: its epilogue runs on the consumer warps, a position each, instead of
+// waiting in the finishers' queue; the sums over the consumer warps are added in the same order.
+__device__ __forceinline__ bool last_by_consumers(const QmmArgs &a, const QPiece &pc) {
+    return pc.last && a.KS == 1 && pc.np == 1 && !(a.head && !a.defer_stats);
+}
+
 // ---------------------------------------------------------------------------
 // consumers: one matmul phase.  `it` counts ring stages, `pk` pieces (their
 // partial-sum slots and queue entries), `act_it` activation stagings and
@@ -1476,6 +1483,29 @@ __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.rfull[b]);
         if (tr) c_hand += clock64() - c0;
+        if (last_by_consumers(a, pc)) {
+            // the CTA's last tile: every consumer warp's partial sums, then a position per warp
+            if (!warp_wait(&sm.rfull[b], use & 1u, cs, a.status)) return false;
+            const int up = phys_unit(a, pc.u);
+            const float *rb0 = sm.red + static_cast<size_t>(b) * NCW * M * rows_p;
+            const size_t wstride = static_cast<size_t>(M) * rows_p;
+            for (int m = warp; m < M; m += NCW) {
+                float v = rb0[m * rows_p + lane], vu = PAIR ? rb0[m * rows_p + 32 + lane] : 0.0f;
+#pragma unroll
+                for (int w2 = 1; w2 < NCW; ++w2) {
+                    v = __fadd_rn(v, rb0[w2 * wstride + m * rows_p + lane]);
+                    if (PAIR) vu = __fadd_rn(vu, rb0[w2 * wstride + m * rows_p + 32 + lane]);
+                }
+                float res = 0.0f, nw = 0.0f;
+                if (!PAIR) {
+                    const int64_t n = static_cast<int64_t>(up) * 32 + lane;
+                    const bool nok = n < a.n_out;
+                    res = (a.residual && nok) ? __ldcg(a.residual + m * a.n_out + n) : 0.0f;
+                    if (a.norm_next && nok) nw = __ldg(a.norm_next + n);
+                }
+                epilogue<PAIR, is_kq(QT)>(a, up, m, lane, v, vu, res, nw);
+            }
+        }
         if (pc.last) break;
     }
     if (lane == 0) mbar_arrive(sm.act_free);  // done with this phase's last split
@@ -1558,6 +1588,11 @@ __device__ inline bool finish_phase(const QmmArgs &a, const Smem &sm, uint32_t &
         ++pk;
         if (!warp_wait(&sm.rfull[b], use & 1u, cs, a.status)) return false;
         const QPiece pc = cs.pq[slot];
+        if (last_by_consumers(a, pc)) {  // the consumers finish this tile
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.rempty[b]);
+            break;
+        }
         const int s = pc.s, u = pc.u;
         const bool direct = (a.KS == 1) && (pc.np == 1);
         // values the epilogue needs, in flight while the partial sums are added
