@@ -88,7 +88,7 @@ struct AtLayout {
     static constexpr int RING = AT_NST * STAGE;
     static constexpr int BARS = RING;                     // full[AT_NST], empty[AT_NST], abort flag
     static constexpr int TOTAL = 1024 + RING + 16 * AT_NST + 16;  // + room to align the ring to 1024 B
-    static_assert(AT_CW * AT_TQ * (D + 2) * 4 <= RING, "the warps' states fit in the ring");
+    static_assert((AT_CW + 1) * AT_TQ * (D + 2) * 4 <= RING, "the warps' states and the chunk's partial fit in the ring");
 };
 
 // byte offset, inside a stage's K or V tiles, of the 16-byte chunk holding halves d .. d+7 of row r
@@ -105,6 +105,24 @@ __device__ __forceinline__ void tma_3d(void *dst, const CUtensorMap *tm, int x, 
         "[%5];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
         : "memory");
+}
+
+// thread-block cluster: a barrier of every thread of every CTA (release / acquire), this CTA's rank,
+// and an fp32 load from the same shared-memory offset in CTA `rank` of the cluster
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t local_addr, int rank) {
+    uint32_t remote;
+    float v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
@@ -137,7 +155,10 @@ __device__ __forceinline__ void split_h2(float x0, float x1, uint32_t &hi, uint3
     lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
-template <int D>
+// CL > 0: the grid's CL chunks of each (query group, KV head) form one thread-block cluster, and the
+// chunks are merged through distributed shared memory at the end (no partials in global memory, no
+// combine launch); CL = 0: partials for attn_combine_kernel.
+template <int D, int CL>
 __global__ void __launch_bounds__(32 * (AT_CW + 1)) attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmk,
                                                                    const __grid_constant__ CUtensorMap tmv) {
     using LY = AtLayout<D>;
@@ -339,6 +360,9 @@ __global__ void __launch_bounds__(32 * (AT_CW + 1)) attn_tc_kernel(const AttnArg
     }
     __syncthreads();
     const int64_t base = ((static_cast<int64_t>(kh) * a.QG + qg) * a.S + sc) * AT_TQ;
+    // the chunk's partial (max, sum, output) per row: to global memory, or (clusters) to shared memory
+    // after the warps' states
+    float *cm = sm_o + AT_CW * AT_TQ * D, *cl = cm + AT_TQ, *co = cl + AT_TQ;
     for (int idx = threadIdx.x; idx < AT_TQ * D; idx += blockDim.x) {
         const int t = idx / D, d = idx % D;
         float mx = sm_m[t];
@@ -351,11 +375,45 @@ __global__ void __launch_bounds__(32 * (AT_CW + 1)) attn_tc_kernel(const AttnArg
             ov = fmaf(sm_o[(static_cast<size_t>(w) * AT_TQ + t) * D + d], f, ov);
             lv = fmaf(sm_l[w * AT_TQ + t], f, lv);
         }
-        a.part_o[(base + t) * D + d] = ov * (1.0f / AT_PS);
-        if (d == 0) {
-            a.part_ml[(base + t) * 2] = mx;
-            a.part_ml[(base + t) * 2 + 1] = lv;
+        if constexpr (CL > 0) {
+            co[t * D + d] = ov * (1.0f / AT_PS);
+            if (d == 0) {
+                cm[t] = mx;
+                cl[t] = lv;
+            }
+        } else {
+            a.part_o[(base + t) * D + d] = ov * (1.0f / AT_PS);
+            if (d == 0) {
+                a.part_ml[(base + t) * 2] = mx;
+                a.part_ml[(base + t) * 2 + 1] = lv;
+            }
         }
+    }
+    if constexpr (CL > 0) {
+        // every chunk's partial is in its CTA's shared memory; CTA r of the cluster merges columns
+        // [r D / CL, (r + 1) D / CL) of every row, reading the CL partials in chunk order
+        cluster_sync();
+        constexpr int DC = D / CL;
+        const uint32_t rank = cluster_rank();
+        for (int idx = threadIdx.x; idx < AT_TQ * DC; idx += blockDim.x) {
+            const int t = idx / DC, d = static_cast<int>(rank) * DC + idx % DC;
+            const int tg = qg * AT_TQ + t;
+            if (tg >= rows) continue;
+            const uint32_t mt = smem_u32(cm + t), lt = smem_u32(cl + t), ot = smem_u32(co + t * D + d);
+            float mx = AT_NEG;
+#pragma unroll
+            for (int r = 0; r < CL; ++r) mx = fmaxf(mx, ld_cluster_f32(mt, r));
+            float lv = 0.0f, ov = 0.0f;
+#pragma unroll
+            for (int r = 0; r < CL; ++r) {
+                const float f = exp2f(ld_cluster_f32(mt, r) - mx);
+                lv = fmaf(ld_cluster_f32(lt, r), f, lv);
+                ov = fmaf(ld_cluster_f32(ot, r), f, ov);
+            }
+            const int i = tg / a.g, h = kh * a.g + tg % a.g;
+            a.out[(static_cast<int64_t>(i) * a.H + h) * D + d] = ov / lv;
+        }
+        cluster_sync();  // no CTA leaves while another still reads its shared memory
     }
 }
 
@@ -472,8 +530,11 @@ __global__ void __launch_bounds__(128) kv_commit_kernel(__half *kc, __half *vc, 
     }
 }
 
+constexpr int AT_CL = 8;                 // chunks per cluster when the chunks merge on chip
+constexpr int64_t AT_CL_MAX_KEYS = 16384;  // ... for contexts of at most this many keys
+
 struct AttnPlan {
-    int32_t QG, S;
+    int32_t QG, S, CL;  // CL: 0, or S = CL chunks per (query group, KV head) merged in a cluster
     int64_t chunk_pairs;
     size_t off_o, total;
 };
@@ -494,6 +555,15 @@ static bool attn_plan(int32_t M, int32_t H, int32_t H_kv, int32_t D, int64_t L, 
     if (cp < AT_MIN_CHUNK_PAIRS) cp = AT_MIN_CHUNK_PAIRS;
     p.chunk_pairs = cp;
     p.S = static_cast<int32_t>((NP + cp - 1) / cp);  // <= want, whatever the context
+    // short contexts: AT_CL chunks of at least two stages each, merged in one cluster per (query group,
+    // KV head) when those clusters fit in one wave: no partials, no combine launch
+    p.CL = 0;
+    const int64_t NKeys = L + M;
+    if (NKeys <= AT_CL_MAX_KEYS && NKeys >= 2 * AT_KT * AT_CL && per * AT_CL <= 3 * static_cast<int64_t>(sms)) {
+        p.CL = AT_CL;
+        p.S = AT_CL;
+        p.chunk_pairs = ((NP + AT_CL - 1) / AT_CL + AT_KT / 2 - 1) / (AT_KT / 2) * (AT_KT / 2);
+    }
     // partials sized for `want` chunks, so one workspace serves every context length
     const size_t nrow = static_cast<size_t>(H_kv) * p.QG * static_cast<size_t>(want) * AT_TQ;
     p.off_o = (nrow * 2 * sizeof(float) + 255) & ~static_cast<size_t>(255);
@@ -529,6 +599,29 @@ bool cache_map(CUtensorMap *tm, const void *base, int D, int64_t NK, int64_t S_m
     return enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// One launch in clusters of AT_CL CTAs along x (with programmatic dependent launch when enabled).
+template <typename K>
+cudaError_t attn_cluster_launch(K kernel, dim3 grid, size_t smem, cudaStream_t s, const AttnArgs &a,
+                                const CUtensorMap &tmk, const CUtensorMap &tmv) {
+    cudaError_t e = allow_max_dynamic_smem(kernel);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(32 * (AT_CW + 1));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = AT_CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a, tmk, tmv);
 }
 
 }  // namespace sdv
@@ -601,15 +694,18 @@ sd_status sd_attn_decode(const float *q, const void *k_cache, const void *v_cach
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const dim3 grid(p.S, p.QG, H_kv);
     cudaError_t e;
-    if (D == 128) {
-        e = allow_max_dynamic_smem(attn_tc_kernel<128>);
+    if (p.CL) {
+        e = D == 128 ? attn_cluster_launch(attn_tc_kernel<128, AT_CL>, grid, AtLayout<128>::TOTAL, s, a, tmk, tmv)
+                     : attn_cluster_launch(attn_tc_kernel<64, AT_CL>, grid, AtLayout<64>::TOTAL, s, a, tmk, tmv);
+    } else if (D == 128) {
+        e = allow_max_dynamic_smem(attn_tc_kernel<128, 0>);
         if (e == cudaSuccess)
-            e = launch(attn_tc_kernel<128>, grid, dim3(32 * (AT_CW + 1)), AtLayout<128>::TOTAL, s, a, tmk, tmv);
+            e = launch(attn_tc_kernel<128, 0>, grid, dim3(32 * (AT_CW + 1)), AtLayout<128>::TOTAL, s, a, tmk, tmv);
         if (e == cudaSuccess) e = launch(attn_combine_kernel<128>, dim3(p.QG, H_kv), dim3(32 * AT_TQ), 0, s, a);
     } else {
-        e = allow_max_dynamic_smem(attn_tc_kernel<64>);
+        e = allow_max_dynamic_smem(attn_tc_kernel<64, 0>);
         if (e == cudaSuccess)
-            e = launch(attn_tc_kernel<64>, grid, dim3(32 * (AT_CW + 1)), AtLayout<64>::TOTAL, s, a, tmk, tmv);
+            e = launch(attn_tc_kernel<64, 0>, grid, dim3(32 * (AT_CW + 1)), AtLayout<64>::TOTAL, s, a, tmk, tmv);
         if (e == cudaSuccess) e = launch(attn_combine_kernel<64>, dim3(p.QG, H_kv), dim3(32 * AT_TQ), 0, s, a);
     }
     return e == cudaSuccess ? SD_OK : SD_ECUDA;

@@ -93,6 +93,11 @@ CASES = [
     (3, 3, 128, 0, 5, True),         # no committed context
     (1, 16, 128, 5000, 16, False),   # 16 positions x 16 heads of a group: two query groups
     (8, 8, 128, 63, 1, False),       # one position
+    # contexts of 1024..16384 keys: the chunks of a (query group, KV head) merged in one cluster
+    (40, 40, 128, 4096, 5, False),   # the 27B-shaped layer at a short context
+    (2, 6, 64, 2000, 4, True),       # D = 64, tree
+    (4, 4, 128, 1019, 5, False),     # 1024 keys: the smallest clustered context
+    (2, 2, 128, 16379, 5, True),     # 16384 keys: the largest
 ]
 
 
