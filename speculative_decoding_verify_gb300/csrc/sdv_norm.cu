@@ -4,14 +4,16 @@
 
 namespace sdv {
 
-// One CTA of 256 threads per row.  Sum of squares: per 32-element block a
+// One CTA of 1024 threads per row.  Sum of squares: per 32-element block a
 // pairwise tree over the block's squares (strides 16..1), then a pairwise tree
 // over the block sums zero-padded to a power of two (at least 256 slots);
 // inv = 1/sqrt(s/K + eps) correctly rounded.  Each warp requantises 32-element
 // blocks of t = x*w and scales them by inv: the requantisation of y = x*inv*w.  The matmul epilogues form the same block sums
 // where they finish a block of the residual stream, so the verify pass reaches
 // identical bits.
-__global__ void __launch_bounds__(256) rmsnorm_quant_kernel(const float *__restrict__ x, int64_t ldx,
+constexpr int NORM_WARPS = 32;
+
+__global__ void __launch_bounds__(NORM_WARPS * 32) rmsnorm_quant_kernel(const float *__restrict__ x, int64_t ldx,
                                                             const float *__restrict__ w, float eps, int64_t K,
                                                             int8_t *__restrict__ q, float *__restrict__ sc) {
     __shared__ float slots[NORM_MAX_KB];
@@ -22,26 +24,37 @@ __global__ void __launch_bounds__(256) rmsnorm_quant_kernel(const float *__restr
     const int m = blockIdx.x;
     const float *xr = x + static_cast<int64_t>(m) * ldx;
     const int KB = static_cast<int>(K / 32);
+    constexpr int UNR = 8;  // blocks a warp loads together: their loads are in flight at once
     float inv = 1.0f;
     if (w) {
         int P = 256;
         while (P < KB) P <<= 1;
-        for (int b = warp; b < P; b += 8) {
-            float t = 0.0f;
-            if (b < KB) {
-                const float v = xr[static_cast<int64_t>(b) * 32 + lane];
-                t = __fmul_rn(v, v);
+        for (int b0 = warp; b0 < P; b0 += NORM_WARPS * UNR) {
+            float v[UNR];
 #pragma unroll
-                for (int s = 16; s >= 1; s >>= 1) {
-                    const float o = __shfl_down_sync(0xffffffffu, t, s);
-                    if (lane < s) t = __fadd_rn(t, o);
-                }
+            for (int u = 0; u < UNR; ++u) {
+                const int b = b0 + NORM_WARPS * u;
+                v[u] = b < KB ? xr[static_cast<int64_t>(b) * 32 + lane] : 0.0f;
             }
-            if (lane == 0) slots[b] = t;
+#pragma unroll
+            for (int u = 0; u < UNR; ++u) {
+                const int b = b0 + NORM_WARPS * u;
+                if (b >= P) break;
+                float t = 0.0f;
+                if (b < KB) {
+                    t = __fmul_rn(v[u], v[u]);
+#pragma unroll
+                    for (int s = 16; s >= 1; s >>= 1) {
+                        const float o = __shfl_down_sync(0xffffffffu, t, s);
+                        if (lane < s) t = __fadd_rn(t, o);
+                    }
+                }
+                if (lane == 0) slots[b] = t;
+            }
         }
         __syncthreads();
         for (int st = P / 2; st >= 1; st >>= 1) {
-            for (int j = tid; j < st; j += 256) slots[j] = __fadd_rn(slots[j], slots[j + st]);
+            for (int j = tid; j < st; j += NORM_WARPS * 32) slots[j] = __fadd_rn(slots[j], slots[j + st]);
             __syncthreads();
         }
         if (tid == 0) {
@@ -52,13 +65,23 @@ __global__ void __launch_bounds__(256) rmsnorm_quant_kernel(const float *__restr
         inv = s_inv;
     }
     // codes from t = x * w (the row factor inv cancels in t / (max|t| / 127)); scale inv * max|t| / 127
-    for (int64_t b = warp; b < KB; b += 8) {
-        float t = xr[b * 32 + lane];
-        if (w) t = __fmul_rn(t, w[b * 32 + lane]);
-        float c;
-        const int v = requant_lane(t, c);
-        q[static_cast<int64_t>(m) * K + b * 32 + lane] = static_cast<int8_t>(v);
-        if (lane == 0) sc[static_cast<int64_t>(m) * KB + b] = w ? __fmul_rn(inv, c) : c;
+    for (int64_t b0 = warp; b0 < KB; b0 += NORM_WARPS * UNR) {
+        float t[UNR];
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) {
+            const int64_t b = b0 + NORM_WARPS * u;
+            t[u] = b < KB ? xr[b * 32 + lane] : 0.0f;
+            if (w && b < KB) t[u] = __fmul_rn(t[u], w[b * 32 + lane]);
+        }
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) {
+            const int64_t b = b0 + NORM_WARPS * u;
+            if (b >= KB) break;
+            float c;
+            const int v = requant_lane(t[u], c);
+            q[static_cast<int64_t>(m) * K + b * 32 + lane] = static_cast<int8_t>(v);
+            if (lane == 0) sc[static_cast<int64_t>(m) * KB + b] = w ? __fmul_rn(inv, c) : c;
+        }
     }
 }
 
@@ -114,7 +137,7 @@ sd_status sd_rmsnorm_quant_acts(const float *x, int64_t ldx, const float *norm_w
     if (!x || !q || !scales || M < 1 || M > 65535 || K <= 0 || K % 32 || ldx < K) return SD_EINVAL;
     if (norm_w && K / 32 > NORM_MAX_KB) return SD_EUNSUPPORTED;
     if (!aligned(x, 4) || !aligned(q, 16)) return SD_EINVAL;
-    return launched(launch(rmsnorm_quant_kernel, dim3(M), dim3(256), 0, cs(stream), x, ldx, norm_w, eps, K, q,
+    return launched(launch(rmsnorm_quant_kernel, dim3(M), dim3(NORM_WARPS * 32), 0, cs(stream), x, ldx, norm_w, eps, K, q,
                            scales));
 }
 
