@@ -589,6 +589,8 @@ def kquant_bench(args, local):
     e2e_ms = (time.perf_counter() - t1) / n_e2e * 1e3
     peak, peak_kind = measured_peaks()
     gbs = wbytes / (ms * 1e-3) / 1e9
+    if args.trace:
+        write_trace(args.trace, stack, h_dev, sdv)
     del stack, gr, layers
     torch.cuda.empty_cache()
     # CPU baseline: the oracle's K-quant matmuls over a bounded sample of the stack's layers

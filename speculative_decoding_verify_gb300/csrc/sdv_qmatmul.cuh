@@ -442,10 +442,11 @@ __device__ __forceinline__ void q6_frag(uint4 lo, uint2 hi, uint32_t (&a)[2][2][
 }
 
 // unsigned byte e of x as an exact float (the byte in the mantissa of 2^23)
-__device__ __forceinline__ float ubyte_f(uint32_t x, int e) {
-    return __int_as_float(static_cast<int>(__byte_perm(x, 0x4B000000u, 0x7440u | static_cast<uint32_t>(e)))) -
-           8388608.0f;
+// 2^23 + byte e of x, exactly (the byte as the low mantissa bits of 2^23)
+__device__ __forceinline__ float ubyte_magic(uint32_t x, int e) {
+    return __int_as_float(static_cast<int>(__byte_perm(x, 0x4B000000u, 0x7440u | static_cast<uint32_t>(e))));
 }
+__device__ __forceinline__ float ubyte_f(uint32_t x, int e) { return ubyte_magic(x, e) - 8388608.0f; }
 
 // the two row tiles' exact dots of one record against one 8-position tile:
 // d[t][i] = dot(row 16t + g + 8(i>>1), position 2c + (i&1))
@@ -1215,8 +1216,12 @@ __device__ __forceinline__ void stage_compute_kq(const uint8_t *sbase, int n, in
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float2 dm = __half22float2(*reinterpret_cast<const __half2 *>(&dw[e]));  // d, dmin
-                    f1[e] = __fmul_rn(dm.x, ubyte_f(scm.x, e));  // exact: 11 x 6 bits
-                    f2[e] = __fmul_rn(dm.y, ubyte_f(scm.y, e));
+                    // (scale, min) of row e: each byte under the exponent of 2^23, less 2^23 (exact), as a pair
+                    const float2 sm = fadd2_rn(make_float2(ubyte_magic(scm.x, e), ubyte_magic(scm.y, e)),
+                                               make_float2(-8388608.0f, -8388608.0f));
+                    const float2 pr = fmul2_rn(dm, sm);  // exact: 11 x 6 bits
+                    f1[e] = pr.x;
+                    f2[e] = pr.y;
                 }
             } else {
                 q6_frag(*reinterpret_cast<const uint4 *>(srp + warp * 768 + lane * 16),
@@ -1230,9 +1235,12 @@ __device__ __forceinline__ void stage_compute_kq(const uint8_t *sbase, int n, in
                 dq[2] = d23.x;
                 dq[3] = d23.y;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    f1[e] = ubyte_f(scb.x ^ 0x80808080u, e) - 128.0f;  // int8 scales, exact
-                    f2[e] = ubyte_f(scb.y ^ 0x80808080u, e) - 128.0f;
+                for (int e = 0; e < 4; ++e) {  // int8 scales: the biased byte less 2^23 + 128, exact
+                    const float2 sc = fadd2_rn(make_float2(ubyte_magic(scb.x ^ 0x80808080u, e),
+                                                           ubyte_magic(scb.y ^ 0x80808080u, e)),
+                                               make_float2(-8388736.0f, -8388736.0f));
+                    f1[e] = sc.x;
+                    f2[e] = sc.y;
                 }
             }
 #pragma unroll
