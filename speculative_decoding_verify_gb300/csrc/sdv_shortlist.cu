@@ -39,7 +39,6 @@ constexpr int SL_CTAS_PER_SM = 4;
 struct SlBest {
     float v;      // best logit (-inf: none)
     int32_t idx;  // its row (-1: none)
-    int32_t cnt;  // unused
 };
 
 constexpr uint32_t SL_REPROBE = 16;  // full-mode calls try the shortlist again every 16 calls
@@ -359,7 +358,7 @@ __global__ void __launch_bounds__(SL_THREADS, SL_CTAS_PER_SM) shortlist_argmax_k
         float v = -INFINITY;
         int32_t i = -1;
         for (int w = 0; w < SL_WARPS; ++w) better(v, i, wv[w][threadIdx.x], wi[w][threadIdx.x]);
-        a.best_part[threadIdx.x * a.G + blockIdx.x] = SlBest{v, i, 0};
+        a.best_part[threadIdx.x * a.G + blockIdx.x] = SlBest{v, i};
     }
     if (!last_cta(a.ticket + 1, &is_last)) return;
     const bool full = *reinterpret_cast<const volatile int *>(a.full) != 0;
