@@ -243,10 +243,25 @@ def oracle_sample(spec, M, budget_s=12.0, max_layers=64):
         layers += 1
         if t_total > budget_s:
             break
-    return {"value": nbytes / t_total / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+    cores = oracle.num_threads()
+    # the same oracle on one host core, over layer 0 only
+    wts = {name: spec.weights(0, name) for name, _, _ in spec.matrices()}
+    n1, n2 = spec.norms(0)
+    one = sum(w.nbytes for w in wts.values())
+    oracle.set_num_threads(1)
+    try:
+        t0 = time.time()
+        oracle.stack_layer(spec.hidden_in(M), wts, n1, n2, spec.hidden, spec.ffn, spec.wq)
+        t1 = time.time() - t0
+    finally:
+        oracle.set_num_threads(cores)
+    return {"value": nbytes / t_total / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"{layers} layer(s) of the 64-layer stack at M={M} (all four 4-bit matrices, "
                       f"{nbytes / 1e6:.0f} MB of weights, {nbytes / spec.weight_bytes():.1%} of the pass's bytes; "
-                      f"the Q8_0 head is not in the sample), {t_total:.1f} s"}
+                      f"the Q8_0 head is not in the sample), {t_total:.1f} s",
+            "single_core": {"value": one / t1 / 1e9, "unit": "GB/s", "cores": 1,
+                            "sample": f"layer 0 ({one / 1e6:.0f} MB), {t1:.2f} s; x 64 layers: about "
+                                      f"{t1 * 64:.0f} s per pass without the head (extrapolated)"}}
 
 
 def reference_arm(args, spec, M):

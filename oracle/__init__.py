@@ -83,6 +83,7 @@ def _get():
             lib = ctypes.CDLL(_SO)
             sig = {
                 "oracle_num_threads": ([], _I),
+                "oracle_set_num_threads": ([_I], None),
                 "oracle_f16_to_f32": ([ctypes.c_uint16], _F),
                 "oracle_dequant": ([_I, _P, _I64, _P], None),
                 "oracle_block_dots": ([_I, _P, _I64, _I64, _P, _I, _P], None),
@@ -130,6 +131,11 @@ def _c(a, dtype):
 
 def num_threads() -> int:
     return _get().oracle_num_threads()
+
+
+def set_num_threads(n: int):
+    """Threads of the calls that follow (for timing on one core); results do not depend on it."""
+    _get().oracle_set_num_threads(int(n))
 
 
 def f16_to_f32(bits: int) -> float:

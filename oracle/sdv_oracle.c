@@ -43,6 +43,15 @@ int oracle_num_threads(void) {
 #endif
 }
 
+/* Threads for the following calls (timing on one core); the results do not depend on it. */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* ------------------------------------------------------------------ */
 /* fp16 decode (IEEE 754 binary16 -> binary32, exact)                  */
 /* ------------------------------------------------------------------ */
