@@ -304,7 +304,11 @@ sd_status sd_head_logits(const void *w, int64_t vocab, int64_t hidden, const int
  * L+path[t] moves to row L+t for t < n, in place.  path NULL: a chain, whose
  * first n rows are already in place (nothing is launched).  The cache length
  * becomes L+n.  A count or path out of range records SD_EDEVICE and moves
- * nothing.  D <= 256.
+ * nothing.  D <= 256.  The same call rolls a drafter's own cache back after
+ * verification ("Speculative Decoding with Open-Weights Models", section
+ * "Engineering the Architecture: KV Cache Synchronization"): its rows for the
+ * rejected drafts are dropped and the accepted path is made contiguous, so
+ * both caches continue from length L+n.
  */
 /*
  * Adaptive draft depth, host only ("Inside OpenJet Engine", section "Cheap
