@@ -492,7 +492,7 @@ def write_trace(path, stack, h_dev, sdv):
     t = tr.cpu().numpy()
     G, P = p.grid, p.n_phases
     smid = t[:G].copy()
-    raw = t[G:G + P * G * 9].reshape(P, G, 9)
+    raw = t[G:G + P * G * 12].reshape(P, G, 12)
     st = raw[:, :, :6].astype(np.float64)
     t0 = st[st > 0].min()
     st = np.where(st > 0, st - t0, np.nan)

@@ -530,12 +530,14 @@ sd_status sd_verify_pass(const sd_pass *pass, sd_stream_t stream);
  * sd_verify_pass, plus global-timer stamps (nanoseconds) written into `trace`
  * (device, 8-byte aligned, >= sd_pass_trace_bytes(pass) bytes, caller-owned).
  * Layout, uint64: trace[c] = SM id of CTA c for c < grid; then for phase p and
- * CTA c 9 values at grid + (p * grid + c) * 9.  Global-timer stamps: the phase
+ * CTA c 12 values at grid + (p * grid + c) * 12.  Global-timer stamps: the phase
  * begins (grid barrier passed), the consumers hold their first activations
  * (matmul phases), the consumers leave the phase, the phase ends, and the
  * producer starts and finishes issuing the phase's weight copies (matmul
  * phases).  Then SM cycles one consumer warp spent in the phase waiting for
- * weight stages, computing records, and handing partial sums on.  Values a
+ * weight stages, computing records, handing partial sums on, staging a
+ * split's activations (the wait for their copy and the RMSNorm row factors
+ * included), finishing the CTA's last tile, and in the whole phase.  Values a
  * phase does not reach are left as they were.  Results equal sd_verify_pass's.
  * SD_EINVAL for a null, misaligned or short buffer. */
 size_t sd_pass_trace_bytes(const sd_pass *pass);

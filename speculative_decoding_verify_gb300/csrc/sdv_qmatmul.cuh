@@ -191,10 +191,12 @@ constexpr int KIND_MATMUL = 0, KIND_NORM = 1, KIND_ACCEPT = 2, KIND_COMBINE = 3,
 // (phase, CTA).  Global-timer nanoseconds: the phase begins (grid barrier passed), the consumers hold
 // their first activations, the consumers leave the phase, the phase ends (every role done), and the
 // producer starts and finishes issuing the phase's weight copies.  SM cycles spent by consumer warp 0
-// in the phase: waiting for weight stages, computing records, and handing partial sums to the
-// finishers (waiting for a free slot included).
+// in the phase: waiting for weight stages, computing records, handing partial sums to the finishers
+// (waiting for a free slot included), staging a split's activations (waiting for their copy, the
+// RMSNorm row factors and their scales), the CTA's last tile epilogue, and the whole phase.
 constexpr int TR_START = 0, TR_ACT = 1, TR_CONS_END = 2, TR_END = 3, TR_PROD_FIRST = 4, TR_PROD_LAST = 5,
-              TR_CYC_WAIT = 6, TR_CYC_COMP = 7, TR_CYC_HAND = 8, TR_SLOTS = 9;
+              TR_CYC_WAIT = 6, TR_CYC_COMP = 7, TR_CYC_HAND = 8, TR_CYC_STAGE = 9, TR_CYC_LAST = 10,
+              TR_CYC_ALL = 11, TR_SLOTS = 12;
 
 // fetch-and-add with release (orders the writes seen through a barrier) and acquire
 __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v) {
@@ -1344,7 +1346,8 @@ __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
     uint32_t stg = it % NS, sph = (it / NS) & 1u;  // ring slot and phase parity of stage `it`
     int cur_s = -1;
     const bool tr = tslot != nullptr && threadIdx.x == 0;  // consumer warp 0 keeps the cycle accounts
-    long long c_wait = 0, c_comp = 0, c_hand = 0, c0 = 0;
+    long long c_wait = 0, c_comp = 0, c_hand = 0, c_stage = 0, c_last = 0, c0 = 0;
+    const long long c_start = tr ? clock64() : 0;
     float2 inv[NT];  // RMSNorm row factors of this lane's positions 8nt + 2c, +1 (1 when not normalised)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) inv[nt] = make_float2(1.0f, 1.0f);
@@ -1360,6 +1363,7 @@ __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
         const int s = pc.s, j0 = pc.j0, j1 = pc.j1;
 
         if (s != cur_s) {
+            if (tr) c0 = clock64();
             const int len = (s == a.KS - 1) ? a.KBlast : a.KBs;
             if (cur_s >= 0 && lane == 0) mbar_arrive(sm.act_free);  // done with the previous split
             if (a.af_frag) {
@@ -1416,6 +1420,7 @@ __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
                 }
             }
             cur_s = s;
+            if (tr) c_stage += clock64() - c0;
         }
 
         float acc[NT][2][4], accu[PAIR ? NT : 1][2][4];
@@ -1493,6 +1498,7 @@ __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
         if (tr) c_hand += clock64() - c0;
         if (last_by_consumers(a, pc)) {
             // the CTA's last tile: every consumer warp's partial sums, then a position per warp
+            if (tr) c0 = clock64();
             if (!warp_wait(&sm.rfull[b], use & 1u, cs, a.status)) return false;
             const int up = phys_unit(a, pc.u);
             const float *rb0 = sm.red + static_cast<size_t>(b) * NCW * M * rows_p;
@@ -1513,6 +1519,7 @@ __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
                 }
                 epilogue<PAIR, is_kq(QT)>(a, up, m, lane, v, vu, res, nw);
             }
+            if (tr) c_last += clock64() - c0;
         }
         if (pc.last) break;
     }
@@ -1522,6 +1529,9 @@ __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
         tslot[TR_CYC_WAIT] = static_cast<uint64_t>(c_wait);
         tslot[TR_CYC_COMP] = static_cast<uint64_t>(c_comp);
         tslot[TR_CYC_HAND] = static_cast<uint64_t>(c_hand);
+        tslot[TR_CYC_STAGE] = static_cast<uint64_t>(c_stage);
+        tslot[TR_CYC_LAST] = static_cast<uint64_t>(c_last);
+        tslot[TR_CYC_ALL] = static_cast<uint64_t>(clock64() - c_start);
     }
     return !cs.abort;
 }
