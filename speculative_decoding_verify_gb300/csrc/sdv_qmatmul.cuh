@@ -939,7 +939,7 @@ __device__ inline void produce_phase(const QmmArgs &a, const Smem &sm, uint32_t 
             const int n = j1 - jj < a.SB ? j1 - jj : a.SB;
             const int stg = static_cast<int>(it % a.NS);
             const uint32_t ph = (it / a.NS) & 1u;
-            if (out_of_time(cs, a.status, 1)) {
+            if ((it & 7u) == 0 && out_of_time(cs, a.status, 1)) {  // every 8th stage
                 cs.abort = 1;
                 break;
             }
@@ -1351,10 +1351,10 @@ __device__ inline bool consume_phase(const QmmArgs &a, const Smem &sm, uint32_t 
     float2 inv[NT];  // RMSNorm row factors of this lane's positions 8nt + 2c, +1 (1 when not normalised)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) inv[nt] = make_float2(1.0f, 1.0f);
+    // launch-wide self-check, once per phase (a clock read per piece measured 0.45 % of the pass); every
+    // wait below is bounded on its own
+    if (out_of_time(cs, a.status, 2)) cs.abort = 1;
     for (;;) {
-        if (out_of_time(cs, a.status, 2)) {  // launch-wide self-check (uniform per warp: lane values may differ)
-            cs.abort = 1;
-        }
         // the next piece's descriptor rides with its first stage
         if (tr) c0 = clock64();
         if (!warp_wait(&sm.full[stg], sph, cs, a.status)) return false;
