@@ -126,13 +126,15 @@ __device__ __forceinline__ uint64_t gtimer_ns() {
 // records SD_ETIMEOUT and unwinds).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
                                                   const volatile int *abort = nullptr) {
+    // the global timer is read only once a wait has lasted 64 polls (then every 64): short waits, the
+    // common case, never pay for the read; the bound counts from the first read
     uint64_t t0 = 0;
-    for (uint32_t k = 0;; ++k) {
+    for (uint32_t k = 1;; ++k) {
         if (mbar_try_wait(bar, parity)) return true;
         if (abort && *abort) return false;
         if ((k & 63u) == 0) {
-            uint64_t now = gtimer_ns();
-            if (k == 0) t0 = now;
+            const uint64_t now = gtimer_ns();
+            if (k == 64) t0 = now;
             else if (now - t0 > limit_ns) return false;
         }
     }
