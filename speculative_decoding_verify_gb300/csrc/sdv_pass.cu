@@ -18,6 +18,14 @@ struct PassHeader {
     uint32_t pad[63];
 };
 
+// The plan: the header, the phase table (5 phases per layer, 4 more), then the combine phases' table of
+// pieces per (unit, split) (up to PASS_NP_TAB_BYTES entries; a larger shape works them out on the GPU).
+constexpr size_t PASS_NP_TAB_BYTES = 16384;
+inline size_t pass_np_tab_offset(int n_layers) {
+    const size_t end = sizeof(PassHeader) + static_cast<size_t>(5 * n_layers + 4) * sizeof(QmmArgs);
+    return (end + 255) / 256 * 256;
+}
+
 static cudaError_t pass_launch(const QmmArgs *phases, int n_phases, uint32_t *ctr, uint64_t *trace, int nt,
                                int sample, int kq, size_t smem, int grid, cudaStream_t s) {
     if (kq) return pass_launch_kq(phases, n_phases, ctr, trace, nt, smem, grid, s);
@@ -83,7 +91,7 @@ extern "C" {
 
 size_t sd_pass_plan_bytes(int32_t n_layers) {
     if (n_layers < 0) return 0;
-    return sizeof(PassHeader) + static_cast<size_t>(5 * n_layers + 4) * sizeof(QmmArgs);
+    return pass_np_tab_offset(n_layers) + PASS_NP_TAB_BYTES;
 }
 
 size_t sd_pass_workspace_bytes(int64_t hidden, int64_t ffn, int64_t vocab, int32_t wq) {
@@ -316,6 +324,34 @@ sd_status sd_pass_prepare(const sd_pass_desc *d, void *plan, size_t plan_bytes, 
     if (static_cast<size_t>(lay.NS) * slot < sizeof(SampleShared) || static_cast<size_t>(lay.NS) * slot < sizeof(TopkShared))
         return SD_EUNSUPPORTED;  // the sampler's state
     for (QmmArgs &a : ph) apply_layout(a, lay, slot);
+    // pieces per (unit, split) of the combine phases, from the host's replay of their schedule: every
+    // combine phase of a pass has the same shape, so one table serves all whose schedule matches the first
+    std::vector<uint8_t> np_tab;
+    const QmmArgs *c0 = nullptr;
+    uint8_t *np_dev = static_cast<uint8_t *>(plan) + pass_np_tab_offset(L);
+    for (QmmArgs &a : ph) {
+        if (a.kind != KIND_COMBINE) continue;
+        if (!c0) {
+            c0 = &a;
+            const size_t n = static_cast<size_t>(a.NU) * np_tab_stride(a.KS);
+            if (n > PASS_NP_TAB_BYTES || a.P > 255) break;  // too large: the GPU works them out
+            np_tab.assign(n, 0);
+            for (int u = 0; u < a.NU; ++u)
+                for (int s = 0; s < a.KS; ++s) {
+                    int first = 0, np = 0;
+                    unit_split_owners(a, s, u, first, np);
+                    if (np < 0 || np > a.P) return SD_EINVAL;
+                    np_tab[static_cast<size_t>(u) * np_tab_stride(a.KS) + s] = static_cast<uint8_t>(np);
+                }
+        }
+        const bool same = a.NU == c0->NU && a.KS == c0->KS && a.KB == c0->KB && a.KBs == c0->KBs &&
+                          a.KBlast == c0->KBlast && a.W == c0->W && a.G == c0->G && a.P == c0->P && a.D == c0->D &&
+                          a.R == c0->R && a.GRS == c0->GRS;
+        a.np_tab = same ? np_dev : nullptr;
+    }
+    if (!np_tab.empty() &&
+        cudaMemcpy(np_dev, np_tab.data(), np_tab.size(), cudaMemcpyHostToDevice) != cudaSuccess)
+        return SD_ECUDA;
     PassHeader hdr = {};
     if (cudaMemcpy(plan, &hdr, sizeof(hdr), cudaMemcpyHostToDevice) != cudaSuccess) return SD_ECUDA;
     if (cudaMemcpy(static_cast<uint8_t *>(plan) + sizeof(PassHeader), ph.data(), ph.size() * sizeof(QmmArgs),

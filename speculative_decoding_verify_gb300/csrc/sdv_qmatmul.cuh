@@ -183,7 +183,13 @@ struct QmmArgs {
     // single-operation calls whose work a previous launch decides (read after griddepcontrol.wait):
     const uint32_t *unit_mask;  // bit per row tile: only set tiles are computed (null: all)
     const int *skip_if;         // non-zero: the call does nothing (null: always runs)
+    // combine phases: pieces of each (unit, split), [NU][np_tab_stride(KS)] bytes from the host's replay of
+    // the schedule (null: worked out here; the walk's divisions cost microseconds after a grid barrier)
+    const uint8_t *np_tab;
 };
+
+// row stride of np_tab: whole 32-bit words, so up to four splits come in one load
+__host__ __device__ __forceinline__ int np_tab_stride(int KS) { return (KS + 3) & ~3; }
 
 constexpr int KIND_MATMUL = 0, KIND_NORM = 1, KIND_ACCEPT = 2, KIND_COMBINE = 3, KIND_HSTATS = 4;
 
@@ -215,14 +221,23 @@ __host__ __device__ __forceinline__ int phys_unit(const QmmArgs &a, int u) {
     return (r == 0 ? 2 : r - 1) * a.ilv3 + q;
 }
 
+// n / d for n >= 0 and d > 0, as a 32-bit division whenever both fit in 32 bits (every schedule
+// quantity of a layer-sized matmul does): a 64-bit division is a long instruction sequence on the GPU,
+// and the schedule walks sit on the path from a grid barrier to a phase's first copy
+__host__ __device__ __forceinline__ int64_t udiv(int64_t n, int64_t d) {
+    return ((static_cast<uint64_t>(n) | static_cast<uint64_t>(d)) >> 32) == 0
+               ? static_cast<int64_t>(static_cast<uint32_t>(n) / static_cast<uint32_t>(d))
+               : n / d;
+}
+
 __host__ __device__ __forceinline__ void decode_step(const QmmArgs &a, int64_t g, int &s, int &u, int &j, int &len) {
     int64_t per = static_cast<int64_t>(a.NU) * a.KBs;
-    int64_t ss = g / per;
+    int64_t ss = udiv(g, per);
     if (ss > a.KS - 1) ss = a.KS - 1;
     s = static_cast<int>(ss);
     int64_t rem = g - per * ss;
     len = (s == a.KS - 1) ? a.KBlast : a.KBs;
-    u = static_cast<int>(rem / len);
+    u = static_cast<int>(udiv(rem, len));
     j = static_cast<int>(rem - static_cast<int64_t>(u) * len);
 }
 
@@ -238,7 +253,7 @@ __host__ __device__ __forceinline__ int64_t seq_len(const QmmArgs &a) { return a
 // wseq / GR granules in all), so the owner is the largest c with floor(c wq / G) <= floor(x / GR)
 __host__ __device__ __forceinline__ int seq_owner(const QmmArgs &a, int64_t wseq, int64_t x) {
     const int64_t wq = wseq >> a.GRS;
-    return wq > 0 ? static_cast<int>((((x >> a.GRS) + 1) * a.G - 1) / wq) : 0;
+    return wq > 0 ? static_cast<int>(udiv(((x >> a.GRS) + 1) * a.G - 1, wq)) : 0;
 }
 
 // CTAs sharing split s of unit u, and the first of them
@@ -281,8 +296,8 @@ __host__ __device__ __forceinline__ void pieces_begin_cta(const QmmArgs &a, Piec
         it.d_next = it.d_end = 0;
         return;
     }
-    it.g = (c * wq / a.G) << a.GRS;
-    it.hi = ((c + 1) * wq / a.G) << a.GRS;
+    it.g = udiv(c * wq, a.G) << a.GRS;
+    it.hi = udiv((c + 1) * wq, a.G) << a.GRS;
     it.d_next = a.D > 0 ? a.R + static_cast<int>(c) * a.D : 0;
     it.d_end = a.D > 0 ? it.d_next + a.D : 0;
 }
@@ -310,7 +325,7 @@ __host__ __device__ __forceinline__ bool pieces_next(const QmmArgs &a, PieceIter
         if (a.D > 0) {
             p.s = 0;
             len = a.KB;
-            p.u = static_cast<int>(it.g / a.KB);
+            p.u = static_cast<int>(udiv(it.g, a.KB));
             p.j0 = static_cast<int>(it.g - static_cast<int64_t>(p.u) * a.KB);
         } else {
             decode_step(a, it.g, p.s, p.u, p.j0, len);
@@ -1299,23 +1314,35 @@ __device__ __forceinline__ void stage_compute_kq(const uint8_t *sbase, int n, in
     }
 }
 
-// Thread 0, right after the grid barrier of a matmul phase whose activations arrive as fragments:
-// start the bulk copy of the CTA's first k-split at once (consume_phase then only waits for it).
-// Returns whether it issued the copy.
-__device__ inline bool pre_issue_staging(const QmmArgs &a, const Smem &sm, uint32_t act_it, CtaShared &cs) {
-    if (a.kind != KIND_MATMUL || !a.af_frag) return false;
+// The k-split of the CTA's first piece in a matmul phase whose activations arrive as fragments, or -1
+// (not such a phase, or no piece here).  A function of the descriptor alone when the call is not
+// restricted, so the one-launch pass walks it while it waits at the grid barrier.
+constexpr int SPLIT_LATER = -2;  // restricted call: its unit mask may only be read after the barrier
+__device__ inline int first_split(const QmmArgs &a) {
+    if (a.kind != KIND_MATMUL || !a.af_frag) return -1;
     PieceIter pit;
     pieces_begin(a, pit);
     Piece pc;
-    if (!pieces_next_on(a, pit, pc)) return false;
+    return pieces_next_on(a, pit, pc) ? pc.s : -1;
+}
+
+// Thread 0, right after the grid barrier of a matmul phase whose activations arrive as fragments:
+// start the bulk copy of the CTA's first k-split s at once (consume_phase then only waits for it).
+// Returns whether it issued the copy.
+__device__ inline bool issue_first_split(const QmmArgs &a, const Smem &sm, uint32_t act_it, CtaShared &cs, int s) {
+    if (s == SPLIT_LATER) s = first_split(a);
+    if (s < 0) return false;
     if (act_it > 0 && !mbar_wait_bounded(sm.act_free, (act_it - 1) & 1u, WAIT_NS, &cs.abort)) {
         set_status(a.status, SD_ETIMEOUT);
         cs.abort = 1;
         return false;
     }
-    stage_issue(a, sm, pc.s, (pc.s == a.KS - 1) ? a.KBlast : a.KBs);
+    stage_issue(a, sm, s, (s == a.KS - 1) ? a.KBlast : a.KBs);
     return true;
 }
+
+// first_split where it may run before the barrier, SPLIT_LATER where it may not
+__device__ __forceinline__ int first_split_early(const QmmArgs &a) { return a.unit_mask ? SPLIT_LATER : first_split(a); }
 
 // The CTA's last piece of a phase, when it is a whole tile finished here (one split, one piece) and no
 // statistics are formed inline: its epilogue runs on the consumer warps, a position each, instead of
@@ -1789,8 +1816,8 @@ __device__ inline void norm_phase(const QmmArgs &a) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int M = a.M, KB = a.KB;
     const int64_t K = static_cast<int64_t>(KB) * 32;
-    const int b0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * KB / gridDim.x);
-    const int b1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * KB / gridDim.x);
+    const int b0 = static_cast<int>(udiv(static_cast<int64_t>(blockIdx.x) * KB, gridDim.x));
+    const int b1 = static_cast<int>(udiv(static_cast<int64_t>(blockIdx.x + 1) * KB, gridDim.x));
     for (int b = b0 + warp; b < b1; b += NCW) {
         for (int m = 0; m < M; ++m) {
             const int64_t i = m * K + static_cast<int64_t>(b) * 32 + lane;
@@ -1814,10 +1841,10 @@ __device__ inline void norm_phase(const QmmArgs &a) {
 template <bool KQ = false>
 __device__ inline void combine_phase(const QmmArgs &a, int widx) {
     constexpr int ROWS = 32, CH = 8, NWW = NCW + NF;
-    constexpr int CKS = 8, CP = 4;  // splits and pieces per split held in registers at once
+    constexpr int CKS = 4, CP = 4;  // splits and pieces per split held in registers at once
     const int lane = threadIdx.x & 31, M = a.M;
-    const int u0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * a.NU / gridDim.x);
-    const int u1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * a.NU / gridDim.x);
+    const int u0 = static_cast<int>(udiv(static_cast<int64_t>(blockIdx.x) * a.NU, gridDim.x));
+    const int u1 = static_cast<int>(udiv(static_cast<int64_t>(blockIdx.x + 1) * a.NU, gridDim.x));
     const int items = (u1 - u0) * M;
     for (int i = widx; i < items; i += NWW) {
         const int u = u0 + i / M, m = i - (i / M) * M, up = phys_unit(a, u);
@@ -1828,20 +1855,27 @@ __device__ inline void combine_phase(const QmmArgs &a, int widx) {
         float v = 0.0f;
         bool first = true;
         if (a.KS <= CKS && a.P <= CP) {  // every partial sum of the unit in one round of loads
+            // every slot the unit has (P per split) is loaded while the pieces per split are worked
+            // out; slots past a split's pieces are never added
             int np[CKS];
             float x[CKS][CP];
-#pragma unroll
-            for (int s2 = 0; s2 < CKS; ++s2) {
-                int f2;
-                np[s2] = 0;
-                if (s2 < a.KS) unit_split_owners(a, s2, u, f2, np[s2]);
-                if (!SD_INB(np[s2] >= 0 && np[s2] <= a.P, a.status, 108)) np[s2] = 0;  // site 108: pieces per split
-            }
+            static_assert(CKS <= 4, "one table word per unit");
+            const uint32_t npw = a.np_tab ? __ldg(reinterpret_cast<const uint32_t *>(a.np_tab) + u) : 0u;
 #pragma unroll
             for (int s2 = 0; s2 < CKS; ++s2) {
                 const float *qs = a.part + (static_cast<int64_t>(u) * a.KS + s2) * a.P * (ROWS * MPAD) + m * ROWS + lane;
 #pragma unroll
-                for (int c = 0; c < CP; ++c) x[s2][c] = c < np[s2] ? __ldcg(qs + c * (ROWS * MPAD)) : 0.0f;
+                for (int c = 0; c < CP; ++c) x[s2][c] = (s2 < a.KS && c < a.P) ? __ldcg(qs + c * (ROWS * MPAD)) : 0.0f;
+            }
+#pragma unroll
+            for (int s2 = 0; s2 < CKS; ++s2) {
+                int f2;
+                np[s2] = 0;
+                if (s2 < a.KS) {
+                    if (a.np_tab) np[s2] = static_cast<int>((npw >> (8 * s2)) & 255u);
+                    else unit_split_owners(a, s2, u, f2, np[s2]);
+                }
+                if (!SD_INB(np[s2] >= 0 && np[s2] <= a.P, a.status, 108)) np[s2] = 0;  // site 108: pieces per split
             }
 #pragma unroll
             for (int s2 = 0; s2 < CKS; ++s2)
@@ -1856,7 +1890,8 @@ __device__ inline void combine_phase(const QmmArgs &a, int widx) {
         }
         for (int s2 = 0; s2 < a.KS; ++s2) {
             int f2, np;
-            unit_split_owners(a, s2, u, f2, np);
+            if (a.np_tab) np = __ldg(a.np_tab + static_cast<int64_t>(u) * np_tab_stride(a.KS) + s2);
+            else unit_split_owners(a, s2, u, f2, np);
             if (!SD_INB(np >= 0 && np <= a.P, a.status, 108)) np = 0;
             const float *qs = a.part + (static_cast<int64_t>(u) * a.KS + s2) * a.P * (ROWS * MPAD) + m * ROWS + lane;
             for (int c0 = 0; c0 < np; c0 += CH) {
@@ -1988,13 +2023,15 @@ __global__ void __launch_bounds__(QMM_THREADS, 1) qmm_kernel(const QmmArgs a) {
         }
         return;
     }
+    // the first split walked before the wait for the previous launch (unless the call is restricted)
+    const int s0 = tid == 0 ? first_split_early(a) : -1;
     pdl_wait();
     pdl_launch_dependents();
     if (warp >= FIN_WARP0) {
         (void)finish_phase<PAIR, NT>(a, sm, pk, fin_it, cs, warp - FIN_WARP0);
     } else {
         // the first split's activations are copied while the first weight stage is still in flight
-        const bool pre = tid == 0 && pre_issue_staging(a, sm, act_it, cs);
+        const bool pre = tid == 0 && issue_first_split(a, sm, act_it, cs, s0);
         (void)consume_phase<QT, PAIR, NT>(a, sm, it, pk, act_it, nrm_it, cs, pre);
     }
 }
@@ -2111,6 +2148,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1)
         }
         bool stop = false, pre = false;
         if (tid == 0) {
+            const int s0 = first_split_early(sa);  // walked while the other CTAs finish phase p - 1
             if (p > 0) {  // grid barrier: every CTA finished phase p - 1
                 const uint32_t target = static_cast<uint32_t>(p) * gridDim.x;
                 const uint64_t t0 = gtimer_ns();
@@ -2122,7 +2160,7 @@ __global__ void __launch_bounds__(QMM_THREADS, 1)
                     }
                 }
             }
-            if (!stop) pre = pre_issue_staging(sa, sm, act_it, cs);
+            if (!stop) pre = issue_first_split(sa, sm, act_it, cs, s0);
             if (trace) tslot(p)[TR_START] = gtimer_ns();
         }
         if (bar_any(BAR_WORK, WORK_THREADS, stop)) {
