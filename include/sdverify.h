@@ -460,11 +460,12 @@ sd_status sd_accept_sample_topk(const float *logits, int64_t vocab, int32_t K, c
  * parent must be NULL, else SD_EUNSUPPORTED); it produces the same tokens as the
  * head followed by sd_accept_sample, or with top_k > 0 by sd_accept_sample_topk.
  * layers is a HOST array read only by sd_pass_prepare.
- * sd_pass_prepare writes the phase table into `plan` (device, 256-byte aligned,
- * >= sd_pass_plan_bytes(n_layers), synchronously) and fills `out`;
- * sd_verify_pass launches it on `stream` (capturable in a CUDA graph).  Every
- * GPU of the pool runs one CTA per SM; the launch fails with SD_ECUDA rather
- * than wait if the GPU cannot hold them all at once.
+ * sd_pass_prepare writes the phase table, and the combine phases' pieces per
+ * (unit, split) from a host replay of their schedule, into `plan` (device,
+ * 256-byte aligned, >= sd_pass_plan_bytes(n_layers), synchronously) and fills
+ * `out`; sd_verify_pass launches it on `stream` (capturable in a CUDA graph).
+ * The launch runs one CTA per SM; it fails with SD_ECUDA rather than wait if
+ * the GPU cannot hold them all at once.
  */
 typedef struct {
     const void *qkv, *o, *gate_up, *down;
